@@ -1,0 +1,550 @@
+/*
+ * mxa_oracle.c -- plain, slow CPU oracle for MXFP8 block-scaled attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only tests/, the smoke check and the CPU-baseline leg of the
+ * benchmark use it.  It shares no code, header, table or constant with the
+ * CUDA library.
+ *
+ * Sources (page titles, sections):
+ *   [FA4]    "Flash Attention 4 + MXFP8 on Blackwell" (aixai.ru write-up):
+ *            "Что такое MXFP8", "Квантование dS без транспонирования".
+ *   [FLAMIA] "FLAMIA 阅读笔记" (reading notes on FLAMIA):
+ *            sec. 2 "前置知识" (attention, softmax gradient, online softmax,
+ *            the two hardware formats), sec. 3 (token blocks, Hadamard),
+ *            sec. 4 "E4M3 为什么常常不受尺度翻倍影响" (scale rule
+ *            e = ceil(log2(a/448))), sec. 6 (packed documents, visible pairs).
+ *
+ * Everything here is written from the format and the equations, in fp64,
+ * without tiling, fusion or reordering:
+ *   - E4M3 (OCP "fn" variant): bias 7, normals (1+m/8)*2^(E-7), subnormals
+ *     m*2^-9, 0x7F/0xFF NaN, max finite 448, no infinity.  Encoding picks the
+ *     nearest representable value (ties to the even code), saturating to 448.
+ *   - UE8M0: byte b is the power of two 2^(b-127).
+ *   - Scale exponent: the smallest integer e with amax / 2^e <= 448
+ *     ([FLAMIA] sec. 4, the saturation bound); an all-zero group takes e = 0.
+ *   - Attention: S = alpha Q K^T, P = softmax over the visible keys,
+ *     O = P V, LSE = m + ln l ([FLAMIA] sec. 2).
+ *   - Backward: dV = P^T G, E = G V^T, D = G.O, U = P (E - D),
+ *     dQ = alpha U K, dK = alpha U^T Q ([FLAMIA] sec. 2).
+ *
+ * Build: gcc -O2 -std=c11 -fopenmp -ffp-contract=off -fPIC -shared.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* Formats                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* bf16 bit pattern -> double (exact: bf16 is the top half of an fp32). */
+double orc_bf16_to_double(uint16_t b)
+{
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* E4M3 decode, from the field definition. */
+double orc_e4m3_decode(uint8_t c)
+{
+    int s = (c >> 7) & 1;
+    int E = (c >> 3) & 0xF;
+    int M = c & 7;
+    double v;
+    if (E == 15 && M == 7)
+        return NAN;
+    if (E == 0)
+        v = ldexp((double)M, -9);
+    else
+        v = ldexp(1.0 + M / 8.0, E - 7);
+    return s ? -v : v;
+}
+
+/* E4M3 encode: nearest of the 127 non-negative finite values (0x00..0x7E),
+ * ties to the even code (= even mantissa), saturating to 448; the sign bit is
+ * kept, so a negative value that rounds to zero gives 0x80. */
+uint8_t orc_e4m3_encode(double y)
+{
+    if (isnan(y))
+        return 0x7F;
+    uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    double a = fabs(y);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    int best = 0;
+    double best_err = a; /* distance to code 0 */
+    for (int c = 1; c <= 0x7E; ++c) {
+        double err = fabs(orc_e4m3_decode((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return sign | (uint8_t)best;
+}
+
+/* Element-wise encode of n values (used by the exhaustive codec checks). */
+void orc_e4m3_encode_array(const double* y, int64_t n, uint8_t* out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_e4m3_encode(y[i]);
+}
+
+/* UE8M0 byte <-> power of two. */
+double orc_ue8m0_decode(uint8_t b)
+{
+    if (b == 0xFF)
+        return NAN;
+    return ldexp(1.0, (int)b - 127);
+}
+
+/* Scale exponent of a group with max magnitude amax: the smallest integer e
+ * such that amax / 2^e <= 448.  All-zero groups take e = 0 (the agreed finite
+ * scale).  The result is clamped to the UE8M0 range [-127, 127]. */
+int orc_mx_exponent(double amax)
+{
+    if (!(amax > 0.0))
+        return 0;
+    int e = ilogb(amax) - 10; /* certainly too small: amax/2^e >= 2^10 > 448 */
+    while (amax > ldexp(448.0, e))
+        ++e;
+    if (e < -127)
+        e = -127;
+    if (e > 127)
+        e = 127;
+    return e;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Document geometry                                                         */
+/* ------------------------------------------------------------------------ */
+
+/* cu_seqlens == NULL means one document covering all T tokens. */
+static void doc_range(const int32_t* cu, int ndocs, int64_t T, int b, int64_t* s, int64_t* e)
+{
+    if (!cu) {
+        *s = 0;
+        *e = T;
+        (void)ndocs;
+        (void)b;
+        return;
+    }
+    *s = cu[b];
+    *e = cu[b + 1];
+}
+
+static int num_docs_eff(const int32_t* cu, int ndocs) { return cu ? ndocs : 1; }
+
+/* Number of 32-token groups of a document of n tokens, counted from its start. */
+static int64_t nblk32(int64_t n) { return (n + 31) / 32; }
+
+/* Offset of document b's first 32-token group in the concatenated group list. */
+int64_t orc_block_offset(const int32_t* cu, int ndocs, int64_t T, int b)
+{
+    int64_t off = 0;
+    for (int i = 0; i < b; ++i) {
+        int64_t s, e;
+        doc_range(cu, ndocs, T, i, &s, &e);
+        off += nblk32(e - s);
+    }
+    return off;
+}
+
+int64_t orc_total_blocks(const int32_t* cu, int ndocs, int64_t T)
+{
+    return orc_block_offset(cu, ndocs, T, num_docs_eff(cu, ndocs));
+}
+
+/* Visible (query, key) pairs of causal documents: sum n (n + 1) / 2
+ * ([FLAMIA] sec. 6). */
+int64_t orc_visible_pairs(const int32_t* cu, int ndocs, int64_t T)
+{
+    int64_t c = 0;
+    for (int b = 0; b < num_docs_eff(cu, ndocs); ++b) {
+        int64_t s, e;
+        doc_range(cu, ndocs, T, b, &s, &e);
+        c += (e - s) * (e - s + 1) / 2;
+    }
+    return c;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Quantizers                                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Row view: one scale per (token, head, 32 consecutive channels).
+ * x: bf16 bits [T, H, d]; codes: [T, H, d]; scales: UE8M0 bytes [T, H, d/32]. */
+void orc_quant_row(const uint16_t* x, int64_t T, int H, int d, uint8_t* codes, uint8_t* scales)
+{
+    int G = d / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int h = 0; h < H; ++h)
+            for (int g = 0; g < G; ++g) {
+                const uint16_t* xs = x + (t * H + h) * d + g * 32;
+                double amax = 0.0;
+                for (int i = 0; i < 32; ++i) {
+                    double v = fabs(orc_bf16_to_double(xs[i]));
+                    if (v > amax)
+                        amax = v;
+                }
+                int e = orc_mx_exponent(amax);
+                for (int i = 0; i < 32; ++i)
+                    codes[(t * H + h) * d + g * 32 + i] = orc_e4m3_encode(ldexp(orc_bf16_to_double(xs[i]), -e));
+                scales[(t * H + h) * G + g] = (uint8_t)(e + 127);
+            }
+}
+
+/* Token view: one scale per (document, 32 consecutive tokens counted from the
+ * document start, head, channel); the last group of a document may be short
+ * and no group crosses a document boundary.
+ * scales: logical [H, d, NB] with NB = sum over docs of ceil(n/32), document
+ * b's groups starting at orc_block_offset(b). */
+void orc_quant_tok(const uint16_t* x, int64_t T, int H, int d, const int32_t* cu, int ndocs,
+                   uint8_t* codes, uint8_t* scales)
+{
+    int nd = num_docs_eff(cu, ndocs);
+    int64_t NB = orc_total_blocks(cu, ndocs, T);
+    for (int b = 0; b < nd; ++b) {
+        int64_t s, e;
+        doc_range(cu, ndocs, T, b, &s, &e);
+        int64_t boff = orc_block_offset(cu, ndocs, T, b);
+        int64_t nbk = nblk32(e - s);
+#pragma omp parallel for schedule(static)
+        for (int64_t kb = 0; kb < nbk; ++kb) {
+            int64_t t0 = s + kb * 32, t1 = t0 + 32 < e ? t0 + 32 : e;
+            for (int h = 0; h < H; ++h)
+                for (int c = 0; c < d; ++c) {
+                    double amax = 0.0;
+                    for (int64_t t = t0; t < t1; ++t) {
+                        double v = fabs(orc_bf16_to_double(x[(t * H + h) * d + c]));
+                        if (v > amax)
+                            amax = v;
+                    }
+                    int ex = orc_mx_exponent(amax);
+                    for (int64_t t = t0; t < t1; ++t)
+                        codes[(t * H + h) * d + c] = orc_e4m3_encode(ldexp(orc_bf16_to_double(x[(t * H + h) * d + c]), -ex));
+                    scales[((int64_t)h * d + c) * NB + boff + kb] = (uint8_t)(ex + 127);
+                }
+        }
+    }
+}
+
+/* Normalized 128-point Hadamard rotation of one vector, in IEEE fp32, in the
+ * Sylvester order: for h = 1, 2, 4, ..., 64, every pair (i, i + h) inside a
+ * block of 2h becomes (a + b, a - b); the result is multiplied by the fp32
+ * value of 128^(-1/2).  ([FLAMIA] sec. 3, "旋转为什么有时适得其反": the
+ * rotation H with H H^T = I leaves Q K^T unchanged.)  The fp32 sequence is the
+ * reading taken because the codes computed from it must match bit for bit. */
+void orc_hadamard128_f32(const float* in, float* out)
+{
+    float v[128];
+    for (int i = 0; i < 128; ++i)
+        v[i] = in[i];
+    for (int h = 1; h < 128; h *= 2)
+        for (int i = 0; i < 128; i += 2 * h)
+            for (int j = i; j < i + h; ++j) {
+                float a = v[j], b = v[j + h];
+                v[j] = a + b;
+                v[j + h] = a - b;
+            }
+    const float r = (float)0.08838834764831845; /* fp32 nearest to 128^-1/2 */
+    for (int i = 0; i < 128; ++i)
+        out[i] = v[i] * r;
+}
+
+/* Token-block view ([FLAMIA] sec. 3, "让同一份码跨两个方向使用"): one
+ * exponent per (document, 32 consecutive tokens from the document start,
+ * head) shared by all d channels; the same codes serve both contraction axes.
+ * With hadamard != 0 (d == 128) every (token, head) vector is first rotated
+ * (orc_hadamard128_f32) and the block statistics are taken on the rotated
+ * fp32 values.  scales: logical [H, NB]. */
+void orc_quant_tokblock(const uint16_t* x, int64_t T, int H, int d, const int32_t* cu, int ndocs,
+                        int hadamard, uint8_t* codes, uint8_t* scales)
+{
+    int nd = num_docs_eff(cu, ndocs);
+    int64_t NB = orc_total_blocks(cu, ndocs, T);
+    float* y = (float*)malloc(sizeof(float) * (size_t)T * H * d);
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int h = 0; h < H; ++h) {
+            float in[128];
+            const uint16_t* xs = x + (t * H + h) * d;
+            float* ys = y + (t * H + h) * d;
+            if (hadamard) {
+                for (int i = 0; i < 128; ++i)
+                    in[i] = (float)orc_bf16_to_double(xs[i]);
+                orc_hadamard128_f32(in, ys);
+            } else {
+                for (int i = 0; i < d; ++i)
+                    ys[i] = (float)orc_bf16_to_double(xs[i]);
+            }
+        }
+    for (int b = 0; b < nd; ++b) {
+        int64_t s, e;
+        doc_range(cu, ndocs, T, b, &s, &e);
+        int64_t boff = orc_block_offset(cu, ndocs, T, b);
+        int64_t nbk = nblk32(e - s);
+#pragma omp parallel for schedule(static)
+        for (int64_t kb = 0; kb < nbk; ++kb) {
+            int64_t t0 = s + kb * 32, t1 = t0 + 32 < e ? t0 + 32 : e;
+            for (int h = 0; h < H; ++h) {
+                double amax = 0.0;
+                for (int64_t t = t0; t < t1; ++t)
+                    for (int c = 0; c < d; ++c) {
+                        double v = fabs((double)y[(t * H + h) * d + c]);
+                        if (v > amax)
+                            amax = v;
+                    }
+                int ex = orc_mx_exponent(amax);
+                for (int64_t t = t0; t < t1; ++t)
+                    for (int c = 0; c < d; ++c)
+                        codes[(t * H + h) * d + c] = orc_e4m3_encode(ldexp((double)y[(t * H + h) * d + c], -ex));
+                scales[(int64_t)h * NB + boff + kb] = (uint8_t)(ex + 127);
+            }
+        }
+    }
+    free(y);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dequantization (exact in fp64): value = decode(code) * 2^(byte - 127)      */
+/* ------------------------------------------------------------------------ */
+
+void orc_dequant_row(const uint8_t* codes, const uint8_t* scales, int64_t T, int H, int d, double* out)
+{
+    int G = d / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int h = 0; h < H; ++h)
+            for (int c = 0; c < d; ++c)
+                out[(t * H + h) * d + c] = orc_e4m3_decode(codes[(t * H + h) * d + c]) *
+                                           orc_ue8m0_decode(scales[(t * H + h) * G + c / 32]);
+}
+
+void orc_dequant_tok(const uint8_t* codes, const uint8_t* scales, int64_t T, int H, int d,
+                     const int32_t* cu, int ndocs, double* out)
+{
+    int64_t NB = orc_total_blocks(cu, ndocs, T);
+    for (int b = 0; b < num_docs_eff(cu, ndocs); ++b) {
+        int64_t s, e;
+        doc_range(cu, ndocs, T, b, &s, &e);
+        int64_t boff = orc_block_offset(cu, ndocs, T, b);
+#pragma omp parallel for schedule(static)
+        for (int64_t t = s; t < e; ++t)
+            for (int h = 0; h < H; ++h)
+                for (int c = 0; c < d; ++c)
+                    out[(t * H + h) * d + c] = orc_e4m3_decode(codes[(t * H + h) * d + c]) *
+                                               orc_ue8m0_decode(scales[((int64_t)h * d + c) * NB + boff + (t - s) / 32]);
+    }
+}
+
+void orc_dequant_tokblock(const uint8_t* codes, const uint8_t* scales, int64_t T, int H, int d,
+                          const int32_t* cu, int ndocs, double* out)
+{
+    int64_t NB = orc_total_blocks(cu, ndocs, T);
+    for (int b = 0; b < num_docs_eff(cu, ndocs); ++b) {
+        int64_t s, e;
+        doc_range(cu, ndocs, T, b, &s, &e);
+        int64_t boff = orc_block_offset(cu, ndocs, T, b);
+#pragma omp parallel for schedule(static)
+        for (int64_t t = s; t < e; ++t)
+            for (int h = 0; h < H; ++h)
+                for (int c = 0; c < d; ++c)
+                    out[(t * H + h) * d + c] = orc_e4m3_decode(codes[(t * H + h) * d + c]) *
+                                               orc_ue8m0_decode(scales[(int64_t)h * NB + boff + (t - s) / 32]);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Direct attention (no tiling)                                              */
+/* ------------------------------------------------------------------------ */
+
+static double dot(const double* a, const double* b, int d)
+{
+    double s = 0.0;
+    for (int k = 0; k < d; ++k)
+        s += a[k] * b[k];
+    return s;
+}
+
+/* Forward of one query row: the visible keys are [s, i] when causal, else
+ * [s, e).  Writes O_i (d values) and returns LSE_i = m + ln l.  Uses the
+ * direct softmax, S_ij = alpha Q_i . K_j, P_ij = exp(S_ij - m) / l. */
+static double fwd_row(const double* Q, const double* K, const double* V, int Hq, int Hkv, int d,
+                      int64_t s, int64_t e, int causal, double alpha, int64_t i, int h, double* o,
+                      double* Srow)
+{
+    int hk = h / (Hq / Hkv);
+    int64_t jend = causal ? i + 1 : e;
+    const double* q = Q + (i * Hq + h) * d;
+    double m = -INFINITY;
+    for (int64_t j = s; j < jend; ++j) {
+        Srow[j - s] = alpha * dot(q, K + (j * Hkv + hk) * d, d);
+        if (Srow[j - s] > m)
+            m = Srow[j - s];
+    }
+    double l = 0.0;
+    for (int k = 0; k < d; ++k)
+        o[k] = 0.0;
+    for (int64_t j = s; j < jend; ++j) {
+        double p = exp(Srow[j - s] - m);
+        l += p;
+        const double* v = V + (j * Hkv + hk) * d;
+        for (int k = 0; k < d; ++k)
+            o[k] += p * v[k];
+    }
+    for (int k = 0; k < d; ++k)
+        o[k] /= l;
+    return m + log(l);
+}
+
+static int doc_of(const int32_t* cu, int ndocs, int64_t t)
+{
+    if (!cu)
+        return 0;
+    int b = 0;
+    while (b + 1 < ndocs && cu[b + 1] <= t)
+        ++b;
+    return b;
+}
+
+/* Attention forward over dequantized operands.
+ * Q [T, Hq, d] (score view), K [T, Hkv, d] (score view), V [T, Hkv, d]
+ * (the view the P V product uses); O [T, Hq, d]; LSE [Hq, T].
+ * sel == NULL: every query row; else nsel (token, head) pairs.  Rows not
+ * computed are left untouched. */
+void orc_attn_fwd(const double* Q, const double* K, const double* V, int64_t T, int Hq, int Hkv, int d,
+                  const int32_t* cu, int ndocs, int causal, double alpha, const int32_t* sel, int64_t nsel,
+                  double* O, double* LSE)
+{
+    int64_t n = sel ? nsel : T * Hq;
+    int64_t maxlen = 0;
+    for (int b = 0; b < num_docs_eff(cu, ndocs); ++b) {
+        int64_t s, e;
+        doc_range(cu, ndocs, T, b, &s, &e);
+        if (e - s > maxlen)
+            maxlen = e - s;
+    }
+#pragma omp parallel
+    {
+        double* Srow = (double*)malloc(sizeof(double) * (size_t)(maxlen + 1));
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < n; ++r) {
+            int64_t i = sel ? sel[2 * r] : r / Hq;
+            int h = sel ? sel[2 * r + 1] : (int)(r % Hq);
+            int b = doc_of(cu, ndocs, i);
+            int64_t s, e;
+            doc_range(cu, ndocs, T, b, &s, &e);
+            LSE[(int64_t)h * T + i] = fwd_row(Q, K, V, Hq, Hkv, d, s, e, causal, alpha, i, h, O + (i * Hq + h) * d, Srow);
+        }
+        free(Srow);
+    }
+}
+
+/* Attention backward over dequantized operands, direct (no tiling).
+ * Inputs (all [T, H*, d] fp64):
+ *   Qs, Ks : score views (rebuild S, exactly as the forward);
+ *   Vo     : the V view the forward's P V used (rebuilds O);
+ *   Vr, Gr : views for E = G V^T and D = G . O (the same G in both);
+ *   Qt, Kt, Gt : views for dK = alpha U^T Q, dQ = alpha U K, dV = P^T G.
+ * Outputs dQ [T, Hq, d], dK [T, Hkv, d], dV [T, Hkv, d]; also O [T, Hq, d],
+ * LSE [Hq, T] and D [Hq, T] of the computed rows.
+ * units == NULL: all (document, kv-head) units; else nunits (doc, kv-head)
+ * pairs.  dK/dV of a kv-head sum over the Hq/Hkv query heads of its group.
+ * Pass 1 (per query row) builds LSE, O, D and dQ; pass 2 (per key row)
+ * rebuilds P and U from LSE and D and sums dK and dV. */
+void orc_attn_bwd(const double* Qs, const double* Ks, const double* Vo, const double* Vr, const double* Gr,
+                  const double* Qt, const double* Kt, const double* Gt, int64_t T, int Hq, int Hkv, int d,
+                  const int32_t* cu, int ndocs, int causal, double alpha, const int32_t* units, int nunits,
+                  double* dQ, double* dK, double* dV, double* O, double* LSE, double* D)
+{
+    int nd = num_docs_eff(cu, ndocs);
+    int nu = units ? nunits : nd * Hkv;
+    int grp = Hq / Hkv;
+    for (int u = 0; u < nu; ++u) {
+        int b = units ? units[2 * u] : u / Hkv;
+        int hk = units ? units[2 * u + 1] : u % Hkv;
+        int64_t s, e;
+        doc_range(cu, ndocs, T, b, &s, &e);
+        int64_t n = e - s;
+        if (n <= 0)
+            continue;
+        /* pass 1: rows */
+#pragma omp parallel
+        {
+            double* Srow = (double*)malloc(sizeof(double) * (size_t)n);
+#pragma omp for schedule(dynamic, 8) collapse(2)
+            for (int hh = 0; hh < grp; ++hh)
+                for (int64_t i = s; i < e; ++i) {
+                    int h = hk * grp + hh;
+                    double* o = O + (i * Hq + h) * d;
+                    double lse = fwd_row(Qs, Ks, Vo, Hq, Hkv, d, s, e, causal, alpha, i, h, o, Srow);
+                    LSE[(int64_t)h * T + i] = lse;
+                    const double* g = Gr + (i * Hq + h) * d;
+                    double Di = dot(g, o, d);
+                    D[(int64_t)h * T + i] = Di;
+                    double* dq = dQ + (i * Hq + h) * d;
+                    for (int k = 0; k < d; ++k)
+                        dq[k] = 0.0;
+                    int64_t jend = causal ? i + 1 : e;
+                    for (int64_t j = s; j < jend; ++j) {
+                        double P = exp(Srow[j - s] - lse);
+                        double E = dot(g, Vr + (j * Hkv + hk) * d, d);
+                        double U = P * (E - Di);
+                        const double* kt = Kt + (j * Hkv + hk) * d;
+                        for (int k = 0; k < d; ++k)
+                            dq[k] += alpha * U * kt[k];
+                    }
+                }
+            free(Srow);
+        }
+        /* pass 2: key columns */
+#pragma omp parallel for schedule(dynamic, 8)
+        for (int64_t j = s; j < e; ++j) {
+            double* dk = dK + (j * Hkv + hk) * d;
+            double* dv = dV + (j * Hkv + hk) * d;
+            for (int k = 0; k < d; ++k) {
+                dk[k] = 0.0;
+                dv[k] = 0.0;
+            }
+            const double* kj = Ks + (j * Hkv + hk) * d;
+            const double* vj = Vr + (j * Hkv + hk) * d;
+            for (int hh = 0; hh < grp; ++hh) {
+                int h = hk * grp + hh;
+                int64_t ibeg = causal ? j : s;
+                for (int64_t i = ibeg; i < e; ++i) {
+                    double S = alpha * dot(Qs + (i * Hq + h) * d, kj, d);
+                    double P = exp(S - LSE[(int64_t)h * T + i]);
+                    const double* g = Gr + (i * Hq + h) * d;
+                    double E = dot(g, vj, d);
+                    double U = P * (E - D[(int64_t)h * T + i]);
+                    const double* gt = Gt + (i * Hq + h) * d;
+                    const double* qt = Qt + (i * Hq + h) * d;
+                    for (int k = 0; k < d; ++k) {
+                        dv[k] += P * gt[k];
+                        dk[k] += alpha * U * qt[k];
+                    }
+                }
+            }
+        }
+    }
+}
+
+int orc_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
