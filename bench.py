@@ -1,0 +1,377 @@
+#!/usr/bin/env python
+"""Benchmark: MXFP8 attention forward + backward on one GB300.
+
+One step is the whole hot path over one batch of seeded synthetic inputs
+already resident in HBM: quantize Q, K, V (row + token views), forward,
+quantize dO, backward (D prep, main kernel, dQ convert).  Workload: B8 H32
+L4096 d128 (the pages' LLM shape), non-causal by default, N(0,1) inputs with
+two x50 outlier channels per head.
+
+FLOP convention (the pages' / FLAMIA's): forward 4 B H L^2 d (halved when
+causal), backward 2.5 x forward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--causal] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs its own
+replica of the workload (weak scaling; no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MXFP8 attention fwd/bwd PFLOP/s and % of dense MXFP8 peak, B8 H32 L4096 d128"
+UNIT = "PFLOP/s"
+# Dense MXFP8 tensor peak: MEASURED_PEAKS.json's bf16 figure x the nominal
+# fp8/bf16 ratio (4.5 / 2.25 = 2); fallback 1.9 PFLOP/s bf16 burst.
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            bf16 = d.get("bf16_tflops") or d.get("bf16_tflops_burst")
+            bf16s = d.get("bf16_tflops_sustained", bf16)
+            hbm = d.get("hbm_gbs")
+            if bf16 and hbm:
+                return {"mxfp8_tflops": 2.0 * float(bf16), "mxfp8_tflops_sustained": 2.0 * float(bf16s),
+                        "hbm_gbs": float(hbm), "source": "measured (MEASURED_PEAKS.json bf16 x nominal fp8/bf16 ratio 2)"}
+        except Exception:
+            pass
+    return {"mxfp8_tflops": 2.0 * FALLBACK_BF16_TFLOPS, "mxfp8_tflops_sustained": 2.0 * 1700.0,
+            "hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback (1.9 PFLOP/s bf16 burst x nominal fp8/bf16 ratio 2)"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def flops(B, H, L, d, causal):
+    f = 4.0 * B * H * L * L * d
+    if causal:
+        f *= 0.5
+    return f, 2.5 * f
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+
+def oracle_sample(L=4096, H=1, d=128, causal=False, seed=1002):
+    """The oracle, as it stands, on a bounded sample of the workload: one
+    document of L tokens, H heads, same value recipe (two x50 outlier
+    channels per head).  Returns (seconds, flop, threads)."""
+    from block_scaled_mxfp8_gb300 import inputs as inp
+    from oracle import oracle as orc
+
+    w = inp.make_custom("cpu_sample", B=1, L=L, Hq=H, Hkv=H, d=d, causal=causal, seed=seed,
+                        outlier_channels=2, outlier_gain=50.0)
+    t = inp.tensors(w)
+    orc.build()
+    t0 = time.perf_counter()
+    v = {}
+    for k in ("q", "k", "v", "do"):
+        rc, rs = orc.quant_row(t[k])
+        tc, ts = orc.quant_tok(t[k])
+        v[k] = (orc.dequant_row(rc, rs), orc.dequant_tok(tc, ts))
+    alpha = 1.0 / math.sqrt(d)
+    orc.attn_fwd(v["q"][0], v["k"][0], v["v"][1], None, causal, alpha)
+    orc.attn_bwd(v["q"][0], v["k"][0], v["v"][1], v["v"][0], v["do"][0], v["q"][1], v["k"][1], v["do"][1],
+                 None, causal, alpha)
+    dt = time.perf_counter() - t0
+    ff, fb = flops(1, H, L, d, causal)
+    return dt, ff + fb, orc.num_threads()
+
+
+# ------------------------------------------------------------------ GPU leg
+
+def run_gpu(args):
+    import torch
+
+    from block_scaled_mxfp8_gb300 import build as mbuild
+    from block_scaled_mxfp8_gb300 import inputs as inp
+    from block_scaled_mxfp8_gb300 import mxa
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    mbuild.build()
+
+    w = inp.workload(args.workload, causal=args.causal)
+    B, L, Hq, Hkv, d = w.B, w.L, w.Hq, w.Hkv, w.d
+    T = w.T
+    t = inp.tensors(w)
+    dev = torch.device("cuda", local)
+    x = {k: v.to(dev) for k, v in t.items()}
+    geo = mxa.Geometry.batched(B, L) if w.lengths is None else mxa.Geometry.packed(w.lengths, dev)
+
+    def alloc_views(H):
+        mk = lambda: mxa.QView(torch.empty((T, H, d), dtype=torch.uint8, device=dev),
+                               torch.empty((H, geo.ntiles, mxa.ATOM_BYTES), dtype=torch.uint8, device=dev))
+        return mk(), mk()
+
+    qv = {k: alloc_views(Hq if k in ("q", "do") else Hkv) for k in ("q", "k", "v", "do")}
+    o = torch.empty((T, Hq, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
+    dq = torch.empty((T, Hq, d), dtype=torch.bfloat16, device=dev)
+    dk = torch.empty((T, Hkv, d), dtype=torch.bfloat16, device=dev)
+    dv = torch.empty((T, Hkv, d), dtype=torch.bfloat16, device=dev)
+    views = {"q_row": qv["q"][0], "k_row": qv["k"][0], "v_row": qv["v"][0], "g_row": qv["do"][0],
+             "q_tok": qv["q"][1], "k_tok": qv["k"][1], "g_tok": qv["do"][1]}
+    bp = mxa.bwd_params(views, o, lse, dq, dk, dv, geo, w.causal, args.dq_mode)
+    ws = torch.empty(mxa.mxa_bwd_workspace_bytes(bp), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step(src, rec=None):
+        e = [ev() for _ in range(4)] if rec is not None else None
+        if e: e[0].record(stream)
+        for k in ("q", "k", "v"):
+            mxa.quantize(src[k], geo, out=qv[k])
+        if e: e[1].record(stream)
+        mxa.fwd(qv["q"][0], qv["k"][0], qv["v"][1], geo, w.causal, out=(o, lse))
+        if e: e[2].record(stream)
+        mxa.quantize(src["do"], geo, out=qv["do"])
+        mxa.bwd(views, o, lse, geo, w.causal, dq_mode=args.dq_mode, workspace=ws, out=(dq, dk, dv))
+        if e:
+            e[3].record(stream)
+            rec.append(e)
+
+    for _ in range(args.warmup):
+        step(x)
+    torch.cuda.synchronize()
+    mxa.check_error()
+
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    recs = []
+    with ClockSampler(local) as clk:
+        t_start, t_end = ev(), ev()
+        t_start.record(stream)
+        for _ in range(args.steps):
+            step(x, recs)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    mxa.check_error()
+    ms_total = t_start.elapsed_time(t_end)
+    if dist is not None:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    ms_quant = statistics.mean(r[0].elapsed_time(r[1]) for r in recs)
+    ms_fwd = statistics.mean(r[1].elapsed_time(r[2]) for r in recs)
+    ms_bwd = statistics.mean(r[2].elapsed_time(r[3]) for r in recs)  # includes the dO quantize
+
+    ffwd, fbwd = flops(B, Hq, L, d, w.causal)
+    step_flop = ffwd + fbwd
+    value = world * step_flop / (ms_step * 1e-3) / 1e15
+
+    # bwd alone (prep + main + dq convert), timed separately after the loop
+    bw_ev = []
+    for _ in range(max(3, min(args.steps, 10))):
+        a_, b_ = ev(), ev()
+        a_.record(stream)
+        mxa.bwd(views, o, lse, geo, w.causal, dq_mode=args.dq_mode, workspace=ws, out=(dq, dk, dv))
+        b_.record(stream)
+        bw_ev.append((a_, b_))
+    torch.cuda.synchronize()
+    ms_bwd_only = statistics.mean(a_.elapsed_time(b_) for a_, b_ in bw_ev)
+
+    pk = peaks()
+    fwd_pf = ffwd / (ms_fwd * 1e-3) / 1e15
+    bwd_pf = fbwd / (ms_bwd_only * 1e-3) / 1e15
+    # dominant kernel: the backward (2.5x the forward's flops)
+    dom = {"kernel": "attn_bwd_kernel (+ D prep, dQ convert in the same call)", "pflops": bwd_pf}
+    if ffwd / (ms_fwd * 1e-3) < 0:  # never; keeps the structure explicit
+        dom = {"kernel": "attn_fwd_kernel", "pflops": fwd_pf}
+    peak_pf = pk["mxfp8_tflops"] / 1e3
+    roofline = {"bound": "tensor", "achieved": round(dom["pflops"] * 1e3, 1), "peak": round(pk["mxfp8_tflops"], 1),
+                "unit": "TFLOP/s", "frac": round(dom["pflops"] / peak_pf, 4), "traffic": None,
+                "kernel": dom["kernel"], "peak_source": pk["source"],
+                "fwd": {"achieved": round(fwd_pf * 1e3, 1), "frac": round(fwd_pf / peak_pf, 4)},
+                "bwd": {"achieved": round(bwd_pf * 1e3, 1), "frac": round(bwd_pf / peak_pf, 4)}}
+
+    # e2e through the C ABI with host buffers: H2D of q, k, v, dO and D2H of o, dq, dk, dv inside the timed region
+    host_in = {k: v.pin_memory() for k, v in t.items()}
+    host_out = {k: torch.empty(s, dtype=torch.bfloat16).pin_memory()
+                for k, s in (("o", o.shape), ("dq", dq.shape), ("dk", dk.shape), ("dv", dv.shape))}
+    dev_in = {k: torch.empty_like(v) for k, v in x.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def e2e_step():
+        for k in dev_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        step(dev_in)
+        host_out["o"].copy_(o, non_blocking=True)
+        host_out["dq"].copy_(dq, non_blocking=True)
+        host_out["dk"].copy_(dk, non_blocking=True)
+        host_out["dv"].copy_(dv, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = max(2, min(args.steps, 5))
+    a_, b_ = ev(), ev()
+    a_.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    b_.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = a_.elapsed_time(b_) / n_e2e
+    e2e = {"value": round(world * step_flop / (ms_e2e * 1e-3) / 1e15, 4), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3)}
+
+    out = {
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "mxfp8 (e4m3 codes, ue8m0 scales, fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": "%s: B%d H%d L%d d%d %s, fwd+bwd, dQ %s" % (
+            w.name, B, Hq, L, d, "causal" if w.causal else "non-causal", "fp16x2^9" if args.dq_mode else "fp32"),
+            "global_batch": B * world, "seq_len": L, "heads": Hq, "head_dim": d, "causal": w.causal,
+            "parallelism": "replicas" if world > 1 else "single-gpu",
+            "l2": "inputs larger than L2 (each bf16 tensor %.0f MB)" % (T * Hq * d * 2 / 1e6),
+            "flop_per_step": step_flop},
+        "pct_of_peak": round(100.0 * value / world / peak_pf, 2),
+        "fwd_pflops": round(fwd_pf, 4), "bwd_pflops": round(bwd_pf, 4),
+        "ms": {"quantize_qkv": round(ms_quant, 3), "fwd": round(ms_fwd, 3), "quantize_do_plus_bwd": round(ms_bwd, 3),
+               "bwd": round(ms_bwd_only, 3)},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": 8 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, fl, thr = oracle_sample(L=min(L, 4096), H=1, d=d, causal=w.causal)
+        out["cpu_baseline"] = {"value": fl / dt / 1e15, "unit": UNIT, "cores": thr, "kind": "oracle",
+                               "sample": "one document of %d tokens, 1 head, d%d (oracle quantize + fwd + bwd), %.1f s"
+                                         % (min(L, 4096), d, dt)}
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out))
+
+
+def run_reference(args):
+    """The oracle on the host cores, per step a bounded sample of the workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from block_scaled_mxfp8_gb300 import inputs as inp
+
+    w = inp.workload(args.workload, causal=args.causal)
+    L = min(w.L, 2048)
+    total, fl_total, thr = 0.0, 0.0, 1
+    for i in range(args.warmup + args.steps):
+        dt, fl, thr = oracle_sample(L=L, H=1, d=w.d, causal=w.causal, seed=1002 + i)
+        if i >= args.warmup:
+            total += dt
+            fl_total += fl
+    v = fl_total / total / 1e15
+    sample = "per step one document of %d tokens, 1 head, d%d of the %s workload (oracle quantize + fwd + bwd)" % (
+        L, w.d, w.name)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "%s: B%d H%d L%d d%d %s, fwd+bwd" % (w.name, w.B, w.Hq, w.L, w.d,
+                                                                    "causal" if w.causal else "non-causal")},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="mxa", choices=["mxa", "reference"])
+    ap.add_argument("--workload", default="llm")
+    ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--dq-mode", type=int, default=0, help="0 = fp32 dQ accumulation, 1 = fp16 x 2^9")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

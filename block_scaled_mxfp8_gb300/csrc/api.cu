@@ -1,0 +1,331 @@
+// api.cu -- the C ABI of libmxa.so (declared in include/mxa.h): argument
+// validation, TMA tensor-map encoding and kernel launches.  Nothing here
+// allocates device memory; every buffer belongs to the caller.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mxa.h"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace mxa {
+
+// Device error word written by kernels whose bounded waits ran out.
+static __device__ int g_err_word;
+
+static int* g_err_ptr[64];
+static std::mutex g_mu;
+
+int* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D map over E4M3 codes [T, H, d]: box of 128 tokens x 1 head x d bytes,
+// swizzled to the tensor core's K-major / MN-major layout.
+bool make_code_map(CUtensorMap* map, const void* codes, int64_t T, int H, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H) * d};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 1, 128};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(codes), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+mxa_status check_view(const mxa_qview& v) {
+  if (!v.codes || !v.scales) return MXA_ERR_ARG;
+  if (!aligned(v.codes, 16) || !aligned(v.scales, 16)) return MXA_ERR_ALIGN;
+  return MXA_OK;
+}
+
+mxa_status check_shape(const mxa_shape& s) {
+  if (s.T < 0 || s.T > 0x7FFFFFFFll) return MXA_ERR_ARG;
+  if (s.Hq <= 0 || s.Hkv <= 0 || s.num_docs <= 0 || s.ntiles <= 0 || s.max_seqlen <= 0) return MXA_ERR_ARG;
+  if (s.num_docs > 65535 || s.Hq > 65535) return MXA_ERR_ARG;
+  if (s.d != 64 && s.d != 128) return MXA_ERR_UNSUPPORTED;
+  if (s.Hq % s.Hkv != 0) return MXA_ERR_UNSUPPORTED;
+  if (!s.cu_seqlens && (s.T % s.num_docs != 0 || s.T / s.num_docs > s.max_seqlen)) return MXA_ERR_ARG;
+  if (!(s.softmax_scale >= 0.0f) || !std::isfinite(s.softmax_scale)) return MXA_ERR_ARG;
+  return MXA_OK;
+}
+
+float alpha_of(const mxa_shape& s) { return s.softmax_scale > 0.0f ? s.softmax_scale : 1.0f / std::sqrt(static_cast<float>(s.d)); }
+
+}  // namespace
+}  // namespace mxa
+
+using namespace mxa;
+
+extern "C" {
+
+int mxa_abi_version(void) { return MXA_ABI_VERSION; }
+
+const char* mxa_status_str(mxa_status s) {
+  switch (s) {
+    case MXA_OK: return "ok";
+    case MXA_ERR_ARG: return "invalid argument";
+    case MXA_ERR_ALIGN: return "misaligned buffer";
+    case MXA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MXA_ERR_WORKSPACE: return "workspace too small";
+    case MXA_ERR_CUDA: return "CUDA error";
+    case MXA_ERR_TIMEOUT: return "kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+int64_t mxa_scale_tiles(int64_t T, int num_docs, const int32_t* cu) {
+  if (T < 0 || num_docs <= 0) return -1;
+  if (!cu) {
+    if (T % num_docs) return -1;
+    return static_cast<int64_t>(num_docs) * ((T / num_docs + 127) / 128);
+  }
+  int64_t nt = 0;
+  if (cu[0] != 0 || cu[num_docs] != T) return -1;
+  for (int b = 0; b < num_docs; ++b) {
+    const int64_t n = static_cast<int64_t>(cu[b + 1]) - cu[b];
+    if (n < 0) return -1;
+    nt += (n + 127) / 128;
+  }
+  return nt;
+}
+
+int64_t mxa_scale_tiles_bound(int64_t T, int num_docs) {
+  if (T < 0 || num_docs <= 0) return -1;
+  return (T + 127) / 128 + num_docs;
+}
+
+size_t mxa_scale_bytes(int H, int64_t ntiles) {
+  if (H <= 0 || ntiles < 0) return 0;
+  return static_cast<size_t>(H) * static_cast<size_t>(ntiles) * kAtomBytes;
+}
+
+mxa_status mxa_quantize(const void* x, int64_t T, int H, int d, const int32_t* cu_seqlens, int num_docs,
+                        int max_seqlen, int64_t ntiles, mxa_scale_mode mode, int views, int hadamard,
+                        mxa_qview* row, mxa_qview* tok, cudaStream_t stream) {
+  if (!x || T < 0 || T > 0x7FFFFFFFll || H <= 0 || H > 65535 || num_docs <= 0 || num_docs > 65535 ||
+      ntiles <= 0 || max_seqlen <= 0)
+    return MXA_ERR_ARG;
+  if (d != 64 && d != 128) return MXA_ERR_UNSUPPORTED;
+  if (!cu_seqlens && (T % num_docs != 0 || T / num_docs > max_seqlen)) return MXA_ERR_ARG;
+  if (!aligned(x, 16)) return MXA_ERR_ALIGN;
+  const bool tokblock = mode == MXA_SCALE_TOKBLOCK32;
+  if (mode != MXA_SCALE_MX32 && !tokblock) return MXA_ERR_ARG;
+  if (views <= 0 || (views & ~(MXA_VIEW_ROW | MXA_VIEW_TOK))) return MXA_ERR_ARG;
+  if (hadamard && (!tokblock || d != 128)) return MXA_ERR_UNSUPPORTED;
+  const bool w_row = (views & MXA_VIEW_ROW) != 0, w_tok = (views & MXA_VIEW_TOK) != 0;
+  if (tokblock) {
+    if (!(w_row && w_tok) || !row || !tok || !row->codes || !row->scales || !tok->scales) return MXA_ERR_ARG;
+    if (tok->codes && tok->codes != row->codes) return MXA_ERR_ARG;
+    if (!aligned(row->codes, 16) || !aligned(row->scales, 16) || !aligned(tok->scales, 16)) return MXA_ERR_ALIGN;
+  } else {
+    if (w_row) {
+      if (!row) return MXA_ERR_ARG;
+      mxa_status st = check_view(*row);
+      if (st != MXA_OK) return st;
+    }
+    if (w_tok) {
+      if (!tok) return MXA_ERR_ARG;
+      mxa_status st = check_view(*tok);
+      if (st != MXA_OK) return st;
+    }
+  }
+  if (T == 0) return MXA_OK;
+  const size_t sbytes = mxa_scale_bytes(H, ntiles);
+  if ((w_row || tokblock) && cudaMemsetAsync(row->scales, 0x7F, sbytes, stream) != cudaSuccess) return MXA_ERR_CUDA;
+  if ((w_tok || tokblock) && cudaMemsetAsync(tok->scales, 0x7F, sbytes, stream) != cudaSuccess) return MXA_ERR_CUDA;
+  QuantArgs a{};
+  a.x = x;
+  a.T = T;
+  a.H = H;
+  a.cu_seqlens = cu_seqlens;
+  a.num_docs = num_docs;
+  a.ntiles = ntiles;
+  a.write_row = w_row || tokblock;
+  a.write_tok = w_tok || tokblock;
+  a.row_codes = (w_row || tokblock) ? row->codes : nullptr;
+  a.row_scales = (w_row || tokblock) ? row->scales : nullptr;
+  a.tok_codes = (w_tok && !tokblock) ? tok->codes : nullptr;
+  a.tok_scales = (w_tok || tokblock) ? tok->scales : nullptr;
+  const int max_groups = (cu_seqlens ? max_seqlen : static_cast<int>(T / num_docs)) + 31;
+  if (launch_quantize(a, d, tokblock, hadamard != 0, max_groups / 32, stream) != cudaSuccess) return MXA_ERR_CUDA;
+  return MXA_OK;
+}
+
+mxa_status mxa_fwd(const mxa_fwd_params* p, cudaStream_t stream) {
+  if (!p) return MXA_ERR_ARG;
+  const mxa_shape& s = p->shape;
+  mxa_status st = check_shape(s);
+  if (st != MXA_OK) return st;
+  if ((st = check_view(p->q_row)) != MXA_OK || (st = check_view(p->k_row)) != MXA_OK ||
+      (st = check_view(p->v_tok)) != MXA_OK)
+    return st;
+  if (!p->o || !p->lse) return MXA_ERR_ARG;
+  if (!aligned(p->o, 16) || !aligned(p->lse, 4)) return MXA_ERR_ALIGN;
+  if (s.T == 0) return MXA_OK;
+  FwdMaps maps;
+  if (!make_code_map(&maps.q, p->q_row.codes, s.T, s.Hq, s.d) ||
+      !make_code_map(&maps.k, p->k_row.codes, s.T, s.Hkv, s.d) ||
+      !make_code_map(&maps.v, p->v_tok.codes, s.T, s.Hkv, s.d))
+    return MXA_ERR_CUDA;
+  FwdArgs a{};
+  a.T = s.T;
+  a.Hq = s.Hq;
+  a.Hkv = s.Hkv;
+  a.cu_seqlens = s.cu_seqlens;
+  a.num_docs = s.num_docs;
+  a.ntiles = s.ntiles;
+  a.causal = s.causal ? 1 : 0;
+  a.alpha = alpha_of(s);
+  a.scale_log2 = a.alpha * 1.4426950408889634f;
+  a.q_sf = p->q_row.scales;
+  a.k_sf = p->k_row.scales;
+  a.v_sf = p->v_tok.scales;
+  a.o = p->o;
+  a.lse = p->lse;
+  a.err = device_error_word();
+  const int maxlen = s.cu_seqlens ? s.max_seqlen : static_cast<int>(s.T / s.num_docs);
+  if (launch_fwd(a, maps, s.d, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
+  return MXA_OK;
+}
+
+size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p) {
+  if (!p || p->shape.T < 0 || p->shape.Hq <= 0 || (p->shape.d != 64 && p->shape.d != 128)) return 0;
+  const size_t T = static_cast<size_t>(p->shape.T), Hq = static_cast<size_t>(p->shape.Hq),
+               d = static_cast<size_t>(p->shape.d);
+  const size_t dbytes = ((Hq * T * 4) + 255) & ~size_t(255);
+  const size_t acc = T * Hq * d * (p->dq_mode == MXA_DQ_FP16_X512 ? 2 : 4);
+  return dbytes + ((acc + 255) & ~size_t(255));
+}
+
+mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (!p) return MXA_ERR_ARG;
+  const mxa_shape& s = p->shape;
+  mxa_status st = check_shape(s);
+  if (st != MXA_OK) return st;
+  const mxa_qview* vs[] = {&p->q_row, &p->k_row, &p->v_row, &p->g_row, &p->q_tok, &p->k_tok, &p->g_tok};
+  for (const mxa_qview* v : vs)
+    if ((st = check_view(*v)) != MXA_OK) return st;
+  if (!p->o || !p->lse || !p->dq || !p->dk || !p->dv) return MXA_ERR_ARG;
+  if (!aligned(p->o, 16) || !aligned(p->lse, 4) || !aligned(p->dq, 16) || !aligned(p->dk, 16) ||
+      !aligned(p->dv, 16))
+    return MXA_ERR_ALIGN;
+  if (p->dq_mode != MXA_DQ_FP32 && p->dq_mode != MXA_DQ_FP16_X512) return MXA_ERR_ARG;
+  if (!workspace || ws_bytes < mxa_bwd_workspace_bytes(p)) return MXA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return MXA_ERR_ALIGN;
+  if (s.T == 0) return MXA_OK;
+  BwdMaps maps;
+  if (!make_code_map(&maps.q, p->q_row.codes, s.T, s.Hq, s.d) ||
+      !make_code_map(&maps.k, p->k_row.codes, s.T, s.Hkv, s.d) ||
+      !make_code_map(&maps.v, p->v_row.codes, s.T, s.Hkv, s.d) ||
+      !make_code_map(&maps.g, p->g_row.codes, s.T, s.Hq, s.d) ||
+      !make_code_map(&maps.qt, p->q_tok.codes, s.T, s.Hq, s.d) ||
+      !make_code_map(&maps.kt, p->k_tok.codes, s.T, s.Hkv, s.d) ||
+      !make_code_map(&maps.gt, p->g_tok.codes, s.T, s.Hq, s.d))
+    return MXA_ERR_CUDA;
+  const size_t T = static_cast<size_t>(s.T), Hq = static_cast<size_t>(s.Hq), d = static_cast<size_t>(s.d);
+  const size_t dbytes = ((Hq * T * 4) + 255) & ~size_t(255);
+  float* dvec = static_cast<float*>(workspace);
+  void* acc = static_cast<uint8_t*>(workspace) + dbytes;
+  const size_t acc_bytes = T * Hq * d * (p->dq_mode == MXA_DQ_FP16_X512 ? 2 : 4);
+  const int maxlen = s.cu_seqlens ? s.max_seqlen : static_cast<int>(s.T / s.num_docs);
+
+  PrepArgs pa{};
+  pa.T = s.T;
+  pa.Hq = s.Hq;
+  pa.d = s.d;
+  pa.g_codes = p->g_row.codes;
+  pa.g_sf = p->g_row.scales;
+  pa.cu_seqlens = s.cu_seqlens;
+  pa.num_docs = s.num_docs;
+  pa.ntiles = s.ntiles;
+  pa.o = p->o;
+  pa.dvec = dvec;
+  pa.dq_acc = acc;
+  pa.dq_acc_bytes = acc_bytes;
+  if (launch_bwd_prep(pa, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
+
+  BwdArgs a{};
+  a.T = s.T;
+  a.Hq = s.Hq;
+  a.Hkv = s.Hkv;
+  a.cu_seqlens = s.cu_seqlens;
+  a.num_docs = s.num_docs;
+  a.ntiles = s.ntiles;
+  a.causal = s.causal ? 1 : 0;
+  a.alpha = alpha_of(s);
+  a.scale_log2 = a.alpha * 1.4426950408889634f;
+  a.q_sf = p->q_row.scales;
+  a.k_sf = p->k_row.scales;
+  a.v_sf = p->v_row.scales;
+  a.g_sf = p->g_row.scales;
+  a.qt_sf = p->q_tok.scales;
+  a.kt_sf = p->k_tok.scales;
+  a.gt_sf = p->g_tok.scales;
+  a.lse = p->lse;
+  a.dvec = dvec;
+  a.dq_mode = p->dq_mode;
+  a.dq_acc32 = p->dq_mode == MXA_DQ_FP32 ? static_cast<float*>(acc) : nullptr;
+  a.dq_acc16 = p->dq_mode == MXA_DQ_FP16_X512 ? static_cast<uint16_t*>(acc) : nullptr;
+  a.dk = p->dk;
+  a.dv = p->dv;
+  a.err = device_error_word();
+  if (launch_bwd(a, maps, s.d, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
+
+  DqConvArgs c{};
+  c.n = static_cast<int64_t>(T * Hq * d);
+  c.acc32 = a.dq_acc32;
+  c.acc16 = a.dq_acc16;
+  c.mode = p->dq_mode;
+  c.dq = p->dq;
+  if (launch_dq_convert(c, stream) != cudaSuccess) return MXA_ERR_CUDA;
+  return MXA_OK;
+}
+
+mxa_status mxa_get_error(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MXA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_word, sizeof(int)) != cudaSuccess) return MXA_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(g_err_word, &zero, sizeof(int));
+    return MXA_ERR_TIMEOUT;
+  }
+  return MXA_OK;
+}
+
+}  // extern "C"

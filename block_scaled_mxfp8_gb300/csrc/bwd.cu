@@ -1,0 +1,612 @@
+// bwd.cu -- MXFP8 block-scaled attention backward (tcgen05, TMEM, TMA).
+//
+// Three launches (FLAMIA notes sec. 2 and Algorithm 1, steps 09-16):
+//   bwd_prep_kernel   : D_i = sum_c G_ic O_ic with G from its ROW view (the
+//                       same G representation the dP product uses) and O the
+//                       forward's bf16 output.
+//   attn_bwd_kernel   : one CTA per (128-key tile, kv head, document); loops
+//                       over the query heads of the kv group and the visible
+//                       128-query tiles:
+//                         S^T  = K Q^T            (ROW views)
+//                         P^T  = exp(alpha S^T - LSE)  (the forward's exp rule)
+//                         dP^T = V G^T            (ROW views)
+//                         dS^T = P^T (dP^T - D), quantized per 32 x 32 block
+//                                from the block max-abs, taken with a warp
+//                                max reduction in the register layout (a warp
+//                                owns 32 key rows) -- no transpose (FA4
+//                                write-up, "Квантование dS без транспонирования")
+//                         dV  += E4M3(2^8 P^T) G  (scale 2^-8; G TOK view)
+//                         dK  += dS^T Q           (Q TOK view)
+//                         dQ_i = dS K             (K TOK view; the dS^T codes in
+//                                shared memory read as an MN-major operand)
+//                       dQ_i is added to a global accumulator in fp32, or in
+//                       fp16 after a 2^9 boost.
+//   dq_convert_kernel : dQ = acc (fp32) or acc * 2^-9 (fp16) -> bf16.
+//
+// TMEM columns (512): X [0,128) holds S^T, then dP^T, then the dQ tile;
+// dV [128,256), dK [256,384); P^T codes [384,416), dS^T codes [416,448);
+// scale factors from 448 (4 columns each).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace mxa {
+
+namespace {
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kStages = 2;
+  static constexpr int kTileBytes = 128 * D;
+  static constexpr uint32_t kSwz = D == 128 ? kSwz128 : kSwz64;
+  static constexpr uint32_t kSBO = 8 * D;
+  static constexpr int kKSteps = D / 32;
+  static constexpr int kThreads = 256;
+  // TMEM columns
+  static constexpr uint32_t kColX = 0, kColDV = 128, kColDK = 256, kColP = 384, kColDS = 416;
+  static constexpr uint32_t kSfK = 448, kSfQ = 452 /*+4s*/, kSfV = 460, kSfG = 464 /*+4s*/, kSfP = 472,
+                            kSfGt = 476 /*+4s*/, kSfDSk = 484, kSfQt = 488 /*+4s*/, kSfDSq = 496, kSfKt = 500;
+  // shared memory (offsets from the 1024-aligned base)
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kTileBytes;
+  static constexpr int kOffKt = kOffV + kTileBytes;
+  static constexpr int kOffDS = kOffKt + kTileBytes;                 // 128 x 128 dS^T codes, SW128
+  static constexpr int kOffStage = kOffDS + 128 * 128;               // per-stage Q, G, Qt, Gt tiles
+  static constexpr int kStageBytes = 4 * kTileBytes;
+  static constexpr int kOffSf = kOffStage + kStages * kStageBytes;   // atoms: K, V, Kt, then 4 per stage
+  static constexpr int kOffLse = kOffSf + (3 + 4 * kStages) * kAtomBytes;  // 2 x 128 floats
+  static constexpr int kOffDv = kOffLse + 2 * 128 * 4;                      // 2 x 128 floats
+  static constexpr int kSmemBytes = kOffDv + 2 * 128 * 4 + 1024;
+};
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                          int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  uint32_t it = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > kWaitBudgetCycles) {
+        *abort_flag = 1;
+        if (err) atomicCAS(err, 0, code);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, const void* smem_atom) {
+  const uint64_t desc = make_sdesc(smem_u32(smem_atom), 512, 128, kSwzNone);
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
+__device__ __forceinline__ int64_t doc_tile_base(const int32_t* cu, int b, int64_t len, int tid, int nthreads,
+                                                 int64_t* s_slot) {
+  if (cu == nullptr) return static_cast<int64_t>(b) * ((len + 127) / 128);
+  if (tid == 0) *s_slot = 0;
+  __syncthreads();
+  int64_t part = 0;
+  for (int i = tid; i < b; i += nthreads) part += (cu[i + 1] - cu[i] + 127) / 128;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if ((tid & 31) == 0 && part) atomicAdd(reinterpret_cast<unsigned long long*>(s_slot), static_cast<unsigned long long>(part));
+  __syncthreads();
+  return *s_slot;
+}
+
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two_codes)));
+  __half2 hv = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(hv);
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------- D prep
+// One warp per (token, head); grid over (32-token group, doc, head).
+__global__ void __launch_bounds__(256) bwd_prep_kernel(PrepArgs a) {
+  __shared__ int64_t s_slot;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
+  int64_t doc_start, n;
+  doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
+  if (static_cast<int64_t>(g) * 32 >= n) return;
+  const int64_t tb = doc_tile_base(a.cu_seqlens, b, n, tid, 256, &s_slot);
+  for (int rr = warp; rr < 32; rr += 8) {
+    const int64_t pos = static_cast<int64_t>(g) * 32 + rr;
+    if (pos >= n) break;
+    const int64_t t = doc_start + pos;
+    const int i = static_cast<int>(pos >> 7), r = static_cast<int>(pos & 127);
+    const uint8_t* atom = a.g_sf + (static_cast<int64_t>(h) * a.ntiles + tb + i) * kAtomBytes;
+    float acc = 0.0f;
+    // lane covers channels [4 lane, 4 lane + 4) for d = 128, [2 lane, 2 lane + 2) for d = 64
+    if (a.d == 128) {
+      const int c0 = 4 * lane;
+      const uint32_t codes = *reinterpret_cast<const uint32_t*>(a.g_codes + (t * a.Hq + h) * 128 + c0);
+      const float sc = exp2f(static_cast<float>(static_cast<int>(atom[atom_offset(r, c0 / 32)]) - 127));
+      const uint2 ov = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.o) + (t * a.Hq + h) * 128 + c0);
+      const float2 g01 = e4m3x2_to_f32x2(codes & 0xFFFFu), g23 = e4m3x2_to_f32x2(codes >> 16);
+      const float o0 = __uint_as_float(ov.x << 16), o1 = __uint_as_float(ov.x & 0xFFFF0000u);
+      const float o2 = __uint_as_float(ov.y << 16), o3 = __uint_as_float(ov.y & 0xFFFF0000u);
+      acc = (g01.x * o0 + g01.y * o1 + g23.x * o2 + g23.y * o3) * sc;
+    } else {
+      const int c0 = 2 * lane;
+      const uint16_t codes = *reinterpret_cast<const uint16_t*>(a.g_codes + (t * a.Hq + h) * 64 + c0);
+      const float sc = exp2f(static_cast<float>(static_cast<int>(atom[atom_offset(r, c0 / 32)]) - 127));
+      const uint32_t ov = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(a.o) + (t * a.Hq + h) * 64 + c0);
+      const float2 g01 = e4m3x2_to_f32x2(codes);
+      acc = (g01.x * __uint_as_float(ov << 16) + g01.y * __uint_as_float(ov & 0xFFFF0000u)) * sc;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) a.dvec[static_cast<int64_t>(h) * a.T + t] = acc;
+  }
+}
+
+// ----------------------------------------------------------------- dQ convert
+__global__ void __launch_bounds__(256) dq_convert_kernel(DqConvArgs a) {
+  const int64_t n4 = a.n / 4;
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.dq);
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float v0, v1, v2, v3;
+    if (a.mode == 0) {
+      const float4 f = reinterpret_cast<const float4*>(a.acc32)[i];
+      v0 = f.x, v1 = f.y, v2 = f.z, v3 = f.w;
+    } else {
+      const uint2 hv = reinterpret_cast<const uint2*>(a.acc16)[i];
+      const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&hv.x));
+      const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&hv.y));
+      const float inv = 1.0f / 512.0f;
+      v0 = f01.x * inv, v1 = f01.y * inv, v2 = f23.x * inv, v3 = f23.y * inv;
+    }
+    __nv_bfloat162 b0 = __floats2bfloat162_rn(v0, v1), b1 = __floats2bfloat162_rn(v2, v3);
+    uint2 o;
+    o.x = *reinterpret_cast<uint32_t*>(&b0);
+    o.y = *reinterpret_cast<uint32_t*>(&b1);
+    reinterpret_cast<uint2*>(out)[i] = o;
+  }
+}
+
+// ----------------------------------------------------------------- main
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
+    attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  __shared__ uint64_t bar_kv, bar_tile_full[C::kStages], bar_tile_empty[C::kStages], bar_s_full, bar_x_free,
+      bar_dp_full, bar_p_ready, bar_dq_full, bar_x_free2, bar_final, bar_drain, bar_lse[2], bar_e[2];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int64_t s_slot;
+  __shared__ uint32_t s_e[2][4][4];  // dS block exponent bytes [parity][key block][query block]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kt = blockIdx.x, b = blockIdx.y, hk = blockIdx.z;
+  const int grp = a.Hq / a.Hkv;
+  int64_t doc_start, n;
+  doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
+  const int n_tiles = static_cast<int>((n + 127) / 128);
+  if (kt >= n_tiles) return;
+  const int qi0 = a.causal ? kt : 0;
+  const int nq = n_tiles - qi0;       // query tiles per head
+  const int n_work = nq * grp;        // (head, query tile) items
+  const int64_t tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, C::kThreads, &s_slot);
+
+  if (tid == 0) {
+    mbar_init(&bar_kv, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bar_tile_full[s], 1);
+      mbar_init(&bar_tile_empty[s], 1);
+    }
+    mbar_init(&bar_s_full, 1);
+    mbar_init(&bar_x_free, 128);
+    mbar_init(&bar_dp_full, 1);
+    mbar_init(&bar_p_ready, 128);
+    mbar_init(&bar_dq_full, 1);
+    mbar_init(&bar_x_free2, 128);
+    mbar_init(&bar_final, 1);
+    mbar_init(&bar_drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_lse[i], 128);
+      mbar_init(&bar_e[i], 128);
+    }
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(&s_tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int* abort_flag = &s_abort;
+
+  uint8_t* sK = smem + C::kOffK;
+  uint8_t* sV = smem + C::kOffV;
+  uint8_t* sKt = smem + C::kOffKt;
+  uint8_t* sDS = smem + C::kOffDS;
+  uint8_t* sSf = smem + C::kOffSf;  // [0]=K, [1]=V, [2]=Kt, then stage s: 3+4s .. (Q, G, Qt, Gt)
+  float* sLse = reinterpret_cast<float*>(smem + C::kOffLse);
+  float* sDv = reinterpret_cast<float*>(smem + C::kOffDv);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&maps.q);
+      tma_prefetch_desc(&maps.g);
+      tma_prefetch_desc(&maps.qt);
+      tma_prefetch_desc(&maps.gt);
+      const int64_t k0 = doc_start + static_cast<int64_t>(kt) * 128;
+      const int64_t katom = (static_cast<int64_t>(hk) * a.ntiles + tile_base + kt) * kAtomBytes;
+      mbar_arrive_expect_tx(&bar_kv, 3 * C::kTileBytes + 3 * kAtomBytes);
+      tma_load_3d(sK, &maps.k, &bar_kv, 0, hk, static_cast<int>(k0));
+      tma_load_3d(sV, &maps.v, &bar_kv, 0, hk, static_cast<int>(k0));
+      tma_load_3d(sKt, &maps.kt, &bar_kv, 0, hk, static_cast<int>(k0));
+      bulk_load(sSf + 0 * kAtomBytes, a.k_sf + katom, kAtomBytes, &bar_kv);
+      bulk_load(sSf + 1 * kAtomBytes, a.v_sf + katom, kAtomBytes, &bar_kv);
+      bulk_load(sSf + 2 * kAtomBytes, a.kt_sf + katom, kAtomBytes, &bar_kv);
+      int issued = 0;
+      for (int u = 0; u < n_work; ++u) {
+        const int s = u % C::kStages;
+        if (u >= C::kStages &&
+            !role_wait(&bar_tile_empty[s], ((u / C::kStages) - 1) & 1, abort_flag, a.err, kErrTimeoutTma))
+          break;
+        const int h = hk * grp + u / nq;
+        const int qi = qi0 + u % nq;
+        const int64_t q0 = doc_start + static_cast<int64_t>(qi) * 128;
+        const int64_t qatom = (static_cast<int64_t>(h) * a.ntiles + tile_base + qi) * kAtomBytes;
+        uint8_t* st = smem + C::kOffStage + s * C::kStageBytes;
+        uint8_t* sf = sSf + (3 + 4 * s) * kAtomBytes;
+        mbar_arrive_expect_tx(&bar_tile_full[s], 4 * C::kTileBytes + 4 * kAtomBytes);
+        tma_load_3d(st + 0 * C::kTileBytes, &maps.q, &bar_tile_full[s], 0, h, static_cast<int>(q0));
+        tma_load_3d(st + 1 * C::kTileBytes, &maps.g, &bar_tile_full[s], 0, h, static_cast<int>(q0));
+        tma_load_3d(st + 2 * C::kTileBytes, &maps.qt, &bar_tile_full[s], 0, h, static_cast<int>(q0));
+        tma_load_3d(st + 3 * C::kTileBytes, &maps.gt, &bar_tile_full[s], 0, h, static_cast<int>(q0));
+        bulk_load(sf + 0 * kAtomBytes, a.q_sf + qatom, kAtomBytes, &bar_tile_full[s]);
+        bulk_load(sf + 1 * kAtomBytes, a.g_sf + qatom, kAtomBytes, &bar_tile_full[s]);
+        bulk_load(sf + 2 * kAtomBytes, a.qt_sf + qatom, kAtomBytes, &bar_tile_full[s]);
+        bulk_load(sf + 3 * kAtomBytes, a.gt_sf + qatom, kAtomBytes, &bar_tile_full[s]);
+        issued = u + 1;
+      }
+      role_wait(&bar_kv, 0, abort_flag, nullptr, 0);
+      for (int u = (issued > C::kStages ? issued - C::kStages : 0); u < issued; ++u)
+        mbar_wait(&bar_tile_full[u % C::kStages], (u / C::kStages) & 1, nullptr, 0);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = role_wait(&bar_kv, 0, abort_flag, a.err, kErrTimeoutMma);
+      if (ok) {
+        tc_fence_after();
+        tmem_cp_atom(tmem + C::kSfK, sSf + 0 * kAtomBytes);
+        tmem_cp_atom(tmem + C::kSfV, sSf + 1 * kAtomBytes);
+        tmem_cp_atom(tmem + C::kSfKt, sSf + 2 * kAtomBytes);
+      }
+      const uint32_t ka = smem_u32(sK), va = smem_u32(sV), kta = smem_u32(sKt), dsa = smem_u32(sDS);
+      for (int u = 0; ok && u < n_work; ++u) {
+        const int s = u % C::kStages;
+        const uint32_t st = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
+        const uint8_t* sf = sSf + (3 + 4 * s) * kAtomBytes;
+        if (!(ok = role_wait(&bar_tile_full[s], (u / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        // X must be free: the previous dQ tile has been read out
+        if (u > 0 && !(ok = role_wait(&bar_x_free2, (u - 1) & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        tc_fence_after();
+        // S^T = K Q^T
+        tmem_cp_atom(tmem + C::kSfQ + 4 * s, sf + 0 * kAtomBytes);
+#pragma unroll
+        for (int kk = 0; kk < C::kKSteps; ++kk)
+          mma_mxf8_ss(tmem + C::kColX, make_sdesc(ka + 32 * kk, 16, C::kSBO, C::kSwz),
+                      make_sdesc(st + 0 * C::kTileBytes + 32 * kk, 16, C::kSBO, C::kSwz),
+                      make_idesc_mxf8(128, 128, 0, 0, kk, kk), tmem + C::kSfK, tmem + C::kSfQ + 4 * s, kk > 0);
+        mma_commit(&bar_s_full);
+        // dP^T = V G^T, once the softmax warps have read S^T out of X
+        if (!(ok = role_wait(&bar_x_free, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        tc_fence_after();
+        tmem_cp_atom(tmem + C::kSfG + 4 * s, sf + 1 * kAtomBytes);
+#pragma unroll
+        for (int kk = 0; kk < C::kKSteps; ++kk)
+          mma_mxf8_ss(tmem + C::kColX, make_sdesc(va + 32 * kk, 16, C::kSBO, C::kSwz),
+                      make_sdesc(st + 1 * C::kTileBytes + 32 * kk, 16, C::kSBO, C::kSwz),
+                      make_idesc_mxf8(128, 128, 0, 0, kk, kk), tmem + C::kSfV, tmem + C::kSfG + 4 * s, kk > 0);
+        mma_commit(&bar_dp_full);
+        // gradients, once P^T, dS^T and their scales are in place
+        if (!(ok = role_wait(&bar_p_ready, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        tc_fence_after();
+        tmem_cp_atom(tmem + C::kSfGt + 4 * s, sf + 3 * kAtomBytes);
+        tmem_cp_atom(tmem + C::kSfQt + 4 * s, sf + 2 * kAtomBytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // dV += P^T G  (contraction over 128 queries)
+          mma_mxf8_ts(tmem + C::kColDV, tmem + C::kColP + 8 * kk,
+                      make_sdesc(st + 3 * C::kTileBytes + kk * 32 * D, 16, C::kSBO, C::kSwz),
+                      make_idesc_mxf8(128, D, 0, 1, kk, kk), tmem + C::kSfP, tmem + C::kSfGt + 4 * s,
+                      (u > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // dK += dS^T Q
+          mma_mxf8_ts(tmem + C::kColDK, tmem + C::kColDS + 8 * kk,
+                      make_sdesc(st + 2 * C::kTileBytes + kk * 32 * D, 16, C::kSBO, C::kSwz),
+                      make_idesc_mxf8(128, D, 0, 1, kk, kk), tmem + C::kSfDSk, tmem + C::kSfQt + 4 * s,
+                      (u > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // dQ tile = dS K  (contraction over 128 keys)
+          mma_mxf8_ss(tmem + C::kColX, make_sdesc(dsa + kk * 32 * 128, 16, 1024, kSwz128),
+                      make_sdesc(kta + kk * 32 * D, 16, C::kSBO, C::kSwz), make_idesc_mxf8(128, D, 1, 1, kk, kk),
+                      tmem + C::kSfDSq, tmem + C::kSfKt, kk > 0 ? 1u : 0u);
+        mma_commit(&bar_dq_full);
+        mma_commit(&bar_tile_empty[s]);
+      }
+      mma_commit(&bar_final);
+      mma_commit(&bar_drain);
+      mbar_wait(&bar_drain, 0, nullptr, 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax / dS / epilogues
+    const int quad = warp & 3;
+    const int j = quad * 32 + lane;  // key row of this thread (TMEM lane)
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const int64_t kpos = static_cast<int64_t>(kt) * 128 + j;
+    const bool key_valid = kpos < n;
+    const float sl2 = a.scale_log2;
+    // constant P^T scale 2^-8
+    tmem_st4(lane_base + C::kSfP, 0x77777777u, 0x77777777u, 0x77777777u, 0x77777777u);
+    tmem_st_wait();
+    bool ok = true;
+    for (int u = 0; u < n_work; ++u) {
+      const int h = hk * grp + u / nq;
+      const int qi = qi0 + u % nq;
+      const int par = u & 1;
+      // LSE (log2 units) and D of the 128 queries of this tile
+      {
+        const int c = quad * 32 + lane;
+        const int64_t qp = static_cast<int64_t>(qi) * 128 + c;
+        float l2 = 0.0f, dd = 0.0f;
+        if (qp < n) {
+          const int64_t t = doc_start + qp;
+          l2 = a.lse[static_cast<int64_t>(h) * a.T + t] * 1.4426950408889634f;
+          dd = a.dvec[static_cast<int64_t>(h) * a.T + t];
+        }
+        sLse[par * 128 + c] = l2;
+        sDv[par * 128 + c] = dd;
+      }
+      mbar_arrive(&bar_lse[par]);
+      ok = role_wait(&bar_lse[par], (u >> 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      ok = role_wait(&bar_s_full, u & 1, abort_flag, a.err, kErrTimeoutSoftmax);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float p[128];
+      {
+        uint32_t rr[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(lane_base + C::kColX + 32 * c, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) p[32 * c + i] = __uint_as_float(rr[i]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bar_x_free);
+      const int64_t qbase = static_cast<int64_t>(qi) * 128;
+      const bool full = key_valid && (qbase + 127 < n) && (!a.causal || kpos <= qbase);
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float v = ex2_approx(fmaf(p[c], sl2, -sLse[par * 128 + c]));
+        const int64_t qp = qbase + c;
+        p[c] = (full || (key_valid && qp < n && (!a.causal || kpos <= qp))) ? v : 0.0f;
+      }
+      // P^T codes, boosted by 2^8 (P <= 1 after the LSE normalisation)
+#pragma unroll
+      for (int c = 0; c < 32; c += 8) {
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          w[k] = pack_e4m3x4(p[4 * (c + k)] * 256.0f, p[4 * (c + k) + 1] * 256.0f, p[4 * (c + k) + 2] * 256.0f,
+                             p[4 * (c + k) + 3] * 256.0f);
+        tmem_st8(lane_base + C::kColP + c, w);
+      }
+      ok = role_wait(&bar_dp_full, u & 1, abort_flag, a.err, kErrTimeoutSoftmax);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t ebytes = 0;  // this warp's 4 block exponents (query block c in byte c)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(lane_base + C::kColX + 32 * c, rr);
+        tmem_ld_wait();
+        float ds[32];
+        float am = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          ds[i] = p[32 * c + i] * (__uint_as_float(rr[i]) - sDv[par * 128 + 32 * c + i]);
+          am = fmaxf(am, fabsf(ds[i]));
+        }
+        // 32 x 32 block max-abs: this thread's 32 values, then the warp's 32 key rows
+        am = warp_max_abs(am);
+        const int e = mx_exponent_bits(__float_as_uint(am));
+        const float sc = exp2i_neg(e);
+        ebytes |= static_cast<uint32_t>(e + 127) << (8 * c);
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          w[k] = pack_e4m3x4(ds[4 * k] * sc, ds[4 * k + 1] * sc, ds[4 * k + 2] * sc, ds[4 * k + 3] * sc);
+        tmem_st8(lane_base + C::kColDS + 8 * c, w);
+        // row j of the dS^T tile in shared memory, 128B-swizzled (queries contiguous)
+        uint4* row = reinterpret_cast<uint4*>(sDS + j * 128);
+        row[(2 * c) ^ (j & 7)] = make_uint4(w[0], w[1], w[2], w[3]);
+        row[(2 * c + 1) ^ (j & 7)] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) s_e[par][quad][c] = (ebytes >> (8 * c)) & 0xFF;
+      }
+      mbar_arrive(&bar_e[par]);
+      ok = role_wait(&bar_e[par], (u >> 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      {
+        // dK operand A = dS^T: row = key, groups along queries -> column q = e[q][0..3]
+        // dQ operand A = dS  : row = query, groups along keys -> column q = e[0..3][q]
+        uint32_t ck[4], cq[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          ck[q] = s_e[par][q][0] | (s_e[par][q][1] << 8) | (s_e[par][q][2] << 16) | (s_e[par][q][3] << 24);
+          cq[q] = s_e[par][0][q] | (s_e[par][1][q] << 8) | (s_e[par][2][q] << 16) | (s_e[par][3][q] << 24);
+        }
+        tmem_st4(lane_base + C::kSfDSk, ck[0], ck[1], ck[2], ck[3]);
+        tmem_st4(lane_base + C::kSfDSq, cq[0], cq[1], cq[2], cq[3]);
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar_p_ready);
+      // dQ tile (rows = queries) -> global accumulator
+      ok = role_wait(&bar_dq_full, u & 1, abort_flag, a.err, kErrTimeoutEpilogue);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        const int64_t qp = qbase + j;  // TMEM lane j is query row j of the dQ tile
+        const bool qv = qp < n;
+        const int64_t t = doc_start + qp;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(lane_base + C::kColX + 32 * c, rr);
+          tmem_ld_wait();
+          if (qv) {
+            if (a.dq_mode == 0) {
+              float* dst = a.dq_acc32 + (t * a.Hq + h) * D + 32 * c;
+#pragma unroll
+              for (int i = 0; i < 32; i += 4)
+                asm volatile("red.global.add.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(dst + i),
+                             "f"(__uint_as_float(rr[i]) * a.alpha), "f"(__uint_as_float(rr[i + 1]) * a.alpha),
+                             "f"(__uint_as_float(rr[i + 2]) * a.alpha), "f"(__uint_as_float(rr[i + 3]) * a.alpha)
+                             : "memory");
+            } else {
+              uint16_t* dst = a.dq_acc16 + (t * a.Hq + h) * D + 32 * c;
+              const float bst = a.alpha * 512.0f;
+#pragma unroll
+              for (int i = 0; i < 32; i += 8) {
+                uint32_t hw[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  __half2 hv = __floats2half2_rn(__uint_as_float(rr[i + 2 * k]) * bst, __uint_as_float(rr[i + 2 * k + 1]) * bst);
+                  hw[k] = *reinterpret_cast<uint32_t*>(&hv);
+                }
+                asm volatile("red.global.add.noftz.v4.f16x2 [%0], {%1,%2,%3,%4};" ::"l"(dst + i), "r"(hw[0]),
+                             "r"(hw[1]), "r"(hw[2]), "r"(hw[3])
+                             : "memory");
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bar_x_free2);
+    }
+    // ---------------------------------------------------------- dK, dV out
+    if (ok) ok = role_wait(&bar_final, 0, abort_flag, a.err, kErrTimeoutEpilogue);
+    if (__all_sync(0xffffffffu, ok)) {
+      tc_fence_after();
+      const int64_t t = doc_start + kpos;
+      __nv_bfloat16* dvrow = reinterpret_cast<__nv_bfloat16*>(a.dv) + (t * a.Hkv + hk) * D;
+      __nv_bfloat16* dkrow = reinterpret_cast<__nv_bfloat16*>(a.dk) + (t * a.Hkv + hk) * D;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
+        const float mul = which == 0 ? 1.0f : a.alpha;
+        __nv_bfloat16* dst = which == 0 ? dvrow : dkrow;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(lane_base + col + 32 * c, rr);
+          tmem_ld_wait();
+          if (key_valid) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              uint4 v;
+              __nv_bfloat162 b0 = __floats2bfloat162_rn(__uint_as_float(rr[i]) * mul, __uint_as_float(rr[i + 1]) * mul);
+              __nv_bfloat162 b1 = __floats2bfloat162_rn(__uint_as_float(rr[i + 2]) * mul, __uint_as_float(rr[i + 3]) * mul);
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(rr[i + 4]) * mul, __uint_as_float(rr[i + 5]) * mul);
+              __nv_bfloat162 b3 = __floats2bfloat162_rn(__uint_as_float(rr[i + 6]) * mul, __uint_as_float(rr[i + 7]) * mul);
+              v.x = *reinterpret_cast<uint32_t*>(&b0);
+              v.y = *reinterpret_cast<uint32_t*>(&b1);
+              v.z = *reinterpret_cast<uint32_t*>(&b2);
+              v.w = *reinterpret_cast<uint32_t*>(&b3);
+              *reinterpret_cast<uint4*>(dst + 32 * c + i) = v;
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+cudaError_t launch_bwd_prep(const PrepArgs& a, int max_seqlen, cudaStream_t stream) {
+  if (cudaMemsetAsync(a.dq_acc, 0, a.dq_acc_bytes, stream) != cudaSuccess) return cudaGetLastError();
+  dim3 grid((max_seqlen + 31) / 32, a.num_docs, a.Hq);
+  bwd_prep_kernel<<<grid, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(const DqConvArgs& a, cudaStream_t stream) {
+  const int64_t n4 = a.n / 4;
+  int blocks = static_cast<int>((n4 + 255) / 256);
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  dq_convert_kernel<<<blocks, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
+  dim3 grid((max_seqlen + 127) / 128, a.num_docs, a.Hkv);
+  if (d == 128) {
+    using C = BwdCfg<128>;
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attn_bwd_kernel<128><<<grid, C::kThreads, C::kSmemBytes, stream>>>(m, a);
+  } else {
+    using C = BwdCfg<64>;
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attn_bwd_kernel<64><<<grid, C::kThreads, C::kSmemBytes, stream>>>(m, a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace mxa

@@ -1,0 +1,125 @@
+// kernels.cuh -- kernel argument structs, shared device helpers and launchers.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mxa {
+
+// Bytes of one scale atom: 128 rows x 4 groups of 32, in the order the
+// tensor core reads after a 32x128b.warpx4 copy: byte (r % 32) * 16 +
+// (r / 32) * 4 + g.
+constexpr int kAtomBytes = 512;
+
+__device__ __forceinline__ int atom_offset(int r, int g) { return (r & 31) * 16 + (r >> 5) * 4 + g; }
+
+// Document b: first token and length.  cu == nullptr: num_docs equal docs.
+__device__ __forceinline__ void doc_bounds(const int32_t* cu, int num_docs, int64_t T, int b, int64_t& start,
+                                           int64_t& len) {
+  if (cu) {
+    start = cu[b];
+    len = static_cast<int64_t>(cu[b + 1]) - cu[b];
+  } else {
+    const int64_t L = T / num_docs;
+    start = static_cast<int64_t>(b) * L;
+    len = L;
+  }
+}
+
+struct QuantArgs {
+  const void* x;  // bf16 [T, H, d]
+  int64_t T;
+  int H;
+  const int32_t* cu_seqlens;
+  int num_docs;
+  int64_t ntiles;  // scale tiles NT (128-token tiles summed over documents)
+  int write_row, write_tok;
+  uint8_t* row_codes;
+  uint8_t* row_scales;  // [H, NT, 512]
+  uint8_t* tok_codes;
+  uint8_t* tok_scales;  // [H, NT, 512]
+};
+
+struct FwdArgs {
+  int64_t T;
+  int Hq, Hkv;
+  const int32_t* cu_seqlens;
+  int num_docs;
+  int64_t ntiles;
+  int causal;
+  float scale_log2;  // alpha * log2(e)
+  float alpha;
+  const uint8_t* q_sf;  // ROW scales of Q [Hq, NT, 512]
+  const uint8_t* k_sf;  // ROW scales of K [Hkv, NT, 512]
+  const uint8_t* v_sf;  // TOK scales of V [Hkv, NT, 512]
+  void* o;              // bf16 [T, Hq, d]
+  float* lse;           // [Hq, T]
+  int* err;
+};
+
+struct BwdArgs {
+  int64_t T;
+  int Hq, Hkv;
+  const int32_t* cu_seqlens;
+  int num_docs;
+  int64_t ntiles;
+  int causal;
+  float scale_log2;
+  float alpha;
+  const uint8_t* q_sf;   // Q ROW
+  const uint8_t* k_sf;   // K ROW
+  const uint8_t* v_sf;   // V ROW
+  const uint8_t* g_sf;   // G ROW
+  const uint8_t* qt_sf;  // Q TOK
+  const uint8_t* kt_sf;  // K TOK
+  const uint8_t* gt_sf;  // G TOK
+  const float* lse;      // [Hq, T]
+  const float* dvec;     // D [Hq, T]
+  float* dq_acc32;       // [T, Hq, d] (FP32 mode)
+  uint16_t* dq_acc16;    // [T, Hq, d] fp16 bits (FP16 x 2^9 mode)
+  void* dk;              // bf16 [T, Hkv, d]
+  void* dv;              // bf16 [T, Hkv, d]
+  int dq_mode;
+  int* err;
+};
+
+struct PrepArgs {
+  int64_t T;
+  int Hq, d;
+  const uint8_t* g_codes;  // G ROW codes [T, Hq, d]
+  const uint8_t* g_sf;     // G ROW scales [Hq, NT, 512]
+  const int32_t* cu_seqlens;
+  int num_docs;
+  int64_t ntiles;
+  const void* o;  // bf16 [T, Hq, d]
+  float* dvec;    // [Hq, T]
+  void* dq_acc;   // zeroed here
+  size_t dq_acc_bytes;
+};
+
+struct DqConvArgs {
+  int64_t n;  // elements
+  const float* acc32;
+  const uint16_t* acc16;
+  int mode;
+  void* dq;  // bf16
+};
+
+// Tensor maps of one attention call (3-D: d, H, T; SW128 for d = 128, SW64 for d = 64).
+struct FwdMaps {
+  CUtensorMap q, k, v;
+};
+struct BwdMaps {
+  CUtensorMap q, k, v, g, qt, kt, gt;
+};
+
+cudaError_t launch_quantize(const QuantArgs& a, int d, bool tokblock, bool hadamard, int max_groups,
+                            cudaStream_t stream);
+cudaError_t launch_fwd(const FwdArgs& a, const FwdMaps& m, int d, int max_seqlen, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream);
+cudaError_t launch_bwd_prep(const PrepArgs& a, int max_seqlen, cudaStream_t stream);
+cudaError_t launch_dq_convert(const DqConvArgs& a, cudaStream_t stream);
+
+int* device_error_word();
+
+}  // namespace mxa

@@ -1,0 +1,235 @@
+// quantize.cu -- bf16 -> MXFP8 quantizer (codes + UE8M0 scales), one pass.
+//
+// One CTA owns one (document, 32-token group, head) tile of 32 tokens x d
+// channels; it reads the bf16 tile once and writes every requested view:
+//   ROW view  : one scale per 32 channels of a token (groups along d), the
+//               view the Q K^T and dP = G V^T contractions use;
+//   TOK view  : one scale per 32 document-relative tokens of a channel
+//               (groups along tokens), the view P V, dV, dQ, dK use;
+//   TOKBLOCK  : one scale for the whole 32 x d tile, written into both
+//               layouts, one code set (FLAMIA notes sec. 3), optionally after
+//               a normalized 128-point Hadamard rotation of each token.
+// Scale rule: e = ceil(log2(amax / 448)) (FLAMIA notes sec. 4), computed
+// exactly from the fp32 bits; codes are cvt.rn.satfinite E4M3 of x * 2^-e.
+// Group max-abs: within a token row by warp shuffles; along tokens by warp
+// shuffles then one shared-memory pass across warps.
+// Memory-bound: 2 B read + (1 + 1/32) B written per element per view.
+#include <cuda_bf16.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace mxa {
+
+namespace {
+
+constexpr uint32_t kInvSqrt128Bits = 0x3DB504F3u;  // fp32 nearest to 128^-1/2
+
+template <int D>
+struct QCfg {
+  static constexpr int TPR = D / 16;            // threads per token row (16 channels each)
+  static constexpr int kThreads = 32 * TPR;     // 32 rows
+  static constexpr int kRowsPerWarp = 32 / TPR;
+  static constexpr int kWarps = kThreads / 32;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// One butterfly stage across threads: partner differs in chunk bit `bit`.
+__device__ __forceinline__ void had_cross(float (&v)[16], int chunk, int lane_xor) {
+  bool upper = ((chunk & lane_xor) == 0);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float other = __shfl_xor_sync(0xffffffffu, v[i], lane_xor);
+    // upper element j: a + b with a = v[j] (mine), b = v[j+h] (partner)
+    // lower element j+h: a - b with a = partner, b = mine
+    v[i] = upper ? (v[i] + other) : (other - v[i]);
+  }
+}
+
+}  // namespace
+
+template <int D, bool TOKBLOCK, bool HAD>
+__global__ void __launch_bounds__(QCfg<D>::kThreads) quantize_kernel(QuantArgs a) {
+  using C = QCfg<D>;
+  __shared__ float s_red[C::kWarps][D];
+  __shared__ int s_e[D];
+  __shared__ float s_blk[C::kWarps];
+  __shared__ int64_t s_tile_base;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int row = tid / C::TPR;      // token row in the 32-token group
+  const int chunk = tid % C::TPR;    // 16-channel chunk
+  const int g = blockIdx.x;          // group index inside the document
+  const int b = blockIdx.y;          // document
+  const int h = blockIdx.z;          // head
+
+  int64_t doc_start, doc_len;
+  doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, doc_len);
+  if (static_cast<int64_t>(g) * 32 >= doc_len) return;  // past this document's last group
+
+  // First scale tile of this document (each document owns ceil(n / 128)
+  // consecutive 128-token tiles in the [H, NT, 512] scale layouts).
+  if (a.cu_seqlens == nullptr) {
+    if (tid == 0) s_tile_base = static_cast<int64_t>(b) * ((doc_len + 127) / 128);
+  } else {
+    int64_t part = 0;
+    for (int i = tid; i < b; i += C::kThreads) part += (a.cu_seqlens[i + 1] - a.cu_seqlens[i] + 127) / 128;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (tid == 0) s_tile_base = 0;
+    __syncthreads();
+    if (lane == 0 && part) atomicAdd(reinterpret_cast<unsigned long long*>(&s_tile_base), static_cast<unsigned long long>(part));
+  }
+  __syncthreads();
+  const int64_t atom_base = (static_cast<int64_t>(h) * a.ntiles + s_tile_base + g / 4) * kAtomBytes;
+
+  const int64_t t = doc_start + static_cast<int64_t>(g) * 32 + row;
+  const bool valid = (static_cast<int64_t>(g) * 32 + row) < doc_len;
+  const int64_t elem0 = (t * a.H + h) * D + chunk * 16;
+
+  float v[16];
+  if (valid) {
+    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.x) + elem0);
+    uint4 p0 = __ldg(src), p1 = __ldg(src + 1);
+    uint32_t w[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = bf16_lo(w[i]);
+      v[2 * i + 1] = bf16_hi(w[i]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+  }
+
+  if constexpr (HAD) {
+    // Sylvester order: in-thread stages h = 1, 2, 4, 8, then across the 8
+    // threads of the row for h = 16, 32, 64 (chunk bits 0, 1, 2).
+#pragma unroll
+    for (int hh = 1; hh < 16; hh *= 2) {
+#pragma unroll
+      for (int i = 0; i < 16; i += 2 * hh) {
+#pragma unroll
+        for (int j = i; j < i + hh; ++j) {
+          float x0 = v[j], x1 = v[j + hh];
+          v[j] = x0 + x1;
+          v[j + hh] = x0 - x1;
+        }
+      }
+    }
+    had_cross(v, chunk, 1);
+    had_cross(v, chunk, 2);
+    had_cross(v, chunk, 4);
+    const float r = __uint_as_float(kInvSqrt128Bits);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], r);
+  }
+
+  float amax_local = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax_local = fmaxf(amax_local, fabsf(v[i]));
+
+  if constexpr (TOKBLOCK) {
+    // one exponent for the whole tile
+    float m = amax_local;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) s_blk[warp] = m;
+    __syncthreads();
+    float bm = 0.0f;
+#pragma unroll
+    for (int w = 0; w < C::kWarps; ++w) bm = fmaxf(bm, s_blk[w]);
+    const int e = mx_exponent_bits(__float_as_uint(bm));
+    const float sc = exp2i_neg(e);
+    const uint8_t eb = static_cast<uint8_t>(e + 127);
+    if (valid) {
+      uint4 out;
+      out.x = pack_e4m3x4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
+      out.y = pack_e4m3x4(v[4] * sc, v[5] * sc, v[6] * sc, v[7] * sc);
+      out.z = pack_e4m3x4(v[8] * sc, v[9] * sc, v[10] * sc, v[11] * sc);
+      out.w = pack_e4m3x4(v[12] * sc, v[13] * sc, v[14] * sc, v[15] * sc);
+      *reinterpret_cast<uint4*>(a.row_codes + elem0) = out;
+      if ((chunk & 1) == 0) a.row_scales[atom_base + row * 16 + (g & 3) * 4 + chunk / 2] = eb;
+    }
+    if (tid < D) a.tok_scales[atom_base + atom_offset(tid, g & 3)] = eb;
+    return;
+  } else {
+    if (a.write_row) {
+      float m = fmaxf(amax_local, __shfl_xor_sync(0xffffffffu, amax_local, 1));  // 32-channel group
+      const int e = mx_exponent_bits(__float_as_uint(m));
+      const float sc = exp2i_neg(e);
+      if (valid) {
+        uint4 out;
+        out.x = pack_e4m3x4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
+        out.y = pack_e4m3x4(v[4] * sc, v[5] * sc, v[6] * sc, v[7] * sc);
+        out.z = pack_e4m3x4(v[8] * sc, v[9] * sc, v[10] * sc, v[11] * sc);
+        out.w = pack_e4m3x4(v[12] * sc, v[13] * sc, v[14] * sc, v[15] * sc);
+        *reinterpret_cast<uint4*>(a.row_codes + elem0) = out;
+        if ((chunk & 1) == 0) a.row_scales[atom_base + row * 16 + (g & 3) * 4 + chunk / 2] = static_cast<uint8_t>(e + 127);
+      }
+    }
+    if (a.write_tok) {
+      // per-channel max over the 32 rows: rows of a warp differ in the lane
+      // bits above log2(TPR); then across warps in shared memory.
+      float cm[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float m = fabsf(v[i]);
+#pragma unroll
+        for (int o = C::TPR; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        cm[i] = m;
+      }
+      if (lane < C::TPR) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s_red[warp][chunk * 16 + i] = cm[i];
+      }
+      __syncthreads();
+      if (tid < D) {
+        float m = 0.0f;
+#pragma unroll
+        for (int w = 0; w < C::kWarps; ++w) m = fmaxf(m, s_red[w][tid]);
+        const int e = mx_exponent_bits(__float_as_uint(m));
+        s_e[tid] = e;
+        a.tok_scales[atom_base + atom_offset(tid, g & 3)] = static_cast<uint8_t>(e + 127);
+      }
+      __syncthreads();
+      if (valid) {
+        float y[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[i] = v[i] * exp2i_neg(s_e[chunk * 16 + i]);
+        uint4 out;
+        out.x = pack_e4m3x4(y[0], y[1], y[2], y[3]);
+        out.y = pack_e4m3x4(y[4], y[5], y[6], y[7]);
+        out.z = pack_e4m3x4(y[8], y[9], y[10], y[11]);
+        out.w = pack_e4m3x4(y[12], y[13], y[14], y[15]);
+        *reinterpret_cast<uint4*>(a.tok_codes + elem0) = out;
+      }
+    }
+  }
+}
+
+cudaError_t launch_quantize(const QuantArgs& a, int d, bool tokblock, bool hadamard, int max_groups,
+                            cudaStream_t stream) {
+  dim3 grid(max_groups, a.num_docs, a.H);
+  if (d == 128) {
+    constexpr int nt = QCfg<128>::kThreads;
+    if (tokblock && hadamard)
+      quantize_kernel<128, true, true><<<grid, nt, 0, stream>>>(a);
+    else if (tokblock)
+      quantize_kernel<128, true, false><<<grid, nt, 0, stream>>>(a);
+    else
+      quantize_kernel<128, false, false><<<grid, nt, 0, stream>>>(a);
+  } else {
+    constexpr int nt = QCfg<64>::kThreads;
+    if (tokblock)
+      quantize_kernel<64, true, false><<<grid, nt, 0, stream>>>(a);
+    else
+      quantize_kernel<64, false, false><<<grid, nt, 0, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace mxa

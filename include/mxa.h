@@ -1,0 +1,204 @@
+/*
+ * mxa.h -- C ABI of libmxa.so: MXFP8 block-scaled attention (forward and
+ * backward) for NVIDIA GB300 (sm_103a).
+ *
+ * What it computes (page titles and sections of the sources):
+ *   - MXFP8 operands: E4M3 codes plus one UE8M0 power-of-two scale per 32
+ *     values ("Flash Attention 4 + MXFP8 on Blackwell", "Что такое MXFP8";
+ *     FLAMIA reading notes sec. 2 "两种硬件格式"), with the scale exponent
+ *     e = ceil(log2(amax / 448)) (FLAMIA notes sec. 4, the saturation bound).
+ *   - Attention S = alpha Q K^T, softmax over the visible keys, O = P V,
+ *     LSE = m + ln l; backward dV = P^T G, dP = G V^T, D = G . O,
+ *     dS = P (dP - D), dQ = alpha dS K, dK = alpha dS^T Q (FLAMIA notes
+ *     sec. 2 and Algorithm 1).
+ *   - P quantised online with a fixed boost 2^4 (2^8 for the backward dV
+ *     product) (FLAMIA notes sec. 5 "概率上限由两个参数共同决定"); dS quantised
+ *     in 32 x 32 blocks from the block max-abs, taken in the register layout
+ *     without a transpose (FA4 write-up "Квантование dS без транспонирования").
+ *   - dQ accumulated in FP32 or in FP16 with a 2^9 boost (FA4 write-up, same
+ *     section).
+ *   - Packed documents through cu_seqlens; scale groups never cross a
+ *     document and only the scale tensors are padded ("Jagged-модуль без
+ *     gather"; FLAMIA notes sec. 6).
+ *   - Token-block mode: one exponent per 32 document-relative tokens x d of a
+ *     head, the same codes serving both contraction axes, optional normalized
+ *     128-point Hadamard rotation of Q/K (FLAMIA notes sec. 3).
+ *
+ * Conventions
+ *   Tensors are token-major "THD": element (t, h, c) of a [T, H, d] tensor
+ *   sits at offset (t * H + h) * d + c.  d is 64 or 128.
+ *   Device pointers everywhere except where a parameter says "host".
+ *   Ownership: the caller owns every buffer, including the backward workspace;
+ *   the library never allocates device memory, never synchronizes a stream
+ *   (except mxa_get_error) and keeps no pointer after a call returns.
+ *   Asynchrony: calls are stream-ordered on the given cudaStream_t.
+ *   Errors: argument errors return a status synchronously and launch
+ *   nothing.  MXA_ERR_CUDA wraps a launch error.  A kernel whose internal wait
+ *   runs out of time (it never spins forever) records an error word that
+ *   mxa_get_error() reports as MXA_ERR_TIMEOUT.
+ *   Inputs must be finite; non-finite inputs give unspecified codes.
+ *
+ * Scale layouts (UE8M0 bytes; 0x7F = 1.0 fills every unused byte)
+ *   Both views store scales in 512-byte "atoms" that the tensor core consumes
+ *   directly (a 128 x 4 block of scales: 128 rows of the MMA operand, 4
+ *   groups of 32 along its contraction axis).  Inside an atom the scale of
+ *   row r, group g sits at byte (r % 32) * 16 + (r / 32) * 4 + g.
+ *   Each document b owns ceil(n_b / 128) consecutive atoms per head, one per
+ *   128-token tile counted from the document start; its first atom index is
+ *   TB_b = sum_{b' < b} ceil(n_b' / 128).  NT = TB_{num_docs} is the number of
+ *   scale tiles (mxa_scale_tiles); a scale buffer holds H * NT atoms:
+ *   atom (h, b, i) at byte offset ((h * NT + TB_b + i) * 512).
+ *   ROW view (groups of 32 channels of one token and head): in atom
+ *     (h, b, i), row r = the token at document position 128 i + r, group g =
+ *     channels [32 g, 32 g + 32).
+ *   TOK view (groups of 32 document-relative tokens of one head and
+ *     channel): in atom (h, b, i), row r = channel r (d <= 128), group g =
+ *     document positions [128 i + 32 g, 128 i + 32 g + 32); the last group of
+ *     a document may be short; groups never cross a document.
+ *   Only the scales are padded per document; codes stay at their packed
+ *   token offsets.  In MXA_SCALE_TOKBLOCK32 mode the one exponent of each
+ *   (document, 32-token block, head) is written into both layouts, and both
+ *   views share one code buffer.
+ */
+#ifndef MXA_H
+#define MXA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MXA_ABI_VERSION 1
+
+typedef enum {
+  MXA_OK = 0,
+  MXA_ERR_ARG = 1,         /* null pointer, bad size or flag */
+  MXA_ERR_ALIGN = 2,       /* code buffer not 16-byte aligned, or scale buffer not 16-byte aligned */
+  MXA_ERR_UNSUPPORTED = 3, /* d not in {64, 128}; Hadamard with d != 128; Hq % Hkv != 0 */
+  MXA_ERR_WORKSPACE = 4,   /* backward workspace too small */
+  MXA_ERR_CUDA = 5,        /* a CUDA launch or runtime call failed */
+  MXA_ERR_TIMEOUT = 6      /* a kernel gave up waiting (reported by mxa_get_error) */
+} mxa_status;
+
+typedef enum {
+  MXA_SCALE_MX32 = 0,      /* 1-D groups of 32 along the contraction axis (row and token views) */
+  MXA_SCALE_TOKBLOCK32 = 1 /* one exponent per 32 document-relative tokens x d, one code set */
+} mxa_scale_mode;
+
+enum { MXA_VIEW_ROW = 1, MXA_VIEW_TOK = 2 };
+
+typedef enum {
+  MXA_DQ_FP32 = 0,     /* dQ partial sums added in fp32 */
+  MXA_DQ_FP16_X512 = 1 /* dQ partial sums boosted by 2^9 and added in fp16; unboosted at the end */
+} mxa_dq_mode;
+
+/* One quantized view of a tensor: E4M3 codes [T, H, d] and its UE8M0 scales
+ * in the layout of the view (see above).  Device pointers. */
+typedef struct {
+  uint8_t* codes;
+  uint8_t* scales;
+} mxa_qview;
+
+/* ABI version (MXA_ABI_VERSION of the built library). */
+int mxa_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* mxa_status_str(mxa_status s);
+
+/* Number of scale tiles NT = sum over documents of ceil(n_b / 128).
+ * cu_seqlens_host: host copy of the [num_docs + 1] offsets, or NULL for
+ * num_docs equal documents of T / num_docs tokens.  Returns -1 on bad input. */
+int64_t mxa_scale_tiles(int64_t T, int num_docs, const int32_t* cu_seqlens_host);
+
+/* Upper bound on NT that needs no host copy of cu_seqlens:
+ * ceil(T / 128) + num_docs. */
+int64_t mxa_scale_tiles_bound(int64_t T, int num_docs);
+
+/* Bytes of the scale buffer of one view (either layout): H * NT * 512. */
+size_t mxa_scale_bytes(int H, int64_t ntiles);
+
+/* Quantize a bf16 tensor x [T, H, d] into MXFP8 views.
+ *   cu_seqlens: device int32 [num_docs + 1] document offsets, or NULL for
+ *     num_docs equal documents (T % num_docs == 0).  max_seqlen bounds every
+ *     document length (it sizes the grid).
+ *   ntiles: NT of the scale layouts (mxa_scale_tiles or _bound); the same
+ *     value must be given to mxa_fwd / mxa_bwd.
+ *   mode: MXA_SCALE_MX32 -> `views` selects MXA_VIEW_ROW and/or MXA_VIEW_TOK;
+ *     each selected view gets its own codes and scales.
+ *     MXA_SCALE_TOKBLOCK32 -> one exponent per (document, 32-token block,
+ *     head); views must be both; codes go to row->codes (tok->codes must be
+ *     NULL or equal to it) and the exponent is written into both layouts.
+ *   hadamard: first rotate every (token, head) vector by the normalized
+ *     128-point Hadamard matrix (TOKBLOCK32 only, d == 128), in fp32, in the
+ *     Sylvester butterfly order, then multiply by fp32(128^-1/2).
+ *   Scale buffers are first filled with 0x7F (stream-ordered memset).
+ *   Code buffers must be 16-byte aligned; scale buffers 16-byte aligned.
+ * Status: MXA_OK, MXA_ERR_ARG, MXA_ERR_ALIGN, MXA_ERR_UNSUPPORTED,
+ * MXA_ERR_CUDA. */
+mxa_status mxa_quantize(const void* x_bf16, int64_t T, int H, int d, const int32_t* cu_seqlens, int num_docs,
+                        int max_seqlen, int64_t ntiles, mxa_scale_mode mode, int views, int hadamard,
+                        mxa_qview* row, mxa_qview* tok, cudaStream_t stream);
+
+/* Shape shared by the forward and backward calls. */
+typedef struct {
+  int64_t T;                  /* total tokens */
+  int Hq, Hkv, d;             /* query heads, key/value heads (Hq % Hkv == 0), head dim (64 or 128) */
+  const int32_t* cu_seqlens;  /* device int32 [num_docs + 1], or NULL: num_docs equal documents */
+  int num_docs;
+  int max_seqlen;             /* longest document (grid size); must bound every document */
+  int64_t ntiles;             /* NT of the scale layouts used when the views were quantized */
+  int causal;                 /* 1: query i sees keys [doc start, i]; 0: the whole document */
+  float softmax_scale;        /* alpha; 0 selects 1/sqrt(d) */
+} mxa_shape;
+
+typedef struct {
+  mxa_shape shape;
+  mxa_qview q_row;  /* Q, ROW view (scores) */
+  mxa_qview k_row;  /* K, ROW view (scores) */
+  mxa_qview v_tok;  /* V, TOK view (P V) */
+  void* o;          /* out: bf16 [T, Hq, d] */
+  float* lse;       /* out: fp32 [Hq, T], natural-log LSE (alpha included) */
+} mxa_fwd_params;
+
+/* Forward: O = softmax(alpha Q K^T) V over the visible keys, and LSE.
+ * Status: MXA_OK, MXA_ERR_ARG, MXA_ERR_ALIGN, MXA_ERR_UNSUPPORTED,
+ * MXA_ERR_CUDA. */
+mxa_status mxa_fwd(const mxa_fwd_params* p, cudaStream_t stream);
+
+typedef struct {
+  mxa_shape shape;
+  mxa_qview q_row, k_row;  /* score views (rebuild S exactly as the forward did) */
+  mxa_qview v_row, g_row;  /* dP = G V^T and D = G . O (the same G in both) */
+  mxa_qview q_tok;         /* dK = alpha dS^T Q */
+  mxa_qview k_tok;         /* dQ = alpha dS K */
+  mxa_qview g_tok;         /* dV = P^T G */
+  const void* o;           /* bf16 [T, Hq, d], the forward's output */
+  const float* lse;        /* fp32 [Hq, T], the forward's LSE */
+  void* dq;                /* out: bf16 [T, Hq, d] */
+  void* dk;                /* out: bf16 [T, Hkv, d] (summed over the query heads of the group) */
+  void* dv;                /* out: bf16 [T, Hkv, d] */
+  mxa_dq_mode dq_mode;
+} mxa_bwd_params;
+
+/* Workspace bytes mxa_bwd needs: D [Hq, T] fp32 plus the dQ accumulator
+ * ([T, Hq, d] fp32 or fp16), plus alignment. */
+size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p);
+
+/* Backward.  workspace: device buffer of at least mxa_bwd_workspace_bytes()
+ * bytes, 256-byte aligned; its contents on entry do not matter.
+ * Status: MXA_OK, MXA_ERR_ARG, MXA_ERR_ALIGN, MXA_ERR_UNSUPPORTED,
+ * MXA_ERR_WORKSPACE, MXA_ERR_CUDA. */
+mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Synchronize `stream`, then report and clear the device error word of the
+ * current device: MXA_OK, MXA_ERR_TIMEOUT (a kernel gave up waiting) or
+ * MXA_ERR_CUDA. */
+mxa_status mxa_get_error(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MXA_H */

@@ -1,0 +1,133 @@
+"""Host-side checks of the C ABI (no GPU work): the library builds, loads and
+exports every entry point include/mxa.h declares; pure host helpers compute
+the documented layouts; invalid arguments return a status without launching."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_scaled_mxfp8_gb300 import build as mbuild
+from block_scaled_mxfp8_gb300 import mxa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mbuild.build()
+    return mxa.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mxa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mxa_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "mxa_quantize" in names and "mxa_fwd" in names and "mxa_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(mxa.EXPORTS) | set(names)
+    assert mxa.mxa_abi_version() == 1
+
+
+def test_struct_layouts_match_header():
+    # sizes of the C structs on this platform (x86-64 / aarch64 LP64)
+    assert ctypes.sizeof(mxa.c_qview) == 16
+    assert ctypes.sizeof(mxa.c_shape) == 56
+    assert ctypes.sizeof(mxa.c_fwd_params) == 120
+    assert ctypes.sizeof(mxa.c_bwd_params) == 216
+
+
+def test_scale_tile_helpers(lib):
+    assert mxa.mxa_scale_tiles(32768, 8) == 8 * 32
+    assert mxa.mxa_scale_tiles(300, 3, [0, 100, 250, 300]) == 1 + 2 + 1
+    assert mxa.mxa_scale_tiles(300, 3, [0, 100, 250, 299]) == -1  # last offset must be T
+    assert mxa.mxa_scale_tiles(10, 3) == -1  # T not divisible
+    assert mxa.mxa_scale_tiles_bound(300, 3) == 3 + 3
+    assert mxa.mxa_scale_bytes(4, 10) == 4 * 10 * 512
+    assert [mxa.atom_index(r, 0) for r in (0, 1, 31, 32, 127)] == [0, 16, 496, 4, 508]
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert isinstance(mxa.status_str(s), str) and mxa.status_str(s)
+
+
+def _qv(p=256):
+    return mxa.c_qview(p, p)
+
+
+def test_quantize_rejects_bad_arguments_without_launch(lib):
+    L = lib
+    q = _qv()
+    P = ctypes.c_void_p
+    call = lambda *a: L.mxa_quantize(*a)
+    ok_args = [P(256), 256, 2, 128, None, 1, 256, 2, 0, 3, 0, ctypes.byref(q), ctypes.byref(q), None]
+    a = list(ok_args)
+    a[0] = None
+    assert call(*a) == mxa.MXA_ERR_ARG
+    a = list(ok_args)
+    a[3] = 96
+    assert call(*a) == mxa.MXA_ERR_UNSUPPORTED
+    a = list(ok_args)
+    a[5] = 3  # 256 % 3 != 0 with cu_seqlens NULL
+    assert call(*a) == mxa.MXA_ERR_ARG
+    a = list(ok_args)
+    a[8] = 7  # bad mode
+    assert call(*a) == mxa.MXA_ERR_ARG
+    a = list(ok_args)
+    a[10] = 1  # hadamard needs token-block mode
+    assert call(*a) == mxa.MXA_ERR_UNSUPPORTED
+    a = list(ok_args)
+    a[0] = P(257)  # misaligned input
+    assert call(*a) == mxa.MXA_ERR_ALIGN
+    a = list(ok_args)
+    q2 = mxa.c_qview(264, 256)  # codes not 16-byte aligned
+    a[11] = ctypes.byref(q2)
+    assert call(*a) == mxa.MXA_ERR_ALIGN
+    a = list(ok_args)
+    a[8], a[10] = 1, 1
+    a[3] = 64  # hadamard with d != 128
+    assert call(*a) == mxa.MXA_ERR_UNSUPPORTED
+    a = list(ok_args)
+    a[9] = 0  # no view
+    assert call(*a) == mxa.MXA_ERR_ARG
+
+
+def _fwd(T=256, Hq=2, Hkv=2, d=128, nd=1, maxlen=256, nt=2):
+    sh = mxa.c_shape(T, Hq, Hkv, d, None, nd, maxlen, nt, 0, 0.0)
+    return mxa.c_fwd_params(sh, _qv(), _qv(), _qv(), 256, 256)
+
+
+def test_fwd_bwd_reject_bad_arguments_without_launch(lib):
+    L = lib
+    assert L.mxa_fwd(None, None) == mxa.MXA_ERR_ARG
+    p = _fwd(Hq=3, Hkv=2)
+    assert L.mxa_fwd(ctypes.byref(p), None) == mxa.MXA_ERR_UNSUPPORTED  # Hq % Hkv
+    p = _fwd(d=96)
+    assert L.mxa_fwd(ctypes.byref(p), None) == mxa.MXA_ERR_UNSUPPORTED
+    p = _fwd()
+    p.o = 0
+    assert L.mxa_fwd(ctypes.byref(p), None) == mxa.MXA_ERR_ARG
+    p = _fwd()
+    p.q_row = mxa.c_qview(0, 256)
+    assert L.mxa_fwd(ctypes.byref(p), None) == mxa.MXA_ERR_ARG
+    p = _fwd(maxlen=100)  # documents longer than max_seqlen
+    assert L.mxa_fwd(ctypes.byref(p), None) == mxa.MXA_ERR_ARG
+    p = _fwd()
+    p.shape.softmax_scale = -1.0
+    assert L.mxa_fwd(ctypes.byref(p), None) == mxa.MXA_ERR_ARG
+    sh = mxa.c_shape(256, 2, 2, 128, None, 1, 256, 2, 1, 0.0)
+    bp = mxa.c_bwd_params(sh, *[_qv()] * 7, 256, 256, 256, 256, 256, 0)
+    need = L.mxa_bwd_workspace_bytes(ctypes.byref(bp))
+    assert need >= 256 * 2 * 128 * 4 + 2 * 256 * 4
+    assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), need - 1, None) == mxa.MXA_ERR_WORKSPACE
+    assert L.mxa_bwd(ctypes.byref(bp), None, need, None) == mxa.MXA_ERR_WORKSPACE
+    bp.dq_mode = 5
+    assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), need, None) == mxa.MXA_ERR_ARG
+    bp.dq_mode = 1
+    assert L.mxa_bwd_workspace_bytes(ctypes.byref(bp)) < need  # fp16 accumulator is half the size
