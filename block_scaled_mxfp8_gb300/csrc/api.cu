@@ -228,7 +228,9 @@ size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p) {
   const size_t T = static_cast<size_t>(p->shape.T), Hq = static_cast<size_t>(p->shape.Hq),
                d = static_cast<size_t>(p->shape.d);
   const size_t dbytes = ((Hq * T * 4) + 255) & ~size_t(255);
-  const size_t acc = T * Hq * d * (p->dq_mode == MXA_DQ_FP16_X512 ? 2 : 4);
+  // FP32 mode: deterministic dQ kernel, no accumulator; FP16 x 2^9 mode:
+  // fp16 partial-sum accumulator [T, Hq, d].
+  const size_t acc = p->dq_mode == MXA_DQ_FP16_X512 ? T * Hq * d * 2 : 0;
   return dbytes + ((acc + 255) & ~size_t(255));
 }
 
@@ -261,7 +263,8 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   const size_t dbytes = ((Hq * T * 4) + 255) & ~size_t(255);
   float* dvec = static_cast<float*>(workspace);
   void* acc = static_cast<uint8_t*>(workspace) + dbytes;
-  const size_t acc_bytes = T * Hq * d * (p->dq_mode == MXA_DQ_FP16_X512 ? 2 : 4);
+  const bool fp16 = p->dq_mode == MXA_DQ_FP16_X512;
+  const size_t acc_bytes = fp16 ? T * Hq * d * 2 : 0;
   const int maxlen = s.cu_seqlens ? s.max_seqlen : static_cast<int>(s.T / s.num_docs);
 
   PrepArgs pa{};
@@ -299,11 +302,17 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   a.lse = p->lse;
   a.dvec = dvec;
   a.dq_mode = p->dq_mode;
-  a.dq_acc32 = p->dq_mode == MXA_DQ_FP32 ? static_cast<float*>(acc) : nullptr;
-  a.dq_acc16 = p->dq_mode == MXA_DQ_FP16_X512 ? static_cast<uint16_t*>(acc) : nullptr;
+  a.dq_acc32 = nullptr;
+  a.dq_acc16 = fp16 ? static_cast<uint16_t*>(acc) : nullptr;
   a.dk = p->dk;
   a.dv = p->dv;
+  a.dq_out = p->dq;
   a.err = device_error_word();
+  if (!fp16) {
+    // FP32: dK/dV kernel and the dQ kernel (dQ summed in TMEM, fixed order)
+    if (launch_bwd_split(a, maps, s.d, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
+    return MXA_OK;
+  }
   if (launch_bwd(a, maps, s.d, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
 
   DqConvArgs c{};

@@ -1,0 +1,85 @@
+// attn_common.cuh -- device helpers shared by the attention kernels.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace mxa {
+
+// 2^x on the MUFU unit (the kernels' one exponential; the backward rebuilds P
+// with the same instruction as the forward).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Bounded wait used by every warp role: gives up after kWaitBudgetCycles,
+// records `code` in the device error word and raises the CTA's abort flag;
+// returns early (false) once another role has raised it.
+__device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                          int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  uint32_t it = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > kWaitBudgetCycles) {
+        *abort_flag = 1;
+        if (err) atomicCAS(err, 0, code);
+        return false;
+      }
+    }
+  }
+}
+
+// Same, collective over the warp: every lane waits, and the warp continues
+// only if all lanes succeeded (tcgen05.ld/st that follow are warp-collective).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                          int code) {
+  const bool ok = role_wait(bar, parity, abort_flag, err, code);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// One 512-byte scale atom (128 rows x 4 groups) from shared memory into 4
+// TMEM columns, replicated into the four 32-lane quadrants.
+__device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, const void* smem_atom) {
+  const uint64_t desc = make_sdesc(smem_u32(smem_atom), 512, 128, kSwzNone);
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
+// First scale tile of document b: sum over earlier documents of ceil(n / 128).
+// Called by every thread of the CTA.
+__device__ __forceinline__ int64_t doc_tile_base(const int32_t* cu, int b, int64_t len, int tid, int nthreads,
+                                                 int64_t* s_slot) {
+  if (cu == nullptr) return static_cast<int64_t>(b) * ((len + 127) / 128);
+  if (tid == 0) *s_slot = 0;
+  __syncthreads();
+  int64_t part = 0;
+  for (int i = tid; i < b; i += nthreads) part += (cu[i + 1] - cu[i] + 127) / 128;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if ((tid & 31) == 0 && part)
+    atomicAdd(reinterpret_cast<unsigned long long*>(s_slot), static_cast<unsigned long long>(part));
+  __syncthreads();
+  return *s_slot;
+}
+
+// Two E4M3 codes (low 16 bits) -> two floats (exact).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two_codes)));
+  __half2 hv = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(hv);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+}  // namespace mxa

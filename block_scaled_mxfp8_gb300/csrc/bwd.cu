@@ -29,8 +29,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include "kernels.cuh"
-#include "ptx.cuh"
+#include "attn_common.cuh"
 
 namespace mxa {
 
@@ -61,55 +60,10 @@ struct BwdCfg {
   static constexpr int kSmemBytes = kOffDv + 2 * 128 * 4 + 1024;
 };
 
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
-__device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
-                                          int code) {
-  if (mbar_try_wait(bar, parity)) return true;
-  long long t0 = clock64();
-  uint32_t it = 0;
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++it & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (clock64() - t0 > kWaitBudgetCycles) {
-        *abort_flag = 1;
-        if (err) atomicCAS(err, 0, code);
-        return false;
-      }
-    }
-  }
-}
 
-__device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, const void* smem_atom) {
-  const uint64_t desc = make_sdesc(smem_u32(smem_atom), 512, 128, kSwzNone);
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
-}
 
-__device__ __forceinline__ int64_t doc_tile_base(const int32_t* cu, int b, int64_t len, int tid, int nthreads,
-                                                 int64_t* s_slot) {
-  if (cu == nullptr) return static_cast<int64_t>(b) * ((len + 127) / 128);
-  if (tid == 0) *s_slot = 0;
-  __syncthreads();
-  int64_t part = 0;
-  for (int i = tid; i < b; i += nthreads) part += (cu[i + 1] - cu[i] + 127) / 128;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-  if ((tid & 31) == 0 && part) atomicAdd(reinterpret_cast<unsigned long long*>(s_slot), static_cast<unsigned long long>(part));
-  __syncthreads();
-  return *s_slot;
-}
 
-__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_codes) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two_codes)));
-  __half2 hv = *reinterpret_cast<__half2*>(&h2);
-  return __half22float2(hv);
-}
 
 }  // namespace
 
@@ -578,7 +532,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 }
 
 cudaError_t launch_bwd_prep(const PrepArgs& a, int max_seqlen, cudaStream_t stream) {
-  if (cudaMemsetAsync(a.dq_acc, 0, a.dq_acc_bytes, stream) != cudaSuccess) return cudaGetLastError();
+  if (a.dq_acc_bytes && cudaMemsetAsync(a.dq_acc, 0, a.dq_acc_bytes, stream) != cudaSuccess) return cudaGetLastError();
   dim3 grid((max_seqlen + 31) / 32, a.num_docs, a.Hq);
   bwd_prep_kernel<<<grid, 256, 0, stream>>>(a);
   return cudaGetLastError();

@@ -1,0 +1,636 @@
+// bwd_split.cu -- deterministic MXFP8 attention backward in two kernels
+// (the FP32 dQ mode): no atomics, every sum in a fixed order.
+//
+//   attn_bwd_dkdv_kernel : one CTA per (128-key tile, kv head, document),
+//       looping over the query heads of the kv group and the visible query
+//       tiles (FLAMIA notes Algorithm 1 steps 11-15 without dQ):
+//         S^T = K Q^T, P^T = exp(alpha S^T - LSE), dP^T = V G^T,
+//         dS^T = P^T (dP^T - D) quantized per 32 x 32 block (warp max-abs in
+//         the register layout: a warp holds 32 key rows, a 32-column chunk is
+//         one block; no transpose),
+//         dV += E4M3(2^8 P^T) G, dK += dS^T Q, both accumulated in TMEM.
+//   attn_bwd_dq_kernel   : one CTA per (128-query tile, query head,
+//       document), looping over the visible key tiles:
+//         S = Q K^T, P = exp(alpha S - LSE), dP = G V^T,
+//         dS = P (dP - D) quantized per 32 x 32 block (a warp holds 32 query
+//         rows), dQ += dS K accumulated in TMEM, written once as bf16.
+// Both recompute S and dP (the FLOP convention counts the backward as 2.5
+// forwards; these two kernels execute 3.5).  The 32 x 32 blocks are the same
+// in both kernels; each quantizes its own fp32 dS.
+#include <cuda_bf16.h>
+
+#include "attn_common.cuh"
+
+namespace mxa {
+
+namespace {
+
+template <int D>
+struct DkdvCfg {
+  static constexpr int kStages = 2;
+  static constexpr int kTileBytes = 128 * D;
+  static constexpr uint32_t kSwz = D == 128 ? kSwz128 : kSwz64;
+  static constexpr uint32_t kSBO = 8 * D;
+  static constexpr int kKSteps = D / 32;
+  static constexpr int kThreads = 256;
+  // TMEM: X holds S^T then dP^T; dV, dK accumulators; P^T and dS^T codes
+  static constexpr uint32_t kColX = 0, kColDV = 128, kColDK = 256, kColP = 384, kColDS = 416;
+  static constexpr uint32_t kSfK = 448, kSfQ = 452 /*+4s*/, kSfV = 460, kSfG = 464 /*+4s*/, kSfP = 472,
+                            kSfGt = 476 /*+4s*/, kSfDS = 484, kSfQt = 488 /*+4s*/;
+  // shared memory
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kTileBytes;
+  static constexpr int kOffStage = kOffV + kTileBytes;  // per stage: Q, G, Qt, Gt
+  static constexpr int kStageBytes = 4 * kTileBytes;
+  static constexpr int kOffSf = kOffStage + kStages * kStageBytes;  // K, V, then 4 per stage
+  static constexpr int kOffLse = kOffSf + (2 + 4 * kStages) * kAtomBytes;
+  static constexpr int kOffDv = kOffLse + 2 * 128 * 4;
+  static constexpr int kSmemBytes = kOffDv + 2 * 128 * 4 + 1024;
+};
+
+template <int D>
+struct DqCfg {
+  static constexpr int kStages = 2;
+  static constexpr int kTileBytes = 128 * D;
+  static constexpr uint32_t kSwz = D == 128 ? kSwz128 : kSwz64;
+  static constexpr uint32_t kSBO = 8 * D;
+  static constexpr int kKSteps = D / 32;
+  static constexpr int kThreads = 256;
+  // TMEM: X holds S then dP; dQ accumulator; dS codes
+  static constexpr uint32_t kColX = 0, kColDQ = 128, kColDS = 256;
+  static constexpr uint32_t kSfQ = 288, kSfG = 292, kSfK = 296 /*+4s*/, kSfV = 304 /*+4s*/, kSfDS = 312,
+                            kSfKt = 316 /*+4s*/;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffG = kOffQ + kTileBytes;
+  static constexpr int kOffStage = kOffG + kTileBytes;  // per stage: K, V, Kt
+  static constexpr int kStageBytes = 3 * kTileBytes;
+  static constexpr int kOffSf = kOffStage + kStages * kStageBytes;  // Q, G, then 3 per stage
+  static constexpr int kSmemBytes = kOffSf + (2 + 3 * kStages) * kAtomBytes + 1024;
+};
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&rr)[32], float mul) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 8) {
+    uint4 v;
+    v.x = pack_bf16x2(__uint_as_float(rr[i]) * mul, __uint_as_float(rr[i + 1]) * mul);
+    v.y = pack_bf16x2(__uint_as_float(rr[i + 2]) * mul, __uint_as_float(rr[i + 3]) * mul);
+    v.z = pack_bf16x2(__uint_as_float(rr[i + 4]) * mul, __uint_as_float(rr[i + 5]) * mul);
+    v.w = pack_bf16x2(__uint_as_float(rr[i + 6]) * mul, __uint_as_float(rr[i + 7]) * mul);
+    *reinterpret_cast<uint4*>(dst + i) = v;
+  }
+}
+
+}  // namespace
+
+// ========================================================================= dK, dV
+template <int D>
+__global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
+  using C = DkdvCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  __shared__ uint64_t bar_kv, bar_tile_full[C::kStages], bar_tile_empty[C::kStages], bar_s_full, bar_x_free,
+      bar_dp_full, bar_x_free2, bar_p_ready, bar_pds_free, bar_final, bar_drain, bar_lse[2];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int64_t s_slot;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kt = blockIdx.x, b = blockIdx.y, hk = blockIdx.z;
+  const int grp = a.Hq / a.Hkv;
+  int64_t doc_start, n;
+  doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
+  const int n_tiles = static_cast<int>((n + 127) / 128);
+  if (kt >= n_tiles) return;
+  const int qi0 = a.causal ? kt : 0;
+  const int nq = n_tiles - qi0;
+  const int n_work = nq * grp;
+  const int64_t tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, C::kThreads, &s_slot);
+
+  if (tid == 0) {
+    mbar_init(&bar_kv, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bar_tile_full[s], 1);
+      mbar_init(&bar_tile_empty[s], 1);
+    }
+    mbar_init(&bar_s_full, 1);
+    mbar_init(&bar_x_free, 128);
+    mbar_init(&bar_dp_full, 1);
+    mbar_init(&bar_x_free2, 128);
+    mbar_init(&bar_p_ready, 128);
+    mbar_init(&bar_pds_free, 1);
+    mbar_init(&bar_final, 1);
+    mbar_init(&bar_drain, 1);
+    mbar_init(&bar_lse[0], 128);
+    mbar_init(&bar_lse[1], 128);
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(&s_tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int* abort_flag = &s_abort;
+  uint8_t* sSf = smem + C::kOffSf;  // [0] K, [1] V, stage s: 2 + 4s + (0 Q, 1 G, 2 Qt, 3 Gt)
+  float* sLse = reinterpret_cast<float*>(smem + C::kOffLse);
+  float* sDv = reinterpret_cast<float*>(smem + C::kOffDv);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      const int64_t k0 = doc_start + static_cast<int64_t>(kt) * 128;
+      const int64_t katom = (static_cast<int64_t>(hk) * a.ntiles + tile_base + kt) * kAtomBytes;
+      mbar_arrive_expect_tx(&bar_kv, 2 * C::kTileBytes + 2 * kAtomBytes);
+      tma_load_3d(smem + C::kOffK, &maps.k, &bar_kv, 0, hk, static_cast<int>(k0));
+      tma_load_3d(smem + C::kOffV, &maps.v, &bar_kv, 0, hk, static_cast<int>(k0));
+      bulk_load(sSf + 0 * kAtomBytes, a.k_sf + katom, kAtomBytes, &bar_kv);
+      bulk_load(sSf + 1 * kAtomBytes, a.v_sf + katom, kAtomBytes, &bar_kv);
+      int issued = 0;
+      for (int u = 0; u < n_work; ++u) {
+        const int s = u % C::kStages;
+        if (u >= C::kStages &&
+            !role_wait(&bar_tile_empty[s], ((u / C::kStages) - 1) & 1, abort_flag, a.err, kErrTimeoutTma))
+          break;
+        const int h = hk * grp + u / nq;
+        const int qi = qi0 + u % nq;
+        const int q0 = static_cast<int>(doc_start + static_cast<int64_t>(qi) * 128);
+        const int64_t qatom = (static_cast<int64_t>(h) * a.ntiles + tile_base + qi) * kAtomBytes;
+        uint8_t* st = smem + C::kOffStage + s * C::kStageBytes;
+        uint8_t* sf = sSf + (2 + 4 * s) * kAtomBytes;
+        mbar_arrive_expect_tx(&bar_tile_full[s], 4 * C::kTileBytes + 4 * kAtomBytes);
+        tma_load_3d(st + 0 * C::kTileBytes, &maps.q, &bar_tile_full[s], 0, h, q0);
+        tma_load_3d(st + 1 * C::kTileBytes, &maps.g, &bar_tile_full[s], 0, h, q0);
+        tma_load_3d(st + 2 * C::kTileBytes, &maps.qt, &bar_tile_full[s], 0, h, q0);
+        tma_load_3d(st + 3 * C::kTileBytes, &maps.gt, &bar_tile_full[s], 0, h, q0);
+        bulk_load(sf + 0 * kAtomBytes, a.q_sf + qatom, kAtomBytes, &bar_tile_full[s]);
+        bulk_load(sf + 1 * kAtomBytes, a.g_sf + qatom, kAtomBytes, &bar_tile_full[s]);
+        bulk_load(sf + 2 * kAtomBytes, a.qt_sf + qatom, kAtomBytes, &bar_tile_full[s]);
+        bulk_load(sf + 3 * kAtomBytes, a.gt_sf + qatom, kAtomBytes, &bar_tile_full[s]);
+        issued = u + 1;
+      }
+      role_wait(&bar_kv, 0, abort_flag, nullptr, 0);
+      for (int u = (issued > C::kStages ? issued - C::kStages : 0); u < issued; ++u)
+        mbar_wait(&bar_tile_full[u % C::kStages], (u / C::kStages) & 1, nullptr, 0);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      const uint32_t ka = smem_u32(smem + C::kOffK), va = smem_u32(smem + C::kOffV);
+      bool ok = role_wait(&bar_kv, 0, abort_flag, a.err, kErrTimeoutMma);
+      if (ok) {
+        tc_fence_after();
+        tmem_cp_atom(tmem + C::kSfK, sSf + 0 * kAtomBytes);
+        tmem_cp_atom(tmem + C::kSfV, sSf + 1 * kAtomBytes);
+      }
+      auto issue_s = [&](int u) -> bool {  // S^T = K Q^T into X
+        const int s = u % C::kStages;
+        if (!role_wait(&bar_tile_full[s], (u / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
+        tc_fence_after();
+        const uint32_t st = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
+        tmem_cp_atom(tmem + C::kSfQ + 4 * s, sSf + (2 + 4 * s + 0) * kAtomBytes);
+#pragma unroll
+        for (int kk = 0; kk < C::kKSteps; ++kk)
+          mma_mxf8_ss(tmem + C::kColX, make_sdesc(ka + 32 * kk, 16, C::kSBO, C::kSwz),
+                      make_sdesc(st + 32 * kk, 16, C::kSBO, C::kSwz), make_idesc_mxf8(128, 128, 0, 0, kk, kk),
+                      tmem + C::kSfK, tmem + C::kSfQ + 4 * s, kk > 0);
+        mma_commit(&bar_s_full);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int u = 0; ok && u < n_work; ++u) {
+        const int s = u % C::kStages;
+        const uint32_t st = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
+        // dP^T = V G^T once S^T has been read out of X
+        if (!(ok = role_wait(&bar_x_free, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        tc_fence_after();
+        tmem_cp_atom(tmem + C::kSfG + 4 * s, sSf + (2 + 4 * s + 1) * kAtomBytes);
+#pragma unroll
+        for (int kk = 0; kk < C::kKSteps; ++kk)
+          mma_mxf8_ss(tmem + C::kColX, make_sdesc(va + 32 * kk, 16, C::kSBO, C::kSwz),
+                      make_sdesc(st + C::kTileBytes + 32 * kk, 16, C::kSBO, C::kSwz),
+                      make_idesc_mxf8(128, 128, 0, 0, kk, kk), tmem + C::kSfV, tmem + C::kSfG + 4 * s, kk > 0);
+        mma_commit(&bar_dp_full);
+        // next S^T as soon as dP^T has been read (overlaps the dS work)
+        if (!(ok = role_wait(&bar_x_free2, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        if (u + 1 < n_work && !(ok = issue_s(u + 1))) break;
+        // dV += P^T G, dK += dS^T Q
+        if (!(ok = role_wait(&bar_p_ready, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        tc_fence_after();
+        tmem_cp_atom(tmem + C::kSfGt + 4 * s, sSf + (2 + 4 * s + 3) * kAtomBytes);
+        tmem_cp_atom(tmem + C::kSfQt + 4 * s, sSf + (2 + 4 * s + 2) * kAtomBytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_mxf8_ts(tmem + C::kColDV, tmem + C::kColP + 8 * kk,
+                      make_sdesc(st + 3 * C::kTileBytes + kk * 32 * D, 16, C::kSBO, C::kSwz),
+                      make_idesc_mxf8(128, D, 0, 1, kk, kk), tmem + C::kSfP, tmem + C::kSfGt + 4 * s,
+                      (u > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_mxf8_ts(tmem + C::kColDK, tmem + C::kColDS + 8 * kk,
+                      make_sdesc(st + 2 * C::kTileBytes + kk * 32 * D, 16, C::kSBO, C::kSwz),
+                      make_idesc_mxf8(128, D, 0, 1, kk, kk), tmem + C::kSfDS, tmem + C::kSfQt + 4 * s,
+                      (u > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar_pds_free);
+        mma_commit(&bar_tile_empty[s]);
+      }
+      mma_commit(&bar_final);
+      mma_commit(&bar_drain);
+      mbar_wait(&bar_drain, 0, nullptr, 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax / dS
+    const int quad = warp & 3;
+    const int j = quad * 32 + lane;  // key row (TMEM lane)
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const int64_t kpos = static_cast<int64_t>(kt) * 128 + j;
+    const bool key_valid = kpos < n;
+    const float sl2 = a.scale_log2;
+    tmem_st4(lane_base + C::kSfP, 0x77777777u, 0x77777777u, 0x77777777u, 0x77777777u);  // 2^-8
+    tmem_st_wait();
+    bool ok = true;
+    for (int u = 0; u < n_work; ++u) {
+      const int h = hk * grp + u / nq;
+      const int qi = qi0 + u % nq;
+      const int par = u & 1;
+      {
+        const int64_t qp = static_cast<int64_t>(qi) * 128 + j;  // thread j loads query j's LSE and D
+        float l2 = 0.0f, dd = 0.0f;
+        if (qp < n) {
+          const int64_t t = doc_start + qp;
+          l2 = a.lse[static_cast<int64_t>(h) * a.T + t] * 1.4426950408889634f;
+          dd = a.dvec[static_cast<int64_t>(h) * a.T + t];
+        }
+        sLse[par * 128 + j] = l2;
+        sDv[par * 128 + j] = dd;
+      }
+      mbar_arrive(&bar_lse[par]);
+      if (!(ok = warp_wait(&bar_lse[par], (u >> 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      if (!(ok = warp_wait(&bar_s_full, u & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      tc_fence_after();
+      float p[128];
+      {
+        uint32_t rr[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(lane_base + C::kColX + 32 * c, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) p[32 * c + i] = __uint_as_float(rr[i]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bar_x_free);
+      const int64_t qbase = static_cast<int64_t>(qi) * 128;
+      const bool full = key_valid && (qbase + 127 < n) && (!a.causal || kpos <= qbase);
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float v = ex2_approx(fmaf(p[c], sl2, -sLse[par * 128 + c]));
+        const int64_t qp = qbase + c;
+        p[c] = (full || (key_valid && qp < n && (!a.causal || kpos <= qp))) ? v : 0.0f;
+      }
+      // the previous tile's dV / dK MMAs must be done with the P, dS codes and scales
+      if (u > 0 && !(ok = warp_wait(&bar_pds_free, (u - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 32; c += 8) {
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          w[k] = pack_e4m3x4(p[4 * (c + k)] * 256.0f, p[4 * (c + k) + 1] * 256.0f, p[4 * (c + k) + 2] * 256.0f,
+                             p[4 * (c + k) + 3] * 256.0f);
+        tmem_st8(lane_base + C::kColP + c, w);
+      }
+      if (!(ok = warp_wait(&bar_dp_full, u & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      tc_fence_after();
+      uint32_t ebytes = 0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(lane_base + C::kColX + 32 * c, rr);
+        tmem_ld_wait();
+        float am = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float ds = p[32 * c + i] * (__uint_as_float(rr[i]) - sDv[par * 128 + 32 * c + i]);
+          rr[i] = __float_as_uint(ds);
+          am = fmaxf(am, fabsf(ds));
+        }
+        am = warp_max_abs(am);  // 32 key rows x 32 queries
+        const int e = mx_exponent_bits(__float_as_uint(am));
+        const float sc = exp2i_neg(e);
+        ebytes |= static_cast<uint32_t>(e + 127) << (8 * c);
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          w[k] = pack_e4m3x4(__uint_as_float(rr[4 * k]) * sc, __uint_as_float(rr[4 * k + 1]) * sc,
+                             __uint_as_float(rr[4 * k + 2]) * sc, __uint_as_float(rr[4 * k + 3]) * sc);
+        tmem_st8(lane_base + C::kColDS + 8 * c, w);
+      }
+      tc_fence_before();
+      mbar_arrive(&bar_x_free2);
+      // dK's A operand is dS^T (rows = keys, groups = 32-query blocks); the
+      // tensor core reads row r's scales from lane r, column r / 32, so each
+      // warp's 32 lanes carry its own key block's four exponents in column quad.
+      tmem_st1(lane_base + C::kSfDS + quad, ebytes);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar_p_ready);
+    }
+    // ---------------------------------------------------------- dK, dV out
+    if (ok) ok = role_wait(&bar_final, 0, abort_flag, a.err, kErrTimeoutEpilogue);
+    if (__all_sync(0xffffffffu, ok)) {
+      tc_fence_after();
+      const int64_t t = doc_start + kpos;
+      __nv_bfloat16* dvrow = reinterpret_cast<__nv_bfloat16*>(a.dv) + (t * a.Hkv + hk) * D;
+      __nv_bfloat16* dkrow = reinterpret_cast<__nv_bfloat16*>(a.dk) + (t * a.Hkv + hk) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(lane_base + C::kColDV + 32 * c, rr);
+        tmem_ld_wait();
+        if (key_valid) store_row_bf16(dvrow + 32 * c, rr, 1.0f);
+        tmem_ld32(lane_base + C::kColDK + 32 * c, rr);
+        tmem_ld_wait();
+        if (key_valid) store_row_bf16(dkrow + 32 * c, rr, a.alpha);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ========================================================================= dQ
+template <int D>
+__global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
+  using C = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  __shared__ uint64_t bar_q, bar_kv_full[C::kStages], bar_kv_empty[C::kStages], bar_s_full, bar_x_free,
+      bar_dp_full, bar_x_free2, bar_ds_ready, bar_ds_free, bar_final, bar_drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int64_t s_slot;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.y, h = blockIdx.z;
+  const int hk = h / (a.Hq / a.Hkv);
+  int64_t doc_start, n;
+  doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
+  const int n_tiles = static_cast<int>((n + 127) / 128);
+  const int qt = a.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+  if (qt >= n_tiles) return;
+  const int n_kt = a.causal ? qt + 1 : n_tiles;
+  const int64_t tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, C::kThreads, &s_slot);
+
+  if (tid == 0) {
+    mbar_init(&bar_q, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bar_kv_full[s], 1);
+      mbar_init(&bar_kv_empty[s], 1);
+    }
+    mbar_init(&bar_s_full, 1);
+    mbar_init(&bar_x_free, 128);
+    mbar_init(&bar_dp_full, 1);
+    mbar_init(&bar_x_free2, 128);
+    mbar_init(&bar_ds_ready, 128);
+    mbar_init(&bar_ds_free, 1);
+    mbar_init(&bar_final, 1);
+    mbar_init(&bar_drain, 1);
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(&s_tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int* abort_flag = &s_abort;
+  uint8_t* sSf = smem + C::kOffSf;  // [0] Q, [1] G, stage s: 2 + 3s + (0 K, 1 V, 2 Kt)
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      const int q0 = static_cast<int>(doc_start + static_cast<int64_t>(qt) * 128);
+      const int64_t qatom = (static_cast<int64_t>(h) * a.ntiles + tile_base + qt) * kAtomBytes;
+      mbar_arrive_expect_tx(&bar_q, 2 * C::kTileBytes + 2 * kAtomBytes);
+      tma_load_3d(smem + C::kOffQ, &maps.q, &bar_q, 0, h, q0);
+      tma_load_3d(smem + C::kOffG, &maps.g, &bar_q, 0, h, q0);
+      bulk_load(sSf + 0 * kAtomBytes, a.q_sf + qatom, kAtomBytes, &bar_q);
+      bulk_load(sSf + 1 * kAtomBytes, a.g_sf + qatom, kAtomBytes, &bar_q);
+      int issued = 0;
+      for (int j = 0; j < n_kt; ++j) {
+        const int s = j % C::kStages;
+        if (j >= C::kStages &&
+            !role_wait(&bar_kv_empty[s], ((j / C::kStages) - 1) & 1, abort_flag, a.err, kErrTimeoutTma))
+          break;
+        const int k0 = static_cast<int>(doc_start + static_cast<int64_t>(j) * 128);
+        const int64_t katom = (static_cast<int64_t>(hk) * a.ntiles + tile_base + j) * kAtomBytes;
+        uint8_t* st = smem + C::kOffStage + s * C::kStageBytes;
+        uint8_t* sf = sSf + (2 + 3 * s) * kAtomBytes;
+        mbar_arrive_expect_tx(&bar_kv_full[s], 3 * C::kTileBytes + 3 * kAtomBytes);
+        tma_load_3d(st + 0 * C::kTileBytes, &maps.k, &bar_kv_full[s], 0, hk, k0);
+        tma_load_3d(st + 1 * C::kTileBytes, &maps.v, &bar_kv_full[s], 0, hk, k0);
+        tma_load_3d(st + 2 * C::kTileBytes, &maps.kt, &bar_kv_full[s], 0, hk, k0);
+        bulk_load(sf + 0 * kAtomBytes, a.k_sf + katom, kAtomBytes, &bar_kv_full[s]);
+        bulk_load(sf + 1 * kAtomBytes, a.v_sf + katom, kAtomBytes, &bar_kv_full[s]);
+        bulk_load(sf + 2 * kAtomBytes, a.kt_sf + katom, kAtomBytes, &bar_kv_full[s]);
+        issued = j + 1;
+      }
+      role_wait(&bar_q, 0, abort_flag, nullptr, 0);
+      for (int j = (issued > C::kStages ? issued - C::kStages : 0); j < issued; ++j)
+        mbar_wait(&bar_kv_full[j % C::kStages], (j / C::kStages) & 1, nullptr, 0);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      const uint32_t qa = smem_u32(smem + C::kOffQ), ga = smem_u32(smem + C::kOffG);
+      bool ok = role_wait(&bar_q, 0, abort_flag, a.err, kErrTimeoutMma);
+      if (ok) {
+        tc_fence_after();
+        tmem_cp_atom(tmem + C::kSfQ, sSf + 0 * kAtomBytes);
+        tmem_cp_atom(tmem + C::kSfG, sSf + 1 * kAtomBytes);
+      }
+      auto issue_s = [&](int j) -> bool {  // S = Q K^T into X
+        const int s = j % C::kStages;
+        if (!role_wait(&bar_kv_full[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
+        tc_fence_after();
+        const uint32_t st = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
+        tmem_cp_atom(tmem + C::kSfK + 4 * s, sSf + (2 + 3 * s + 0) * kAtomBytes);
+#pragma unroll
+        for (int kk = 0; kk < C::kKSteps; ++kk)
+          mma_mxf8_ss(tmem + C::kColX, make_sdesc(qa + 32 * kk, 16, C::kSBO, C::kSwz),
+                      make_sdesc(st + 32 * kk, 16, C::kSBO, C::kSwz), make_idesc_mxf8(128, 128, 0, 0, kk, kk),
+                      tmem + C::kSfQ, tmem + C::kSfK + 4 * s, kk > 0);
+        mma_commit(&bar_s_full);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < n_kt; ++j) {
+        const int s = j % C::kStages;
+        const uint32_t st = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
+        if (!(ok = role_wait(&bar_x_free, j & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        tc_fence_after();
+        tmem_cp_atom(tmem + C::kSfV + 4 * s, sSf + (2 + 3 * s + 1) * kAtomBytes);
+#pragma unroll
+        for (int kk = 0; kk < C::kKSteps; ++kk)  // dP = G V^T
+          mma_mxf8_ss(tmem + C::kColX, make_sdesc(ga + 32 * kk, 16, C::kSBO, C::kSwz),
+                      make_sdesc(st + C::kTileBytes + 32 * kk, 16, C::kSBO, C::kSwz),
+                      make_idesc_mxf8(128, 128, 0, 0, kk, kk), tmem + C::kSfG, tmem + C::kSfV + 4 * s, kk > 0);
+        mma_commit(&bar_dp_full);
+        if (!(ok = role_wait(&bar_x_free2, j & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        if (j + 1 < n_kt && !(ok = issue_s(j + 1))) break;
+        if (!(ok = role_wait(&bar_ds_ready, j & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        tc_fence_after();
+        tmem_cp_atom(tmem + C::kSfKt + 4 * s, sSf + (2 + 3 * s + 2) * kAtomBytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // dQ += dS K (contraction over 128 keys)
+          mma_mxf8_ts(tmem + C::kColDQ, tmem + C::kColDS + 8 * kk,
+                      make_sdesc(st + 2 * C::kTileBytes + kk * 32 * D, 16, C::kSBO, C::kSwz),
+                      make_idesc_mxf8(128, D, 0, 1, kk, kk), tmem + C::kSfDS, tmem + C::kSfKt + 4 * s,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar_ds_free);
+        mma_commit(&bar_kv_empty[s]);
+      }
+      mma_commit(&bar_final);
+      mma_commit(&bar_drain);
+      mbar_wait(&bar_drain, 0, nullptr, 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax / dS
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // query row (TMEM lane)
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const int64_t qpos = static_cast<int64_t>(qt) * 128 + r;
+    const bool q_valid = qpos < n;
+    const int64_t t = doc_start + qpos;
+    const float sl2 = a.scale_log2;
+    float lse2 = 0.0f, dd = 0.0f;
+    if (q_valid) {
+      lse2 = a.lse[static_cast<int64_t>(h) * a.T + t] * 1.4426950408889634f;
+      dd = a.dvec[static_cast<int64_t>(h) * a.T + t];
+    }
+    bool ok = true;
+    for (int j = 0; j < n_kt; ++j) {
+      if (!(ok = warp_wait(&bar_s_full, j & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      tc_fence_after();
+      float p[128];
+      {
+        uint32_t rr[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(lane_base + C::kColX + 32 * c, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) p[32 * c + i] = __uint_as_float(rr[i]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bar_x_free);
+      const int64_t kbase = static_cast<int64_t>(j) * 128;
+      const bool full = q_valid && (kbase + 127 < n) && (!a.causal || kbase + 127 <= qpos);
+      const float nl = -lse2;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float v = ex2_approx(fmaf(p[c], sl2, nl));
+        const int64_t kp = kbase + c;
+        p[c] = (full || (q_valid && kp < n && (!a.causal || kp <= qpos))) ? v : 0.0f;
+      }
+      if (!(ok = warp_wait(&bar_dp_full, j & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      // the previous dQ MMA must be done with the dS codes and scales
+      if (j > 0 && !(ok = warp_wait(&bar_ds_free, (j - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      tc_fence_after();
+      uint32_t ebytes = 0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(lane_base + C::kColX + 32 * c, rr);
+        tmem_ld_wait();
+        float am = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float ds = p[32 * c + i] * (__uint_as_float(rr[i]) - dd);
+          rr[i] = __float_as_uint(ds);
+          am = fmaxf(am, fabsf(ds));
+        }
+        am = warp_max_abs(am);  // 32 query rows x 32 keys
+        const int e = mx_exponent_bits(__float_as_uint(am));
+        const float sc = exp2i_neg(e);
+        ebytes |= static_cast<uint32_t>(e + 127) << (8 * c);
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          w[k] = pack_e4m3x4(__uint_as_float(rr[4 * k]) * sc, __uint_as_float(rr[4 * k + 1]) * sc,
+                             __uint_as_float(rr[4 * k + 2]) * sc, __uint_as_float(rr[4 * k + 3]) * sc);
+        tmem_st8(lane_base + C::kColDS + 8 * c, w);
+      }
+      tc_fence_before();
+      mbar_arrive(&bar_x_free2);
+      // dQ's A operand is dS (rows = queries, groups = 32-key blocks): row r
+      // reads lane r, column r / 32 -> this warp's query block in column quad.
+      tmem_st1(lane_base + C::kSfDS + quad, ebytes);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar_ds_ready);
+    }
+    if (ok) ok = role_wait(&bar_final, 0, abort_flag, a.err, kErrTimeoutEpilogue);
+    if (__all_sync(0xffffffffu, ok)) {
+      tc_fence_after();
+      __nv_bfloat16* dqrow = reinterpret_cast<__nv_bfloat16*>(a.dq_out) + (t * a.Hq + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(lane_base + C::kColDQ + 32 * c, rr);
+        tmem_ld_wait();
+        if (q_valid) store_row_bf16(dqrow + 32 * c, rr, a.alpha);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+cudaError_t launch_bwd_split(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
+  const int tiles = (max_seqlen + 127) / 128;
+  dim3 g1(tiles, a.num_docs, a.Hkv), g2(tiles, a.num_docs, a.Hq);
+  cudaError_t e;
+  if (d == 128) {
+    e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DkdvCfg<128>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_bwd_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DqCfg<128>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attn_bwd_dkdv_kernel<128><<<g1, DkdvCfg<128>::kThreads, DkdvCfg<128>::kSmemBytes, stream>>>(m, a);
+    attn_bwd_dq_kernel<128><<<g2, DqCfg<128>::kThreads, DqCfg<128>::kSmemBytes, stream>>>(m, a);
+  } else {
+    e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DkdvCfg<64>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_bwd_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DqCfg<64>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attn_bwd_dkdv_kernel<64><<<g1, DkdvCfg<64>::kThreads, DkdvCfg<64>::kSmemBytes, stream>>>(m, a);
+    attn_bwd_dq_kernel<64><<<g2, DqCfg<64>::kThreads, DqCfg<64>::kSmemBytes, stream>>>(m, a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace mxa

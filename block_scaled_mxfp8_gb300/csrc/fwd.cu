@@ -25,8 +25,7 @@
 // P1 [480,512).
 #include <cuda_bf16.h>
 
-#include "kernels.cuh"
-#include "ptx.cuh"
+#include "attn_common.cuh"
 
 namespace mxa {
 
@@ -52,51 +51,6 @@ struct FwdCfg {
   static constexpr int kOffOnes = (kOffSfV + kStages * kAtomBytes + 1023) / 1024 * 1024;  // 16 x 128 B of E4M3 1.0
   static constexpr int kSmemBytes = kOffOnes + 16 * 128 + 1024;            // + alignment slack
 };
-
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Wait helper shared by all roles: bounded, and gives up early once another
-// role has recorded an abort.
-__device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
-                                          int code) {
-  if (mbar_try_wait(bar, parity)) return true;
-  long long t0 = clock64();
-  uint32_t it = 0;
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++it & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (clock64() - t0 > kWaitBudgetCycles) {
-        *abort_flag = 1;
-        if (err) atomicCAS(err, 0, code);
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, const void* smem_atom) {
-  const uint64_t desc = make_sdesc(smem_u32(smem_atom), 512, 128, kSwzNone);
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
-}
-
-__device__ __forceinline__ int64_t doc_tile_base(const int32_t* cu, int b, int64_t len, int tid, int nthreads,
-                                                 int64_t* s_slot) {
-  if (cu == nullptr) return static_cast<int64_t>(b) * ((len + 127) / 128);
-  if (tid == 0) *s_slot = 0;
-  __syncthreads();
-  int64_t part = 0;
-  for (int i = tid; i < b; i += nthreads) part += (cu[i + 1] - cu[i] + 127) / 128;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-  if ((tid & 31) == 0 && part) atomicAdd(reinterpret_cast<unsigned long long*>(s_slot), static_cast<unsigned long long>(part));
-  __syncthreads();
-  return *s_slot;
-}
 
 }  // namespace
 

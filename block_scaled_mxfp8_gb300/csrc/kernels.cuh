@@ -79,6 +79,7 @@ struct BwdArgs {
   uint16_t* dq_acc16;    // [T, Hq, d] fp16 bits (FP16 x 2^9 mode)
   void* dk;              // bf16 [T, Hkv, d]
   void* dv;              // bf16 [T, Hkv, d]
+  void* dq_out;          // bf16 [T, Hq, d] (written directly by the deterministic dQ kernel)
   int dq_mode;
   int* err;
 };
@@ -117,6 +118,7 @@ cudaError_t launch_quantize(const QuantArgs& a, int d, bool tokblock, bool hadam
                             cudaStream_t stream);
 cudaError_t launch_fwd(const FwdArgs& a, const FwdMaps& m, int d, int max_seqlen, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream);
+cudaError_t launch_bwd_split(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const PrepArgs& a, int max_seqlen, cudaStream_t stream);
 cudaError_t launch_dq_convert(const DqConvArgs& a, cudaStream_t stream);
 

@@ -91,8 +91,10 @@ typedef enum {
 enum { MXA_VIEW_ROW = 1, MXA_VIEW_TOK = 2 };
 
 typedef enum {
-  MXA_DQ_FP32 = 0,     /* dQ partial sums added in fp32 */
-  MXA_DQ_FP16_X512 = 1 /* dQ partial sums boosted by 2^9 and added in fp16; unboosted at the end */
+  MXA_DQ_FP32 = 0,     /* dQ summed in fp32 over the key tiles, in a fixed order (deterministic; a
+                          separate dQ kernel recomputes S and dP per query tile) */
+  MXA_DQ_FP16_X512 = 1 /* dQ partial sums of each key tile boosted by 2^9 and added into an fp16
+                          accumulator with atomics (order varies); unboosted at the end */
 } mxa_dq_mode;
 
 /* One quantized view of a tensor: E4M3 codes [T, H, d] and its UE8M0 scales
@@ -183,8 +185,8 @@ typedef struct {
   mxa_dq_mode dq_mode;
 } mxa_bwd_params;
 
-/* Workspace bytes mxa_bwd needs: D [Hq, T] fp32 plus the dQ accumulator
- * ([T, Hq, d] fp32 or fp16), plus alignment. */
+/* Workspace bytes mxa_bwd needs: D [Hq, T] fp32, plus (FP16_X512 mode) the
+ * fp16 dQ accumulator [T, Hq, d], each rounded up to 256 bytes. */
 size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p);
 
 /* Backward.  workspace: device buffer of at least mxa_bwd_workspace_bytes()
