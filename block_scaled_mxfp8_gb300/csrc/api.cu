@@ -227,7 +227,9 @@ size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p) {
   if (!p || p->shape.T < 0 || p->shape.Hq <= 0 || (p->shape.d != 64 && p->shape.d != 128)) return 0;
   const size_t T = static_cast<size_t>(p->shape.T), Hq = static_cast<size_t>(p->shape.Hq),
                d = static_cast<size_t>(p->shape.d);
-  const size_t dbytes = ((Hq * T * 4) + 255) & ~size_t(255);
+  const size_t NT = static_cast<size_t>(p->shape.ntiles > 0 ? p->shape.ntiles : 0);
+  const size_t dbytes = 2 * Hq * NT * 128 * 4;  // tile-padded D and LSE*log2(e)
+  (void)T;
   // FP32 mode: deterministic dQ kernel, no accumulator; FP16 x 2^9 mode:
   // fp16 partial-sum accumulator [T, Hq, d].
   const size_t acc = p->dq_mode == MXA_DQ_FP16_X512 ? T * Hq * d * 2 : 0;
@@ -260,8 +262,10 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
       !make_code_map(&maps.gt, p->g_tok.codes, s.T, s.Hq, s.d))
     return MXA_ERR_CUDA;
   const size_t T = static_cast<size_t>(s.T), Hq = static_cast<size_t>(s.Hq), d = static_cast<size_t>(s.d);
-  const size_t dbytes = ((Hq * T * 4) + 255) & ~size_t(255);
-  float* dvec = static_cast<float*>(workspace);
+  const size_t pad_elems = Hq * static_cast<size_t>(s.ntiles) * 128;
+  const size_t dbytes = 2 * pad_elems * 4;
+  float* dpad = static_cast<float*>(workspace);
+  float* lpad = dpad + pad_elems;
   void* acc = static_cast<uint8_t*>(workspace) + dbytes;
   const bool fp16 = p->dq_mode == MXA_DQ_FP16_X512;
   const size_t acc_bytes = fp16 ? T * Hq * d * 2 : 0;
@@ -277,7 +281,9 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   pa.num_docs = s.num_docs;
   pa.ntiles = s.ntiles;
   pa.o = p->o;
-  pa.dvec = dvec;
+  pa.lse = p->lse;
+  pa.dpad = dpad;
+  pa.lpad = lpad;
   pa.dq_acc = acc;
   pa.dq_acc_bytes = acc_bytes;
   if (launch_bwd_prep(pa, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
@@ -299,8 +305,8 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   a.qt_sf = p->q_tok.scales;
   a.kt_sf = p->k_tok.scales;
   a.gt_sf = p->g_tok.scales;
-  a.lse = p->lse;
-  a.dvec = dvec;
+  a.lpad = lpad;
+  a.dpad = dpad;
   a.dq_mode = p->dq_mode;
   a.dq_acc32 = nullptr;
   a.dq_acc16 = fp16 ? static_cast<uint16_t*>(acc) : nullptr;

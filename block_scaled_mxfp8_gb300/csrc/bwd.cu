@@ -68,32 +68,40 @@ struct BwdCfg {
 }  // namespace
 
 // ----------------------------------------------------------------- D prep
-// One warp per (token, head); grid over (32-token group, doc, head).
+// D_i = sum_c G~row_ic O_ic and LSE_i * log2(e), written tile-padded
+// [Hq, NT, 128] so that the backward kernels fetch a tile's 128 values with
+// one bulk copy; rows past a document's end get D = 0 and LSE = +inf (their
+// recomputed P is exp(-inf) = 0).  One CTA per (128-token tile, doc, head),
+// one warp per row.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(PrepArgs a) {
   __shared__ int64_t s_slot;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
+  const int i = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
   int64_t doc_start, n;
   doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
-  if (static_cast<int64_t>(g) * 32 >= n) return;
+  if (static_cast<int64_t>(i) * 128 >= n) return;
   const int64_t tb = doc_tile_base(a.cu_seqlens, b, n, tid, 256, &s_slot);
-  for (int rr = warp; rr < 32; rr += 8) {
-    const int64_t pos = static_cast<int64_t>(g) * 32 + rr;
-    if (pos >= n) break;
+  const int64_t slot = (static_cast<int64_t>(h) * a.ntiles + tb + i) * 128;
+  const uint8_t* atom = a.g_sf + (static_cast<int64_t>(h) * a.ntiles + tb + i) * kAtomBytes;
+  for (int r = warp; r < 128; r += 8) {
+    const int64_t pos = static_cast<int64_t>(i) * 128 + r;
+    if (pos >= n) {
+      if (lane == 0) {
+        a.dpad[slot + r] = 0.0f;
+        a.lpad[slot + r] = INFINITY;
+      }
+      continue;
+    }
     const int64_t t = doc_start + pos;
-    const int i = static_cast<int>(pos >> 7), r = static_cast<int>(pos & 127);
-    const uint8_t* atom = a.g_sf + (static_cast<int64_t>(h) * a.ntiles + tb + i) * kAtomBytes;
-    float acc = 0.0f;
-    // lane covers channels [4 lane, 4 lane + 4) for d = 128, [2 lane, 2 lane + 2) for d = 64
+    float acc;
     if (a.d == 128) {
       const int c0 = 4 * lane;
       const uint32_t codes = *reinterpret_cast<const uint32_t*>(a.g_codes + (t * a.Hq + h) * 128 + c0);
       const float sc = exp2f(static_cast<float>(static_cast<int>(atom[atom_offset(r, c0 / 32)]) - 127));
       const uint2 ov = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.o) + (t * a.Hq + h) * 128 + c0);
       const float2 g01 = e4m3x2_to_f32x2(codes & 0xFFFFu), g23 = e4m3x2_to_f32x2(codes >> 16);
-      const float o0 = __uint_as_float(ov.x << 16), o1 = __uint_as_float(ov.x & 0xFFFF0000u);
-      const float o2 = __uint_as_float(ov.y << 16), o3 = __uint_as_float(ov.y & 0xFFFF0000u);
-      acc = (g01.x * o0 + g01.y * o1 + g23.x * o2 + g23.y * o3) * sc;
+      acc = (g01.x * __uint_as_float(ov.x << 16) + g01.y * __uint_as_float(ov.x & 0xFFFF0000u) +
+             g23.x * __uint_as_float(ov.y << 16) + g23.y * __uint_as_float(ov.y & 0xFFFF0000u)) * sc;
     } else {
       const int c0 = 2 * lane;
       const uint16_t codes = *reinterpret_cast<const uint16_t*>(a.g_codes + (t * a.Hq + h) * 64 + c0);
@@ -104,7 +112,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(PrepArgs a) {
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) a.dvec[static_cast<int64_t>(h) * a.T + t] = acc;
+    if (lane == 0) {
+      a.dpad[slot + r] = acc;
+      a.lpad[slot + r] = a.lse[static_cast<int64_t>(h) * a.T + t] * 1.4426950408889634f;
+    }
   }
 }
 
@@ -330,9 +341,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const int64_t qp = static_cast<int64_t>(qi) * 128 + c;
         float l2 = 0.0f, dd = 0.0f;
         if (qp < n) {
-          const int64_t t = doc_start + qp;
-          l2 = a.lse[static_cast<int64_t>(h) * a.T + t] * 1.4426950408889634f;
-          dd = a.dvec[static_cast<int64_t>(h) * a.T + t];
+          const int64_t slot = (static_cast<int64_t>(h) * a.ntiles + tile_base + qi) * 128 + c;
+          l2 = a.lpad[slot];
+          dd = a.dpad[slot];
         }
         sLse[par * 128 + c] = l2;
         sDv[par * 128 + c] = dd;
@@ -533,7 +544,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
 cudaError_t launch_bwd_prep(const PrepArgs& a, int max_seqlen, cudaStream_t stream) {
   if (a.dq_acc_bytes && cudaMemsetAsync(a.dq_acc, 0, a.dq_acc_bytes, stream) != cudaSuccess) return cudaGetLastError();
-  dim3 grid((max_seqlen + 31) / 32, a.num_docs, a.Hq);
+  dim3 grid((max_seqlen + 127) / 128, a.num_docs, a.Hq);
   bwd_prep_kernel<<<grid, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }

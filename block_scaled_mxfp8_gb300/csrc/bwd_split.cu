@@ -17,6 +17,15 @@
 // Both recompute S and dP (the FLOP convention counts the backward as 2.5
 // forwards; these two kernels execute 3.5).  The 32 x 32 blocks are the same
 // in both kernels; each quantizes its own fp32 dS.
+//
+// Warps: 0 = TMA producer, 1 = MMA issuer, 2 = TMEM owner, 4..11 = softmax.
+// Two softmax warps share each TMEM lane quadrant and split the tile's 128
+// columns into halves of 64 (two 32 x 32 dS blocks each), so every SM
+// sub-partition has two softmax warps to interleave.  The halves write their
+// dS block exponents into separate scale-factor columns; the gradient MMA
+// reads K steps 0-1 from the first and 2-3 from the second.
+// LSE (times log2 e; +inf past a document's end) and D come tile-padded from
+// the prep kernel and are bulk-loaded with the tiles.
 #include <cuda_bf16.h>
 
 #include "attn_common.cuh"
@@ -25,6 +34,9 @@ namespace mxa {
 
 namespace {
 
+constexpr int kSplitThreads = 384;
+constexpr int kSoftmaxThreads = 256;
+
 template <int D>
 struct DkdvCfg {
   static constexpr int kStages = 2;
@@ -32,20 +44,17 @@ struct DkdvCfg {
   static constexpr uint32_t kSwz = D == 128 ? kSwz128 : kSwz64;
   static constexpr uint32_t kSBO = 8 * D;
   static constexpr int kKSteps = D / 32;
-  static constexpr int kThreads = 256;
   // TMEM: X holds S^T then dP^T; dV, dK accumulators; P^T and dS^T codes
   static constexpr uint32_t kColX = 0, kColDV = 128, kColDK = 256, kColP = 384, kColDS = 416;
   static constexpr uint32_t kSfK = 448, kSfQ = 452 /*+4s*/, kSfV = 460, kSfG = 464 /*+4s*/, kSfP = 472,
-                            kSfGt = 476 /*+4s*/, kSfDS = 484, kSfQt = 488 /*+4s*/;
-  // shared memory
+                            kSfGt = 476 /*+4s*/, kSfDS0 = 484, kSfDS1 = 488, kSfQt = 492 /*+4s*/;
+  // shared memory: K, V, then per stage Q, G, Qt, Gt tiles + LSE + D rows
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffStage = kOffV + kTileBytes;  // per stage: Q, G, Qt, Gt
-  static constexpr int kStageBytes = 4 * kTileBytes;
+  static constexpr int kOffStage = kOffV + kTileBytes;
+  static constexpr int kStageBytes = 4 * kTileBytes + 2 * 512;
   static constexpr int kOffSf = kOffStage + kStages * kStageBytes;  // K, V, then 4 per stage
-  static constexpr int kOffLse = kOffSf + (2 + 4 * kStages) * kAtomBytes;
-  static constexpr int kOffDv = kOffLse + 2 * 128 * 4;
-  static constexpr int kSmemBytes = kOffDv + 2 * 128 * 4 + 1024;
+  static constexpr int kSmemBytes = kOffSf + (2 + 4 * kStages) * kAtomBytes + 1024;
 };
 
 template <int D>
@@ -55,11 +64,10 @@ struct DqCfg {
   static constexpr uint32_t kSwz = D == 128 ? kSwz128 : kSwz64;
   static constexpr uint32_t kSBO = 8 * D;
   static constexpr int kKSteps = D / 32;
-  static constexpr int kThreads = 256;
   // TMEM: X holds S then dP; dQ accumulator; dS codes
   static constexpr uint32_t kColX = 0, kColDQ = 128, kColDS = 256;
-  static constexpr uint32_t kSfQ = 288, kSfG = 292, kSfK = 296 /*+4s*/, kSfV = 304 /*+4s*/, kSfDS = 312,
-                            kSfKt = 316 /*+4s*/;
+  static constexpr uint32_t kSfQ = 288, kSfG = 292, kSfK = 296 /*+4s*/, kSfV = 304 /*+4s*/, kSfDS0 = 312,
+                            kSfDS1 = 316, kSfKt = 320 /*+4s*/;
   static constexpr int kOffQ = 0;
   static constexpr int kOffG = kOffQ + kTileBytes;
   static constexpr int kOffStage = kOffG + kTileBytes;  // per stage: K, V, Kt
@@ -80,18 +88,49 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
   }
 }
 
+// 64 fp32 columns of this thread's TMEM lane: two 32-column loads, one wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t a[32], b[32];
+  tmem_ld32(taddr, a);
+  tmem_ld32(taddr + 32, b);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = __uint_as_float(a[i]);
+    v[32 + i] = __uint_as_float(b[i]);
+  }
+}
+
+// Quantize one 32 x 32 dS block held as 32 values per thread across the warp:
+// block max-abs by a warp reduction, exponent e (shifted by `shift` when the
+// values carry a 2^shift boost, floored at the UE8M0 minimum), E4M3 codes
+// into w.  Returns the scale byte of the unboosted block.
+__device__ __forceinline__ uint32_t quant_ds_block(const float (&x)[32], int shift, uint32_t (&w)[8]) {
+  float am = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(x[i]));
+  am = warp_max_abs(am);
+  int e = mx_exponent_bits(__float_as_uint(am)) - shift;
+  if (e < -127) e = -127;
+  const float sc = exp2i_neg(e + shift);
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    w[k] = pack_e4m3x4(x[4 * k] * sc, x[4 * k + 1] * sc, x[4 * k + 2] * sc, x[4 * k + 3] * sc);
+  return static_cast<uint32_t>(e + 127);
+}
+
 }  // namespace
 
 // ========================================================================= dK, dV
 template <int D>
-__global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1)
+__global__ void __launch_bounds__(kSplitThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   __shared__ uint64_t bar_kv, bar_tile_full[C::kStages], bar_tile_empty[C::kStages], bar_s_full, bar_x_free,
-      bar_dp_full, bar_x_free2, bar_p_ready, bar_pds_free, bar_final, bar_drain, bar_lse[2];
+      bar_dp_full, bar_x_free2, bar_p_ready, bar_pds_free, bar_final, bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int64_t s_slot;
@@ -106,7 +145,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1)
   const int qi0 = a.causal ? kt : 0;
   const int nq = n_tiles - qi0;
   const int n_work = nq * grp;
-  const int64_t tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, C::kThreads, &s_slot);
+  const int64_t tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, kSplitThreads, &s_slot);
 
   if (tid == 0) {
     mbar_init(&bar_kv, 1);
@@ -115,15 +154,13 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1)
       mbar_init(&bar_tile_empty[s], 1);
     }
     mbar_init(&bar_s_full, 1);
-    mbar_init(&bar_x_free, 128);
+    mbar_init(&bar_x_free, kSoftmaxThreads);
     mbar_init(&bar_dp_full, 1);
-    mbar_init(&bar_x_free2, 128);
-    mbar_init(&bar_p_ready, 128);
+    mbar_init(&bar_x_free2, kSoftmaxThreads);
+    mbar_init(&bar_p_ready, kSoftmaxThreads);
     mbar_init(&bar_pds_free, 1);
     mbar_init(&bar_final, 1);
     mbar_init(&bar_drain, 1);
-    mbar_init(&bar_lse[0], 128);
-    mbar_init(&bar_lse[1], 128);
     s_abort = 0;
     fence_barrier_init();
   }
@@ -137,8 +174,6 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1)
   const uint32_t tmem = s_tmem;
   volatile int* abort_flag = &s_abort;
   uint8_t* sSf = smem + C::kOffSf;  // [0] K, [1] V, stage s: 2 + 4s + (0 Q, 1 G, 2 Qt, 3 Gt)
-  float* sLse = reinterpret_cast<float*>(smem + C::kOffLse);
-  float* sDv = reinterpret_cast<float*>(smem + C::kOffDv);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -159,18 +194,20 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1)
         const int h = hk * grp + u / nq;
         const int qi = qi0 + u % nq;
         const int q0 = static_cast<int>(doc_start + static_cast<int64_t>(qi) * 128);
-        const int64_t qatom = (static_cast<int64_t>(h) * a.ntiles + tile_base + qi) * kAtomBytes;
+        const int64_t qslot = static_cast<int64_t>(h) * a.ntiles + tile_base + qi;
         uint8_t* st = smem + C::kOffStage + s * C::kStageBytes;
         uint8_t* sf = sSf + (2 + 4 * s) * kAtomBytes;
-        mbar_arrive_expect_tx(&bar_tile_full[s], 4 * C::kTileBytes + 4 * kAtomBytes);
+        mbar_arrive_expect_tx(&bar_tile_full[s], 4 * C::kTileBytes + 4 * kAtomBytes + 2 * 512);
         tma_load_3d(st + 0 * C::kTileBytes, &maps.q, &bar_tile_full[s], 0, h, q0);
         tma_load_3d(st + 1 * C::kTileBytes, &maps.g, &bar_tile_full[s], 0, h, q0);
         tma_load_3d(st + 2 * C::kTileBytes, &maps.qt, &bar_tile_full[s], 0, h, q0);
         tma_load_3d(st + 3 * C::kTileBytes, &maps.gt, &bar_tile_full[s], 0, h, q0);
-        bulk_load(sf + 0 * kAtomBytes, a.q_sf + qatom, kAtomBytes, &bar_tile_full[s]);
-        bulk_load(sf + 1 * kAtomBytes, a.g_sf + qatom, kAtomBytes, &bar_tile_full[s]);
-        bulk_load(sf + 2 * kAtomBytes, a.qt_sf + qatom, kAtomBytes, &bar_tile_full[s]);
-        bulk_load(sf + 3 * kAtomBytes, a.gt_sf + qatom, kAtomBytes, &bar_tile_full[s]);
+        bulk_load(st + 4 * C::kTileBytes, a.lpad + qslot * 128, 512, &bar_tile_full[s]);
+        bulk_load(st + 4 * C::kTileBytes + 512, a.dpad + qslot * 128, 512, &bar_tile_full[s]);
+        bulk_load(sf + 0 * kAtomBytes, a.q_sf + qslot * kAtomBytes, kAtomBytes, &bar_tile_full[s]);
+        bulk_load(sf + 1 * kAtomBytes, a.g_sf + qslot * kAtomBytes, kAtomBytes, &bar_tile_full[s]);
+        bulk_load(sf + 2 * kAtomBytes, a.qt_sf + qslot * kAtomBytes, kAtomBytes, &bar_tile_full[s]);
+        bulk_load(sf + 3 * kAtomBytes, a.gt_sf + qslot * kAtomBytes, kAtomBytes, &bar_tile_full[s]);
         issued = u + 1;
       }
       role_wait(&bar_kv, 0, abort_flag, nullptr, 0);
@@ -233,8 +270,8 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1)
         for (int kk = 0; kk < 4; ++kk)
           mma_mxf8_ts(tmem + C::kColDK, tmem + C::kColDS + 8 * kk,
                       make_sdesc(st + 2 * C::kTileBytes + kk * 32 * D, 16, C::kSBO, C::kSwz),
-                      make_idesc_mxf8(128, D, 0, 1, kk, kk), tmem + C::kSfDS, tmem + C::kSfQt + 4 * s,
-                      (u > 0 || kk > 0) ? 1u : 0u);
+                      make_idesc_mxf8(128, D, 0, 1, kk & 1, kk), tmem + (kk < 2 ? C::kSfDS0 : C::kSfDS1),
+                      tmem + C::kSfQt + 4 * s, (u > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bar_pds_free);
         mma_commit(&bar_tile_empty[s]);
       }
@@ -245,98 +282,81 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / dS
     const int quad = warp & 3;
-    const int j = quad * 32 + lane;  // key row (TMEM lane)
+    const int hf = (warp - 4) >> 2;       // column half: queries [64 hf, 64 hf + 64)
+    const int j = quad * 32 + lane;       // key row (TMEM lane)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const int64_t kpos = static_cast<int64_t>(kt) * 128 + j;
     const bool key_valid = kpos < n;
+    const float kb8 = key_valid ? 8.0f : -INFINITY;  // 2^8 boost of P^T; invalid key rows -> 0
     const float sl2 = a.scale_log2;
-    tmem_st4(lane_base + C::kSfP, 0x77777777u, 0x77777777u, 0x77777777u, 0x77777777u);  // 2^-8
-    tmem_st_wait();
+    if (hf == 0) {
+      tmem_st4(lane_base + C::kSfP, 0x77777777u, 0x77777777u, 0x77777777u, 0x77777777u);  // 2^-8
+      tmem_st_wait();
+    }
     bool ok = true;
     for (int u = 0; u < n_work; ++u) {
-      const int h = hk * grp + u / nq;
+      const int s = u % C::kStages;
       const int qi = qi0 + u % nq;
-      const int par = u & 1;
-      {
-        const int64_t qp = static_cast<int64_t>(qi) * 128 + j;  // thread j loads query j's LSE and D
-        float l2 = 0.0f, dd = 0.0f;
-        if (qp < n) {
-          const int64_t t = doc_start + qp;
-          l2 = a.lse[static_cast<int64_t>(h) * a.T + t] * 1.4426950408889634f;
-          dd = a.dvec[static_cast<int64_t>(h) * a.T + t];
-        }
-        sLse[par * 128 + j] = l2;
-        sDv[par * 128 + j] = dd;
-      }
-      mbar_arrive(&bar_lse[par]);
-      if (!(ok = warp_wait(&bar_lse[par], (u >> 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      const float* lrow = reinterpret_cast<const float*>(smem + C::kOffStage + s * C::kStageBytes + 4 * C::kTileBytes) + 64 * hf;
+      const float* drow = lrow + 128;
       if (!(ok = warp_wait(&bar_s_full, u & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
-      float p[128];
-      {
-        uint32_t rr[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(lane_base + C::kColX + 32 * c, rr);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) p[32 * c + i] = __uint_as_float(rr[i]);
-        }
-      }
+      float p[64];
+      tmem_ld64(lane_base + C::kColX + 64 * hf, p);
       tc_fence_before();
       mbar_arrive(&bar_x_free);
-      const int64_t qbase = static_cast<int64_t>(qi) * 128;
-      const bool full = key_valid && (qbase + 127 < n) && (!a.causal || kpos <= qbase);
+      // P^T boosted by 2^8 (P <= 1 after the LSE normalization); rows past the
+      // document end have LSE = +inf, so their P is 0 without a test
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float v = ex2_approx(fmaf(p[c], sl2, -sLse[par * 128 + c]));
-        const int64_t qp = qbase + c;
-        p[c] = (full || (key_valid && qp < n && (!a.causal || kpos <= qp))) ? v : 0.0f;
+      for (int c = 0; c < 64; c += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(lrow + c);
+        p[c] = ex2_approx(fmaf(p[c], sl2, kb8 - l4.x));
+        p[c + 1] = ex2_approx(fmaf(p[c + 1], sl2, kb8 - l4.y));
+        p[c + 2] = ex2_approx(fmaf(p[c + 2], sl2, kb8 - l4.z));
+        p[c + 3] = ex2_approx(fmaf(p[c + 3], sl2, kb8 - l4.w));
       }
-      // the previous tile's dV / dK MMAs must be done with the P, dS codes and scales
+      if (a.causal && qi == kt) {  // diagonal tile: query index (in tile) >= key index
+#pragma unroll
+        for (int c = 0; c < 64; ++c) p[c] = (64 * hf + c >= j) ? p[c] : 0.0f;
+      }
+      // the previous tile's dV / dK MMAs must be done with the codes and scales
       if (u > 0 && !(ok = warp_wait(&bar_pds_free, (u - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 32; c += 8) {
+      for (int c = 0; c < 16; c += 8) {
         uint32_t w[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          w[k] = pack_e4m3x4(p[4 * (c + k)] * 256.0f, p[4 * (c + k) + 1] * 256.0f, p[4 * (c + k) + 2] * 256.0f,
-                             p[4 * (c + k) + 3] * 256.0f);
-        tmem_st8(lane_base + C::kColP + c, w);
+          w[k] = pack_e4m3x4(p[4 * (c + k)], p[4 * (c + k) + 1], p[4 * (c + k) + 2], p[4 * (c + k) + 3]);
+        tmem_st8(lane_base + C::kColP + 16 * hf + c, w);
       }
       if (!(ok = warp_wait(&bar_dp_full, u & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
       uint32_t ebytes = 0;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t rr[32];
-        tmem_ld32(lane_base + C::kColX + 32 * c, rr);
+        tmem_ld32(lane_base + C::kColX + 64 * hf + 32 * cc, rr);
         tmem_ld_wait();
-        float am = 0.0f;
+        float x[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float ds = p[32 * c + i] * (__uint_as_float(rr[i]) - sDv[par * 128 + 32 * c + i]);
-          rr[i] = __float_as_uint(ds);
-          am = fmaxf(am, fabsf(ds));
+        for (int i = 0; i < 32; i += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(drow + 32 * cc + i);
+          x[i] = p[32 * cc + i] * (__uint_as_float(rr[i]) - d4.x);
+          x[i + 1] = p[32 * cc + i + 1] * (__uint_as_float(rr[i + 1]) - d4.y);
+          x[i + 2] = p[32 * cc + i + 2] * (__uint_as_float(rr[i + 2]) - d4.z);
+          x[i + 3] = p[32 * cc + i + 3] * (__uint_as_float(rr[i + 3]) - d4.w);
         }
-        am = warp_max_abs(am);  // 32 key rows x 32 queries
-        const int e = mx_exponent_bits(__float_as_uint(am));
-        const float sc = exp2i_neg(e);
-        ebytes |= static_cast<uint32_t>(e + 127) << (8 * c);
         uint32_t w[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          w[k] = pack_e4m3x4(__uint_as_float(rr[4 * k]) * sc, __uint_as_float(rr[4 * k + 1]) * sc,
-                             __uint_as_float(rr[4 * k + 2]) * sc, __uint_as_float(rr[4 * k + 3]) * sc);
-        tmem_st8(lane_base + C::kColDS + 8 * c, w);
+        ebytes |= quant_ds_block(x, 8, w) << (8 * cc);  // 32 key rows x 32 queries
+        tmem_st8(lane_base + C::kColDS + 16 * hf + 8 * cc, w);
       }
       tc_fence_before();
       mbar_arrive(&bar_x_free2);
-      // dK's A operand is dS^T (rows = keys, groups = 32-query blocks); the
-      // tensor core reads row r's scales from lane r, column r / 32, so each
-      // warp's 32 lanes carry its own key block's four exponents in column quad.
-      tmem_st1(lane_base + C::kSfDS + quad, ebytes);
+      // dK's A operand is dS^T (rows = keys, groups = 32-query blocks); row r's
+      // scales sit in lane r, column base + r / 32.  Half hf owns query
+      // blocks 2 hf, 2 hf + 1 (bytes 0, 1 of its own scale columns).
+      tmem_st1(lane_base + (hf ? C::kSfDS1 : C::kSfDS0) + quad, ebytes | 0x7F7F0000u);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bar_p_ready);
@@ -348,15 +368,16 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1)
       const int64_t t = doc_start + kpos;
       __nv_bfloat16* dvrow = reinterpret_cast<__nv_bfloat16*>(a.dv) + (t * a.Hkv + hk) * D;
       __nv_bfloat16* dkrow = reinterpret_cast<__nv_bfloat16*>(a.dk) + (t * a.Hkv + hk) * D;
+      // half 0 writes dV, half 1 writes dK
+      const uint32_t col = hf ? C::kColDK : C::kColDV;
+      __nv_bfloat16* dst = hf ? dkrow : dvrow;
+      const float mul = hf ? a.alpha : 1.0f;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t rr[32];
-        tmem_ld32(lane_base + C::kColDV + 32 * c, rr);
+        tmem_ld32(lane_base + col + 32 * c, rr);
         tmem_ld_wait();
-        if (key_valid) store_row_bf16(dvrow + 32 * c, rr, 1.0f);
-        tmem_ld32(lane_base + C::kColDK + 32 * c, rr);
-        tmem_ld_wait();
-        if (key_valid) store_row_bf16(dkrow + 32 * c, rr, a.alpha);
+        if (key_valid) store_row_bf16(dst + 32 * c, rr, mul);
       }
     }
   }
@@ -370,7 +391,7 @@ __global__ void __launch_bounds__(DkdvCfg<D>::kThreads, 1)
 
 // ========================================================================= dQ
 template <int D>
-__global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
+__global__ void __launch_bounds__(kSplitThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -391,7 +412,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   const int qt = a.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
   if (qt >= n_tiles) return;
   const int n_kt = a.causal ? qt + 1 : n_tiles;
-  const int64_t tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, C::kThreads, &s_slot);
+  const int64_t tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, kSplitThreads, &s_slot);
 
   if (tid == 0) {
     mbar_init(&bar_q, 1);
@@ -400,10 +421,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       mbar_init(&bar_kv_empty[s], 1);
     }
     mbar_init(&bar_s_full, 1);
-    mbar_init(&bar_x_free, 128);
+    mbar_init(&bar_x_free, kSoftmaxThreads);
     mbar_init(&bar_dp_full, 1);
-    mbar_init(&bar_x_free2, 128);
-    mbar_init(&bar_ds_ready, 128);
+    mbar_init(&bar_x_free2, kSoftmaxThreads);
+    mbar_init(&bar_ds_ready, kSoftmaxThreads);
     mbar_init(&bar_ds_free, 1);
     mbar_init(&bar_final, 1);
     mbar_init(&bar_drain, 1);
@@ -500,8 +521,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         for (int kk = 0; kk < 4; ++kk)  // dQ += dS K (contraction over 128 keys)
           mma_mxf8_ts(tmem + C::kColDQ, tmem + C::kColDS + 8 * kk,
                       make_sdesc(st + 2 * C::kTileBytes + kk * 32 * D, 16, C::kSBO, C::kSwz),
-                      make_idesc_mxf8(128, D, 0, 1, kk, kk), tmem + C::kSfDS, tmem + C::kSfKt + 4 * s,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+                      make_idesc_mxf8(128, D, 0, 1, kk & 1, kk), tmem + (kk < 2 ? C::kSfDS0 : C::kSfDS1),
+                      tmem + C::kSfKt + 4 * s, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bar_ds_free);
         mma_commit(&bar_kv_empty[s]);
       }
@@ -512,42 +533,32 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / dS
     const int quad = warp & 3;
-    const int r = quad * 32 + lane;  // query row (TMEM lane)
+    const int hf = (warp - 4) >> 2;       // column half: keys [64 hf, 64 hf + 64)
+    const int r = quad * 32 + lane;       // query row (TMEM lane)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const int64_t qpos = static_cast<int64_t>(qt) * 128 + r;
     const bool q_valid = qpos < n;
-    const int64_t t = doc_start + qpos;
+    const int64_t slot = (static_cast<int64_t>(h) * a.ntiles + tile_base + qt) * 128 + r;
+    const float nl = -a.lpad[slot];  // -inf for rows past the document end -> P = 0
+    const float dd = a.dpad[slot];
     const float sl2 = a.scale_log2;
-    float lse2 = 0.0f, dd = 0.0f;
-    if (q_valid) {
-      lse2 = a.lse[static_cast<int64_t>(h) * a.T + t] * 1.4426950408889634f;
-      dd = a.dvec[static_cast<int64_t>(h) * a.T + t];
-    }
     bool ok = true;
     for (int j = 0; j < n_kt; ++j) {
       if (!(ok = warp_wait(&bar_s_full, j & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
-      float p[128];
-      {
-        uint32_t rr[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(lane_base + C::kColX + 32 * c, rr);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) p[32 * c + i] = __uint_as_float(rr[i]);
-        }
-      }
+      float p[64];
+      tmem_ld64(lane_base + C::kColX + 64 * hf, p);
       tc_fence_before();
       mbar_arrive(&bar_x_free);
-      const int64_t kbase = static_cast<int64_t>(j) * 128;
-      const bool full = q_valid && (kbase + 127 < n) && (!a.causal || kbase + 127 <= qpos);
-      const float nl = -lse2;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float v = ex2_approx(fmaf(p[c], sl2, nl));
-        const int64_t kp = kbase + c;
-        p[c] = (full || (q_valid && kp < n && (!a.causal || kp <= qpos))) ? v : 0.0f;
+      for (int c = 0; c < 64; ++c) p[c] = ex2_approx(fmaf(p[c], sl2, nl));
+      // keys past the document end (last tile) or after the query (diagonal tile)
+      const int64_t rem = n - static_cast<int64_t>(j) * 128;
+      int lim = rem < 128 ? static_cast<int>(rem) : 128;
+      if (a.causal && j == qt) lim = min(lim, r + 1);
+      if (lim < 128) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) p[c] = (64 * hf + c < lim) ? p[c] : 0.0f;
       }
       if (!(ok = warp_wait(&bar_dp_full, j & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       // the previous dQ MMA must be done with the dS codes and scales
@@ -555,33 +566,23 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       tc_fence_after();
       uint32_t ebytes = 0;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t rr[32];
-        tmem_ld32(lane_base + C::kColX + 32 * c, rr);
+        tmem_ld32(lane_base + C::kColX + 64 * hf + 32 * cc, rr);
         tmem_ld_wait();
-        float am = 0.0f;
+        float x[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float ds = p[32 * c + i] * (__uint_as_float(rr[i]) - dd);
-          rr[i] = __float_as_uint(ds);
-          am = fmaxf(am, fabsf(ds));
-        }
-        am = warp_max_abs(am);  // 32 query rows x 32 keys
-        const int e = mx_exponent_bits(__float_as_uint(am));
-        const float sc = exp2i_neg(e);
-        ebytes |= static_cast<uint32_t>(e + 127) << (8 * c);
+        for (int i = 0; i < 32; ++i) x[i] = p[32 * cc + i] * (__uint_as_float(rr[i]) - dd);
         uint32_t w[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          w[k] = pack_e4m3x4(__uint_as_float(rr[4 * k]) * sc, __uint_as_float(rr[4 * k + 1]) * sc,
-                             __uint_as_float(rr[4 * k + 2]) * sc, __uint_as_float(rr[4 * k + 3]) * sc);
-        tmem_st8(lane_base + C::kColDS + 8 * c, w);
+        ebytes |= quant_ds_block(x, 0, w) << (8 * cc);  // 32 query rows x 32 keys
+        tmem_st8(lane_base + C::kColDS + 16 * hf + 8 * cc, w);
       }
       tc_fence_before();
       mbar_arrive(&bar_x_free2);
-      // dQ's A operand is dS (rows = queries, groups = 32-key blocks): row r
-      // reads lane r, column r / 32 -> this warp's query block in column quad.
-      tmem_st1(lane_base + C::kSfDS + quad, ebytes);
+      // dQ's A operand is dS (rows = queries, groups = 32-key blocks): row r's
+      // scales sit in lane r, column base + r / 32; half hf owns key blocks
+      // 2 hf, 2 hf + 1.
+      tmem_st1(lane_base + (hf ? C::kSfDS1 : C::kSfDS0) + quad, ebytes | 0x7F7F0000u);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bar_ds_ready);
@@ -589,13 +590,16 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     if (ok) ok = role_wait(&bar_final, 0, abort_flag, a.err, kErrTimeoutEpilogue);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
+      const int64_t t = doc_start + qpos;
       __nv_bfloat16* dqrow = reinterpret_cast<__nv_bfloat16*>(a.dq_out) + (t * a.Hq + h) * D;
+      // each half writes half of the row's channels
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t rr[32];
-        tmem_ld32(lane_base + C::kColDQ + 32 * c, rr);
+        const int cb = (D / 2) * hf + 32 * c;
+        tmem_ld32(lane_base + C::kColDQ + cb, rr);
         tmem_ld_wait();
-        if (q_valid) store_row_bf16(dqrow + 32 * c, rr, a.alpha);
+        if (q_valid) store_row_bf16(dqrow + cb, rr, a.alpha);
       }
     }
   }
@@ -618,8 +622,8 @@ cudaError_t launch_bwd_split(const BwdArgs& a, const BwdMaps& m, int d, int max_
     e = cudaFuncSetAttribute(attn_bwd_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DqCfg<128>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attn_bwd_dkdv_kernel<128><<<g1, DkdvCfg<128>::kThreads, DkdvCfg<128>::kSmemBytes, stream>>>(m, a);
-    attn_bwd_dq_kernel<128><<<g2, DqCfg<128>::kThreads, DqCfg<128>::kSmemBytes, stream>>>(m, a);
+    attn_bwd_dkdv_kernel<128><<<g1, kSplitThreads, DkdvCfg<128>::kSmemBytes, stream>>>(m, a);
+    attn_bwd_dq_kernel<128><<<g2, kSplitThreads, DqCfg<128>::kSmemBytes, stream>>>(m, a);
   } else {
     e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DkdvCfg<64>::kSmemBytes);
@@ -627,8 +631,8 @@ cudaError_t launch_bwd_split(const BwdArgs& a, const BwdMaps& m, int d, int max_
     e = cudaFuncSetAttribute(attn_bwd_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DqCfg<64>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attn_bwd_dkdv_kernel<64><<<g1, DkdvCfg<64>::kThreads, DkdvCfg<64>::kSmemBytes, stream>>>(m, a);
-    attn_bwd_dq_kernel<64><<<g2, DqCfg<64>::kThreads, DqCfg<64>::kSmemBytes, stream>>>(m, a);
+    attn_bwd_dkdv_kernel<64><<<g1, kSplitThreads, DkdvCfg<64>::kSmemBytes, stream>>>(m, a);
+    attn_bwd_dq_kernel<64><<<g2, kSplitThreads, DqCfg<64>::kSmemBytes, stream>>>(m, a);
   }
   return cudaGetLastError();
 }

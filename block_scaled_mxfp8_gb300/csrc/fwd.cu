@@ -16,7 +16,8 @@
 //   O = O / L -> bf16, LSE = m + ln l with l the fp32 sum of the unquantized
 //   weights (FLAMIA notes sec. 2, online softmax).
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM
-// owner, warps 4..7 = softmax / correction / epilogue (thread = query row).
+// owner, warps 4..11 = softmax / correction / epilogue (two warps per query
+// row quadrant, each taking half of the 128 key columns).
 // S is double buffered in TMEM so that S_{j+1} = Q K_{j+1}^T runs on the
 // tensor core while the softmax warps work on S_j.
 //
@@ -38,7 +39,7 @@ struct FwdCfg {
   static constexpr uint32_t kSwz = D == 128 ? kSwz128 : kSwz64;
   static constexpr uint32_t kSBO = 8 * D;
   static constexpr int kKSteps = D / 32;
-  static constexpr int kThreads = 256;
+  static constexpr int kThreads = 384;  // 4 role warps + 8 softmax warps
   static constexpr uint32_t kColS = 0, kColO = 256, kColL = 384, kColSfQ = 400, kColSfK = 404, kColSfV = 416,
                             kColSfP = 428, kColSf1 = 432, kColP = 448;
   // shared memory map (offsets from the 1024-aligned base)
@@ -62,7 +63,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   __shared__ uint64_t bar_q, bar_kv_full[C::kStages], bar_kv_empty[C::kStages], bar_s_full[2], bar_s_empty[2],
-      bar_p_full[2], bar_o_done, bar_drain;
+      bar_p_full[2], bar_o_done, bar_drain, bar_mx[2], bar_lsum;
+  __shared__ float s_mx[2][2][128];  // [tile parity][half][row] partial row maxima
+  __shared__ float s_l[2][128];      // [half][row] partial row sums
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int64_t s_slot;
@@ -87,11 +90,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_s_full[i], 1);
-      mbar_init(&bar_s_empty[i], 128);
-      mbar_init(&bar_p_full[i], 128);
+      mbar_init(&bar_s_empty[i], 256);
+      mbar_init(&bar_p_full[i], 256);
+      mbar_init(&bar_mx[i], 256);
     }
     mbar_init(&bar_o_done, 1);
     mbar_init(&bar_drain, 1);
+    mbar_init(&bar_lsum, 256);
     s_abort = 0;
     fence_barrier_init();
   }
@@ -202,50 +207,59 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
+    // Two warps per TMEM lane quadrant: warp half hf handles key columns
+    // [64 hf, 64 hf + 64) of its 32 rows; the halves exchange their row maxima
+    // through shared memory once per tile and keep separate partial sums.
     const int quad = warp & 3;
+    const int hf = (warp - 4) >> 2;
     const int r = quad * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const int64_t qpos = static_cast<int64_t>(qt) * 128 + r;  // document-relative query index
     const float sl2 = a.scale_log2;
-    // P scale factor 2^-4 in every cell of its 4 columns
-    tmem_st4(lane_base + C::kColSfP, 0x7B7B7B7Bu, 0x7B7B7B7Bu, 0x7B7B7B7Bu, 0x7B7B7B7Bu);
-    tmem_st4(lane_base + C::kColSf1, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-    tmem_st_wait();
+    if (hf == 0) {
+      // P scale 2^-4 and the ones tile's scale 1 in every cell of their columns
+      tmem_st4(lane_base + C::kColSfP, 0x7B7B7B7Bu, 0x7B7B7B7Bu, 0x7B7B7B7Bu, 0x7B7B7B7Bu);
+      tmem_st4(lane_base + C::kColSf1, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      tmem_st_wait();
+    }
     float m = -INFINITY;  // running (lazy) max of the scaled scores, log2 units
-    float l16 = 0.0f;     // sum of 2^(s - m + 4)
+    float l16 = 0.0f;     // this half's sum of 2^(s - m + 4)
     bool ok = true;
     for (int j = 0; j < n_kt; ++j) {
       const int bb = j & 1;
-      ok = role_wait(&bar_s_full[bb], (j >> 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
+      if (!(ok = warp_wait(&bar_s_full[bb], (j >> 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
-      float sv[128];
+      float sv[64];
       {
-        uint32_t rr[32];
+        uint32_t x0[32], x1[32];
+        tmem_ld32(lane_base + C::kColS + 128 * bb + 64 * hf, x0);
+        tmem_ld32(lane_base + C::kColS + 128 * bb + 64 * hf + 32, x1);
+        tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(lane_base + C::kColS + 128 * bb + 32 * c, rr);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) sv[32 * c + i] = __uint_as_float(rr[i]);
+        for (int i = 0; i < 32; ++i) {
+          sv[i] = __uint_as_float(x0[i]);
+          sv[32 + i] = __uint_as_float(x1[i]);
         }
       }
       tc_fence_before();
       mbar_arrive(&bar_s_empty[bb]);
       if (j == n_kt - 1) {
-        const int64_t kbase = static_cast<int64_t>(j) * 128;
+        // keys past the document end, or (causal diagonal) after the query
+        const int64_t rem = n - static_cast<int64_t>(j) * 128;
+        int lim = rem < 128 ? static_cast<int>(rem) : 128;
+        if (a.causal) lim = min(lim, r + 1);
+        if (lim < 128) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const int64_t kp = kbase + c;
-          if (kp >= n || (a.causal && kp > qpos)) sv[c] = -INFINITY;
+          for (int c = 0; c < 64; ++c) sv[c] = (64 * hf + c < lim) ? sv[c] : -INFINITY;
         }
       }
       float mt = sv[0];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mt = fmaxf(mt, sv[c]);
+      for (int c = 1; c < 64; ++c) mt = fmaxf(mt, sv[c]);
+      s_mx[bb][hf][r] = mt;
+      mbar_arrive(&bar_mx[bb]);
+      if (!(ok = warp_wait(&bar_mx[bb], (j >> 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      mt = fmaxf(mt, s_mx[bb][hf ^ 1][r]);
       const float mts = mt * sl2;
       bool rescale_o = false;
       float factor = 1.0f;
@@ -257,10 +271,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         rescale_o = true;
       }
       const float neg = 4.0f - m;
-      uint32_t pw[32];
+      uint32_t pw[16];
       float lsum = 0.0f;
 #pragma unroll
-      for (int c = 0; c < 128; c += 4) {
+      for (int c = 0; c < 64; c += 4) {
         const float p0 = ex2_approx(fmaf(sv[c], sl2, neg));
         const float p1 = ex2_approx(fmaf(sv[c + 1], sl2, neg));
         const float p2 = ex2_approx(fmaf(sv[c + 2], sl2, neg));
@@ -269,29 +283,26 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         pw[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
       }
       l16 = l16 * factor + lsum;
-      // tcgen05.ld/st are warp-collective: the whole warp rescales its 32 O
-      // rows when any of them needs it (factor 1 for the others).
+      // tcgen05.ld/st are warp-collective: the whole warp rescales its rows'
+      // half of O when any of them needs it (factor 1 for the others).
       if (__any_sync(0xffffffffu, rescale_o)) {
-        ok = role_wait(&bar_o_done, (j - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
+        if (!(ok = warp_wait(&bar_o_done, (j - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
+          const uint32_t col = C::kColO + (D / 2) * hf + 32 * c;
           uint32_t rr[32];
-          tmem_ld32(lane_base + C::kColO + 32 * c, rr);
+          tmem_ld32(lane_base + col, rr);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint32_t w[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(__uint_as_float(rr[i + k]) * factor);
-            tmem_st8(lane_base + C::kColO + 32 * c + i, w);
+            tmem_st8(lane_base + col + i, w);
           }
         }
-        {
+        if (hf == 0) {
           uint32_t rr[16];
           tmem_ld16(lane_base + C::kColL, rr);
           tmem_ld_wait();
@@ -302,17 +313,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
       }
 #pragma unroll
-      for (int c = 0; c < 32; c += 8) {
+      for (int c = 0; c < 16; c += 8) {
         uint32_t w[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) w[k] = pw[c + k];
-        tmem_st8(lane_base + C::kColP + 32 * bb + c, w);
+        tmem_st8(lane_base + C::kColP + 32 * bb + 16 * hf + c, w);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bar_p_full[bb]);
     }
     // ---------------------------------------------------------- epilogue
+    s_l[hf][r] = l16;
+    mbar_arrive(&bar_lsum);
+    if (ok) ok = role_wait(&bar_lsum, 0, abort_flag, a.err, kErrTimeoutEpilogue);
     if (ok) ok = role_wait(&bar_o_done, (n_kt - 1) & 1, abort_flag, a.err, kErrTimeoutEpilogue);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
@@ -327,27 +341,25 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       const int64_t t = doc_start + qpos;
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + (t * a.Hq + h) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
+        const int cb = (D / 2) * hf + 32 * c;
         uint32_t rr[32];
-        tmem_ld32(lane_base + C::kColO + 32 * c, rr);
+        tmem_ld32(lane_base + C::kColO + cb, rr);
         tmem_ld_wait();
         if (valid) {
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint4 v;
-            __nv_bfloat162 b0 = __floats2bfloat162_rn(__uint_as_float(rr[i]) * inv, __uint_as_float(rr[i + 1]) * inv);
-            __nv_bfloat162 b1 = __floats2bfloat162_rn(__uint_as_float(rr[i + 2]) * inv, __uint_as_float(rr[i + 3]) * inv);
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(rr[i + 4]) * inv, __uint_as_float(rr[i + 5]) * inv);
-            __nv_bfloat162 b3 = __floats2bfloat162_rn(__uint_as_float(rr[i + 6]) * inv, __uint_as_float(rr[i + 7]) * inv);
-            v.x = *reinterpret_cast<uint32_t*>(&b0);
-            v.y = *reinterpret_cast<uint32_t*>(&b1);
-            v.z = *reinterpret_cast<uint32_t*>(&b2);
-            v.w = *reinterpret_cast<uint32_t*>(&b3);
-            *reinterpret_cast<uint4*>(orow + 32 * c + i) = v;
+            v.x = pack_bf16x2(__uint_as_float(rr[i]) * inv, __uint_as_float(rr[i + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(rr[i + 2]) * inv, __uint_as_float(rr[i + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(rr[i + 4]) * inv, __uint_as_float(rr[i + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(rr[i + 6]) * inv, __uint_as_float(rr[i + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + cb + i) = v;
           }
         }
       }
-      if (valid) a.lse[static_cast<int64_t>(h) * a.T + t] = (m - 4.0f + log2f(l16)) * 0.69314718055994531f;
+      if (valid && hf == 0)
+        a.lse[static_cast<int64_t>(h) * a.T + t] = (m - 4.0f + log2f(s_l[0][r] + s_l[1][r])) * 0.69314718055994531f;
     }
   }
   tc_fence_before();

@@ -73,8 +73,8 @@ struct BwdArgs {
   const uint8_t* qt_sf;  // Q TOK
   const uint8_t* kt_sf;  // K TOK
   const uint8_t* gt_sf;  // G TOK
-  const float* lse;      // [Hq, T]
-  const float* dvec;     // D [Hq, T]
+  const float* lpad;     // LSE * log2(e), tile-padded [Hq, NT, 128]; +inf on rows past a document's end
+  const float* dpad;     // D, tile-padded [Hq, NT, 128]; 0 on rows past a document's end
   float* dq_acc32;       // [T, Hq, d] (FP32 mode)
   uint16_t* dq_acc16;    // [T, Hq, d] fp16 bits (FP16 x 2^9 mode)
   void* dk;              // bf16 [T, Hkv, d]
@@ -92,9 +92,11 @@ struct PrepArgs {
   const int32_t* cu_seqlens;
   int num_docs;
   int64_t ntiles;
-  const void* o;  // bf16 [T, Hq, d]
-  float* dvec;    // [Hq, T]
-  void* dq_acc;   // zeroed here
+  const void* o;     // bf16 [T, Hq, d]
+  const float* lse;  // [Hq, T], the forward's LSE
+  float* dpad;       // D, tile-padded [Hq, NT, 128]
+  float* lpad;       // LSE * log2(e), tile-padded [Hq, NT, 128]
+  void* dq_acc;      // zeroed here
   size_t dq_acc_bytes;
 };
 

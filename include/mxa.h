@@ -185,8 +185,9 @@ typedef struct {
   mxa_dq_mode dq_mode;
 } mxa_bwd_params;
 
-/* Workspace bytes mxa_bwd needs: D [Hq, T] fp32, plus (FP16_X512 mode) the
- * fp16 dQ accumulator [T, Hq, d], each rounded up to 256 bytes. */
+/* Workspace bytes mxa_bwd needs: D and LSE * log2(e), fp32, each padded to
+ * whole 128-token tiles per document ([Hq, ntiles, 128]), plus (FP16_X512
+ * mode) the fp16 dQ accumulator [T, Hq, d] rounded up to 256 bytes. */
 size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p);
 
 /* Backward.  workspace: device buffer of at least mxa_bwd_workspace_bytes()
