@@ -89,8 +89,9 @@ _lib = None
 
 EXPORTS = [
     "mxa_abi_version", "mxa_status_str", "mxa_scale_tiles", "mxa_scale_tiles_bound", "mxa_scale_bytes",
-    "mxa_quantize", "mxa_fwd", "mxa_bwd_workspace_bytes", "mxa_bwd", "mxa_get_error",
+    "mxa_quantize", "mxa_fwd", "mxa_bwd_workspace_bytes", "mxa_bwd", "mxa_bwd_noalloc", "mxa_get_error",
 ]
+MXA_BWD_NOALLOC_MAX_WORKSPACE = 32 * 1024 * 1024
 
 
 def lib():
@@ -120,6 +121,8 @@ def lib():
         L.mxa_bwd_workspace_bytes.argtypes = [ctypes.POINTER(c_bwd_params)]
         L.mxa_bwd.restype = i32
         L.mxa_bwd.argtypes = [ctypes.POINTER(c_bwd_params), P, ctypes.c_size_t, P]
+        L.mxa_bwd_noalloc.restype = i32
+        L.mxa_bwd_noalloc.argtypes = [ctypes.POINTER(c_bwd_params), P]
         L.mxa_get_error.restype = i32
         L.mxa_get_error.argtypes = [P]
         _lib = L
@@ -187,6 +190,12 @@ def mxa_bwd_workspace_bytes(params: c_bwd_params) -> int:
 
 def mxa_bwd(params: c_bwd_params, workspace, ws_bytes: int, stream=None) -> int:
     return lib().mxa_bwd(ctypes.byref(params), _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def mxa_bwd_noalloc(params: c_bwd_params, stream=None) -> int:
+    """Backward with the library-owned scratch array as workspace (for callers
+    that cannot allocate device memory); see include/mxa.h."""
+    return lib().mxa_bwd_noalloc(ctypes.byref(params), _stream(stream))
 
 
 def mxa_get_error(stream=None) -> int:

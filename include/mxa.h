@@ -196,6 +196,32 @@ size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p);
  * MXA_ERR_WORKSPACE, MXA_ERR_CUDA. */
 mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* Size of the library-owned scratch array that mxa_bwd_noalloc uses in place
+ * of a caller workspace: 32 MiB on every GPU that loads the library. */
+#define MXA_BWD_NOALLOC_MAX_WORKSPACE (32u * 1024u * 1024u)
+
+/* Backward without a caller workspace.  The pages have no counterpart to this
+ * entry point; it exists for callers that cannot allocate device memory --
+ * for instance code running under a framework whose caching allocator owns
+ * all device memory and offers no side buffers, or a plugin host that gives
+ * the library a fixed memory budget -- and therefore cannot provide
+ * mxa_bwd's workspace.
+ * Same arguments, results and status codes as mxa_bwd, computed the same way;
+ * the workspace is a file-scope device array of MXA_BWD_NOALLOC_MAX_WORKSPACE
+ * bytes that the library owns (held on every GPU that loads the library until
+ * the process exits).  Calls whose mxa_bwd_workspace_bytes() exceeds it are
+ * rejected with MXA_ERR_WORKSPACE before any work; FP32-mode calls need
+ * 2 * Hq * ntiles * 512 bytes (B8 H32 L4096: 8 MiB), FP16_X512 calls also need
+ * the fp16 dQ accumulator, so only small ones fit.
+ * The device address of the array is resolved on the first call made with a
+ * given device current (cudaGetSymbolAddress); make that first call before
+ * any stream capture.  The function allocates nothing.  Every call on a device
+ * shares the one array and it keeps the last call's contents (each call
+ * rewrites what it reads); calls that overlap on the GPU -- on different
+ * streams, or from several threads -- race on it and must be serialized by
+ * the caller. */
+mxa_status mxa_bwd_noalloc(const mxa_bwd_params* p, cudaStream_t stream);
+
 /* Synchronize `stream`, then report and clear the device error word of the
  * current device: MXA_OK, MXA_ERR_TIMEOUT (a kernel gave up waiting) or
  * MXA_ERR_CUDA. */
