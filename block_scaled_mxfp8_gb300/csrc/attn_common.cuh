@@ -83,3 +83,27 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 }  // namespace mxa
+
+namespace mxa {
+
+// Quantize one 32 x 32 dS block held as 32 values per lane across a warp
+// (lane = row): block max-abs by a warp reduction in this register layout (no
+// transpose), exponent e = ceil(log2(amax / 448)) shifted down by `shift` when
+// the values carry a 2^shift boost and floored at the UE8M0 minimum, E4M3
+// codes of x * 2^-(e + shift) into w.  Returns the UE8M0 byte of e.
+__device__ __forceinline__ uint32_t quant_ds_block32(const float (&x)[32], int shift, uint32_t (&w)[8]) {
+  float am = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(x[i]));
+  am = warp_max_abs(am);
+  // an all-zero block keeps the unit scale whatever its boost
+  int e = am == 0.0f ? 0 : mx_exponent_bits(__float_as_uint(am)) - shift;
+  if (e < -127) e = -127;
+  const float sc = exp2i_neg(e + shift);
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    w[k] = pack_e4m3x4(x[4 * k] * sc, x[4 * k + 1] * sc, x[4 * k + 2] * sc, x[4 * k + 3] * sc);
+  return static_cast<uint32_t>(e + 127);
+}
+
+}  // namespace mxa

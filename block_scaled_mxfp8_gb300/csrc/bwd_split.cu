@@ -64,10 +64,11 @@ struct DqCfg {
   static constexpr uint32_t kSwz = D == 128 ? kSwz128 : kSwz64;
   static constexpr uint32_t kSBO = 8 * D;
   static constexpr int kKSteps = D / 32;
-  // TMEM: X holds S then dP; dQ accumulator; dS codes
-  static constexpr uint32_t kColX = 0, kColDQ = 128, kColDS = 256;
-  static constexpr uint32_t kSfQ = 288, kSfG = 292, kSfK = 296 /*+4s*/, kSfV = 304 /*+4s*/, kSfDS0 = 312,
-                            kSfDS1 = 316, kSfKt = 320 /*+4s*/;
+  // TMEM: S and dP side by side (both MMAs issue back to back), dQ
+  // accumulator, dS codes, scale atoms
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384;
+  static constexpr uint32_t kSfQ = 416, kSfG = 420, kSfK = 424 /*+4s*/, kSfV = 432 /*+4s*/, kSfDS0 = 440,
+                            kSfDS1 = 444, kSfKt = 448 /*+4s*/;
   static constexpr int kOffQ = 0;
   static constexpr int kOffG = kOffQ + kTileBytes;
   static constexpr int kOffStage = kOffG + kTileBytes;  // per stage: K, V, Kt
@@ -101,24 +102,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   }
 }
 
-// Quantize one 32 x 32 dS block held as 32 values per thread across the warp:
-// block max-abs by a warp reduction, exponent e (shifted by `shift` when the
-// values carry a 2^shift boost, floored at the UE8M0 minimum), E4M3 codes
-// into w.  Returns the scale byte of the unboosted block.
-__device__ __forceinline__ uint32_t quant_ds_block(const float (&x)[32], int shift, uint32_t (&w)[8]) {
-  float am = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(x[i]));
-  am = warp_max_abs(am);
-  int e = mx_exponent_bits(__float_as_uint(am)) - shift;
-  if (e < -127) e = -127;
-  const float sc = exp2i_neg(e + shift);
-#pragma unroll
-  for (int k = 0; k < 8; ++k)
-    w[k] = pack_e4m3x4(x[4 * k] * sc, x[4 * k + 1] * sc, x[4 * k + 2] * sc, x[4 * k + 3] * sc);
-  return static_cast<uint32_t>(e + 127);
-}
-
 }  // namespace
 
 // ========================================================================= dK, dV
@@ -130,7 +113,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   __shared__ uint64_t bar_kv, bar_tile_full[C::kStages], bar_tile_empty[C::kStages], bar_s_full, bar_x_free,
-      bar_dp_full, bar_x_free2, bar_p_ready, bar_pds_free, bar_final, bar_drain;
+      bar_dp_full, bar_x_free2, bar_p_ready, bar_ds_ready, bar_pv_free, bar_dk_free, bar_final, bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int64_t s_slot;
@@ -158,7 +141,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     mbar_init(&bar_dp_full, 1);
     mbar_init(&bar_x_free2, kSoftmaxThreads);
     mbar_init(&bar_p_ready, kSoftmaxThreads);
-    mbar_init(&bar_pds_free, 1);
+    mbar_init(&bar_ds_ready, kSoftmaxThreads);
+    mbar_init(&bar_pv_free, 1);
+    mbar_init(&bar_dk_free, 1);
     mbar_init(&bar_final, 1);
     mbar_init(&bar_drain, 1);
     s_abort = 0;
@@ -238,6 +223,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         mma_commit(&bar_s_full);
         return true;
       };
+      // Pipe order per unit u: dP^T_u, dV_u, S^T_{u+1}, dK_u.  X is written
+      // only by S^T and dP^T; between two writes of X the pipe always holds
+      // an MMA that does not touch X (dV_u, dK_u), which covers the softmax
+      // warps' read of X.
       if (ok) ok = issue_s(0);
       for (int u = 0; ok && u < n_work; ++u) {
         const int s = u % C::kStages;
@@ -252,27 +241,31 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
                       make_sdesc(st + C::kTileBytes + 32 * kk, 16, C::kSBO, C::kSwz),
                       make_idesc_mxf8(128, 128, 0, 0, kk, kk), tmem + C::kSfV, tmem + C::kSfG + 4 * s, kk > 0);
         mma_commit(&bar_dp_full);
-        // next S^T as soon as dP^T has been read (overlaps the dS work)
-        if (!(ok = role_wait(&bar_x_free2, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
-        if (u + 1 < n_work && !(ok = issue_s(u + 1))) break;
-        // dV += P^T G, dK += dS^T Q
+        // dV += P^T G (P^T codes written while dP^T ran)
         if (!(ok = role_wait(&bar_p_ready, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
         tc_fence_after();
         tmem_cp_atom(tmem + C::kSfGt + 4 * s, sSf + (2 + 4 * s + 3) * kAtomBytes);
-        tmem_cp_atom(tmem + C::kSfQt + 4 * s, sSf + (2 + 4 * s + 2) * kAtomBytes);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_mxf8_ts(tmem + C::kColDV, tmem + C::kColP + 8 * kk,
                       make_sdesc(st + 3 * C::kTileBytes + kk * 32 * D, 16, C::kSBO, C::kSwz),
                       make_idesc_mxf8(128, D, 0, 1, kk, kk), tmem + C::kSfP, tmem + C::kSfGt + 4 * s,
                       (u > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar_pv_free);
+        // next S^T as soon as dP^T has been read (runs while dS is formed)
+        if (!(ok = role_wait(&bar_x_free2, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        if (u + 1 < n_work && !(ok = issue_s(u + 1))) break;
+        // dK += dS^T Q
+        if (!(ok = role_wait(&bar_ds_ready, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        tc_fence_after();
+        tmem_cp_atom(tmem + C::kSfQt + 4 * s, sSf + (2 + 4 * s + 2) * kAtomBytes);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_mxf8_ts(tmem + C::kColDK, tmem + C::kColDS + 8 * kk,
                       make_sdesc(st + 2 * C::kTileBytes + kk * 32 * D, 16, C::kSBO, C::kSwz),
                       make_idesc_mxf8(128, D, 0, 1, kk & 1, kk), tmem + (kk < 2 ? C::kSfDS0 : C::kSfDS1),
                       tmem + C::kSfQt + 4 * s, (u > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar_pds_free);
+        mma_commit(&bar_dk_free);
         mma_commit(&bar_tile_empty[s]);
       }
       mma_commit(&bar_final);
@@ -319,8 +312,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) p[c] = (64 * hf + c >= j) ? p[c] : 0.0f;
       }
-      // the previous tile's dV / dK MMAs must be done with the codes and scales
-      if (u > 0 && !(ok = warp_wait(&bar_pds_free, (u - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      // the previous unit's dV MMA must be done with the P^T codes
+      if (u > 0 && !(ok = warp_wait(&bar_pv_free, (u - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < 16; c += 8) {
@@ -330,36 +323,49 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
           w[k] = pack_e4m3x4(p[4 * (c + k)], p[4 * (c + k) + 1], p[4 * (c + k) + 2], p[4 * (c + k) + 3]);
         tmem_st8(lane_base + C::kColP + 16 * hf + c, w);
       }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar_p_ready);
       if (!(ok = warp_wait(&bar_dp_full, u & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
-      uint32_t ebytes = 0;
+      // dS^T = P^T (dP^T - D), in place; X is released once both chunks are in
+      // registers
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t rr[32];
         tmem_ld32(lane_base + C::kColX + 64 * hf + 32 * cc, rr);
         tmem_ld_wait();
-        float x[32];
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
           const float4 d4 = *reinterpret_cast<const float4*>(drow + 32 * cc + i);
-          x[i] = p[32 * cc + i] * (__uint_as_float(rr[i]) - d4.x);
-          x[i + 1] = p[32 * cc + i + 1] * (__uint_as_float(rr[i + 1]) - d4.y);
-          x[i + 2] = p[32 * cc + i + 2] * (__uint_as_float(rr[i + 2]) - d4.z);
-          x[i + 3] = p[32 * cc + i + 3] * (__uint_as_float(rr[i + 3]) - d4.w);
+          p[32 * cc + i] *= __uint_as_float(rr[i]) - d4.x;
+          p[32 * cc + i + 1] *= __uint_as_float(rr[i + 1]) - d4.y;
+          p[32 * cc + i + 2] *= __uint_as_float(rr[i + 2]) - d4.z;
+          p[32 * cc + i + 3] *= __uint_as_float(rr[i + 3]) - d4.w;
         }
-        uint32_t w[8];
-        ebytes |= quant_ds_block(x, 8, w) << (8 * cc);  // 32 key rows x 32 queries
-        tmem_st8(lane_base + C::kColDS + 16 * hf + 8 * cc, w);
       }
       tc_fence_before();
       mbar_arrive(&bar_x_free2);
+      // the previous unit's dK MMA must be done with the dS^T codes and scales
+      if (u > 0 && !(ok = warp_wait(&bar_dk_free, (u - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      tc_fence_after();
+      uint32_t ebytes = 0;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        float x[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = p[32 * cc + i];
+        uint32_t w[8];
+        ebytes |= quant_ds_block32(x, 8, w) << (8 * cc);  // 32 key rows x 32 queries
+        tmem_st8(lane_base + C::kColDS + 16 * hf + 8 * cc, w);
+      }
       // dK's A operand is dS^T (rows = keys, groups = 32-query blocks); row r's
       // scales sit in lane r, column base + r / 32.  Half hf owns query
       // blocks 2 hf, 2 hf + 1 (bytes 0, 1 of its own scale columns).
       tmem_st1(lane_base + (hf ? C::kSfDS1 : C::kSfDS0) + quad, ebytes | 0x7F7F0000u);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bar_p_ready);
+      mbar_arrive(&bar_ds_ready);
     }
     // ---------------------------------------------------------- dK, dV out
     if (ok) ok = role_wait(&bar_final, 0, abort_flag, a.err, kErrTimeoutEpilogue);
@@ -397,8 +403,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  __shared__ uint64_t bar_q, bar_kv_full[C::kStages], bar_kv_empty[C::kStages], bar_s_full, bar_x_free,
-      bar_dp_full, bar_x_free2, bar_ds_ready, bar_ds_free, bar_final, bar_drain;
+  __shared__ uint64_t bar_q, bar_kv_full[C::kStages], bar_kv_empty[C::kStages], bar_sdp_full, bar_x_free,
+      bar_ds_ready, bar_ds_free, bar_final, bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int64_t s_slot;
@@ -420,10 +426,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       mbar_init(&bar_kv_full[s], 1);
       mbar_init(&bar_kv_empty[s], 1);
     }
-    mbar_init(&bar_s_full, 1);
+    mbar_init(&bar_sdp_full, 1);
     mbar_init(&bar_x_free, kSoftmaxThreads);
-    mbar_init(&bar_dp_full, 1);
-    mbar_init(&bar_x_free2, kSoftmaxThreads);
     mbar_init(&bar_ds_ready, kSoftmaxThreads);
     mbar_init(&bar_ds_free, 1);
     mbar_init(&bar_final, 1);
@@ -485,35 +489,33 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         tmem_cp_atom(tmem + C::kSfQ, sSf + 0 * kAtomBytes);
         tmem_cp_atom(tmem + C::kSfG, sSf + 1 * kAtomBytes);
       }
-      auto issue_s = [&](int j) -> bool {  // S = Q K^T into X
+      auto issue_sdp = [&](int j) -> bool {  // S = Q K^T and dP = G V^T, back to back
         const int s = j % C::kStages;
         if (!role_wait(&bar_kv_full[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
+        // S and dP of the previous key tile must have been read out of TMEM
+        if (j >= 1 && !role_wait(&bar_x_free, (j - 1) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
         tc_fence_after();
         const uint32_t st = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
         tmem_cp_atom(tmem + C::kSfK + 4 * s, sSf + (2 + 3 * s + 0) * kAtomBytes);
+        tmem_cp_atom(tmem + C::kSfV + 4 * s, sSf + (2 + 3 * s + 1) * kAtomBytes);
 #pragma unroll
         for (int kk = 0; kk < C::kKSteps; ++kk)
-          mma_mxf8_ss(tmem + C::kColX, make_sdesc(qa + 32 * kk, 16, C::kSBO, C::kSwz),
+          mma_mxf8_ss(tmem + C::kColS, make_sdesc(qa + 32 * kk, 16, C::kSBO, C::kSwz),
                       make_sdesc(st + 32 * kk, 16, C::kSBO, C::kSwz), make_idesc_mxf8(128, 128, 0, 0, kk, kk),
                       tmem + C::kSfQ, tmem + C::kSfK + 4 * s, kk > 0);
-        mma_commit(&bar_s_full);
+#pragma unroll
+        for (int kk = 0; kk < C::kKSteps; ++kk)
+          mma_mxf8_ss(tmem + C::kColDP, make_sdesc(ga + 32 * kk, 16, C::kSBO, C::kSwz),
+                      make_sdesc(st + C::kTileBytes + 32 * kk, 16, C::kSBO, C::kSwz),
+                      make_idesc_mxf8(128, 128, 0, 0, kk, kk), tmem + C::kSfG, tmem + C::kSfV + 4 * s, kk > 0);
+        mma_commit(&bar_sdp_full);
         return true;
       };
-      if (ok) ok = issue_s(0);
+      if (ok) ok = issue_sdp(0);
       for (int j = 0; ok && j < n_kt; ++j) {
         const int s = j % C::kStages;
         const uint32_t st = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
-        if (!(ok = role_wait(&bar_x_free, j & 1, abort_flag, a.err, kErrTimeoutMma))) break;
-        tc_fence_after();
-        tmem_cp_atom(tmem + C::kSfV + 4 * s, sSf + (2 + 3 * s + 1) * kAtomBytes);
-#pragma unroll
-        for (int kk = 0; kk < C::kKSteps; ++kk)  // dP = G V^T
-          mma_mxf8_ss(tmem + C::kColX, make_sdesc(ga + 32 * kk, 16, C::kSBO, C::kSwz),
-                      make_sdesc(st + C::kTileBytes + 32 * kk, 16, C::kSBO, C::kSwz),
-                      make_idesc_mxf8(128, 128, 0, 0, kk, kk), tmem + C::kSfG, tmem + C::kSfV + 4 * s, kk > 0);
-        mma_commit(&bar_dp_full);
-        if (!(ok = role_wait(&bar_x_free2, j & 1, abort_flag, a.err, kErrTimeoutMma))) break;
-        if (j + 1 < n_kt && !(ok = issue_s(j + 1))) break;
+        if (j + 1 < n_kt && !(ok = issue_sdp(j + 1))) break;  // overlaps the dS work of tile j
         if (!(ok = role_wait(&bar_ds_ready, j & 1, abort_flag, a.err, kErrTimeoutMma))) break;
         tc_fence_after();
         tmem_cp_atom(tmem + C::kSfKt + 4 * s, sSf + (2 + 3 * s + 2) * kAtomBytes);
@@ -544,12 +546,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     const float sl2 = a.scale_log2;
     bool ok = true;
     for (int j = 0; j < n_kt; ++j) {
-      if (!(ok = warp_wait(&bar_s_full, j & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      if (!(ok = warp_wait(&bar_sdp_full, j & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
       float p[64];
-      tmem_ld64(lane_base + C::kColX + 64 * hf, p);
-      tc_fence_before();
-      mbar_arrive(&bar_x_free);
+      tmem_ld64(lane_base + C::kColS + 64 * hf, p);
 #pragma unroll
       for (int c = 0; c < 64; ++c) p[c] = ex2_approx(fmaf(p[c], sl2, nl));
       // keys past the document end (last tile) or after the query (diagonal tile)
@@ -560,25 +560,30 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) p[c] = (64 * hf + c < lim) ? p[c] : 0.0f;
       }
-      if (!(ok = warp_wait(&bar_dp_full, j & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      // dS = P (dP - D), in place
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t rr[32];
+        tmem_ld32(lane_base + C::kColDP + 64 * hf + 32 * cc, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) p[32 * cc + i] *= (__uint_as_float(rr[i]) - dd);
+      }
+      tc_fence_before();
+      mbar_arrive(&bar_x_free);  // S and dP read: the next tile's S, dP may start
       // the previous dQ MMA must be done with the dS codes and scales
       if (j > 0 && !(ok = warp_wait(&bar_ds_free, (j - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
       uint32_t ebytes = 0;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        uint32_t rr[32];
-        tmem_ld32(lane_base + C::kColX + 64 * hf + 32 * cc, rr);
-        tmem_ld_wait();
         float x[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = p[32 * cc + i] * (__uint_as_float(rr[i]) - dd);
+        for (int i = 0; i < 32; ++i) x[i] = p[32 * cc + i];
         uint32_t w[8];
-        ebytes |= quant_ds_block(x, 0, w) << (8 * cc);  // 32 query rows x 32 keys
+        ebytes |= quant_ds_block32(x, 0, w) << (8 * cc);  // 32 query rows x 32 keys
         tmem_st8(lane_base + C::kColDS + 16 * hf + 8 * cc, w);
       }
-      tc_fence_before();
-      mbar_arrive(&bar_x_free2);
       // dQ's A operand is dS (rows = queries, groups = 32-key blocks): row r's
       // scales sit in lane r, column base + r / 32; half hf owns key blocks
       // 2 hf, 2 hf + 1.

@@ -1,29 +1,34 @@
 // fwd.cu -- MXFP8 block-scaled attention forward (tcgen05, TMEM, TMA).
 //
-// One CTA computes one 128-query tile of one (document, query head):
-//   S_j   = Q K_j^T         block-scaled MXFP8 MMA (kind::mxf8f6f4), K-major
-//                           operands, Q/K ROW-view scales in TMEM;
-//   P_j   = online softmax of alpha * S_j with a lazily updated row max
-//           (rescale only when the tile max exceeds the running max by more
-//           than tau = 4 in log2 units), quantized in registers as
-//           E4M3(2^4 * p) (FLAMIA notes sec. 5: 2^(c+tau) <= 448 with
-//           (c, tau) = (4, 4)), stored to TMEM;
-//   O    += P_j V_j          block-scaled MMA with A = P from TMEM (scale
-//                           2^-4), B = V MN-major with TOK-view scales;
-//   L    += P_j 1            the same quantized weights against a ones tile
-//                           (N = 16), so that O / L is the convex combination
-//                           of the V rows with exactly the weights used;
+// One CTA computes one 128-query tile of one (document, query head), walking
+// the visible keys 256 at a time:
+//   S_j  = Q K_j^T          block-scaled MXFP8 MMA (kind::mxf8f6f4), M = 128
+//                           queries, N = 256 keys (the tensor core's cadence
+//                           is ~one instruction per 128 clocks whatever N <=
+//                           256 is, so N = 256 halves the cost per key), Q/K
+//                           ROW-view scales in TMEM;
+//   P_j  = online softmax of alpha * S_j with a lazily updated row max
+//          (rescale only when the tile max exceeds the running max by more
+//          than tau = 4 in log2 units), quantized in registers as E4M3(2^4 p)
+//          (FLAMIA notes sec. 5: 2^(c+tau) <= 448 with (c, tau) = (4, 4)),
+//          stored to TMEM;
+//   [O | L] += P_j [V_j | 1]  one block-scaled MMA with A = P from TMEM
+//          (scale 2^-4) and B = V (MN-major, TOK-view scales) widened by 16
+//          columns of ones, so that L is the row sum of exactly the quantized
+//          weights used for O (the ones come from one shared 4 KB block that
+//          every K step reaches through the descriptor's leading byte offset);
 //   O = O / L -> bf16, LSE = m + ln l with l the fp32 sum of the unquantized
 //   weights (FLAMIA notes sec. 2, online softmax).
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM
 // owner, warps 4..11 = softmax / correction / epilogue (two warps per query
-// row quadrant, each taking half of the 128 key columns).
-// S is double buffered in TMEM so that S_{j+1} = Q K_{j+1}^T runs on the
-// tensor core while the softmax warps work on S_j.
+// row quadrant, each taking 128 of the 256 key columns; they exchange row
+// maxima through shared memory).  The next S MMA starts once the softmax
+// warps have read S out of TMEM; the P V MMA runs after P is stored.
 //
-// TMEM columns: S0 [0,128) S1 [128,256) O [256,256+D) L [384,400) Q-scale 400,
-// K-scale 404+4s, V-scale 416+4s, P-scale 428, ones-scale 432, P0 [448,480),
-// P1 [480,512).
+// TMEM columns: S [0,256), O [256,256+D) and L [256+D,256+D+16), Q-scale 400,
+// K-scale 404+8s (two atoms per 256 keys), V-scale atoms 420 and 428 each
+// followed by a column block of 1.0 for the ones rows, P-scale 436, P
+// [448,512).
 #include <cuda_bf16.h>
 
 #include "attn_common.cuh"
@@ -34,24 +39,50 @@ namespace {
 
 template <int D>
 struct FwdCfg {
-  static constexpr int kStages = 3;
-  static constexpr int kTileBytes = 128 * D;
+  static constexpr int kStages = 2;
+  static constexpr int kHalfBytes = 128 * D;          // one 128-key box of K or V
+  static constexpr int kKVBytes = 2 * kHalfBytes;     // 256 keys
   static constexpr uint32_t kSwz = D == 128 ? kSwz128 : kSwz64;
   static constexpr uint32_t kSBO = 8 * D;
-  static constexpr int kKSteps = D / 32;
-  static constexpr int kThreads = 384;  // 4 role warps + 8 softmax warps
-  static constexpr uint32_t kColS = 0, kColO = 256, kColL = 384, kColSfQ = 400, kColSfK = 404, kColSfV = 416,
-                            kColSfP = 428, kColSf1 = 432, kColP = 448;
+  static constexpr int kKSteps = D / 32;              // K steps of S = Q K^T
+  static constexpr int kKStepBytes = 32 * D;          // 32 keys of V (P V K step)
+  static constexpr int kThreads = 384;                // 4 role warps + 8 softmax warps
+  static constexpr uint32_t kColS = 0, kColO = 256, kColL = 256 + D, kColSfQ = 400, kColSfK = 404, kColSfVA = 420,
+                            kColOneA = 424, kColSfVB = 428, kColOneB = 432, kColSfP = 436, kColP = 448;
   // shared memory map (offsets from the 1024-aligned base)
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffSfQ = kOffV + kStages * kTileBytes;
-  static constexpr int kOffSfK = kOffSfQ + kAtomBytes;
-  static constexpr int kOffSfV = kOffSfK + kStages * kAtomBytes;
-  static constexpr int kOffOnes = (kOffSfV + kStages * kAtomBytes + 1023) / 1024 * 1024;  // 16 x 128 B of E4M3 1.0
-  static constexpr int kSmemBytes = kOffOnes + 16 * 128 + 1024;            // + alignment slack
+  static constexpr int kOffK = kOffQ + 128 * D;
+  static constexpr int kOffV = kOffK + kStages * kKVBytes;
+  static constexpr int kOffOnes = kOffV + kStages * kKVBytes;  // 32 rows x D bytes of E4M3 1.0
+  static constexpr int kOffSfQ = kOffOnes + 4096;
+  static constexpr int kOffSfK = kOffSfQ + kAtomBytes;         // 2 atoms per stage
+  static constexpr int kOffSfV = kOffSfK + kStages * 2 * kAtomBytes;
+  static constexpr int kSmemBytes = kOffSfV + kStages * 2 * kAtomBytes + 1024;  // + alignment slack
 };
+
+__device__ __forceinline__ float max64(const float (&v)[64]) {
+  float a = fmaxf(v[0], v[1]), b = fmaxf(v[2], v[3]), c = fmaxf(v[4], v[5]), d = fmaxf(v[6], v[7]);
+#pragma unroll
+  for (int i = 8; i < 64; i += 8) {
+    a = fmaxf(a, fmaxf(v[i], v[i + 1]));
+    b = fmaxf(b, fmaxf(v[i + 2], v[i + 3]));
+    c = fmaxf(c, fmaxf(v[i + 4], v[i + 5]));
+    d = fmaxf(d, fmaxf(v[i + 6], v[i + 7]));
+  }
+  return fmaxf(fmaxf(a, b), fmaxf(c, d));
+}
+
+__device__ __forceinline__ void ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t x0[32], x1[32];
+  tmem_ld32(taddr, x0);
+  tmem_ld32(taddr + 32, x1);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = __uint_as_float(x0[i]);
+    v[32 + i] = __uint_as_float(x1[i]);
+  }
+}
 
 }  // namespace
 
@@ -62,9 +93,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  __shared__ uint64_t bar_q, bar_kv_full[C::kStages], bar_kv_empty[C::kStages], bar_s_full[2], bar_s_empty[2],
-      bar_p_full[2], bar_o_done, bar_drain, bar_mx[2], bar_lsum;
-  __shared__ float s_mx[2][2][128];  // [tile parity][half][row] partial row maxima
+  __shared__ uint64_t bar_q, bar_kv_full[C::kStages], bar_kv_empty[C::kStages], bar_s_full, bar_s_empty, bar_p_full,
+      bar_o_done, bar_drain, bar_mx[2], bar_lsum;
+  __shared__ float s_mx[2][2][128];  // [iteration parity][half][row] partial row maxima
   __shared__ float s_l[2][128];      // [half][row] partial row sums
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -79,7 +110,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   // heaviest query tiles first when causal
   const int qt = a.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
   if (qt >= nq_tiles) return;
-  const int n_kt = a.causal ? qt + 1 : nq_tiles;
+  // visible keys [0, nkeys), walked 256 at a time
+  const int64_t nkeys = a.causal ? min(n, static_cast<int64_t>(qt + 1) * 128) : n;
+  const int n_it = static_cast<int>((nkeys + 255) / 256);
   const int64_t tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, C::kThreads, &s_slot);
 
   if (tid == 0) {
@@ -88,14 +121,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       mbar_init(&bar_kv_full[s], 1);
       mbar_init(&bar_kv_empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_s_full[i], 1);
-      mbar_init(&bar_s_empty[i], 256);
-      mbar_init(&bar_p_full[i], 256);
-      mbar_init(&bar_mx[i], 256);
-    }
+    mbar_init(&bar_s_full, 1);
+    mbar_init(&bar_s_empty, 256);
+    mbar_init(&bar_p_full, 256);
     mbar_init(&bar_o_done, 1);
     mbar_init(&bar_drain, 1);
+    mbar_init(&bar_mx[0], 256);
+    mbar_init(&bar_mx[1], 256);
     mbar_init(&bar_lsum, 256);
     s_abort = 0;
     fence_barrier_init();
@@ -104,7 +136,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     tmem_alloc(&s_tmem, 512);
     tmem_relinquish();
   }
-  for (int i = tid; i < 16 * 128 / 16; i += C::kThreads)
+  for (int i = tid; i < 4096 / 16; i += C::kThreads)
     reinterpret_cast<uint4*>(smem + C::kOffOnes)[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
   fence_proxy_async_smem();
   tc_fence_before();
@@ -113,33 +145,43 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   const uint32_t tmem = s_tmem;
   volatile int* abort_flag = &s_abort;
 
-  uint8_t* sQ = smem + C::kOffQ;
-  uint8_t* sSfQ = smem + C::kOffSfQ;
-
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&maps.q);
       tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.v);
-      const int64_t q0 = doc_start + static_cast<int64_t>(qt) * 128;
-      mbar_arrive_expect_tx(&bar_q, C::kTileBytes + kAtomBytes);
-      tma_load_3d(sQ, &maps.q, &bar_q, 0, h, static_cast<int>(q0));
-      bulk_load(sSfQ, a.q_sf + ((static_cast<int64_t>(h) * a.ntiles + tile_base + qt) * kAtomBytes), kAtomBytes,
-                &bar_q);
+      const int q0 = static_cast<int>(doc_start + static_cast<int64_t>(qt) * 128);
+      mbar_arrive_expect_tx(&bar_q, 128 * D + kAtomBytes);
+      tma_load_3d(smem + C::kOffQ, &maps.q, &bar_q, 0, h, q0);
+      bulk_load(smem + C::kOffSfQ, a.q_sf + ((static_cast<int64_t>(h) * a.ntiles + tile_base + qt) * kAtomBytes),
+                kAtomBytes, &bar_q);
       int issued = 0;
-      for (int j = 0; j < n_kt; ++j) {
+      for (int j = 0; j < n_it; ++j) {
         const int s = j % C::kStages;
         if (j >= C::kStages) {
           if (!role_wait(&bar_kv_empty[s], ((j / C::kStages) - 1) & 1, abort_flag, a.err, kErrTimeoutTma)) break;
         }
-        const int64_t k0 = doc_start + static_cast<int64_t>(j) * 128;
-        const int64_t atom = (static_cast<int64_t>(hk) * a.ntiles + tile_base + j) * kAtomBytes;
-        mbar_arrive_expect_tx(&bar_kv_full[s], 2 * C::kTileBytes + 2 * kAtomBytes);
-        tma_load_3d(smem + C::kOffK + s * C::kTileBytes, &maps.k, &bar_kv_full[s], 0, hk, static_cast<int>(k0));
-        tma_load_3d(smem + C::kOffV + s * C::kTileBytes, &maps.v, &bar_kv_full[s], 0, hk, static_cast<int>(k0));
-        bulk_load(smem + C::kOffSfK + s * kAtomBytes, a.k_sf + atom, kAtomBytes, &bar_kv_full[s]);
-        bulk_load(smem + C::kOffSfV + s * kAtomBytes, a.v_sf + atom, kAtomBytes, &bar_kv_full[s]);
+        const int t0 = 2 * j;  // first 128-key tile of this iteration
+        // the second half may lie past the document: reuse the first half's
+        // atoms then (its keys are masked; the scales just have to be finite)
+        const int t1 = (t0 + 1 < nq_tiles) ? t0 + 1 : t0;
+        const int k0 = static_cast<int>(doc_start + static_cast<int64_t>(t0) * 128);
+        const int64_t atom0 = (static_cast<int64_t>(hk) * a.ntiles + tile_base + t0) * kAtomBytes;
+        const int64_t atom1 = (static_cast<int64_t>(hk) * a.ntiles + tile_base + t1) * kAtomBytes;
+        uint8_t* sk = smem + C::kOffK + s * C::kKVBytes;
+        uint8_t* sv = smem + C::kOffV + s * C::kKVBytes;
+        uint8_t* sfk = smem + C::kOffSfK + s * 2 * kAtomBytes;
+        uint8_t* sfv = smem + C::kOffSfV + s * 2 * kAtomBytes;
+        mbar_arrive_expect_tx(&bar_kv_full[s], 2 * C::kKVBytes + 4 * kAtomBytes);
+        tma_load_3d(sk, &maps.k, &bar_kv_full[s], 0, hk, k0);
+        tma_load_3d(sk + C::kHalfBytes, &maps.k, &bar_kv_full[s], 0, hk, k0 + 128);
+        tma_load_3d(sv, &maps.v, &bar_kv_full[s], 0, hk, k0);
+        tma_load_3d(sv + C::kHalfBytes, &maps.v, &bar_kv_full[s], 0, hk, k0 + 128);
+        bulk_load(sfk, a.k_sf + atom0, kAtomBytes, &bar_kv_full[s]);
+        bulk_load(sfk + kAtomBytes, a.k_sf + atom1, kAtomBytes, &bar_kv_full[s]);
+        bulk_load(sfv, a.v_sf + atom0, kAtomBytes, &bar_kv_full[s]);
+        bulk_load(sfv + kAtomBytes, a.v_sf + atom1, kAtomBytes, &bar_kv_full[s]);
         issued = j + 1;
       }
       // drain: every load issued must have landed before the CTA exits
@@ -150,53 +192,45 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_s[4] = {make_idesc_mxf8(128, 128, 0, 0, 0, 0), make_idesc_mxf8(128, 128, 0, 0, 1, 1),
-                                   make_idesc_mxf8(128, 128, 0, 0, 2, 2), make_idesc_mxf8(128, 128, 0, 0, 3, 3)};
-      const uint32_t idesc_pv[4] = {make_idesc_mxf8(128, D, 0, 1, 0, 0), make_idesc_mxf8(128, D, 0, 1, 1, 1),
-                                    make_idesc_mxf8(128, D, 0, 1, 2, 2), make_idesc_mxf8(128, D, 0, 1, 3, 3)};
-      const uint32_t idesc_l[4] = {make_idesc_mxf8(128, 16, 0, 0, 0, 0), make_idesc_mxf8(128, 16, 0, 0, 1, 1),
-                                   make_idesc_mxf8(128, 16, 0, 0, 2, 2), make_idesc_mxf8(128, 16, 0, 0, 3, 3)};
+      const uint32_t qa = smem_u32(smem + C::kOffQ), onesa = smem_u32(smem + C::kOffOnes);
       bool ok = role_wait(&bar_q, 0, abort_flag, a.err, kErrTimeoutMma);
       if (ok) {
         tc_fence_after();
-        tmem_cp_atom(tmem + C::kColSfQ, sSfQ);
+        tmem_cp_atom(tmem + C::kColSfQ, smem + C::kOffSfQ);
       }
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % C::kStages, bb = j & 1;
+      auto issue_s = [&](int j) -> bool {  // S = Q K^T, 128 x 256
+        const int s = j % C::kStages;
         if (!role_wait(&bar_kv_full[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
-        if (j >= 2 && !role_wait(&bar_s_empty[bb], ((j >> 1) - 1) & 1, abort_flag, a.err, kErrTimeoutMma))
-          return false;
+        if (j >= 1 && !role_wait(&bar_s_empty, (j - 1) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
         tc_fence_after();
-        tmem_cp_atom(tmem + C::kColSfK + 4 * s, smem + C::kOffSfK + s * kAtomBytes);
-        const uint32_t qa = smem_u32(sQ), ka = smem_u32(smem + C::kOffK + s * C::kTileBytes);
+        uint8_t* sfk = smem + C::kOffSfK + s * 2 * kAtomBytes;
+        tmem_cp_atom(tmem + C::kColSfK + 8 * s, sfk);
+        tmem_cp_atom(tmem + C::kColSfK + 8 * s + 4, sfk + kAtomBytes);
+        const uint32_t ka = smem_u32(smem + C::kOffK + s * C::kKVBytes);
 #pragma unroll
-        for (int kk = 0; kk < C::kKSteps; ++kk) {
-          mma_mxf8_ss(tmem + C::kColS + 128 * bb, make_sdesc(qa + 32 * kk, 16, C::kSBO, C::kSwz),
-                      make_sdesc(ka + 32 * kk, 16, C::kSBO, C::kSwz), idesc_s[kk], tmem + C::kColSfQ,
-                      tmem + C::kColSfK + 4 * s, kk > 0);
-        }
-        mma_commit(&bar_s_full[bb]);
+        for (int kk = 0; kk < C::kKSteps; ++kk)
+          mma_mxf8_ss(tmem + C::kColS, make_sdesc(qa + 32 * kk, 16, C::kSBO, C::kSwz),
+                      make_sdesc(ka + 32 * kk, 16, C::kSBO, C::kSwz), make_idesc_mxf8(128, 256, 0, 0, kk, kk),
+                      tmem + C::kColSfQ, tmem + C::kColSfK + 8 * s, kk > 0);
+        mma_commit(&bar_s_full);
         return true;
       };
       if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < n_kt; ++j) {
-        if (j + 1 < n_kt && !issue_s(j + 1)) break;
-        const int s = j % C::kStages, bb = j & 1;
-        if (!role_wait(&bar_p_full[bb], (j >> 1) & 1, abort_flag, a.err, kErrTimeoutMma)) break;
+      for (int j = 0; ok && j < n_it; ++j) {
+        if (j + 1 < n_it && !issue_s(j + 1)) break;  // waits until S_j has been read out
+        const int s = j % C::kStages;
+        if (!role_wait(&bar_p_full, j & 1, abort_flag, a.err, kErrTimeoutMma)) break;
         tc_fence_after();
-        tmem_cp_atom(tmem + C::kColSfV + 4 * s, smem + C::kOffSfV + s * kAtomBytes);
-        const uint32_t va = smem_u32(smem + C::kOffV + s * C::kTileBytes);
+        uint8_t* sfv = smem + C::kOffSfV + s * 2 * kAtomBytes;
+        tmem_cp_atom(tmem + C::kColSfVA, sfv);
+        tmem_cp_atom(tmem + C::kColSfVB, sfv + kAtomBytes);
+        const uint32_t va = smem_u32(smem + C::kOffV + s * C::kKVBytes);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          mma_mxf8_ts(tmem + C::kColO, tmem + C::kColP + 32 * bb + 8 * kk,
-                      make_sdesc(va + kk * 32 * D, 16, C::kSBO, C::kSwz), idesc_pv[kk], tmem + C::kColSfP,
-                      tmem + C::kColSfV + 4 * s, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        const uint32_t onesa = smem_u32(smem + C::kOffOnes);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          mma_mxf8_ts(tmem + C::kColL, tmem + C::kColP + 32 * bb + 8 * kk, make_sdesc(onesa + 32 * kk, 16, 1024, kSwz128),
-                      idesc_l[kk], tmem + C::kColSfP, tmem + C::kColSf1, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk) {  // [O | L] += P [V | 1], 32 keys per step
+          const uint32_t vk = va + kk * C::kKStepBytes;
+          mma_mxf8_ts(tmem + C::kColO, tmem + C::kColP + 8 * kk, make_sdesc(vk, onesa - vk, C::kSBO, C::kSwz),
+                      make_idesc_mxf8(128, D + 16, 0, 1, kk & 3, kk & 3), tmem + C::kColSfP,
+                      tmem + (kk < 4 ? C::kColSfVA : C::kColSfVB), (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&bar_o_done);
         mma_commit(&bar_kv_empty[s]);
@@ -208,8 +242,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
     // Two warps per TMEM lane quadrant: warp half hf handles key columns
-    // [64 hf, 64 hf + 64) of its 32 rows; the halves exchange their row maxima
-    // through shared memory once per tile and keep separate partial sums.
+    // [128 hf, 128 hf + 128) of its 32 rows, in two passes of 64 columns
+    // (max, then exponentials); the halves exchange their row maxima through
+    // shared memory once per iteration and keep separate partial sums.
     const int quad = warp & 3;
     const int hf = (warp - 4) >> 2;
     const int r = quad * 32 + lane;
@@ -217,49 +252,45 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const int64_t qpos = static_cast<int64_t>(qt) * 128 + r;  // document-relative query index
     const float sl2 = a.scale_log2;
     if (hf == 0) {
-      // P scale 2^-4 and the ones tile's scale 1 in every cell of their columns
+      // 1.0 for the ones rows of both V atoms, 2^-4 for P
+      tmem_st4(lane_base + C::kColOneA, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      tmem_st4(lane_base + C::kColOneB, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
       tmem_st4(lane_base + C::kColSfP, 0x7B7B7B7Bu, 0x7B7B7B7Bu, 0x7B7B7B7Bu, 0x7B7B7B7Bu);
-      tmem_st4(lane_base + C::kColSf1, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
       tmem_st_wait();
     }
     float m = -INFINITY;  // running (lazy) max of the scaled scores, log2 units
     float l16 = 0.0f;     // this half's sum of 2^(s - m + 4)
     bool ok = true;
-    for (int j = 0; j < n_kt; ++j) {
-      const int bb = j & 1;
-      if (!(ok = warp_wait(&bar_s_full[bb], (j >> 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+    for (int j = 0; j < n_it; ++j) {
+      if (!(ok = warp_wait(&bar_s_full, j & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
-      float sv[64];
-      {
-        uint32_t x0[32], x1[32];
-        tmem_ld32(lane_base + C::kColS + 128 * bb + 64 * hf, x0);
-        tmem_ld32(lane_base + C::kColS + 128 * bb + 64 * hf + 32, x1);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          sv[i] = __uint_as_float(x0[i]);
-          sv[32 + i] = __uint_as_float(x1[i]);
+      // columns >= lim are masked (keys past the document end, or after the
+      // query on the causal diagonal); only the last iteration has any
+      int lim = 256;
+      if (j == n_it - 1) {
+        const int64_t rem = n - static_cast<int64_t>(j) * 256;
+        lim = rem < 256 ? static_cast<int>(rem) : 256;
+        if (a.causal) {
+          const int64_t c = qpos - static_cast<int64_t>(j) * 256 + 1;
+          if (c < lim) lim = static_cast<int>(c);
         }
       }
-      tc_fence_before();
-      mbar_arrive(&bar_s_empty[bb]);
-      if (j == n_kt - 1) {
-        // keys past the document end, or (causal diagonal) after the query
-        const int64_t rem = n - static_cast<int64_t>(j) * 128;
-        int lim = rem < 128 ? static_cast<int>(rem) : 128;
-        if (a.causal) lim = min(lim, r + 1);
-        if (lim < 128) {
+      const uint32_t scol = C::kColS + 128 * hf;
+      float mt = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 64; ++c) sv[c] = (64 * hf + c < lim) ? sv[c] : -INFINITY;
+      for (int ps = 0; ps < 2; ++ps) {
+        float sv[64];
+        ld64(lane_base + scol + 64 * ps, sv);
+        if (lim < 256) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) sv[c] = (128 * hf + 64 * ps + c < lim) ? sv[c] : -INFINITY;
         }
+        mt = fmaxf(mt, max64(sv));
       }
-      float mt = sv[0];
-#pragma unroll
-      for (int c = 1; c < 64; ++c) mt = fmaxf(mt, sv[c]);
-      s_mx[bb][hf][r] = mt;
-      mbar_arrive(&bar_mx[bb]);
-      if (!(ok = warp_wait(&bar_mx[bb], (j >> 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
-      mt = fmaxf(mt, s_mx[bb][hf ^ 1][r]);
+      s_mx[j & 1][hf][r] = mt;
+      mbar_arrive(&bar_mx[j & 1]);
+      if (!(ok = warp_wait(&bar_mx[j & 1], (j >> 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      mt = fmaxf(mt, s_mx[j & 1][hf ^ 1][r]);
       const float mts = mt * sl2;
       bool rescale_o = false;
       float factor = 1.0f;
@@ -270,24 +301,39 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         m = mts;
         rescale_o = true;
       }
+      // exponentials into registers; S is released after its second read, so
+      // the next S MMA does not wait for this tile's P V
       const float neg = 4.0f - m;
-      uint32_t pw[16];
       float lsum = 0.0f;
+      uint32_t pw[32];  // E4M3 codes of this half's 128 weights
 #pragma unroll
-      for (int c = 0; c < 64; c += 4) {
-        const float p0 = ex2_approx(fmaf(sv[c], sl2, neg));
-        const float p1 = ex2_approx(fmaf(sv[c + 1], sl2, neg));
-        const float p2 = ex2_approx(fmaf(sv[c + 2], sl2, neg));
-        const float p3 = ex2_approx(fmaf(sv[c + 3], sl2, neg));
-        lsum += (p0 + p1) + (p2 + p3);
-        pw[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
+      for (int ps = 0; ps < 2; ++ps) {
+        float sv[64];
+        ld64(lane_base + scol + 64 * ps, sv);
+        if (ps == 1) {  // S fully read: the next S MMA may overwrite it
+          tc_fence_before();
+          mbar_arrive(&bar_s_empty);
+        }
+        if (lim < 256) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) sv[c] = (128 * hf + 64 * ps + c < lim) ? sv[c] : -INFINITY;
+        }
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          const float p0 = ex2_approx(fmaf(sv[c], sl2, neg));
+          const float p1 = ex2_approx(fmaf(sv[c + 1], sl2, neg));
+          const float p2 = ex2_approx(fmaf(sv[c + 2], sl2, neg));
+          const float p3 = ex2_approx(fmaf(sv[c + 3], sl2, neg));
+          lsum += (p0 + p1) + (p2 + p3);
+          pw[16 * ps + (c >> 2)] = pack_e4m3x4(p0, p1, p2, p3);
+        }
       }
-      l16 = l16 * factor + lsum;
+      // the previous P V must be done before P is overwritten and O rescaled
+      if (j > 0 && !(ok = warp_wait(&bar_o_done, (j - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      tc_fence_after();
       // tcgen05.ld/st are warp-collective: the whole warp rescales its rows'
       // half of O when any of them needs it (factor 1 for the others).
       if (__any_sync(0xffffffffu, rescale_o)) {
-        if (!(ok = warp_wait(&bar_o_done, (j - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
-        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
           const uint32_t col = C::kColO + (D / 2) * hf + 32 * c;
@@ -313,21 +359,22 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
       }
 #pragma unroll
-      for (int c = 0; c < 16; c += 8) {
+      for (int q = 0; q < 4; ++q) {
         uint32_t w[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) w[k] = pw[c + k];
-        tmem_st8(lane_base + C::kColP + 32 * bb + 16 * hf + c, w);
+        for (int k = 0; k < 8; ++k) w[k] = pw[8 * q + k];
+        tmem_st8(lane_base + C::kColP + 32 * hf + 8 * q, w);
       }
+      l16 = l16 * factor + lsum;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bar_p_full[bb]);
+      mbar_arrive(&bar_p_full);
     }
     // ---------------------------------------------------------- epilogue
     s_l[hf][r] = l16;
     mbar_arrive(&bar_lsum);
     if (ok) ok = role_wait(&bar_lsum, 0, abort_flag, a.err, kErrTimeoutEpilogue);
-    if (ok) ok = role_wait(&bar_o_done, (n_kt - 1) & 1, abort_flag, a.err, kErrTimeoutEpilogue);
+    if (ok) ok = role_wait(&bar_o_done, (n_it - 1) & 1, abort_flag, a.err, kErrTimeoutEpilogue);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       float inv;

@@ -91,6 +91,8 @@ EXPORTS = [
     "mxa_abi_version", "mxa_status_str", "mxa_scale_tiles", "mxa_scale_tiles_bound", "mxa_scale_bytes",
     "mxa_quantize", "mxa_fwd", "mxa_bwd_workspace_bytes", "mxa_bwd", "mxa_bwd_noalloc", "mxa_get_error",
 ]
+# include/mxa_testing.h: the kernels' P and dS quantization run on caller data
+EXPORTS_TESTING = ["mxa_test_e4m3", "mxa_test_ds_blocks"]
 MXA_BWD_NOALLOC_MAX_WORKSPACE = 32 * 1024 * 1024
 
 
@@ -125,6 +127,10 @@ def lib():
         L.mxa_bwd_noalloc.argtypes = [ctypes.POINTER(c_bwd_params), P]
         L.mxa_get_error.restype = i32
         L.mxa_get_error.argtypes = [P]
+        L.mxa_test_e4m3.restype = i32
+        L.mxa_test_e4m3.argtypes = [P, i64, P, P]
+        L.mxa_test_ds_blocks.restype = i32
+        L.mxa_test_ds_blocks.argtypes = [P, i32, i32, P, P, P]
         _lib = L
     return _lib
 
@@ -196,6 +202,16 @@ def mxa_bwd_noalloc(params: c_bwd_params, stream=None) -> int:
     """Backward with the library-owned scratch array as workspace (for callers
     that cannot allocate device memory); see include/mxa.h."""
     return lib().mxa_bwd_noalloc(ctypes.byref(params), _stream(stream))
+
+
+def mxa_test_e4m3(x: torch.Tensor, codes: torch.Tensor, stream=None) -> int:
+    """include/mxa_testing.h: E4M3 codes of fp32 x through the kernels' packed conversion."""
+    return lib().mxa_test_e4m3(_ptr(x), x.numel(), _ptr(codes), _stream(stream))
+
+
+def mxa_test_ds_blocks(x: torch.Tensor, shift: int, codes: torch.Tensor, scales: torch.Tensor, stream=None) -> int:
+    """include/mxa_testing.h: the kernels' 32 x 32 dS block quantization of x [nblocks, 32, 32]."""
+    return lib().mxa_test_ds_blocks(_ptr(x), x.shape[0], shift, _ptr(codes), _ptr(scales), _stream(stream))
 
 
 def mxa_get_error(stream=None) -> int:

@@ -1,0 +1,48 @@
+/*
+ * mxa_testing.h -- test hooks of libmxa.so: run the device functions the
+ * attention kernels use to quantize P and dS on caller data, so that tests
+ * can check them bit for bit against an independent codec.  Not part of the
+ * attention API (include/mxa.h).
+ *
+ *   P quantization: E4M3 round-to-nearest-even with saturation to +-448
+ *   (FLAMIA notes sec. 5, the P cap 2^(c+tau) <= 448: larger values saturate
+ *   silently).
+ *   dS quantization: one UE8M0 scale per 32 x 32 block from the block
+ *   max-abs, e = ceil(log2(amax / 448)), taken with a warp-wide max over the
+ *   register layout the kernels hold (one warp = 32 rows of 32 values) (FA4
+ *   write-up, "Квантование dS без транспонирования").
+ */
+#ifndef MXA_TESTING_H
+#define MXA_TESTING_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#include "mxa.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* codes[i] = E4M3 code of x[i] (device pointers, n % 4 == 0, x 16-byte and
+ * codes 4-byte aligned), through the kernels' packed conversion.  The caller
+ * owns both buffers.  Status: MXA_OK, MXA_ERR_ARG, MXA_ERR_ALIGN,
+ * MXA_ERR_CUDA (launch failure; asynchronous faults surface at the next
+ * synchronization). */
+mxa_status mxa_test_e4m3(const float* x, int64_t n, uint8_t* codes, cudaStream_t stream);
+
+/* Quantize nblocks blocks of 32 x 32 fp32 values (row-major, device) with the
+ * kernels' dS block routine: codes [nblocks][32][32], scale bytes
+ * [nblocks].  `shift` is the power-of-two boost the values carry (0, or 8 as
+ * in the dK/dV kernel, whose dS inherits the 2^8 P boost); the returned
+ * scale is that of the unboosted block.  codes must be 4-byte aligned; the
+ * caller owns all buffers.  Status: MXA_OK, MXA_ERR_ARG (shift outside
+ * [0, 16], negative count, null pointer), MXA_ERR_ALIGN, MXA_ERR_CUDA. */
+mxa_status mxa_test_ds_blocks(const float* x, int nblocks, int shift, uint8_t* codes, uint8_t* scales,
+                              cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MXA_TESTING_H */

@@ -19,8 +19,8 @@ def lib():
     return mxa.lib()
 
 
-def declared_functions():
-    src = open(os.path.join(ROOT, "include", "mxa.h")).read()
+def declared_functions(header="mxa.h"):
+    src = open(os.path.join(ROOT, "include", header)).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(mxa_[a-z_0-9]+)\s*\(", src)))
 
@@ -32,6 +32,13 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), n
     assert set(names) <= set(mxa.EXPORTS) | set(names)
     assert mxa.mxa_abi_version() == 1
+
+
+def test_exports_testing_hooks(lib):
+    names = [n for n in declared_functions("mxa_testing.h") if n.startswith("mxa_test_")]
+    assert names == sorted(mxa.EXPORTS_TESTING)
+    for n in names:
+        assert hasattr(lib, n), n
 
 
 def test_struct_layouts_match_header():
