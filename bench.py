@@ -74,7 +74,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -171,6 +171,10 @@ def run_gpu(args):
     mbuild.build()
 
     w = inp.workload(args.workload, causal=args.causal)
+    if args.batch:  # smaller batch of the same per-document shape (profiler captures)
+        if w.lengths is not None:
+            raise SystemExit("--batch applies to batched workloads only")
+        w.B = args.batch
     B, L, Hq, Hkv, d = w.B, w.L, w.Hq, w.Hkv, w.d
     T = w.T
     t = inp.tensors(w)
@@ -378,6 +382,7 @@ def main():
     ap.add_argument("--causal", action="store_true")
     ap.add_argument("--dq-mode", type=int, default=0, help="0 = fp32 dQ accumulation, 1 = fp16 x 2^9")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling only)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

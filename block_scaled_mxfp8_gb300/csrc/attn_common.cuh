@@ -47,10 +47,22 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 
 // One 512-byte scale atom (128 rows x 4 groups) from shared memory into 4
 // TMEM columns, replicated into the four 32-lane quadrants.
-__device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, const void* smem_atom) {
-  const uint64_t desc = make_sdesc(smem_u32(smem_atom), 512, 128, kSwzNone);
+__device__ __forceinline__ uint64_t atom_desc(const void* smem_atom) {
+  return make_sdesc(smem_u32(smem_atom), 512, 128, kSwzNone);
+}
+__device__ __forceinline__ void tmem_cp_desc(uint32_t taddr, uint64_t desc) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
+__device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, const void* smem_atom) {
+  tmem_cp_desc(taddr, atom_desc(smem_atom));
+}
+
+// A shared-memory descriptor advanced by `bytes` (a multiple of 16): only the
+// start-address field (bits 0-13, in 16-byte units) changes, and the kernels
+// keep every operand below 256 KB so the field never carries.  The MMA
+// issuers build their descriptors once and step them with this, keeping the
+// single issuing thread's work per MMA to a few integer adds.
+__device__ __forceinline__ uint64_t sdesc_adv(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
 // First scale tile of document b: sum over earlier documents of ceil(n / 128).
 // Called by every thread of the CTA.

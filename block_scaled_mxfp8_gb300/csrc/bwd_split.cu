@@ -18,12 +18,13 @@
 // forwards; these two kernels execute 3.5).  The 32 x 32 blocks are the same
 // in both kernels; each quantizes its own fp32 dS.
 //
-// Warps: 0 = TMA producer, 1 = MMA issuer, 2 = TMEM owner, 4..11 = softmax.
-// Two softmax warps share each TMEM lane quadrant and split the tile's 128
-// columns into halves of 64 (two 32 x 32 dS blocks each), so every SM
-// sub-partition has two softmax warps to interleave.  The halves write their
-// dS block exponents into separate scale-factor columns; the gradient MMA
-// reads K steps 0-1 from the first and 2-3 from the second.
+// Warps: 0 = TMA producer, 1 = TMEM owner and MMA issuer, 2..17 = softmax.
+// Four softmax warps share each TMEM lane quadrant and split the tile's 128
+// columns into quarters of 32, so each warp owns exactly one 32 x 32 dS block
+// per tile (its block max is a warp reduction) and every SM sub-partition has
+// four softmax warps to interleave.  Quarter p writes its block exponent into
+// its own scale-factor column block, which the gradient MMA reads for K step
+// p.
 // LSE (times log2 e; +inf past a document's end) and D come tile-padded from
 // the prep kernel and are bulk-loaded with the tiles.
 #include <cuda_bf16.h>
@@ -34,71 +35,68 @@ namespace mxa {
 
 namespace {
 
-constexpr int kSplitThreads = 384;
-constexpr int kSoftmaxThreads = 256;
+constexpr int kSplitThreads = 576;
+constexpr int kSoftmaxThreads = 512;
 
 template <int D>
 struct DkdvCfg {
-  static constexpr int kStages = 2;
+  // ring A (Q, G tiles, LSE row) feeds S^T and dP^T and is released after
+  // dP^T; ring B (Qt, Gt tiles, D row) feeds dV and dK and is released after
+  // dK, so the next units' Q and G load while the gradient MMAs still run
+  static constexpr int kStagesA = 3, kStagesB = 2;
   static constexpr int kTileBytes = 128 * D;
   static constexpr uint32_t kSwz = D == 128 ? kSwz128 : kSwz64;
   static constexpr uint32_t kSBO = 8 * D;
   static constexpr int kKSteps = D / 32;
-  // TMEM: X holds S^T then dP^T; dV, dK accumulators; P^T and dS^T codes
+  // TMEM: X holds S^T then dP^T; dV, dK accumulators; P^T and dS^T codes;
+  // scale slots indexed by unit parity (+4 (u & 1))
   static constexpr uint32_t kColX = 0, kColDV = 128, kColDK = 256, kColP = 384, kColDS = 416;
-  static constexpr uint32_t kSfK = 448, kSfQ = 452 /*+4s*/, kSfV = 460, kSfG = 464 /*+4s*/, kSfP = 472,
-                            kSfGt = 476 /*+4s*/, kSfDS0 = 484, kSfDS1 = 488, kSfQt = 492 /*+4s*/;
-  // shared memory: K, V, then per stage Q, G, Qt, Gt tiles + LSE + D rows
+  static constexpr uint32_t kSfK = 448, kSfQ = 452 /*+4t*/, kSfV = 460, kSfG = 464 /*+4t*/, kSfP = 472,
+                            kSfGt = 476 /*+4t*/, kSfQt = 484 /*+4t*/, kSfDS = 492 /*+4 per query block*/;
+  // shared memory: K, V, ring A stages (Q, G), ring B stages (Qt, Gt), the
+  // LSE and D rows of the stages, then the scale atoms
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffStage = kOffV + kTileBytes;
-  static constexpr int kStageBytes = 4 * kTileBytes + 2 * 512;
-  static constexpr int kOffSf = kOffStage + kStages * kStageBytes;  // K, V, then 4 per stage
-  static constexpr int kSmemBytes = kOffSf + (2 + 4 * kStages) * kAtomBytes + 1024;
+  static constexpr int kOffA = kOffV + kTileBytes;
+  static constexpr int kOffB = kOffA + kStagesA * 2 * kTileBytes;
+  static constexpr int kOffRowsA = kOffB + kStagesB * 2 * kTileBytes;  // LSE rows, 512 B each
+  static constexpr int kOffRowsB = kOffRowsA + kStagesA * 512;         // D rows
+  static constexpr int kOffSf = kOffRowsB + kStagesB * 512;  // K, V, then 2 per A stage, 2 per B stage
+  static constexpr int kSmemBytes = kOffSf + (2 + 2 * kStagesA + 2 * kStagesB) * kAtomBytes + 1024;
 };
 
 template <int D>
 struct DqCfg {
-  static constexpr int kStages = 2;
+  // ring A (K, V tiles) feeds S and dP and is released once they complete;
+  // ring B (Kt tiles) feeds dQ
+  static constexpr int kStagesA = 3, kStagesB = 3;
   static constexpr int kTileBytes = 128 * D;
   static constexpr uint32_t kSwz = D == 128 ? kSwz128 : kSwz64;
   static constexpr uint32_t kSBO = 8 * D;
   static constexpr int kKSteps = D / 32;
   // TMEM: S and dP side by side (both MMAs issue back to back), dQ
-  // accumulator, dS codes, scale atoms
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384;
-  static constexpr uint32_t kSfQ = 416, kSfG = 420, kSfK = 424 /*+4s*/, kSfV = 432 /*+4s*/, kSfDS0 = 440,
-                            kSfDS1 = 444, kSfKt = 448 /*+4s*/;
+  // accumulator, dS codes and scales double-buffered by tile parity (t = j & 1)
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384 /*+32t*/;
+  static constexpr uint32_t kSfQ = 448, kSfG = 452, kSfK = 456 /*+4t*/, kSfV = 464 /*+4t*/,
+                            kSfDS = 472 /*+16t, +4 per key block*/, kSfKt = 504 /*+4t*/;
   static constexpr int kOffQ = 0;
   static constexpr int kOffG = kOffQ + kTileBytes;
-  static constexpr int kOffStage = kOffG + kTileBytes;  // per stage: K, V, Kt
-  static constexpr int kStageBytes = 3 * kTileBytes;
-  static constexpr int kOffSf = kOffStage + kStages * kStageBytes;  // Q, G, then 3 per stage
-  static constexpr int kSmemBytes = kOffSf + (2 + 3 * kStages) * kAtomBytes + 1024;
+  static constexpr int kOffA = kOffG + kTileBytes;                     // per A stage: K, V
+  static constexpr int kOffB = kOffA + kStagesA * 2 * kTileBytes;      // per B stage: Kt
+  static constexpr int kOffSf = kOffB + kStagesB * kTileBytes;         // Q, G, 2 per A stage, 1 per B stage
+  static constexpr int kSmemBytes = kOffSf + (2 + 2 * kStagesA + kStagesB) * kAtomBytes + 1024;
 };
 
+template <int kCount = 32>
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&rr)[32], float mul) {
 #pragma unroll
-  for (int i = 0; i < 32; i += 8) {
+  for (int i = 0; i < kCount; i += 8) {
     uint4 v;
     v.x = pack_bf16x2(__uint_as_float(rr[i]) * mul, __uint_as_float(rr[i + 1]) * mul);
     v.y = pack_bf16x2(__uint_as_float(rr[i + 2]) * mul, __uint_as_float(rr[i + 3]) * mul);
     v.z = pack_bf16x2(__uint_as_float(rr[i + 4]) * mul, __uint_as_float(rr[i + 5]) * mul);
     v.w = pack_bf16x2(__uint_as_float(rr[i + 6]) * mul, __uint_as_float(rr[i + 7]) * mul);
     *reinterpret_cast<uint4*>(dst + i) = v;
-  }
-}
-
-// 64 fp32 columns of this thread's TMEM lane: two 32-column loads, one wait.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
-  uint32_t a[32], b[32];
-  tmem_ld32(taddr, a);
-  tmem_ld32(taddr + 32, b);
-  tmem_ld_wait();
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    v[i] = __uint_as_float(a[i]);
-    v[32 + i] = __uint_as_float(b[i]);
   }
 }
 
@@ -112,8 +110,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  __shared__ uint64_t bar_kv, bar_tile_full[C::kStages], bar_tile_empty[C::kStages], bar_s_full, bar_x_free,
-      bar_dp_full, bar_x_free2, bar_p_ready, bar_ds_ready, bar_pv_free, bar_dk_free, bar_final, bar_drain;
+  __shared__ uint64_t bar_kv, bar_a_full[C::kStagesA], bar_a_empty[C::kStagesA], bar_b_full[C::kStagesB],
+      bar_b_empty[C::kStagesB], bar_s_full, bar_x_free, bar_dp_full, bar_x_free2, bar_p_ready, bar_ds_ready,
+      bar_final, bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int64_t s_slot;
@@ -132,9 +131,13 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 
   if (tid == 0) {
     mbar_init(&bar_kv, 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&bar_tile_full[s], 1);
-      mbar_init(&bar_tile_empty[s], 1);
+    for (int s = 0; s < C::kStagesA; ++s) {
+      mbar_init(&bar_a_full[s], 1);
+      mbar_init(&bar_a_empty[s], 1 + kSoftmaxThreads / 32);  // dP^T commit + one lane per softmax warp
+    }
+    for (int s = 0; s < C::kStagesB; ++s) {
+      mbar_init(&bar_b_full[s], 1);
+      mbar_init(&bar_b_empty[s], 1);
     }
     mbar_init(&bar_s_full, 1);
     mbar_init(&bar_x_free, kSoftmaxThreads);
@@ -142,14 +145,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     mbar_init(&bar_x_free2, kSoftmaxThreads);
     mbar_init(&bar_p_ready, kSoftmaxThreads);
     mbar_init(&bar_ds_ready, kSoftmaxThreads);
-    mbar_init(&bar_pv_free, 1);
-    mbar_init(&bar_dk_free, 1);
     mbar_init(&bar_final, 1);
     mbar_init(&bar_drain, 1);
     s_abort = 0;
     fence_barrier_init();
   }
-  if (warp == 2) {
+  if (warp == 1) {
     tmem_alloc(&s_tmem, 512);
     tmem_relinquish();
   }
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   volatile int* abort_flag = &s_abort;
-  uint8_t* sSf = smem + C::kOffSf;  // [0] K, [1] V, stage s: 2 + 4s + (0 Q, 1 G, 2 Qt, 3 Gt)
+  uint8_t* sSf = smem + C::kOffSf;  // [0] K, [1] V, A stage s: 2 + 2s (Q, G), B stage s: 2 + 2 kStagesA + 2s (Qt, Gt)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -170,56 +171,83 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       tma_load_3d(smem + C::kOffV, &maps.v, &bar_kv, 0, hk, static_cast<int>(k0));
       bulk_load(sSf + 0 * kAtomBytes, a.k_sf + katom, kAtomBytes, &bar_kv);
       bulk_load(sSf + 1 * kAtomBytes, a.v_sf + katom, kAtomBytes, &bar_kv);
-      int issued = 0;
+      int issued_a = 0, issued_b = 0;
       for (int u = 0; u < n_work; ++u) {
-        const int s = u % C::kStages;
-        if (u >= C::kStages &&
-            !role_wait(&bar_tile_empty[s], ((u / C::kStages) - 1) & 1, abort_flag, a.err, kErrTimeoutTma))
-          break;
+        const int sa = u % C::kStagesA, sb = u % C::kStagesB;
         const int h = hk * grp + u / nq;
         const int qi = qi0 + u % nq;
         const int q0 = static_cast<int>(doc_start + static_cast<int64_t>(qi) * 128);
         const int64_t qslot = static_cast<int64_t>(h) * a.ntiles + tile_base + qi;
-        uint8_t* st = smem + C::kOffStage + s * C::kStageBytes;
-        uint8_t* sf = sSf + (2 + 4 * s) * kAtomBytes;
-        mbar_arrive_expect_tx(&bar_tile_full[s], 4 * C::kTileBytes + 4 * kAtomBytes + 2 * 512);
-        tma_load_3d(st + 0 * C::kTileBytes, &maps.q, &bar_tile_full[s], 0, h, q0);
-        tma_load_3d(st + 1 * C::kTileBytes, &maps.g, &bar_tile_full[s], 0, h, q0);
-        tma_load_3d(st + 2 * C::kTileBytes, &maps.qt, &bar_tile_full[s], 0, h, q0);
-        tma_load_3d(st + 3 * C::kTileBytes, &maps.gt, &bar_tile_full[s], 0, h, q0);
-        bulk_load(st + 4 * C::kTileBytes, a.lpad + qslot * 128, 512, &bar_tile_full[s]);
-        bulk_load(st + 4 * C::kTileBytes + 512, a.dpad + qslot * 128, 512, &bar_tile_full[s]);
-        bulk_load(sf + 0 * kAtomBytes, a.q_sf + qslot * kAtomBytes, kAtomBytes, &bar_tile_full[s]);
-        bulk_load(sf + 1 * kAtomBytes, a.g_sf + qslot * kAtomBytes, kAtomBytes, &bar_tile_full[s]);
-        bulk_load(sf + 2 * kAtomBytes, a.qt_sf + qslot * kAtomBytes, kAtomBytes, &bar_tile_full[s]);
-        bulk_load(sf + 3 * kAtomBytes, a.gt_sf + qslot * kAtomBytes, kAtomBytes, &bar_tile_full[s]);
-        issued = u + 1;
+        if (u >= C::kStagesA &&
+            !role_wait(&bar_a_empty[sa], ((u / C::kStagesA) - 1) & 1, abort_flag, a.err, kErrTimeoutTma))
+          break;
+        uint8_t* st = smem + C::kOffA + sa * 2 * C::kTileBytes;
+        uint8_t* sf = sSf + (2 + 2 * sa) * kAtomBytes;
+        mbar_arrive_expect_tx(&bar_a_full[sa], 2 * C::kTileBytes + 2 * kAtomBytes + 512);
+        tma_load_3d(st, &maps.q, &bar_a_full[sa], 0, h, q0);
+        tma_load_3d(st + C::kTileBytes, &maps.g, &bar_a_full[sa], 0, h, q0);
+        bulk_load(smem + C::kOffRowsA + sa * 512, a.lpad + qslot * 128, 512, &bar_a_full[sa]);
+        bulk_load(sf, a.q_sf + qslot * kAtomBytes, kAtomBytes, &bar_a_full[sa]);
+        bulk_load(sf + kAtomBytes, a.g_sf + qslot * kAtomBytes, kAtomBytes, &bar_a_full[sa]);
+        issued_a = u + 1;
+        if (u >= C::kStagesB &&
+            !role_wait(&bar_b_empty[sb], ((u / C::kStagesB) - 1) & 1, abort_flag, a.err, kErrTimeoutTma))
+          break;
+        st = smem + C::kOffB + sb * 2 * C::kTileBytes;
+        sf = sSf + (2 + 2 * C::kStagesA + 2 * sb) * kAtomBytes;
+        mbar_arrive_expect_tx(&bar_b_full[sb], 2 * C::kTileBytes + 2 * kAtomBytes + 512);
+        tma_load_3d(st, &maps.qt, &bar_b_full[sb], 0, h, q0);
+        tma_load_3d(st + C::kTileBytes, &maps.gt, &bar_b_full[sb], 0, h, q0);
+        bulk_load(smem + C::kOffRowsB + sb * 512, a.dpad + qslot * 128, 512, &bar_b_full[sb]);
+        bulk_load(sf, a.qt_sf + qslot * kAtomBytes, kAtomBytes, &bar_b_full[sb]);
+        bulk_load(sf + kAtomBytes, a.gt_sf + qslot * kAtomBytes, kAtomBytes, &bar_b_full[sb]);
+        issued_b = u + 1;
+        if (u + C::kStagesA < n_work) {  // warm L2 with the unit after ring A
+          const int un = u + C::kStagesA;
+          const int hn = hk * grp + un / nq;
+          const int qn = static_cast<int>(doc_start + static_cast<int64_t>(qi0 + un % nq) * 128);
+          tma_prefetch_l2_3d(&maps.q, 0, hn, qn);
+          tma_prefetch_l2_3d(&maps.g, 0, hn, qn);
+          tma_prefetch_l2_3d(&maps.qt, 0, hn, qn);
+          tma_prefetch_l2_3d(&maps.gt, 0, hn, qn);
+        }
       }
       role_wait(&bar_kv, 0, abort_flag, nullptr, 0);
-      for (int u = (issued > C::kStages ? issued - C::kStages : 0); u < issued; ++u)
-        mbar_wait(&bar_tile_full[u % C::kStages], (u / C::kStages) & 1, nullptr, 0);
+      for (int u = (issued_a > C::kStagesA ? issued_a - C::kStagesA : 0); u < issued_a; ++u)
+        mbar_wait(&bar_a_full[u % C::kStagesA], (u / C::kStagesA) & 1, nullptr, 0);
+      for (int u = (issued_b > C::kStagesB ? issued_b - C::kStagesB : 0); u < issued_b; ++u)
+        mbar_wait(&bar_b_full[u % C::kStagesB], (u / C::kStagesB) & 1, nullptr, 0);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      const uint32_t ka = smem_u32(smem + C::kOffK), va = smem_u32(smem + C::kOffV);
+      // descriptors built once; per MMA only constant offsets are added
+      const uint64_t dKa = make_sdesc(smem_u32(smem + C::kOffK), 16, C::kSBO, C::kSwz);
+      const uint64_t dVa = make_sdesc(smem_u32(smem + C::kOffV), 16, C::kSBO, C::kSwz);
+      const uint64_t dA = make_sdesc(smem_u32(smem + C::kOffA), 16, C::kSBO, C::kSwz);
+      const uint64_t dB = make_sdesc(smem_u32(smem + C::kOffB), 16, C::kSBO, C::kSwz);
+      const uint64_t dSf = atom_desc(sSf);
+      const uint32_t tX = tmem + C::kColX, tDV = tmem + C::kColDV, tDK = tmem + C::kColDK;
+      const uint32_t tP = tmem + C::kColP, tDS = tmem + C::kColDS;
+      const uint32_t tSfK = tmem + C::kSfK, tSfV = tmem + C::kSfV, tSfP = tmem + C::kSfP;
+      const uint32_t tSfDS = tmem + C::kSfDS;
       bool ok = role_wait(&bar_kv, 0, abort_flag, a.err, kErrTimeoutMma);
       if (ok) {
         tc_fence_after();
-        tmem_cp_atom(tmem + C::kSfK, sSf + 0 * kAtomBytes);
-        tmem_cp_atom(tmem + C::kSfV, sSf + 1 * kAtomBytes);
+        tmem_cp_desc(tSfK, dSf);
+        tmem_cp_desc(tSfV, sdesc_adv(dSf, kAtomBytes));
       }
       auto issue_s = [&](int u) -> bool {  // S^T = K Q^T into X
-        const int s = u % C::kStages;
-        if (!role_wait(&bar_tile_full[s], (u / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
+        const int sa = u % C::kStagesA;
+        if (!role_wait(&bar_a_full[sa], (u / C::kStagesA) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
         tc_fence_after();
-        const uint32_t st = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
-        tmem_cp_atom(tmem + C::kSfQ + 4 * s, sSf + (2 + 4 * s + 0) * kAtomBytes);
+        const uint64_t dq = sdesc_adv(dA, sa * 2 * C::kTileBytes);
+        const uint32_t tSfQ = tmem + C::kSfQ + 4 * (u & 1);
+        tmem_cp_desc(tSfQ, sdesc_adv(dSf, (2 + 2 * sa) * kAtomBytes));
 #pragma unroll
         for (int kk = 0; kk < C::kKSteps; ++kk)
-          mma_mxf8_ss(tmem + C::kColX, make_sdesc(ka + 32 * kk, 16, C::kSBO, C::kSwz),
-                      make_sdesc(st + 32 * kk, 16, C::kSBO, C::kSwz), make_idesc_mxf8(128, 128, 0, 0, kk, kk),
-                      tmem + C::kSfK, tmem + C::kSfQ + 4 * s, kk > 0);
+          mma_mxf8_ss(tX, sdesc_adv(dKa, 32 * kk), sdesc_adv(dq, 32 * kk), make_idesc_mxf8(128, 128, 0, 0, kk, kk),
+                      tSfK, tSfQ, kk > 0);
         mma_commit(&bar_s_full);
         return true;
       };
@@ -229,140 +257,139 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       // warps' read of X.
       if (ok) ok = issue_s(0);
       for (int u = 0; ok && u < n_work; ++u) {
-        const int s = u % C::kStages;
-        const uint32_t st = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
-        // dP^T = V G^T once S^T has been read out of X
+        const int sa = u % C::kStagesA, sb = u % C::kStagesB, t = u & 1;
+        const uint64_t da = sdesc_adv(dA, sa * 2 * C::kTileBytes);  // Q, G of this unit
+        const uint64_t db = sdesc_adv(dB, sb * 2 * C::kTileBytes);  // Qt, Gt of this unit
+        // dP^T = V G^T once S^T has been read out of X; ring B (D row, Qt,
+        // Gt) must have landed before the softmax warps see dP^T
         if (!(ok = role_wait(&bar_x_free, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        if (!(ok = role_wait(&bar_b_full[sb], (u / C::kStagesB) & 1, abort_flag, a.err, kErrTimeoutMma))) break;
         tc_fence_after();
-        tmem_cp_atom(tmem + C::kSfG + 4 * s, sSf + (2 + 4 * s + 1) * kAtomBytes);
+        const uint32_t tSfG = tmem + C::kSfG + 4 * t;
+        tmem_cp_desc(tSfG, sdesc_adv(dSf, (2 + 2 * sa + 1) * kAtomBytes));
 #pragma unroll
         for (int kk = 0; kk < C::kKSteps; ++kk)
-          mma_mxf8_ss(tmem + C::kColX, make_sdesc(va + 32 * kk, 16, C::kSBO, C::kSwz),
-                      make_sdesc(st + C::kTileBytes + 32 * kk, 16, C::kSBO, C::kSwz),
-                      make_idesc_mxf8(128, 128, 0, 0, kk, kk), tmem + C::kSfV, tmem + C::kSfG + 4 * s, kk > 0);
+          mma_mxf8_ss(tX, sdesc_adv(dVa, 32 * kk), sdesc_adv(da, C::kTileBytes + 32 * kk),
+                      make_idesc_mxf8(128, 128, 0, 0, kk, kk), tSfV, tSfG, kk > 0);
         mma_commit(&bar_dp_full);
+        mma_commit(&bar_a_empty[sa]);
         // dV += P^T G (P^T codes written while dP^T ran)
         if (!(ok = role_wait(&bar_p_ready, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
         tc_fence_after();
-        tmem_cp_atom(tmem + C::kSfGt + 4 * s, sSf + (2 + 4 * s + 3) * kAtomBytes);
+        const uint32_t tSfGt = tmem + C::kSfGt + 4 * t;
+        tmem_cp_desc(tSfGt, sdesc_adv(dSf, (2 + 2 * C::kStagesA + 2 * sb + 1) * kAtomBytes));
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_mxf8_ts(tmem + C::kColDV, tmem + C::kColP + 8 * kk,
-                      make_sdesc(st + 3 * C::kTileBytes + kk * 32 * D, 16, C::kSBO, C::kSwz),
-                      make_idesc_mxf8(128, D, 0, 1, kk, kk), tmem + C::kSfP, tmem + C::kSfGt + 4 * s,
-                      (u > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar_pv_free);
+          mma_mxf8_ts(tDV, tP + 8 * kk, sdesc_adv(db, C::kTileBytes + kk * 32 * D),
+                      make_idesc_mxf8(128, D, 0, 1, kk, kk), tSfP, tSfGt, (u > 0 || kk > 0) ? 1u : 0u);
         // next S^T as soon as dP^T has been read (runs while dS is formed)
         if (!(ok = role_wait(&bar_x_free2, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
         if (u + 1 < n_work && !(ok = issue_s(u + 1))) break;
         // dK += dS^T Q
         if (!(ok = role_wait(&bar_ds_ready, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
         tc_fence_after();
-        tmem_cp_atom(tmem + C::kSfQt + 4 * s, sSf + (2 + 4 * s + 2) * kAtomBytes);
+        const uint32_t tSfQt = tmem + C::kSfQt + 4 * t;
+        tmem_cp_desc(tSfQt, sdesc_adv(dSf, (2 + 2 * C::kStagesA + 2 * sb) * kAtomBytes));
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_mxf8_ts(tmem + C::kColDK, tmem + C::kColDS + 8 * kk,
-                      make_sdesc(st + 2 * C::kTileBytes + kk * 32 * D, 16, C::kSBO, C::kSwz),
-                      make_idesc_mxf8(128, D, 0, 1, kk & 1, kk), tmem + (kk < 2 ? C::kSfDS0 : C::kSfDS1),
-                      tmem + C::kSfQt + 4 * s, (u > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar_dk_free);
-        mma_commit(&bar_tile_empty[s]);
+          mma_mxf8_ts(tDK, tDS + 8 * kk, sdesc_adv(db, kk * 32 * D), make_idesc_mxf8(128, D, 0, 1, 0, kk),
+                      tSfDS + 4 * kk, tSfQt, (u > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar_b_empty[sb]);
       }
       mma_commit(&bar_final);
       mma_commit(&bar_drain);
       mbar_wait(&bar_drain, 0, nullptr, 0);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 2) {
     // ------------------------------------------------------------ softmax / dS
+    // Warp w serves TMEM lane quadrant w % 4 (key rows) and query columns
+    // [32 part, 32 part + 32): one 32 x 32 block of P^T and dS^T per unit.
     const int quad = warp & 3;
-    const int hf = (warp - 4) >> 2;       // column half: queries [64 hf, 64 hf + 64)
+    const int part = (warp - 2) >> 2;
     const int j = quad * 32 + lane;       // key row (TMEM lane)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const int64_t kpos = static_cast<int64_t>(kt) * 128 + j;
     const bool key_valid = kpos < n;
     const float kb8 = key_valid ? 8.0f : -INFINITY;  // 2^8 boost of P^T; invalid key rows -> 0
     const float sl2 = a.scale_log2;
-    if (hf == 0) {
+    if (part == 0) {
       tmem_st4(lane_base + C::kSfP, 0x77777777u, 0x77777777u, 0x77777777u, 0x77777777u);  // 2^-8
       tmem_st_wait();
     }
     bool ok = true;
     for (int u = 0; u < n_work; ++u) {
-      const int s = u % C::kStages;
+      const int sa = u % C::kStagesA, sb = u % C::kStagesB;
       const int qi = qi0 + u % nq;
-      const float* lrow = reinterpret_cast<const float*>(smem + C::kOffStage + s * C::kStageBytes + 4 * C::kTileBytes) + 64 * hf;
-      const float* drow = lrow + 128;
+      const float* lrow = reinterpret_cast<const float*>(smem + C::kOffRowsA + sa * 512) + 32 * part;
+      const float* drow = reinterpret_cast<const float*>(smem + C::kOffRowsB + sb * 512) + 32 * part;
       if (!(ok = warp_wait(&bar_s_full, u & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
-      float p[64];
-      tmem_ld64(lane_base + C::kColX + 64 * hf, p);
+      float p[32];
+      {
+        uint32_t rr[32];
+        tmem_ld32(lane_base + C::kColX + 32 * part, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) p[c] = __uint_as_float(rr[c]);
+      }
       tc_fence_before();
       mbar_arrive(&bar_x_free);
       // P^T boosted by 2^8 (P <= 1 after the LSE normalization); rows past the
       // document end have LSE = +inf, so their P is 0 without a test
 #pragma unroll
-      for (int c = 0; c < 64; c += 4) {
+      for (int c = 0; c < 32; c += 4) {
         const float4 l4 = *reinterpret_cast<const float4*>(lrow + c);
         p[c] = ex2_approx(fmaf(p[c], sl2, kb8 - l4.x));
         p[c + 1] = ex2_approx(fmaf(p[c + 1], sl2, kb8 - l4.y));
         p[c + 2] = ex2_approx(fmaf(p[c + 2], sl2, kb8 - l4.z));
         p[c + 3] = ex2_approx(fmaf(p[c + 3], sl2, kb8 - l4.w));
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_a_empty[sa]);  // this warp is done with the LSE row
       if (a.causal && qi == kt) {  // diagonal tile: query index (in tile) >= key index
 #pragma unroll
-        for (int c = 0; c < 64; ++c) p[c] = (64 * hf + c >= j) ? p[c] : 0.0f;
+        for (int c = 0; c < 32; ++c) p[c] = (32 * part + c >= j) ? p[c] : 0.0f;
       }
-      // the previous unit's dV MMA must be done with the P^T codes
-      if (u > 0 && !(ok = warp_wait(&bar_pv_free, (u - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 16; c += 8) {
+      // the previous unit's dV MMA, issued before S^T_u, is done with the P^T
+      // codes: s_full(u) completed only after it
+      {
         uint32_t w[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          w[k] = pack_e4m3x4(p[4 * (c + k)], p[4 * (c + k) + 1], p[4 * (c + k) + 2], p[4 * (c + k) + 3]);
-        tmem_st8(lane_base + C::kColP + 16 * hf + c, w);
+        for (int k = 0; k < 8; ++k) w[k] = pack_e4m3x4(p[4 * k], p[4 * k + 1], p[4 * k + 2], p[4 * k + 3]);
+        tmem_st8(lane_base + C::kColP + 8 * part, w);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bar_p_ready);
       if (!(ok = warp_wait(&bar_dp_full, u & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
-      // dS^T = P^T (dP^T - D), in place; X is released once both chunks are in
-      // registers
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
+      // dS^T = P^T (dP^T - D), in place
+      {
         uint32_t rr[32];
-        tmem_ld32(lane_base + C::kColX + 64 * hf + 32 * cc, rr);
+        tmem_ld32(lane_base + C::kColX + 32 * part, rr);
         tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&bar_x_free2);
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(drow + 32 * cc + i);
-          p[32 * cc + i] *= __uint_as_float(rr[i]) - d4.x;
-          p[32 * cc + i + 1] *= __uint_as_float(rr[i + 1]) - d4.y;
-          p[32 * cc + i + 2] *= __uint_as_float(rr[i + 2]) - d4.z;
-          p[32 * cc + i + 3] *= __uint_as_float(rr[i + 3]) - d4.w;
+          const float4 d4 = *reinterpret_cast<const float4*>(drow + i);
+          p[i] *= __uint_as_float(rr[i]) - d4.x;
+          p[i + 1] *= __uint_as_float(rr[i + 1]) - d4.y;
+          p[i + 2] *= __uint_as_float(rr[i + 2]) - d4.z;
+          p[i + 3] *= __uint_as_float(rr[i + 3]) - d4.w;
         }
       }
-      tc_fence_before();
-      mbar_arrive(&bar_x_free2);
-      // the previous unit's dK MMA must be done with the dS^T codes and scales
-      if (u > 0 && !(ok = warp_wait(&bar_dk_free, (u - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
-      tc_fence_after();
-      uint32_t ebytes = 0;
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        float x[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = p[32 * cc + i];
+      // the previous unit's dK MMA, issued before dP^T_u, is done with the
+      // dS^T codes and scales: dp_full(u) completed only after it
+      {
         uint32_t w[8];
-        ebytes |= quant_ds_block32(x, 8, w) << (8 * cc);  // 32 key rows x 32 queries
-        tmem_st8(lane_base + C::kColDS + 16 * hf + 8 * cc, w);
+        const uint32_t eb = quant_ds_block32(p, 8, w);  // 32 key rows x 32 queries
+        tmem_st8(lane_base + C::kColDS + 8 * part, w);
+        // dK's A operand is dS^T (rows = keys, K = queries): for K step
+        // `part` the scale of row r sits in lane r, column kSfDS + 4 part +
+        // r / 32, byte 0
+        tmem_st1(lane_base + C::kSfDS + 4 * part + quad, eb | 0x7F7F7F00u);
       }
-      // dK's A operand is dS^T (rows = keys, groups = 32-query blocks); row r's
-      // scales sit in lane r, column base + r / 32.  Half hf owns query
-      // blocks 2 hf, 2 hf + 1 (bytes 0, 1 of its own scale columns).
-      tmem_st1(lane_base + (hf ? C::kSfDS1 : C::kSfDS0) + quad, ebytes | 0x7F7F0000u);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bar_ds_ready);
@@ -374,22 +401,30 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       const int64_t t = doc_start + kpos;
       __nv_bfloat16* dvrow = reinterpret_cast<__nv_bfloat16*>(a.dv) + (t * a.Hkv + hk) * D;
       __nv_bfloat16* dkrow = reinterpret_cast<__nv_bfloat16*>(a.dk) + (t * a.Hkv + hk) * D;
-      // half 0 writes dV, half 1 writes dK
-      const uint32_t col = hf ? C::kColDK : C::kColDV;
-      __nv_bfloat16* dst = hf ? dkrow : dvrow;
-      const float mul = hf ? a.alpha : 1.0f;
+      // each warp writes D/4 channels of dV and of dK for its key rows
+      constexpr int kCols = D / 4;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int g = 0; g < 2; ++g) {
+        const uint32_t col = (g ? C::kColDK : C::kColDV) + kCols * part;
+        __nv_bfloat16* dst = (g ? dkrow : dvrow) + kCols * part;
+        const float mul = g ? a.alpha : 1.0f;
         uint32_t rr[32];
-        tmem_ld32(lane_base + col + 32 * c, rr);
+        if constexpr (kCols == 32) {
+          tmem_ld32(lane_base + col, rr);
+        } else {
+          uint32_t r16[16];
+          tmem_ld16(lane_base + col, r16);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) rr[i] = r16[i];
+        }
         tmem_ld_wait();
-        if (key_valid) store_row_bf16(dst + 32 * c, rr, mul);
+        if (key_valid) store_row_bf16<kCols>(dst, rr, mul);
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -403,8 +438,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  __shared__ uint64_t bar_q, bar_kv_full[C::kStages], bar_kv_empty[C::kStages], bar_sdp_full, bar_x_free,
-      bar_ds_ready, bar_ds_free, bar_final, bar_drain;
+  __shared__ uint64_t bar_q, bar_a_full[C::kStagesA], bar_a_empty[C::kStagesA], bar_b_full[C::kStagesB],
+      bar_b_empty[C::kStagesB], bar_sdp_full, bar_x_free, bar_ds_ready, bar_final, bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int64_t s_slot;
@@ -422,20 +457,23 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 
   if (tid == 0) {
     mbar_init(&bar_q, 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&bar_kv_full[s], 1);
-      mbar_init(&bar_kv_empty[s], 1);
+    for (int s = 0; s < C::kStagesA; ++s) {
+      mbar_init(&bar_a_full[s], 1);
+      mbar_init(&bar_a_empty[s], 1);
+    }
+    for (int s = 0; s < C::kStagesB; ++s) {
+      mbar_init(&bar_b_full[s], 1);
+      mbar_init(&bar_b_empty[s], 1);
     }
     mbar_init(&bar_sdp_full, 1);
     mbar_init(&bar_x_free, kSoftmaxThreads);
     mbar_init(&bar_ds_ready, kSoftmaxThreads);
-    mbar_init(&bar_ds_free, 1);
     mbar_init(&bar_final, 1);
     mbar_init(&bar_drain, 1);
     s_abort = 0;
     fence_barrier_init();
   }
-  if (warp == 2) {
+  if (warp == 1) {
     tmem_alloc(&s_tmem, 512);
     tmem_relinquish();
   }
@@ -444,7 +482,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   volatile int* abort_flag = &s_abort;
-  uint8_t* sSf = smem + C::kOffSf;  // [0] Q, [1] G, stage s: 2 + 3s + (0 K, 1 V, 2 Kt)
+  uint8_t* sSf = smem + C::kOffSf;  // [0] Q, [1] G, A stage s: 2 + 2s (K, V), B stage s: 2 + 2 kStagesA + s (Kt)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -456,86 +494,109 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       tma_load_3d(smem + C::kOffG, &maps.g, &bar_q, 0, h, q0);
       bulk_load(sSf + 0 * kAtomBytes, a.q_sf + qatom, kAtomBytes, &bar_q);
       bulk_load(sSf + 1 * kAtomBytes, a.g_sf + qatom, kAtomBytes, &bar_q);
-      int issued = 0;
+      int issued_a = 0, issued_b = 0;
       for (int j = 0; j < n_kt; ++j) {
-        const int s = j % C::kStages;
-        if (j >= C::kStages &&
-            !role_wait(&bar_kv_empty[s], ((j / C::kStages) - 1) & 1, abort_flag, a.err, kErrTimeoutTma))
-          break;
+        const int sa = j % C::kStagesA, sb = j % C::kStagesB;
         const int k0 = static_cast<int>(doc_start + static_cast<int64_t>(j) * 128);
         const int64_t katom = (static_cast<int64_t>(hk) * a.ntiles + tile_base + j) * kAtomBytes;
-        uint8_t* st = smem + C::kOffStage + s * C::kStageBytes;
-        uint8_t* sf = sSf + (2 + 3 * s) * kAtomBytes;
-        mbar_arrive_expect_tx(&bar_kv_full[s], 3 * C::kTileBytes + 3 * kAtomBytes);
-        tma_load_3d(st + 0 * C::kTileBytes, &maps.k, &bar_kv_full[s], 0, hk, k0);
-        tma_load_3d(st + 1 * C::kTileBytes, &maps.v, &bar_kv_full[s], 0, hk, k0);
-        tma_load_3d(st + 2 * C::kTileBytes, &maps.kt, &bar_kv_full[s], 0, hk, k0);
-        bulk_load(sf + 0 * kAtomBytes, a.k_sf + katom, kAtomBytes, &bar_kv_full[s]);
-        bulk_load(sf + 1 * kAtomBytes, a.v_sf + katom, kAtomBytes, &bar_kv_full[s]);
-        bulk_load(sf + 2 * kAtomBytes, a.kt_sf + katom, kAtomBytes, &bar_kv_full[s]);
-        issued = j + 1;
+        if (j >= C::kStagesA &&
+            !role_wait(&bar_a_empty[sa], ((j / C::kStagesA) - 1) & 1, abort_flag, a.err, kErrTimeoutTma))
+          break;
+        uint8_t* st = smem + C::kOffA + sa * 2 * C::kTileBytes;
+        uint8_t* sf = sSf + (2 + 2 * sa) * kAtomBytes;
+        mbar_arrive_expect_tx(&bar_a_full[sa], 2 * C::kTileBytes + 2 * kAtomBytes);
+        tma_load_3d(st, &maps.k, &bar_a_full[sa], 0, hk, k0);
+        tma_load_3d(st + C::kTileBytes, &maps.v, &bar_a_full[sa], 0, hk, k0);
+        bulk_load(sf, a.k_sf + katom, kAtomBytes, &bar_a_full[sa]);
+        bulk_load(sf + kAtomBytes, a.v_sf + katom, kAtomBytes, &bar_a_full[sa]);
+        issued_a = j + 1;
+        if (j >= C::kStagesB &&
+            !role_wait(&bar_b_empty[sb], ((j / C::kStagesB) - 1) & 1, abort_flag, a.err, kErrTimeoutTma))
+          break;
+        mbar_arrive_expect_tx(&bar_b_full[sb], C::kTileBytes + kAtomBytes);
+        tma_load_3d(smem + C::kOffB + sb * C::kTileBytes, &maps.kt, &bar_b_full[sb], 0, hk, k0);
+        bulk_load(sSf + (2 + 2 * C::kStagesA + sb) * kAtomBytes, a.kt_sf + katom, kAtomBytes, &bar_b_full[sb]);
+        issued_b = j + 1;
+        if (j + C::kStagesA < n_kt) {  // warm L2 with the key tile after ring A
+          const int kn = k0 + 128 * C::kStagesA;
+          tma_prefetch_l2_3d(&maps.k, 0, hk, kn);
+          tma_prefetch_l2_3d(&maps.v, 0, hk, kn);
+          tma_prefetch_l2_3d(&maps.kt, 0, hk, kn);
+        }
       }
       role_wait(&bar_q, 0, abort_flag, nullptr, 0);
-      for (int j = (issued > C::kStages ? issued - C::kStages : 0); j < issued; ++j)
-        mbar_wait(&bar_kv_full[j % C::kStages], (j / C::kStages) & 1, nullptr, 0);
+      for (int j = (issued_a > C::kStagesA ? issued_a - C::kStagesA : 0); j < issued_a; ++j)
+        mbar_wait(&bar_a_full[j % C::kStagesA], (j / C::kStagesA) & 1, nullptr, 0);
+      for (int j = (issued_b > C::kStagesB ? issued_b - C::kStagesB : 0); j < issued_b; ++j)
+        mbar_wait(&bar_b_full[j % C::kStagesB], (j / C::kStagesB) & 1, nullptr, 0);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      const uint32_t qa = smem_u32(smem + C::kOffQ), ga = smem_u32(smem + C::kOffG);
+      const uint64_t dQa = make_sdesc(smem_u32(smem + C::kOffQ), 16, C::kSBO, C::kSwz);
+      const uint64_t dGa = make_sdesc(smem_u32(smem + C::kOffG), 16, C::kSBO, C::kSwz);
+      const uint64_t dA = make_sdesc(smem_u32(smem + C::kOffA), 16, C::kSBO, C::kSwz);
+      const uint64_t dB = make_sdesc(smem_u32(smem + C::kOffB), 16, C::kSBO, C::kSwz);
+      const uint64_t dSf = atom_desc(sSf);
+      const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColDQ, tDS = tmem + C::kColDS;
+      const uint32_t tSfQ = tmem + C::kSfQ, tSfG = tmem + C::kSfG;
+      const uint32_t tSfDS = tmem + C::kSfDS;
       bool ok = role_wait(&bar_q, 0, abort_flag, a.err, kErrTimeoutMma);
       if (ok) {
         tc_fence_after();
-        tmem_cp_atom(tmem + C::kSfQ, sSf + 0 * kAtomBytes);
-        tmem_cp_atom(tmem + C::kSfG, sSf + 1 * kAtomBytes);
+        tmem_cp_desc(tSfQ, dSf);
+        tmem_cp_desc(tSfG, sdesc_adv(dSf, kAtomBytes));
       }
       auto issue_sdp = [&](int j) -> bool {  // S = Q K^T and dP = G V^T, back to back
-        const int s = j % C::kStages;
-        if (!role_wait(&bar_kv_full[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
+        const int sa = j % C::kStagesA;
+        if (!role_wait(&bar_a_full[sa], (j / C::kStagesA) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
         // S and dP of the previous key tile must have been read out of TMEM
         if (j >= 1 && !role_wait(&bar_x_free, (j - 1) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
         tc_fence_after();
-        const uint32_t st = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
-        tmem_cp_atom(tmem + C::kSfK + 4 * s, sSf + (2 + 3 * s + 0) * kAtomBytes);
-        tmem_cp_atom(tmem + C::kSfV + 4 * s, sSf + (2 + 3 * s + 1) * kAtomBytes);
+        const uint64_t dstage = sdesc_adv(dA, sa * 2 * C::kTileBytes);  // K, V
+        const uint64_t dsf = sdesc_adv(dSf, (2 + 2 * sa) * kAtomBytes);
+        const uint32_t tSfK = tmem + C::kSfK + 4 * (j & 1), tSfV = tmem + C::kSfV + 4 * (j & 1);
+        tmem_cp_desc(tSfK, dsf);
+        tmem_cp_desc(tSfV, sdesc_adv(dsf, kAtomBytes));
 #pragma unroll
         for (int kk = 0; kk < C::kKSteps; ++kk)
-          mma_mxf8_ss(tmem + C::kColS, make_sdesc(qa + 32 * kk, 16, C::kSBO, C::kSwz),
-                      make_sdesc(st + 32 * kk, 16, C::kSBO, C::kSwz), make_idesc_mxf8(128, 128, 0, 0, kk, kk),
-                      tmem + C::kSfQ, tmem + C::kSfK + 4 * s, kk > 0);
+          mma_mxf8_ss(tS, sdesc_adv(dQa, 32 * kk), sdesc_adv(dstage, 32 * kk), make_idesc_mxf8(128, 128, 0, 0, kk, kk),
+                      tSfQ, tSfK, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < C::kKSteps; ++kk)
-          mma_mxf8_ss(tmem + C::kColDP, make_sdesc(ga + 32 * kk, 16, C::kSBO, C::kSwz),
-                      make_sdesc(st + C::kTileBytes + 32 * kk, 16, C::kSBO, C::kSwz),
-                      make_idesc_mxf8(128, 128, 0, 0, kk, kk), tmem + C::kSfG, tmem + C::kSfV + 4 * s, kk > 0);
+          mma_mxf8_ss(tDP, sdesc_adv(dGa, 32 * kk), sdesc_adv(dstage, C::kTileBytes + 32 * kk),
+                      make_idesc_mxf8(128, 128, 0, 0, kk, kk), tSfG, tSfV, kk > 0);
         mma_commit(&bar_sdp_full);
+        mma_commit(&bar_a_empty[sa]);
         return true;
       };
       if (ok) ok = issue_sdp(0);
       for (int j = 0; ok && j < n_kt; ++j) {
-        const int s = j % C::kStages;
-        const uint32_t st = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
+        const int sb = j % C::kStagesB;
         if (j + 1 < n_kt && !(ok = issue_sdp(j + 1))) break;  // overlaps the dS work of tile j
         if (!(ok = role_wait(&bar_ds_ready, j & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        if (!(ok = role_wait(&bar_b_full[sb], (j / C::kStagesB) & 1, abort_flag, a.err, kErrTimeoutMma))) break;
         tc_fence_after();
-        tmem_cp_atom(tmem + C::kSfKt + 4 * s, sSf + (2 + 3 * s + 2) * kAtomBytes);
+        const uint32_t tSfKt = tmem + C::kSfKt + 4 * (j & 1);
+        tmem_cp_desc(tSfKt, sdesc_adv(dSf, (2 + 2 * C::kStagesA + sb) * kAtomBytes));
+        const uint64_t dkt = sdesc_adv(dB, sb * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // dQ += dS K (contraction over 128 keys)
-          mma_mxf8_ts(tmem + C::kColDQ, tmem + C::kColDS + 8 * kk,
-                      make_sdesc(st + 2 * C::kTileBytes + kk * 32 * D, 16, C::kSBO, C::kSwz),
-                      make_idesc_mxf8(128, D, 0, 1, kk & 1, kk), tmem + (kk < 2 ? C::kSfDS0 : C::kSfDS1),
-                      tmem + C::kSfKt + 4 * s, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar_ds_free);
-        mma_commit(&bar_kv_empty[s]);
+          mma_mxf8_ts(tDQ, tDS + 32 * (j & 1) + 8 * kk, sdesc_adv(dkt, kk * 32 * D),
+                      make_idesc_mxf8(128, D, 0, 1, 0, kk), tSfDS + 16 * (j & 1) + 4 * kk, tSfKt,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar_b_empty[sb]);
       }
       mma_commit(&bar_final);
       mma_commit(&bar_drain);
       mbar_wait(&bar_drain, 0, nullptr, 0);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 2) {
     // ------------------------------------------------------------ softmax / dS
+    // Warp w serves TMEM lane quadrant w % 4 (query rows) and key columns
+    // [32 part, 32 part + 32): one 32 x 32 block of P and dS per key tile.
     const int quad = warp & 3;
-    const int hf = (warp - 4) >> 2;       // column half: keys [64 hf, 64 hf + 64)
+    const int part = (warp - 2) >> 2;
     const int r = quad * 32 + lane;       // query row (TMEM lane)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const int64_t qpos = static_cast<int64_t>(qt) * 128 + r;
@@ -548,46 +609,37 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     for (int j = 0; j < n_kt; ++j) {
       if (!(ok = warp_wait(&bar_sdp_full, j & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
-      float p[64];
-      tmem_ld64(lane_base + C::kColS + 64 * hf, p);
-#pragma unroll
-      for (int c = 0; c < 64; ++c) p[c] = ex2_approx(fmaf(p[c], sl2, nl));
-      // keys past the document end (last tile) or after the query (diagonal tile)
-      const int64_t rem = n - static_cast<int64_t>(j) * 128;
-      int lim = rem < 128 ? static_cast<int>(rem) : 128;
-      if (a.causal && j == qt) lim = min(lim, r + 1);
-      if (lim < 128) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) p[c] = (64 * hf + c < lim) ? p[c] : 0.0f;
-      }
-      // dS = P (dP - D), in place
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t rr[32];
-        tmem_ld32(lane_base + C::kColDP + 64 * hf + 32 * cc, rr);
+      float p[32];
+      {
+        uint32_t rs[32], rd[32];
+        tmem_ld32(lane_base + C::kColS + 32 * part, rs);
+        tmem_ld32(lane_base + C::kColDP + 32 * part, rd);
         tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&bar_x_free);  // S and dP read: the next tile's S, dP may start
+        // keys past the document end (last tile) or after the query (diagonal tile)
+        const int64_t rem = n - static_cast<int64_t>(j) * 128;
+        int lim = rem < 128 ? static_cast<int>(rem) : 128;
+        if (a.causal && j == qt) lim = min(lim, r + 1);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) p[32 * cc + i] *= (__uint_as_float(rr[i]) - dd);
+        for (int c = 0; c < 32; ++c) {
+          const float pc = ex2_approx(fmaf(__uint_as_float(rs[c]), sl2, nl));
+          // dS = P (dP - D)
+          p[c] = (32 * part + c < lim) ? pc * (__uint_as_float(rd[c]) - dd) : 0.0f;
+        }
       }
-      tc_fence_before();
-      mbar_arrive(&bar_x_free);  // S and dP read: the next tile's S, dP may start
-      // the previous dQ MMA must be done with the dS codes and scales
-      if (j > 0 && !(ok = warp_wait(&bar_ds_free, (j - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
-      tc_fence_after();
-      uint32_t ebytes = 0;
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        float x[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = p[32 * cc + i];
+      // dS codes and scales alternate between two TMEM buffers: dQ_{j-2},
+      // the last reader of this buffer, was issued before S_j and dP_j, so
+      // sdp_full(j) has completed only after it
+      {
+        const uint32_t t = j & 1;
         uint32_t w[8];
-        ebytes |= quant_ds_block32(x, 0, w) << (8 * cc);  // 32 query rows x 32 keys
-        tmem_st8(lane_base + C::kColDS + 16 * hf + 8 * cc, w);
+        const uint32_t eb = quant_ds_block32(p, 0, w);  // 32 query rows x 32 keys
+        tmem_st8(lane_base + C::kColDS + 32 * t + 8 * part, w);
+        // dQ's A operand is dS (rows = queries, K = keys): for K step `part`
+        // the scale of row r sits in lane r, column kSfDS + 16 t + 4 part + r / 32
+        tmem_st1(lane_base + C::kSfDS + 16 * t + 4 * part + quad, eb | 0x7F7F7F00u);
       }
-      // dQ's A operand is dS (rows = queries, groups = 32-key blocks): row r's
-      // scales sit in lane r, column base + r / 32; half hf owns key blocks
-      // 2 hf, 2 hf + 1.
-      tmem_st1(lane_base + (hf ? C::kSfDS1 : C::kSfDS0) + quad, ebytes | 0x7F7F0000u);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bar_ds_ready);
@@ -597,20 +649,24 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       tc_fence_after();
       const int64_t t = doc_start + qpos;
       __nv_bfloat16* dqrow = reinterpret_cast<__nv_bfloat16*>(a.dq_out) + (t * a.Hq + h) * D;
-      // each half writes half of the row's channels
+      // each warp writes D/4 channels of the row
+      constexpr int kCols = D / 4;
+      uint32_t rr[32];
+      if constexpr (kCols == 32) {
+        tmem_ld32(lane_base + C::kColDQ + kCols * part, rr);
+      } else {
+        uint32_t r16[16];
+        tmem_ld16(lane_base + C::kColDQ + kCols * part, r16);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t rr[32];
-        const int cb = (D / 2) * hf + 32 * c;
-        tmem_ld32(lane_base + C::kColDQ + cb, rr);
-        tmem_ld_wait();
-        if (q_valid) store_row_bf16(dqrow + cb, rr, a.alpha);
+        for (int i = 0; i < 16; ++i) rr[i] = r16[i];
       }
+      tmem_ld_wait();
+      if (q_valid) store_row_bf16<kCols>(dqrow + kCols * part, rr, a.alpha);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

@@ -19,14 +19,17 @@
 //          every K step reaches through the descriptor's leading byte offset);
 //   O = O / L -> bf16, LSE = m + ln l with l the fp32 sum of the unquantized
 //   weights (FLAMIA notes sec. 2, online softmax).
-// Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM
-// owner, warps 4..11 = softmax / correction / epilogue (two warps per query
-// row quadrant, each taking 128 of the 256 key columns; they exchange row
-// maxima through shared memory).  The next S MMA starts once the softmax
-// warps have read S out of TMEM; the P V MMA runs after P is stored.
+// Warp roles: warp 0 = TMA producer, warp 1 = TMEM owner and MMA issuer,
+// warps 2..17 = softmax / correction / epilogue: four warps per TMEM lane
+// quadrant, each taking 64 of the 256 key columns of its 32 query rows.  A
+// softmax warp copies its S columns into registers and releases S at once,
+// so the next S MMA runs while the exponentials of this tile are formed; the
+// four warps of a quadrant merge their row maxima through shared memory.
+// K and V tiles stream through separate three-stage rings (256 keys per
+// stage).
 //
 // TMEM columns: S [0,256), O [256,256+D) and L [256+D,256+D+16), Q-scale 400,
-// K-scale 404+8s (two atoms per 256 keys), V-scale atoms 420 and 428 each
+// K-scale 404 + 8 (j mod 2) (two atoms per 256 keys), V-scale atoms 420 and 428 each
 // followed by a column block of 1.0 for the ones rows, P-scale 436, P
 // [448,512).
 #include <cuda_bf16.h>
@@ -39,14 +42,15 @@ namespace {
 
 template <int D>
 struct FwdCfg {
-  static constexpr int kStages = 2;
+  static constexpr int kStages = 3;
   static constexpr int kHalfBytes = 128 * D;          // one 128-key box of K or V
   static constexpr int kKVBytes = 2 * kHalfBytes;     // 256 keys
   static constexpr uint32_t kSwz = D == 128 ? kSwz128 : kSwz64;
   static constexpr uint32_t kSBO = 8 * D;
   static constexpr int kKSteps = D / 32;              // K steps of S = Q K^T
   static constexpr int kKStepBytes = 32 * D;          // 32 keys of V (P V K step)
-  static constexpr int kThreads = 384;                // 4 role warps + 8 softmax warps
+  static constexpr int kThreads = 576;                // 2 role warps + 16 softmax warps
+  static constexpr int kSoftmaxThreads = 512;
   static constexpr uint32_t kColS = 0, kColO = 256, kColL = 256 + D, kColSfQ = 400, kColSfK = 404, kColSfVA = 420,
                             kColOneA = 424, kColSfVB = 428, kColOneB = 432, kColSfP = 436, kColP = 448;
   // shared memory map (offsets from the 1024-aligned base)
@@ -93,10 +97,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  __shared__ uint64_t bar_q, bar_kv_full[C::kStages], bar_kv_empty[C::kStages], bar_s_full, bar_s_empty, bar_p_full,
-      bar_o_done, bar_drain, bar_mx[2], bar_lsum;
-  __shared__ float s_mx[2][2][128];  // [iteration parity][half][row] partial row maxima
-  __shared__ float s_l[2][128];      // [half][row] partial row sums
+  __shared__ uint64_t bar_q, bar_k_full[C::kStages], bar_k_empty[C::kStages], bar_v_full[C::kStages],
+      bar_v_empty[C::kStages], bar_s_full, bar_s_empty, bar_p_full, bar_o_done, bar_drain, bar_mx[2][4], bar_lsum;
+  __shared__ float s_mx[2][4][128];  // [iteration parity][column quarter][row] partial row maxima
+  __shared__ float s_l[4][128];      // [column quarter][row] partial row sums
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int64_t s_slot;
@@ -118,21 +122,25 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   if (tid == 0) {
     mbar_init(&bar_q, 1);
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&bar_kv_full[s], 1);
-      mbar_init(&bar_kv_empty[s], 1);
+      mbar_init(&bar_k_full[s], 1);
+      mbar_init(&bar_k_empty[s], 1);
+      mbar_init(&bar_v_full[s], 1);
+      mbar_init(&bar_v_empty[s], 1);
     }
     mbar_init(&bar_s_full, 1);
-    mbar_init(&bar_s_empty, 256);
-    mbar_init(&bar_p_full, 256);
+    mbar_init(&bar_s_empty, C::kSoftmaxThreads);
+    mbar_init(&bar_p_full, C::kSoftmaxThreads);
     mbar_init(&bar_o_done, 1);
     mbar_init(&bar_drain, 1);
-    mbar_init(&bar_mx[0], 256);
-    mbar_init(&bar_mx[1], 256);
-    mbar_init(&bar_lsum, 256);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(&bar_mx[0][q], 128);
+      mbar_init(&bar_mx[1][q], 128);
+    }
+    mbar_init(&bar_lsum, C::kSoftmaxThreads);
     s_abort = 0;
     fence_barrier_init();
   }
-  if (warp == 2) {
+  if (warp == 1) {
     tmem_alloc(&s_tmem, 512);
     tmem_relinquish();
   }
@@ -156,12 +164,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       tma_load_3d(smem + C::kOffQ, &maps.q, &bar_q, 0, h, q0);
       bulk_load(smem + C::kOffSfQ, a.q_sf + ((static_cast<int64_t>(h) * a.ntiles + tile_base + qt) * kAtomBytes),
                 kAtomBytes, &bar_q);
-      int issued = 0;
-      for (int j = 0; j < n_it; ++j) {
+      // K and V stream through separate rings: a K stage is released as soon
+      // as its S MMA has completed, a V stage after its P V MMA, so the keys
+      // of later tiles are loaded well ahead of the P V chain.
+      int issued_k = 0, issued_v = 0;
+      bool ok = true;
+      for (int j = 0; ok && j < n_it; ++j) {
         const int s = j % C::kStages;
-        if (j >= C::kStages) {
-          if (!role_wait(&bar_kv_empty[s], ((j / C::kStages) - 1) & 1, abort_flag, a.err, kErrTimeoutTma)) break;
-        }
         const int t0 = 2 * j;  // first 128-key tile of this iteration
         // the second half may lie past the document: reuse the first half's
         // atoms then (its keys are masked; the scales just have to be finite)
@@ -169,89 +178,121 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         const int k0 = static_cast<int>(doc_start + static_cast<int64_t>(t0) * 128);
         const int64_t atom0 = (static_cast<int64_t>(hk) * a.ntiles + tile_base + t0) * kAtomBytes;
         const int64_t atom1 = (static_cast<int64_t>(hk) * a.ntiles + tile_base + t1) * kAtomBytes;
+        if (j >= C::kStages &&
+            !(ok = role_wait(&bar_k_empty[s], ((j / C::kStages) - 1) & 1, abort_flag, a.err, kErrTimeoutTma)))
+          break;
         uint8_t* sk = smem + C::kOffK + s * C::kKVBytes;
-        uint8_t* sv = smem + C::kOffV + s * C::kKVBytes;
         uint8_t* sfk = smem + C::kOffSfK + s * 2 * kAtomBytes;
+        mbar_arrive_expect_tx(&bar_k_full[s], C::kKVBytes + 2 * kAtomBytes);
+        tma_load_3d(sk, &maps.k, &bar_k_full[s], 0, hk, k0);
+        tma_load_3d(sk + C::kHalfBytes, &maps.k, &bar_k_full[s], 0, hk, k0 + 128);
+        bulk_load(sfk, a.k_sf + atom0, kAtomBytes, &bar_k_full[s]);
+        bulk_load(sfk + kAtomBytes, a.k_sf + atom1, kAtomBytes, &bar_k_full[s]);
+        issued_k = j + 1;
+        if (j >= C::kStages &&
+            !(ok = role_wait(&bar_v_empty[s], ((j / C::kStages) - 1) & 1, abort_flag, a.err, kErrTimeoutTma)))
+          break;
+        uint8_t* sv = smem + C::kOffV + s * C::kKVBytes;
         uint8_t* sfv = smem + C::kOffSfV + s * 2 * kAtomBytes;
-        mbar_arrive_expect_tx(&bar_kv_full[s], 2 * C::kKVBytes + 4 * kAtomBytes);
-        tma_load_3d(sk, &maps.k, &bar_kv_full[s], 0, hk, k0);
-        tma_load_3d(sk + C::kHalfBytes, &maps.k, &bar_kv_full[s], 0, hk, k0 + 128);
-        tma_load_3d(sv, &maps.v, &bar_kv_full[s], 0, hk, k0);
-        tma_load_3d(sv + C::kHalfBytes, &maps.v, &bar_kv_full[s], 0, hk, k0 + 128);
-        bulk_load(sfk, a.k_sf + atom0, kAtomBytes, &bar_kv_full[s]);
-        bulk_load(sfk + kAtomBytes, a.k_sf + atom1, kAtomBytes, &bar_kv_full[s]);
-        bulk_load(sfv, a.v_sf + atom0, kAtomBytes, &bar_kv_full[s]);
-        bulk_load(sfv + kAtomBytes, a.v_sf + atom1, kAtomBytes, &bar_kv_full[s]);
-        issued = j + 1;
+        mbar_arrive_expect_tx(&bar_v_full[s], C::kKVBytes + 2 * kAtomBytes);
+        tma_load_3d(sv, &maps.v, &bar_v_full[s], 0, hk, k0);
+        tma_load_3d(sv + C::kHalfBytes, &maps.v, &bar_v_full[s], 0, hk, k0 + 128);
+        bulk_load(sfv, a.v_sf + atom0, kAtomBytes, &bar_v_full[s]);
+        bulk_load(sfv + kAtomBytes, a.v_sf + atom1, kAtomBytes, &bar_v_full[s]);
+        issued_v = j + 1;
+        // warm L2 with the keys the rings will load next
+        if (j + C::kStages < n_it) {
+          const int kp = k0 + 256 * C::kStages;
+          tma_prefetch_l2_3d(&maps.k, 0, hk, kp);
+          tma_prefetch_l2_3d(&maps.k, 0, hk, kp + 128);
+          tma_prefetch_l2_3d(&maps.v, 0, hk, kp);
+          tma_prefetch_l2_3d(&maps.v, 0, hk, kp + 128);
+        }
       }
       // drain: every load issued must have landed before the CTA exits
       role_wait(&bar_q, 0, abort_flag, nullptr, 0);
-      for (int j = (issued > C::kStages ? issued - C::kStages : 0); j < issued; ++j)
-        mbar_wait(&bar_kv_full[j % C::kStages], (j / C::kStages) & 1, nullptr, 0);
+      for (int j = (issued_k > C::kStages ? issued_k - C::kStages : 0); j < issued_k; ++j)
+        mbar_wait(&bar_k_full[j % C::kStages], (j / C::kStages) & 1, nullptr, 0);
+      for (int j = (issued_v > C::kStages ? issued_v - C::kStages : 0); j < issued_v; ++j)
+        mbar_wait(&bar_v_full[j % C::kStages], (j / C::kStages) & 1, nullptr, 0);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t qa = smem_u32(smem + C::kOffQ), onesa = smem_u32(smem + C::kOffOnes);
+      // descriptors built once; per MMA only constant offsets are added.  The
+      // P V operand B = [V | 1] keeps its second atom column (the ones block)
+      // fixed, so stepping its start address by x bytes lowers its leading
+      // byte offset by x.
+      const uint32_t onesa = smem_u32(smem + C::kOffOnes), va0 = smem_u32(smem + C::kOffV);
+      const uint64_t dQa = make_sdesc(smem_u32(smem + C::kOffQ), 16, C::kSBO, C::kSwz);
+      const uint64_t dK0 = make_sdesc(smem_u32(smem + C::kOffK), 16, C::kSBO, C::kSwz);
+      const uint64_t dV0 = make_sdesc(va0, onesa - va0, C::kSBO, C::kSwz);
+      const uint64_t dSfK0 = atom_desc(smem + C::kOffSfK), dSfV0 = atom_desc(smem + C::kOffSfV);
+      auto v_adv = [](uint64_t d, uint32_t bytes) -> uint64_t {
+        return d + (bytes >> 4) - (static_cast<uint64_t>(bytes >> 4) << 16);
+      };
+      const uint32_t tS = tmem + C::kColS, tO = tmem + C::kColO, tP = tmem + C::kColP;
+      const uint32_t tSfQ = tmem + C::kColSfQ, tSfP = tmem + C::kColSfP;
+      const uint32_t tSfVA = tmem + C::kColSfVA, tSfVB = tmem + C::kColSfVB;
       bool ok = role_wait(&bar_q, 0, abort_flag, a.err, kErrTimeoutMma);
       if (ok) {
         tc_fence_after();
-        tmem_cp_atom(tmem + C::kColSfQ, smem + C::kOffSfQ);
+        tmem_cp_atom(tSfQ, smem + C::kOffSfQ);
       }
       auto issue_s = [&](int j) -> bool {  // S = Q K^T, 128 x 256
         const int s = j % C::kStages;
-        if (!role_wait(&bar_kv_full[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
+        if (!role_wait(&bar_k_full[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
         if (j >= 1 && !role_wait(&bar_s_empty, (j - 1) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
         tc_fence_after();
-        uint8_t* sfk = smem + C::kOffSfK + s * 2 * kAtomBytes;
-        tmem_cp_atom(tmem + C::kColSfK + 8 * s, sfk);
-        tmem_cp_atom(tmem + C::kColSfK + 8 * s + 4, sfk + kAtomBytes);
-        const uint32_t ka = smem_u32(smem + C::kOffK + s * C::kKVBytes);
+        // K-scale slots alternate between two pairs of atoms (an S MMA may be
+        // issued while the previous one is still in the pipe)
+        const uint32_t tSfK = tmem + C::kColSfK + 8 * (j & 1);
+        const uint64_t dsf = sdesc_adv(dSfK0, s * 2 * kAtomBytes);
+        tmem_cp_desc(tSfK, dsf);
+        tmem_cp_desc(tSfK + 4, sdesc_adv(dsf, kAtomBytes));
+        const uint64_t dk = sdesc_adv(dK0, s * C::kKVBytes);
 #pragma unroll
         for (int kk = 0; kk < C::kKSteps; ++kk)
-          mma_mxf8_ss(tmem + C::kColS, make_sdesc(qa + 32 * kk, 16, C::kSBO, C::kSwz),
-                      make_sdesc(ka + 32 * kk, 16, C::kSBO, C::kSwz), make_idesc_mxf8(128, 256, 0, 0, kk, kk),
-                      tmem + C::kColSfQ, tmem + C::kColSfK + 8 * s, kk > 0);
+          mma_mxf8_ss(tS, sdesc_adv(dQa, 32 * kk), sdesc_adv(dk, 32 * kk), make_idesc_mxf8(128, 256, 0, 0, kk, kk),
+                      tSfQ, tSfK, kk > 0);
         mma_commit(&bar_s_full);
+        mma_commit(&bar_k_empty[s]);
         return true;
       };
       if (ok) ok = issue_s(0);
       for (int j = 0; ok && j < n_it; ++j) {
         if (j + 1 < n_it && !issue_s(j + 1)) break;  // waits until S_j has been read out
         const int s = j % C::kStages;
+        if (!role_wait(&bar_v_full[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma)) break;
         if (!role_wait(&bar_p_full, j & 1, abort_flag, a.err, kErrTimeoutMma)) break;
         tc_fence_after();
-        uint8_t* sfv = smem + C::kOffSfV + s * 2 * kAtomBytes;
-        tmem_cp_atom(tmem + C::kColSfVA, sfv);
-        tmem_cp_atom(tmem + C::kColSfVB, sfv + kAtomBytes);
-        const uint32_t va = smem_u32(smem + C::kOffV + s * C::kKVBytes);
+        const uint64_t dsf = sdesc_adv(dSfV0, s * 2 * kAtomBytes);
+        tmem_cp_desc(tSfVA, dsf);
+        tmem_cp_desc(tSfVB, sdesc_adv(dsf, kAtomBytes));
+        const uint64_t dv = v_adv(dV0, s * C::kKVBytes);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // [O | L] += P [V | 1], 32 keys per step
-          const uint32_t vk = va + kk * C::kKStepBytes;
-          mma_mxf8_ts(tmem + C::kColO, tmem + C::kColP + 8 * kk, make_sdesc(vk, onesa - vk, C::kSBO, C::kSwz),
-                      make_idesc_mxf8(128, D + 16, 0, 1, kk & 3, kk & 3), tmem + C::kColSfP,
-                      tmem + (kk < 4 ? C::kColSfVA : C::kColSfVB), (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk)  // [O | L] += P [V | 1], 32 keys per step
+          mma_mxf8_ts(tO, tP + 8 * kk, v_adv(dv, kk * C::kKStepBytes), make_idesc_mxf8(128, D + 16, 0, 1, kk & 3, kk & 3),
+                      tSfP, kk < 4 ? tSfVA : tSfVB, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bar_o_done);
-        mma_commit(&bar_kv_empty[s]);
+        mma_commit(&bar_v_empty[s]);
       }
       // drain the tensor pipe before the TMEM is released
       mma_commit(&bar_drain);
       mbar_wait(&bar_drain, 0, nullptr, 0);
     }
-  } else if (warp >= 4) {
+  } else {
     // ------------------------------------------------------------ softmax
-    // Two warps per TMEM lane quadrant: warp half hf handles key columns
-    // [128 hf, 128 hf + 128) of its 32 rows, in two passes of 64 columns
-    // (max, then exponentials); the halves exchange their row maxima through
-    // shared memory once per iteration and keep separate partial sums.
+    // Warp w serves TMEM lane quadrant w % 4 (rows 32 quad .. 32 quad + 31)
+    // and key columns [64 part, 64 part + 64) of each 256-key tile; for the
+    // O rescale and the epilogue it owns O columns [D/4 part, D/4 part + D/4).
     const int quad = warp & 3;
-    const int hf = (warp - 4) >> 2;
+    const int part = (warp - 2) >> 2;
     const int r = quad * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const int64_t qpos = static_cast<int64_t>(qt) * 128 + r;  // document-relative query index
     const float sl2 = a.scale_log2;
-    if (hf == 0) {
+    if (part == 0) {
       // 1.0 for the ones rows of both V atoms, 2^-4 for P
       tmem_st4(lane_base + C::kColOneA, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
       tmem_st4(lane_base + C::kColOneB, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
@@ -259,38 +300,34 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       tmem_st_wait();
     }
     float m = -INFINITY;  // running (lazy) max of the scaled scores, log2 units
-    float l16 = 0.0f;     // this half's sum of 2^(s - m + 4)
+    float l16 = 0.0f;     // this warp's sum of 2^(s - m + 4) over its columns
     bool ok = true;
     for (int j = 0; j < n_it; ++j) {
       if (!(ok = warp_wait(&bar_s_full, j & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
+      float sv[64];
+      ld64(lane_base + C::kColS + 64 * part, sv);
+      tc_fence_before();
+      mbar_arrive(&bar_s_empty);  // S is in registers: the next S MMA may start
       // columns >= lim are masked (keys past the document end, or after the
       // query on the causal diagonal); only the last iteration has any
-      int lim = 256;
       if (j == n_it - 1) {
         const int64_t rem = n - static_cast<int64_t>(j) * 256;
-        lim = rem < 256 ? static_cast<int>(rem) : 256;
+        int lim = rem < 256 ? static_cast<int>(rem) : 256;
         if (a.causal) {
           const int64_t c = qpos - static_cast<int64_t>(j) * 256 + 1;
           if (c < lim) lim = static_cast<int>(c);
         }
-      }
-      const uint32_t scol = C::kColS + 128 * hf;
-      float mt = -INFINITY;
-#pragma unroll
-      for (int ps = 0; ps < 2; ++ps) {
-        float sv[64];
-        ld64(lane_base + scol + 64 * ps, sv);
         if (lim < 256) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) sv[c] = (128 * hf + 64 * ps + c < lim) ? sv[c] : -INFINITY;
+          for (int c = 0; c < 64; ++c) sv[c] = (64 * part + c < lim) ? sv[c] : -INFINITY;
         }
-        mt = fmaxf(mt, max64(sv));
       }
-      s_mx[j & 1][hf][r] = mt;
-      mbar_arrive(&bar_mx[j & 1]);
-      if (!(ok = warp_wait(&bar_mx[j & 1], (j >> 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
-      mt = fmaxf(mt, s_mx[j & 1][hf ^ 1][r]);
+      float mt = max64(sv);
+      s_mx[j & 1][part][r] = mt;
+      mbar_arrive(&bar_mx[j & 1][quad]);
+      if (!(ok = warp_wait(&bar_mx[j & 1][quad], (j >> 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      mt = fmaxf(fmaxf(s_mx[j & 1][0][r], s_mx[j & 1][1][r]), fmaxf(s_mx[j & 1][2][r], s_mx[j & 1][3][r]));
       const float mts = mt * sl2;
       bool rescale_o = false;
       float factor = 1.0f;
@@ -301,42 +338,27 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         m = mts;
         rescale_o = true;
       }
-      // exponentials into registers; S is released after its second read, so
-      // the next S MMA does not wait for this tile's P V
       const float neg = 4.0f - m;
       float lsum = 0.0f;
-      uint32_t pw[32];  // E4M3 codes of this half's 128 weights
+      uint32_t pw[16];  // E4M3 codes of this warp's 64 weights
 #pragma unroll
-      for (int ps = 0; ps < 2; ++ps) {
-        float sv[64];
-        ld64(lane_base + scol + 64 * ps, sv);
-        if (ps == 1) {  // S fully read: the next S MMA may overwrite it
-          tc_fence_before();
-          mbar_arrive(&bar_s_empty);
-        }
-        if (lim < 256) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) sv[c] = (128 * hf + 64 * ps + c < lim) ? sv[c] : -INFINITY;
-        }
-#pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          const float p0 = ex2_approx(fmaf(sv[c], sl2, neg));
-          const float p1 = ex2_approx(fmaf(sv[c + 1], sl2, neg));
-          const float p2 = ex2_approx(fmaf(sv[c + 2], sl2, neg));
-          const float p3 = ex2_approx(fmaf(sv[c + 3], sl2, neg));
-          lsum += (p0 + p1) + (p2 + p3);
-          pw[16 * ps + (c >> 2)] = pack_e4m3x4(p0, p1, p2, p3);
-        }
+      for (int c = 0; c < 64; c += 4) {
+        const float p0 = ex2_approx(fmaf(sv[c], sl2, neg));
+        const float p1 = ex2_approx(fmaf(sv[c + 1], sl2, neg));
+        const float p2 = ex2_approx(fmaf(sv[c + 2], sl2, neg));
+        const float p3 = ex2_approx(fmaf(sv[c + 3], sl2, neg));
+        lsum += (p0 + p1) + (p2 + p3);
+        pw[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
       }
       // the previous P V must be done before P is overwritten and O rescaled
       if (j > 0 && !(ok = warp_wait(&bar_o_done, (j - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
       // tcgen05.ld/st are warp-collective: the whole warp rescales its rows'
-      // half of O when any of them needs it (factor 1 for the others).
+      // share of O when any of them needs it (factor 1 for the others).
       if (__any_sync(0xffffffffu, rescale_o)) {
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          const uint32_t col = C::kColO + (D / 2) * hf + 32 * c;
+        for (int c = 0; c < D / 128; ++c) {
+          const uint32_t col = C::kColO + (D / 4) * part + 32 * c;
           uint32_t rr[32];
           tmem_ld32(lane_base + col, rr);
           tmem_ld_wait();
@@ -348,7 +370,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             tmem_st8(lane_base + col + i, w);
           }
         }
-        if (hf == 0) {
+        if (D == 64) {
+          uint32_t rr[16];
+          tmem_ld16(lane_base + C::kColO + 16 * part, rr);
+          tmem_ld_wait();
+          uint32_t w0[8], w1[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            w0[k] = __float_as_uint(__uint_as_float(rr[k]) * factor);
+            w1[k] = __float_as_uint(__uint_as_float(rr[8 + k]) * factor);
+          }
+          tmem_st8(lane_base + C::kColO + 16 * part, w0);
+          tmem_st8(lane_base + C::kColO + 16 * part + 8, w1);
+        }
+        if (part == 0) {
           uint32_t rr[16];
           tmem_ld16(lane_base + C::kColL, rr);
           tmem_ld_wait();
@@ -358,12 +393,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           tmem_st8(lane_base + C::kColL, w);
         }
       }
+      {
+        uint32_t w0[8], w1[8];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t w[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) w[k] = pw[8 * q + k];
-        tmem_st8(lane_base + C::kColP + 32 * hf + 8 * q, w);
+        for (int k = 0; k < 8; ++k) {
+          w0[k] = pw[k];
+          w1[k] = pw[8 + k];
+        }
+        tmem_st8(lane_base + C::kColP + 16 * part, w0);
+        tmem_st8(lane_base + C::kColP + 16 * part + 8, w1);
       }
       l16 = l16 * factor + lsum;
       tmem_st_wait();
@@ -371,7 +409,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       mbar_arrive(&bar_p_full);
     }
     // ---------------------------------------------------------- epilogue
-    s_l[hf][r] = l16;
+    s_l[part][r] = l16;
     mbar_arrive(&bar_lsum);
     if (ok) ok = role_wait(&bar_lsum, 0, abort_flag, a.err, kErrTimeoutEpilogue);
     if (ok) ok = role_wait(&bar_o_done, (n_it - 1) & 1, abort_flag, a.err, kErrTimeoutEpilogue);
@@ -387,31 +425,33 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       const bool valid = qpos < n;
       const int64_t t = doc_start + qpos;
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + (t * a.Hq + h) * D;
+      constexpr int kCols = D / 4;  // 32 (d128) or 16 (d64) output channels per warp
+      uint32_t rr[kCols];
+      if constexpr (kCols == 32) {
+        tmem_ld32(lane_base + C::kColO + kCols * part, rr);
+      } else {
+        tmem_ld16(lane_base + C::kColO + kCols * part, rr);
+      }
+      tmem_ld_wait();
+      if (valid) {
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        const int cb = (D / 2) * hf + 32 * c;
-        uint32_t rr[32];
-        tmem_ld32(lane_base + C::kColO + cb, rr);
-        tmem_ld_wait();
-        if (valid) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(rr[i]) * inv, __uint_as_float(rr[i + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(rr[i + 2]) * inv, __uint_as_float(rr[i + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(rr[i + 4]) * inv, __uint_as_float(rr[i + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(rr[i + 6]) * inv, __uint_as_float(rr[i + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + cb + i) = v;
-          }
+        for (int i = 0; i < kCols; i += 8) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(rr[i]) * inv, __uint_as_float(rr[i + 1]) * inv);
+          v.y = pack_bf16x2(__uint_as_float(rr[i + 2]) * inv, __uint_as_float(rr[i + 3]) * inv);
+          v.z = pack_bf16x2(__uint_as_float(rr[i + 4]) * inv, __uint_as_float(rr[i + 5]) * inv);
+          v.w = pack_bf16x2(__uint_as_float(rr[i + 6]) * inv, __uint_as_float(rr[i + 7]) * inv);
+          *reinterpret_cast<uint4*>(orow + kCols * part + i) = v;
         }
       }
-      if (valid && hf == 0)
-        a.lse[static_cast<int64_t>(h) * a.T + t] = (m - 4.0f + log2f(s_l[0][r] + s_l[1][r])) * 0.69314718055994531f;
+      if (valid && part == 0)
+        a.lse[static_cast<int64_t>(h) * a.T + t] =
+            (m - 4.0f + log2f((s_l[0][r] + s_l[1][r]) + (s_l[2][r] + s_l[3][r]))) * 0.69314718055994531f;
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
