@@ -65,7 +65,39 @@ bool make_code_map(CUtensorMap* map, const void* codes, int64_t T, int H, int d)
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over the emitted dS codes: rows of 128 query bytes, one 128 x 128
+// tile per key-tile / query-tile pair, loaded with the 128-byte swizzle.
+bool make_ds_map(CUtensorMap* map, const void* codes, int64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(codes), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Most 128-token tiles in one document.
+int64_t max_doc_tiles(const mxa_shape& s) {
+  const int64_t maxlen = s.cu_seqlens ? s.max_seqlen : (s.num_docs > 0 ? s.T / s.num_docs : 0);
+  return (maxlen + 127) / 128;
+}
+
+// Bytes of the tile-padded D and LSE rows (both backward paths).
+size_t bwd_rows_bytes(const mxa_shape& s) {
+  return 2 * static_cast<size_t>(s.Hq) * static_cast<size_t>(s.ntiles > 0 ? s.ntiles : 0) * 128 * 4;
+}
+
+// Bytes of the emitted dS (codes + one scale atom per tile pair).
+size_t bwd_ds_bytes(const mxa_shape& s) {
+  return static_cast<size_t>(s.Hq) * static_cast<size_t>(s.ntiles > 0 ? s.ntiles : 0) *
+         static_cast<size_t>(max_doc_tiles(s)) * (16384 + 512);
+}
 
 mxa_status check_view(const mxa_qview& v) {
   if (!v.codes || !v.scales) return MXA_ERR_ARG;
@@ -223,17 +255,19 @@ mxa_status mxa_fwd(const mxa_fwd_params* p, cudaStream_t stream) {
   return MXA_OK;
 }
 
-size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p) {
+size_t mxa_bwd_workspace_min_bytes(const mxa_bwd_params* p) {
   if (!p || p->shape.T < 0 || p->shape.Hq <= 0 || (p->shape.d != 64 && p->shape.d != 128)) return 0;
   const size_t T = static_cast<size_t>(p->shape.T), Hq = static_cast<size_t>(p->shape.Hq),
                d = static_cast<size_t>(p->shape.d);
-  const size_t NT = static_cast<size_t>(p->shape.ntiles > 0 ? p->shape.ntiles : 0);
-  const size_t dbytes = 2 * Hq * NT * 128 * 4;  // tile-padded D and LSE*log2(e)
-  (void)T;
-  // FP32 mode: deterministic dQ kernel, no accumulator; FP16 x 2^9 mode:
-  // fp16 partial-sum accumulator [T, Hq, d].
+  // FP16 x 2^9 mode adds its fp16 partial-sum accumulator [T, Hq, d]
   const size_t acc = p->dq_mode == MXA_DQ_FP16_X512 ? T * Hq * d * 2 : 0;
-  return dbytes + ((acc + 255) & ~size_t(255));
+  return bwd_rows_bytes(p->shape) + ((acc + 255) & ~size_t(255));
+}
+
+size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p) {
+  const size_t base = mxa_bwd_workspace_min_bytes(p);
+  if (base == 0 || p->dq_mode == MXA_DQ_FP16_X512) return base;
+  return base + bwd_ds_bytes(p->shape);
 }
 
 mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cudaStream_t stream) {
@@ -249,7 +283,7 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
       !aligned(p->dv, 16))
     return MXA_ERR_ALIGN;
   if (p->dq_mode != MXA_DQ_FP32 && p->dq_mode != MXA_DQ_FP16_X512) return MXA_ERR_ARG;
-  if (!workspace || ws_bytes < mxa_bwd_workspace_bytes(p)) return MXA_ERR_WORKSPACE;
+  if (!workspace || ws_bytes < mxa_bwd_workspace_min_bytes(p)) return MXA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return MXA_ERR_ALIGN;
   if (s.T == 0) return MXA_OK;
   BwdMaps maps;
@@ -314,8 +348,19 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   a.dv = p->dv;
   a.dq_out = p->dq;
   a.err = device_error_word();
+  a.mt = static_cast<int>(max_doc_tiles(s));
   if (!fp16) {
-    // FP32: dK/dV kernel and the dQ kernel (dQ summed in TMEM, fixed order)
+    // FP32: dK/dV kernel, then dQ summed in TMEM in a fixed order -- over the
+    // dS the dK/dV kernel emitted when the workspace holds it, else by a
+    // kernel that forms dS again
+    if (ws_bytes >= mxa_bwd_workspace_bytes(p)) {
+      a.ds_codes = static_cast<uint8_t*>(workspace) + dbytes;
+      a.ds_sf = a.ds_codes + static_cast<size_t>(s.Hq) * static_cast<size_t>(s.ntiles) * a.mt * 16384;
+      if (!make_ds_map(&maps.ds, a.ds_codes, static_cast<int64_t>(s.Hq) * s.ntiles * a.mt * 128))
+        return MXA_ERR_CUDA;
+      if (launch_bwd_emit(a, maps, s.d, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
+      return MXA_OK;
+    }
     if (launch_bwd_split(a, maps, s.d, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
     return MXA_OK;
   }

@@ -389,6 +389,17 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         // `part` the scale of row r sits in lane r, column kSfDS + 4 part +
         // r / 32, byte 0
         tmem_st1(lane_base + C::kSfDS + 4 * part + quad, eb | 0x7F7F7F00u);
+        if (a.ds_codes) {
+          // the same block for the dQ product: codes of key row j, queries
+          // [32 part, 32 part + 32); its scale at rows (queries) 32 part +
+          // lane, group quad of the pair's atom
+          const int h = hk * grp + u / nq;
+          const int64_t pair = (static_cast<int64_t>(h) * a.ntiles + tile_base + kt) * a.mt + qi;
+          uint4* dst = reinterpret_cast<uint4*>(a.ds_codes + pair * 16384 + j * 128 + 32 * part);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          a.ds_sf[pair * kAtomBytes + lane * 16 + part * 4 + quad] = static_cast<uint8_t>(eb);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
@@ -696,6 +707,25 @@ cudaError_t launch_bwd_split(const BwdArgs& a, const BwdMaps& m, int d, int max_
     attn_bwd_dq_kernel<64><<<g2, kSplitThreads, DqCfg<64>::kSmemBytes, stream>>>(m, a);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_emit(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
+  const int tiles = (max_seqlen + 127) / 128;
+  dim3 g1(tiles, a.num_docs, a.Hkv);
+  cudaError_t e;
+  if (d == 128) {
+    e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DkdvCfg<128>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attn_bwd_dkdv_kernel<128><<<g1, kSplitThreads, DkdvCfg<128>::kSmemBytes, stream>>>(m, a);
+  } else {
+    e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DkdvCfg<64>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attn_bwd_dkdv_kernel<64><<<g1, kSplitThreads, DkdvCfg<64>::kSmemBytes, stream>>>(m, a);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return launch_dq_gemm(a, m, d, max_seqlen, stream);
 }
 
 }  // namespace mxa

@@ -1,0 +1,189 @@
+// dq_gemm.cu -- dQ = alpha * dS K over the dS blocks the dK/dV kernel emitted.
+//
+// FLAMIA notes, Algorithm 1 step 14 (dQ_i += dS_ij K_j), with dS taken from
+// where it was formed once: the dK/dV kernel quantizes every 32 x 32 dS block
+// (FA4 write-up, "Квантование dS без транспонирования") and stores its E4M3
+// codes plus one UE8M0 scale per block.  The dQ product is then a plain
+// block-scaled GEMM per (128-query tile, query head, document), summed over
+// the visible key tiles in TMEM in a fixed order (deterministic, no atomics):
+//   A = dS   [128 queries x 128 keys]: the stored tile has key rows of query
+//            bytes, i.e. an MN-major A operand, loaded by TMA with the 128-byte
+//            swizzle; its scales (rows = queries, groups = key blocks) come
+//            as one 512-byte atom per tile pair;
+//   B = K    TOK view (rows = channels, groups = 32-key blocks), MN-major.
+// Warps: 0 = TMA producer, 1 = TMEM owner and MMA issuer, 2..5 = epilogue.
+#include <cuda_bf16.h>
+
+#include "attn_common.cuh"
+
+namespace mxa {
+
+namespace {
+
+template <int D>
+struct DqGemmCfg {
+  static constexpr int kStages = 4;
+  static constexpr int kThreads = 192;
+  static constexpr int kTileBytes = 128 * D;  // one Kt tile
+  static constexpr uint32_t kSwz = D == 128 ? kSwz128 : kSwz64;
+  static constexpr uint32_t kSBO = 8 * D;
+  // TMEM: dQ accumulator [0, D), then dS and K scale slots (4 columns each,
+  // alternating by tile parity)
+  static constexpr uint32_t kColDQ = 0, kSfDS = D /*+4t*/, kSfKt = D + 8 /*+4t*/;
+  static constexpr uint32_t kTmemCols = D == 128 ? 256 : 128;
+  // shared memory per stage: dS tile (16 KB), Kt tile, dS atom, Kt atom
+  static constexpr int kStageBytes = 16384 + kTileBytes + 2 * kAtomBytes;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+};
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 1)
+    attn_dq_gemm_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
+  using C = DqGemmCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_full[C::kStages], bar_empty[C::kStages], bar_final, bar_drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int64_t s_slot;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.y, h = blockIdx.z;
+  const int hk = h / (a.Hq / a.Hkv);
+  int64_t doc_start, n;
+  doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
+  const int n_tiles = static_cast<int>((n + 127) / 128);
+  const int qt = a.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+  if (qt >= n_tiles) return;
+  const int n_kt = a.causal ? qt + 1 : n_tiles;
+  const int64_t tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, C::kThreads, &s_slot);
+
+  if (tid == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    mbar_init(&bar_final, 1);
+    mbar_init(&bar_drain, 1);
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int* abort_flag = &s_abort;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      int issued = 0;
+      for (int j = 0; j < n_kt; ++j) {
+        const int s = j % C::kStages;
+        if (j >= C::kStages &&
+            !role_wait(&bar_empty[s], ((j / C::kStages) - 1) & 1, abort_flag, a.err, kErrTimeoutTma))
+          break;
+        // pair (h, b, key tile j, query tile qt)
+        const int64_t pair = (static_cast<int64_t>(h) * a.ntiles + tile_base + j) * a.mt + qt;
+        const int k0 = static_cast<int>(doc_start + static_cast<int64_t>(j) * 128);
+        const int64_t katom = (static_cast<int64_t>(hk) * a.ntiles + tile_base + j) * kAtomBytes;
+        uint8_t* st = smem + s * C::kStageBytes;
+        mbar_arrive_expect_tx(&bar_full[s], 16384 + C::kTileBytes + 2 * kAtomBytes);
+        tma_load_2d(st, &maps.ds, &bar_full[s], 0, static_cast<int>(pair * 128));
+        tma_load_3d(st + 16384, &maps.kt, &bar_full[s], 0, hk, k0);
+        bulk_load(st + 16384 + C::kTileBytes, a.ds_sf + pair * kAtomBytes, kAtomBytes, &bar_full[s]);
+        bulk_load(st + 16384 + C::kTileBytes + kAtomBytes, a.kt_sf + katom, kAtomBytes, &bar_full[s]);
+        issued = j + 1;
+      }
+      for (int j = (issued > C::kStages ? issued - C::kStages : 0); j < issued; ++j)
+        mbar_wait(&bar_full[j % C::kStages], (j / C::kStages) & 1, nullptr, 0);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      const uint64_t dA0 = make_sdesc(smem_u32(smem), 16, 1024, kSwz128);           // dS: 128-byte query rows
+      const uint64_t dB0 = make_sdesc(smem_u32(smem + 16384), 16, C::kSBO, C::kSwz);  // Kt
+      const uint64_t dSf0 = atom_desc(smem + 16384 + C::kTileBytes);
+      bool ok = true;
+      for (int j = 0; j < n_kt; ++j) {
+        const int s = j % C::kStages, t = j & 1;
+        if (!(ok = role_wait(&bar_full[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        tc_fence_after();
+        const uint32_t tSfA = tmem + C::kSfDS + 4 * t, tSfB = tmem + C::kSfKt + 4 * t;
+        const uint64_t dsf = sdesc_adv(dSf0, s * C::kStageBytes);
+        tmem_cp_desc(tSfA, dsf);
+        tmem_cp_desc(tSfB, sdesc_adv(dsf, kAtomBytes));
+        const uint64_t da = sdesc_adv(dA0, s * C::kStageBytes), db = sdesc_adv(dB0, s * C::kStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // 32 keys per step: 32 rows of each operand
+          mma_mxf8_ss(tmem + C::kColDQ, sdesc_adv(da, kk * 4096), sdesc_adv(db, kk * 32 * D),
+                      make_idesc_mxf8(128, D, 1, 1, kk, kk), tSfA, tSfB, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar_empty[s]);
+      }
+      mma_commit(&bar_final);
+      mma_commit(&bar_drain);
+      mbar_wait(&bar_drain, 0, nullptr, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const int64_t qpos = static_cast<int64_t>(qt) * 128 + r;
+    bool ok = role_wait(&bar_final, 0, abort_flag, a.err, kErrTimeoutEpilogue);
+    if (__all_sync(0xffffffffu, ok)) {
+      tc_fence_after();
+      const int64_t t = doc_start + qpos;
+      __nv_bfloat16* dqrow = reinterpret_cast<__nv_bfloat16*>(a.dq_out) + (t * a.Hq + h) * D;
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t rr[32];
+        tmem_ld32(lane_base + C::kColDQ + c, rr);
+        tmem_ld_wait();
+        if (qpos < n) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(rr[i]) * a.alpha, __uint_as_float(rr[i + 1]) * a.alpha);
+            v.y = pack_bf16x2(__uint_as_float(rr[i + 2]) * a.alpha, __uint_as_float(rr[i + 3]) * a.alpha);
+            v.z = pack_bf16x2(__uint_as_float(rr[i + 4]) * a.alpha, __uint_as_float(rr[i + 5]) * a.alpha);
+            v.w = pack_bf16x2(__uint_as_float(rr[i + 6]) * a.alpha, __uint_as_float(rr[i + 7]) * a.alpha);
+            *reinterpret_cast<uint4*>(dqrow + c + i) = v;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+cudaError_t launch_dq_gemm(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
+  dim3 grid((max_seqlen + 127) / 128, a.num_docs, a.Hq);
+  if (d == 128) {
+    using C = DqGemmCfg<128>;
+    cudaError_t e = cudaFuncSetAttribute(attn_dq_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attn_dq_gemm_kernel<128><<<grid, C::kThreads, C::kSmemBytes, stream>>>(m, a);
+  } else {
+    using C = DqGemmCfg<64>;
+    cudaError_t e = cudaFuncSetAttribute(attn_dq_gemm_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attn_dq_gemm_kernel<64><<<grid, C::kThreads, C::kSmemBytes, stream>>>(m, a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace mxa

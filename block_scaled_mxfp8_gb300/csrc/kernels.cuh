@@ -80,6 +80,14 @@ struct BwdArgs {
   void* dk;              // bf16 [T, Hkv, d]
   void* dv;              // bf16 [T, Hkv, d]
   void* dq_out;          // bf16 [T, Hq, d] (written directly by the deterministic dQ kernel)
+  // dS emitted by the dK/dV kernel for the dQ product (null: the dQ kernel
+  // recomputes it).  Tile pair (h, document b, key tile kt, query tile qi)
+  // has index ((h * NT + TB_b + kt) * mt + qi): codes at 16 KB per pair, 128
+  // key rows of 128 query bytes; UE8M0 scales as one 512-byte atom per pair
+  // with rows = queries and groups = 32-key blocks.
+  uint8_t* ds_codes;
+  uint8_t* ds_sf;
+  int mt;                // max 128-token tiles of one document
   int dq_mode;
   int* err;
 };
@@ -114,6 +122,7 @@ struct FwdMaps {
 };
 struct BwdMaps {
   CUtensorMap q, k, v, g, qt, kt, gt;
+  CUtensorMap ds;  // 2-D map over the emitted dS codes: 128-byte rows, box 128 x 128
 };
 
 cudaError_t launch_quantize(const QuantArgs& a, int d, bool tokblock, bool hadamard, int max_groups,
@@ -121,6 +130,9 @@ cudaError_t launch_quantize(const QuantArgs& a, int d, bool tokblock, bool hadam
 cudaError_t launch_fwd(const FwdArgs& a, const FwdMaps& m, int d, int max_seqlen, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream);
 cudaError_t launch_bwd_split(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream);
+// dK/dV kernel emitting dS, then the dQ product over the emitted dS
+cudaError_t launch_bwd_emit(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream);
+cudaError_t launch_dq_gemm(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const PrepArgs& a, int max_seqlen, cudaStream_t stream);
 cudaError_t launch_dq_convert(const DqConvArgs& a, cudaStream_t stream);
 

@@ -28,7 +28,9 @@ void* g_scratch_addr[64];  // per device, resolved on the first call made with t
 extern "C" mxa_status mxa_bwd_noalloc(const mxa_bwd_params* p, cudaStream_t stream) {
   using namespace mxa;
   if (!p) return MXA_ERR_ARG;
-  const size_t need = mxa_bwd_workspace_bytes(p);
+  // the smallest workspace mxa_bwd accepts must fit; a call whose emitted dS
+  // also fits takes the faster dQ path inside mxa_bwd
+  const size_t need = mxa_bwd_workspace_min_bytes(p);
   if (need == 0) return MXA_ERR_ARG;
   if (need > MXA_BWD_NOALLOC_MAX_WORKSPACE) return MXA_ERR_WORKSPACE;
   int dev = -1;
@@ -44,7 +46,8 @@ extern "C" mxa_status mxa_bwd_noalloc(const mxa_bwd_params* p, cudaStream_t stre
     scratch = g_scratch_addr[dev];
   }
   // mxa_bwd writes every byte it later reads (D and LSE rows, pad rows
-  // included) and zeroes the fp16 dQ accumulator itself, so the contents a
-  // previous call left behind never leak into this one.
+  // included, the emitted dS of every visible tile pair) and zeroes the fp16
+  // dQ accumulator itself, so the contents a previous call left behind never
+  // leak into this one.
   return mxa_bwd(p, scratch, MXA_BWD_NOALLOC_MAX_WORKSPACE, stream);
 }

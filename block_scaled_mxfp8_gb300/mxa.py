@@ -89,7 +89,8 @@ _lib = None
 
 EXPORTS = [
     "mxa_abi_version", "mxa_status_str", "mxa_scale_tiles", "mxa_scale_tiles_bound", "mxa_scale_bytes",
-    "mxa_quantize", "mxa_fwd", "mxa_bwd_workspace_bytes", "mxa_bwd", "mxa_bwd_noalloc", "mxa_get_error",
+    "mxa_quantize", "mxa_fwd", "mxa_bwd_workspace_bytes", "mxa_bwd_workspace_min_bytes", "mxa_bwd",
+    "mxa_bwd_noalloc", "mxa_get_error",
 ]
 # include/mxa_testing.h: the kernels' P and dS quantization run on caller data
 EXPORTS_TESTING = ["mxa_test_e4m3", "mxa_test_ds_blocks"]
@@ -121,6 +122,8 @@ def lib():
         L.mxa_fwd.argtypes = [ctypes.POINTER(c_fwd_params), P]
         L.mxa_bwd_workspace_bytes.restype = ctypes.c_size_t
         L.mxa_bwd_workspace_bytes.argtypes = [ctypes.POINTER(c_bwd_params)]
+        L.mxa_bwd_workspace_min_bytes.restype = ctypes.c_size_t
+        L.mxa_bwd_workspace_min_bytes.argtypes = [ctypes.POINTER(c_bwd_params)]
         L.mxa_bwd.restype = i32
         L.mxa_bwd.argtypes = [ctypes.POINTER(c_bwd_params), P, ctypes.c_size_t, P]
         L.mxa_bwd_noalloc.restype = i32
@@ -192,6 +195,10 @@ def mxa_fwd(params: c_fwd_params, stream=None) -> int:
 
 def mxa_bwd_workspace_bytes(params: c_bwd_params) -> int:
     return int(lib().mxa_bwd_workspace_bytes(ctypes.byref(params)))
+
+
+def mxa_bwd_workspace_min_bytes(params: c_bwd_params) -> int:
+    return int(lib().mxa_bwd_workspace_min_bytes(ctypes.byref(params)))
 
 
 def mxa_bwd(params: c_bwd_params, workspace, ws_bytes: int, stream=None) -> int:

@@ -185,13 +185,28 @@ typedef struct {
   mxa_dq_mode dq_mode;
 } mxa_bwd_params;
 
-/* Workspace bytes mxa_bwd needs: D and LSE * log2(e), fp32, each padded to
- * whole 128-token tiles per document ([Hq, ntiles, 128]), plus (FP16_X512
- * mode) the fp16 dQ accumulator [T, Hq, d] rounded up to 256 bytes. */
+/* Workspace bytes of mxa_bwd's fastest path.
+ *   Both modes: D and LSE * log2(e), fp32, each padded to whole 128-token
+ *   tiles per document ([Hq, ntiles, 128]).
+ *   FP32 mode: plus the dS blocks the dK/dV pass emits for the dQ product --
+ *   E4M3 codes (16 KB) and one 512-byte scale atom per (query head, key tile,
+ *   query tile of the same document) pair, with mt = ceil(max document
+ *   length / 128) query-tile slots per key tile: Hq * ntiles * mt * 16896
+ *   bytes (B8 H32 L4096: 4.4 GB).
+ *   FP16_X512 mode: plus the fp16 dQ accumulator [T, Hq, d], rounded up to
+ *   256 bytes. */
 size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p);
 
-/* Backward.  workspace: device buffer of at least mxa_bwd_workspace_bytes()
- * bytes, 256-byte aligned; its contents on entry do not matter.
+/* Smallest workspace mxa_bwd accepts: the padded D and LSE rows, plus the
+ * fp16 accumulator in FP16_X512 mode.  An FP32-mode workspace smaller than
+ * mxa_bwd_workspace_bytes() selects a dQ kernel that forms dS again from S
+ * and dP instead of reading the emitted blocks (slower; same blocks, so the
+ * same tolerances). */
+size_t mxa_bwd_workspace_min_bytes(const mxa_bwd_params* p);
+
+/* Backward.  workspace: device buffer of ws_bytes >= mxa_bwd_workspace_min_bytes()
+ * bytes (mxa_bwd_workspace_bytes() for the fastest path), 256-byte aligned;
+ * its contents on entry do not matter.
  * Status: MXA_OK, MXA_ERR_ARG, MXA_ERR_ALIGN, MXA_ERR_UNSUPPORTED,
  * MXA_ERR_WORKSPACE, MXA_ERR_CUDA. */
 mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cudaStream_t stream);
@@ -209,10 +224,11 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
  * Same arguments, results and status codes as mxa_bwd, computed the same way;
  * the workspace is a file-scope device array of MXA_BWD_NOALLOC_MAX_WORKSPACE
  * bytes that the library owns (held on every GPU that loads the library until
- * the process exits).  Calls whose mxa_bwd_workspace_bytes() exceeds it are
- * rejected with MXA_ERR_WORKSPACE before any work; FP32-mode calls need
- * 2 * Hq * ntiles * 512 bytes (B8 H32 L4096: 8 MiB), FP16_X512 calls also need
- * the fp16 dQ accumulator, so only small ones fit.
+ * the process exits).  Calls whose mxa_bwd_workspace_min_bytes() exceeds it
+ * are rejected with MXA_ERR_WORKSPACE before any work; FP32-mode calls need
+ * 2 * Hq * ntiles * 512 bytes (B8 H32 L4096: 8 MiB) and take the fast dQ path
+ * only when their full mxa_bwd_workspace_bytes() also fits; FP16_X512 calls
+ * also need the fp16 dQ accumulator, so only small ones fit.
  * The device address of the array is resolved on the first call made with a
  * given device current (cudaGetSymbolAddress); make that first call before
  * any stream capture.  The function allocates nothing.  Every call on a device

@@ -131,10 +131,16 @@ def test_fwd_bwd_reject_bad_arguments_without_launch(lib):
     sh = mxa.c_shape(256, 2, 2, 128, None, 1, 256, 2, 1, 0.0)
     bp = mxa.c_bwd_params(sh, *[_qv()] * 7, 256, 256, 256, 256, 256, 0)
     need = L.mxa_bwd_workspace_bytes(ctypes.byref(bp))
-    assert need >= 2 * 256 * 4  # D [Hq, T] (fp32 mode sums dQ in tensor memory, no accumulator)
-    assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), need - 1, None) == mxa.MXA_ERR_WORKSPACE
+    need_min = L.mxa_bwd_workspace_min_bytes(ctypes.byref(bp))
+    # padded D and LSE rows [Hq, NT, 128] fp32; fp32 mode adds the emitted dS:
+    # one 16 KB code tile + one 512-byte scale atom per (head, key tile,
+    # query-tile slot) pair
+    assert need_min == 2 * 2 * 2 * 128 * 4
+    assert need == need_min + 2 * 2 * 2 * (16384 + 512)
+    assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), need_min - 1, None) == mxa.MXA_ERR_WORKSPACE
     assert L.mxa_bwd(ctypes.byref(bp), None, need, None) == mxa.MXA_ERR_WORKSPACE
     bp.dq_mode = 5
     assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), need, None) == mxa.MXA_ERR_ARG
     bp.dq_mode = 1
-    assert L.mxa_bwd_workspace_bytes(ctypes.byref(bp)) >= need + 256 * 2 * 128 * 2  # + fp16 dQ accumulator
+    # FP16 x 2^9 mode: the fp16 dQ accumulator instead of the emitted dS
+    assert L.mxa_bwd_workspace_bytes(ctypes.byref(bp)) == need_min + 256 * 2 * 128 * 2

@@ -51,3 +51,42 @@ def test_bwd_matches_oracle(w, mode):
     assert_close("dV", to_np(dv), r["dV"])
     assert_close("dK", to_np(dk), r["dK"])
     assert_close("dQ", to_np(dq), r["dQ"])
+
+
+RECOMPUTE_CASES = [
+    inp.workload("tiny", causal=True),
+    inp.make_custom("d128_ragged_gqa_causal", lengths=[1, 129, 300, 64, 7], Hq=4, Hkv=2, d=128, causal=True,
+                    seed=31),
+]
+
+
+@pytest.mark.parametrize("w", RECOMPUTE_CASES, ids=[c.name for c in RECOMPUTE_CASES])
+def test_bwd_min_workspace_forms_ds_again(w):
+    """FP32 mode with the smallest accepted workspace: the dQ kernel forms dS
+    from S and dP again instead of reading the blocks the dK/dV pass emitted.
+    Both paths quantize the same 32 x 32 blocks, so both meet the oracle bar,
+    and dK, dV (computed identically) are bit-identical."""
+    from block_scaled_mxfp8_gb300 import mxa
+
+    t = inp.tensors(w, with_grad=True)
+    geo, gv = gpu_views(w, t)
+    o, lse = mxa.fwd(gv["q"][0], gv["k"][0], gv["v"][1], geo, w.causal)
+    views = {"q_row": gv["q"][0], "k_row": gv["k"][0], "v_row": gv["v"][0], "g_row": gv["do"][0],
+             "q_tok": gv["q"][1], "k_tok": gv["k"][1], "g_tok": gv["do"][1]}
+    full = mxa.bwd(views, o, lse, geo, w.causal)
+    T, Hq, d = views["q_row"].codes.shape
+    Hkv = views["k_row"].codes.shape[1]
+    out = tuple(torch.empty((T, H, d), dtype=torch.bfloat16, device="cuda") for H in (Hq, Hkv, Hkv))
+    p = mxa.bwd_params(views, o, lse, *out, geo, w.causal)
+    need_min, need = mxa.mxa_bwd_workspace_min_bytes(p), mxa.mxa_bwd_workspace_bytes(p)
+    assert 0 < need_min < need
+    ws = torch.empty(need_min, dtype=torch.uint8, device="cuda")
+    assert mxa.mxa_bwd(p, ws, need_min) == mxa.MXA_OK
+    torch.cuda.synchronize()
+    mxa.check_error()
+    _, dd = oracle_views(w, t)
+    r = orc.attn_bwd(dd["q"]["row"], dd["k"]["row"], dd["v"]["tok"], dd["v"]["row"], dd["do"]["row"],
+                     dd["q"]["tok"], dd["k"]["tok"], dd["do"]["tok"], w.cu_seqlens.numpy(), w.causal,
+                     1.0 / math.sqrt(w.d))
+    assert_close("dQ (dS formed again)", to_np(out[0]), r["dQ"])
+    assert torch.equal(out[1], full[1]) and torch.equal(out[2], full[2])
