@@ -65,21 +65,6 @@ bool make_code_map(CUtensorMap* map, const void* codes, int64_t T, int H, int d)
   return r == CUDA_SUCCESS;
 }
 
-// 2-D map over the emitted dS codes: rows of 128 query bytes, one 128 x 128
-// tile per key-tile / query-tile pair, loaded with the 128-byte swizzle.
-bool make_ds_map(CUtensorMap* map, const void* codes, int64_t rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {128};
-  cuuint32_t box[2] = {128, 128};
-  cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(codes), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // Most 128-token tiles in one document.
@@ -93,10 +78,10 @@ size_t bwd_rows_bytes(const mxa_shape& s) {
   return 2 * static_cast<size_t>(s.Hq) * static_cast<size_t>(s.ntiles > 0 ? s.ntiles : 0) * 128 * 4;
 }
 
-// Bytes of the emitted dS (codes + one scale atom per tile pair).
+// Bytes of the emitted dS (16 KB of codes + 16 block scales per tile pair).
 size_t bwd_ds_bytes(const mxa_shape& s) {
   return static_cast<size_t>(s.Hq) * static_cast<size_t>(s.ntiles > 0 ? s.ntiles : 0) *
-         static_cast<size_t>(max_doc_tiles(s)) * (16384 + 512);
+         static_cast<size_t>(max_doc_tiles(s)) * (16384 + 16);
 }
 
 mxa_status check_view(const mxa_qview& v) {
@@ -356,8 +341,6 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
     if (ws_bytes >= mxa_bwd_workspace_bytes(p)) {
       a.ds_codes = static_cast<uint8_t*>(workspace) + dbytes;
       a.ds_sf = a.ds_codes + static_cast<size_t>(s.Hq) * static_cast<size_t>(s.ntiles) * a.mt * 16384;
-      if (!make_ds_map(&maps.ds, a.ds_codes, static_cast<int64_t>(s.Hq) * s.ntiles * a.mt * 128))
-        return MXA_ERR_CUDA;
       if (launch_bwd_emit(a, maps, s.d, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
       return MXA_OK;
     }

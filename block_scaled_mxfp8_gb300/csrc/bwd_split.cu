@@ -62,7 +62,11 @@ struct DkdvCfg {
   static constexpr int kOffRowsA = kOffB + kStagesB * 2 * kTileBytes;  // LSE rows, 512 B each
   static constexpr int kOffRowsB = kOffRowsA + kStagesA * 512;         // D rows
   static constexpr int kOffSf = kOffRowsB + kStagesB * 512;  // K, V, then 2 per A stage, 2 per B stage
-  static constexpr int kSmemBytes = kOffSf + (2 + 2 * kStagesA + 2 * kStagesB) * kAtomBytes + 1024;
+  // staging of the dS codes emitted for the dQ product: the 128 x 128 tile as
+  // the 128-byte-swizzled image a TMA load would produce, stored with one bulk
+  // copy and read back by the dQ kernel with one bulk copy
+  static constexpr int kOffDsStage = (kOffSf + (2 + 2 * kStagesA + 2 * kStagesB) * kAtomBytes + 1023) & ~1023;
+  static constexpr int kSmemBytes = kOffDsStage + 16384 + 1024;
 };
 
 template <int D>
@@ -261,8 +265,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         const uint64_t da = sdesc_adv(dA, sa * 2 * C::kTileBytes);  // Q, G of this unit
         const uint64_t db = sdesc_adv(dB, sb * 2 * C::kTileBytes);  // Qt, Gt of this unit
         // dP^T = V G^T once S^T has been read out of X; ring B (D row, Qt,
-        // Gt) must have landed before the softmax warps see dP^T
+        // Gt) must have landed before the softmax warps see dP^T, and the
+        // previous unit's staged dS must have been read before they see it
         if (!(ok = role_wait(&bar_x_free, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        if (a.ds_codes) bulk_store_wait_read();
         if (!(ok = role_wait(&bar_b_full[sb], (u / C::kStagesB) & 1, abort_flag, a.err, kErrTimeoutMma))) break;
         tc_fence_after();
         const uint32_t tSfG = tmem + C::kSfG + 4 * t;
@@ -287,6 +293,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         if (u + 1 < n_work && !(ok = issue_s(u + 1))) break;
         // dK += dS^T Q
         if (!(ok = role_wait(&bar_ds_ready, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        if (a.ds_codes) {  // the staged dS tile of this unit to the workspace
+          const int h = hk * grp + u / nq;
+          const int64_t pair = (static_cast<int64_t>(h) * a.ntiles + tile_base + kt) * a.mt + (qi0 + u % nq);
+          bulk_store(a.ds_codes + pair * 16384, smem + C::kOffDsStage, 16384);
+        }
         tc_fence_after();
         const uint32_t tSfQt = tmem + C::kSfQt + 4 * t;
         tmem_cp_desc(tSfQt, sdesc_adv(dSf, (2 + 2 * C::kStagesA + 2 * sb) * kAtomBytes));
@@ -299,6 +310,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       mma_commit(&bar_final);
       mma_commit(&bar_drain);
       mbar_wait(&bar_drain, 0, nullptr, 0);
+      if (a.ds_codes) bulk_store_wait_all();  // the last staged tile is out before the CTA exits
     }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ softmax / dS
@@ -391,14 +403,18 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         tmem_st1(lane_base + C::kSfDS + 4 * part + quad, eb | 0x7F7F7F00u);
         if (a.ds_codes) {
           // the same block for the dQ product: codes of key row j, queries
-          // [32 part, 32 part + 32); its scale at rows (queries) 32 part +
-          // lane, group quad of the pair's atom
-          const int h = hk * grp + u / nq;
-          const int64_t pair = (static_cast<int64_t>(h) * a.ntiles + tile_base + kt) * a.mt + qi;
-          uint4* dst = reinterpret_cast<uint4*>(a.ds_codes + pair * 16384 + j * 128 + 32 * part);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          a.ds_sf[pair * kAtomBytes + lane * 16 + part * 4 + quad] = static_cast<uint8_t>(eb);
+          // [32 part, 32 part + 32) -- 16-byte chunks 2 part, 2 part + 1 of
+          // the row, placed at chunk ^ (j & 7) (the 128-byte swizzle); its
+          // scale byte at 4 part + quad of the pair's 16 (query block major)
+          uint8_t* row = smem + C::kOffDsStage + j * 128;
+          *reinterpret_cast<uint4*>(row + (((2 * part) ^ (j & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(row + (((2 * part + 1) ^ (j & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+          fence_proxy_async_smem();  // the MMA thread's bulk store reads it
+          if (lane == 0) {
+            const int h = hk * grp + u / nq;
+            const int64_t pair = (static_cast<int64_t>(h) * a.ntiles + tile_base + kt) * a.mt + qi;
+            a.ds_sf[pair * 16 + part * 4 + quad] = static_cast<uint8_t>(eb);
+          }
         }
       }
       tmem_st_wait();

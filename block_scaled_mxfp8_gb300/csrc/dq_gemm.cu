@@ -7,9 +7,12 @@
 // block-scaled GEMM per (128-query tile, query head, document), summed over
 // the visible key tiles in TMEM in a fixed order (deterministic, no atomics):
 //   A = dS   [128 queries x 128 keys]: the stored tile has key rows of query
-//            bytes, i.e. an MN-major A operand, loaded by TMA with the 128-byte
-//            swizzle; its scales (rows = queries, groups = key blocks) come
-//            as one 512-byte atom per tile pair;
+//            bytes, i.e. an MN-major A operand, kept as the image of its
+//            128-byte-swizzled shared-memory layout so that one bulk copy
+//            loads it; its 16 block scales come as 16 bytes per tile pair and
+//            the epilogue warps (idle until the end) spread them into the
+//            scale-factor layout in TMEM, each warp its quarter of the query
+//            rows;
 //   B = K    TOK view (rows = channels, groups = 32-key blocks), MN-major.
 // Warps: 0 = TMA producer, 1 = TMEM owner and MMA issuer, 2..5 = epilogue.
 #include <cuda_bf16.h>
@@ -27,12 +30,14 @@ struct DqGemmCfg {
   static constexpr int kTileBytes = 128 * D;  // one Kt tile
   static constexpr uint32_t kSwz = D == 128 ? kSwz128 : kSwz64;
   static constexpr uint32_t kSBO = 8 * D;
-  // TMEM: dQ accumulator [0, D), then dS and K scale slots (4 columns each,
-  // alternating by tile parity)
-  static constexpr uint32_t kColDQ = 0, kSfDS = D /*+4t*/, kSfKt = D + 8 /*+4t*/;
+  // TMEM: dQ accumulator [0, D), then dS and K scale slots, 4 columns per
+  // pipeline stage
+  static constexpr uint32_t kColDQ = 0, kSfDS = D /*+4s*/, kSfKt = D + 16 /*+4s*/;
   static constexpr uint32_t kTmemCols = D == 128 ? 256 : 128;
-  // shared memory per stage: dS tile (16 KB), Kt tile, dS atom, Kt atom
-  static constexpr int kStageBytes = 16384 + kTileBytes + 2 * kAtomBytes;
+  // shared memory per stage: dS tile (16 KB), Kt tile, Kt atom, 16 dS block
+  // scales (padded so stages stay 1024-byte aligned)
+  static constexpr int kOffKt = 16384, kOffKtSf = 16384 + kTileBytes, kOffDsSf = kOffKtSf + kAtomBytes;
+  static constexpr int kStageBytes = 16384 + kTileBytes + 1024;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
 };
 
@@ -44,7 +49,7 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 1)
   using C = DqGemmCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_full[C::kStages], bar_empty[C::kStages], bar_final, bar_drain;
+  __shared__ uint64_t bar_full[C::kStages], bar_empty[C::kStages], bar_sfa[C::kStages], bar_final, bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int64_t s_slot;
@@ -64,6 +69,7 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 1)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
+      mbar_init(&bar_sfa[s], 128);  // the four epilogue warps
     }
     mbar_init(&bar_final, 1);
     mbar_init(&bar_drain, 1);
@@ -94,11 +100,11 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 1)
         const int k0 = static_cast<int>(doc_start + static_cast<int64_t>(j) * 128);
         const int64_t katom = (static_cast<int64_t>(hk) * a.ntiles + tile_base + j) * kAtomBytes;
         uint8_t* st = smem + s * C::kStageBytes;
-        mbar_arrive_expect_tx(&bar_full[s], 16384 + C::kTileBytes + 2 * kAtomBytes);
-        tma_load_2d(st, &maps.ds, &bar_full[s], 0, static_cast<int>(pair * 128));
-        tma_load_3d(st + 16384, &maps.kt, &bar_full[s], 0, hk, k0);
-        bulk_load(st + 16384 + C::kTileBytes, a.ds_sf + pair * kAtomBytes, kAtomBytes, &bar_full[s]);
-        bulk_load(st + 16384 + C::kTileBytes + kAtomBytes, a.kt_sf + katom, kAtomBytes, &bar_full[s]);
+        mbar_arrive_expect_tx(&bar_full[s], 16384 + C::kTileBytes + kAtomBytes + 16);
+        bulk_load(st, a.ds_codes + pair * 16384, 16384, &bar_full[s]);  // stored as its swizzled image
+        tma_load_3d(st + C::kOffKt, &maps.kt, &bar_full[s], 0, hk, k0);
+        bulk_load(st + C::kOffKtSf, a.kt_sf + katom, kAtomBytes, &bar_full[s]);
+        bulk_load(st + C::kOffDsSf, a.ds_sf + pair * 16, 16, &bar_full[s]);
         issued = j + 1;
       }
       for (int j = (issued > C::kStages ? issued - C::kStages : 0); j < issued; ++j)
@@ -108,17 +114,17 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 1)
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       const uint64_t dA0 = make_sdesc(smem_u32(smem), 16, 1024, kSwz128);           // dS: 128-byte query rows
-      const uint64_t dB0 = make_sdesc(smem_u32(smem + 16384), 16, C::kSBO, C::kSwz);  // Kt
-      const uint64_t dSf0 = atom_desc(smem + 16384 + C::kTileBytes);
+      const uint64_t dB0 = make_sdesc(smem_u32(smem + C::kOffKt), 16, C::kSBO, C::kSwz);  // Kt
+      const uint64_t dSf0 = atom_desc(smem + C::kOffKtSf);
       bool ok = true;
       for (int j = 0; j < n_kt; ++j) {
-        const int s = j % C::kStages, t = j & 1;
+        const int s = j % C::kStages;
+        // operands landed and the epilogue warps have laid out the dS scales
         if (!(ok = role_wait(&bar_full[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        if (!(ok = role_wait(&bar_sfa[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma))) break;
         tc_fence_after();
-        const uint32_t tSfA = tmem + C::kSfDS + 4 * t, tSfB = tmem + C::kSfKt + 4 * t;
-        const uint64_t dsf = sdesc_adv(dSf0, s * C::kStageBytes);
-        tmem_cp_desc(tSfA, dsf);
-        tmem_cp_desc(tSfB, sdesc_adv(dsf, kAtomBytes));
+        const uint32_t tSfA = tmem + C::kSfDS + 4 * s, tSfB = tmem + C::kSfKt + 4 * s;
+        tmem_cp_desc(tSfB, sdesc_adv(dSf0, s * C::kStageBytes));
         const uint64_t da = sdesc_adv(dA0, s * C::kStageBytes), db = sdesc_adv(dB0, s * C::kStageBytes);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // 32 keys per step: 32 rows of each operand
@@ -136,7 +142,22 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 1)
     const int r = quad * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const int64_t qpos = static_cast<int64_t>(qt) * 128 + r;
-    bool ok = role_wait(&bar_final, 0, abort_flag, a.err, kErrTimeoutEpilogue);
+    // per key tile: the scales of this warp's 32 query rows (query block
+    // `quad`) for the 4 key blocks go to lane r, column kSfDS + 4 s + r / 32,
+    // byte = key block -- the A scale-factor layout of the MMA.  Stage s was
+    // reloaded only after the MMAs of tile j - kStages completed, so its
+    // slot is free.
+    bool ok = true;
+    for (int j = 0; j < n_kt; ++j) {
+      const int s = j % C::kStages;
+      if (!(ok = warp_wait(&bar_full[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutEpilogue))) break;
+      const uint32_t sc = *reinterpret_cast<const uint32_t*>(smem + s * C::kStageBytes + C::kOffDsSf + 4 * quad);
+      tmem_st1(lane_base + C::kSfDS + 4 * s + quad, sc);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar_sfa[s]);
+    }
+    if (ok) ok = role_wait(&bar_final, 0, abort_flag, a.err, kErrTimeoutEpilogue);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       const int64_t t = doc_start + qpos;

@@ -83,8 +83,10 @@ struct BwdArgs {
   // dS emitted by the dK/dV kernel for the dQ product (null: the dQ kernel
   // recomputes it).  Tile pair (h, document b, key tile kt, query tile qi)
   // has index ((h * NT + TB_b + kt) * mt + qi): codes at 16 KB per pair, 128
-  // key rows of 128 query bytes; UE8M0 scales as one 512-byte atom per pair
-  // with rows = queries and groups = 32-key blocks.
+  // key rows of 128 query bytes kept as their 128-byte-swizzled shared-memory
+  // image (16-byte chunk c of row r at chunk c ^ (r % 8)); the 16 UE8M0 block
+  // scales of a pair at 16 bytes per pair, byte 4 * (query block) + (key
+  // block).
   uint8_t* ds_codes;
   uint8_t* ds_sf;
   int mt;                // max 128-token tiles of one document
@@ -122,7 +124,6 @@ struct FwdMaps {
 };
 struct BwdMaps {
   CUtensorMap q, k, v, g, qt, kt, gt;
-  CUtensorMap ds;  // 2-D map over the emitted dS codes: 128-byte rows, box 128 x 128
 };
 
 cudaError_t launch_quantize(const QuantArgs& a, int d, bool tokblock, bool hadamard, int max_groups,

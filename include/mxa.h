@@ -189,10 +189,10 @@ typedef struct {
  *   Both modes: D and LSE * log2(e), fp32, each padded to whole 128-token
  *   tiles per document ([Hq, ntiles, 128]).
  *   FP32 mode: plus the dS blocks the dK/dV pass emits for the dQ product --
- *   E4M3 codes (16 KB) and one 512-byte scale atom per (query head, key tile,
- *   query tile of the same document) pair, with mt = ceil(max document
- *   length / 128) query-tile slots per key tile: Hq * ntiles * mt * 16896
- *   bytes (B8 H32 L4096: 4.4 GB).
+ *   E4M3 codes (16 KB) and the 16 UE8M0 block scales per (query head, key
+ *   tile, query tile of the same document) pair, with mt = ceil(max document
+ *   length / 128) query-tile slots per key tile: Hq * ntiles * mt * 16400
+ *   bytes (B8 H32 L4096: 4.3 GB).
  *   FP16_X512 mode: plus the fp16 dQ accumulator [T, Hq, d], rounded up to
  *   256 bytes. */
 size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p);

@@ -133,10 +133,10 @@ def test_fwd_bwd_reject_bad_arguments_without_launch(lib):
     need = L.mxa_bwd_workspace_bytes(ctypes.byref(bp))
     need_min = L.mxa_bwd_workspace_min_bytes(ctypes.byref(bp))
     # padded D and LSE rows [Hq, NT, 128] fp32; fp32 mode adds the emitted dS:
-    # one 16 KB code tile + one 512-byte scale atom per (head, key tile,
-    # query-tile slot) pair
+    # one 16 KB code tile + 16 block scales per (head, key tile, query-tile
+    # slot) pair
     assert need_min == 2 * 2 * 2 * 128 * 4
-    assert need == need_min + 2 * 2 * 2 * (16384 + 512)
+    assert need == need_min + 2 * 2 * 2 * (16384 + 16)
     assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), need_min - 1, None) == mxa.MXA_ERR_WORKSPACE
     assert L.mxa_bwd(ctypes.byref(bp), None, need, None) == mxa.MXA_ERR_WORKSPACE
     bp.dq_mode = 5
