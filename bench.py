@@ -118,8 +118,11 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def flops(B, H, L, d, causal):
-    f = 4.0 * B * H * L * L * d
+def flops(B, H, L, d, causal, lengths=None):
+    """FLOP convention of the pages: forward 4 * H * d * sum_b n_b^2 (B * L^2 for
+    equal lengths), halved when causal; backward 2.5 x forward."""
+    sq = float(sum(int(n) * int(n) for n in lengths)) if lengths is not None else float(B) * L * L
+    f = 4.0 * H * sq * d
     if causal:
         f *= 0.5
     return f, 2.5 * f
@@ -173,7 +176,7 @@ def run_gpu(args):
         dist.init_process_group("nccl")
     mbuild.build()
 
-    w = inp.workload(args.workload, causal=args.causal)
+    w = inp.workload(args.workload, causal=True if args.causal else None)
     if args.batch:  # smaller batch of the same per-document shape (profiler captures)
         if w.lengths is not None:
             raise SystemExit("--batch applies to batched workloads only")
@@ -246,7 +249,7 @@ def run_gpu(args):
     ms_fwd = statistics.mean(r[1].elapsed_time(r[2]) for r in recs)
     ms_bwd = statistics.mean(r[2].elapsed_time(r[3]) for r in recs)  # includes the dO quantize
 
-    ffwd, fbwd = flops(B, Hq, L, d, w.causal)
+    ffwd, fbwd = flops(B, Hq, L, d, w.causal, w.lengths)
     step_flop = ffwd + fbwd
     value = world * step_flop / (ms_step * 1e-3) / 1e15
 
@@ -353,7 +356,7 @@ def run_reference(args):
         return
     from block_scaled_mxfp8_gb300 import inputs as inp
 
-    w = inp.workload(args.workload, causal=args.causal)
+    w = inp.workload(args.workload, causal=True if args.causal else None)
     L = min(w.L, 2048)
     total, fl_total, thr = 0.0, 0.0, 1
     for i in range(args.warmup + args.steps):
