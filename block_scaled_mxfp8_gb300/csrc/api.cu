@@ -84,6 +84,20 @@ size_t bwd_ds_bytes(const mxa_shape& s) {
          static_cast<size_t>(max_doc_tiles(s)) * (16384 + 16);
 }
 
+// Bytes of the cost-sorted tile lists of this shape.
+size_t lists_bytes(const mxa_shape& s) {
+  return tile_list_bytes(s.num_docs, s.ntiles > 0 ? s.ntiles : 0);
+}
+
+// Whether the attention kernels take their CTAs from the tile lists: packed
+// documents (equal documents fill the max_seqlen grid exactly, in the same
+// order), no document longer than the list builder's limit, and a grid of
+// NT x heads CTAs that fits one dimension.
+bool uses_list(const mxa_shape& s) {
+  return s.cu_seqlens != nullptr && tile_lists_supported(static_cast<int>(max_doc_tiles(s))) &&
+         s.ntiles * static_cast<int64_t>(s.Hq) <= 0x7FFFFFFFll;
+}
+
 mxa_status check_view(const mxa_qview& v) {
   if (!v.codes || !v.scales) return MXA_ERR_ARG;
   if (!aligned(v.codes, 16) || !aligned(v.scales, 16)) return MXA_ERR_ALIGN;
@@ -203,6 +217,11 @@ mxa_status mxa_quantize(const void* x, int64_t T, int H, int d, const int32_t* c
   return MXA_OK;
 }
 
+size_t mxa_fwd_workspace_bytes(const mxa_fwd_params* p) {
+  if (!p || check_shape(p->shape) != MXA_OK || !uses_list(p->shape)) return 0;
+  return lists_bytes(p->shape);
+}
+
 mxa_status mxa_fwd(const mxa_fwd_params* p, cudaStream_t stream) {
   if (!p) return MXA_ERR_ARG;
   const mxa_shape& s = p->shape;
@@ -213,6 +232,8 @@ mxa_status mxa_fwd(const mxa_fwd_params* p, cudaStream_t stream) {
     return st;
   if (!p->o || !p->lse) return MXA_ERR_ARG;
   if (!aligned(p->o, 16) || !aligned(p->lse, 4)) return MXA_ERR_ALIGN;
+  const bool use_list = p->workspace && uses_list(s) && p->workspace_bytes >= lists_bytes(s);
+  if (use_list && !aligned(p->workspace, 256)) return MXA_ERR_ALIGN;
   if (s.T == 0) return MXA_OK;
   FwdMaps maps;
   if (!make_code_map(&maps.q, p->q_row.codes, s.T, s.Hq, s.d) ||
@@ -236,6 +257,13 @@ mxa_status mxa_fwd(const mxa_fwd_params* p, cudaStream_t stream) {
   a.lse = p->lse;
   a.err = device_error_word();
   const int maxlen = s.cu_seqlens ? s.max_seqlen : static_cast<int>(s.T / s.num_docs);
+  if (use_list) {
+    if (launch_tile_lists(s.cu_seqlens, s.num_docs, s.T, a.causal, static_cast<int>(max_doc_tiles(s)), s.ntiles,
+                          p->workspace, stream) != cudaSuccess)
+      return MXA_ERR_CUDA;
+    a.items = tile_list_q(p->workspace);
+    a.item_count = static_cast<const int32_t*>(p->workspace);
+  }
   if (launch_fwd(a, maps, s.d, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
   return MXA_OK;
 }
@@ -246,7 +274,7 @@ size_t mxa_bwd_workspace_min_bytes(const mxa_bwd_params* p) {
                d = static_cast<size_t>(p->shape.d);
   // FP16 x 2^9 mode adds its fp16 partial-sum accumulator [T, Hq, d]
   const size_t acc = p->dq_mode == MXA_DQ_FP16_X512 ? T * Hq * d * 2 : 0;
-  return bwd_rows_bytes(p->shape) + ((acc + 255) & ~size_t(255));
+  return bwd_rows_bytes(p->shape) + lists_bytes(p->shape) + ((acc + 255) & ~size_t(255));
 }
 
 size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p) {
@@ -285,7 +313,9 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   const size_t dbytes = 2 * pad_elems * 4;
   float* dpad = static_cast<float*>(workspace);
   float* lpad = dpad + pad_elems;
-  void* acc = static_cast<uint8_t*>(workspace) + dbytes;
+  void* lists = static_cast<uint8_t*>(workspace) + dbytes;
+  const size_t lbytes = lists_bytes(s);
+  void* acc = static_cast<uint8_t*>(lists) + lbytes;
   const bool fp16 = p->dq_mode == MXA_DQ_FP16_X512;
   const size_t acc_bytes = fp16 ? T * Hq * d * 2 : 0;
   const int maxlen = s.cu_seqlens ? s.max_seqlen : static_cast<int>(s.T / s.num_docs);
@@ -334,12 +364,19 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   a.dq_out = p->dq;
   a.err = device_error_word();
   a.mt = static_cast<int>(max_doc_tiles(s));
+  if (!fp16 && uses_list(s)) {
+    if (launch_tile_lists(s.cu_seqlens, s.num_docs, s.T, a.causal, a.mt, s.ntiles, lists, stream) != cudaSuccess)
+      return MXA_ERR_CUDA;
+    a.q_items = tile_list_q(lists);
+    a.k_items = tile_list_k(lists, s.ntiles);
+    a.item_count = static_cast<const int32_t*>(lists);
+  }
   if (!fp16) {
     // FP32: dK/dV kernel, then dQ summed in TMEM in a fixed order -- over the
     // dS the dK/dV kernel emitted when the workspace holds it, else by a
     // kernel that forms dS again
     if (ws_bytes >= mxa_bwd_workspace_bytes(p)) {
-      a.ds_codes = static_cast<uint8_t*>(workspace) + dbytes;
+      a.ds_codes = static_cast<uint8_t*>(acc);
       a.ds_sf = a.ds_codes + static_cast<size_t>(s.Hq) * static_cast<size_t>(s.ntiles) * a.mt * 16384;
       if (launch_bwd_emit(a, maps, s.d, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
       return MXA_OK;

@@ -45,6 +45,20 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
+// Work item of this CTA from a cost-sorted tile list: CTA i takes item i / H
+// for head i % H; false when i / H is past the list's end.
+__device__ __forceinline__ bool list_item(const TileItem* items, const int32_t* count, int H, int& b, int& h,
+                                          int& tile, int64_t& tile_base) {
+  const int i = static_cast<int>(blockIdx.x) / H;
+  h = static_cast<int>(blockIdx.x) - i * H;
+  if (i >= __ldg(count)) return false;
+  const int4 it = __ldg(reinterpret_cast<const int4*>(items + i));
+  b = it.x;
+  tile = it.y;
+  tile_base = it.z;
+  return true;
+}
+
 // One 512-byte scale atom (128 rows x 4 groups) from shared memory into 4
 // TMEM columns, replicated into the four 32-lane quadrants.
 __device__ __forceinline__ uint64_t atom_desc(const void* smem_atom) {

@@ -122,7 +122,15 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   __shared__ int64_t s_slot;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int kt = blockIdx.x, b = blockIdx.y, hk = blockIdx.z;
+  int kt, b, hk;
+  int64_t tile_base = -1;
+  if (a.k_items) {
+    if (!list_item(a.k_items, a.item_count, a.Hkv, b, hk, kt, tile_base)) return;
+  } else {
+    kt = blockIdx.x;
+    b = blockIdx.y;
+    hk = blockIdx.z;
+  }
   const int grp = a.Hq / a.Hkv;
   int64_t doc_start, n;
   doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
@@ -131,7 +139,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   const int qi0 = a.causal ? kt : 0;
   const int nq = n_tiles - qi0;
   const int n_work = nq * grp;
-  const int64_t tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, kSplitThreads, &s_slot);
+  if (tile_base < 0) tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, kSplitThreads, &s_slot);
 
   if (tid == 0) {
     mbar_init(&bar_kv, 1);
@@ -472,15 +480,22 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   __shared__ int64_t s_slot;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.y, h = blockIdx.z;
+  int b, h, qt;
+  int64_t tile_base = -1;
+  if (a.q_items) {
+    if (!list_item(a.q_items, a.item_count, a.Hq, b, h, qt, tile_base)) return;
+  } else {
+    b = blockIdx.y;
+    h = blockIdx.z;
+    qt = a.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+  }
   const int hk = h / (a.Hq / a.Hkv);
   int64_t doc_start, n;
   doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
   const int n_tiles = static_cast<int>((n + 127) / 128);
-  const int qt = a.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
   if (qt >= n_tiles) return;
   const int n_kt = a.causal ? qt + 1 : n_tiles;
-  const int64_t tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, kSplitThreads, &s_slot);
+  if (tile_base < 0) tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, kSplitThreads, &s_slot);
 
   if (tid == 0) {
     mbar_init(&bar_q, 1);
@@ -701,7 +716,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 
 cudaError_t launch_bwd_split(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
   const int tiles = (max_seqlen + 127) / 128;
-  dim3 g1(tiles, a.num_docs, a.Hkv), g2(tiles, a.num_docs, a.Hq);
+  const dim3 g1 = a.k_items ? dim3(static_cast<unsigned>(a.ntiles * a.Hkv)) : dim3(tiles, a.num_docs, a.Hkv);
+  const dim3 g2 = a.q_items ? dim3(static_cast<unsigned>(a.ntiles * a.Hq)) : dim3(tiles, a.num_docs, a.Hq);
   cudaError_t e;
   if (d == 128) {
     e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -727,7 +743,7 @@ cudaError_t launch_bwd_split(const BwdArgs& a, const BwdMaps& m, int d, int max_
 
 cudaError_t launch_bwd_emit(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
   const int tiles = (max_seqlen + 127) / 128;
-  dim3 g1(tiles, a.num_docs, a.Hkv);
+  const dim3 g1 = a.k_items ? dim3(static_cast<unsigned>(a.ntiles * a.Hkv)) : dim3(tiles, a.num_docs, a.Hkv);
   cudaError_t e;
   if (d == 128) {
     e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,

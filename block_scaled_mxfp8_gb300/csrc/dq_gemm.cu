@@ -55,15 +55,22 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 1)
   __shared__ int64_t s_slot;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.y, h = blockIdx.z;
+  int b, h, qt;
+  int64_t tile_base = -1;
+  if (a.q_items) {
+    if (!list_item(a.q_items, a.item_count, a.Hq, b, h, qt, tile_base)) return;
+  } else {
+    b = blockIdx.y;
+    h = blockIdx.z;
+    qt = a.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+  }
   const int hk = h / (a.Hq / a.Hkv);
   int64_t doc_start, n;
   doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
   const int n_tiles = static_cast<int>((n + 127) / 128);
-  const int qt = a.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
   if (qt >= n_tiles) return;
   const int n_kt = a.causal ? qt + 1 : n_tiles;
-  const int64_t tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, C::kThreads, &s_slot);
+  if (tile_base < 0) tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, C::kThreads, &s_slot);
 
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -190,7 +197,8 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 1)
 }
 
 cudaError_t launch_dq_gemm(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
-  dim3 grid((max_seqlen + 127) / 128, a.num_docs, a.Hq);
+  const dim3 grid = a.q_items ? dim3(static_cast<unsigned>(a.ntiles * a.Hq))
+                              : dim3((max_seqlen + 127) / 128, a.num_docs, a.Hq);
   if (d == 128) {
     using C = DqGemmCfg<128>;
     cudaError_t e = cudaFuncSetAttribute(attn_dq_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,

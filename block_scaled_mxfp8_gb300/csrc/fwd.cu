@@ -3,10 +3,11 @@
 // One CTA computes one 128-query tile of one (document, query head), walking
 // the visible keys 256 at a time:
 //   S_j  = Q K_j^T          block-scaled MXFP8 MMA (kind::mxf8f6f4), M = 128
-//                           queries, N = 256 keys (the tensor core's cadence
-//                           is ~one instruction per 128 clocks whatever N <=
-//                           256 is, so N = 256 halves the cost per key), Q/K
-//                           ROW-view scales in TMEM;
+//                           queries, N = 256 keys (per key, half the MMA
+//                           groups, barrier round trips and pipe drains of
+//                           N = 128; a double-buffered N = 128 variant
+//                           measured 1.36x slower), Q/K ROW-view scales in
+//                           TMEM;
 //   P_j  = online softmax of alpha * S_j with a lazily updated row max
 //          (rescale only when the tile max exceeds the running max by more
 //          than tau = 4 in log2 units), quantized in registers as E4M3(2^4 p)
@@ -106,18 +107,25 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   __shared__ int64_t s_slot;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.y, h = blockIdx.z;
+  int b, h, qt;
+  int64_t tile_base = -1;
+  if (a.items) {
+    if (!list_item(a.items, a.item_count, a.Hq, b, h, qt, tile_base)) return;
+  } else {
+    // heaviest query tiles first when causal
+    b = blockIdx.y;
+    h = blockIdx.z;
+    qt = a.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+  }
   const int hk = h / (a.Hq / a.Hkv);
   int64_t doc_start, n;
   doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
   const int nq_tiles = static_cast<int>((n + 127) / 128);
-  // heaviest query tiles first when causal
-  const int qt = a.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
   if (qt >= nq_tiles) return;
   // visible keys [0, nkeys), walked 256 at a time
   const int64_t nkeys = a.causal ? min(n, static_cast<int64_t>(qt + 1) * 128) : n;
   const int n_it = static_cast<int>((nkeys + 255) / 256);
-  const int64_t tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, C::kThreads, &s_slot);
+  if (tile_base < 0) tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, C::kThreads, &s_slot);
 
   if (tid == 0) {
     mbar_init(&bar_q, 1);
@@ -458,7 +466,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, const FwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
-  dim3 grid((max_seqlen + 127) / 128, a.num_docs, a.Hq);
+  const dim3 grid = a.items ? dim3(static_cast<unsigned>(a.ntiles * a.Hq))
+                            : dim3((max_seqlen + 127) / 128, a.num_docs, a.Hq);
   if (d == 128) {
     using C = FwdCfg<128>;
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);

@@ -26,6 +26,26 @@ __device__ __forceinline__ void doc_bounds(const int32_t* cu, int num_docs, int6
   }
 }
 
+// One work item of the cost-sorted tile lists: (document, 128-token tile,
+// first scale tile of the document, cost in 128-key tiles visited).
+struct alignas(16) TileItem {
+  int32_t doc, tile, tile_base, cost;
+};
+constexpr int kTileListHeader = 256;     // the item count, padded
+constexpr int kTileListMaxCost = 4094;   // most tiles per document the list builder handles
+
+// Bytes of the lists for num_docs documents and NT = ntiles (256-byte multiple).
+size_t tile_list_bytes(int num_docs, int64_t ntiles);
+bool tile_lists_supported(int max_tiles);
+// Build both lists into ws (one CTA; stream-ordered).
+cudaError_t launch_tile_lists(const int32_t* cu, int num_docs, int64_t T, int causal, int max_tiles, int64_t ntiles,
+                              void* ws, cudaStream_t stream);
+// The query list and the key list inside a list workspace.
+inline const TileItem* tile_list_q(const void* ws) {
+  return reinterpret_cast<const TileItem*>(static_cast<const uint8_t*>(ws) + kTileListHeader);
+}
+inline const TileItem* tile_list_k(const void* ws, int64_t ntiles) { return tile_list_q(ws) + ntiles; }
+
 struct QuantArgs {
   const void* x;  // bf16 [T, H, d]
   int64_t T;
@@ -55,6 +75,10 @@ struct FwdArgs {
   void* o;              // bf16 [T, Hq, d]
   float* lse;           // [Hq, T]
   int* err;
+  // cost-sorted query-tile list (null: one CTA per (tile slot, document,
+  // head) of the max_seqlen grid); CTA i takes item i / Hq for head i % Hq
+  const TileItem* items;
+  const int32_t* item_count;
 };
 
 struct BwdArgs {
@@ -92,6 +116,12 @@ struct BwdArgs {
   int mt;                // max 128-token tiles of one document
   int dq_mode;
   int* err;
+  // cost-sorted tile lists (null: max_seqlen grids); CTA i of the dK/dV
+  // kernel takes key item i / Hkv for KV head i % Hkv, the dQ kernels query
+  // item i / Hq for head i % Hq
+  const TileItem* q_items;
+  const TileItem* k_items;
+  const int32_t* item_count;
 };
 
 struct PrepArgs {

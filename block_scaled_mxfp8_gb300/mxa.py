@@ -63,6 +63,8 @@ class c_fwd_params(ctypes.Structure):
         ("v_tok", c_qview),
         ("o", ctypes.c_void_p),
         ("lse", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
     ]
 
 
@@ -89,7 +91,7 @@ _lib = None
 
 EXPORTS = [
     "mxa_abi_version", "mxa_status_str", "mxa_scale_tiles", "mxa_scale_tiles_bound", "mxa_scale_bytes",
-    "mxa_quantize", "mxa_fwd", "mxa_bwd_workspace_bytes", "mxa_bwd_workspace_min_bytes", "mxa_bwd",
+    "mxa_quantize", "mxa_fwd", "mxa_fwd_workspace_bytes", "mxa_bwd_workspace_bytes", "mxa_bwd_workspace_min_bytes", "mxa_bwd",
     "mxa_bwd_noalloc", "mxa_get_error",
 ]
 # include/mxa_testing.h: the kernels' P and dS quantization run on caller data
@@ -120,6 +122,8 @@ def lib():
                                    ctypes.POINTER(c_qview), ctypes.POINTER(c_qview), P]
         L.mxa_fwd.restype = i32
         L.mxa_fwd.argtypes = [ctypes.POINTER(c_fwd_params), P]
+        L.mxa_fwd_workspace_bytes.restype = ctypes.c_size_t
+        L.mxa_fwd_workspace_bytes.argtypes = [ctypes.POINTER(c_fwd_params)]
         L.mxa_bwd_workspace_bytes.restype = ctypes.c_size_t
         L.mxa_bwd_workspace_bytes.argtypes = [ctypes.POINTER(c_bwd_params)]
         L.mxa_bwd_workspace_min_bytes.restype = ctypes.c_size_t
@@ -191,6 +195,10 @@ def mxa_quantize(x, T, H, d, cu_seqlens, num_docs, max_seqlen, ntiles, mode, vie
 
 def mxa_fwd(params: c_fwd_params, stream=None) -> int:
     return lib().mxa_fwd(ctypes.byref(params), _stream(stream))
+
+
+def mxa_fwd_workspace_bytes(params: c_fwd_params) -> int:
+    return int(lib().mxa_fwd_workspace_bytes(ctypes.byref(params)))
 
 
 def mxa_bwd_workspace_bytes(params: c_bwd_params) -> int:
@@ -291,8 +299,10 @@ def _shape(geo: Geometry, Hq: int, Hkv: int, d: int, causal: bool, softmax_scale
 
 
 def fwd(q_row: QView, k_row: QView, v_tok: QView, geo: Geometry, causal: bool, softmax_scale: float = 0.0,
-        out=None, stream=None):
-    """-> (O bf16 [T, Hq, d], LSE fp32 [Hq, T])."""
+        out=None, stream=None, workspace=None, use_list: bool = True):
+    """-> (O bf16 [T, Hq, d], LSE fp32 [Hq, T]).  With use_list (default) the
+    CTAs are scheduled from the cost-sorted tile list, in `workspace` when it
+    is large enough, else in a fresh device buffer."""
     T, Hq, d = q_row.codes.shape
     Hkv = k_row.codes.shape[1]
     if out is None:
@@ -301,7 +311,13 @@ def fwd(q_row: QView, k_row: QView, v_tok: QView, geo: Geometry, causal: bool, s
     else:
         o, lse = out
     p = c_fwd_params(_shape(geo, Hq, Hkv, d, causal, softmax_scale), q_row.c(), k_row.c(), v_tok.c(),
-                     o.data_ptr(), lse.data_ptr())
+                     o.data_ptr(), lse.data_ptr(), None, 0)
+    need = mxa_fwd_workspace_bytes(p) if use_list else 0
+    if need:
+        if workspace is None or workspace.numel() < need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q_row.codes.device)
+        p.workspace = workspace.data_ptr()
+        p.workspace_bytes = workspace.numel()
     _check(mxa_fwd(p, stream), "mxa_fwd")
     return o, lse
 

@@ -71,7 +71,7 @@
 extern "C" {
 #endif
 
-#define MXA_ABI_VERSION 1
+#define MXA_ABI_VERSION 2
 
 typedef enum {
   MXA_OK = 0,
@@ -163,7 +163,21 @@ typedef struct {
   mxa_qview v_tok;  /* V, TOK view (P V) */
   void* o;          /* out: bf16 [T, Hq, d] */
   float* lse;       /* out: fp32 [Hq, T], natural-log LSE (alpha included) */
+  void* workspace;  /* optional device buffer (256-byte aligned) for the tile work list, or NULL */
+  size_t workspace_bytes;
 } mxa_fwd_params;
+
+/* Workspace bytes that let mxa_fwd take its CTAs from a cost-sorted work
+ * list of packed documents (FLAMIA notes, Algorithm 2): one item per
+ * (document, 128-query tile), so that no CTA is launched for a tile slot past
+ * a document's end, ordered by the number of key tiles it visits, longest
+ * first (CTA i: item i / Hq, head i % Hq).  256 + 32 * ntiles + 4 * num_docs
+ * bytes, rounded up to 256.  Returns 0 when the list brings nothing (equal
+ * documents, cu_seqlens NULL) or cannot be built (max_seqlen above 4094
+ * tiles); with workspace NULL or smaller, mxa_fwd launches one CTA per (tile
+ * slot of max_seqlen, document, head).  Every call rebuilds the list on the
+ * device (cu_seqlens stays device-only). */
+size_t mxa_fwd_workspace_bytes(const mxa_fwd_params* p);
 
 /* Forward: O = softmax(alpha Q K^T) V over the visible keys, and LSE.
  * Status: MXA_OK, MXA_ERR_ARG, MXA_ERR_ALIGN, MXA_ERR_UNSUPPORTED,
@@ -187,7 +201,10 @@ typedef struct {
 
 /* Workspace bytes of mxa_bwd's fastest path.
  *   Both modes: D and LSE * log2(e), fp32, each padded to whole 128-token
- *   tiles per document ([Hq, ntiles, 128]).
+ *   tiles per document ([Hq, ntiles, 128]); then the key-tile and query-tile
+ *   work lists that schedule the dK/dV and dQ CTAs of packed documents as
+ *   mxa_fwd schedules its own (256 + 32 * ntiles + 4 * num_docs bytes,
+ *   rounded up to 256; reserved in every case).
  *   FP32 mode: plus the dS blocks the dK/dV pass emits for the dQ product --
  *   E4M3 codes (16 KB) and the 16 UE8M0 block scales per (query head, key
  *   tile, query tile of the same document) pair, with mt = ceil(max document
@@ -197,8 +214,8 @@ typedef struct {
  *   256 bytes. */
 size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p);
 
-/* Smallest workspace mxa_bwd accepts: the padded D and LSE rows, plus the
- * fp16 accumulator in FP16_X512 mode.  An FP32-mode workspace smaller than
+/* Smallest workspace mxa_bwd accepts: the padded D and LSE rows and the tile
+ * lists, plus the fp16 accumulator in FP16_X512 mode.  An FP32-mode workspace smaller than
  * mxa_bwd_workspace_bytes() selects a dQ kernel that forms dS again from S
  * and dP instead of reading the emitted blocks (slower; same blocks, so the
  * same tolerances). */

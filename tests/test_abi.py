@@ -31,7 +31,7 @@ def test_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) <= set(mxa.EXPORTS) | set(names)
-    assert mxa.mxa_abi_version() == 1
+    assert mxa.mxa_abi_version() == 2
 
 
 def test_exports_testing_hooks(lib):
@@ -45,7 +45,7 @@ def test_struct_layouts_match_header():
     # sizes of the C structs on this platform (x86-64 / aarch64 LP64)
     assert ctypes.sizeof(mxa.c_qview) == 16
     assert ctypes.sizeof(mxa.c_shape) == 56
-    assert ctypes.sizeof(mxa.c_fwd_params) == 120
+    assert ctypes.sizeof(mxa.c_fwd_params) == 136
     assert ctypes.sizeof(mxa.c_bwd_params) == 216
 
 
@@ -107,7 +107,7 @@ def test_quantize_rejects_bad_arguments_without_launch(lib):
 
 def _fwd(T=256, Hq=2, Hkv=2, d=128, nd=1, maxlen=256, nt=2):
     sh = mxa.c_shape(T, Hq, Hkv, d, None, nd, maxlen, nt, 0, 0.0)
-    return mxa.c_fwd_params(sh, _qv(), _qv(), _qv(), 256, 256)
+    return mxa.c_fwd_params(sh, _qv(), _qv(), _qv(), 256, 256, None, 0)
 
 
 def test_fwd_bwd_reject_bad_arguments_without_launch(lib):
@@ -128,6 +128,18 @@ def test_fwd_bwd_reject_bad_arguments_without_launch(lib):
     p = _fwd()
     p.shape.softmax_scale = -1.0
     assert L.mxa_fwd(ctypes.byref(p), None) == mxa.MXA_ERR_ARG
+    # the tile work list: nothing to do for equal documents (masked or not);
+    # packed documents take 256 bytes of header, 2 x 16 bytes per tile and
+    # 4 per document, rounded up to 256
+    p = _fwd()
+    assert L.mxa_fwd_workspace_bytes(ctypes.byref(p)) == 0
+    p.shape.causal = 1
+    assert L.mxa_fwd_workspace_bytes(ctypes.byref(p)) == 0
+    pj = _fwd(T=1000, nd=3, maxlen=600, nt=10)
+    pj.shape.cu_seqlens = 4096  # never read: sizing needs no device data
+    assert L.mxa_fwd_workspace_bytes(ctypes.byref(pj)) == 768  # 256 + 2 * 10 * 16 + 3 * 4 = 588
+    pj.workspace, pj.workspace_bytes = 8, 768  # used, but not 256-byte aligned
+    assert L.mxa_fwd(ctypes.byref(pj), None) == mxa.MXA_ERR_ALIGN
     sh = mxa.c_shape(256, 2, 2, 128, None, 1, 256, 2, 1, 0.0)
     bp = mxa.c_bwd_params(sh, *[_qv()] * 7, 256, 256, 256, 256, 256, 0)
     need = L.mxa_bwd_workspace_bytes(ctypes.byref(bp))
@@ -135,7 +147,7 @@ def test_fwd_bwd_reject_bad_arguments_without_launch(lib):
     # padded D and LSE rows [Hq, NT, 128] fp32; fp32 mode adds the emitted dS:
     # one 16 KB code tile + 16 block scales per (head, key tile, query-tile
     # slot) pair
-    assert need_min == 2 * 2 * 2 * 128 * 4
+    assert need_min == 2 * 2 * 2 * 128 * 4 + 512  # + the tile lists
     assert need == need_min + 2 * 2 * 2 * (16384 + 16)
     assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), need_min - 1, None) == mxa.MXA_ERR_WORKSPACE
     assert L.mxa_bwd(ctypes.byref(bp), None, need, None) == mxa.MXA_ERR_WORKSPACE

@@ -58,3 +58,49 @@ def test_fwd_first_causal_query_is_exact():
     for s in w.cu_seqlens.numpy()[:-1]:
         want = torch.from_numpy(O[s]).to(torch.bfloat16).float().numpy()
         assert np.array_equal(on[s], want), s
+
+
+SCHED_CASES = [
+    inp.make_custom("sched_ragged_causal", lengths=[300, 0, 129, 1, 700, 128], Hq=4, Hkv=2, d=128, causal=True,
+                    seed=26),
+    inp.make_custom("sched_ragged", lengths=[513, 64, 0, 250], Hq=2, Hkv=1, d=128, causal=False, seed=27),
+    inp.make_custom("sched_batched_causal", B=3, L=640, Hq=2, Hkv=2, d=64, causal=True, seed=28),
+]
+
+
+@pytest.mark.parametrize("w", SCHED_CASES, ids=[c.name for c in SCHED_CASES])
+def test_fwd_work_list_schedule(w):
+    """The cost-sorted work list (FLAMIA notes, Algorithm 2) only changes
+    which CTA computes which tile: O and LSE are bit-identical to the
+    max_seqlen grid.  The lists hold every (document, tile) pair once, the
+    items that visit the most tiles first."""
+    from block_scaled_mxfp8_gb300 import mxa
+
+    t = inp.tensors(w, with_grad=False)
+    geo, gv = gpu_views(w, t, names=("q", "k", "v"))
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    o1, l1 = mxa.fwd(gv["q"][0], gv["k"][0], gv["v"][1], geo, w.causal, workspace=ws)
+    o0, l0 = mxa.fwd(gv["q"][0], gv["k"][0], gv["v"][1], geo, w.causal, use_list=False)
+    torch.cuda.synchronize()
+    mxa.check_error()
+    assert torch.equal(o1.view(torch.int16), o0.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l0.view(torch.int32))
+
+    lengths = np.diff(w.cu_seqlens.numpy())
+    tiles = [(int(n) + 127) // 128 for n in lengths]
+    pairs = sorted((b, t_) for b, n in enumerate(tiles) for t_ in range(n))
+    if geo.cu_seqlens is None:  # equal documents: the grid itself, no list
+        return
+    raw = ws.cpu().numpy()
+    count = int(raw[:4].view(np.int32)[0])
+    assert count == len(pairs)
+    nt = geo.ntiles
+    items = raw[256:256 + 2 * nt * 16].view(np.int32).reshape(2, nt, 4)[:, :count]
+    base = np.concatenate([[0], np.cumsum(tiles)])[:-1]
+    for which, cost_of in ((0, lambda b, t_: t_ + 1 if w.causal else tiles[b]),
+                           (1, lambda b, t_: tiles[b] - t_ if w.causal else tiles[b])):
+        it = items[which]
+        assert sorted(map(tuple, it[:, :2].tolist())) == pairs
+        assert all(it[i, 2] == base[it[i, 0]] for i in range(count))
+        assert all(it[i, 3] == cost_of(it[i, 0], it[i, 1]) for i in range(count))
+        assert all(it[i, 3] >= it[i + 1, 3] for i in range(count - 1))
