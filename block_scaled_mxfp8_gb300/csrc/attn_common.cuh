@@ -16,6 +16,40 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Two fp32 values in one 64-bit register pair for the packed fp32x2 ALU
+// instructions (one instruction for two elements; each lane rounds exactly as
+// the scalar instruction does, so results are bit-identical).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // Bounded wait used by every warp role: gives up after kWaitBudgetCycles,
 // records `code` in the device error word and raises the CTA's abort flag;
 // returns early (false) once another role has raised it.
@@ -126,9 +160,13 @@ __device__ __forceinline__ uint32_t quant_ds_block32(const float (&x)[32], int s
   int e = am == 0.0f ? 0 : mx_exponent_bits(__float_as_uint(am)) - shift;
   if (e < -127) e = -127;
   const float sc = exp2i_neg(e + shift);
+  const uint64_t sc2 = f2_pack(sc, sc);
 #pragma unroll
-  for (int k = 0; k < 8; ++k)
-    w[k] = pack_e4m3x4(x[4 * k] * sc, x[4 * k + 1] * sc, x[4 * k + 2] * sc, x[4 * k + 3] * sc);
+  for (int k = 0; k < 8; ++k) {
+    const float2 a = f2_unpack(f2_mul(f2_pack(x[4 * k], x[4 * k + 1]), sc2));
+    const float2 b = f2_unpack(f2_mul(f2_pack(x[4 * k + 2], x[4 * k + 3]), sc2));
+    w[k] = pack_e4m3x4(a.x, a.y, b.x, b.y);
+  }
   return static_cast<uint32_t>(e + 127);
 }
 

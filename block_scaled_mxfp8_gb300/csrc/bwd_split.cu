@@ -332,6 +332,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     const bool key_valid = kpos < n;
     const float kb8 = key_valid ? 8.0f : -INFINITY;  // 2^8 boost of P^T; invalid key rows -> 0
     const float sl2 = a.scale_log2;
+    const uint64_t kb8x2 = f2_pack(kb8, kb8), sl2x2 = f2_pack(sl2, sl2);
     if (part == 0) {
       tmem_st4(lane_base + C::kSfP, 0x77777777u, 0x77777777u, 0x77777777u, 0x77777777u);  // 2^-8
       tmem_st_wait();
@@ -359,10 +360,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 #pragma unroll
       for (int c = 0; c < 32; c += 4) {
         const float4 l4 = *reinterpret_cast<const float4*>(lrow + c);
-        p[c] = ex2_approx(fmaf(p[c], sl2, kb8 - l4.x));
-        p[c + 1] = ex2_approx(fmaf(p[c + 1], sl2, kb8 - l4.y));
-        p[c + 2] = ex2_approx(fmaf(p[c + 2], sl2, kb8 - l4.z));
-        p[c + 3] = ex2_approx(fmaf(p[c + 3], sl2, kb8 - l4.w));
+        const float2 a = f2_unpack(f2_fma(f2_pack(p[c], p[c + 1]), sl2x2, f2_sub(kb8x2, f2_pack(l4.x, l4.y))));
+        const float2 b = f2_unpack(f2_fma(f2_pack(p[c + 2], p[c + 3]), sl2x2, f2_sub(kb8x2, f2_pack(l4.z, l4.w))));
+        p[c] = ex2_approx(a.x);
+        p[c + 1] = ex2_approx(a.y);
+        p[c + 2] = ex2_approx(b.x);
+        p[c + 3] = ex2_approx(b.y);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_a_empty[sa]);  // this warp is done with the LSE row
@@ -393,10 +396,16 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
           const float4 d4 = *reinterpret_cast<const float4*>(drow + i);
-          p[i] *= __uint_as_float(rr[i]) - d4.x;
-          p[i + 1] *= __uint_as_float(rr[i + 1]) - d4.y;
-          p[i + 2] *= __uint_as_float(rr[i + 2]) - d4.z;
-          p[i + 3] *= __uint_as_float(rr[i + 3]) - d4.w;
+          const float2 a = f2_unpack(f2_mul(f2_pack(p[i], p[i + 1]),
+                                            f2_sub(f2_pack(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])),
+                                                   f2_pack(d4.x, d4.y))));
+          const float2 b = f2_unpack(f2_mul(f2_pack(p[i + 2], p[i + 3]),
+                                            f2_sub(f2_pack(__uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3])),
+                                                   f2_pack(d4.z, d4.w))));
+          p[i] = a.x;
+          p[i + 1] = a.y;
+          p[i + 2] = b.x;
+          p[i + 3] = b.y;
         }
       }
       // the previous unit's dK MMA, issued before dP^T_u, is done with the

@@ -65,16 +65,27 @@ struct FwdCfg {
   static constexpr int kSmemBytes = kOffSfV + kStages * 2 * kAtomBytes + 1024;  // + alignment slack
 };
 
+// Three-input max (one instruction for two comparisons).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Row maximum of 64 scores in four independent chains.
 __device__ __forceinline__ float max64(const float (&v)[64]) {
-  float a = fmaxf(v[0], v[1]), b = fmaxf(v[2], v[3]), c = fmaxf(v[4], v[5]), d = fmaxf(v[6], v[7]);
+  float a = fmax3(v[0], v[1], v[2]), b = fmax3(v[3], v[4], v[5]), c = fmax3(v[6], v[7], v[8]),
+        d = fmax3(v[9], v[10], v[11]);
 #pragma unroll
-  for (int i = 8; i < 64; i += 8) {
-    a = fmaxf(a, fmaxf(v[i], v[i + 1]));
-    b = fmaxf(b, fmaxf(v[i + 2], v[i + 3]));
-    c = fmaxf(c, fmaxf(v[i + 4], v[i + 5]));
-    d = fmaxf(d, fmaxf(v[i + 6], v[i + 7]));
+  for (int i = 12; i < 60; i += 8) {
+    a = fmax3(a, v[i], v[i + 1]);
+    b = fmax3(b, v[i + 2], v[i + 3]);
+    c = fmax3(c, v[i + 4], v[i + 5]);
+    d = fmax3(d, v[i + 6], v[i + 7]);
   }
-  return fmaxf(fmaxf(a, b), fmaxf(c, d));
+  a = fmax3(a, v[60], v[61]);
+  b = fmax3(b, v[62], v[63]);
+  return fmax3(fmaxf(a, b), c, d);
 }
 
 __device__ __forceinline__ void ld64(uint32_t taddr, float (&v)[64]) {
@@ -347,17 +358,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         rescale_o = true;
       }
       const float neg = 4.0f - m;
-      float lsum = 0.0f;
+      const uint64_t neg2 = f2_pack(neg, neg), sl2x2 = f2_pack(sl2, sl2);
+      uint64_t lsum2 = 0;  // two partial sums (+0.0, +0.0)
       uint32_t pw[16];  // E4M3 codes of this warp's 64 weights
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
-        const float p0 = ex2_approx(fmaf(sv[c], sl2, neg));
-        const float p1 = ex2_approx(fmaf(sv[c + 1], sl2, neg));
-        const float p2 = ex2_approx(fmaf(sv[c + 2], sl2, neg));
-        const float p3 = ex2_approx(fmaf(sv[c + 3], sl2, neg));
-        lsum += (p0 + p1) + (p2 + p3);
+        const float2 x01 = f2_unpack(f2_fma(f2_pack(sv[c], sv[c + 1]), sl2x2, neg2));
+        const float2 x23 = f2_unpack(f2_fma(f2_pack(sv[c + 2], sv[c + 3]), sl2x2, neg2));
+        const float p0 = ex2_approx(x01.x), p1 = ex2_approx(x01.y);
+        const float p2 = ex2_approx(x23.x), p3 = ex2_approx(x23.y);
+        lsum2 = f2_add(lsum2, f2_add(f2_pack(p0, p1), f2_pack(p2, p3)));
         pw[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
       }
+      const float2 ls = f2_unpack(lsum2);
+      const float lsum = ls.x + ls.y;
       // the previous P V must be done before P is overwritten and O rescaled
       if (j > 0 && !(ok = warp_wait(&bar_o_done, (j - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
