@@ -18,7 +18,9 @@
 // forwards; these two kernels execute 3.5).  The 32 x 32 blocks are the same
 // in both kernels; each quantizes its own fp32 dS.
 //
-// Warps: 0 = TMA producer, 1 = TMEM owner and MMA issuer, 2..17 = softmax.
+// Warps: 0 = TMA producer, 1 = TMEM owner and MMA issuer, 2..17 = softmax;
+// the dK/dV kernel adds warp 18, which issues its gradient MMAs (dV, dK) so
+// that the S^T / dP^T issuer never waits behind them.
 // Four softmax warps share each TMEM lane quadrant and split the tile's 128
 // columns into quarters of 32, so each warp owns exactly one 32 x 32 dS block
 // per tile (its block max is a warp reduction) and every SM sub-partition has
@@ -36,6 +38,7 @@ namespace mxa {
 namespace {
 
 constexpr int kSplitThreads = 576;
+constexpr int kDkdvThreads = 608;  // + warp 18, the gradient-MMA issuer
 constexpr int kSoftmaxThreads = 512;
 
 template <int D>
@@ -108,7 +111,7 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
 
 // ========================================================================= dK, dV
 template <int D>
-__global__ void __launch_bounds__(kSplitThreads, 1)
+__global__ void __launch_bounds__(kDkdvThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -116,7 +119,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 
   __shared__ uint64_t bar_kv, bar_a_full[C::kStagesA], bar_a_empty[C::kStagesA], bar_b_full[C::kStagesB],
       bar_b_empty[C::kStagesB], bar_s_full, bar_x_free, bar_dp_full, bar_x_free2, bar_p_ready, bar_ds_ready,
-      bar_final, bar_drain;
+      bar_dv_done, bar_dk_done, bar_final, bar_drain, bar_drain2;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int64_t s_slot;
@@ -139,7 +142,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   const int qi0 = a.causal ? kt : 0;
   const int nq = n_tiles - qi0;
   const int n_work = nq * grp;
-  if (tile_base < 0) tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, kSplitThreads, &s_slot);
+  if (tile_base < 0) tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, kDkdvThreads, &s_slot);
 
   if (tid == 0) {
     mbar_init(&bar_kv, 1);
@@ -157,8 +160,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     mbar_init(&bar_x_free2, kSoftmaxThreads);
     mbar_init(&bar_p_ready, kSoftmaxThreads);
     mbar_init(&bar_ds_ready, kSoftmaxThreads);
+    mbar_init(&bar_dv_done, 1);
+    mbar_init(&bar_dk_done, 1);
     mbar_init(&bar_final, 1);
     mbar_init(&bar_drain, 1);
+    mbar_init(&bar_drain2, 1);
     s_abort = 0;
     fence_barrier_init();
   }
@@ -232,17 +238,14 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---------------------------------------------------------- MMA issuer
+      // ---------------------------------------------------------- S^T / dP^T issuer
       // descriptors built once; per MMA only constant offsets are added
       const uint64_t dKa = make_sdesc(smem_u32(smem + C::kOffK), 16, C::kSBO, C::kSwz);
       const uint64_t dVa = make_sdesc(smem_u32(smem + C::kOffV), 16, C::kSBO, C::kSwz);
       const uint64_t dA = make_sdesc(smem_u32(smem + C::kOffA), 16, C::kSBO, C::kSwz);
-      const uint64_t dB = make_sdesc(smem_u32(smem + C::kOffB), 16, C::kSBO, C::kSwz);
       const uint64_t dSf = atom_desc(sSf);
-      const uint32_t tX = tmem + C::kColX, tDV = tmem + C::kColDV, tDK = tmem + C::kColDK;
-      const uint32_t tP = tmem + C::kColP, tDS = tmem + C::kColDS;
-      const uint32_t tSfK = tmem + C::kSfK, tSfV = tmem + C::kSfV, tSfP = tmem + C::kSfP;
-      const uint32_t tSfDS = tmem + C::kSfDS;
+      const uint32_t tX = tmem + C::kColX;
+      const uint32_t tSfK = tmem + C::kSfK, tSfV = tmem + C::kSfV;
       bool ok = role_wait(&bar_kv, 0, abort_flag, a.err, kErrTimeoutMma);
       if (ok) {
         tc_fence_after();
@@ -263,20 +266,15 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         mma_commit(&bar_s_full);
         return true;
       };
-      // Pipe order per unit u: dP^T_u, dV_u, S^T_{u+1}, dK_u.  X is written
-      // only by S^T and dP^T; between two writes of X the pipe always holds
-      // an MMA that does not touch X (dV_u, dK_u), which covers the softmax
-      // warps' read of X.
+      // Per unit u: dP^T_u once S^T_u has been read out of X, then S^T_{u+1}
+      // once dP^T_u has been read; warp 18 issues the gradient MMAs.
       if (ok) ok = issue_s(0);
       for (int u = 0; ok && u < n_work; ++u) {
         const int sa = u % C::kStagesA, sb = u % C::kStagesB, t = u & 1;
         const uint64_t da = sdesc_adv(dA, sa * 2 * C::kTileBytes);  // Q, G of this unit
-        const uint64_t db = sdesc_adv(dB, sb * 2 * C::kTileBytes);  // Qt, Gt of this unit
-        // dP^T = V G^T once S^T has been read out of X; ring B (D row, Qt,
-        // Gt) must have landed before the softmax warps see dP^T, and the
-        // previous unit's staged dS must have been read before they see it
+        // dP^T = V G^T; ring B (its D row) must have landed before the
+        // softmax warps see dP^T
         if (!(ok = role_wait(&bar_x_free, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
-        if (a.ds_codes) bulk_store_wait_read();
         if (!(ok = role_wait(&bar_b_full[sb], (u / C::kStagesB) & 1, abort_flag, a.err, kErrTimeoutMma))) break;
         tc_fence_after();
         const uint32_t tSfG = tmem + C::kSfG + 4 * t;
@@ -287,8 +285,30 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
                       make_idesc_mxf8(128, 128, 0, 0, kk, kk), tSfV, tSfG, kk > 0);
         mma_commit(&bar_dp_full);
         mma_commit(&bar_a_empty[sa]);
-        // dV += P^T G (P^T codes written while dP^T ran)
+        // next S^T as soon as dP^T has been read (runs while dS is formed)
+        if (!(ok = role_wait(&bar_x_free2, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        if (u + 1 < n_work && !(ok = issue_s(u + 1))) break;
+      }
+      // drain this thread's MMAs before the TMEM is released
+      mma_commit(&bar_drain);
+      mbar_wait(&bar_drain, 0, nullptr, 0);
+    }
+  } else if (warp == 18) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- dV / dK issuer
+      const uint64_t dB = make_sdesc(smem_u32(smem + C::kOffB), 16, C::kSBO, C::kSwz);
+      const uint64_t dSf = atom_desc(sSf);
+      const uint32_t tDV = tmem + C::kColDV, tDK = tmem + C::kColDK;
+      const uint32_t tP = tmem + C::kColP, tDS = tmem + C::kColDS;
+      const uint32_t tSfP = tmem + C::kSfP, tSfDS = tmem + C::kSfDS;
+      bool ok = true;
+      for (int u = 0; u < n_work; ++u) {
+        const int sb = u % C::kStagesB, t = u & 1;
+        const uint64_t db = sdesc_adv(dB, sb * 2 * C::kTileBytes);  // Qt, Gt of this unit
+        // dV += P^T G once the softmax warps have written P^T and ring B has
+        // landed
         if (!(ok = role_wait(&bar_p_ready, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        if (!(ok = role_wait(&bar_b_full[sb], (u / C::kStagesB) & 1, abort_flag, a.err, kErrTimeoutMma))) break;
         tc_fence_after();
         const uint32_t tSfGt = tmem + C::kSfGt + 4 * t;
         tmem_cp_desc(tSfGt, sdesc_adv(dSf, (2 + 2 * C::kStagesA + 2 * sb + 1) * kAtomBytes));
@@ -296,10 +316,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         for (int kk = 0; kk < 4; ++kk)
           mma_mxf8_ts(tDV, tP + 8 * kk, sdesc_adv(db, C::kTileBytes + kk * 32 * D),
                       make_idesc_mxf8(128, D, 0, 1, kk, kk), tSfP, tSfGt, (u > 0 || kk > 0) ? 1u : 0u);
-        // next S^T as soon as dP^T has been read (runs while dS is formed)
-        if (!(ok = role_wait(&bar_x_free2, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
-        if (u + 1 < n_work && !(ok = issue_s(u + 1))) break;
-        // dK += dS^T Q
+        mma_commit(&bar_dv_done);
+        // dK += dS^T Q once dS^T is in TMEM (and its copy staged)
         if (!(ok = role_wait(&bar_ds_ready, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
         if (a.ds_codes) {  // the staged dS tile of this unit to the workspace
           const int h = hk * grp + u / nq;
@@ -314,10 +332,14 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
           mma_mxf8_ts(tDK, tDS + 8 * kk, sdesc_adv(db, kk * 32 * D), make_idesc_mxf8(128, D, 0, 1, 0, kk),
                       tSfDS + 4 * kk, tSfQt, (u > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bar_b_empty[sb]);
+        // the staging buffer is free for the next unit's dS once the bulk
+        // store has read it; dk_done tells the softmax warps both
+        if (a.ds_codes) bulk_store_wait_read();
+        mma_commit(&bar_dk_done);
       }
       mma_commit(&bar_final);
-      mma_commit(&bar_drain);
-      mbar_wait(&bar_drain, 0, nullptr, 0);
+      mma_commit(&bar_drain2);
+      mbar_wait(&bar_drain2, 0, nullptr, 0);
       if (a.ds_codes) bulk_store_wait_all();  // the last staged tile is out before the CTA exits
     }
   } else if (warp >= 2) {
@@ -373,8 +395,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 #pragma unroll
         for (int c = 0; c < 32; ++c) p[c] = (32 * part + c >= j) ? p[c] : 0.0f;
       }
-      // the previous unit's dV MMA, issued before S^T_u, is done with the P^T
-      // codes: s_full(u) completed only after it
+      // the previous unit's dV MMA must be done with the P^T codes
+      if (u > 0 && !(ok = warp_wait(&bar_dv_done, (u - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      tc_fence_after();
       {
         uint32_t w[8];
 #pragma unroll
@@ -408,11 +431,13 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
           p[i + 3] = b.y;
         }
       }
-      // the previous unit's dK MMA, issued before dP^T_u, is done with the
-      // dS^T codes and scales: dp_full(u) completed only after it
       {
         uint32_t w[8];
         const uint32_t eb = quant_ds_block32(p, 8, w);  // 32 key rows x 32 queries
+        // the previous unit's dK MMA must be done with the dS^T codes and
+        // scales, and its bulk store with the staging buffer
+        if (u > 0 && !(ok = warp_wait(&bar_dk_done, (u - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+        tc_fence_after();
         tmem_st8(lane_base + C::kColDS + 8 * part, w);
         // dK's A operand is dS^T (rows = keys, K = queries): for K step
         // `part` the scale of row r sits in lane r, column kSfDS + 4 part +
@@ -735,7 +760,7 @@ cudaError_t launch_bwd_split(const BwdArgs& a, const BwdMaps& m, int d, int max_
     e = cudaFuncSetAttribute(attn_bwd_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DqCfg<128>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attn_bwd_dkdv_kernel<128><<<g1, kSplitThreads, DkdvCfg<128>::kSmemBytes, stream>>>(m, a);
+    attn_bwd_dkdv_kernel<128><<<g1, kDkdvThreads, DkdvCfg<128>::kSmemBytes, stream>>>(m, a);
     attn_bwd_dq_kernel<128><<<g2, kSplitThreads, DqCfg<128>::kSmemBytes, stream>>>(m, a);
   } else {
     e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -744,7 +769,7 @@ cudaError_t launch_bwd_split(const BwdArgs& a, const BwdMaps& m, int d, int max_
     e = cudaFuncSetAttribute(attn_bwd_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DqCfg<64>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attn_bwd_dkdv_kernel<64><<<g1, kSplitThreads, DkdvCfg<64>::kSmemBytes, stream>>>(m, a);
+    attn_bwd_dkdv_kernel<64><<<g1, kDkdvThreads, DkdvCfg<64>::kSmemBytes, stream>>>(m, a);
     attn_bwd_dq_kernel<64><<<g2, kSplitThreads, DqCfg<64>::kSmemBytes, stream>>>(m, a);
   }
   return cudaGetLastError();
@@ -758,12 +783,12 @@ cudaError_t launch_bwd_emit(const BwdArgs& a, const BwdMaps& m, int d, int max_s
     e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DkdvCfg<128>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attn_bwd_dkdv_kernel<128><<<g1, kSplitThreads, DkdvCfg<128>::kSmemBytes, stream>>>(m, a);
+    attn_bwd_dkdv_kernel<128><<<g1, kDkdvThreads, DkdvCfg<128>::kSmemBytes, stream>>>(m, a);
   } else {
     e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DkdvCfg<64>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attn_bwd_dkdv_kernel<64><<<g1, kSplitThreads, DkdvCfg<64>::kSmemBytes, stream>>>(m, a);
+    attn_bwd_dkdv_kernel<64><<<g1, kDkdvThreads, DkdvCfg<64>::kSmemBytes, stream>>>(m, a);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return launch_dq_gemm(a, m, d, max_seqlen, stream);
