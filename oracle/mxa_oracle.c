@@ -540,6 +540,112 @@ void orc_attn_bwd(const double* Qs, const double* Ks, const double* Vo, const do
     }
 }
 
+/* Cross-attention (query and key/value documents of different lengths, no
+ * mask): the queries of document b, rows [cu_q[b], cu_q[b+1]) of Q, attend
+ * to that document's keys and values, rows [cu_k[b], cu_k[b+1]) of K and V.
+ * The arithmetic is the direct softmax of orc_attn_fwd with the key range
+ * taken from the key side.  Q [Tq, Hq, d]; K, V [Tk, Hkv, d]; O [Tq, Hq, d];
+ * LSE [Hq, Tq].  Both offset arrays are required. */
+void orc_attn_fwd_x(const double* Q, const double* K, const double* V, int64_t Tq, int64_t Tk, int Hq, int Hkv,
+                    int d, const int32_t* cu_q, const int32_t* cu_k, int ndocs, double alpha, double* O,
+                    double* LSE)
+{
+    int64_t maxk = 0;
+    for (int b = 0; b < ndocs; ++b)
+        if (cu_k[b + 1] - cu_k[b] > maxk)
+            maxk = cu_k[b + 1] - cu_k[b];
+    (void)Tk;
+#pragma omp parallel
+    {
+        double* Srow = (double*)malloc(sizeof(double) * (size_t)(maxk + 1));
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < Tq * Hq; ++r) {
+            int64_t i = r / Hq;
+            int h = (int)(r % Hq);
+            int b = 0;
+            while (b + 1 < ndocs && cu_q[b + 1] <= i)
+                ++b;
+            LSE[(int64_t)h * Tq + i] =
+                fwd_row(Q, K, V, Hq, Hkv, d, cu_k[b], cu_k[b + 1], 0, alpha, i, h, O + (i * Hq + h) * d, Srow);
+        }
+        free(Srow);
+    }
+}
+
+/* Cross-attention backward, direct: orc_attn_bwd's two passes with the query
+ * rows of document b from the query side and its key rows from the key side
+ * (no mask).  Views as in orc_attn_bwd; Ks, Vo, Vr, Kt have Tk rows, the rest
+ * Tq.  dQ [Tq, Hq, d]; dK, dV [Tk, Hkv, d]; O [Tq, Hq, d]; LSE, D [Hq, Tq]. */
+void orc_attn_bwd_x(const double* Qs, const double* Ks, const double* Vo, const double* Vr, const double* Gr,
+                    const double* Qt, const double* Kt, const double* Gt, int64_t Tq, int64_t Tk, int Hq, int Hkv,
+                    int d, const int32_t* cu_q, const int32_t* cu_k, int ndocs, double alpha, double* dQ, double* dK,
+                    double* dV, double* O, double* LSE, double* D)
+{
+    int grp = Hq / Hkv;
+    (void)Tk;
+    for (int b = 0; b < ndocs; ++b) {
+        int64_t sq = cu_q[b], eq = cu_q[b + 1], sk = cu_k[b], ek = cu_k[b + 1];
+        for (int hk = 0; hk < Hkv; ++hk) {
+            /* pass 1: query rows */
+#pragma omp parallel
+            {
+                double* Srow = (double*)malloc(sizeof(double) * (size_t)(ek - sk + 1));
+#pragma omp for schedule(dynamic, 8) collapse(2)
+                for (int hh = 0; hh < grp; ++hh)
+                    for (int64_t i = sq; i < eq; ++i) {
+                        int h = hk * grp + hh;
+                        double* o = O + (i * Hq + h) * d;
+                        double lse = fwd_row(Qs, Ks, Vo, Hq, Hkv, d, sk, ek, 0, alpha, i, h, o, Srow);
+                        LSE[(int64_t)h * Tq + i] = lse;
+                        const double* g = Gr + (i * Hq + h) * d;
+                        double Di = dot(g, o, d);
+                        D[(int64_t)h * Tq + i] = Di;
+                        double* dq = dQ + (i * Hq + h) * d;
+                        for (int k = 0; k < d; ++k)
+                            dq[k] = 0.0;
+                        for (int64_t j = sk; j < ek; ++j) {
+                            double P = exp(Srow[j - sk] - lse);
+                            double E = dot(g, Vr + (j * Hkv + hk) * d, d);
+                            double U = P * (E - Di);
+                            const double* kt = Kt + (j * Hkv + hk) * d;
+                            for (int k = 0; k < d; ++k)
+                                dq[k] += alpha * U * kt[k];
+                        }
+                    }
+                free(Srow);
+            }
+            /* pass 2: key rows */
+#pragma omp parallel for schedule(dynamic, 8)
+            for (int64_t j = sk; j < ek; ++j) {
+                double* dk = dK + (j * Hkv + hk) * d;
+                double* dv = dV + (j * Hkv + hk) * d;
+                for (int k = 0; k < d; ++k) {
+                    dk[k] = 0.0;
+                    dv[k] = 0.0;
+                }
+                const double* kj = Ks + (j * Hkv + hk) * d;
+                const double* vj = Vr + (j * Hkv + hk) * d;
+                for (int hh = 0; hh < grp; ++hh) {
+                    int h = hk * grp + hh;
+                    for (int64_t i = sq; i < eq; ++i) {
+                        double S = alpha * dot(Qs + (i * Hq + h) * d, kj, d);
+                        double P = exp(S - LSE[(int64_t)h * Tq + i]);
+                        const double* g = Gr + (i * Hq + h) * d;
+                        double E = dot(g, vj, d);
+                        double U = P * (E - D[(int64_t)h * Tq + i]);
+                        const double* gt = Gt + (i * Hq + h) * d;
+                        const double* qt = Qt + (i * Hq + h) * d;
+                        for (int k = 0; k < d; ++k) {
+                            dv[k] += P * gt[k];
+                            dk[k] += alpha * U * qt[k];
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
 int orc_num_threads(void)
 {
 #ifdef _OPENMP

@@ -77,6 +77,8 @@ def _L():
                 "orc_dequant_tokblock": (None, [P, P, i64, i32, i32, P, i32, P]),
                 "orc_attn_fwd": (None, [P, P, P, i64, i32, i32, i32, P, i32, i32, f64, P, i64, P, P]),
                 "orc_attn_bwd": (None, [P] * 8 + [i64, i32, i32, i32, P, i32, i32, f64, P, i32] + [P] * 6),
+                "orc_attn_fwd_x": (None, [P, P, P, i64, i64, i32, i32, i32, P, P, i32, f64, P, P]),
+                "orc_attn_bwd_x": (None, [P] * 8 + [i64, i64, i32, i32, i32, P, P, i32, f64] + [P] * 6),
                 "orc_num_threads": (i32, []),
             }
             for name, (res, args) in sig.items():
@@ -288,6 +290,50 @@ def attn_bwd(Qs, Ks, Vo, Vr, Gr, Qt, Kt, Gt, cu_seqlens=None, causal=False, alph
     _L().orc_attn_bwd(*[_p(a) for a in arrs], T, Hq, Hkv, d, _p(cu), nd, int(bool(causal)), float(alpha),
                       _p(units), -1 if units is None else len(units),
                       *[_p(out[k]) for k in ("dQ", "dK", "dV", "O", "LSE", "D")])
+    return out
+
+
+def attn_fwd_x(Q, K, V, cu_q, cu_k, alpha=None):
+    """Cross-attention forward in fp64 (no mask): the queries of document b
+    (rows cu_q[b]..cu_q[b+1]) attend to its keys and values (rows
+    cu_k[b]..cu_k[b+1]).  Q [Tq,Hq,d], K/V [Tk,Hkv,d].  Returns
+    (O [Tq,Hq,d], LSE [Hq,Tq])."""
+    Q, K, V = (np.ascontiguousarray(a, dtype=np.float64) for a in (Q, K, V))
+    Tq, Hq, d = Q.shape
+    Tk, Hkv = K.shape[:2]
+    if alpha is None:
+        alpha = 1.0 / math.sqrt(d)
+    cq, nd = _cu(cu_q)
+    ck, ndk = _cu(cu_k)
+    assert nd == ndk and cq[-1] == Tq and ck[-1] == Tk
+    O = np.full((Tq, Hq, d), np.nan)
+    LSE = np.full((Hq, Tq), np.nan)
+    _L().orc_attn_fwd_x(_p(Q), _p(K), _p(V), Tq, Tk, Hq, Hkv, d, _p(cq), _p(ck), nd, float(alpha), _p(O), _p(LSE))
+    return O, LSE
+
+
+def attn_bwd_x(Qs, Ks, Vo, Vr, Gr, Qt, Kt, Gt, cu_q, cu_k, alpha=None):
+    """Cross-attention backward in fp64 (no mask); views as in attn_bwd, with
+    Ks, Vo, Vr, Kt over the key side's Tk rows.  Returns a dict with dQ, dK,
+    dV, O, LSE, D."""
+    arrs = [np.ascontiguousarray(a, dtype=np.float64) for a in (Qs, Ks, Vo, Vr, Gr, Qt, Kt, Gt)]
+    Tq, Hq, d = arrs[0].shape
+    Tk, Hkv = arrs[1].shape[:2]
+    if alpha is None:
+        alpha = 1.0 / math.sqrt(d)
+    cq, nd = _cu(cu_q)
+    ck, ndk = _cu(cu_k)
+    assert nd == ndk and cq[-1] == Tq and ck[-1] == Tk
+    out = {
+        "dQ": np.full((Tq, Hq, d), np.nan),
+        "dK": np.full((Tk, Hkv, d), np.nan),
+        "dV": np.full((Tk, Hkv, d), np.nan),
+        "O": np.full((Tq, Hq, d), np.nan),
+        "LSE": np.full((Hq, Tq), np.nan),
+        "D": np.full((Hq, Tq), np.nan),
+    }
+    _L().orc_attn_bwd_x(*[_p(a) for a in arrs], Tq, Tk, Hq, Hkv, d, _p(cq), _p(ck), nd, float(alpha),
+                        *[_p(out[k]) for k in ("dQ", "dK", "dV", "O", "LSE", "D")])
     return out
 
 

@@ -177,3 +177,63 @@ def test_prefix_invariance_of_O_and_dQ_not_dK():
     np.testing.assert_array_equal(r1["O"][:40], r2["O"][:40])
     np.testing.assert_array_equal(r1["dQ"][:40], r2["dQ"][:40])
     assert not np.allclose(r1["dK"][:40], r2["dK"][:40])
+
+
+def _torch_cross_ref(Q, K, V, G, lq, lk, alpha):
+    """fp64 SDPA + autograd per document with Lq != Lk (no mask)."""
+    Hq, Hkv = Q.shape[1], K.shape[1]
+    q = torch.tensor(Q, requires_grad=True)
+    k = torch.tensor(K, requires_grad=True)
+    v = torch.tensor(V, requires_grad=True)
+    outs, lses = [], []
+    sq = sk = 0
+    for nq, nk in zip(lq, lk):
+        qq = q[sq:sq + nq].permute(1, 0, 2)
+        kk = k[sk:sk + nk].permute(1, 0, 2).repeat_interleave(Hq // Hkv, 0)
+        vv = v[sk:sk + nk].permute(1, 0, 2).repeat_interleave(Hq // Hkv, 0)
+        outs.append(F.scaled_dot_product_attention(qq, kk, vv, scale=alpha).permute(1, 0, 2))
+        lses.append(torch.logsumexp(alpha * qq @ kk.transpose(1, 2), -1))
+        sq, sk = sq + nq, sk + nk
+    O = torch.cat(outs, 0)
+    O.backward(torch.tensor(G))
+    return O.detach().numpy(), torch.cat(lses, 1).detach().numpy(), q.grad.numpy(), k.grad.numpy(), v.grad.numpy()
+
+
+def test_cross_attention_matches_torch_sdpa_autograd():
+    """Cross-attention oracle (queries and keys of a document have their own
+    lengths) against torch's fp64 SDPA + autograd, GQA 4/2, d = 16."""
+    lq, lk = [5, 1, 12, 7], [9, 30, 1, 16]
+    Tq, Tk, Hq, Hkv, d = sum(lq), sum(lk), 4, 2, 16
+    Q, G = _rand((Tq, Hq, d), 71), _rand((Tq, Hq, d), 72)
+    K, V = _rand((Tk, Hkv, d), 73), _rand((Tk, Hkv, d), 74)
+    cq = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+    alpha = 1.0 / math.sqrt(d)
+    O, LSE = orc.attn_fwd_x(Q, K, V, cq, ck, alpha)
+    r = orc.attn_bwd_x(Q, K, V, V, G, Q, K, G, cq, ck, alpha)
+    Ot, Lt, dQt, dKt, dVt = _torch_cross_ref(Q, K, V, G, lq, lk, alpha)
+    for name, a, b in (("O", O, Ot), ("LSE", LSE, Lt), ("bwd O", r["O"], Ot), ("bwd LSE", r["LSE"], Lt),
+                       ("dQ", r["dQ"], dQt), ("dK", r["dK"], dKt), ("dV", r["dV"], dVt)):
+        np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-12, err_msg=name)
+
+
+def test_cross_attention_reduces_to_self_attention_and_one_key():
+    """With the key side equal to the query side the cross oracle is the
+    self-attention oracle; a document with a single key gives O = V of that
+    key for every query and LSE = alpha q . k."""
+    lens = [6, 11]
+    T, Hq, Hkv, d = sum(lens), 2, 1, 8
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    Q, K, V = _rand((T, Hq, d), 81), _rand((T, Hkv, d), 82), _rand((T, Hkv, d), 83)
+    O1, L1 = orc.attn_fwd_x(Q, K, V, cu, cu)
+    O2, L2 = orc.attn_fwd(Q, K, V, cu, False)
+    np.testing.assert_array_equal(O1, O2)
+    np.testing.assert_array_equal(L1, L2)
+    ck = np.array([0, 1, 2], np.int32)
+    K1, V1 = K[:2], V[:2]
+    O, LSE = orc.attn_fwd_x(Q, K1, V1, cu, ck, 0.5)
+    for b in range(2):
+        for i in range(cu[b], cu[b + 1]):
+            for h in range(Hq):
+                np.testing.assert_allclose(O[i, h], V1[b, 0], rtol=1e-15)
+                np.testing.assert_allclose(LSE[h, i], 0.5 * Q[i, h] @ K1[b, 0], rtol=1e-13)
