@@ -27,6 +27,8 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -118,10 +120,15 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def flops(B, H, L, d, causal, lengths=None):
+def flops(B, H, L, d, causal, lengths=None, lengths_k=None):
     """FLOP convention of the pages: forward 4 * H * d * sum_b n_b^2 (B * L^2 for
-    equal lengths), halved when causal; backward 2.5 x forward."""
-    sq = float(sum(int(n) * int(n) for n in lengths)) if lengths is not None else float(B) * L * L
+    equal lengths; sum_b nq_b * nk_b for cross-attention), halved when causal;
+    backward 2.5 x forward."""
+    if lengths_k is not None:
+        lq = lengths if lengths is not None else [L] * B
+        sq = float(sum(int(a) * int(b) for a, b in zip(lq, lengths_k)))
+    else:
+        sq = float(sum(int(n) * int(n) for n in lengths)) if lengths is not None else float(B) * L * L
     f = 4.0 * H * sq * d
     if causal:
         f *= 0.5
@@ -156,6 +163,31 @@ def oracle_sample(L=4096, H=1, d=128, causal=False, seed=1002):
     return dt, ff + fb, orc.num_threads()
 
 
+def oracle_sample_cross(Lq=512, Lk=8192, H=1, d=128, seed=1006):
+    """The oracle on one cross-attention document: Lq queries against Lk keys
+    and values, H heads.  Returns (seconds, flop, threads)."""
+    from block_scaled_mxfp8_gb300 import inputs as inp
+    from oracle import oracle as orc
+
+    t = inp.cross_tensors([Lq], [Lk], H, H, d, seed)
+    cq = np.array([0, Lq], np.int32)
+    ck = np.array([0, Lk], np.int32)
+    orc.build()
+    t0 = time.perf_counter()
+    v = {}
+    for k, cu in (("q", cq), ("do", cq), ("k", ck), ("v", ck)):
+        rc, rs = orc.quant_row(t[k])
+        tc, ts = orc.quant_tok(t[k], cu)
+        v[k] = (orc.dequant_row(rc, rs), orc.dequant_tok(tc, ts, cu))
+    alpha = 1.0 / math.sqrt(d)
+    orc.attn_fwd_x(v["q"][0], v["k"][0], v["v"][1], cq, ck, alpha)
+    orc.attn_bwd_x(v["q"][0], v["k"][0], v["v"][1], v["v"][0], v["do"][0], v["q"][1], v["k"][1], v["do"][1],
+                   cq, ck, alpha)
+    dt = time.perf_counter() - t0
+    ff, fb = flops(1, H, Lq, d, False, [Lq], [Lk])
+    return dt, ff + fb, orc.num_threads()
+
+
 # ------------------------------------------------------------------ GPU leg
 
 def run_gpu(args):
@@ -187,21 +219,27 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     x = {k: v.to(dev) for k, v in t.items()}
     geo = mxa.Geometry.batched(B, L) if w.lengths is None else mxa.Geometry.packed(w.lengths, dev)
+    cross = w.lengths_k is not None
+    gk = mxa.Geometry.packed(w.lengths_k, dev) if cross else geo  # key/value documents
+    kv_geo = gk if cross else None
+    Tk = gk.T
 
-    def alloc_views(H):
-        mk = lambda: mxa.QView(torch.empty((T, H, d), dtype=torch.uint8, device=dev),
-                               torch.empty((H, geo.ntiles, mxa.ATOM_BYTES), dtype=torch.uint8, device=dev))
+    def alloc_views(H, g):
+        mk = lambda: mxa.QView(torch.empty((g.T, H, d), dtype=torch.uint8, device=dev),
+                               torch.empty((H, g.ntiles, mxa.ATOM_BYTES), dtype=torch.uint8, device=dev))
         return mk(), mk()
 
-    qv = {k: alloc_views(Hq if k in ("q", "do") else Hkv) for k in ("q", "k", "v", "do")}
+    qv = {k: alloc_views(Hq, geo) for k in ("q", "do")}
+    qv.update({k: alloc_views(Hkv, gk) for k in ("k", "v")})
     o = torch.empty((T, Hq, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
     dq = torch.empty((T, Hq, d), dtype=torch.bfloat16, device=dev)
-    dk = torch.empty((T, Hkv, d), dtype=torch.bfloat16, device=dev)
-    dv = torch.empty((T, Hkv, d), dtype=torch.bfloat16, device=dev)
+    dk = torch.empty((Tk, Hkv, d), dtype=torch.bfloat16, device=dev)
+    dv = torch.empty((Tk, Hkv, d), dtype=torch.bfloat16, device=dev)
     views = {"q_row": qv["q"][0], "k_row": qv["k"][0], "v_row": qv["v"][0], "g_row": qv["do"][0],
              "q_tok": qv["q"][1], "k_tok": qv["k"][1], "g_tok": qv["do"][1]}
-    bp = mxa.bwd_params(views, o, lse, dq, dk, dv, geo, w.causal, args.dq_mode)
+    bp = mxa.bwd_params(views, o, lse, dq, dk, dv, geo, w.causal, args.dq_mode, kv_geo=kv_geo)
+    fws = torch.empty(max(1, mxa.mxa_fwd_workspace_bytes(mxa.c_fwd_params(bp.shape))), dtype=torch.uint8, device=dev)
     ws = torch.empty(mxa.mxa_bwd_workspace_bytes(bp), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)
@@ -209,13 +247,14 @@ def run_gpu(args):
     def step(src, rec=None):
         e = [ev() for _ in range(4)] if rec is not None else None
         if e: e[0].record(stream)
-        for k in ("q", "k", "v"):
-            mxa.quantize(src[k], geo, out=qv[k])
+        mxa.quantize(src["q"], geo, out=qv["q"])
+        for k in ("k", "v"):
+            mxa.quantize(src[k], gk, out=qv[k])
         if e: e[1].record(stream)
-        mxa.fwd(qv["q"][0], qv["k"][0], qv["v"][1], geo, w.causal, out=(o, lse))
+        mxa.fwd(qv["q"][0], qv["k"][0], qv["v"][1], geo, w.causal, out=(o, lse), workspace=fws, kv_geo=kv_geo)
         if e: e[2].record(stream)
         mxa.quantize(src["do"], geo, out=qv["do"])
-        mxa.bwd(views, o, lse, geo, w.causal, dq_mode=args.dq_mode, workspace=ws, out=(dq, dk, dv))
+        mxa.bwd(views, o, lse, geo, w.causal, dq_mode=args.dq_mode, workspace=ws, out=(dq, dk, dv), kv_geo=kv_geo)
         if e:
             e[3].record(stream)
             rec.append(e)
@@ -249,7 +288,7 @@ def run_gpu(args):
     ms_fwd = statistics.mean(r[1].elapsed_time(r[2]) for r in recs)
     ms_bwd = statistics.mean(r[2].elapsed_time(r[3]) for r in recs)  # includes the dO quantize
 
-    ffwd, fbwd = flops(B, Hq, L, d, w.causal, w.lengths)
+    ffwd, fbwd = flops(B, Hq, L, d, w.causal, w.lengths, w.lengths_k)
     step_flop = ffwd + fbwd
     value = world * step_flop / (ms_step * 1e-3) / 1e15
 
@@ -258,7 +297,7 @@ def run_gpu(args):
     for _ in range(max(3, min(args.steps, 10))):
         a_, b_ = ev(), ev()
         a_.record(stream)
-        mxa.bwd(views, o, lse, geo, w.causal, dq_mode=args.dq_mode, workspace=ws, out=(dq, dk, dv))
+        mxa.bwd(views, o, lse, geo, w.causal, dq_mode=args.dq_mode, workspace=ws, out=(dq, dk, dv), kv_geo=kv_geo)
         b_.record(stream)
         bw_ev.append((a_, b_))
     torch.cuda.synchronize()
@@ -318,8 +357,10 @@ def run_gpu(args):
         "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "mxfp8 (e4m3 codes, ue8m0 scales, fp32 accumulate)", "data": "synthetic",
-        "config": {"workload": "%s: B%d H%d L%d d%d %s, fwd+bwd, dQ %s" % (
-            w.name, B, Hq, L, d, "causal" if w.causal else "non-causal", "fp16x2^9" if args.dq_mode else "fp32"),
+        "config": {"workload": ("%s: B%d H%d L%d d%d %s, fwd+bwd, dQ %s" % (
+            w.name, B, Hq, L, d, "causal" if w.causal else "non-causal", "fp16x2^9" if args.dq_mode else "fp32"))
+            if not cross else ("%s: B%d Lq%d x jagged Lk U[1,%d] (T_k %d) H%d d%d, fwd+bwd, dQ fp32" % (
+                w.name, B, L, max(w.lengths_k), Tk, Hq, d)),
             "global_batch": B * world, "seq_len": L, "heads": Hq, "head_dim": d, "causal": w.causal,
             "parallelism": "replicas" if world > 1 else "single-gpu",
             "l2": "inputs larger than L2 (each bf16 tensor %.0f MB)" % (T * Hq * d * 2 / 1e6),
@@ -338,11 +379,15 @@ def run_gpu(args):
         dt = fl = 0.0
         heads = 0
         while dt < 12.0 and heads < 32:
-            t_, f_, thr = oracle_sample(L=min(L, 4096), H=1, d=d, causal=w.causal, seed=1002 + heads)
+            if cross:
+                t_, f_, thr = oracle_sample_cross(Lq=L, Lk=8192, H=1, d=d, seed=1006 + heads)
+            else:
+                t_, f_, thr = oracle_sample(L=min(L, 4096), H=1, d=d, causal=w.causal, seed=1002 + heads)
             dt, fl, heads = dt + t_, fl + f_, heads + 1
+        what = ("(document, head) pairs of %d x 8192 tokens" % L) if cross else \
+            ("(document, head) pairs of %d tokens" % min(L, 4096))
         out["cpu_baseline"] = {"value": fl / dt / 1e15, "unit": UNIT, "cores": thr, "kind": "oracle",
-                               "sample": "%d (document, head) pairs of %d tokens, d%d (oracle quantize + fwd + bwd), "
-                                         "%.1f s" % (heads, min(L, 4096), d, dt)}
+                               "sample": "%d %s, d%d (oracle quantize + fwd + bwd), %.1f s" % (heads, what, d, dt)}
     if dist is not None:
         dist.destroy_process_group()
     if rank == 0:
@@ -357,16 +402,22 @@ def run_reference(args):
     from block_scaled_mxfp8_gb300 import inputs as inp
 
     w = inp.workload(args.workload, causal=True if args.causal else None)
+    cross = w.lengths_k is not None
     L = min(w.L, 2048)
     total, fl_total, thr = 0.0, 0.0, 1
     for i in range(args.warmup + args.steps):
-        dt, fl, thr = oracle_sample(L=L, H=1, d=w.d, causal=w.causal, seed=1002 + i)
+        if cross:
+            dt, fl, thr = oracle_sample_cross(Lq=w.L, Lk=2048, H=1, d=w.d, seed=1006 + i)
+        else:
+            dt, fl, thr = oracle_sample(L=L, H=1, d=w.d, causal=w.causal, seed=1002 + i)
         if i >= args.warmup:
             total += dt
             fl_total += fl
     v = fl_total / total / 1e15
     sample = "per step one document of %d tokens, 1 head, d%d of the %s workload (oracle quantize + fwd + bwd)" % (
-        L, w.d, w.name)
+        L, w.d, w.name) if not cross else (
+        "per step one document of %d queries x 2048 keys, 1 head, d%d of the %s workload (oracle quantize + fwd + bwd)"
+        % (w.L, w.d, w.name))
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",

@@ -67,10 +67,29 @@ bool make_code_map(CUtensorMap* map, const void* codes, int64_t T, int H, int d)
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-// Most 128-token tiles in one document.
+bool is_cross(const mxa_shape& s) { return s.T_k != 0; }
+
+// Most 128-token tiles in one document (query side).
 int64_t max_doc_tiles(const mxa_shape& s) {
   const int64_t maxlen = s.cu_seqlens ? s.max_seqlen : (s.num_docs > 0 ? s.T / s.num_docs : 0);
   return (maxlen + 127) / 128;
+}
+
+// The two sides of a call: queries, and keys/values (the same for
+// self-attention).
+Side q_side(const mxa_shape& s) {
+  return Side{s.cu_seqlens, s.T, s.ntiles, static_cast<int>(max_doc_tiles(s))};
+}
+Side k_side(const mxa_shape& s) {
+  if (!is_cross(s)) return q_side(s);
+  const int64_t maxlen = s.cu_seqlens_k ? s.max_seqlen_k : (s.num_docs > 0 ? s.T_k / s.num_docs : 0);
+  return Side{s.cu_seqlens_k, s.T_k, s.ntiles_k, static_cast<int>((maxlen + 127) / 128)};
+}
+
+// Longest document of either side, in tokens (sizes the grids).
+int max_len(const mxa_shape& s) {
+  const Side q = q_side(s), k = k_side(s);
+  return static_cast<int>(128 * (q.max_tiles > k.max_tiles ? q.max_tiles : k.max_tiles));
 }
 
 // Bytes of the tile-padded D and LSE rows (both backward paths).
@@ -80,22 +99,25 @@ size_t bwd_rows_bytes(const mxa_shape& s) {
 
 // Bytes of the emitted dS (16 KB of codes + 16 block scales per tile pair).
 size_t bwd_ds_bytes(const mxa_shape& s) {
-  return static_cast<size_t>(s.Hq) * static_cast<size_t>(s.ntiles > 0 ? s.ntiles : 0) *
+  const int64_t ntk = k_side(s).ntiles;
+  return static_cast<size_t>(s.Hq) * static_cast<size_t>(ntk > 0 ? ntk : 0) *
          static_cast<size_t>(max_doc_tiles(s)) * (16384 + 16);
 }
 
-// Bytes of the cost-sorted tile lists of this shape.
-size_t lists_bytes(const mxa_shape& s) {
-  return tile_list_bytes(s.num_docs, s.ntiles > 0 ? s.ntiles : 0);
+// Bytes of one side's cost-sorted tile list.
+size_t list_bytes(const mxa_shape& s, const Side& sd) {
+  return tile_list_bytes(s.num_docs, sd.ntiles > 0 ? sd.ntiles : 0);
 }
 
 // Whether the attention kernels take their CTAs from the tile lists: packed
-// documents (equal documents fill the max_seqlen grid exactly, in the same
-// order), no document longer than the list builder's limit, and a grid of
-// NT x heads CTAs that fits one dimension.
+// documents or cross-attention (equal self-attention documents fill the
+// max_seqlen grid exactly, in the same order), no document longer than the
+// list builder's limit, and grids of NT x heads CTAs that fit one dimension.
 bool uses_list(const mxa_shape& s) {
-  return s.cu_seqlens != nullptr && tile_lists_supported(static_cast<int>(max_doc_tiles(s))) &&
-         s.ntiles * static_cast<int64_t>(s.Hq) <= 0x7FFFFFFFll;
+  const Side q = q_side(s), k = k_side(s);
+  return (s.cu_seqlens != nullptr || is_cross(s)) && tile_lists_supported(q.max_tiles) &&
+         tile_lists_supported(k.max_tiles) && q.ntiles * static_cast<int64_t>(s.Hq) <= 0x7FFFFFFFll &&
+         k.ntiles * static_cast<int64_t>(s.Hkv) <= 0x7FFFFFFFll;
 }
 
 mxa_status check_view(const mxa_qview& v) {
@@ -112,7 +134,21 @@ mxa_status check_shape(const mxa_shape& s) {
   if (s.Hq % s.Hkv != 0) return MXA_ERR_UNSUPPORTED;
   if (!s.cu_seqlens && (s.T % s.num_docs != 0 || s.T / s.num_docs > s.max_seqlen)) return MXA_ERR_ARG;
   if (!(s.softmax_scale >= 0.0f) || !std::isfinite(s.softmax_scale)) return MXA_ERR_ARG;
+  if (is_cross(s)) {
+    if (s.T_k < 0 || s.T_k > 0x7FFFFFFFll || s.ntiles_k <= 0 || s.max_seqlen_k <= 0) return MXA_ERR_ARG;
+    if (!s.cu_seqlens_k && (s.T_k % s.num_docs != 0 || s.T_k / s.num_docs > s.max_seqlen_k)) return MXA_ERR_ARG;
+    if (s.causal) return MXA_ERR_UNSUPPORTED;
+  }
   return MXA_OK;
+}
+
+// Key/value side of the kernel arguments.
+template <class A>
+void set_k_side(A& a, const mxa_shape& s) {
+  const Side k = k_side(s);
+  a.Tk = k.T;
+  a.cu_k = k.cu;
+  a.ntiles_k = k.ntiles;
 }
 
 float alpha_of(const mxa_shape& s) { return s.softmax_scale > 0.0f ? s.softmax_scale : 1.0f / std::sqrt(static_cast<float>(s.d)); }
@@ -219,7 +255,7 @@ mxa_status mxa_quantize(const void* x, int64_t T, int H, int d, const int32_t* c
 
 size_t mxa_fwd_workspace_bytes(const mxa_fwd_params* p) {
   if (!p || check_shape(p->shape) != MXA_OK || !uses_list(p->shape)) return 0;
-  return lists_bytes(p->shape);
+  return list_bytes(p->shape, q_side(p->shape));
 }
 
 mxa_status mxa_fwd(const mxa_fwd_params* p, cudaStream_t stream) {
@@ -232,13 +268,14 @@ mxa_status mxa_fwd(const mxa_fwd_params* p, cudaStream_t stream) {
     return st;
   if (!p->o || !p->lse) return MXA_ERR_ARG;
   if (!aligned(p->o, 16) || !aligned(p->lse, 4)) return MXA_ERR_ALIGN;
-  const bool use_list = p->workspace && uses_list(s) && p->workspace_bytes >= lists_bytes(s);
+  const bool use_list = p->workspace && uses_list(s) && p->workspace_bytes >= list_bytes(s, q_side(s));
   if (use_list && !aligned(p->workspace, 256)) return MXA_ERR_ALIGN;
   if (s.T == 0) return MXA_OK;
+  const Side qs = q_side(s), ks = k_side(s);
   FwdMaps maps;
   if (!make_code_map(&maps.q, p->q_row.codes, s.T, s.Hq, s.d) ||
-      !make_code_map(&maps.k, p->k_row.codes, s.T, s.Hkv, s.d) ||
-      !make_code_map(&maps.v, p->v_tok.codes, s.T, s.Hkv, s.d))
+      !make_code_map(&maps.k, p->k_row.codes, ks.T, s.Hkv, s.d) ||
+      !make_code_map(&maps.v, p->v_tok.codes, ks.T, s.Hkv, s.d))
     return MXA_ERR_CUDA;
   FwdArgs a{};
   a.T = s.T;
@@ -247,6 +284,7 @@ mxa_status mxa_fwd(const mxa_fwd_params* p, cudaStream_t stream) {
   a.cu_seqlens = s.cu_seqlens;
   a.num_docs = s.num_docs;
   a.ntiles = s.ntiles;
+  set_k_side(a, s);
   a.causal = s.causal ? 1 : 0;
   a.alpha = alpha_of(s);
   a.scale_log2 = a.alpha * 1.4426950408889634f;
@@ -256,12 +294,10 @@ mxa_status mxa_fwd(const mxa_fwd_params* p, cudaStream_t stream) {
   a.o = p->o;
   a.lse = p->lse;
   a.err = device_error_word();
-  const int maxlen = s.cu_seqlens ? s.max_seqlen : static_cast<int>(s.T / s.num_docs);
+  const int maxlen = max_len(s);
   if (use_list) {
-    if (launch_tile_lists(s.cu_seqlens, s.num_docs, s.T, a.causal, static_cast<int>(max_doc_tiles(s)), s.ntiles,
-                          p->workspace, stream) != cudaSuccess)
-      return MXA_ERR_CUDA;
-    a.items = tile_list_q(p->workspace);
+    if (launch_tile_list(qs, ks, s.num_docs, a.causal, 0, p->workspace, stream) != cudaSuccess) return MXA_ERR_CUDA;
+    a.items = tile_list_items(p->workspace);
     a.item_count = static_cast<const int32_t*>(p->workspace);
   }
   if (launch_fwd(a, maps, s.d, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
@@ -274,7 +310,8 @@ size_t mxa_bwd_workspace_min_bytes(const mxa_bwd_params* p) {
                d = static_cast<size_t>(p->shape.d);
   // FP16 x 2^9 mode adds its fp16 partial-sum accumulator [T, Hq, d]
   const size_t acc = p->dq_mode == MXA_DQ_FP16_X512 ? T * Hq * d * 2 : 0;
-  return bwd_rows_bytes(p->shape) + lists_bytes(p->shape) + ((acc + 255) & ~size_t(255));
+  return bwd_rows_bytes(p->shape) + list_bytes(p->shape, q_side(p->shape)) + list_bytes(p->shape, k_side(p->shape)) +
+         ((acc + 255) & ~size_t(255));
 }
 
 size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p) {
@@ -296,16 +333,18 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
       !aligned(p->dv, 16))
     return MXA_ERR_ALIGN;
   if (p->dq_mode != MXA_DQ_FP32 && p->dq_mode != MXA_DQ_FP16_X512) return MXA_ERR_ARG;
+  if (is_cross(s) && p->dq_mode != MXA_DQ_FP32) return MXA_ERR_UNSUPPORTED;
   if (!workspace || ws_bytes < mxa_bwd_workspace_min_bytes(p)) return MXA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return MXA_ERR_ALIGN;
   if (s.T == 0) return MXA_OK;
+  const Side qs = q_side(s), ks = k_side(s);
   BwdMaps maps;
   if (!make_code_map(&maps.q, p->q_row.codes, s.T, s.Hq, s.d) ||
-      !make_code_map(&maps.k, p->k_row.codes, s.T, s.Hkv, s.d) ||
-      !make_code_map(&maps.v, p->v_row.codes, s.T, s.Hkv, s.d) ||
+      !make_code_map(&maps.k, p->k_row.codes, ks.T, s.Hkv, s.d) ||
+      !make_code_map(&maps.v, p->v_row.codes, ks.T, s.Hkv, s.d) ||
       !make_code_map(&maps.g, p->g_row.codes, s.T, s.Hq, s.d) ||
       !make_code_map(&maps.qt, p->q_tok.codes, s.T, s.Hq, s.d) ||
-      !make_code_map(&maps.kt, p->k_tok.codes, s.T, s.Hkv, s.d) ||
+      !make_code_map(&maps.kt, p->k_tok.codes, ks.T, s.Hkv, s.d) ||
       !make_code_map(&maps.gt, p->g_tok.codes, s.T, s.Hq, s.d))
     return MXA_ERR_CUDA;
   const size_t T = static_cast<size_t>(s.T), Hq = static_cast<size_t>(s.Hq), d = static_cast<size_t>(s.d);
@@ -313,9 +352,9 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   const size_t dbytes = 2 * pad_elems * 4;
   float* dpad = static_cast<float*>(workspace);
   float* lpad = dpad + pad_elems;
-  void* lists = static_cast<uint8_t*>(workspace) + dbytes;
-  const size_t lbytes = lists_bytes(s);
-  void* acc = static_cast<uint8_t*>(lists) + lbytes;
+  void* qlist = static_cast<uint8_t*>(workspace) + dbytes;
+  void* klist = static_cast<uint8_t*>(qlist) + list_bytes(s, qs);
+  void* acc = static_cast<uint8_t*>(klist) + list_bytes(s, ks);
   const bool fp16 = p->dq_mode == MXA_DQ_FP16_X512;
   const size_t acc_bytes = fp16 ? T * Hq * d * 2 : 0;
   const int maxlen = s.cu_seqlens ? s.max_seqlen : static_cast<int>(s.T / s.num_docs);
@@ -344,6 +383,7 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   a.cu_seqlens = s.cu_seqlens;
   a.num_docs = s.num_docs;
   a.ntiles = s.ntiles;
+  set_k_side(a, s);
   a.causal = s.causal ? 1 : 0;
   a.alpha = alpha_of(s);
   a.scale_log2 = a.alpha * 1.4426950408889634f;
@@ -365,23 +405,26 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   a.err = device_error_word();
   a.mt = static_cast<int>(max_doc_tiles(s));
   if (!fp16 && uses_list(s)) {
-    if (launch_tile_lists(s.cu_seqlens, s.num_docs, s.T, a.causal, a.mt, s.ntiles, lists, stream) != cudaSuccess)
+    if (launch_tile_list(qs, ks, s.num_docs, a.causal, 0, qlist, stream) != cudaSuccess ||
+        launch_tile_list(ks, qs, s.num_docs, a.causal, 1, klist, stream) != cudaSuccess)
       return MXA_ERR_CUDA;
-    a.q_items = tile_list_q(lists);
-    a.k_items = tile_list_k(lists, s.ntiles);
-    a.item_count = static_cast<const int32_t*>(lists);
+    a.q_items = tile_list_items(qlist);
+    a.q_count = static_cast<const int32_t*>(qlist);
+    a.k_items = tile_list_items(klist);
+    a.k_count = static_cast<const int32_t*>(klist);
   }
+  const int amaxlen = max_len(s);  // grids of the attention kernels
   if (!fp16) {
     // FP32: dK/dV kernel, then dQ summed in TMEM in a fixed order -- over the
     // dS the dK/dV kernel emitted when the workspace holds it, else by a
     // kernel that forms dS again
     if (ws_bytes >= mxa_bwd_workspace_bytes(p)) {
       a.ds_codes = static_cast<uint8_t*>(acc);
-      a.ds_sf = a.ds_codes + static_cast<size_t>(s.Hq) * static_cast<size_t>(s.ntiles) * a.mt * 16384;
-      if (launch_bwd_emit(a, maps, s.d, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
+      a.ds_sf = a.ds_codes + static_cast<size_t>(s.Hq) * static_cast<size_t>(ks.ntiles) * a.mt * 16384;
+      if (launch_bwd_emit(a, maps, s.d, amaxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
       return MXA_OK;
     }
-    if (launch_bwd_split(a, maps, s.d, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
+    if (launch_bwd_split(a, maps, s.d, amaxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
     return MXA_OK;
   }
   if (launch_bwd(a, maps, s.d, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;

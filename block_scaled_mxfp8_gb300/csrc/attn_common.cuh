@@ -82,7 +82,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 // Work item of this CTA from a cost-sorted tile list: CTA i takes item i / H
 // for head i % H; false when i / H is past the list's end.
 __device__ __forceinline__ bool list_item(const TileItem* items, const int32_t* count, int H, int& b, int& h,
-                                          int& tile, int64_t& tile_base) {
+                                          int& tile, int64_t& tile_base, int64_t& other_base) {
   const int i = static_cast<int>(blockIdx.x) / H;
   h = static_cast<int>(blockIdx.x) - i * H;
   if (i >= __ldg(count)) return false;
@@ -90,6 +90,7 @@ __device__ __forceinline__ bool list_item(const TileItem* items, const int32_t* 
   b = it.x;
   tile = it.y;
   tile_base = it.z;
+  other_base = it.w;
   return true;
 }
 

@@ -122,27 +122,31 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       bar_dv_done, bar_dk_done, bar_final, bar_drain, bar_drain2;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int64_t s_slot;
+  __shared__ int64_t s_slot, s_slot_k;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int kt, b, hk;
-  int64_t tile_base = -1;
+  int64_t ktile_base = -1, tile_base = -1;  // first scale tiles of the document: keys, queries
   if (a.k_items) {
-    if (!list_item(a.k_items, a.item_count, a.Hkv, b, hk, kt, tile_base)) return;
+    if (!list_item(a.k_items, a.k_count, a.Hkv, b, hk, kt, ktile_base, tile_base)) return;
   } else {
     kt = blockIdx.x;
     b = blockIdx.y;
     hk = blockIdx.z;
   }
   const int grp = a.Hq / a.Hkv;
-  int64_t doc_start, n;
+  int64_t doc_start, n, kdoc_start, nk;  // the document's queries and keys (the same for self-attention)
   doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
-  const int n_tiles = static_cast<int>((n + 127) / 128);
-  if (kt >= n_tiles) return;
+  doc_bounds(a.cu_k, a.num_docs, a.Tk, b, kdoc_start, nk);
+  const int n_tiles = static_cast<int>((n + 127) / 128);  // query tiles
+  if (static_cast<int64_t>(kt) * 128 >= nk) return;
   const int qi0 = a.causal ? kt : 0;
-  const int nq = n_tiles - qi0;
+  const int nq = n_tiles > qi0 ? n_tiles - qi0 : 0;
   const int n_work = nq * grp;
   if (tile_base < 0) tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, kDkdvThreads, &s_slot);
+  if (ktile_base < 0)
+    ktile_base = (a.cu_k == a.cu_seqlens && a.Tk == a.T) ? tile_base
+                                                          : doc_tile_base(a.cu_k, b, nk, tid, kDkdvThreads, &s_slot_k);
 
   if (tid == 0) {
     mbar_init(&bar_kv, 1);
@@ -182,8 +186,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------- producer
-      const int64_t k0 = doc_start + static_cast<int64_t>(kt) * 128;
-      const int64_t katom = (static_cast<int64_t>(hk) * a.ntiles + tile_base + kt) * kAtomBytes;
+      const int64_t k0 = kdoc_start + static_cast<int64_t>(kt) * 128;
+      const int64_t katom = (static_cast<int64_t>(hk) * a.ntiles_k + ktile_base + kt) * kAtomBytes;
       mbar_arrive_expect_tx(&bar_kv, 2 * C::kTileBytes + 2 * kAtomBytes);
       tma_load_3d(smem + C::kOffK, &maps.k, &bar_kv, 0, hk, static_cast<int>(k0));
       tma_load_3d(smem + C::kOffV, &maps.v, &bar_kv, 0, hk, static_cast<int>(k0));
@@ -268,7 +272,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       };
       // Per unit u: dP^T_u once S^T_u has been read out of X, then S^T_{u+1}
       // once dP^T_u has been read; warp 18 issues the gradient MMAs.
-      if (ok) ok = issue_s(0);
+      if (ok && n_work > 0) ok = issue_s(0);
       for (int u = 0; ok && u < n_work; ++u) {
         const int sa = u % C::kStagesA, sb = u % C::kStagesB, t = u & 1;
         const uint64_t da = sdesc_adv(dA, sa * 2 * C::kTileBytes);  // Q, G of this unit
@@ -321,7 +325,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         if (!(ok = role_wait(&bar_ds_ready, u & 1, abort_flag, a.err, kErrTimeoutMma))) break;
         if (a.ds_codes) {  // the staged dS tile of this unit to the workspace
           const int h = hk * grp + u / nq;
-          const int64_t pair = (static_cast<int64_t>(h) * a.ntiles + tile_base + kt) * a.mt + (qi0 + u % nq);
+          const int64_t pair = (static_cast<int64_t>(h) * a.ntiles_k + ktile_base + kt) * a.mt + (qi0 + u % nq);
           bulk_store(a.ds_codes + pair * 16384, smem + C::kOffDsStage, 16384);
         }
         tc_fence_after();
@@ -351,7 +355,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     const int j = quad * 32 + lane;       // key row (TMEM lane)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const int64_t kpos = static_cast<int64_t>(kt) * 128 + j;
-    const bool key_valid = kpos < n;
+    const bool key_valid = kpos < nk;
     const float kb8 = key_valid ? 8.0f : -INFINITY;  // 2^8 boost of P^T; invalid key rows -> 0
     const float sl2 = a.scale_log2;
     const uint64_t kb8x2 = f2_pack(kb8, kb8), sl2x2 = f2_pack(sl2, sl2);
@@ -454,7 +458,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           fence_proxy_async_smem();  // the MMA thread's bulk store reads it
           if (lane == 0) {
             const int h = hk * grp + u / nq;
-            const int64_t pair = (static_cast<int64_t>(h) * a.ntiles + tile_base + kt) * a.mt + qi;
+            const int64_t pair = (static_cast<int64_t>(h) * a.ntiles_k + ktile_base + kt) * a.mt + qi;
             a.ds_sf[pair * 16 + part * 4 + quad] = static_cast<uint8_t>(eb);
           }
         }
@@ -467,7 +471,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     if (ok) ok = role_wait(&bar_final, 0, abort_flag, a.err, kErrTimeoutEpilogue);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
-      const int64_t t = doc_start + kpos;
+      const int64_t t = kdoc_start + kpos;
       __nv_bfloat16* dvrow = reinterpret_cast<__nv_bfloat16*>(a.dv) + (t * a.Hkv + hk) * D;
       __nv_bfloat16* dkrow = reinterpret_cast<__nv_bfloat16*>(a.dk) + (t * a.Hkv + hk) * D;
       // each warp writes D/4 channels of dV and of dK for its key rows
@@ -487,6 +491,10 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           for (int i = 0; i < 16; ++i) rr[i] = r16[i];
         }
         tmem_ld_wait();
+        if (n_work == 0) {  // a document with keys but no queries: zero gradients
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rr[i] = 0u;
+        }
         if (key_valid) store_row_bf16<kCols>(dst, rr, mul);
       }
     }
@@ -511,25 +519,29 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       bar_b_empty[C::kStagesB], bar_sdp_full, bar_x_free, bar_ds_ready, bar_final, bar_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int64_t s_slot;
+  __shared__ int64_t s_slot, s_slot_k;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int b, h, qt;
-  int64_t tile_base = -1;
+  int64_t tile_base = -1, ktile_base = -1;  // first scale tiles of the document: queries, keys
   if (a.q_items) {
-    if (!list_item(a.q_items, a.item_count, a.Hq, b, h, qt, tile_base)) return;
+    if (!list_item(a.q_items, a.q_count, a.Hq, b, h, qt, tile_base, ktile_base)) return;
   } else {
     b = blockIdx.y;
     h = blockIdx.z;
     qt = a.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
   }
   const int hk = h / (a.Hq / a.Hkv);
-  int64_t doc_start, n;
+  int64_t doc_start, n, kdoc_start, nk;  // the document's queries and keys
   doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
+  doc_bounds(a.cu_k, a.num_docs, a.Tk, b, kdoc_start, nk);
   const int n_tiles = static_cast<int>((n + 127) / 128);
   if (qt >= n_tiles) return;
-  const int n_kt = a.causal ? qt + 1 : n_tiles;
+  const int n_kt = a.causal ? qt + 1 : static_cast<int>((nk + 127) / 128);
   if (tile_base < 0) tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, kSplitThreads, &s_slot);
+  if (ktile_base < 0)
+    ktile_base = (a.cu_k == a.cu_seqlens && a.Tk == a.T) ? tile_base
+                                                          : doc_tile_base(a.cu_k, b, nk, tid, kSplitThreads, &s_slot_k);
 
   if (tid == 0) {
     mbar_init(&bar_q, 1);
@@ -573,8 +585,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
       int issued_a = 0, issued_b = 0;
       for (int j = 0; j < n_kt; ++j) {
         const int sa = j % C::kStagesA, sb = j % C::kStagesB;
-        const int k0 = static_cast<int>(doc_start + static_cast<int64_t>(j) * 128);
-        const int64_t katom = (static_cast<int64_t>(hk) * a.ntiles + tile_base + j) * kAtomBytes;
+        const int k0 = static_cast<int>(kdoc_start + static_cast<int64_t>(j) * 128);
+        const int64_t katom = (static_cast<int64_t>(hk) * a.ntiles_k + ktile_base + j) * kAtomBytes;
         if (j >= C::kStagesA &&
             !role_wait(&bar_a_empty[sa], ((j / C::kStagesA) - 1) & 1, abort_flag, a.err, kErrTimeoutTma))
           break;
@@ -646,7 +658,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         mma_commit(&bar_a_empty[sa]);
         return true;
       };
-      if (ok) ok = issue_sdp(0);
+      if (ok && n_kt > 0) ok = issue_sdp(0);
       for (int j = 0; ok && j < n_kt; ++j) {
         const int sb = j % C::kStagesB;
         if (j + 1 < n_kt && !(ok = issue_sdp(j + 1))) break;  // overlaps the dS work of tile j
@@ -694,7 +706,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         tc_fence_before();
         mbar_arrive(&bar_x_free);  // S and dP read: the next tile's S, dP may start
         // keys past the document end (last tile) or after the query (diagonal tile)
-        const int64_t rem = n - static_cast<int64_t>(j) * 128;
+        const int64_t rem = nk - static_cast<int64_t>(j) * 128;
         int lim = rem < 128 ? static_cast<int>(rem) : 128;
         if (a.causal && j == qt) lim = min(lim, r + 1);
 #pragma unroll
@@ -750,7 +762,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 
 cudaError_t launch_bwd_split(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
   const int tiles = (max_seqlen + 127) / 128;
-  const dim3 g1 = a.k_items ? dim3(static_cast<unsigned>(a.ntiles * a.Hkv)) : dim3(tiles, a.num_docs, a.Hkv);
+  const dim3 g1 = a.k_items ? dim3(static_cast<unsigned>(a.ntiles_k * a.Hkv)) : dim3(tiles, a.num_docs, a.Hkv);
   const dim3 g2 = a.q_items ? dim3(static_cast<unsigned>(a.ntiles * a.Hq)) : dim3(tiles, a.num_docs, a.Hq);
   cudaError_t e;
   if (d == 128) {
@@ -777,7 +789,7 @@ cudaError_t launch_bwd_split(const BwdArgs& a, const BwdMaps& m, int d, int max_
 
 cudaError_t launch_bwd_emit(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
   const int tiles = (max_seqlen + 127) / 128;
-  const dim3 g1 = a.k_items ? dim3(static_cast<unsigned>(a.ntiles * a.Hkv)) : dim3(tiles, a.num_docs, a.Hkv);
+  const dim3 g1 = a.k_items ? dim3(static_cast<unsigned>(a.ntiles_k * a.Hkv)) : dim3(tiles, a.num_docs, a.Hkv);
   cudaError_t e;
   if (d == 128) {
     e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,

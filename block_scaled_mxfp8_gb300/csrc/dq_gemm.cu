@@ -56,21 +56,22 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int b, h, qt;
-  int64_t tile_base = -1;
+  int64_t tile_base = -1, ktile_base = -1;  // first scale tiles of the document: queries, keys
   if (a.q_items) {
-    if (!list_item(a.q_items, a.item_count, a.Hq, b, h, qt, tile_base)) return;
+    if (!list_item(a.q_items, a.q_count, a.Hq, b, h, qt, tile_base, ktile_base)) return;
   } else {
     b = blockIdx.y;
     h = blockIdx.z;
     qt = a.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
   }
   const int hk = h / (a.Hq / a.Hkv);
-  int64_t doc_start, n;
+  int64_t doc_start, n, kdoc_start, nk;  // the document's queries and keys
   doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
+  doc_bounds(a.cu_k, a.num_docs, a.Tk, b, kdoc_start, nk);
   const int n_tiles = static_cast<int>((n + 127) / 128);
   if (qt >= n_tiles) return;
-  const int n_kt = a.causal ? qt + 1 : n_tiles;
-  if (tile_base < 0) tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, C::kThreads, &s_slot);
+  const int n_kt = a.causal ? qt + 1 : static_cast<int>((nk + 127) / 128);
+  if (ktile_base < 0) ktile_base = doc_tile_base(a.cu_k, b, nk, tid, C::kThreads, &s_slot);
 
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -103,9 +104,9 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 1)
             !role_wait(&bar_empty[s], ((j / C::kStages) - 1) & 1, abort_flag, a.err, kErrTimeoutTma))
           break;
         // pair (h, b, key tile j, query tile qt)
-        const int64_t pair = (static_cast<int64_t>(h) * a.ntiles + tile_base + j) * a.mt + qt;
-        const int k0 = static_cast<int>(doc_start + static_cast<int64_t>(j) * 128);
-        const int64_t katom = (static_cast<int64_t>(hk) * a.ntiles + tile_base + j) * kAtomBytes;
+        const int64_t pair = (static_cast<int64_t>(h) * a.ntiles_k + ktile_base + j) * a.mt + qt;
+        const int k0 = static_cast<int>(kdoc_start + static_cast<int64_t>(j) * 128);
+        const int64_t katom = (static_cast<int64_t>(hk) * a.ntiles_k + ktile_base + j) * kAtomBytes;
         uint8_t* st = smem + s * C::kStageBytes;
         mbar_arrive_expect_tx(&bar_full[s], 16384 + C::kTileBytes + kAtomBytes + 16);
         bulk_load(st, a.ds_codes + pair * 16384, 16384, &bar_full[s]);  // stored as its swizzled image

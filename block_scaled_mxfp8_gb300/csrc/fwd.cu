@@ -115,13 +115,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   __shared__ float s_l[4][128];      // [column quarter][row] partial row sums
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int64_t s_slot;
+  __shared__ int64_t s_slot, s_slot_k;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int b, h, qt;
-  int64_t tile_base = -1;
+  int64_t tile_base = -1, ktile_base = -1;  // first scale tiles of the document: queries, keys
   if (a.items) {
-    if (!list_item(a.items, a.item_count, a.Hq, b, h, qt, tile_base)) return;
+    if (!list_item(a.items, a.item_count, a.Hq, b, h, qt, tile_base, ktile_base)) return;
   } else {
     // heaviest query tiles first when causal
     b = blockIdx.y;
@@ -129,14 +129,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     qt = a.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
   }
   const int hk = h / (a.Hq / a.Hkv);
-  int64_t doc_start, n;
+  int64_t doc_start, n, kdoc_start, nk;  // the document's queries and keys (the same for self-attention)
   doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
+  doc_bounds(a.cu_k, a.num_docs, a.Tk, b, kdoc_start, nk);
   const int nq_tiles = static_cast<int>((n + 127) / 128);
+  const int nk_tiles = static_cast<int>((nk + 127) / 128);
   if (qt >= nq_tiles) return;
   // visible keys [0, nkeys), walked 256 at a time
-  const int64_t nkeys = a.causal ? min(n, static_cast<int64_t>(qt + 1) * 128) : n;
+  const int64_t nkeys = a.causal ? min(nk, static_cast<int64_t>(qt + 1) * 128) : nk;
   const int n_it = static_cast<int>((nkeys + 255) / 256);
   if (tile_base < 0) tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, C::kThreads, &s_slot);
+  if (ktile_base < 0)
+    ktile_base = (a.cu_k == a.cu_seqlens && a.Tk == a.T) ? tile_base
+                                                          : doc_tile_base(a.cu_k, b, nk, tid, C::kThreads, &s_slot_k);
 
   if (tid == 0) {
     mbar_init(&bar_q, 1);
@@ -193,10 +198,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         const int t0 = 2 * j;  // first 128-key tile of this iteration
         // the second half may lie past the document: reuse the first half's
         // atoms then (its keys are masked; the scales just have to be finite)
-        const int t1 = (t0 + 1 < nq_tiles) ? t0 + 1 : t0;
-        const int k0 = static_cast<int>(doc_start + static_cast<int64_t>(t0) * 128);
-        const int64_t atom0 = (static_cast<int64_t>(hk) * a.ntiles + tile_base + t0) * kAtomBytes;
-        const int64_t atom1 = (static_cast<int64_t>(hk) * a.ntiles + tile_base + t1) * kAtomBytes;
+        const int t1 = (t0 + 1 < nk_tiles) ? t0 + 1 : t0;
+        const int k0 = static_cast<int>(kdoc_start + static_cast<int64_t>(t0) * 128);
+        const int64_t atom0 = (static_cast<int64_t>(hk) * a.ntiles_k + ktile_base + t0) * kAtomBytes;
+        const int64_t atom1 = (static_cast<int64_t>(hk) * a.ntiles_k + ktile_base + t1) * kAtomBytes;
         if (j >= C::kStages &&
             !(ok = role_wait(&bar_k_empty[s], ((j / C::kStages) - 1) & 1, abort_flag, a.err, kErrTimeoutTma)))
           break;
@@ -331,7 +336,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       // columns >= lim are masked (keys past the document end, or after the
       // query on the causal diagonal); only the last iteration has any
       if (j == n_it - 1) {
-        const int64_t rem = n - static_cast<int64_t>(j) * 256;
+        const int64_t rem = nk - static_cast<int64_t>(j) * 256;
         int lim = rem < 256 ? static_cast<int>(rem) : 256;
         if (a.causal) {
           const int64_t c = qpos - static_cast<int64_t>(j) * 256 + 1;

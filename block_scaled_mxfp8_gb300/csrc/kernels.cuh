@@ -26,25 +26,37 @@ __device__ __forceinline__ void doc_bounds(const int32_t* cu, int num_docs, int6
   }
 }
 
-// One work item of the cost-sorted tile lists: (document, 128-token tile,
-// first scale tile of the document, cost in 128-key tiles visited).
+// One work item of a cost-sorted tile list: (document, 128-token tile of the
+// list's side, first scale tile of the document on that side, first scale
+// tile of the document on the other side).  A query list's items are query
+// tiles (the other side: keys and values); a key list's items are key tiles.
 struct alignas(16) TileItem {
-  int32_t doc, tile, tile_base, cost;
+  int32_t doc, tile, tile_base, other_base;
 };
 constexpr int kTileListHeader = 256;     // the item count, padded
 constexpr int kTileListMaxCost = 4094;   // most tiles per document the list builder handles
 
-// Bytes of the lists for num_docs documents and NT = ntiles (256-byte multiple).
+// One side of an attention call: documents of `cu` (device offsets, or
+// nullptr for num_docs equal documents of T / num_docs tokens).
+struct Side {
+  const int32_t* cu;
+  int64_t T;
+  int64_t ntiles;  // NT of its scale layouts
+  int max_tiles;   // 128-token tiles of its longest document
+};
+
+// Bytes of one list over `ntiles` items of num_docs documents (256-byte multiple).
 size_t tile_list_bytes(int num_docs, int64_t ntiles);
 bool tile_lists_supported(int max_tiles);
-// Build both lists into ws (one CTA; stream-ordered).
-cudaError_t launch_tile_lists(const int32_t* cu, int num_docs, int64_t T, int causal, int max_tiles, int64_t ntiles,
-                              void* ws, cudaStream_t stream);
-// The query list and the key list inside a list workspace.
-inline const TileItem* tile_list_q(const void* ws) {
+// Build one list into ws (one CTA; stream-ordered): items are the tiles of
+// `items`, ordered by the tiles of `other` each visits (longest first); with
+// causal (self-attention only) a query tile t visits t + 1 key tiles
+// (key_list = 0) and a key tile t feeds n_t - t query tiles (key_list = 1).
+cudaError_t launch_tile_list(const Side& items, const Side& other, int num_docs, int causal, int key_list, void* ws,
+                             cudaStream_t stream);
+inline const TileItem* tile_list_items(const void* ws) {
   return reinterpret_cast<const TileItem*>(static_cast<const uint8_t*>(ws) + kTileListHeader);
 }
-inline const TileItem* tile_list_k(const void* ws, int64_t ntiles) { return tile_list_q(ws) + ntiles; }
 
 struct QuantArgs {
   const void* x;  // bf16 [T, H, d]
@@ -66,12 +78,16 @@ struct FwdArgs {
   const int32_t* cu_seqlens;
   int num_docs;
   int64_t ntiles;
+  // key/value side (the query side's own values for self-attention)
+  int64_t Tk;
+  const int32_t* cu_k;
+  int64_t ntiles_k;
   int causal;
   float scale_log2;  // alpha * log2(e)
   float alpha;
   const uint8_t* q_sf;  // ROW scales of Q [Hq, NT, 512]
-  const uint8_t* k_sf;  // ROW scales of K [Hkv, NT, 512]
-  const uint8_t* v_sf;  // TOK scales of V [Hkv, NT, 512]
+  const uint8_t* k_sf;  // ROW scales of K [Hkv, NT_k, 512]
+  const uint8_t* v_sf;  // TOK scales of V [Hkv, NT_k, 512]
   void* o;              // bf16 [T, Hq, d]
   float* lse;           // [Hq, T]
   int* err;
@@ -87,6 +103,10 @@ struct BwdArgs {
   const int32_t* cu_seqlens;
   int num_docs;
   int64_t ntiles;
+  // key/value side (the query side's own values for self-attention)
+  int64_t Tk;
+  const int32_t* cu_k;
+  int64_t ntiles_k;
   int causal;
   float scale_log2;
   float alpha;
@@ -101,27 +121,28 @@ struct BwdArgs {
   const float* dpad;     // D, tile-padded [Hq, NT, 128]; 0 on rows past a document's end
   float* dq_acc32;       // [T, Hq, d] (FP32 mode)
   uint16_t* dq_acc16;    // [T, Hq, d] fp16 bits (FP16 x 2^9 mode)
-  void* dk;              // bf16 [T, Hkv, d]
-  void* dv;              // bf16 [T, Hkv, d]
+  void* dk;              // bf16 [Tk, Hkv, d]
+  void* dv;              // bf16 [Tk, Hkv, d]
   void* dq_out;          // bf16 [T, Hq, d] (written directly by the deterministic dQ kernel)
   // dS emitted by the dK/dV kernel for the dQ product (null: the dQ kernel
   // recomputes it).  Tile pair (h, document b, key tile kt, query tile qi)
-  // has index ((h * NT + TB_b + kt) * mt + qi): codes at 16 KB per pair, 128
+  // has index ((h * NT_k + TBk_b + kt) * mt + qi): codes at 16 KB per pair, 128
   // key rows of 128 query bytes kept as their 128-byte-swizzled shared-memory
   // image (16-byte chunk c of row r at chunk c ^ (r % 8)); the 16 UE8M0 block
   // scales of a pair at 16 bytes per pair, byte 4 * (query block) + (key
   // block).
   uint8_t* ds_codes;
   uint8_t* ds_sf;
-  int mt;                // max 128-token tiles of one document
+  int mt;                // max 128-token query tiles of one document
   int dq_mode;
   int* err;
   // cost-sorted tile lists (null: max_seqlen grids); CTA i of the dK/dV
   // kernel takes key item i / Hkv for KV head i % Hkv, the dQ kernels query
   // item i / Hq for head i % Hq
   const TileItem* q_items;
+  const int32_t* q_count;
   const TileItem* k_items;
-  const int32_t* item_count;
+  const int32_t* k_count;
 };
 
 struct PrepArgs {

@@ -45,6 +45,17 @@ class Workload:
     outlier_gain: float = 1.0
     seed: int = 1001
     extra: dict = field(default_factory=dict)
+    lengths_k: Optional[list] = None  # cross-attention: key/value tokens of each document
+
+    @property
+    def T_k(self) -> int:
+        return int(sum(self.lengths_k)) if self.lengths_k is not None else self.T
+
+    @property
+    def cu_seqlens_k(self) -> torch.Tensor:
+        if self.lengths_k is None:
+            return self.cu_seqlens
+        return torch.tensor(np.concatenate([[0], np.cumsum(self.lengths_k)]), dtype=torch.int32)
 
     @property
     def T(self) -> int:
@@ -97,6 +108,12 @@ def workload(name: str, causal: Optional[bool] = None) -> Workload:
         lens = lognormal_lengths(256, 512.0, 1.0, 16, 4096, seed=1004)
         w = Workload("jagged", B=len(lens), L=max(lens), Hq=4, Hkv=4, d=128, causal=True,
                      lengths=lens, seed=1004)
+    elif name == "cross":
+        # cross-attention module: 768 sequences of 512 query tokens against
+        # jagged key/value sets of up to 16384 tokens (uniform, mean ~8192),
+        # model width 384 = 3 heads of 128
+        _, lk = cross_lengths(768, 512, 16384, seed=1006)
+        w = Workload("cross", B=768, L=512, Hq=3, Hkv=3, d=128, causal=False, seed=1006, lengths_k=lk)
     elif name == "tokblock":
         lens = uniform_packed_lengths(8192, 64, 2048, seed=1005)
         w = Workload("tokblock", B=len(lens), L=max(lens), Hq=32, Hkv=8, d=128, causal=True,
@@ -128,7 +145,13 @@ def _randn_bf16(gen: torch.Generator, shape, std: float, outlier_channels: int, 
 
 
 def tensors(w: Workload, with_grad: bool = True) -> dict:
-    """bf16 CPU tensors q [T,Hq,d], k/v [T,Hkv,d] and (with_grad) do [T,Hq,d]."""
+    """bf16 CPU tensors q [T,Hq,d], k/v [T,Hkv,d] (T_k rows for
+    cross-attention) and (with_grad) do [T,Hq,d]."""
+    if w.lengths_k is not None:
+        out = cross_tensors(w.doc_lengths, w.lengths_k, w.Hq, w.Hkv, w.d, w.seed, w.std)
+        if not with_grad:
+            del out["do"]
+        return out
     gen = torch.Generator().manual_seed(w.seed)
     T = w.T
     out = {
@@ -139,3 +162,25 @@ def tensors(w: Workload, with_grad: bool = True) -> dict:
     if with_grad:
         out["do"] = _randn_bf16(gen, (T, w.Hq, w.d), w.std, 0, 1.0)
     return out
+
+
+def cross_lengths(n_docs: int, lq: int, max_k: int, seed: int) -> tuple:
+    """Cross-attention document lengths: every document has lq query tokens
+    and a jagged key/value length drawn uniformly from [1, max_k] (mean about
+    max_k / 2: the "sparsity 0.5" of the production shapes)."""
+    g = torch.Generator().manual_seed(seed)
+    lk = torch.randint(1, max_k + 1, (n_docs,), generator=g).tolist()
+    return [lq] * n_docs, [int(x) for x in lk]
+
+
+def cross_tensors(lq: list, lk: list, Hq: int, Hkv: int, d: int, seed: int, std: float = 1.0) -> dict:
+    """bf16 CPU tensors of a cross-attention call: q, do [sum lq, Hq, d] and
+    k, v [sum lk, Hkv, d], N(0, std^2) from one seeded generator."""
+    gen = torch.Generator().manual_seed(seed)
+    Tq, Tk = int(sum(lq)), int(sum(lk))
+    return {
+        "q": _randn_bf16(gen, (Tq, Hq, d), std, 0, 1.0),
+        "k": _randn_bf16(gen, (Tk, Hkv, d), std, 0, 1.0),
+        "v": _randn_bf16(gen, (Tk, Hkv, d), std, 0, 1.0),
+        "do": _randn_bf16(gen, (Tq, Hq, d), std, 0, 1.0),
+    }

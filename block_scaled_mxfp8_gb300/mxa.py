@@ -52,6 +52,10 @@ class c_shape(ctypes.Structure):
         ("ntiles", ctypes.c_int64),
         ("causal", ctypes.c_int),
         ("softmax_scale", ctypes.c_float),
+        ("T_k", ctypes.c_int64),
+        ("cu_seqlens_k", ctypes.c_void_p),
+        ("max_seqlen_k", ctypes.c_int),
+        ("ntiles_k", ctypes.c_int64),
     ]
 
 
@@ -293,13 +297,22 @@ def quantize(x: torch.Tensor, geo: Geometry, mode: int = MXA_SCALE_MX32, views: 
     return row, tok
 
 
-def _shape(geo: Geometry, Hq: int, Hkv: int, d: int, causal: bool, softmax_scale: float) -> c_shape:
-    return c_shape(geo.T, Hq, Hkv, d, geo.cu_seqlens.data_ptr() if geo.cu_seqlens is not None else None,
-                   geo.num_docs, geo.max_seqlen, geo.ntiles, int(bool(causal)), float(softmax_scale))
+def _shape(geo: Geometry, Hq: int, Hkv: int, d: int, causal: bool, softmax_scale: float,
+           kv_geo: Optional[Geometry] = None) -> c_shape:
+    """kv_geo: the key/value documents of a cross-attention call (None: self-attention)."""
+    sh = c_shape(geo.T, Hq, Hkv, d, geo.cu_seqlens.data_ptr() if geo.cu_seqlens is not None else None,
+                 geo.num_docs, geo.max_seqlen, geo.ntiles, int(bool(causal)), float(softmax_scale))
+    if kv_geo is not None:
+        assert kv_geo.num_docs == geo.num_docs
+        sh.T_k = kv_geo.T
+        sh.cu_seqlens_k = kv_geo.cu_seqlens.data_ptr() if kv_geo.cu_seqlens is not None else None
+        sh.max_seqlen_k = kv_geo.max_seqlen
+        sh.ntiles_k = kv_geo.ntiles
+    return sh
 
 
 def fwd(q_row: QView, k_row: QView, v_tok: QView, geo: Geometry, causal: bool, softmax_scale: float = 0.0,
-        out=None, stream=None, workspace=None, use_list: bool = True):
+        out=None, stream=None, workspace=None, use_list: bool = True, kv_geo: Optional[Geometry] = None):
     """-> (O bf16 [T, Hq, d], LSE fp32 [Hq, T]).  With use_list (default) the
     CTAs are scheduled from the cost-sorted tile list, in `workspace` when it
     is large enough, else in a fresh device buffer."""
@@ -310,7 +323,7 @@ def fwd(q_row: QView, k_row: QView, v_tok: QView, geo: Geometry, causal: bool, s
         lse = torch.empty((Hq, T), dtype=torch.float32, device=q_row.codes.device)
     else:
         o, lse = out
-    p = c_fwd_params(_shape(geo, Hq, Hkv, d, causal, softmax_scale), q_row.c(), k_row.c(), v_tok.c(),
+    p = c_fwd_params(_shape(geo, Hq, Hkv, d, causal, softmax_scale, kv_geo), q_row.c(), k_row.c(), v_tok.c(),
                      o.data_ptr(), lse.data_ptr(), None, 0)
     need = mxa_fwd_workspace_bytes(p) if use_list else 0
     if need:
@@ -323,29 +336,30 @@ def fwd(q_row: QView, k_row: QView, v_tok: QView, geo: Geometry, causal: bool, s
 
 
 def bwd_params(views: dict, o, lse, dq, dk, dv, geo: Geometry, causal: bool, dq_mode: int = MXA_DQ_FP32,
-               softmax_scale: float = 0.0) -> c_bwd_params:
+               softmax_scale: float = 0.0, kv_geo: Optional[Geometry] = None) -> c_bwd_params:
     T, Hq, d = views["q_row"].codes.shape
     Hkv = views["k_row"].codes.shape[1]
-    return c_bwd_params(_shape(geo, Hq, Hkv, d, causal, softmax_scale), views["q_row"].c(), views["k_row"].c(),
+    return c_bwd_params(_shape(geo, Hq, Hkv, d, causal, softmax_scale, kv_geo), views["q_row"].c(), views["k_row"].c(),
                         views["v_row"].c(), views["g_row"].c(), views["q_tok"].c(), views["k_tok"].c(),
                         views["g_tok"].c(), o.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
                         dv.data_ptr(), int(dq_mode))
 
 
 def bwd(views: dict, o, lse, geo: Geometry, causal: bool, dq_mode: int = MXA_DQ_FP32, softmax_scale: float = 0.0,
-        workspace=None, out=None, stream=None):
-    """views: dict with q_row, k_row, v_row, g_row, q_tok, k_tok, g_tok QViews.
-    -> (dQ bf16 [T, Hq, d], dK, dV bf16 [T, Hkv, d])."""
+        workspace=None, out=None, stream=None, kv_geo: Optional[Geometry] = None):
+    """views: dict with q_row, k_row, v_row, g_row, q_tok, k_tok, g_tok QViews
+    (k_*, v_* over kv_geo's tokens for cross-attention).
+    -> (dQ bf16 [T, Hq, d], dK, dV bf16 [Tk, Hkv, d])."""
     T, Hq, d = views["q_row"].codes.shape
-    Hkv = views["k_row"].codes.shape[1]
+    Tk, Hkv = views["k_row"].codes.shape[:2]
     dev = o.device
     if out is None:
         dq = torch.empty((T, Hq, d), dtype=torch.bfloat16, device=dev)
-        dk = torch.empty((T, Hkv, d), dtype=torch.bfloat16, device=dev)
-        dv = torch.empty((T, Hkv, d), dtype=torch.bfloat16, device=dev)
+        dk = torch.empty((Tk, Hkv, d), dtype=torch.bfloat16, device=dev)
+        dv = torch.empty((Tk, Hkv, d), dtype=torch.bfloat16, device=dev)
     else:
         dq, dk, dv = out
-    p = bwd_params(views, o, lse, dq, dk, dv, geo, causal, dq_mode, softmax_scale)
+    p = bwd_params(views, o, lse, dq, dk, dv, geo, causal, dq_mode, softmax_scale, kv_geo)
     need = mxa_bwd_workspace_bytes(p)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)

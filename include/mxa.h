@@ -71,7 +71,7 @@
 extern "C" {
 #endif
 
-#define MXA_ABI_VERSION 2
+#define MXA_ABI_VERSION 3
 
 typedef enum {
   MXA_OK = 0,
@@ -144,9 +144,17 @@ mxa_status mxa_quantize(const void* x_bf16, int64_t T, int H, int d, const int32
                         int max_seqlen, int64_t ntiles, mxa_scale_mode mode, int views, int hadamard,
                         mxa_qview* row, mxa_qview* tok, cudaStream_t stream);
 
-/* Shape shared by the forward and backward calls. */
+/* Shape shared by the forward and backward calls.
+ * Self-attention (T_k = 0): queries, keys and values share one token layout
+ * (T, cu_seqlens, max_seqlen, ntiles).
+ * Cross-attention (T_k > 0): the queries of document b attend to that
+ * document's own keys and values, laid out by T_k, cu_seqlens_k, max_seqlen_k
+ * and ntiles_k (the K and V views are quantized with those); Lq != Lk per
+ * document, e.g. a few hundred query tokens against thousands of jagged
+ * key/value tokens.  No causal mask (causal must be 0), FP32 dQ mode only,
+ * and every document with queries must have at least one key. */
 typedef struct {
-  int64_t T;                  /* total tokens */
+  int64_t T;                  /* total query tokens */
   int Hq, Hkv, d;             /* query heads, key/value heads (Hq % Hkv == 0), head dim (64 or 128) */
   const int32_t* cu_seqlens;  /* device int32 [num_docs + 1], or NULL: num_docs equal documents */
   int num_docs;
@@ -154,6 +162,10 @@ typedef struct {
   int64_t ntiles;             /* NT of the scale layouts used when the views were quantized */
   int causal;                 /* 1: query i sees keys [doc start, i]; 0: the whole document */
   float softmax_scale;        /* alpha; 0 selects 1/sqrt(d) */
+  int64_t T_k;                /* 0: self-attention; else total key/value tokens */
+  const int32_t* cu_seqlens_k;  /* device int32 [num_docs + 1] of the keys, or NULL: equal documents */
+  int max_seqlen_k;           /* longest key/value document */
+  int64_t ntiles_k;           /* NT of the K and V scale layouts */
 } mxa_shape;
 
 typedef struct {
@@ -171,10 +183,11 @@ typedef struct {
  * list of packed documents (FLAMIA notes, Algorithm 2): one item per
  * (document, 128-query tile), so that no CTA is launched for a tile slot past
  * a document's end, ordered by the number of key tiles it visits, longest
- * first (CTA i: item i / Hq, head i % Hq).  256 + 32 * ntiles + 4 * num_docs
+ * first (CTA i: item i / Hq, head i % Hq).  256 + 16 * ntiles + 8 * num_docs
  * bytes, rounded up to 256.  Returns 0 when the list brings nothing (equal
- * documents, cu_seqlens NULL) or cannot be built (max_seqlen above 4094
- * tiles); with workspace NULL or smaller, mxa_fwd launches one CTA per (tile
+ * documents on both sides: cu_seqlens and cu_seqlens_k NULL) or cannot be
+ * built (a side's longest document above 4094 tiles); with workspace NULL or
+ * smaller, mxa_fwd launches one CTA per (tile
  * slot of max_seqlen, document, head).  Every call rebuilds the list on the
  * device (cu_seqlens stays device-only). */
 size_t mxa_fwd_workspace_bytes(const mxa_fwd_params* p);
@@ -191,11 +204,12 @@ typedef struct {
   mxa_qview q_tok;         /* dK = alpha dS^T Q */
   mxa_qview k_tok;         /* dQ = alpha dS K */
   mxa_qview g_tok;         /* dV = P^T G */
+  /* (for cross-attention k_row, v_row, k_tok are the key/value side's views) */
   const void* o;           /* bf16 [T, Hq, d], the forward's output */
   const float* lse;        /* fp32 [Hq, T], the forward's LSE */
   void* dq;                /* out: bf16 [T, Hq, d] */
-  void* dk;                /* out: bf16 [T, Hkv, d] (summed over the query heads of the group) */
-  void* dv;                /* out: bf16 [T, Hkv, d] */
+  void* dk;                /* out: bf16 [T (T_k for cross-attention), Hkv, d], summed over the query heads of the group */
+  void* dv;                /* out: bf16 [T (T_k for cross-attention), Hkv, d] */
   mxa_dq_mode dq_mode;
 } mxa_bwd_params;
 
@@ -203,13 +217,14 @@ typedef struct {
  *   Both modes: D and LSE * log2(e), fp32, each padded to whole 128-token
  *   tiles per document ([Hq, ntiles, 128]); then the key-tile and query-tile
  *   work lists that schedule the dK/dV and dQ CTAs of packed documents as
- *   mxa_fwd schedules its own (256 + 32 * ntiles + 4 * num_docs bytes,
- *   rounded up to 256; reserved in every case).
+ *   mxa_fwd schedules its own (for each of the query and the key side:
+ *   256 + 16 * NT of that side + 8 * num_docs bytes, rounded up to 256;
+ *   reserved in every case).
  *   FP32 mode: plus the dS blocks the dK/dV pass emits for the dQ product --
  *   E4M3 codes (16 KB) and the 16 UE8M0 block scales per (query head, key
- *   tile, query tile of the same document) pair, with mt = ceil(max document
- *   length / 128) query-tile slots per key tile: Hq * ntiles * mt * 16400
- *   bytes (B8 H32 L4096: 4.3 GB).
+ *   tile, query tile of the same document) pair, with mt = ceil(max_seqlen /
+ *   128) query-tile slots per key tile: Hq * NT_k * mt * 16400 bytes, NT_k
+ *   the key side's ntiles (B8 H32 L4096: 4.3 GB).
  *   FP16_X512 mode: plus the fp16 dQ accumulator [T, Hq, d], rounded up to
  *   256 bytes. */
 size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p);

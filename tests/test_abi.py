@@ -31,7 +31,7 @@ def test_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) <= set(mxa.EXPORTS) | set(names)
-    assert mxa.mxa_abi_version() == 2
+    assert mxa.mxa_abi_version() == 3
 
 
 def test_exports_testing_hooks(lib):
@@ -44,9 +44,9 @@ def test_exports_testing_hooks(lib):
 def test_struct_layouts_match_header():
     # sizes of the C structs on this platform (x86-64 / aarch64 LP64)
     assert ctypes.sizeof(mxa.c_qview) == 16
-    assert ctypes.sizeof(mxa.c_shape) == 56
-    assert ctypes.sizeof(mxa.c_fwd_params) == 136
-    assert ctypes.sizeof(mxa.c_bwd_params) == 216
+    assert ctypes.sizeof(mxa.c_shape) == 88
+    assert ctypes.sizeof(mxa.c_fwd_params) == 168
+    assert ctypes.sizeof(mxa.c_bwd_params) == 248
 
 
 def test_scale_tile_helpers(lib):
@@ -129,15 +129,15 @@ def test_fwd_bwd_reject_bad_arguments_without_launch(lib):
     p.shape.softmax_scale = -1.0
     assert L.mxa_fwd(ctypes.byref(p), None) == mxa.MXA_ERR_ARG
     # the tile work list: nothing to do for equal documents (masked or not);
-    # packed documents take 256 bytes of header, 2 x 16 bytes per tile and
-    # 4 per document, rounded up to 256
+    # packed documents take 256 bytes of header, 16 bytes per query tile and
+    # 2 x 4 per document, rounded up to 256
     p = _fwd()
     assert L.mxa_fwd_workspace_bytes(ctypes.byref(p)) == 0
     p.shape.causal = 1
     assert L.mxa_fwd_workspace_bytes(ctypes.byref(p)) == 0
     pj = _fwd(T=1000, nd=3, maxlen=600, nt=10)
     pj.shape.cu_seqlens = 4096  # never read: sizing needs no device data
-    assert L.mxa_fwd_workspace_bytes(ctypes.byref(pj)) == 768  # 256 + 2 * 10 * 16 + 3 * 4 = 588
+    assert L.mxa_fwd_workspace_bytes(ctypes.byref(pj)) == 512  # 256 + 10 * 16 + 2 * 3 * 4 = 440
     pj.workspace, pj.workspace_bytes = 8, 768  # used, but not 256-byte aligned
     assert L.mxa_fwd(ctypes.byref(pj), None) == mxa.MXA_ERR_ALIGN
     sh = mxa.c_shape(256, 2, 2, 128, None, 1, 256, 2, 1, 0.0)
@@ -147,7 +147,7 @@ def test_fwd_bwd_reject_bad_arguments_without_launch(lib):
     # padded D and LSE rows [Hq, NT, 128] fp32; fp32 mode adds the emitted dS:
     # one 16 KB code tile + 16 block scales per (head, key tile, query-tile
     # slot) pair
-    assert need_min == 2 * 2 * 2 * 128 * 4 + 512  # + the tile lists
+    assert need_min == 2 * 2 * 2 * 128 * 4 + 2 * 512  # + the query and key tile lists
     assert need == need_min + 2 * 2 * 2 * (16384 + 16)
     assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), need_min - 1, None) == mxa.MXA_ERR_WORKSPACE
     assert L.mxa_bwd(ctypes.byref(bp), None, need, None) == mxa.MXA_ERR_WORKSPACE
@@ -156,3 +156,30 @@ def test_fwd_bwd_reject_bad_arguments_without_launch(lib):
     bp.dq_mode = 1
     # FP16 x 2^9 mode: the fp16 dQ accumulator instead of the emitted dS
     assert L.mxa_bwd_workspace_bytes(ctypes.byref(bp)) == need_min + 256 * 2 * 128 * 2
+
+
+def test_cross_attention_shape_checks(lib):
+    """Cross-attention (T_k > 0): no causal mask, FP32 dQ only, equal key
+    documents must divide T_k; the list sizes follow each side's NT."""
+    L = lib
+    p = _fwd(T=1024, nd=2, maxlen=512, nt=8)
+    p.shape.T_k, p.shape.max_seqlen_k, p.shape.ntiles_k = 4096, 2048, 32
+    # equal documents on both sides but Lq != Lk: a work list (8 query tiles)
+    assert L.mxa_fwd_workspace_bytes(ctypes.byref(p)) == 512  # 256 + 8 * 16 + 2 * 2 * 4 = 400
+    p.shape.causal = 1
+    assert L.mxa_fwd(ctypes.byref(p), None) == mxa.MXA_ERR_UNSUPPORTED
+    p.shape.causal = 0
+    p.shape.T_k = 4095  # not divisible by the 2 documents
+    assert L.mxa_fwd(ctypes.byref(p), None) == mxa.MXA_ERR_ARG
+    p.shape.T_k, p.shape.max_seqlen_k = 4096, 1000  # documents longer than max_seqlen_k
+    assert L.mxa_fwd(ctypes.byref(p), None) == mxa.MXA_ERR_ARG
+    sh = mxa.c_shape(1024, 2, 2, 128, None, 2, 512, 8, 0, 0.0)
+    sh.T_k, sh.max_seqlen_k, sh.ntiles_k = 4096, 2048, 32
+    bp = mxa.c_bwd_params(sh, *[_qv()] * 7, 256, 256, 256, 256, 256, 0)
+    need_min = L.mxa_bwd_workspace_min_bytes(ctypes.byref(bp))
+    # rows [Hq, NT_q, 128] x 2 fp32, then the query list (8 tiles) and the key list (32 tiles)
+    assert need_min == 2 * 2 * 8 * 128 * 4 + 512 + 1024  # 256 + 32 * 16 + 16 = 784 -> 1024
+    # the emitted dS: Hq x NT_k x mt(query tiles of the longest document) pairs
+    assert L.mxa_bwd_workspace_bytes(ctypes.byref(bp)) == need_min + 2 * 32 * 4 * (16384 + 16)
+    bp.dq_mode = 1
+    assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), 1 << 30, None) == mxa.MXA_ERR_UNSUPPORTED

@@ -72,8 +72,8 @@ SCHED_CASES = [
 def test_fwd_work_list_schedule(w):
     """The cost-sorted work list (FLAMIA notes, Algorithm 2) only changes
     which CTA computes which tile: O and LSE are bit-identical to the
-    max_seqlen grid.  The lists hold every (document, tile) pair once, the
-    items that visit the most tiles first."""
+    max_seqlen grid.  The list holds every (document, query tile) pair once,
+    the items that visit the most key tiles first."""
     from block_scaled_mxfp8_gb300 import mxa
 
     t = inp.tensors(w, with_grad=False)
@@ -95,12 +95,12 @@ def test_fwd_work_list_schedule(w):
     count = int(raw[:4].view(np.int32)[0])
     assert count == len(pairs)
     nt = geo.ntiles
-    items = raw[256:256 + 2 * nt * 16].view(np.int32).reshape(2, nt, 4)[:, :count]
+    it = raw[256:256 + nt * 16].view(np.int32).reshape(nt, 4)[:count]
     base = np.concatenate([[0], np.cumsum(tiles)])[:-1]
-    for which, cost_of in ((0, lambda b, t_: t_ + 1 if w.causal else tiles[b]),
-                           (1, lambda b, t_: tiles[b] - t_ if w.causal else tiles[b])):
-        it = items[which]
-        assert sorted(map(tuple, it[:, :2].tolist())) == pairs
-        assert all(it[i, 2] == base[it[i, 0]] for i in range(count))
-        assert all(it[i, 3] == cost_of(it[i, 0], it[i, 1]) for i in range(count))
-        assert all(it[i, 3] >= it[i + 1, 3] for i in range(count - 1))
+    # the forward's query list: every (document, tile) once, with the first
+    # scale tile of its document on both sides (the same for self-attention),
+    # ordered by the key tiles each query tile visits, most first
+    assert sorted(map(tuple, it[:, :2].tolist())) == pairs
+    assert all(it[i, 2] == base[it[i, 0]] and it[i, 3] == base[it[i, 0]] for i in range(count))
+    cost = [it[i, 1] + 1 if w.causal else tiles[it[i, 0]] for i in range(count)]
+    assert all(cost[i] >= cost[i + 1] for i in range(count - 1))
