@@ -317,6 +317,146 @@ void orc_quant_tokblock(const uint16_t* x, int64_t T, int H, int d, const int32_
 }
 
 /* ------------------------------------------------------------------------ */
+/* RMSNorm feeding the quantizers (fused producer)                           */
+/* ------------------------------------------------------------------------ */
+
+/* RMSNorm of every (token, head) vector of x (bf16 bits [T, H, d]) in IEEE
+ * fp32 ([FA4 write-up], "Fused RMSNorm+Quantize": the normalization runs as
+ * the prologue of the quantizer that reads the data anyway).  The fp32
+ * sequence is the reading taken so that the codes computed from y match bit
+ * for bit:
+ *   s_k = sum of x_c * x_c over channels 16k .. 16k + 15, in channel order;
+ *   s = the d/16 partial sums added pairwise: (s0 + s1), (s2 + s3), ... then
+ *       the pairs of those, and so on;
+ *   r = 1 / sqrt(s / d + eps) (correctly rounded sqrt and division), 0 when
+ *       s / d + eps is 0;
+ *   y_c = (x_c * r) * w_c (w == NULL: w_c = 1).
+ * y: fp32 [T, H, d]. */
+void orc_rmsnorm_f32(const uint16_t* x, int64_t T, int H, int d, const float* w, float eps, float* y)
+{
+    int nk = d / 16;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T * H; ++r) {
+        const uint16_t* xs = x + r * d;
+        float part[8];
+        for (int k = 0; k < nk; ++k) {
+            float acc = 0.0f;
+            for (int i = 0; i < 16; ++i) {
+                float v = (float)orc_bf16_to_double(xs[16 * k + i]);
+                float sq = v * v;
+                acc = acc + sq;
+            }
+            part[k] = acc;
+        }
+        for (int span = 1; span < nk; span *= 2)
+            for (int k = 0; k + span < nk; k += 2 * span)
+                part[k] = part[k] + part[k + span];
+        float ms = part[0] / (float)d;
+        float den = ms + eps;
+        float rr = den == 0.0f ? 0.0f : 1.0f / sqrtf(den);
+        for (int c = 0; c < d; ++c) {
+            float v = (float)orc_bf16_to_double(xs[c]);
+            float t = v * rr;
+            y[r * d + c] = w ? t * w[c] : t;
+        }
+    }
+}
+
+/* The quantizers of fp32 input (the RMSNorm output): the same rules as
+ * orc_quant_row, orc_quant_tok and orc_quant_tokblock, reading fp32 values. */
+void orc_quant_row_f32(const float* x, int64_t T, int H, int d, uint8_t* codes, uint8_t* scales)
+{
+    int G = d / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int h = 0; h < H; ++h)
+            for (int g = 0; g < G; ++g) {
+                const float* xs = x + (t * H + h) * d + g * 32;
+                double amax = 0.0;
+                for (int i = 0; i < 32; ++i) {
+                    double v = fabs((double)xs[i]);
+                    if (v > amax)
+                        amax = v;
+                }
+                int e = orc_mx_exponent(amax);
+                for (int i = 0; i < 32; ++i)
+                    codes[(t * H + h) * d + g * 32 + i] = orc_e4m3_encode(ldexp((double)xs[i], -e));
+                scales[(t * H + h) * G + g] = (uint8_t)(e + 127);
+            }
+}
+
+void orc_quant_tok_f32(const float* x, int64_t T, int H, int d, const int32_t* cu, int ndocs, uint8_t* codes,
+                       uint8_t* scales)
+{
+    int nd = num_docs_eff(cu, ndocs);
+    int64_t NB = orc_total_blocks(cu, ndocs, T);
+    for (int b = 0; b < nd; ++b) {
+        int64_t s, e;
+        doc_range(cu, ndocs, T, b, &s, &e);
+        int64_t boff = orc_block_offset(cu, ndocs, T, b);
+        int64_t nbk = nblk32(e - s);
+#pragma omp parallel for schedule(static)
+        for (int64_t kb = 0; kb < nbk; ++kb) {
+            int64_t t0 = s + kb * 32, t1 = t0 + 32 < e ? t0 + 32 : e;
+            for (int h = 0; h < H; ++h)
+                for (int c = 0; c < d; ++c) {
+                    double amax = 0.0;
+                    for (int64_t t = t0; t < t1; ++t) {
+                        double v = fabs((double)x[(t * H + h) * d + c]);
+                        if (v > amax)
+                            amax = v;
+                    }
+                    int ex = orc_mx_exponent(amax);
+                    for (int64_t t = t0; t < t1; ++t)
+                        codes[(t * H + h) * d + c] = orc_e4m3_encode(ldexp((double)x[(t * H + h) * d + c], -ex));
+                    scales[((int64_t)h * d + c) * NB + boff + kb] = (uint8_t)(ex + 127);
+                }
+        }
+    }
+}
+
+void orc_quant_tokblock_f32(const float* x, int64_t T, int H, int d, const int32_t* cu, int ndocs, int hadamard,
+                            uint8_t* codes, uint8_t* scales)
+{
+    int nd = num_docs_eff(cu, ndocs);
+    int64_t NB = orc_total_blocks(cu, ndocs, T);
+    float* y = (float*)malloc(sizeof(float) * (size_t)T * H * d);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T * H; ++r) {
+        if (hadamard)
+            orc_hadamard128_f32(x + r * d, y + r * d);
+        else
+            for (int i = 0; i < d; ++i)
+                y[r * d + i] = x[r * d + i];
+    }
+    for (int b = 0; b < nd; ++b) {
+        int64_t s, e;
+        doc_range(cu, ndocs, T, b, &s, &e);
+        int64_t boff = orc_block_offset(cu, ndocs, T, b);
+        int64_t nbk = nblk32(e - s);
+#pragma omp parallel for schedule(static)
+        for (int64_t kb = 0; kb < nbk; ++kb) {
+            int64_t t0 = s + kb * 32, t1 = t0 + 32 < e ? t0 + 32 : e;
+            for (int h = 0; h < H; ++h) {
+                double amax = 0.0;
+                for (int64_t t = t0; t < t1; ++t)
+                    for (int c = 0; c < d; ++c) {
+                        double v = fabs((double)y[(t * H + h) * d + c]);
+                        if (v > amax)
+                            amax = v;
+                    }
+                int ex = orc_mx_exponent(amax);
+                for (int64_t t = t0; t < t1; ++t)
+                    for (int c = 0; c < d; ++c)
+                        codes[(t * H + h) * d + c] = orc_e4m3_encode(ldexp((double)y[(t * H + h) * d + c], -ex));
+                scales[(int64_t)h * NB + boff + kb] = (uint8_t)(ex + 127);
+            }
+        }
+    }
+    free(y);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Dequantization (exact in fp64): value = decode(code) * 2^(byte - 127)      */
 /* ------------------------------------------------------------------------ */
 

@@ -77,6 +77,10 @@ def _L():
                 "orc_dequant_tokblock": (None, [P, P, i64, i32, i32, P, i32, P]),
                 "orc_attn_fwd": (None, [P, P, P, i64, i32, i32, i32, P, i32, i32, f64, P, i64, P, P]),
                 "orc_attn_bwd": (None, [P] * 8 + [i64, i32, i32, i32, P, i32, i32, f64, P, i32] + [P] * 6),
+                "orc_rmsnorm_f32": (None, [P, i64, i32, i32, P, ctypes.c_float, P]),
+                "orc_quant_row_f32": (None, [P, i64, i32, i32, P, P]),
+                "orc_quant_tok_f32": (None, [P, i64, i32, i32, P, i32, P, P]),
+                "orc_quant_tokblock_f32": (None, [P, i64, i32, i32, P, i32, i32, P, P]),
                 "orc_attn_fwd_x": (None, [P, P, P, i64, i64, i32, i32, i32, P, P, i32, f64, P, P]),
                 "orc_attn_bwd_x": (None, [P] * 8 + [i64, i64, i32, i32, i32, P, P, i32, f64] + [P] * 6),
                 "orc_num_threads": (i32, []),
@@ -195,6 +199,54 @@ def quant_tok(x, cu_seqlens=None):
     codes = np.zeros((T, H, d), np.uint8)
     scales = np.zeros((H, d, NB), np.uint8)
     _L().orc_quant_tok(_p(xu), T, H, d, _p(cu), nd, _p(codes), _p(scales))
+    return codes, scales
+
+
+def rmsnorm_f32(x, weight=None, eps=1e-6):
+    """RMSNorm of every (token, head) vector in IEEE fp32 in the written order
+    of orc_rmsnorm_f32.  x bf16 [T,H,d]; weight fp32 [d] or None.
+    -> float32 [T,H,d]."""
+    xu = _u16(x)
+    T, H, d = xu.shape
+    y = np.empty((T, H, d), np.float32)
+    w = None if weight is None else np.ascontiguousarray(np.asarray(weight, dtype=np.float32))
+    _L().orc_rmsnorm_f32(_p(xu), T, H, d, _p(w), float(eps), _p(y))
+    return y
+
+
+def quant_row_f32(y):
+    """quant_row of fp32 values y [T,H,d]."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    T, H, d = y.shape
+    codes = np.empty((T, H, d), np.uint8)
+    scales = np.empty((T, H, d // 32), np.uint8)
+    _L().orc_quant_row_f32(_p(y), T, H, d, _p(codes), _p(scales))
+    return codes, scales
+
+
+def quant_tok_f32(y, cu_seqlens=None):
+    """quant_tok of fp32 values y [T,H,d]."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    T, H, d = y.shape
+    cu, nd = _cu(cu_seqlens)
+    NB = total_blocks(cu_seqlens, T)
+    codes = np.zeros((T, H, d), np.uint8)
+    scales = np.zeros((H, d, NB), np.uint8)
+    _L().orc_quant_tok_f32(_p(y), T, H, d, _p(cu), nd, _p(codes), _p(scales))
+    return codes, scales
+
+
+def quant_tokblock_f32(y, cu_seqlens=None, hadamard=False):
+    """quant_tokblock of fp32 values y [T,H,d]."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    T, H, d = y.shape
+    if hadamard and d != 128:
+        raise ValueError("hadamard rotation needs d == 128")
+    cu, nd = _cu(cu_seqlens)
+    NB = total_blocks(cu_seqlens, T)
+    codes = np.zeros((T, H, d), np.uint8)
+    scales = np.zeros((H, NB), np.uint8)
+    _L().orc_quant_tokblock_f32(_p(y), T, H, d, _p(cu), nd, int(bool(hadamard)), _p(codes), _p(scales))
     return codes, scales
 
 
