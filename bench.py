@@ -303,6 +303,44 @@ def run_gpu(args):
     torch.cuda.synchronize()
     ms_bwd_only = statistics.mean(a_.elapsed_time(b_) for a_, b_ in bw_ev)
 
+    # fused RMSNorm + quantize of Q into both views (one pass over x) against
+    # torch's RMSNorm followed by the quantizer (the normalization as a pass of
+    # its own); effective bandwidth = algorithmic bytes (x read once, codes and
+    # scales of both views written) / time
+    rms = None
+    try:
+        import torch.nn.functional as F
+
+        wq = (torch.rand(d, generator=torch.Generator().manual_seed(7)) + 0.5).to(dev)
+        wq16 = wq.to(torch.bfloat16)
+        xq = x["q"]
+
+        def fused():
+            mxa.quantize(xq, geo, out=qv["q"], rmsnorm=(wq, 1e-6))
+
+        def unfused():
+            mxa.quantize(F.rms_norm(xq, (d,), weight=wq16, eps=1e-6), geo, out=qv["q"])
+
+        res = {}
+        for nm, fn in (("fused", fused), ("unfused", unfused)):
+            for _ in range(3):
+                fn()
+            a_, b_ = ev(), ev()
+            a_.record(stream)
+            for _ in range(10):
+                fn()
+            b_.record(stream)
+            torch.cuda.synchronize()
+            res[nm] = a_.elapsed_time(b_) / 10
+        nbytes = T * Hq * d * 2 + 2 * (T * Hq * d + T * Hq * d // 32)
+        rms = {"tensor": "q [T, Hq, d] bf16, both views", "fused_ms": round(res["fused"], 4),
+               "unfused_ms": round(res["unfused"], 4), "fused_tbps": round(nbytes / res["fused"] / 1e9, 3),
+               "unfused_tbps": round(nbytes / res["unfused"] / 1e9, 3),
+               "speedup": round(res["unfused"] / res["fused"], 2)}
+        mxa.check_error()
+    except (AttributeError, RuntimeError) as exc:  # torch without rms_norm
+        rms = {"unavailable": str(exc)[:200]}
+
     pk = peaks()
     fwd_pf = ffwd / (ms_fwd * 1e-3) / 1e15
     bwd_pf = fbwd / (ms_bwd_only * 1e-3) / 1e15
@@ -370,6 +408,7 @@ def run_gpu(args):
         "ms": {"quantize_qkv": round(ms_quant, 3), "fwd": round(ms_fwd, 3), "quantize_do_plus_bwd": round(ms_bwd, 3),
                "bwd": round(ms_bwd_only, 3)},
         "roofline": roofline,
+        "rmsnorm_quantize": rms,
         "e2e": e2e,
         "gpu_launches": 8 * args.steps,
         "clocks": clk.summary(),

@@ -201,9 +201,14 @@ size_t mxa_scale_bytes(int H, int64_t ntiles) {
   return static_cast<size_t>(H) * static_cast<size_t>(ntiles) * kAtomBytes;
 }
 
-mxa_status mxa_quantize(const void* x, int64_t T, int H, int d, const int32_t* cu_seqlens, int num_docs,
-                        int max_seqlen, int64_t ntiles, mxa_scale_mode mode, int views, int hadamard,
-                        mxa_qview* row, mxa_qview* tok, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+mxa_status quantize_impl(const void* x, int64_t T, int H, int d, const int32_t* cu_seqlens, int num_docs,
+                         int max_seqlen, int64_t ntiles, mxa_scale_mode mode, int views, int hadamard,
+                         mxa_qview* row, mxa_qview* tok, int rms, const float* rms_w, float rms_eps,
+                         cudaStream_t stream) {
   if (!x || T < 0 || T > 0x7FFFFFFFll || H <= 0 || H > 65535 || num_docs <= 0 || num_docs > 65535 ||
       ntiles <= 0 || max_seqlen <= 0)
     return MXA_ERR_ARG;
@@ -248,9 +253,33 @@ mxa_status mxa_quantize(const void* x, int64_t T, int H, int d, const int32_t* c
   a.row_scales = (w_row || tokblock) ? row->scales : nullptr;
   a.tok_codes = (w_tok && !tokblock) ? tok->codes : nullptr;
   a.tok_scales = (w_tok || tokblock) ? tok->scales : nullptr;
+  a.rms = rms;
+  a.rms_w = rms_w;
+  a.rms_eps = rms_eps;
   const int max_groups = (cu_seqlens ? max_seqlen : static_cast<int>(T / num_docs)) + 31;
   if (launch_quantize(a, d, tokblock, hadamard != 0, max_groups / 32, stream) != cudaSuccess) return MXA_ERR_CUDA;
   return MXA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mxa_status mxa_quantize(const void* x, int64_t T, int H, int d, const int32_t* cu_seqlens, int num_docs,
+                        int max_seqlen, int64_t ntiles, mxa_scale_mode mode, int views, int hadamard,
+                        mxa_qview* row, mxa_qview* tok, cudaStream_t stream) {
+  return quantize_impl(x, T, H, d, cu_seqlens, num_docs, max_seqlen, ntiles, mode, views, hadamard, row, tok, 0,
+                       nullptr, 0.0f, stream);
+}
+
+mxa_status mxa_rmsnorm_quantize(const void* x, const float* weight, float eps, int64_t T, int H, int d,
+                                const int32_t* cu_seqlens, int num_docs, int max_seqlen, int64_t ntiles,
+                                mxa_scale_mode mode, int views, int hadamard, mxa_qview* row, mxa_qview* tok,
+                                cudaStream_t stream) {
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return MXA_ERR_ARG;
+  if (weight && !aligned(weight, 4)) return MXA_ERR_ALIGN;
+  return quantize_impl(x, T, H, d, cu_seqlens, num_docs, max_seqlen, ntiles, mode, views, hadamard, row, tok, 1,
+                       weight, eps, stream);
 }
 
 size_t mxa_fwd_workspace_bytes(const mxa_fwd_params* p) {

@@ -70,6 +70,11 @@ struct QuantArgs {
   uint8_t* row_scales;  // [H, NT, 512]
   uint8_t* tok_codes;
   uint8_t* tok_scales;  // [H, NT, 512]
+  // RMSNorm prologue (rms != 0): every (token, head) vector becomes
+  // x / sqrt(mean(x^2) + rms_eps) * rms_w before it is quantized
+  int rms;
+  const float* rms_w;  // fp32 [d] or null (all ones)
+  float rms_eps;
 };
 
 struct FwdArgs {

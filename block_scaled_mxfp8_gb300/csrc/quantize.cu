@@ -105,6 +105,26 @@ __global__ void __launch_bounds__(QCfg<D>::kThreads) quantize_kernel(QuantArgs a
     for (int i = 0; i < 16; ++i) v[i] = 0.0f;
   }
 
+  if (a.rms) {
+    // RMSNorm in IEEE fp32, in a fixed order: this thread's 16 squares in
+    // channel order, then the TPR partial sums of the row pairwise (xor 1, 2,
+    // 4: every lane of the row ends with the same tree sum); r = 1 / sqrt(s /
+    // d + eps) with correctly rounded sqrt and division (0 when s / d + eps
+    // is 0); y = (x * r) * w.  (FA4 write-up, "Fused RMSNorm+Quantize".)
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ss = __fadd_rn(ss, __fmul_rn(v[i], v[i]));
+#pragma unroll
+    for (int o = 1; o < C::TPR; o <<= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+    const float den = __fadd_rn(__fdiv_rn(ss, static_cast<float>(D)), a.rms_eps);
+    const float r = den == 0.0f ? 0.0f : __fdiv_rn(1.0f, __fsqrt_rn(den));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float t = __fmul_rn(v[i], r);
+      v[i] = a.rms_w ? __fmul_rn(t, __ldg(a.rms_w + chunk * 16 + i)) : t;
+    }
+  }
+
   if constexpr (HAD) {
     // Sylvester order: in-thread stages h = 1, 2, 4, 8, then across the 8
     // threads of the row for h = 16, 32, 64 (chunk bits 0, 1, 2).

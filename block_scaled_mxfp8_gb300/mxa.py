@@ -95,7 +95,7 @@ _lib = None
 
 EXPORTS = [
     "mxa_abi_version", "mxa_status_str", "mxa_scale_tiles", "mxa_scale_tiles_bound", "mxa_scale_bytes",
-    "mxa_quantize", "mxa_fwd", "mxa_fwd_workspace_bytes", "mxa_bwd_workspace_bytes", "mxa_bwd_workspace_min_bytes", "mxa_bwd",
+    "mxa_quantize", "mxa_rmsnorm_quantize", "mxa_fwd", "mxa_fwd_workspace_bytes", "mxa_bwd_workspace_bytes", "mxa_bwd_workspace_min_bytes", "mxa_bwd",
     "mxa_bwd_noalloc", "mxa_get_error",
 ]
 # include/mxa_testing.h: the kernels' P and dS quantization run on caller data
@@ -124,6 +124,9 @@ def lib():
         L.mxa_quantize.restype = i32
         L.mxa_quantize.argtypes = [P, i64, i32, i32, P, i32, i32, i64, i32, i32, i32,
                                    ctypes.POINTER(c_qview), ctypes.POINTER(c_qview), P]
+        L.mxa_rmsnorm_quantize.restype = i32
+        L.mxa_rmsnorm_quantize.argtypes = [P, P, ctypes.c_float, i64, i32, i32, P, i32, i32, i64, i32, i32, i32,
+                                           ctypes.POINTER(c_qview), ctypes.POINTER(c_qview), P]
         L.mxa_fwd.restype = i32
         L.mxa_fwd.argtypes = [ctypes.POINTER(c_fwd_params), P]
         L.mxa_fwd_workspace_bytes.restype = ctypes.c_size_t
@@ -273,9 +276,11 @@ class Geometry:
 
 
 def quantize(x: torch.Tensor, geo: Geometry, mode: int = MXA_SCALE_MX32, views: int = MXA_VIEW_ROW | MXA_VIEW_TOK,
-             hadamard: bool = False, out=None, stream=None):
+             hadamard: bool = False, out=None, stream=None, rmsnorm=None):
     """x bf16 [T, H, d] on the GPU -> (row QView or None, tok QView or None).
-    In token-block mode both views share one code tensor."""
+    In token-block mode both views share one code tensor.  rmsnorm: None, or
+    (weight fp32 [d] on the GPU or None, eps) to quantize the RMSNorm of x
+    (mxa_rmsnorm_quantize)."""
     T, H, d = x.shape
     assert T == geo.T and x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous()
     sb = mxa_scale_bytes(H, geo.ntiles)
@@ -291,9 +296,18 @@ def quantize(x: torch.Tensor, geo: Geometry, mode: int = MXA_SCALE_MX32, views: 
             codes = row.codes if mode == MXA_SCALE_TOKBLOCK32 else torch.empty((T, H, d), dtype=torch.uint8, device=dev)
             tok = QView(codes, torch.empty((H, geo.ntiles, ATOM_BYTES), dtype=torch.uint8, device=dev))
     assert row is None or row.scales.numel() == sb
-    st = mxa_quantize(x, T, H, d, geo.cu_seqlens, geo.num_docs, geo.max_seqlen, geo.ntiles, mode, views, hadamard,
-                      row.c() if row is not None else None, tok.c() if tok is not None else None, stream)
-    _check(st, "mxa_quantize")
+    if rmsnorm is None:
+        st = mxa_quantize(x, T, H, d, geo.cu_seqlens, geo.num_docs, geo.max_seqlen, geo.ntiles, mode, views,
+                          hadamard, row.c() if row is not None else None, tok.c() if tok is not None else None, stream)
+        _check(st, "mxa_quantize")
+    else:
+        w, eps = rmsnorm
+        assert w is None or (w.dtype == torch.float32 and w.is_cuda and w.numel() == d)
+        st = lib().mxa_rmsnorm_quantize(_ptr(x), _ptr(w), float(eps), T, H, d, _ptr(geo.cu_seqlens), geo.num_docs,
+                                        geo.max_seqlen, geo.ntiles, mode, views, int(bool(hadamard)),
+                                        ctypes.byref(row.c()) if row is not None else None,
+                                        ctypes.byref(tok.c()) if tok is not None else None, _stream(stream))
+        _check(st, "mxa_rmsnorm_quantize")
     return row, tok
 
 

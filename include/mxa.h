@@ -144,6 +144,25 @@ mxa_status mxa_quantize(const void* x_bf16, int64_t T, int H, int d, const int32
                         int max_seqlen, int64_t ntiles, mxa_scale_mode mode, int views, int hadamard,
                         mxa_qview* row, mxa_qview* tok, cudaStream_t stream);
 
+/* Fused RMSNorm + quantize (FA4 write-up, "Fused RMSNorm+Quantize": the
+ * normalization becomes the prologue of the pass that reads the data anyway,
+ * instead of a pass of its own).  Every (token, head) vector of x is
+ * normalized in IEEE fp32,
+ *   y = x * (1 / sqrt(mean(x^2) + eps)) * weight,
+ * and y (never rounded to bf16) is quantized exactly as mxa_quantize
+ * quantizes x, into the same views, layouts and modes (the Hadamard rotation,
+ * when asked for, applies to y).  The fp32 order is fixed: per 16-channel
+ * chunk the squares summed in channel order, the chunk sums added pairwise,
+ * correctly rounded sqrt and division; an all-zero vector with eps = 0 gives
+ * y = 0.
+ *   weight: device fp32 [d], or NULL for all ones; eps >= 0.
+ * Status: as mxa_quantize, plus MXA_ERR_ARG for a negative or non-finite eps
+ * and MXA_ERR_ALIGN for a weight not 4-byte aligned. */
+mxa_status mxa_rmsnorm_quantize(const void* x_bf16, const float* weight, float eps, int64_t T, int H, int d,
+                                const int32_t* cu_seqlens, int num_docs, int max_seqlen, int64_t ntiles,
+                                mxa_scale_mode mode, int views, int hadamard, mxa_qview* row, mxa_qview* tok,
+                                cudaStream_t stream);
+
 /* Shape shared by the forward and backward calls.
  * Self-attention (T_k = 0): queries, keys and values share one token layout
  * (T, cu_seqlens, max_seqlen, ntiles).

@@ -183,3 +183,13 @@ def test_cross_attention_shape_checks(lib):
     assert L.mxa_bwd_workspace_bytes(ctypes.byref(bp)) == need_min + 2 * 32 * 4 * (16384 + 16)
     bp.dq_mode = 1
     assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), 1 << 30, None) == mxa.MXA_ERR_UNSUPPORTED
+
+
+def test_rmsnorm_quantize_rejects_bad_eps_without_launch(lib):
+    L = lib
+    qv = mxa.c_qview(256, 256)
+    for eps in (-1.0, float("inf"), float("nan")):
+        st = L.mxa_rmsnorm_quantize(256, None, eps, 256, 1, 128, None, 1, 256, 2, 0, 1, 0, qv, None, None)
+        assert st == mxa.MXA_ERR_ARG
+    st = L.mxa_rmsnorm_quantize(256, 258, 1e-6, 256, 1, 128, None, 1, 256, 2, 0, 1, 0, qv, None, None)
+    assert st == mxa.MXA_ERR_ALIGN
