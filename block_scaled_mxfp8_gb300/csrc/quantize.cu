@@ -1,7 +1,9 @@
 // quantize.cu -- bf16 -> MXFP8 quantizer (codes + UE8M0 scales), one pass.
 //
-// One CTA owns one (document, 32-token group, head) tile of 32 tokens x d
-// channels; it reads the bf16 tile once and writes every requested view:
+// One CTA owns one (document, 128-token tile, head): it issues the loads of
+// the tile's four 32-token groups (32 bytes per thread each) before any
+// arithmetic, then quantizes the groups one after another, reading the bf16
+// data once and writing every requested view:
 //   ROW view  : one scale per 32 channels of a token (groups along d), the
 //               view the Q K^T and dP = G V^T contractions use;
 //   TOK view  : one scale per 32 document-relative tokens of a channel
@@ -60,15 +62,32 @@ __global__ void __launch_bounds__(QCfg<D>::kThreads) quantize_kernel(QuantArgs a
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int row = tid / C::TPR;      // token row in the 32-token group
+  const int row = tid / C::TPR;      // token row in a 32-token group
   const int chunk = tid % C::TPR;    // 16-channel chunk
-  const int g = blockIdx.x;          // group index inside the document
+  const int tile = blockIdx.x;       // 128-token tile inside the document
   const int b = blockIdx.y;          // document
   const int h = blockIdx.z;          // head
 
   int64_t doc_start, doc_len;
   doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, doc_len);
-  if (static_cast<int64_t>(g) * 32 >= doc_len) return;  // past this document's last group
+  if (static_cast<int64_t>(tile) * 128 >= doc_len) return;  // past this document's last tile
+
+  // the raw bf16 words of all four 32-token groups first: 4 x 32 bytes per
+  // thread in flight before any arithmetic
+  uint4 raw[4][2];
+#pragma unroll
+  for (int gq = 0; gq < 4; ++gq) {
+    const int64_t tok = static_cast<int64_t>(tile) * 128 + gq * 32 + row;
+    if (tok < doc_len) {
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.x) +
+                                                        ((doc_start + tok) * a.H + h) * D + chunk * 16);
+      raw[gq][0] = __ldg(src);
+      raw[gq][1] = __ldg(src + 1);
+    } else {
+      raw[gq][0] = make_uint4(0u, 0u, 0u, 0u);
+      raw[gq][1] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
 
   // First scale tile of this document (each document owns ceil(n / 128)
   // consecutive 128-token tiles in the [H, NT, 512] scale layouts).
@@ -84,103 +103,86 @@ __global__ void __launch_bounds__(QCfg<D>::kThreads) quantize_kernel(QuantArgs a
     if (lane == 0 && part) atomicAdd(reinterpret_cast<unsigned long long*>(&s_tile_base), static_cast<unsigned long long>(part));
   }
   __syncthreads();
-  const int64_t atom_base = (static_cast<int64_t>(h) * a.ntiles + s_tile_base + g / 4) * kAtomBytes;
+  const int64_t atom_base = (static_cast<int64_t>(h) * a.ntiles + s_tile_base + tile) * kAtomBytes;
 
-  const int64_t t = doc_start + static_cast<int64_t>(g) * 32 + row;
-  const bool valid = (static_cast<int64_t>(g) * 32 + row) < doc_len;
-  const int64_t elem0 = (t * a.H + h) * D + chunk * 16;
+#pragma unroll
+  for (int gq = 0; gq < 4; ++gq) {
+    const int g = tile * 4 + gq;  // 32-token group inside the document
+    const int64_t t = doc_start + static_cast<int64_t>(g) * 32 + row;
+    const bool valid = (static_cast<int64_t>(g) * 32 + row) < doc_len;
+    const int64_t elem0 = (t * a.H + h) * D + chunk * 16;
 
-  float v[16];
-  if (valid) {
-    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.x) + elem0);
-    uint4 p0 = __ldg(src), p1 = __ldg(src + 1);
-    uint32_t w[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    float v[16];
+    {
+      const uint32_t w[8] = {raw[gq][0].x, raw[gq][0].y, raw[gq][0].z, raw[gq][0].w,
+                             raw[gq][1].x, raw[gq][1].y, raw[gq][1].z, raw[gq][1].w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      v[2 * i] = bf16_lo(w[i]);
-      v[2 * i + 1] = bf16_hi(w[i]);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = 0.0f;
-  }
-
-  if (a.rms) {
-    // RMSNorm in IEEE fp32, in a fixed order: this thread's 16 squares in
-    // channel order, then the TPR partial sums of the row pairwise (xor 1, 2,
-    // 4: every lane of the row ends with the same tree sum); r = 1 / sqrt(s /
-    // d + eps) with correctly rounded sqrt and division (0 when s / d + eps
-    // is 0); y = (x * r) * w.  (FA4 write-up, "Fused RMSNorm+Quantize".)
-    float ss = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) ss = __fadd_rn(ss, __fmul_rn(v[i], v[i]));
-#pragma unroll
-    for (int o = 1; o < C::TPR; o <<= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
-    const float den = __fadd_rn(__fdiv_rn(ss, static_cast<float>(D)), a.rms_eps);
-    const float r = den == 0.0f ? 0.0f : __fdiv_rn(1.0f, __fsqrt_rn(den));
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float t = __fmul_rn(v[i], r);
-      v[i] = a.rms_w ? __fmul_rn(t, __ldg(a.rms_w + chunk * 16 + i)) : t;
-    }
-  }
-
-  if constexpr (HAD) {
-    // Sylvester order: in-thread stages h = 1, 2, 4, 8, then across the 8
-    // threads of the row for h = 16, 32, 64 (chunk bits 0, 1, 2).
-#pragma unroll
-    for (int hh = 1; hh < 16; hh *= 2) {
-#pragma unroll
-      for (int i = 0; i < 16; i += 2 * hh) {
-#pragma unroll
-        for (int j = i; j < i + hh; ++j) {
-          float x0 = v[j], x1 = v[j + hh];
-          v[j] = x0 + x1;
-          v[j + hh] = x0 - x1;
-        }
+      for (int i = 0; i < 8; ++i) {
+        v[2 * i] = bf16_lo(w[i]);
+        v[2 * i + 1] = bf16_hi(w[i]);
       }
     }
-    had_cross(v, chunk, 1);
-    had_cross(v, chunk, 2);
-    had_cross(v, chunk, 4);
-    const float r = __uint_as_float(kInvSqrt128Bits);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], r);
-  }
 
-  float amax_local = 0.0f;
+    if (a.rms) {
+      // RMSNorm in IEEE fp32, in a fixed order: this thread's 16 squares in
+      // channel order, then the TPR partial sums of the row pairwise (xor 1, 2,
+      // 4: every lane of the row ends with the same tree sum); r = 1 / sqrt(s /
+      // d + eps) with correctly rounded sqrt and division (0 when s / d + eps
+      // is 0); y = (x * r) * w.  (FA4 write-up, "Fused RMSNorm+Quantize".)
+      float ss = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) amax_local = fmaxf(amax_local, fabsf(v[i]));
-
-  if constexpr (TOKBLOCK) {
-    // one exponent for the whole tile
-    float m = amax_local;
+      for (int i = 0; i < 16; ++i) ss = __fadd_rn(ss, __fmul_rn(v[i], v[i]));
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) s_blk[warp] = m;
-    __syncthreads();
-    float bm = 0.0f;
+      for (int o = 1; o < C::TPR; o <<= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+      const float den = __fadd_rn(__fdiv_rn(ss, static_cast<float>(D)), a.rms_eps);
+      const float r = den == 0.0f ? 0.0f : __fdiv_rn(1.0f, __fsqrt_rn(den));
 #pragma unroll
-    for (int w = 0; w < C::kWarps; ++w) bm = fmaxf(bm, s_blk[w]);
-    const int e = mx_exponent_bits(__float_as_uint(bm));
-    const float sc = exp2i_neg(e);
-    const uint8_t eb = static_cast<uint8_t>(e + 127);
-    if (valid) {
-      uint4 out;
-      out.x = pack_e4m3x4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
-      out.y = pack_e4m3x4(v[4] * sc, v[5] * sc, v[6] * sc, v[7] * sc);
-      out.z = pack_e4m3x4(v[8] * sc, v[9] * sc, v[10] * sc, v[11] * sc);
-      out.w = pack_e4m3x4(v[12] * sc, v[13] * sc, v[14] * sc, v[15] * sc);
-      *reinterpret_cast<uint4*>(a.row_codes + elem0) = out;
-      if ((chunk & 1) == 0) a.row_scales[atom_base + row * 16 + (g & 3) * 4 + chunk / 2] = eb;
+      for (int i = 0; i < 16; ++i) {
+        const float t = __fmul_rn(v[i], r);
+        v[i] = a.rms_w ? __fmul_rn(t, __ldg(a.rms_w + chunk * 16 + i)) : t;
+      }
     }
-    if (tid < D) a.tok_scales[atom_base + atom_offset(tid, g & 3)] = eb;
-    return;
-  } else {
-    if (a.write_row) {
-      float m = fmaxf(amax_local, __shfl_xor_sync(0xffffffffu, amax_local, 1));  // 32-channel group
-      const int e = mx_exponent_bits(__float_as_uint(m));
+
+    if constexpr (HAD) {
+      // Sylvester order: in-thread stages h = 1, 2, 4, 8, then across the 8
+      // threads of the row for h = 16, 32, 64 (chunk bits 0, 1, 2).
+#pragma unroll
+      for (int hh = 1; hh < 16; hh *= 2) {
+#pragma unroll
+        for (int i = 0; i < 16; i += 2 * hh) {
+#pragma unroll
+          for (int j = i; j < i + hh; ++j) {
+            float x0 = v[j], x1 = v[j + hh];
+            v[j] = x0 + x1;
+            v[j + hh] = x0 - x1;
+          }
+        }
+      }
+      had_cross(v, chunk, 1);
+      had_cross(v, chunk, 2);
+      had_cross(v, chunk, 4);
+      const float r = __uint_as_float(kInvSqrt128Bits);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], r);
+    }
+
+    float amax_local = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax_local = fmaxf(amax_local, fabsf(v[i]));
+
+    if constexpr (TOKBLOCK) {
+      // one exponent for the whole tile
+      float m = amax_local;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) s_blk[warp] = m;
+      __syncthreads();
+      float bm = 0.0f;
+#pragma unroll
+      for (int w = 0; w < C::kWarps; ++w) bm = fmaxf(bm, s_blk[w]);
+      const int e = mx_exponent_bits(__float_as_uint(bm));
       const float sc = exp2i_neg(e);
+      const uint8_t eb = static_cast<uint8_t>(e + 127);
       if (valid) {
         uint4 out;
         out.x = pack_e4m3x4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
@@ -188,52 +190,71 @@ __global__ void __launch_bounds__(QCfg<D>::kThreads) quantize_kernel(QuantArgs a
         out.z = pack_e4m3x4(v[8] * sc, v[9] * sc, v[10] * sc, v[11] * sc);
         out.w = pack_e4m3x4(v[12] * sc, v[13] * sc, v[14] * sc, v[15] * sc);
         *reinterpret_cast<uint4*>(a.row_codes + elem0) = out;
-        if ((chunk & 1) == 0) a.row_scales[atom_base + row * 16 + (g & 3) * 4 + chunk / 2] = static_cast<uint8_t>(e + 127);
+        if ((chunk & 1) == 0) a.row_scales[atom_base + row * 16 + (g & 3) * 4 + chunk / 2] = eb;
       }
-    }
-    if (a.write_tok) {
-      // per-channel max over the 32 rows: rows of a warp differ in the lane
-      // bits above log2(TPR); then across warps in shared memory.
-      float cm[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float m = fabsf(v[i]);
-#pragma unroll
-        for (int o = C::TPR; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        cm[i] = m;
-      }
-      if (lane < C::TPR) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) s_red[warp][chunk * 16 + i] = cm[i];
-      }
-      __syncthreads();
-      if (tid < D) {
-        float m = 0.0f;
-#pragma unroll
-        for (int w = 0; w < C::kWarps; ++w) m = fmaxf(m, s_red[w][tid]);
+      if (tid < D) a.tok_scales[atom_base + atom_offset(tid, g & 3)] = eb;
+      __syncthreads();  // s_blk is rewritten by the next group
+      continue;
+    } else {
+      if (a.write_row) {
+        float m = fmaxf(amax_local, __shfl_xor_sync(0xffffffffu, amax_local, 1));  // 32-channel group
         const int e = mx_exponent_bits(__float_as_uint(m));
-        s_e[tid] = e;
-        a.tok_scales[atom_base + atom_offset(tid, g & 3)] = static_cast<uint8_t>(e + 127);
+        const float sc = exp2i_neg(e);
+        if (valid) {
+          uint4 out;
+          out.x = pack_e4m3x4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
+          out.y = pack_e4m3x4(v[4] * sc, v[5] * sc, v[6] * sc, v[7] * sc);
+          out.z = pack_e4m3x4(v[8] * sc, v[9] * sc, v[10] * sc, v[11] * sc);
+          out.w = pack_e4m3x4(v[12] * sc, v[13] * sc, v[14] * sc, v[15] * sc);
+          *reinterpret_cast<uint4*>(a.row_codes + elem0) = out;
+          if ((chunk & 1) == 0) a.row_scales[atom_base + row * 16 + (g & 3) * 4 + chunk / 2] = static_cast<uint8_t>(e + 127);
+        }
       }
-      __syncthreads();
-      if (valid) {
-        float y[16];
+      if (a.write_tok) {
+        // per-channel max over the 32 rows: rows of a warp differ in the lane
+        // bits above log2(TPR); then across warps in shared memory.
+        float cm[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) y[i] = v[i] * exp2i_neg(s_e[chunk * 16 + i]);
-        uint4 out;
-        out.x = pack_e4m3x4(y[0], y[1], y[2], y[3]);
-        out.y = pack_e4m3x4(y[4], y[5], y[6], y[7]);
-        out.z = pack_e4m3x4(y[8], y[9], y[10], y[11]);
-        out.w = pack_e4m3x4(y[12], y[13], y[14], y[15]);
-        *reinterpret_cast<uint4*>(a.tok_codes + elem0) = out;
+        for (int i = 0; i < 16; ++i) {
+          float m = fabsf(v[i]);
+#pragma unroll
+          for (int o = C::TPR; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          cm[i] = m;
+        }
+        if (lane < C::TPR) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) s_red[warp][chunk * 16 + i] = cm[i];
+        }
+        __syncthreads();
+        if (tid < D) {
+          float m = 0.0f;
+#pragma unroll
+          for (int w = 0; w < C::kWarps; ++w) m = fmaxf(m, s_red[w][tid]);
+          const int e = mx_exponent_bits(__float_as_uint(m));
+          s_e[tid] = e;
+          a.tok_scales[atom_base + atom_offset(tid, g & 3)] = static_cast<uint8_t>(e + 127);
+        }
+        __syncthreads();
+        if (valid) {
+          float y[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) y[i] = v[i] * exp2i_neg(s_e[chunk * 16 + i]);
+          uint4 out;
+          out.x = pack_e4m3x4(y[0], y[1], y[2], y[3]);
+          out.y = pack_e4m3x4(y[4], y[5], y[6], y[7]);
+          out.z = pack_e4m3x4(y[8], y[9], y[10], y[11]);
+          out.w = pack_e4m3x4(y[12], y[13], y[14], y[15]);
+          *reinterpret_cast<uint4*>(a.tok_codes + elem0) = out;
+        }
+        __syncthreads();  // s_red / s_e are rewritten by the next group
       }
     }
-  }
+  }  // 32-token groups
 }
 
 cudaError_t launch_quantize(const QuantArgs& a, int d, bool tokblock, bool hadamard, int max_groups,
                             cudaStream_t stream) {
-  dim3 grid(max_groups, a.num_docs, a.H);
+  dim3 grid((max_groups + 3) / 4, a.num_docs, a.H);  // one CTA per 128-token tile
   if (d == 128) {
     constexpr int nt = QCfg<128>::kThreads;
     if (tokblock && hadamard)
