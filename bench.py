@@ -120,6 +120,11 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# dram__bytes_read.sum + dram__bytes_write.sum of attn_bwd_dkdv_kernel and
+# attn_dq_gemm_kernel at B2 H32 L4096 d128 (one ncu --set full capture)
+BWD_DRAM_BYTES_B2 = (0.265042 + 1.156755 + 1.111560 + 0.063097) * 1e9
+
+
 def flops(B, H, L, d, causal, lengths=None, lengths_k=None):
     """FLOP convention of the pages: forward 4 * H * d * sum_b n_b^2 (B * L^2 for
     equal lengths; sum_b nq_b * nk_b for cross-attention), halved when causal;
@@ -350,8 +355,14 @@ def run_gpu(args):
     peak_pf = pk["mxfp8_tflops"] / 1e3
     sm_mhz = clk.summary().get("sm_mhz") or 2070.0
     micro_tflops = MXFP8_MMA_FLOP_PER_SM_CLK * GB300_SMS * sm_mhz * 1e6 / 1e12
+    # DRAM bytes of the backward call's dK/dV and dQ kernels from one ncu
+    # capture at B2 (profiles/ncu_full_b2h32l4096_attention_kernels.md),
+    # scaled by the tile pairs (B / 2); only for the workload it was taken on
+    traffic = None
+    if w.name == "llm" and not w.causal and not args.dq_mode and w.lengths is None:
+        traffic = round(BWD_DRAM_BYTES_B2 * B / 2)
     roofline = {"bound": "tensor", "achieved": round(dom["pflops"] * 1e3, 1), "peak": round(pk["mxfp8_tflops"], 1),
-                "unit": "TFLOP/s", "frac": round(dom["pflops"] / peak_pf, 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(dom["pflops"] / peak_pf, 4), "traffic": traffic,
                 "kernel": dom["kernel"], "peak_source": pk["source"],
                 "fwd": {"achieved": round(fwd_pf * 1e3, 1), "frac": round(fwd_pf / peak_pf, 4)},
                 "bwd": {"achieved": round(bwd_pf * 1e3, 1), "frac": round(bwd_pf / peak_pf, 4)},
