@@ -50,6 +50,13 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return d;
 }
 
+// Three-input max (one instruction for two comparisons).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Bounded wait used by every warp role: gives up after kWaitBudgetCycles,
 // records `code` in the device error word and raises the CTA's abort flag;
 // returns early (false) once another role has raised it.
@@ -153,9 +160,19 @@ namespace mxa {
 // the values carry a 2^shift boost and floored at the UE8M0 minimum, E4M3
 // codes of x * 2^-(e + shift) into w.  Returns the UE8M0 byte of e.
 __device__ __forceinline__ uint32_t quant_ds_block32(const float (&x)[32], int shift, uint32_t (&w)[8]) {
-  float am = 0.0f;
+  // max-abs in four independent chains of three-input max
+  float m0 = fmax3(fabsf(x[0]), fabsf(x[1]), fabsf(x[2])), m1 = fmax3(fabsf(x[3]), fabsf(x[4]), fabsf(x[5]));
+  float m2 = fmax3(fabsf(x[6]), fabsf(x[7]), fabsf(x[8])), m3 = fmax3(fabsf(x[9]), fabsf(x[10]), fabsf(x[11]));
 #pragma unroll
-  for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(x[i]));
+  for (int i = 12; i < 28; i += 8) {
+    m0 = fmax3(m0, fabsf(x[i]), fabsf(x[i + 1]));
+    m1 = fmax3(m1, fabsf(x[i + 2]), fabsf(x[i + 3]));
+    m2 = fmax3(m2, fabsf(x[i + 4]), fabsf(x[i + 5]));
+    m3 = fmax3(m3, fabsf(x[i + 6]), fabsf(x[i + 7]));
+  }
+  m0 = fmax3(m0, fabsf(x[28]), fabsf(x[29]));
+  m1 = fmax3(m1, fabsf(x[30]), fabsf(x[31]));
+  float am = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
   am = warp_max_abs(am);
   // an all-zero block keeps the unit scale whatever its boost
   int e = am == 0.0f ? 0 : mx_exponent_bits(__float_as_uint(am)) - shift;

@@ -65,13 +65,6 @@ struct FwdCfg {
   static constexpr int kSmemBytes = kOffSfV + kStages * 2 * kAtomBytes + 1024;  // + alignment slack
 };
 
-// Three-input max (one instruction for two comparisons).
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
 // Row maximum of 64 scores in four independent chains.
 __device__ __forceinline__ float max64(const float (&v)[64]) {
   float a = fmax3(v[0], v[1], v[2]), b = fmax3(v[3], v[4], v[5]), c = fmax3(v[6], v[7], v[8]),
@@ -364,7 +357,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       }
       const float neg = 4.0f - m;
       const uint64_t neg2 = f2_pack(neg, neg), sl2x2 = f2_pack(sl2, sl2);
-      uint64_t lsum2 = 0;  // two partial sums (+0.0, +0.0)
+      uint64_t lsa = 0, lsb = 0;  // four partial sums (+0.0) in two pairs
       uint32_t pw[16];  // E4M3 codes of this warp's 64 weights
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
@@ -372,11 +365,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         const float2 x23 = f2_unpack(f2_fma(f2_pack(sv[c + 2], sv[c + 3]), sl2x2, neg2));
         const float p0 = ex2_approx(x01.x), p1 = ex2_approx(x01.y);
         const float p2 = ex2_approx(x23.x), p3 = ex2_approx(x23.y);
-        lsum2 = f2_add(lsum2, f2_add(f2_pack(p0, p1), f2_pack(p2, p3)));
+        lsa = f2_add(lsa, f2_pack(p0, p1));
+        lsb = f2_add(lsb, f2_pack(p2, p3));
         pw[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
       }
-      const float2 ls = f2_unpack(lsum2);
-      const float lsum = ls.x + ls.y;
+      const float2 la = f2_unpack(lsa), lb = f2_unpack(lsb);
+      const float lsum = (la.x + la.y) + (lb.x + lb.y);
       // the previous P V must be done before P is overwritten and O rescaled
       if (j > 0 && !(ok = warp_wait(&bar_o_done, (j - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();

@@ -166,9 +166,11 @@ __global__ void __launch_bounds__(QCfg<D>::kThreads) quantize_kernel(QuantArgs a
       for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], r);
     }
 
-    float amax_local = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) amax_local = fmaxf(amax_local, fabsf(v[i]));
+    // max-abs of this thread's 16 values in independent chains
+    float amax_local = fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
+                             fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
+    amax_local = fmaxf(amax_local, fmaxf(fmaxf(fmaxf(fabsf(v[8]), fabsf(v[9])), fmaxf(fabsf(v[10]), fabsf(v[11]))),
+                                         fmaxf(fmaxf(fabsf(v[12]), fabsf(v[13])), fmaxf(fabsf(v[14]), fabsf(v[15])))));
 
     if constexpr (TOKBLOCK) {
       // one exponent for the whole tile
