@@ -20,8 +20,10 @@
 //          every K step reaches through the descriptor's leading byte offset);
 //   O = O / L -> bf16, LSE = m + ln l with l the fp32 sum of the unquantized
 //   weights (FLAMIA notes sec. 2, online softmax).
-// Warp roles: warp 0 = TMA producer, warp 1 = TMEM owner and MMA issuer,
-// warps 2..17 = softmax / correction / epilogue: four warps per TMEM lane
+// Warp roles: warp 0 = TMA producer, warp 1 = TMEM owner and S issuer,
+// warp 18 = P V issuer (an MMA issue blocks its thread for about the pipe
+// time, so S_{j+1} must not queue behind P_{j-1} V), warps 2..17 = softmax /
+// correction / epilogue: four warps per TMEM lane
 // quadrant, each taking 64 of the 256 key columns of its 32 query rows.  A
 // softmax warp copies its S columns into registers and releases S at once,
 // so the next S MMA runs while the exponentials of this tile are formed; the
@@ -50,7 +52,7 @@ struct FwdCfg {
   static constexpr uint32_t kSBO = 8 * D;
   static constexpr int kKSteps = D / 32;              // K steps of S = Q K^T
   static constexpr int kKStepBytes = 32 * D;          // 32 keys of V (P V K step)
-  static constexpr int kThreads = 576;                // 2 role warps + 16 softmax warps
+  static constexpr int kThreads = 608;                // 3 role warps + 16 softmax warps
   static constexpr int kSoftmaxThreads = 512;
   static constexpr uint32_t kColS = 0, kColO = 256, kColL = 256 + D, kColSfQ = 400, kColSfK = 404, kColSfVA = 420,
                             kColOneA = 424, kColSfVB = 428, kColOneB = 432, kColSfP = 436, kColP = 448;
@@ -103,7 +105,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   __shared__ uint64_t bar_q, bar_k_full[C::kStages], bar_k_empty[C::kStages], bar_v_full[C::kStages],
-      bar_v_empty[C::kStages], bar_s_full, bar_s_empty, bar_p_full, bar_o_done, bar_drain, bar_mx[2][4], bar_lsum;
+      bar_v_empty[C::kStages], bar_s_full, bar_s_empty, bar_p_full, bar_o_done, bar_drain, bar_drain2, bar_mx[2][4],
+      bar_lsum;
   __shared__ float s_mx[2][4][128];  // [iteration parity][column quarter][row] partial row maxima
   __shared__ float s_l[4][128];      // [column quarter][row] partial row sums
   __shared__ uint32_t s_tmem;
@@ -149,6 +152,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     mbar_init(&bar_p_full, C::kSoftmaxThreads);
     mbar_init(&bar_o_done, 1);
     mbar_init(&bar_drain, 1);
+    mbar_init(&bar_drain2, 1);
     for (int q = 0; q < 4; ++q) {
       mbar_init(&bar_mx[0][q], 128);
       mbar_init(&bar_mx[1][q], 128);
@@ -234,23 +238,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         mbar_wait(&bar_v_full[j % C::kStages], (j / C::kStages) & 1, nullptr, 0);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
     if (lane == 0) {
-      // descriptors built once; per MMA only constant offsets are added.  The
-      // P V operand B = [V | 1] keeps its second atom column (the ones block)
-      // fixed, so stepping its start address by x bytes lowers its leading
-      // byte offset by x.
-      const uint32_t onesa = smem_u32(smem + C::kOffOnes), va0 = smem_u32(smem + C::kOffV);
+      // descriptors built once; per MMA only constant offsets are added
       const uint64_t dQa = make_sdesc(smem_u32(smem + C::kOffQ), 16, C::kSBO, C::kSwz);
       const uint64_t dK0 = make_sdesc(smem_u32(smem + C::kOffK), 16, C::kSBO, C::kSwz);
-      const uint64_t dV0 = make_sdesc(va0, onesa - va0, C::kSBO, C::kSwz);
-      const uint64_t dSfK0 = atom_desc(smem + C::kOffSfK), dSfV0 = atom_desc(smem + C::kOffSfV);
-      auto v_adv = [](uint64_t d, uint32_t bytes) -> uint64_t {
-        return d + (bytes >> 4) - (static_cast<uint64_t>(bytes >> 4) << 16);
-      };
-      const uint32_t tS = tmem + C::kColS, tO = tmem + C::kColO, tP = tmem + C::kColP;
-      const uint32_t tSfQ = tmem + C::kColSfQ, tSfP = tmem + C::kColSfP;
-      const uint32_t tSfVA = tmem + C::kColSfVA, tSfVB = tmem + C::kColSfVB;
+      const uint64_t dSfK0 = atom_desc(smem + C::kOffSfK);
+      const uint32_t tS = tmem + C::kColS, tSfQ = tmem + C::kColSfQ;
       bool ok = role_wait(&bar_q, 0, abort_flag, a.err, kErrTimeoutMma);
       if (ok) {
         tc_fence_after();
@@ -277,8 +271,27 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         return true;
       };
       if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < n_it; ++j) {
-        if (j + 1 < n_it && !issue_s(j + 1)) break;  // waits until S_j has been read out
+      for (int j = 0; ok && j + 1 < n_it; ++j)
+        if (!(ok = issue_s(j + 1))) break;  // waits until S_j has been read out
+      // drain this thread's MMAs before the TMEM is released
+      mma_commit(&bar_drain);
+      mbar_wait(&bar_drain, 0, nullptr, 0);
+    }
+  } else if (warp == 18) {
+    // ------------------------------------------------------------ P V issuer
+    if (lane == 0) {
+      // the P V operand B = [V | 1] keeps its second atom column (the ones
+      // block) fixed, so stepping its start address by x bytes lowers its
+      // leading byte offset by x
+      const uint32_t onesa = smem_u32(smem + C::kOffOnes), va0 = smem_u32(smem + C::kOffV);
+      const uint64_t dV0 = make_sdesc(va0, onesa - va0, C::kSBO, C::kSwz);
+      const uint64_t dSfV0 = atom_desc(smem + C::kOffSfV);
+      auto v_adv = [](uint64_t d, uint32_t bytes) -> uint64_t {
+        return d + (bytes >> 4) - (static_cast<uint64_t>(bytes >> 4) << 16);
+      };
+      const uint32_t tO = tmem + C::kColO, tP = tmem + C::kColP, tSfP = tmem + C::kColSfP;
+      const uint32_t tSfVA = tmem + C::kColSfVA, tSfVB = tmem + C::kColSfVB;
+      for (int j = 0; j < n_it; ++j) {
         const int s = j % C::kStages;
         if (!role_wait(&bar_v_full[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma)) break;
         if (!role_wait(&bar_p_full, j & 1, abort_flag, a.err, kErrTimeoutMma)) break;
@@ -294,9 +307,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         mma_commit(&bar_o_done);
         mma_commit(&bar_v_empty[s]);
       }
-      // drain the tensor pipe before the TMEM is released
-      mma_commit(&bar_drain);
-      mbar_wait(&bar_drain, 0, nullptr, 0);
+      mma_commit(&bar_drain2);
+      mbar_wait(&bar_drain2, 0, nullptr, 0);
     }
   } else {
     // ------------------------------------------------------------ softmax
