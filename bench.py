@@ -140,6 +140,18 @@ def flops(B, H, L, d, causal, lengths=None, lengths_k=None):
     return f, 2.5 * f
 
 
+def job_time_ms(ms_local, dist=None, device="cpu"):
+    """Whole-job time of a replica run: the slowest rank's timed region (the
+    replicas share no data; this max is the only exchange)."""
+    if dist is None:
+        return float(ms_local)
+    import torch
+
+    t = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------------ CPU oracle leg
 
 def oracle_sample(L=4096, H=1, d=128, causal=False, seed=1002):
@@ -283,11 +295,7 @@ def run_gpu(args):
     if dist is not None:
         dist.barrier()
     mxa.check_error()
-    ms_total = t_start.elapsed_time(t_end)
-    if dist is not None:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = job_time_ms(t_start.elapsed_time(t_end), dist, dev)
     ms_step = ms_total / args.steps
     ms_quant = statistics.mean(r[0].elapsed_time(r[1]) for r in recs)
     ms_fwd = statistics.mean(r[1].elapsed_time(r[2]) for r in recs)
