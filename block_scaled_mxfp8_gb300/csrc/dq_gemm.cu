@@ -25,7 +25,7 @@ namespace {
 
 template <int D>
 struct DqGemmCfg {
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 3;
   static constexpr int kThreads = 192;
   static constexpr int kTileBytes = 128 * D;  // one Kt tile
   static constexpr uint32_t kSwz = D == 128 ? kSwz128 : kSwz64;
@@ -44,7 +44,7 @@ struct DqGemmCfg {
 }  // namespace
 
 template <int D>
-__global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 1)
+__global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 2)
     attn_dq_gemm_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   using C = DqGemmCfg<D>;
   extern __shared__ uint8_t smem_raw[];
