@@ -224,15 +224,6 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         bulk_load(sf, a.qt_sf + qslot * kAtomBytes, kAtomBytes, &bar_b_full[sb]);
         bulk_load(sf + kAtomBytes, a.gt_sf + qslot * kAtomBytes, kAtomBytes, &bar_b_full[sb]);
         issued_b = u + 1;
-        if (u + C::kStagesA < n_work) {  // warm L2 with the unit after ring A
-          const int un = u + C::kStagesA;
-          const int hn = hk * grp + un / nq;
-          const int qn = static_cast<int>(doc_start + static_cast<int64_t>(qi0 + un % nq) * 128);
-          tma_prefetch_l2_3d(&maps.q, 0, hn, qn);
-          tma_prefetch_l2_3d(&maps.g, 0, hn, qn);
-          tma_prefetch_l2_3d(&maps.qt, 0, hn, qn);
-          tma_prefetch_l2_3d(&maps.gt, 0, hn, qn);
-        }
       }
       role_wait(&bar_kv, 0, abort_flag, nullptr, 0);
       for (int u = (issued_a > C::kStagesA ? issued_a - C::kStagesA : 0); u < issued_a; ++u)
@@ -605,12 +596,6 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         tma_load_3d(smem + C::kOffB + sb * C::kTileBytes, &maps.kt, &bar_b_full[sb], 0, hk, k0);
         bulk_load(sSf + (2 + 2 * C::kStagesA + sb) * kAtomBytes, a.kt_sf + katom, kAtomBytes, &bar_b_full[sb]);
         issued_b = j + 1;
-        if (j + C::kStagesA < n_kt) {  // warm L2 with the key tile after ring A
-          const int kn = k0 + 128 * C::kStagesA;
-          tma_prefetch_l2_3d(&maps.k, 0, hk, kn);
-          tma_prefetch_l2_3d(&maps.v, 0, hk, kn);
-          tma_prefetch_l2_3d(&maps.kt, 0, hk, kn);
-        }
       }
       role_wait(&bar_q, 0, abort_flag, nullptr, 0);
       for (int j = (issued_a > C::kStagesA ? issued_a - C::kStagesA : 0); j < issued_a; ++j)

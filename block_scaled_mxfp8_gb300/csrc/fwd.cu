@@ -221,14 +221,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         bulk_load(sfv, a.v_sf + atom0, kAtomBytes, &bar_v_full[s]);
         bulk_load(sfv + kAtomBytes, a.v_sf + atom1, kAtomBytes, &bar_v_full[s]);
         issued_v = j + 1;
-        // warm L2 with the keys the rings will load next
-        if (j + C::kStages < n_it) {
-          const int kp = k0 + 256 * C::kStages;
-          tma_prefetch_l2_3d(&maps.k, 0, hk, kp);
-          tma_prefetch_l2_3d(&maps.k, 0, hk, kp + 128);
-          tma_prefetch_l2_3d(&maps.v, 0, hk, kp);
-          tma_prefetch_l2_3d(&maps.v, 0, hk, kp + 128);
-        }
       }
       // drain: every load issued must have landed before the CTA exits
       role_wait(&bar_q, 0, abort_flag, nullptr, 0);
