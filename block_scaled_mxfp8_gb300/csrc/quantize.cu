@@ -56,7 +56,8 @@ template <int D, bool TOKBLOCK, bool HAD>
 __global__ void __launch_bounds__(QCfg<D>::kThreads) quantize_kernel(QuantArgs a) {
   using C = QCfg<D>;
   __shared__ float s_red[C::kWarps][D];
-  __shared__ int s_e[D];
+  __shared__ uint32_t s_red2[C::kWarps][D / 2];  // per-warp channel maxima, bf16 patterns, 2 per word
+  __shared__ __align__(16) float s_sc[D];         // 2^-e of each channel
   __shared__ float s_blk[C::kWarps];
   __shared__ int64_t s_tile_base;
 
@@ -215,32 +216,70 @@ __global__ void __launch_bounds__(QCfg<D>::kThreads) quantize_kernel(QuantArgs a
       if (a.write_tok) {
         // per-channel max over the 32 rows: rows of a warp differ in the lane
         // bits above log2(TPR); then across warps in shared memory.
-        float cm[16];
+        if (!a.rms) {
+          // on the bf16 bit patterns: |x| is the pattern without its sign
+          // bit, and the patterns of non-negative values order as unsigned
+          // integers, so one halfword max serves two channels
+          uint32_t m2[8] = {raw[gq][0].x & 0x7FFF7FFFu, raw[gq][0].y & 0x7FFF7FFFu, raw[gq][0].z & 0x7FFF7FFFu,
+                            raw[gq][0].w & 0x7FFF7FFFu, raw[gq][1].x & 0x7FFF7FFFu, raw[gq][1].y & 0x7FFF7FFFu,
+                            raw[gq][1].z & 0x7FFF7FFFu, raw[gq][1].w & 0x7FFF7FFFu};
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float m = fabsf(v[i]);
+          for (int o = C::TPR; o < 32; o <<= 1) {
 #pragma unroll
-          for (int o = C::TPR; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-          cm[i] = m;
-        }
-        if (lane < C::TPR) {
+            for (int k = 0; k < 8; ++k) m2[k] = __vmaxu2(m2[k], __shfl_xor_sync(0xffffffffu, m2[k], o));
+          }
+          if (lane < C::TPR) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) s_red[warp][chunk * 16 + i] = cm[i];
-        }
-        __syncthreads();
-        if (tid < D) {
-          float m = 0.0f;
+            for (int k = 0; k < 8; ++k) s_red2[warp][chunk * 8 + k] = m2[k];
+          }
+          __syncthreads();
+          if (tid < D / 2) {  // channels 2 tid (low halfword) and 2 tid + 1 (high)
+            uint32_t mm = 0u;
 #pragma unroll
-          for (int w = 0; w < C::kWarps; ++w) m = fmaxf(m, s_red[w][tid]);
-          const int e = mx_exponent_bits(__float_as_uint(m));
-          s_e[tid] = e;
-          a.tok_scales[atom_base + atom_offset(tid, g & 3)] = static_cast<uint8_t>(e + 127);
+            for (int w = 0; w < C::kWarps; ++w) mm = __vmaxu2(mm, s_red2[w][tid]);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int ch = 2 * tid + hf;
+              const int e = mx_exponent_bits(hf ? (mm & 0xFFFF0000u) : (mm << 16));
+              s_sc[ch] = exp2i_neg(e);
+              a.tok_scales[atom_base + atom_offset(ch, g & 3)] = static_cast<uint8_t>(e + 127);
+            }
+          }
+        } else {
+          float cm[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float m = fabsf(v[i]);
+#pragma unroll
+            for (int o = C::TPR; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            cm[i] = m;
+          }
+          if (lane < C::TPR) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) s_red[warp][chunk * 16 + i] = cm[i];
+          }
+          __syncthreads();
+          if (tid < D) {
+            float m = 0.0f;
+#pragma unroll
+            for (int w = 0; w < C::kWarps; ++w) m = fmaxf(m, s_red[w][tid]);
+            const int e = mx_exponent_bits(__float_as_uint(m));
+            s_sc[tid] = exp2i_neg(e);
+            a.tok_scales[atom_base + atom_offset(tid, g & 3)] = static_cast<uint8_t>(e + 127);
+          }
         }
         __syncthreads();
         if (valid) {
           float y[16];
+          const float4* sc4 = reinterpret_cast<const float4*>(s_sc + chunk * 16);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) y[i] = v[i] * exp2i_neg(s_e[chunk * 16 + i]);
+          for (int i = 0; i < 4; ++i) {
+            const float4 f = sc4[i];
+            y[4 * i] = v[4 * i] * f.x;
+            y[4 * i + 1] = v[4 * i + 1] * f.y;
+            y[4 * i + 2] = v[4 * i + 2] * f.z;
+            y[4 * i + 3] = v[4 * i + 3] * f.w;
+          }
           uint4 out;
           out.x = pack_e4m3x4(y[0], y[1], y[2], y[3]);
           out.y = pack_e4m3x4(y[4], y[5], y[6], y[7]);
@@ -248,7 +287,7 @@ __global__ void __launch_bounds__(QCfg<D>::kThreads) quantize_kernel(QuantArgs a
           out.w = pack_e4m3x4(y[12], y[13], y[14], y[15]);
           *reinterpret_cast<uint4*>(a.tok_codes + elem0) = out;
         }
-        __syncthreads();  // s_red / s_e are rewritten by the next group
+        __syncthreads();  // s_red / s_sc are rewritten by the next group
       }
     }
   }  // 32-token groups
