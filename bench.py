@@ -261,17 +261,19 @@ def run_gpu(args):
     stream = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
-    def step(src, rec=None):
+    def step(src, rec=None, outs=None):
+        o_, lse_, dq_, dk_, dv_ = outs if outs is not None else (o, lse, dq, dk, dv)
         e = [ev() for _ in range(4)] if rec is not None else None
         if e: e[0].record(stream)
         mxa.quantize(src["q"], geo, out=qv["q"])
         for k in ("k", "v"):
             mxa.quantize(src[k], gk, out=qv[k])
         if e: e[1].record(stream)
-        mxa.fwd(qv["q"][0], qv["k"][0], qv["v"][1], geo, w.causal, out=(o, lse), workspace=fws, kv_geo=kv_geo)
+        mxa.fwd(qv["q"][0], qv["k"][0], qv["v"][1], geo, w.causal, out=(o_, lse_), workspace=fws, kv_geo=kv_geo)
         if e: e[2].record(stream)
         mxa.quantize(src["do"], geo, out=qv["do"])
-        mxa.bwd(views, o, lse, geo, w.causal, dq_mode=args.dq_mode, workspace=ws, out=(dq, dk, dv), kv_geo=kv_geo)
+        mxa.bwd(views, o_, lse_, geo, w.causal, dq_mode=args.dq_mode, workspace=ws, out=(dq_, dk_, dv_),
+                kv_geo=kv_geo)
         if e:
             e[3].record(stream)
             rec.append(e)
@@ -388,25 +390,56 @@ def run_gpu(args):
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
-    def e2e_step():
-        for k in dev_in:
-            dev_in[k].copy_(host_in[k], non_blocking=True)
-        step(dev_in)
-        host_out["o"].copy_(o, non_blocking=True)
-        host_out["dq"].copy_(dq, non_blocking=True)
-        host_out["dk"].copy_(dk, non_blocking=True)
-        host_out["dv"].copy_(dv, non_blocking=True)
+    # Pipelined like a training loop: step i+1's inputs go up on one stream and
+    # step i-1's outputs come down on another while step i computes; inputs and
+    # outputs are double-buffered on the device.  Every byte of every step
+    # crosses the host link inside the timed region.
+    dev_in2 = [dev_in, {k: torch.empty_like(v) for k, v in x.items()}]
+    outs2 = [(o, lse, dq, dk, dv), tuple(torch.empty_like(tn) for tn in (o, lse, dq, dk, dv))]
+    s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
 
-    e2e_step()
-    torch.cuda.synchronize()
-    n_e2e = max(2, min(args.steps, 5))
-    a_, b_ = ev(), ev()
-    a_.record(stream)
-    for _ in range(n_e2e):
-        e2e_step()
-    b_.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = a_.elapsed_time(b_) / n_e2e
+    def e2e_run(n):
+        start, end = ev(), ev()
+        start.record(stream)
+        in_ready = [ev(), ev()]
+        done = [None, None]
+        out_free = [None, None]
+        s_h2d.wait_event(start)
+        with torch.cuda.stream(s_h2d):
+            for k in dev_in2[0]:
+                dev_in2[0][k].copy_(host_in[k], non_blocking=True)
+        in_ready[0].record(s_h2d)
+        for i in range(n):
+            bb = i % 2
+            stream.wait_event(in_ready[bb])
+            if out_free[bb] is not None:
+                stream.wait_event(out_free[bb])
+            step(dev_in2[bb], outs=outs2[bb])
+            done[bb] = ev()
+            done[bb].record(stream)
+            if i + 1 < n:  # the next inputs, once the step that last read that buffer is done
+                nb = (i + 1) % 2
+                if done[nb] is not None:
+                    s_h2d.wait_event(done[nb])
+                with torch.cuda.stream(s_h2d):
+                    for k in dev_in2[nb]:
+                        dev_in2[nb][k].copy_(host_in[k], non_blocking=True)
+                in_ready[nb] = ev()
+                in_ready[nb].record(s_h2d)
+            s_d2h.wait_event(done[bb])
+            with torch.cuda.stream(s_d2h):
+                for k, tn in zip(("o", "dq", "dk", "dv"), (outs2[bb][0], outs2[bb][2], outs2[bb][3], outs2[bb][4])):
+                    host_out[k].copy_(tn, non_blocking=True)
+            out_free[bb] = ev()
+            out_free[bb].record(s_d2h)
+        stream.wait_stream(s_d2h)
+        end.record(stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end)
+
+    e2e_run(2)
+    n_e2e = max(3, min(args.steps, 10))
+    ms_e2e = e2e_run(n_e2e) / n_e2e
     e2e = {"value": round(world * step_flop / (ms_e2e * 1e-3) / 1e15, 4), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3)}
 
