@@ -361,7 +361,8 @@ def run_gpu(args):
     bwd_pf = fbwd / (ms_bwd_only * 1e-3) / 1e15
     # dominant kernel: the backward (2.5x the forward's flops)
     dom = {"kernel": ("mxa_bwd call: bwd_prep_kernel + attn_bwd_dkdv_kernel + attn_dq_gemm_kernel "
-                      "(FP32 dQ; the dK/dV kernel takes ~80% of the call)"), "pflops": bwd_pf}
+                      "(%s dQ; the dK/dV kernel takes ~80%% of the call)" % ("FP16x2^9" if args.dq_mode else "FP32")),
+           "pflops": bwd_pf}
     peak_pf = pk["mxfp8_tflops"] / 1e3
     sm_mhz = clk.summary().get("sm_mhz") or 2070.0
     micro_tflops = MXFP8_MMA_FLOP_PER_SM_CLK * GB300_SMS * sm_mhz * 1e6 / 1e12

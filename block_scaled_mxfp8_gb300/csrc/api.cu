@@ -333,20 +333,38 @@ mxa_status mxa_fwd(const mxa_fwd_params* p, cudaStream_t stream) {
   return MXA_OK;
 }
 
+namespace {
+
+// Backward workspace: padded D and LSE rows, the query and key tile lists, then
+// either the dS blocks the dK/dV kernel emits for the dQ GEMM (both modes) or,
+// in FP16 x 2^9 mode without room for them, the fp16 dQ accumulator of the
+// fused kernel.
+size_t bwd_head_bytes(const mxa_shape& s) {
+  return bwd_rows_bytes(s) + list_bytes(s, q_side(s)) + list_bytes(s, k_side(s));
+}
+
+size_t bwd_acc16_bytes(const mxa_shape& s) {
+  const size_t b = static_cast<size_t>(s.T) * static_cast<size_t>(s.Hq) * static_cast<size_t>(s.d) * 2;
+  return (b + 255) & ~size_t(255);
+}
+
+bool bwd_shape_sizable(const mxa_bwd_params* p) {
+  return p && p->shape.T >= 0 && p->shape.Hq > 0 && (p->shape.d == 64 || p->shape.d == 128);
+}
+
+}  // namespace
+
 size_t mxa_bwd_workspace_min_bytes(const mxa_bwd_params* p) {
-  if (!p || p->shape.T < 0 || p->shape.Hq <= 0 || (p->shape.d != 64 && p->shape.d != 128)) return 0;
-  const size_t T = static_cast<size_t>(p->shape.T), Hq = static_cast<size_t>(p->shape.Hq),
-               d = static_cast<size_t>(p->shape.d);
-  // FP16 x 2^9 mode adds its fp16 partial-sum accumulator [T, Hq, d]
-  const size_t acc = p->dq_mode == MXA_DQ_FP16_X512 ? T * Hq * d * 2 : 0;
-  return bwd_rows_bytes(p->shape) + list_bytes(p->shape, q_side(p->shape)) + list_bytes(p->shape, k_side(p->shape)) +
-         ((acc + 255) & ~size_t(255));
+  if (!bwd_shape_sizable(p)) return 0;
+  const size_t head = bwd_head_bytes(p->shape);
+  if (p->dq_mode != MXA_DQ_FP16_X512) return head;
+  const size_t acc = bwd_acc16_bytes(p->shape), ds = bwd_ds_bytes(p->shape);
+  return head + (acc < ds ? acc : ds);
 }
 
 size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p) {
-  const size_t base = mxa_bwd_workspace_min_bytes(p);
-  if (base == 0 || p->dq_mode == MXA_DQ_FP16_X512) return base;
-  return base + bwd_ds_bytes(p->shape);
+  if (!bwd_shape_sizable(p)) return 0;
+  return bwd_head_bytes(p->shape) + bwd_ds_bytes(p->shape);
 }
 
 mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cudaStream_t stream) {
@@ -385,7 +403,11 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   void* klist = static_cast<uint8_t*>(qlist) + list_bytes(s, qs);
   void* acc = static_cast<uint8_t*>(klist) + list_bytes(s, ks);
   const bool fp16 = p->dq_mode == MXA_DQ_FP16_X512;
-  const size_t acc_bytes = fp16 ? T * Hq * d * 2 : 0;
+  // dS emitted by the dK/dV kernel and summed by the dQ GEMM, else (FP32: dS
+  // formed again by the dQ kernel; FP16: the fused kernel's fp16 accumulator)
+  const bool emit = ws_bytes >= mxa_bwd_workspace_bytes(p);
+  if (fp16 && !emit && ws_bytes < bwd_head_bytes(s) + bwd_acc16_bytes(s)) return MXA_ERR_WORKSPACE;
+  const size_t acc_bytes = fp16 && !emit ? T * Hq * d * 2 : 0;
   const int maxlen = s.cu_seqlens ? s.max_seqlen : static_cast<int>(s.T / s.num_docs);
 
   PrepArgs pa{};
@@ -427,13 +449,13 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   a.dpad = dpad;
   a.dq_mode = p->dq_mode;
   a.dq_acc32 = nullptr;
-  a.dq_acc16 = fp16 ? static_cast<uint16_t*>(acc) : nullptr;
+  a.dq_acc16 = acc_bytes ? static_cast<uint16_t*>(acc) : nullptr;
   a.dk = p->dk;
   a.dv = p->dv;
   a.dq_out = p->dq;
   a.err = device_error_word();
   a.mt = static_cast<int>(max_doc_tiles(s));
-  if (!fp16 && uses_list(s)) {
+  if ((!fp16 || emit) && uses_list(s)) {
     if (launch_tile_list(qs, ks, s.num_docs, a.causal, 0, qlist, stream) != cudaSuccess ||
         launch_tile_list(ks, qs, s.num_docs, a.causal, 1, klist, stream) != cudaSuccess)
       return MXA_ERR_CUDA;
@@ -443,11 +465,11 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
     a.k_count = static_cast<const int32_t*>(klist);
   }
   const int amaxlen = max_len(s);  // grids of the attention kernels
-  if (!fp16) {
-    // FP32: dK/dV kernel, then dQ summed in TMEM in a fixed order -- over the
-    // dS the dK/dV kernel emitted when the workspace holds it, else by a
-    // kernel that forms dS again
-    if (ws_bytes >= mxa_bwd_workspace_bytes(p)) {
+  // dK/dV kernel, then dQ summed in a fixed key-tile order (FP32 in TMEM, or
+  // FP16 x 2^9 in registers) over the dS the dK/dV kernel emitted when the
+  // workspace holds it; FP32 otherwise by a kernel that forms dS again
+  if (!fp16 || emit) {
+    if (emit) {
       a.ds_codes = static_cast<uint8_t*>(acc);
       a.ds_sf = a.ds_codes + static_cast<size_t>(s.Hq) * static_cast<size_t>(ks.ntiles) * a.mt * 16384;
       if (launch_bwd_emit(a, maps, s.d, amaxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;

@@ -15,6 +15,14 @@
 //            rows;
 //   B = K    TOK view (rows = channels, groups = 32-key blocks), MN-major.
 // Warps: 0 = TMA producer, 1 = TMEM owner and MMA issuer, 2..5 = epilogue.
+//
+// FP16 x 2^9 dQ mode (F16): the FA4 write-up's reduced-precision dQ sum --
+// every key tile's partial product is rounded to fp16 after a 2^9 boost (and
+// alpha) and added to an fp16 sum, RNE at each step, then brought back by
+// 2^-9.  Here the partial of key tile j lands in TMEM (the MMAs of each tile
+// start a fresh accumulation), the epilogue warps fold it into their fp16
+// registers in key-tile order and hand the columns back before tile j + 1
+// overwrites them.
 #include <cuda_bf16.h>
 
 #include "attn_common.cuh"
@@ -43,13 +51,14 @@ struct DqGemmCfg {
 
 }  // namespace
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 2)
     attn_dq_gemm_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   using C = DqGemmCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_full[C::kStages], bar_empty[C::kStages], bar_sfa[C::kStages], bar_final, bar_drain;
+  __shared__ uint64_t bar_full[C::kStages], bar_empty[C::kStages], bar_sfa[C::kStages], bar_final, bar_drain,
+      bar_pfull, bar_pfree;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int64_t s_slot;
@@ -81,6 +90,8 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 2)
     }
     mbar_init(&bar_final, 1);
     mbar_init(&bar_drain, 1);
+    mbar_init(&bar_pfull, 1);
+    mbar_init(&bar_pfree, 128);  // the four epilogue warps
     s_abort = 0;
     fence_barrier_init();
   }
@@ -130,6 +141,8 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 2)
         // operands landed and the epilogue warps have laid out the dS scales
         if (!(ok = role_wait(&bar_full[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma))) break;
         if (!(ok = role_wait(&bar_sfa[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        // F16: the previous partial must have been read out of TMEM
+        if (F16 && j > 0 && !(ok = role_wait(&bar_pfree, (j - 1) & 1, abort_flag, a.err, kErrTimeoutMma))) break;
         tc_fence_after();
         const uint32_t tSfA = tmem + C::kSfDS + 4 * s, tSfB = tmem + C::kSfKt + 4 * s;
         tmem_cp_desc(tSfB, sdesc_adv(dSf0, s * C::kStageBytes));
@@ -137,8 +150,9 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 2)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // 32 keys per step: 32 rows of each operand
           mma_mxf8_ss(tmem + C::kColDQ, sdesc_adv(da, kk * 4096), sdesc_adv(db, kk * 32 * D),
-                      make_idesc_mxf8(128, D, 1, 1, kk, kk), tSfA, tSfB, (j > 0 || kk > 0) ? 1u : 0u);
+                      make_idesc_mxf8(128, D, 1, 1, kk, kk), tSfA, tSfB, ((!F16 && j > 0) || kk > 0) ? 1u : 0u);
         mma_commit(&bar_empty[s]);
+        if (F16) mma_commit(&bar_pfull);
       }
       mma_commit(&bar_final);
       mma_commit(&bar_drain);
@@ -156,6 +170,33 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 2)
     // reloaded only after the MMAs of tile j - kStages completed, so its
     // slot is free.
     bool ok = true;
+    // F16: this row's fp16 sum, two channels per register
+    __half2 acc[F16 ? D / 2 : 1];
+    if constexpr (F16) {
+#pragma unroll
+      for (int i = 0; i < D / 2; ++i) acc[i] = __float2half2_rn(0.0f);
+    }
+    const float bst = a.alpha * 512.0f;  // alpha and the 2^9 boost of the fp16 sum
+    // fold the partial of key tile jj into the fp16 sum (F16 only)
+    auto fold = [&](int jj) -> bool {
+      if (!warp_wait(&bar_pfull, jj & 1, abort_flag, a.err, kErrTimeoutEpilogue)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t rr[32];
+        tmem_ld32(lane_base + C::kColDQ + c, rr);
+        tmem_ld_wait();
+        if (c + 32 == D) {  // every column read: tile jj + 1 may overwrite them
+          tc_fence_before();
+          mbar_arrive(&bar_pfree);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i += 2)
+          acc[(c + i) / 2] = __hadd2(acc[(c + i) / 2], __floats2half2_rn(__uint_as_float(rr[i]) * bst,
+                                                                           __uint_as_float(rr[i + 1]) * bst));
+      }
+      return true;
+    };
     for (int j = 0; j < n_kt; ++j) {
       const int s = j % C::kStages;
       if (!(ok = warp_wait(&bar_full[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutEpilogue))) break;
@@ -164,26 +205,48 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 2)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bar_sfa[s]);
+      if constexpr (F16) {
+        if (j > 0 && !(ok = fold(j - 1))) break;
+      }
+    }
+    if constexpr (F16) {
+      if (ok && n_kt > 0) ok = fold(n_kt - 1);
     }
     if (ok) ok = role_wait(&bar_final, 0, abort_flag, a.err, kErrTimeoutEpilogue);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       const int64_t t = doc_start + qpos;
       __nv_bfloat16* dqrow = reinterpret_cast<__nv_bfloat16*>(a.dq_out) + (t * a.Hq + h) * D;
-#pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t rr[32];
-        tmem_ld32(lane_base + C::kColDQ + c, rr);
-        tmem_ld_wait();
+      if constexpr (F16) {
         if (qpos < n) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
+          for (int c = 0; c < D; c += 8) {
             uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(rr[i]) * a.alpha, __uint_as_float(rr[i + 1]) * a.alpha);
-            v.y = pack_bf16x2(__uint_as_float(rr[i + 2]) * a.alpha, __uint_as_float(rr[i + 3]) * a.alpha);
-            v.z = pack_bf16x2(__uint_as_float(rr[i + 4]) * a.alpha, __uint_as_float(rr[i + 5]) * a.alpha);
-            v.w = pack_bf16x2(__uint_as_float(rr[i + 6]) * a.alpha, __uint_as_float(rr[i + 7]) * a.alpha);
-            *reinterpret_cast<uint4*>(dqrow + c + i) = v;
+            uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 f = __half22float2(acc[c / 2 + k]);
+              vw[k] = pack_bf16x2(f.x * (1.0f / 512.0f), f.y * (1.0f / 512.0f));
+            }
+            *reinterpret_cast<uint4*>(dqrow + c) = v;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t rr[32];
+          tmem_ld32(lane_base + C::kColDQ + c, rr);
+          tmem_ld_wait();
+          if (qpos < n) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(rr[i]) * a.alpha, __uint_as_float(rr[i + 1]) * a.alpha);
+              v.y = pack_bf16x2(__uint_as_float(rr[i + 2]) * a.alpha, __uint_as_float(rr[i + 3]) * a.alpha);
+              v.z = pack_bf16x2(__uint_as_float(rr[i + 4]) * a.alpha, __uint_as_float(rr[i + 5]) * a.alpha);
+              v.w = pack_bf16x2(__uint_as_float(rr[i + 6]) * a.alpha, __uint_as_float(rr[i + 7]) * a.alpha);
+              *reinterpret_cast<uint4*>(dqrow + c + i) = v;
+            }
           }
         }
       }
@@ -197,23 +260,28 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 2)
   }
 }
 
-cudaError_t launch_dq_gemm(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
+namespace {
+
+template <int D, bool F16>
+cudaError_t launch_dq_gemm_t(const BwdArgs& a, const BwdMaps& m, int max_seqlen, cudaStream_t stream) {
+  using C = DqGemmCfg<D>;
   const dim3 grid = a.q_items ? dim3(static_cast<unsigned>(a.ntiles * a.Hq))
                               : dim3((max_seqlen + 127) / 128, a.num_docs, a.Hq);
-  if (d == 128) {
-    using C = DqGemmCfg<128>;
-    cudaError_t e = cudaFuncSetAttribute(attn_dq_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attn_dq_gemm_kernel<128><<<grid, C::kThreads, C::kSmemBytes, stream>>>(m, a);
-  } else {
-    using C = DqGemmCfg<64>;
-    cudaError_t e = cudaFuncSetAttribute(attn_dq_gemm_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attn_dq_gemm_kernel<64><<<grid, C::kThreads, C::kSmemBytes, stream>>>(m, a);
-  }
+  cudaError_t e = cudaFuncSetAttribute(attn_dq_gemm_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  attn_dq_gemm_kernel<D, F16><<<grid, C::kThreads, C::kSmemBytes, stream>>>(m, a);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dq_gemm(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
+  const bool f16 = a.dq_mode == 1;
+  if (d == 128) return f16 ? launch_dq_gemm_t<128, true>(a, m, max_seqlen, stream)
+                           : launch_dq_gemm_t<128, false>(a, m, max_seqlen, stream);
+  return f16 ? launch_dq_gemm_t<64, true>(a, m, max_seqlen, stream)
+             : launch_dq_gemm_t<64, false>(a, m, max_seqlen, stream);
 }
 
 }  // namespace mxa

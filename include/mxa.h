@@ -93,8 +93,10 @@ enum { MXA_VIEW_ROW = 1, MXA_VIEW_TOK = 2 };
 typedef enum {
   MXA_DQ_FP32 = 0,     /* dQ summed in fp32 over the key tiles, in a fixed order (deterministic; a
                           separate dQ kernel recomputes S and dP per query tile) */
-  MXA_DQ_FP16_X512 = 1 /* dQ partial sums of each key tile boosted by 2^9 and added into an fp16
-                          accumulator with atomics (order varies); unboosted at the end */
+  MXA_DQ_FP16_X512 = 1 /* dQ partial product of each 128-key tile boosted by 2^9, rounded to
+                          fp16 and added into an fp16 sum, unboosted at the end: in key-tile
+                          order in the dQ GEMM when the workspace holds the emitted dS
+                          (deterministic), else with atomics in a fused kernel (order varies) */
 } mxa_dq_mode;
 
 /* One quantized view of a tensor: E4M3 codes [T, H, d] and its UE8M0 scales
@@ -239,20 +241,21 @@ typedef struct {
  *   mxa_fwd schedules its own (for each of the query and the key side:
  *   256 + 16 * NT of that side + 8 * num_docs bytes, rounded up to 256;
  *   reserved in every case).
- *   FP32 mode: plus the dS blocks the dK/dV pass emits for the dQ product --
+ *   Then the dS blocks the dK/dV pass emits for the dQ product --
  *   E4M3 codes (16 KB) and the 16 UE8M0 block scales per (query head, key
  *   tile, query tile of the same document) pair, with mt = ceil(max_seqlen /
  *   128) query-tile slots per key tile: Hq * NT_k * mt * 16400 bytes, NT_k
- *   the key side's ntiles (B8 H32 L4096: 4.3 GB).
- *   FP16_X512 mode: plus the fp16 dQ accumulator [T, Hq, d], rounded up to
- *   256 bytes. */
+ *   the key side's ntiles (B8 H32 L4096: 4.3 GB). */
 size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p);
 
 /* Smallest workspace mxa_bwd accepts: the padded D and LSE rows and the tile
- * lists, plus the fp16 accumulator in FP16_X512 mode.  An FP32-mode workspace smaller than
- * mxa_bwd_workspace_bytes() selects a dQ kernel that forms dS again from S
- * and dP instead of reading the emitted blocks (slower; same blocks, so the
- * same tolerances). */
+ * lists; in FP16_X512 mode plus the smaller of the emitted dS blocks and the
+ * fp16 dQ accumulator [T, Hq, d] (rounded up to 256 bytes).  A workspace
+ * smaller than mxa_bwd_workspace_bytes() selects, in FP32 mode, a dQ kernel
+ * that forms dS again from S and dP instead of reading the emitted blocks
+ * (slower; same blocks, so the same tolerances), and in FP16_X512 mode a fused
+ * kernel that adds the boosted partials into the fp16 accumulator with
+ * atomics (slower, order varies). */
 size_t mxa_bwd_workspace_min_bytes(const mxa_bwd_params* p);
 
 /* Backward.  workspace: device buffer of ws_bytes >= mxa_bwd_workspace_min_bytes()
@@ -279,7 +282,8 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
  * are rejected with MXA_ERR_WORKSPACE before any work; FP32-mode calls need
  * 2 * Hq * ntiles * 512 bytes (B8 H32 L4096: 8 MiB) and take the fast dQ path
  * only when their full mxa_bwd_workspace_bytes() also fits; FP16_X512 calls
- * also need the fp16 dQ accumulator, so only small ones fit.
+ * also need the emitted dS or the fp16 dQ accumulator, so only small ones
+ * fit.
  * The device address of the array is resolved on the first call made with a
  * given device current (cudaGetSymbolAddress); make that first call before
  * any stream capture.  The function allocates nothing.  Every call on a device

@@ -154,8 +154,10 @@ def test_fwd_bwd_reject_bad_arguments_without_launch(lib):
     bp.dq_mode = 5
     assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), need, None) == mxa.MXA_ERR_ARG
     bp.dq_mode = 1
-    # FP16 x 2^9 mode: the fp16 dQ accumulator instead of the emitted dS
-    assert L.mxa_bwd_workspace_bytes(ctypes.byref(bp)) == need_min + 256 * 2 * 128 * 2
+    # FP16 x 2^9 mode: the emitted dS as in FP32 mode, or at least the fused
+    # kernel's fp16 dQ accumulator (whichever is smaller)
+    assert L.mxa_bwd_workspace_bytes(ctypes.byref(bp)) == need
+    assert L.mxa_bwd_workspace_min_bytes(ctypes.byref(bp)) == need_min + min(256 * 2 * 128 * 2, 2 * 2 * 2 * 16400)
 
 
 def test_cross_attention_shape_checks(lib):
