@@ -45,6 +45,7 @@ FALLBACK_HBM_GBS = 6800.0
 # clock sampled during the timed region it gives the microbenchmark peak.
 MXFP8_MMA_FLOP_PER_SM_CLK = 16374.0
 GB300_SMS = 152
+DQ_MODE_NAMES = {0: "FP32", 1: "FP16x2^9", 2: "FP16 per-row boost"}
 
 
 def peaks():
@@ -361,7 +362,7 @@ def run_gpu(args):
     bwd_pf = fbwd / (ms_bwd_only * 1e-3) / 1e15
     # dominant kernel: the backward (2.5x the forward's flops)
     dom = {"kernel": ("mxa_bwd call: bwd_prep_kernel + attn_bwd_dkdv_kernel + attn_dq_gemm_kernel "
-                      "(%s dQ; the dK/dV kernel takes ~80%% of the call)" % ("FP16x2^9" if args.dq_mode else "FP32")),
+                      "(%s dQ; the dK/dV kernel takes ~80%% of the call)" % DQ_MODE_NAMES[args.dq_mode]),
            "pflops": bwd_pf}
     peak_pf = pk["mxfp8_tflops"] / 1e3
     sm_mhz = clk.summary().get("sm_mhz") or 2070.0
@@ -449,7 +450,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "mxfp8 (e4m3 codes, ue8m0 scales, fp32 accumulate)", "data": "synthetic",
         "config": {"workload": ("%s: B%d H%d L%d d%d %s, fwd+bwd, dQ %s" % (
-            w.name, B, Hq, L, d, "causal" if w.causal else "non-causal", "fp16x2^9" if args.dq_mode else "fp32"))
+            w.name, B, Hq, L, d, "causal" if w.causal else "non-causal", DQ_MODE_NAMES[args.dq_mode].lower()))
             if not cross else ("%s: B%d Lq%d x jagged Lk U[1,%d] (T_k %d) H%d d%d, fwd+bwd, dQ fp32" % (
                 w.name, B, L, max(w.lengths_k), Tk, Hq, d)),
             "global_batch": B * world, "seq_len": L, "heads": Hq, "head_dim": d, "causal": w.causal,
@@ -529,7 +530,8 @@ def main():
     ap.add_argument("--impl", default="mxa", choices=["mxa", "reference"])
     ap.add_argument("--workload", default="llm")
     ap.add_argument("--causal", action="store_true")
-    ap.add_argument("--dq-mode", type=int, default=0, help="0 = fp32 dQ accumulation, 1 = fp16 x 2^9")
+    ap.add_argument("--dq-mode", type=int, default=0, choices=[0, 1, 2],
+                    help="0 = fp32 dQ accumulation, 1 = fp16 x 2^9, 2 = fp16 with a per-row boost")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling only)")
     args = ap.parse_args()

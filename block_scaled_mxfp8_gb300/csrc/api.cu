@@ -339,8 +339,18 @@ namespace {
 // either the dS blocks the dK/dV kernel emits for the dQ GEMM (both modes) or,
 // in FP16 x 2^9 mode without room for them, the fp16 dQ accumulator of the
 // fused kernel.
-size_t bwd_head_bytes(const mxa_shape& s) {
-  return bwd_rows_bytes(s) + list_bytes(s, q_side(s)) + list_bytes(s, k_side(s));
+size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// FP16 per-row boost mode: the boost of every query row (fp32 [Hq, T]) and
+// the key bound of every (token, kv head) (int32 [T, Hkv]).
+size_t bwd_boost_bytes(const mxa_shape& s, int dq_mode) {
+  if (dq_mode != MXA_DQ_FP16_ROW || s.T <= 0) return 0;
+  const size_t T = static_cast<size_t>(s.T);
+  return round256(static_cast<size_t>(s.Hq) * T * 4) + round256(T * static_cast<size_t>(s.Hkv > 0 ? s.Hkv : 0) * 4);
+}
+
+size_t bwd_head_bytes(const mxa_shape& s, int dq_mode = MXA_DQ_FP32) {
+  return bwd_rows_bytes(s) + bwd_boost_bytes(s, dq_mode) + list_bytes(s, q_side(s)) + list_bytes(s, k_side(s));
 }
 
 size_t bwd_acc16_bytes(const mxa_shape& s) {
@@ -356,7 +366,8 @@ bool bwd_shape_sizable(const mxa_bwd_params* p) {
 
 size_t mxa_bwd_workspace_min_bytes(const mxa_bwd_params* p) {
   if (!bwd_shape_sizable(p)) return 0;
-  const size_t head = bwd_head_bytes(p->shape);
+  const size_t head = bwd_head_bytes(p->shape, p->dq_mode);
+  if (p->dq_mode == MXA_DQ_FP16_ROW) return head + bwd_ds_bytes(p->shape);  // the dQ GEMM only
   if (p->dq_mode != MXA_DQ_FP16_X512) return head;
   const size_t acc = bwd_acc16_bytes(p->shape), ds = bwd_ds_bytes(p->shape);
   return head + (acc < ds ? acc : ds);
@@ -364,7 +375,7 @@ size_t mxa_bwd_workspace_min_bytes(const mxa_bwd_params* p) {
 
 size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p) {
   if (!bwd_shape_sizable(p)) return 0;
-  return bwd_head_bytes(p->shape) + bwd_ds_bytes(p->shape);
+  return bwd_head_bytes(p->shape, p->dq_mode) + bwd_ds_bytes(p->shape);
 }
 
 mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cudaStream_t stream) {
@@ -379,7 +390,8 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   if (!aligned(p->o, 16) || !aligned(p->lse, 4) || !aligned(p->dq, 16) || !aligned(p->dk, 16) ||
       !aligned(p->dv, 16))
     return MXA_ERR_ALIGN;
-  if (p->dq_mode != MXA_DQ_FP32 && p->dq_mode != MXA_DQ_FP16_X512) return MXA_ERR_ARG;
+  if (p->dq_mode != MXA_DQ_FP32 && p->dq_mode != MXA_DQ_FP16_X512 && p->dq_mode != MXA_DQ_FP16_ROW)
+    return MXA_ERR_ARG;
   if (is_cross(s) && p->dq_mode != MXA_DQ_FP32) return MXA_ERR_UNSUPPORTED;
   if (!workspace || ws_bytes < mxa_bwd_workspace_min_bytes(p)) return MXA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return MXA_ERR_ALIGN;
@@ -399,14 +411,18 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   const size_t dbytes = 2 * pad_elems * 4;
   float* dpad = static_cast<float*>(workspace);
   float* lpad = dpad + pad_elems;
-  void* qlist = static_cast<uint8_t*>(workspace) + dbytes;
+  const bool rowboost = p->dq_mode == MXA_DQ_FP16_ROW;
+  float* boost = rowboost ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dbytes) : nullptr;
+  int32_t* key_bound =
+      rowboost ? reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(boost) + round256(Hq * T * 4)) : nullptr;
+  void* qlist = static_cast<uint8_t*>(workspace) + dbytes + bwd_boost_bytes(s, p->dq_mode);
   void* klist = static_cast<uint8_t*>(qlist) + list_bytes(s, qs);
   void* acc = static_cast<uint8_t*>(klist) + list_bytes(s, ks);
-  const bool fp16 = p->dq_mode == MXA_DQ_FP16_X512;
+  const bool fp16 = p->dq_mode != MXA_DQ_FP32;
   // dS emitted by the dK/dV kernel and summed by the dQ GEMM, else (FP32: dS
   // formed again by the dQ kernel; FP16: the fused kernel's fp16 accumulator)
   const bool emit = ws_bytes >= mxa_bwd_workspace_bytes(p);
-  if (fp16 && !emit && ws_bytes < bwd_head_bytes(s) + bwd_acc16_bytes(s)) return MXA_ERR_WORKSPACE;
+  if (fp16 && !emit && (rowboost || ws_bytes < bwd_head_bytes(s) + bwd_acc16_bytes(s))) return MXA_ERR_WORKSPACE;
   const size_t acc_bytes = fp16 && !emit ? T * Hq * d * 2 : 0;
   const int maxlen = s.cu_seqlens ? s.max_seqlen : static_cast<int>(s.T / s.num_docs);
 
@@ -425,6 +441,27 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   pa.lpad = lpad;
   pa.dq_acc = acc;
   pa.dq_acc_bytes = acc_bytes;
+  pa.dq_boost = boost;
+  pa.key_bound = key_bound;
+  pa.Hkv = s.Hkv;
+  pa.causal = s.causal ? 1 : 0;
+  pa.alpha = alpha_of(s);
+  if (rowboost) {
+    KeyBoundArgs kb{};
+    kb.T = s.T;
+    kb.Hkv = s.Hkv;
+    kb.d = s.d;
+    kb.cu_seqlens = s.cu_seqlens;
+    kb.num_docs = s.num_docs;
+    kb.ntiles = s.ntiles;
+    kb.causal = s.causal ? 1 : 0;
+    kb.v_codes = p->v_row.codes;
+    kb.v_sf = p->v_row.scales;
+    kb.k_codes = p->k_row.codes;
+    kb.k_sf = p->k_row.scales;
+    kb.key_bound = key_bound;
+    if (launch_key_bound(kb, stream) != cudaSuccess) return MXA_ERR_CUDA;
+  }
   if (launch_bwd_prep(pa, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
 
   BwdArgs a{};
@@ -450,6 +487,7 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   a.dq_mode = p->dq_mode;
   a.dq_acc32 = nullptr;
   a.dq_acc16 = acc_bytes ? static_cast<uint16_t*>(acc) : nullptr;
+  a.dq_boost = boost;
   a.dk = p->dk;
   a.dv = p->dv;
   a.dq_out = p->dq;

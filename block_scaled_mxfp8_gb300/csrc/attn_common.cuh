@@ -8,6 +8,29 @@
 
 namespace mxa {
 
+// ---- exact ceil(log2 x) helpers of the FP16 per-row dQ boost
+constexpr int kCl2None = -2000;  // stands for cl2 of an all-zero operand
+
+// cl2 of a nonzero E4M3 magnitude code (7 bits): normal codes are
+// 2^(E-7) (1 + M/8), subnormal ones M 2^-9.
+__device__ __forceinline__ int cl2_e4m3(uint32_t c) {
+  const int E = static_cast<int>(c >> 3), M = static_cast<int>(c & 7u);
+  if (E) return E - 7 + (M != 0);
+  return (M <= 1 ? 0 : 32 - __clz(M - 1)) - 9;
+}
+
+// cl2 of a positive normal fp32 value
+__device__ __forceinline__ int cl2_f32(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return static_cast<int>((u >> 23) & 0xFFu) - 127 + ((u & 0x7FFFFFu) != 0);
+}
+
+// cl2 of a count n >= 1
+__device__ __forceinline__ int cl2_count(int64_t n) {
+  return n <= 1 ? 0 : 64 - __clzll(static_cast<unsigned long long>(n - 1));
+}
+
+
 // 2^x on the MUFU unit (the kernels' one exponential; the backward rebuilds P
 // with the same instruction as the forward).
 __device__ __forceinline__ float ex2_approx(float x) {

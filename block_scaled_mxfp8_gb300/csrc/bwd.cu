@@ -116,7 +116,110 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(PrepArgs a) {
       a.dpad[slot + r] = acc;
       a.lpad[slot + r] = a.lse[static_cast<int64_t>(h) * a.T + t] * 1.4426950408889634f;
     }
+    if (a.dq_boost != nullptr) {
+      // g_i = cl2(max_c |G~_ic|): this lane's codes (one 32-channel group)
+      // with the group's scale, then the warp maximum
+      const int c0 = a.d == 128 ? 4 * lane : 2 * lane;
+      uint32_t w = a.d == 128 ? *reinterpret_cast<const uint32_t*>(a.g_codes + (t * a.Hq + h) * 128 + c0)
+                              : *reinterpret_cast<const uint16_t*>(a.g_codes + (t * a.Hq + h) * 64 + c0);
+      w &= 0x7F7F7F7Fu;
+      w = __vmaxu4(w, w >> 16);
+      w = __vmaxu4(w, w >> 8);
+      const uint32_t cmax = w & 0xFFu;
+      int g = cmax ? cl2_e4m3(cmax) + static_cast<int>(atom[atom_offset(r, c0 / 32)]) - 127 : kCl2None;
+      g = __reduce_max_sync(0xffffffffu, g);
+      if (lane == 0) {
+        const int64_t nvis = a.causal ? pos + 1 : n;
+        const int lg = cl2_count(nvis);
+        const int sp = 1 + (lg > 14 ? lg - 14 : 0);
+        const int kb = a.key_bound[t * a.Hkv + h / (a.Hq / a.Hkv)];
+        int beta = 11 - cl2_f32(a.alpha) - (a.d == 128 ? 7 : 6) - sp - g - kb;
+        beta = beta < -100 ? -100 : (beta > 100 ? 100 : beta);
+        a.dq_boost[static_cast<int64_t>(h) * a.T + t] = __uint_as_float(static_cast<uint32_t>(beta + 127) << 23);
+      }
+    }
   }
+}
+
+// ----------------------------------------------------------------- key bound
+// FP16 per-row boost (FLAMIA notes sec. 4, the strict accumulator scale): for
+// every (key token j, kv head), v_j = cl2(max_c |V~_jc|) and k_j =
+// cl2(max_c |K~_jc|) from the ROW views, and the bound a query at position j
+// uses: the running maxima of v and k over the document's keys up to j
+// (causal), or over the whole document, summed.  One CTA per (document, kv
+// head) walks the document in chunks of 256 tokens (block max-scan + carry).
+namespace {
+
+__device__ __forceinline__ int row_cl2max(const uint8_t* codes, const uint8_t* atom, int r, int d) {
+  int best = kCl2None;
+  for (int g = 0; g < d / 32; ++g) {
+    const uint4* p = reinterpret_cast<const uint4*>(codes + g * 32);
+    const uint4 x = __ldg(p), y = __ldg(p + 1);
+    uint32_t m = __vmaxu4(__vmaxu4(__vmaxu4(x.x & 0x7F7F7F7Fu, x.y & 0x7F7F7F7Fu),
+                                   __vmaxu4(x.z & 0x7F7F7F7Fu, x.w & 0x7F7F7F7Fu)),
+                          __vmaxu4(__vmaxu4(y.x & 0x7F7F7F7Fu, y.y & 0x7F7F7F7Fu),
+                                   __vmaxu4(y.z & 0x7F7F7F7Fu, y.w & 0x7F7F7F7Fu)));
+    m = __vmaxu4(m, m >> 16);
+    m = __vmaxu4(m, m >> 8);
+    const uint32_t c = m & 0xFFu;
+    if (c) {
+      const int e = cl2_e4m3(c) + static_cast<int>(atom[atom_offset(r, g)]) - 127;
+      best = e > best ? e : best;
+    }
+  }
+  return best;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(256) key_bound_kernel(KeyBoundArgs a) {
+  __shared__ int s_warp[2][8];
+  __shared__ int64_t s_slot;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.x, hk = blockIdx.y;
+  int64_t doc_start, n;
+  doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
+  const int64_t tb = doc_tile_base(a.cu_seqlens, b, n, tid, 256, &s_slot);
+  int cv = kCl2None, ck = kCl2None;  // maxima over the earlier chunks
+  for (int64_t c0 = 0; c0 < n; c0 += 256) {
+    const int64_t pos = c0 + tid;
+    int v = kCl2None, k = kCl2None;
+    if (pos < n) {
+      const int64_t t = doc_start + pos;
+      const int64_t atom = (static_cast<int64_t>(hk) * a.ntiles + tb + pos / 128) * kAtomBytes;
+      const int r = static_cast<int>(pos % 128);
+      v = row_cl2max(a.v_codes + (t * a.Hkv + hk) * a.d, a.v_sf + atom, r, a.d);
+      k = row_cl2max(a.k_codes + (t * a.Hkv + hk) * a.d, a.k_sf + atom, r, a.d);
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int yv = __shfl_up_sync(0xffffffffu, v, o), yk = __shfl_up_sync(0xffffffffu, k, o);
+      if (lane >= o) {
+        v = yv > v ? yv : v;
+        k = yk > k ? yk : k;
+      }
+    }
+    if (lane == 31) {
+      s_warp[0][warp] = v;
+      s_warp[1][warp] = k;
+    }
+    __syncthreads();
+    int pv = cv, pk = ck;
+    for (int w = 0; w < warp; ++w) {
+      pv = s_warp[0][w] > pv ? s_warp[0][w] : pv;
+      pk = s_warp[1][w] > pk ? s_warp[1][w] : pk;
+    }
+    v = pv > v ? pv : v;
+    k = pk > k ? pk : k;
+    if (a.causal && pos < n) a.key_bound[(doc_start + pos) * a.Hkv + hk] = v + k;
+    for (int w = 0; w < 8; ++w) {
+      cv = s_warp[0][w] > cv ? s_warp[0][w] : cv;
+      ck = s_warp[1][w] > ck ? s_warp[1][w] : ck;
+    }
+    __syncthreads();  // s_warp is rewritten by the next chunk
+  }
+  if (!a.causal)
+    for (int64_t pos = tid; pos < n; pos += 256) a.key_bound[(doc_start + pos) * a.Hkv + hk] = cv + ck;
 }
 
 // ----------------------------------------------------------------- dQ convert
@@ -540,6 +643,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+cudaError_t launch_key_bound(const KeyBoundArgs& a, cudaStream_t stream) {
+  key_bound_kernel<<<dim3(a.num_docs, a.Hkv), 256, 0, stream>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_prep(const PrepArgs& a, int max_seqlen, cudaStream_t stream) {

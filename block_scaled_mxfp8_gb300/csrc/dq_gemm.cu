@@ -176,7 +176,11 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 2)
 #pragma unroll
       for (int i = 0; i < D / 2; ++i) acc[i] = __float2half2_rn(0.0f);
     }
-    const float bst = a.alpha * 512.0f;  // alpha and the 2^9 boost of the fp16 sum
+    // alpha and the boost of the fp16 sum: 2^9, or the row's own 2^beta
+    float boost = 512.0f;
+    if (F16 && a.dq_boost != nullptr && qpos < n) boost = a.dq_boost[static_cast<int64_t>(h) * a.T + doc_start + qpos];
+    const float bst = a.alpha * boost;
+    const float unboost = __uint_as_float((254u << 23) - __float_as_uint(boost));  // 2^-beta, exact
     // fold the partial of key tile jj into the fp16 sum (F16 only)
     auto fold = [&](int jj) -> bool {
       if (!warp_wait(&bar_pfull, jj & 1, abort_flag, a.err, kErrTimeoutEpilogue)) return false;
@@ -226,7 +230,7 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 2)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const float2 f = __half22float2(acc[c / 2 + k]);
-              vw[k] = pack_bf16x2(f.x * (1.0f / 512.0f), f.y * (1.0f / 512.0f));
+              vw[k] = pack_bf16x2(f.x * unboost, f.y * unboost);
             }
             *reinterpret_cast<uint4*>(dqrow + c) = v;
           }
@@ -277,7 +281,7 @@ cudaError_t launch_dq_gemm_t(const BwdArgs& a, const BwdMaps& m, int max_seqlen,
 }  // namespace
 
 cudaError_t launch_dq_gemm(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
-  const bool f16 = a.dq_mode == 1;
+  const bool f16 = a.dq_mode != 0;  // FP16 x 2^9 or the per-row boost
   if (d == 128) return f16 ? launch_dq_gemm_t<128, true>(a, m, max_seqlen, stream)
                            : launch_dq_gemm_t<128, false>(a, m, max_seqlen, stream);
   return f16 ? launch_dq_gemm_t<64, true>(a, m, max_seqlen, stream)

@@ -126,6 +126,7 @@ struct BwdArgs {
   const float* dpad;     // D, tile-padded [Hq, NT, 128]; 0 on rows past a document's end
   float* dq_acc32;       // [T, Hq, d] (FP32 mode)
   uint16_t* dq_acc16;    // [T, Hq, d] fp16 bits (FP16 x 2^9 mode)
+  const float* dq_boost; // [Hq, T]: per-row boost 2^beta of the FP16 per-row mode (else null: 2^9)
   void* dk;              // bf16 [Tk, Hkv, d]
   void* dv;              // bf16 [Tk, Hkv, d]
   void* dq_out;          // bf16 [T, Hq, d] (written directly by the deterministic dQ kernel)
@@ -164,6 +165,30 @@ struct PrepArgs {
   float* lpad;       // LSE * log2(e), tile-padded [Hq, NT, 128]
   void* dq_acc;      // zeroed here
   size_t dq_acc_bytes;
+  // FP16 per-row boost mode (null otherwise): 2^beta of every query row,
+  // from its G row, the key bound of its kv head and its visible key count
+  float* dq_boost;           // [Hq, T]
+  const int32_t* key_bound;  // [T, Hkv]: V + K exponent bound over the keys a row sees
+  int Hkv;
+  int causal;
+  float alpha;
+};
+
+// Key bound of the FP16 per-row boost: for every (token t, kv head), the
+// maxima over the keys that query t sees of cl2(max_c |V~_jc|) and of
+// cl2(max_c |K~_jc|) (ROW views), summed.
+struct KeyBoundArgs {
+  int64_t T;
+  int Hkv, d;
+  const int32_t* cu_seqlens;
+  int num_docs;
+  int64_t ntiles;
+  int causal;
+  const uint8_t* v_codes;
+  const uint8_t* v_sf;
+  const uint8_t* k_codes;
+  const uint8_t* k_sf;
+  int32_t* key_bound;  // [T, Hkv]
 };
 
 struct DqConvArgs {
@@ -190,6 +215,7 @@ cudaError_t launch_bwd_split(const BwdArgs& a, const BwdMaps& m, int d, int max_
 // dK/dV kernel emitting dS, then the dQ product over the emitted dS
 cudaError_t launch_bwd_emit(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream);
 cudaError_t launch_dq_gemm(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream);
+cudaError_t launch_key_bound(const KeyBoundArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const PrepArgs& a, int max_seqlen, cudaStream_t stream);
 cudaError_t launch_dq_convert(const DqConvArgs& a, cudaStream_t stream);
 

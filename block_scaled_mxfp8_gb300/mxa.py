@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_PKG, "_build", "libmxa.so")
 MXA_OK, MXA_ERR_ARG, MXA_ERR_ALIGN, MXA_ERR_UNSUPPORTED, MXA_ERR_WORKSPACE, MXA_ERR_CUDA, MXA_ERR_TIMEOUT = range(7)
 MXA_SCALE_MX32, MXA_SCALE_TOKBLOCK32 = 0, 1
 MXA_VIEW_ROW, MXA_VIEW_TOK = 1, 2
-MXA_DQ_FP32, MXA_DQ_FP16_X512 = 0, 1
+MXA_DQ_FP32, MXA_DQ_FP16_X512, MXA_DQ_FP16_ROW = 0, 1, 2
 ATOM_BYTES = 512
 
 

@@ -71,7 +71,7 @@
 extern "C" {
 #endif
 
-#define MXA_ABI_VERSION 3
+#define MXA_ABI_VERSION 4
 
 typedef enum {
   MXA_OK = 0,
@@ -96,7 +96,30 @@ typedef enum {
   MXA_DQ_FP16_X512 = 1 /* dQ partial product of each 128-key tile boosted by 2^9, rounded to
                           fp16 and added into an fp16 sum, unboosted at the end: in key-tile
                           order in the dQ GEMM when the workspace holds the emitted dS
-                          (deterministic), else with atomics in a fused kernel (order varies) */
+                          (deterministic), else with atomics in a fused kernel (order varies) */,
+  MXA_DQ_FP16_ROW = 2  /* as FP16_X512 in the dQ GEMM, with a boost 2^beta_i per query row and
+                          head instead of 2^9, chosen from magnitudes that query row i may
+                          depend on -- its own G row and the maxima of V and K over the keys it
+                          sees -- so no later position changes its rounding (FLAMIA notes sec.
+                          4, the strict accumulator scale).  With the E4M3 decoding x~ of the
+                          ROW views and cl2(x) = ceil(log2 x) (exact, on the scale exponents and
+                          code bits):
+                            beta_i = clamp(11 - cl2(alpha) - log2(d) - s(n_i) - g_i - V_i - K_i,
+                                           -100, 100)
+                            g_i = cl2(max_c |G~_ic|); V_i, K_i = max over the keys j that row i
+                            sees (j <= i when causal, else the document) of cl2(max_c |V~_jc|),
+                            cl2(max_c |K~_jc|); n_i = number of those keys;
+                            s(n) = 1 + max(0, cl2(n) - 14).
+                          Then 2^(15 - beta_i) bounds |dQ_i| and every partial sum of it, so
+                          the fp16 sum cannot overflow: |dP_ij| <= d |G~_i| |V~_j| (max-abs
+                          norms); O_i averages token-view V values, each within 32/15 of the
+                          ROW view's maximum, so |D_i| <= 2.2 d |G~_i| V*; the E4M3 dS is
+                          within 2x of dS; sum_j P_ij <= 16/15 + n_i 2^-14 <= 2^s(n_i) (weights
+                          below the E4M3 range drop out of the forward's row sum); the
+                          token-view K is within 32/15 of K*: |dQ_ic| <= alpha 2 (3.2 d
+                          |G~_i| V*) 2^s (32/15) K* < 2^(4 + cl2(alpha) + log2 d + s + g + V + K).
+                          An all-zero operand counts as cl2 = -2000 (beta = 100).  Needs the
+                          full mxa_bwd_workspace_bytes(); self-attention only. */
 } mxa_dq_mode;
 
 /* One quantized view of a tensor: E4M3 codes [T, H, d] and its UE8M0 scales
@@ -245,7 +268,11 @@ typedef struct {
  *   E4M3 codes (16 KB) and the 16 UE8M0 block scales per (query head, key
  *   tile, query tile of the same document) pair, with mt = ceil(max_seqlen /
  *   128) query-tile slots per key tile: Hq * NT_k * mt * 16400 bytes, NT_k
- *   the key side's ntiles (B8 H32 L4096: 4.3 GB). */
+ *   the key side's ntiles (B8 H32 L4096: 4.3 GB).
+ *   FP16_ROW mode: after the D and LSE rows, before the lists, the boost
+ *   2^beta_i of every query row as fp32 [Hq, T] and the key bound V_t + K_t
+ *   of every (token, kv head) as int32 [T, Hkv], each rounded up to 256
+ *   bytes. */
 size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p);
 
 /* Smallest workspace mxa_bwd accepts: the padded D and LSE rows and the tile

@@ -786,6 +786,89 @@ void orc_attn_bwd_x(const double* Qs, const double* Ks, const double* Vo, const 
     }
 }
 
+/* ------------------------------------------------------------------------ */
+/* FP16 dQ reduction with a per-row boost                                    */
+/* ------------------------------------------------------------------------ */
+
+/* ceil(log2 x) of a positive finite value, exactly: x = f 2^e, f in [0.5, 1). */
+static int cl2d(double x)
+{
+    int e;
+    double f = frexp(x, &e);
+    return f == 0.5 ? e - 1 : e;
+}
+
+#define ORC_CL2_NONE (-2000) /* cl2 of an all-zero vector */
+
+/* cl2(max_c |x_c|) of one d-vector, or ORC_CL2_NONE. */
+static int cl2_maxabs(const double* x, int d)
+{
+    double m = 0.0;
+    for (int c = 0; c < d; ++c)
+        if (fabs(x[c]) > m)
+            m = fabs(x[c]);
+    return m > 0.0 ? cl2d(m) : ORC_CL2_NONE;
+}
+
+/* The power-of-two boost 2^beta of every query row of the FP16 dQ reduction
+ * in its strict form ([FLAMIA] sec. 4, "最后一条通道在累加器里": dQ partial
+ * sums boosted by a power of two, the strict option taking each row's own G
+ * norm with the maxima of V and K over the visible keys only).  The pages
+ * give the shape of the choice, b_i = 2^floor(log2(h / a_i)) for a bound a_i
+ * of the row's magnitude and a target h; this restates the bound the library
+ * documents for its MXA_DQ_FP16_ROW mode:
+ *   a_i = 2^(4 + cl2(alpha) + log2(d) + s(n_i) + g_i + V_i + K_i), h = 2^15,
+ *   g_i = cl2(max_c |G_ic|), V_i = max_{j visible} cl2(max_c |V_jc|),
+ *   K_i = max_{j visible} cl2(max_c |K_jc|), n_i = visible keys,
+ *   s(n) = 1 + max(0, cl2(n) - 14), cl2(1) = 0,
+ *   beta_i = clamp(15 - log2(a_i), -100, 100).
+ * Gr [T, Hq, d], Vr and Kr [T, Hkv, d]: the decoded ROW views (fp64).
+ * alpha: the fp32 softmax scale.  beta: [Hq, T]. */
+void orc_dq_row_boost(const double* Gr, const double* Vr, const double* Kr, int64_t T, int Hq, int Hkv, int d,
+                      const int32_t* cu, int ndocs, int causal, float alpha, int32_t* beta)
+{
+    int nd = num_docs_eff(cu, ndocs);
+    int grp = Hq / Hkv;
+    int log2d = 0;
+    while ((1 << log2d) < d)
+        ++log2d;
+    int ca = cl2d((double)alpha);
+    for (int b = 0; b < nd; ++b) {
+        int64_t s, e;
+        doc_range(cu, ndocs, T, b, &s, &e);
+        if (e <= s)
+            continue;
+        int* ve = (int*)malloc(sizeof(int) * (size_t)(e - s));
+        int* ke = (int*)malloc(sizeof(int) * (size_t)(e - s));
+        for (int hk = 0; hk < Hkv; ++hk) {
+            for (int64_t j = s; j < e; ++j) {
+                ve[j - s] = cl2_maxabs(Vr + (j * Hkv + hk) * d, d);
+                ke[j - s] = cl2_maxabs(Kr + (j * Hkv + hk) * d, d);
+            }
+            for (int h = hk * grp; h < (hk + 1) * grp; ++h) {
+                for (int64_t i = s; i < e; ++i) {
+                    int64_t jend = causal ? i + 1 : e;
+                    int Vi = ORC_CL2_NONE, Ki = ORC_CL2_NONE;
+                    for (int64_t j = s; j < jend; ++j) {
+                        if (ve[j - s] > Vi)
+                            Vi = ve[j - s];
+                        if (ke[j - s] > Ki)
+                            Ki = ke[j - s];
+                    }
+                    int64_t n = jend - s;
+                    int ln = n <= 1 ? 0 : cl2d((double)n);
+                    int sp = 1 + (ln > 14 ? ln - 14 : 0);
+                    int g = cl2_maxabs(Gr + (i * Hq + h) * d, d);
+                    int bt = 15 - (4 + ca + log2d + sp + g + Vi + Ki);
+                    beta[(int64_t)h * T + i] = bt < -100 ? -100 : (bt > 100 ? 100 : bt);
+                }
+            }
+        }
+        free(ve);
+        free(ke);
+    }
+}
+
 int orc_num_threads(void)
 {
 #ifdef _OPENMP

@@ -83,6 +83,7 @@ def _L():
                 "orc_quant_tokblock_f32": (None, [P, i64, i32, i32, P, i32, i32, P, P]),
                 "orc_attn_fwd_x": (None, [P, P, P, i64, i64, i32, i32, i32, P, P, i32, f64, P, P]),
                 "orc_attn_bwd_x": (None, [P] * 8 + [i64, i64, i32, i32, i32, P, P, i32, f64] + [P] * 6),
+                "orc_dq_row_boost": (None, [P, P, P, i64, i32, i32, i32, P, i32, i32, ctypes.c_float, P]),
                 "orc_num_threads": (i32, []),
             }
             for name, (res, args) in sig.items():
@@ -343,6 +344,23 @@ def attn_bwd(Qs, Ks, Vo, Vr, Gr, Qt, Kt, Gt, cu_seqlens=None, causal=False, alph
                       _p(units), -1 if units is None else len(units),
                       *[_p(out[k]) for k in ("dQ", "dK", "dV", "O", "LSE", "D")])
     return out
+
+
+def dq_row_boost(Gr, Vr, Kr, cu_seqlens=None, causal=False, alpha=None):
+    """Per-row exponent beta of the strict FP16 dQ reduction (FLAMIA sec. 4,
+    the accumulator scale): see orc_dq_row_boost.  Gr [T,Hq,d], Vr/Kr
+    [T,Hkv,d] decoded ROW views; alpha is rounded to fp32 as the library's
+    softmax scale is.  Returns int32 [Hq, T]."""
+    Gr, Vr, Kr = (np.ascontiguousarray(a, dtype=np.float64) for a in (Gr, Vr, Kr))
+    T, Hq, d = Gr.shape
+    Hkv = Vr.shape[1]
+    if alpha is None:
+        alpha = 1.0 / math.sqrt(d)
+    cu, nd = _cu(cu_seqlens)
+    beta = np.zeros((Hq, T), dtype=np.int32)
+    _L().orc_dq_row_boost(_p(Gr), _p(Vr), _p(Kr), T, Hq, Hkv, d, _p(cu), nd, int(bool(causal)), float(alpha),
+                          _p(beta))
+    return beta
 
 
 def attn_fwd_x(Q, K, V, cu_q, cu_k, alpha=None):

@@ -31,7 +31,7 @@ def test_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) <= set(mxa.EXPORTS) | set(names)
-    assert mxa.mxa_abi_version() == 3
+    assert mxa.mxa_abi_version() == 4
 
 
 def test_exports_testing_hooks(lib):
@@ -158,6 +158,15 @@ def test_fwd_bwd_reject_bad_arguments_without_launch(lib):
     # kernel's fp16 dQ accumulator (whichever is smaller)
     assert L.mxa_bwd_workspace_bytes(ctypes.byref(bp)) == need
     assert L.mxa_bwd_workspace_min_bytes(ctypes.byref(bp)) == need_min + min(256 * 2 * 128 * 2, 2 * 2 * 2 * 16400)
+    # FP16 per-row boost: boost rows fp32 [Hq, T] and key bounds int32 [T, Hkv]
+    # after the D and LSE rows; the dQ GEMM path only (min == full)
+    bp.dq_mode = mxa.MXA_DQ_FP16_ROW
+    full2 = need + 256 * 2 * 4 + 256 * 2 * 4
+    assert L.mxa_bwd_workspace_bytes(ctypes.byref(bp)) == full2
+    assert L.mxa_bwd_workspace_min_bytes(ctypes.byref(bp)) == full2
+    assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), full2 - 1, None) == mxa.MXA_ERR_WORKSPACE
+    bp.dq_mode = 3
+    assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), full2, None) == mxa.MXA_ERR_ARG
 
 
 def test_cross_attention_shape_checks(lib):
@@ -183,8 +192,9 @@ def test_cross_attention_shape_checks(lib):
     assert need_min == 2 * 2 * 8 * 128 * 4 + 512 + 1024  # 256 + 32 * 16 + 16 = 784 -> 1024
     # the emitted dS: Hq x NT_k x mt(query tiles of the longest document) pairs
     assert L.mxa_bwd_workspace_bytes(ctypes.byref(bp)) == need_min + 2 * 32 * 4 * (16384 + 16)
-    bp.dq_mode = 1
-    assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), 1 << 30, None) == mxa.MXA_ERR_UNSUPPORTED
+    for mode in (mxa.MXA_DQ_FP16_X512, mxa.MXA_DQ_FP16_ROW):
+        bp.dq_mode = mode
+        assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), 1 << 30, None) == mxa.MXA_ERR_UNSUPPORTED
 
 
 def test_rmsnorm_quantize_rejects_bad_eps_without_launch(lib):
