@@ -341,12 +341,15 @@ namespace {
 // fused kernel.
 size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
 
-// FP16 per-row boost mode: the boost of every query row (fp32 [Hq, T]) and
-// the key bound of every (token, kv head) (int32 [T, Hkv]).
+// FP16 per-row boost mode: the boost of every query row (fp32 [Hq, T]), the
+// key bound of every (token, kv head) (int32 [T, Hkv]) and the per-tile key
+// maxima (int32 [Hkv, NT]).
 size_t bwd_boost_bytes(const mxa_shape& s, int dq_mode) {
   if (dq_mode != MXA_DQ_FP16_ROW || s.T <= 0) return 0;
   const size_t T = static_cast<size_t>(s.T);
-  return round256(static_cast<size_t>(s.Hq) * T * 4) + round256(T * static_cast<size_t>(s.Hkv > 0 ? s.Hkv : 0) * 4);
+  const size_t hkv = static_cast<size_t>(s.Hkv > 0 ? s.Hkv : 0);
+  return round256(static_cast<size_t>(s.Hq) * T * 4) + round256(T * hkv * 4) +
+         round256(hkv * static_cast<size_t>(s.ntiles > 0 ? s.ntiles : 0) * 4);
 }
 
 size_t bwd_head_bytes(const mxa_shape& s, int dq_mode = MXA_DQ_FP32) {
@@ -460,7 +463,9 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
     kb.k_codes = p->k_row.codes;
     kb.k_sf = p->k_row.scales;
     kb.key_bound = key_bound;
-    if (launch_key_bound(kb, stream) != cudaSuccess) return MXA_ERR_CUDA;
+    kb.tile_max = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(key_bound) +
+                                             round256(T * static_cast<size_t>(s.Hkv) * 4));
+    if (launch_key_bound(kb, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
   }
   if (launch_bwd_prep(pa, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
 

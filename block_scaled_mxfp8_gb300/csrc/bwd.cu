@@ -146,15 +146,18 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(PrepArgs a) {
 // every (key token j, kv head), v_j = cl2(max_c |V~_jc|) and k_j =
 // cl2(max_c |K~_jc|) from the ROW views, and the bound a query at position j
 // uses: the running maxima of v and k over the document's keys up to j
-// (causal), or over the whole document, summed.  One CTA per (document, kv
-// head) walks the document in chunks of 256 tokens (block max-scan + carry).
+// (causal), or over the whole document, summed.  Two passes over 128-token
+// tiles: per-token values and tile maxima, then the prefix over the tiles.
 namespace {
 
-__device__ __forceinline__ int row_cl2max(const uint8_t* codes, const uint8_t* atom, int r, int d) {
+// cl2(max_c |x~_c|) of one ROW-view vector of D codes (D / 32 groups of 32
+// codes with their scale bytes), or kCl2None; the codes are already loaded.
+template <int D>
+__device__ __forceinline__ int row_cl2max(const uint4 (&w)[D / 16], const uint8_t* atom, int r) {
   int best = kCl2None;
-  for (int g = 0; g < d / 32; ++g) {
-    const uint4* p = reinterpret_cast<const uint4*>(codes + g * 32);
-    const uint4 x = __ldg(p), y = __ldg(p + 1);
+#pragma unroll
+  for (int g = 0; g < D / 32; ++g) {
+    const uint4 x = w[2 * g], y = w[2 * g + 1];
     uint32_t m = __vmaxu4(__vmaxu4(__vmaxu4(x.x & 0x7F7F7F7Fu, x.y & 0x7F7F7F7Fu),
                                    __vmaxu4(x.z & 0x7F7F7F7Fu, x.w & 0x7F7F7F7Fu)),
                           __vmaxu4(__vmaxu4(y.x & 0x7F7F7F7Fu, y.y & 0x7F7F7F7Fu),
@@ -172,54 +175,117 @@ __device__ __forceinline__ int row_cl2max(const uint8_t* codes, const uint8_t* a
 
 }  // namespace
 
-__global__ void __launch_bounds__(256) key_bound_kernel(KeyBoundArgs a) {
-  __shared__ int s_warp[2][8];
+__device__ __forceinline__ uint32_t pack_vk(int v, int k) {
+  return (static_cast<uint32_t>(v & 0xFFFF) << 16) | static_cast<uint32_t>(k & 0xFFFF);
+}
+__device__ __forceinline__ int unpack_v(uint32_t x) { return static_cast<int16_t>(x >> 16); }
+__device__ __forceinline__ int unpack_k(uint32_t x) { return static_cast<int16_t>(x & 0xFFFFu); }
+
+// Pass 1, one CTA per (128-token tile, document, kv head), one thread per
+// token: v_j and k_j (int16 each, packed into key_bound) and the tile's maxima.
+// Both code rows are loaded before any arithmetic (2 D bytes in flight per
+// thread).
+template <int D>
+__global__ void __launch_bounds__(128) key_bound_tiles_kernel(KeyBoundArgs a) {
+  __shared__ int s_m[2][4];
   __shared__ int64_t s_slot;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.x, hk = blockIdx.y;
+  const int tile = blockIdx.x, b = blockIdx.y, hk = blockIdx.z;
   int64_t doc_start, n;
   doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
-  const int64_t tb = doc_tile_base(a.cu_seqlens, b, n, tid, 256, &s_slot);
-  int cv = kCl2None, ck = kCl2None;  // maxima over the earlier chunks
-  for (int64_t c0 = 0; c0 < n; c0 += 256) {
-    const int64_t pos = c0 + tid;
-    int v = kCl2None, k = kCl2None;
-    if (pos < n) {
-      const int64_t t = doc_start + pos;
-      const int64_t atom = (static_cast<int64_t>(hk) * a.ntiles + tb + pos / 128) * kAtomBytes;
-      const int r = static_cast<int>(pos % 128);
-      v = row_cl2max(a.v_codes + (t * a.Hkv + hk) * a.d, a.v_sf + atom, r, a.d);
-      k = row_cl2max(a.k_codes + (t * a.Hkv + hk) * a.d, a.k_sf + atom, r, a.d);
-    }
+  if (static_cast<int64_t>(tile) * 128 >= n) return;
+  const int64_t tb = doc_tile_base(a.cu_seqlens, b, n, tid, 128, &s_slot);
+  const int64_t pos = static_cast<int64_t>(tile) * 128 + tid;
+  int v = kCl2None, k = kCl2None;
+  if (pos < n) {
+    const int64_t t = doc_start + pos;
+    const int64_t atom = (static_cast<int64_t>(hk) * a.ntiles + tb + tile) * kAtomBytes;
+    uint4 wv[D / 16], wk[D / 16];
+    const uint4* pv = reinterpret_cast<const uint4*>(a.v_codes + (t * a.Hkv + hk) * D);
+    const uint4* pk = reinterpret_cast<const uint4*>(a.k_codes + (t * a.Hkv + hk) * D);
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int yv = __shfl_up_sync(0xffffffffu, v, o), yk = __shfl_up_sync(0xffffffffu, k, o);
-      if (lane >= o) {
-        v = yv > v ? yv : v;
-        k = yk > k ? yk : k;
-      }
+    for (int i = 0; i < D / 16; ++i) {
+      wv[i] = __ldg(pv + i);
+      wk[i] = __ldg(pk + i);
     }
-    if (lane == 31) {
-      s_warp[0][warp] = v;
-      s_warp[1][warp] = k;
-    }
-    __syncthreads();
-    int pv = cv, pk = ck;
-    for (int w = 0; w < warp; ++w) {
-      pv = s_warp[0][w] > pv ? s_warp[0][w] : pv;
-      pk = s_warp[1][w] > pk ? s_warp[1][w] : pk;
-    }
-    v = pv > v ? pv : v;
-    k = pk > k ? pk : k;
-    if (a.causal && pos < n) a.key_bound[(doc_start + pos) * a.Hkv + hk] = v + k;
-    for (int w = 0; w < 8; ++w) {
-      cv = s_warp[0][w] > cv ? s_warp[0][w] : cv;
-      ck = s_warp[1][w] > ck ? s_warp[1][w] : ck;
-    }
-    __syncthreads();  // s_warp is rewritten by the next chunk
+    v = row_cl2max<D>(wv, a.v_sf + atom, tid);
+    k = row_cl2max<D>(wk, a.k_sf + atom, tid);
+    a.key_bound[t * a.Hkv + hk] = static_cast<int32_t>(pack_vk(v, k));
   }
-  if (!a.causal)
-    for (int64_t pos = tid; pos < n; pos += 256) a.key_bound[(doc_start + pos) * a.Hkv + hk] = cv + ck;
+  v = __reduce_max_sync(0xffffffffu, v);
+  k = __reduce_max_sync(0xffffffffu, k);
+  if (lane == 0) {
+    s_m[0][warp] = v;
+    s_m[1][warp] = k;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const int vm = max(max(s_m[0][0], s_m[0][1]), max(s_m[0][2], s_m[0][3]));
+    const int km = max(max(s_m[1][0], s_m[1][1]), max(s_m[1][2], s_m[1][3]));
+    a.tile_max[static_cast<int64_t>(hk) * a.ntiles + tb + tile] = static_cast<int32_t>(pack_vk(vm, km));
+  }
+}
+
+// Pass 2, same grid: the maxima of the earlier tiles of the document (causal)
+// or of all its tiles, then the running maxima inside the tile (causal), and
+// key_bound = V + K.
+__global__ void __launch_bounds__(128) key_bound_scan_kernel(KeyBoundArgs a) {
+  __shared__ int s_m[2][4];
+  __shared__ int64_t s_slot;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tile = blockIdx.x, b = blockIdx.y, hk = blockIdx.z;
+  int64_t doc_start, n;
+  doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
+  if (static_cast<int64_t>(tile) * 128 >= n) return;
+  const int64_t tb = doc_tile_base(a.cu_seqlens, b, n, tid, 128, &s_slot);
+  const int ntl = static_cast<int>((n + 127) / 128);
+  const int upto = a.causal ? tile : ntl;
+  int cv = kCl2None, ck = kCl2None;
+  for (int i = tid; i < upto; i += 128) {
+    const uint32_t x = static_cast<uint32_t>(a.tile_max[static_cast<int64_t>(hk) * a.ntiles + tb + i]);
+    cv = max(cv, unpack_v(x));
+    ck = max(ck, unpack_k(x));
+  }
+  cv = __reduce_max_sync(0xffffffffu, cv);
+  ck = __reduce_max_sync(0xffffffffu, ck);
+  if (lane == 0) {
+    s_m[0][warp] = cv;
+    s_m[1][warp] = ck;
+  }
+  __syncthreads();
+  cv = max(max(s_m[0][0], s_m[0][1]), max(s_m[0][2], s_m[0][3]));
+  ck = max(max(s_m[1][0], s_m[1][1]), max(s_m[1][2], s_m[1][3]));
+  const int64_t pos = static_cast<int64_t>(tile) * 128 + tid;
+  const int64_t t = doc_start + pos;
+  if (!a.causal) {
+    if (pos < n) a.key_bound[t * a.Hkv + hk] = cv + ck;
+    return;
+  }
+  int v = kCl2None, k = kCl2None;
+  if (pos < n) {
+    const uint32_t x = static_cast<uint32_t>(a.key_bound[t * a.Hkv + hk]);
+    v = unpack_v(x);
+    k = unpack_k(x);
+  }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int yv = __shfl_up_sync(0xffffffffu, v, o), yk = __shfl_up_sync(0xffffffffu, k, o);
+    if (lane >= o) {
+      v = max(v, yv);
+      k = max(k, yk);
+    }
+  }
+  __syncthreads();  // the carry has been read from s_m
+  if (lane == 31) {
+    s_m[0][warp] = v;
+    s_m[1][warp] = k;
+  }
+  __syncthreads();
+  for (int w = 0; w < warp; ++w) {
+    v = max(v, s_m[0][w]);
+    k = max(k, s_m[1][w]);
+  }
+  if (pos < n) a.key_bound[t * a.Hkv + hk] = max(v, cv) + max(k, ck);
 }
 
 // ----------------------------------------------------------------- dQ convert
@@ -645,8 +711,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   }
 }
 
-cudaError_t launch_key_bound(const KeyBoundArgs& a, cudaStream_t stream) {
-  key_bound_kernel<<<dim3(a.num_docs, a.Hkv), 256, 0, stream>>>(a);
+cudaError_t launch_key_bound(const KeyBoundArgs& a, int max_seqlen, cudaStream_t stream) {
+  const dim3 grid((max_seqlen + 127) / 128, a.num_docs, a.Hkv);
+  if (a.d == 128) key_bound_tiles_kernel<128><<<grid, 128, 0, stream>>>(a);
+  else key_bound_tiles_kernel<64><<<grid, 128, 0, stream>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  key_bound_scan_kernel<<<grid, 128, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

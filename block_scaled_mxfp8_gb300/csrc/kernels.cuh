@@ -189,6 +189,7 @@ struct KeyBoundArgs {
   const uint8_t* k_codes;
   const uint8_t* k_sf;
   int32_t* key_bound;  // [T, Hkv]
+  int32_t* tile_max;   // [Hkv, NT]: per 128-token tile, the maxima of v and k (int16 each)
 };
 
 struct DqConvArgs {
@@ -215,7 +216,7 @@ cudaError_t launch_bwd_split(const BwdArgs& a, const BwdMaps& m, int d, int max_
 // dK/dV kernel emitting dS, then the dQ product over the emitted dS
 cudaError_t launch_bwd_emit(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream);
 cudaError_t launch_dq_gemm(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream);
-cudaError_t launch_key_bound(const KeyBoundArgs& a, cudaStream_t stream);
+cudaError_t launch_key_bound(const KeyBoundArgs& a, int max_seqlen, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const PrepArgs& a, int max_seqlen, cudaStream_t stream);
 cudaError_t launch_dq_convert(const DqConvArgs& a, cudaStream_t stream);
 

@@ -270,9 +270,9 @@ typedef struct {
  *   128) query-tile slots per key tile: Hq * NT_k * mt * 16400 bytes, NT_k
  *   the key side's ntiles (B8 H32 L4096: 4.3 GB).
  *   FP16_ROW mode: after the D and LSE rows, before the lists, the boost
- *   2^beta_i of every query row as fp32 [Hq, T] and the key bound V_t + K_t
- *   of every (token, kv head) as int32 [T, Hkv], each rounded up to 256
- *   bytes. */
+ *   2^beta_i of every query row as fp32 [Hq, T], the key bound V_t + K_t
+ *   of every (token, kv head) as int32 [T, Hkv] and per-tile key maxima as
+ *   int32 [Hkv, ntiles], each rounded up to 256 bytes. */
 size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p);
 
 /* Smallest workspace mxa_bwd accepts: the padded D and LSE rows and the tile

@@ -158,10 +158,11 @@ def test_fwd_bwd_reject_bad_arguments_without_launch(lib):
     # kernel's fp16 dQ accumulator (whichever is smaller)
     assert L.mxa_bwd_workspace_bytes(ctypes.byref(bp)) == need
     assert L.mxa_bwd_workspace_min_bytes(ctypes.byref(bp)) == need_min + min(256 * 2 * 128 * 2, 2 * 2 * 2 * 16400)
-    # FP16 per-row boost: boost rows fp32 [Hq, T] and key bounds int32 [T, Hkv]
-    # after the D and LSE rows; the dQ GEMM path only (min == full)
+    # FP16 per-row boost: boost rows fp32 [Hq, T], key bounds int32 [T, Hkv]
+    # and tile maxima int32 [Hkv, NT] after the D and LSE rows; the dQ GEMM
+    # path only (min == full)
     bp.dq_mode = mxa.MXA_DQ_FP16_ROW
-    full2 = need + 256 * 2 * 4 + 256 * 2 * 4
+    full2 = need + 256 * 2 * 4 + 256 * 2 * 4 + 256
     assert L.mxa_bwd_workspace_bytes(ctypes.byref(bp)) == full2
     assert L.mxa_bwd_workspace_min_bytes(ctypes.byref(bp)) == full2
     assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), full2 - 1, None) == mxa.MXA_ERR_WORKSPACE
