@@ -14,8 +14,9 @@ Sources (page titles, sections):
     "Что такое MXFP8" (32-value groups, E8M0 scale).
   * "FLAMIA 阅读笔记": sec. 2 (attention and its backward, online softmax),
     sec. 3 (token blocks, Hadamard), sec. 4 (scale rule, two-value
-    counterexample, scale doubling), sec. 5 (P cap 2^(c+tau) <= 448, cosine
-    example), sec. 6 (visible-pair count).
+    counterexample, scale doubling, the strict accumulator scale of the FP16
+    dQ reduction), sec. 5 (P cap 2^(c+tau) <= 448, cosine example), sec. 6
+    (visible-pair count).
 
 Parity pins live in ``tests/test_oracle_*.py``.  Unpinned: none of the
 functions below is unpinned; the GPU-side quantisation of P and dS has no
