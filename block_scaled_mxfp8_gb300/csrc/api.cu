@@ -201,6 +201,11 @@ size_t mxa_scale_bytes(int H, int64_t ntiles) {
   return static_cast<size_t>(H) * static_cast<size_t>(ntiles) * kAtomBytes;
 }
 
+size_t mxa_key_scale_bytes(int H, int64_t ntiles) {
+  if (H <= 0 || ntiles < 0) return 0;
+  return static_cast<size_t>(H) * static_cast<size_t>(ntiles) * 128;
+}
+
 }  // extern "C"
 
 namespace {
@@ -282,6 +287,32 @@ mxa_status mxa_rmsnorm_quantize(const void* x, const float* weight, float eps, i
                        weight, eps, stream);
 }
 
+mxa_status mxa_quantize_key(const void* x, int64_t T, int H, int d, const int32_t* cu_seqlens, int num_docs,
+                            int max_seqlen, int64_t ntiles, mxa_qview* key, cudaStream_t stream) {
+  if (!x || !key || T < 0 || T > 0x7FFFFFFFll || H <= 0 || H > 65535 || num_docs <= 0 || num_docs > 65535 ||
+      ntiles <= 0 || max_seqlen <= 0)
+    return MXA_ERR_ARG;
+  if (d != 64 && d != 128) return MXA_ERR_UNSUPPORTED;
+  if (!cu_seqlens && (T % num_docs != 0 || T / num_docs > max_seqlen)) return MXA_ERR_ARG;
+  if (!aligned(x, 16)) return MXA_ERR_ALIGN;
+  mxa_status st = check_view(*key);
+  if (st != MXA_OK) return st;
+  if (T == 0) return MXA_OK;
+  if (cudaMemsetAsync(key->scales, 0x7F, mxa_key_scale_bytes(H, ntiles), stream) != cudaSuccess) return MXA_ERR_CUDA;
+  KeyQuantArgs a{};
+  a.x = x;
+  a.T = T;
+  a.H = H;
+  a.cu_seqlens = cu_seqlens;
+  a.num_docs = num_docs;
+  a.ntiles = ntiles;
+  a.codes = key->codes;
+  a.scales = key->scales;
+  const int maxlen = cu_seqlens ? max_seqlen : static_cast<int>(T / num_docs);
+  if (launch_quantize_key(a, d, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
+  return MXA_OK;
+}
+
 size_t mxa_fwd_workspace_bytes(const mxa_fwd_params* p) {
   if (!p || check_shape(p->shape) != MXA_OK || !uses_list(p->shape)) return 0;
   return list_bytes(p->shape, q_side(p->shape));
@@ -297,6 +328,12 @@ mxa_status mxa_fwd(const mxa_fwd_params* p, cudaStream_t stream) {
     return st;
   if (!p->o || !p->lse) return MXA_ERR_ARG;
   if (!aligned(p->o, 16) || !aligned(p->lse, 4)) return MXA_ERR_ALIGN;
+  // strict causal fold on the diagonal tile (self-attention only)
+  const bool fold = p->v_key.codes != nullptr;
+  if (fold) {
+    if ((st = check_view(p->v_key)) != MXA_OK) return st;
+    if (is_cross(s)) return MXA_ERR_UNSUPPORTED;
+  }
   const bool use_list = p->workspace && uses_list(s) && p->workspace_bytes >= list_bytes(s, q_side(s));
   if (use_list && !aligned(p->workspace, 256)) return MXA_ERR_ALIGN;
   if (s.T == 0) return MXA_OK;
@@ -306,6 +343,7 @@ mxa_status mxa_fwd(const mxa_fwd_params* p, cudaStream_t stream) {
       !make_code_map(&maps.k, p->k_row.codes, ks.T, s.Hkv, s.d) ||
       !make_code_map(&maps.v, p->v_tok.codes, ks.T, s.Hkv, s.d))
     return MXA_ERR_CUDA;
+  if (fold && s.causal && !make_code_map(&maps.vkey, p->v_key.codes, ks.T, s.Hkv, s.d)) return MXA_ERR_CUDA;
   FwdArgs a{};
   a.T = s.T;
   a.Hq = s.Hq;
@@ -320,6 +358,7 @@ mxa_status mxa_fwd(const mxa_fwd_params* p, cudaStream_t stream) {
   a.q_sf = p->q_row.scales;
   a.k_sf = p->k_row.scales;
   a.v_sf = p->v_tok.scales;
+  a.vkey_sf = (fold && s.causal) ? p->v_key.scales : nullptr;
   a.o = p->o;
   a.lse = p->lse;
   a.err = device_error_word();

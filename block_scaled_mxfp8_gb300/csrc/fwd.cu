@@ -31,9 +31,19 @@
 // K and V tiles stream through separate three-stage rings (256 keys per
 // stage).
 //
+// Strict causal mode (a per-key view of V given): on each query's diagonal
+// 128-key tile, where a 32-key scale group of V would straddle the query,
+// every key carries its own power-of-two scale 2^e_k, folded into the
+// probability operand (FLAMIA notes sec. 4): P'_ik = p_ik 2^e_k is
+// quantized per query row and 32 keys by the MX rule, multiplied with the
+// per-key codes (B scale 1), and the MMA of those K steps runs with N = D so
+// that the ones column skips them; the weights the codes stand for,
+// q(P') 2^e_blk 2^-e_k, are summed in registers and added to L at the end.
+//
 // TMEM columns: S [0,256), O [256,256+D) and L [256+D,256+D+16), Q-scale 400,
 // K-scale 404 + 8 (j mod 2) (two atoms per 256 keys), V-scale atoms 420 and 428 each
-// followed by a column block of 1.0 for the ones rows, P-scale 436, P
+// followed by a column block of 1.0 for the ones rows, P-scale 436, the folded
+// P' scales 440 (K steps 0, 1 of the diagonal half) and 444 (K steps 2, 3), P
 // [448,512).
 #include <cuda_bf16.h>
 
@@ -55,7 +65,8 @@ struct FwdCfg {
   static constexpr int kThreads = 608;                // 3 role warps + 16 softmax warps
   static constexpr int kSoftmaxThreads = 512;
   static constexpr uint32_t kColS = 0, kColO = 256, kColL = 256 + D, kColSfQ = 400, kColSfK = 404, kColSfVA = 420,
-                            kColOneA = 424, kColSfVB = 428, kColOneB = 432, kColSfP = 436, kColP = 448;
+                            kColOneA = 424, kColSfVB = 428, kColOneB = 432, kColSfP = 436, kColSfPd = 440,
+                            kColP = 448;
   // shared memory map (offsets from the 1024-aligned base)
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 128 * D;
@@ -64,7 +75,8 @@ struct FwdCfg {
   static constexpr int kOffSfQ = kOffOnes + 4096;
   static constexpr int kOffSfK = kOffSfQ + kAtomBytes;         // 2 atoms per stage
   static constexpr int kOffSfV = kOffSfK + kStages * 2 * kAtomBytes;
-  static constexpr int kSmemBytes = kOffSfV + kStages * 2 * kAtomBytes + 1024;  // + alignment slack
+  static constexpr int kOffSfOne = kOffSfV + kStages * 2 * kAtomBytes;  // an atom of scale 1.0 (per-key V codes)
+  static constexpr int kSmemBytes = kOffSfOne + kAtomBytes + 1024;      // + alignment slack
 };
 
 // Row maximum of 64 scores in four independent chains.
@@ -95,9 +107,70 @@ __device__ __forceinline__ void ld64(uint32_t taddr, float (&v)[64]) {
   }
 }
 
+// 2^(b - 127) of a UE8M0 byte (b = 0: 2^-127).
+__device__ __forceinline__ float ue8m0_f32(uint32_t b) {
+  return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
+}
+
+// The diagonal tile's fold for one thread's 64 key columns, 32 at a time,
+// read again from TMEM at tS (the last iteration's S is never overwritten):
+// the weights p = 2^(s sl2 - m + 4) (summed into lsa/lsb as elsewhere),
+// times 2^e_k of each key (kexp: its 64 exponent bytes, 16-byte aligned),
+// quantized per 32 keys by the MX rule into pw; columns at or past lim are
+// masked.  Returns the sum of the weights the codes stand for,
+// code 2^e_blk 2^-e_k; the two block scale bytes go to sfb (byte blk).
+__device__ __forceinline__ float fold_keys(uint32_t tS, int col0, int lim, const uint8_t* kexp, uint64_t sl2x2,
+                                           uint64_t neg2, uint64_t& lsa, uint64_t& lsb, uint32_t (&pw)[16],
+                                           uint32_t& sfb) {
+  float lw = 0.0f;
+  sfb = 0u;
+#pragma unroll
+  for (int blk = 0; blk < 2; ++blk) {
+    float x[32];
+    {
+      uint32_t rr[32];
+      tmem_ld32(tS + 32 * blk, rr);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 32; ++c) x[c] = (col0 + 32 * blk + c < lim) ? __uint_as_float(rr[c]) : -INFINITY;
+    }
+    float am = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 32; c += 4) {
+      const float2 x01 = f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), sl2x2, neg2));
+      const float2 x23 = f2_unpack(f2_fma(f2_pack(x[c + 2], x[c + 3]), sl2x2, neg2));
+      const float p0 = ex2_approx(x01.x), p1 = ex2_approx(x01.y);
+      const float p2 = ex2_approx(x23.x), p3 = ex2_approx(x23.y);
+      lsa = f2_add(lsa, f2_pack(p0, p1));
+      lsb = f2_add(lsb, f2_pack(p2, p3));
+      const uint32_t eb = __ldg(reinterpret_cast<const uint32_t*>(kexp + 32 * blk + c));
+      x[c] = p0 * ue8m0_f32(eb & 0xFFu);
+      x[c + 1] = p1 * ue8m0_f32((eb >> 8) & 0xFFu);
+      x[c + 2] = p2 * ue8m0_f32((eb >> 16) & 0xFFu);
+      x[c + 3] = p3 * ue8m0_f32(eb >> 24);
+      am = fmax3(am, fmaxf(x[c], x[c + 1]), fmaxf(x[c + 2], x[c + 3]));
+    }
+    const int e = mx_exponent_bits(__float_as_uint(am));
+    const float sc = exp2i_neg(e), up = exp2i_neg(-e);
+#pragma unroll
+    for (int c = 0; c < 32; c += 4) {
+      const uint32_t w = pack_e4m3x4(x[c] * sc, x[c + 1] * sc, x[c + 2] * sc, x[c + 3] * sc);
+      pw[8 * blk + (c >> 2)] = w;
+      const float2 d01 = e4m3x2_to_f32x2(w & 0xFFFFu), d23 = e4m3x2_to_f32x2(w >> 16);
+      const uint32_t eb = __ldg(reinterpret_cast<const uint32_t*>(kexp + 32 * blk + c));
+      lw += (d01.x * up) * exp2i_neg(static_cast<int>(eb & 0xFFu) - 127);
+      lw += (d01.y * up) * exp2i_neg(static_cast<int>((eb >> 8) & 0xFFu) - 127);
+      lw += (d23.x * up) * exp2i_neg(static_cast<int>((eb >> 16) & 0xFFu) - 127);
+      lw += (d23.y * up) * exp2i_neg(static_cast<int>(eb >> 24) - 127);
+    }
+    sfb |= static_cast<uint32_t>(e + 127) << (8 * blk);
+  }
+  return lw;
+}
+
 }  // namespace
 
-template <int D>
+template <int D, bool FOLD>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdArgs a) {
   using C = FwdCfg<D>;
@@ -167,6 +240,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   }
   for (int i = tid; i < 4096 / 16; i += C::kThreads)
     reinterpret_cast<uint4*>(smem + C::kOffOnes)[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+  for (int i = tid; i < kAtomBytes / 16; i += C::kThreads)
+    reinterpret_cast<uint4*>(smem + C::kOffSfOne)[i] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  // strict causal fold: the last iteration's half (qt % 2) is the diagonal tile
+  const bool fold = FOLD && a.causal;
+  const int dh = qt & 1;
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -216,8 +294,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         uint8_t* sv = smem + C::kOffV + s * C::kKVBytes;
         uint8_t* sfv = smem + C::kOffSfV + s * 2 * kAtomBytes;
         mbar_arrive_expect_tx(&bar_v_full[s], C::kKVBytes + 2 * kAtomBytes);
-        tma_load_3d(sv, &maps.v, &bar_v_full[s], 0, hk, k0);
-        tma_load_3d(sv + C::kHalfBytes, &maps.v, &bar_v_full[s], 0, hk, k0 + 128);
+        const bool fold_it = fold && j == n_it - 1;  // the diagonal half from the per-key view
+        tma_load_3d(sv, (fold_it && dh == 0) ? &maps.vkey : &maps.v, &bar_v_full[s], 0, hk, k0);
+        tma_load_3d(sv + C::kHalfBytes, (fold_it && dh == 1) ? &maps.vkey : &maps.v, &bar_v_full[s], 0, hk, k0 + 128);
         bulk_load(sfv, a.v_sf + atom0, kAtomBytes, &bar_v_full[s]);
         bulk_load(sfv + kAtomBytes, a.v_sf + atom1, kAtomBytes, &bar_v_full[s]);
         issued_v = j + 1;
@@ -281,21 +360,27 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       auto v_adv = [](uint64_t d, uint32_t bytes) -> uint64_t {
         return d + (bytes >> 4) - (static_cast<uint64_t>(bytes >> 4) << 16);
       };
-      const uint32_t tO = tmem + C::kColO, tP = tmem + C::kColP, tSfP = tmem + C::kColSfP;
+      const uint32_t tO = tmem + C::kColO, tP = tmem + C::kColP, tSfP = tmem + C::kColSfP, tSfPd = tmem + C::kColSfPd;
+      const uint64_t dSfOne = atom_desc(smem + C::kOffSfOne);
       const uint32_t tSfVA = tmem + C::kColSfVA, tSfVB = tmem + C::kColSfVB;
       for (int j = 0; j < n_it; ++j) {
         const int s = j % C::kStages;
         if (!role_wait(&bar_v_full[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma)) break;
         if (!role_wait(&bar_p_full, j & 1, abort_flag, a.err, kErrTimeoutMma)) break;
         tc_fence_after();
+        const bool fold_it = fold && j == n_it - 1;
         const uint64_t dsf = sdesc_adv(dSfV0, s * 2 * kAtomBytes);
-        tmem_cp_desc(tSfVA, dsf);
-        tmem_cp_desc(tSfVB, sdesc_adv(dsf, kAtomBytes));
+        tmem_cp_desc(tSfVA, (fold_it && dh == 0) ? dSfOne : dsf);
+        tmem_cp_desc(tSfVB, (fold_it && dh == 1) ? dSfOne : sdesc_adv(dsf, kAtomBytes));
         const uint64_t dv = v_adv(dV0, s * C::kKVBytes);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // [O | L] += P [V | 1], 32 keys per step
-          mma_mxf8_ts(tO, tP + 8 * kk, v_adv(dv, kk * C::kKStepBytes), make_idesc_mxf8(128, D + 16, 0, 1, kk & 3, kk & 3),
-                      tSfP, kk < 4 ? tSfVA : tSfVB, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk) {  // [O | L] += P [V | 1], 32 keys per step
+          // folded K steps: per-row P' scales, per-key codes, and N = D (L is summed in registers)
+          const bool fk = fold_it && (kk >> 2) == dh;
+          mma_mxf8_ts(tO, tP + 8 * kk, v_adv(dv, kk * C::kKStepBytes),
+                      make_idesc_mxf8(128, fk ? D : D + 16, 0, 1, kk & 3, kk & 3),
+                      fk ? tSfPd + ((kk & 2) ? 4u : 0u) : tSfP, kk < 4 ? tSfVA : tSfVB, (j > 0 || kk > 0) ? 1u : 0u);
+        }
         mma_commit(&bar_o_done);
         mma_commit(&bar_v_empty[s]);
       }
@@ -322,6 +407,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
     float m = -INFINITY;  // running (lazy) max of the scaled scores, log2 units
     float l16 = 0.0f;     // this warp's sum of 2^(s - m + 4) over its columns
+    float ldiag = 0.0f;   // folded diagonal columns (FOLD): the weights their codes stand for
     bool ok = true;
     for (int j = 0; j < n_it; ++j) {
       if (!(ok = warp_wait(&bar_s_full, j & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
@@ -332,9 +418,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       mbar_arrive(&bar_s_empty);  // S is in registers: the next S MMA may start
       // columns >= lim are masked (keys past the document end, or after the
       // query on the causal diagonal); only the last iteration has any
+      int lim = 256;
       if (j == n_it - 1) {
         const int64_t rem = nk - static_cast<int64_t>(j) * 256;
-        int lim = rem < 256 ? static_cast<int>(rem) : 256;
+        lim = rem < 256 ? static_cast<int>(rem) : 256;
         if (a.causal) {
           const int64_t c = qpos - static_cast<int64_t>(j) * 256 + 1;
           if (c < lim) lim = static_cast<int>(c);
@@ -363,15 +450,24 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       const uint64_t neg2 = f2_pack(neg, neg), sl2x2 = f2_pack(sl2, sl2);
       uint64_t lsa = 0, lsb = 0;  // four partial sums (+0.0) in two pairs
       uint32_t pw[16];  // E4M3 codes of this warp's 64 weights
+      const bool diag = fold && j == n_it - 1 && (part >> 1) == dh;  // warp-uniform
+      uint32_t sfb = 0u;
+      if (!FOLD || !diag) {
 #pragma unroll
-      for (int c = 0; c < 64; c += 4) {
-        const float2 x01 = f2_unpack(f2_fma(f2_pack(sv[c], sv[c + 1]), sl2x2, neg2));
-        const float2 x23 = f2_unpack(f2_fma(f2_pack(sv[c + 2], sv[c + 3]), sl2x2, neg2));
-        const float p0 = ex2_approx(x01.x), p1 = ex2_approx(x01.y);
-        const float p2 = ex2_approx(x23.x), p3 = ex2_approx(x23.y);
-        lsa = f2_add(lsa, f2_pack(p0, p1));
-        lsb = f2_add(lsb, f2_pack(p2, p3));
-        pw[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
+        for (int c = 0; c < 64; c += 4) {
+          const float2 x01 = f2_unpack(f2_fma(f2_pack(sv[c], sv[c + 1]), sl2x2, neg2));
+          const float2 x23 = f2_unpack(f2_fma(f2_pack(sv[c + 2], sv[c + 3]), sl2x2, neg2));
+          const float p0 = ex2_approx(x01.x), p1 = ex2_approx(x01.y);
+          const float p2 = ex2_approx(x23.x), p3 = ex2_approx(x23.y);
+          lsa = f2_add(lsa, f2_pack(p0, p1));
+          lsb = f2_add(lsb, f2_pack(p2, p3));
+          pw[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
+        }
+      } else if constexpr (FOLD) {
+        // the 128 exponents of the diagonal tile (tile qt of this document),
+        // 64 per column quarter; the sums run in units of 2^4 p like l16
+        const uint8_t* kexp = a.vkey_sf + (static_cast<int64_t>(hk) * a.ntiles_k + ktile_base + qt) * 128 + 64 * (part & 1);
+        ldiag = fold_keys(lane_base + C::kColS + 64 * part, 64 * part, lim, kexp, sl2x2, neg2, lsa, lsb, pw, sfb);
       }
       const float2 la = f2_unpack(lsa), lb = f2_unpack(lsb);
       const float lsum = (la.x + la.y) + (lb.x + lb.y);
@@ -427,6 +523,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
         tmem_st8(lane_base + C::kColP + 16 * part, w0);
         tmem_st8(lane_base + C::kColP + 16 * part + 8, w1);
+        if (FOLD && diag) {
+          // K steps 2 (part & 1) and 2 (part & 1) + 1 of the diagonal half: the
+          // scale of row r at lane r, column base + r / 32, byte = sf_id
+          const uint32_t v = (part & 1) ? (0x00007F7Fu | (sfb << 16)) : (0x7F7F0000u | sfb);
+          tmem_st1(lane_base + C::kColSfPd + 4 * (part & 1) + quad, v);
+        }
       }
       l16 = l16 * factor + lsum;
       tmem_st_wait();
@@ -435,6 +537,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
     // ---------------------------------------------------------- epilogue
     s_l[part][r] = l16;
+    // the folded weights through the maxima buffer of the parity the last
+    // iteration did not use (every warp of the quadrant read it before the
+    // last iteration's max barrier)
+    if (FOLD && fold) s_mx[n_it & 1][part][r] = ldiag;
     mbar_arrive(&bar_lsum);
     if (ok) ok = role_wait(&bar_lsum, 0, abort_flag, a.err, kErrTimeoutEpilogue);
     if (ok) ok = role_wait(&bar_o_done, (n_it - 1) & 1, abort_flag, a.err, kErrTimeoutEpilogue);
@@ -445,7 +551,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         uint32_t rr[16];
         tmem_ld16(lane_base + C::kColL, rr);
         tmem_ld_wait();
-        inv = 1.0f / __uint_as_float(rr[0]);
+        float lq = __uint_as_float(rr[0]);
+        if (FOLD && fold) lq += s_mx[n_it & 1][2 * dh][r] + s_mx[n_it & 1][2 * dh + 1][r];
+        inv = 1.0f / lq;
       }
       const bool valid = qpos < n;
       const int64_t t = doc_start + qpos;
@@ -482,21 +590,26 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   }
 }
 
+namespace {
+
+template <int D, bool FOLD>
+cudaError_t launch_fwd_t(const FwdArgs& a, const FwdMaps& m, const dim3& grid, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_fwd_kernel<D, FOLD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  attn_fwd_kernel<D, FOLD><<<grid, C::kThreads, C::kSmemBytes, stream>>>(m, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_fwd(const FwdArgs& a, const FwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
   const dim3 grid = a.items ? dim3(static_cast<unsigned>(a.ntiles * a.Hq))
                             : dim3((max_seqlen + 127) / 128, a.num_docs, a.Hq);
-  if (d == 128) {
-    using C = FwdCfg<128>;
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attn_fwd_kernel<128><<<grid, C::kThreads, C::kSmemBytes, stream>>>(m, a);
-  } else {
-    using C = FwdCfg<64>;
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attn_fwd_kernel<64><<<grid, C::kThreads, C::kSmemBytes, stream>>>(m, a);
-  }
-  return cudaGetLastError();
+  const bool fold = a.vkey_sf != nullptr && a.causal;
+  if (d == 128) return fold ? launch_fwd_t<128, true>(a, m, grid, stream) : launch_fwd_t<128, false>(a, m, grid, stream);
+  return fold ? launch_fwd_t<64, true>(a, m, grid, stream) : launch_fwd_t<64, false>(a, m, grid, stream);
 }
 
 }  // namespace mxa

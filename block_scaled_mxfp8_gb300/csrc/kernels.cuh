@@ -77,6 +77,18 @@ struct QuantArgs {
   float rms_eps;
 };
 
+// Per-key view: one UE8M0 exponent per (token, head) over all d channels.
+struct KeyQuantArgs {
+  const void* x;  // bf16 [T, H, d]
+  int64_t T;
+  int H;
+  const int32_t* cu_seqlens;
+  int num_docs;
+  int64_t ntiles;
+  uint8_t* codes;   // [T, H, d]
+  uint8_t* scales;  // [H, NT, 128], tile-padded per document
+};
+
 struct FwdArgs {
   int64_t T;
   int Hq, Hkv;
@@ -93,6 +105,9 @@ struct FwdArgs {
   const uint8_t* q_sf;  // ROW scales of Q [Hq, NT, 512]
   const uint8_t* k_sf;  // ROW scales of K [Hkv, NT_k, 512]
   const uint8_t* v_sf;  // TOK scales of V [Hkv, NT_k, 512]
+  // per-key view of V (null: no fold): UE8M0 exponent per key [Hkv, NT, 128];
+  // its codes are read through FwdMaps::vkey on the causal diagonal tile
+  const uint8_t* vkey_sf;
   void* o;              // bf16 [T, Hq, d]
   float* lse;           // [Hq, T]
   int* err;
@@ -202,12 +217,13 @@ struct DqConvArgs {
 
 // Tensor maps of one attention call (3-D: d, H, T; SW128 for d = 128, SW64 for d = 64).
 struct FwdMaps {
-  CUtensorMap q, k, v;
+  CUtensorMap q, k, v, vkey;  // vkey: set only when FwdArgs::vkey_sf is
 };
 struct BwdMaps {
   CUtensorMap q, k, v, g, qt, kt, gt;
 };
 
+cudaError_t launch_quantize_key(const KeyQuantArgs& a, int d, int max_seqlen, cudaStream_t stream);
 cudaError_t launch_quantize(const QuantArgs& a, int d, bool tokblock, bool hadamard, int max_groups,
                             cudaStream_t stream);
 cudaError_t launch_fwd(const FwdArgs& a, const FwdMaps& m, int d, int max_seqlen, cudaStream_t stream);

@@ -293,6 +293,80 @@ __global__ void __launch_bounds__(QCfg<D>::kThreads) quantize_kernel(QuantArgs a
   }  // 32-token groups
 }
 
+// ------------------------------------------------------------ per-key view
+// FLAMIA notes sec. 4 (moving the scale across the boundary): on the causal
+// diagonal tile each key's V row gets its own power-of-two scale, which the
+// forward folds into the probability operand.  The view: e_t by the MX rule
+// over all d channels of token t and head h, codes E4M3(x * 2^-e_t).  One CTA
+// per (128-token tile, document, head); D / 8 threads per token row, 8
+// channels each.
+template <int D>
+__global__ void __launch_bounds__(256) quantize_key_kernel(KeyQuantArgs a) {
+  constexpr int TPR = D / 8;
+  constexpr int RPP = 256 / TPR;  // rows per pass
+  __shared__ int64_t s_slot;
+  const int tid = threadIdx.x, row0 = tid / TPR, chunk = tid % TPR;
+  const int tile = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
+  int64_t doc_start, n;
+  doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
+  if (static_cast<int64_t>(tile) * 128 >= n) return;
+  // first scale tile of this document (a sum of ceil(n / 128) over the
+  // earlier documents)
+  if (a.cu_seqlens == nullptr) {
+    if (tid == 0) s_slot = static_cast<int64_t>(b) * ((n + 127) / 128);
+  } else {
+    int64_t part = 0;
+    for (int i = tid; i < b; i += 256) part += (a.cu_seqlens[i + 1] - a.cu_seqlens[i] + 127) / 128;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (tid == 0) s_slot = 0;
+    __syncthreads();
+    if ((tid & 31) == 0 && part) atomicAdd(reinterpret_cast<unsigned long long*>(&s_slot), static_cast<unsigned long long>(part));
+  }
+  __syncthreads();
+  const int64_t tb = s_slot;
+  uint4 raw[128 / RPP];
+#pragma unroll
+  for (int i = 0; i < 128 / RPP; ++i) {
+    const int64_t pos = static_cast<int64_t>(tile) * 128 + row0 + i * RPP;
+    raw[i] = pos < n ? __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.x) +
+                                                            ((doc_start + pos) * a.H + h) * D + chunk * 8))
+                     : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int i = 0; i < 128 / RPP; ++i) {
+    const int r = row0 + i * RPP;
+    const int64_t pos = static_cast<int64_t>(tile) * 128 + r;
+    const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[2 * k] = bf16_lo(w[k]);
+      v[2 * k + 1] = bf16_hi(w[k]);
+    }
+    float m = fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
+                    fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
+#pragma unroll
+    for (int o = TPR / 2; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));  // the row's lanes
+    const int e = mx_exponent_bits(__float_as_uint(m));
+    const float sc = exp2i_neg(e);
+    if (pos < n) {
+      uint2 out;
+      out.x = pack_e4m3x4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
+      out.y = pack_e4m3x4(v[4] * sc, v[5] * sc, v[6] * sc, v[7] * sc);
+      *reinterpret_cast<uint2*>(a.codes + ((doc_start + pos) * a.H + h) * D + chunk * 8) = out;
+      if (chunk == 0) a.scales[(static_cast<int64_t>(h) * a.ntiles + tb + tile) * 128 + r] = static_cast<uint8_t>(e + 127);
+    }
+  }
+}
+
+cudaError_t launch_quantize_key(const KeyQuantArgs& a, int d, int max_seqlen, cudaStream_t stream) {
+  const dim3 grid((max_seqlen + 127) / 128, a.num_docs, a.H);
+  if (d == 128) quantize_key_kernel<128><<<grid, 256, 0, stream>>>(a);
+  else quantize_key_kernel<64><<<grid, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quantize(const QuantArgs& a, int d, bool tokblock, bool hadamard, int max_groups,
                             cudaStream_t stream) {
   dim3 grid((max_groups + 3) / 4, a.num_docs, a.H);  // one CTA per 128-token tile

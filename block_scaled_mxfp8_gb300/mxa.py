@@ -69,6 +69,7 @@ class c_fwd_params(ctypes.Structure):
         ("lse", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
+        ("v_key", c_qview),
     ]
 
 
@@ -95,7 +96,7 @@ _lib = None
 
 EXPORTS = [
     "mxa_abi_version", "mxa_status_str", "mxa_scale_tiles", "mxa_scale_tiles_bound", "mxa_scale_bytes",
-    "mxa_quantize", "mxa_rmsnorm_quantize", "mxa_fwd", "mxa_fwd_workspace_bytes", "mxa_bwd_workspace_bytes", "mxa_bwd_workspace_min_bytes", "mxa_bwd",
+    "mxa_quantize", "mxa_rmsnorm_quantize", "mxa_quantize_key", "mxa_key_scale_bytes", "mxa_fwd", "mxa_fwd_workspace_bytes", "mxa_bwd_workspace_bytes", "mxa_bwd_workspace_min_bytes", "mxa_bwd",
     "mxa_bwd_noalloc", "mxa_get_error",
 ]
 # include/mxa_testing.h: the kernels' P and dS quantization run on caller data
@@ -127,6 +128,10 @@ def lib():
         L.mxa_rmsnorm_quantize.restype = i32
         L.mxa_rmsnorm_quantize.argtypes = [P, P, ctypes.c_float, i64, i32, i32, P, i32, i32, i64, i32, i32, i32,
                                            ctypes.POINTER(c_qview), ctypes.POINTER(c_qview), P]
+        L.mxa_quantize_key.restype = i32
+        L.mxa_quantize_key.argtypes = [P, i64, i32, i32, P, i32, i32, i64, ctypes.POINTER(c_qview), P]
+        L.mxa_key_scale_bytes.restype = ctypes.c_size_t
+        L.mxa_key_scale_bytes.argtypes = [i32, i64]
         L.mxa_fwd.restype = i32
         L.mxa_fwd.argtypes = [ctypes.POINTER(c_fwd_params), P]
         L.mxa_fwd_workspace_bytes.restype = ctypes.c_size_t
@@ -311,6 +316,20 @@ def quantize(x: torch.Tensor, geo: Geometry, mode: int = MXA_SCALE_MX32, views: 
     return row, tok
 
 
+def quantize_key(x: torch.Tensor, geo: Geometry, stream=None) -> QView:
+    """Per-key view of x bf16 [T, H, d] (mxa_quantize_key): codes [T, H, d],
+    one UE8M0 exponent per (token, head) in scales [H, NT, 128]."""
+    T, H, d = x.shape
+    assert T == geo.T and x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous()
+    key = QView(torch.empty((T, H, d), dtype=torch.uint8, device=x.device),
+                torch.empty((H, geo.ntiles, 128), dtype=torch.uint8, device=x.device))
+    assert key.scales.numel() == lib().mxa_key_scale_bytes(H, geo.ntiles)
+    st = lib().mxa_quantize_key(_ptr(x), T, H, d, _ptr(geo.cu_seqlens), geo.num_docs, geo.max_seqlen, geo.ntiles,
+                                ctypes.byref(key.c()), _stream(stream))
+    _check(st, "mxa_quantize_key")
+    return key
+
+
 def _shape(geo: Geometry, Hq: int, Hkv: int, d: int, causal: bool, softmax_scale: float,
            kv_geo: Optional[Geometry] = None) -> c_shape:
     """kv_geo: the key/value documents of a cross-attention call (None: self-attention)."""
@@ -326,10 +345,12 @@ def _shape(geo: Geometry, Hq: int, Hkv: int, d: int, causal: bool, softmax_scale
 
 
 def fwd(q_row: QView, k_row: QView, v_tok: QView, geo: Geometry, causal: bool, softmax_scale: float = 0.0,
-        out=None, stream=None, workspace=None, use_list: bool = True, kv_geo: Optional[Geometry] = None):
+        out=None, stream=None, workspace=None, use_list: bool = True, kv_geo: Optional[Geometry] = None,
+        v_key: Optional[QView] = None):
     """-> (O bf16 [T, Hq, d], LSE fp32 [Hq, T]).  With use_list (default) the
     CTAs are scheduled from the cost-sorted tile list, in `workspace` when it
-    is large enough, else in a fresh device buffer."""
+    is large enough, else in a fresh device buffer.  v_key: the per-key view
+    of V (quantize_key) for the strict causal fold on the diagonal tile."""
     T, Hq, d = q_row.codes.shape
     Hkv = k_row.codes.shape[1]
     if out is None:
@@ -345,6 +366,8 @@ def fwd(q_row: QView, k_row: QView, v_tok: QView, geo: Geometry, causal: bool, s
             workspace = torch.empty(need, dtype=torch.uint8, device=q_row.codes.device)
         p.workspace = workspace.data_ptr()
         p.workspace_bytes = workspace.numel()
+    if v_key is not None:
+        p.v_key = v_key.c()
     _check(mxa_fwd(p, stream), "mxa_fwd")
     return o, lse
 

@@ -188,6 +188,26 @@ mxa_status mxa_rmsnorm_quantize(const void* x_bf16, const float* weight, float e
                                 mxa_scale_mode mode, int views, int hadamard, mxa_qview* row, mxa_qview* tok,
                                 cudaStream_t stream);
 
+/* Bytes of the scale buffer of a per-key view: H * NT * 128. */
+size_t mxa_key_scale_bytes(int H, int64_t ntiles);
+
+/* Per-key view of V for the strict causal forward (FLAMIA notes sec. 4,
+ * moving the scale across the boundary: on the diagonal tile each key gets
+ * its own power-of-two scale, which is folded into the probability operand,
+ * P_ij (s_j v_j) = (P_ij s_j) v_j, so that no key's representation depends on
+ * a later key of its 32-token group).  For every (token t, head h): e_t by
+ * the MX rule over all d channels, e = ceil(log2(amax / 448)) (0 for an
+ * all-zero vector), codes E4M3(x * 2^-e_t) (round to nearest even,
+ * saturating).
+ *   key->codes: [T, H, d], 16-byte aligned;
+ *   key->scales: UE8M0 bytes [H, NT, 128], 16-byte aligned, tile-padded per
+ *     document like the other scale layouts (byte (h NT + TB_b + t / 128) 128
+ *     + t % 128 for document-relative token t of document b whose first tile
+ *     is TB_b); first filled with 0x7F (stream-ordered memset).
+ * Other arguments and the status codes as mxa_quantize. */
+mxa_status mxa_quantize_key(const void* x_bf16, int64_t T, int H, int d, const int32_t* cu_seqlens, int num_docs,
+                            int max_seqlen, int64_t ntiles, mxa_qview* key, cudaStream_t stream);
+
 /* Shape shared by the forward and backward calls.
  * Self-attention (T_k = 0): queries, keys and values share one token layout
  * (T, cu_seqlens, max_seqlen, ntiles).
@@ -221,6 +241,12 @@ typedef struct {
   float* lse;       /* out: fp32 [Hq, T], natural-log LSE (alpha included) */
   void* workspace;  /* optional device buffer (256-byte aligned) for the tile work list, or NULL */
   size_t workspace_bytes;
+  mxa_qview v_key;  /* optional V per-key view (mxa_quantize_key), causal self-attention only:
+                       with codes != NULL the P V product of every query's diagonal 128-key
+                       tile uses it, with each key's scale folded into P (P'_ij = P_ij 2^e_j,
+                       quantized per query row and 32 keys by the MX rule), so that O_i and
+                       LSE_i depend on no key after i (FLAMIA notes sec. 4).  Other key tiles
+                       are fully visible and keep v_tok.  NULL codes: no fold. */
 } mxa_fwd_params;
 
 /* Workspace bytes that let mxa_fwd take its CTAs from a cost-sorted work

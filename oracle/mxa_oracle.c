@@ -204,6 +204,29 @@ void orc_quant_row(const uint16_t* x, int64_t T, int H, int d, uint8_t* codes, u
             }
 }
 
+/* Per-key view ([FLAMIA] sec. 4, moving the scale across the boundary: each
+ * key of a diagonal tile carries its own power-of-two scale): one scale per
+ * (token, head) over all d channels, by the same rule as every MX group.
+ * codes [T, H, d]; scales: logical [T, H]. */
+void orc_quant_key(const uint16_t* x, int64_t T, int H, int d, uint8_t* codes, uint8_t* scales)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int h = 0; h < H; ++h) {
+            const uint16_t* xs = x + (t * H + h) * d;
+            double amax = 0.0;
+            for (int i = 0; i < d; ++i) {
+                double v = fabs(orc_bf16_to_double(xs[i]));
+                if (v > amax)
+                    amax = v;
+            }
+            int e = orc_mx_exponent(amax);
+            for (int i = 0; i < d; ++i)
+                codes[(t * H + h) * d + i] = orc_e4m3_encode(ldexp(orc_bf16_to_double(xs[i]), -e));
+            scales[t * H + h] = (uint8_t)(e + 127);
+        }
+}
+
 /* Token view: one scale per (document, 32 consecutive tokens counted from the
  * document start, head, channel); the last group of a document may be short
  * and no group crosses a document boundary.
@@ -588,6 +611,60 @@ void orc_attn_fwd(const double* Q, const double* K, const double* V, int64_t T, 
             LSE[(int64_t)h * T + i] = fwd_row(Q, K, V, Hq, Hkv, d, s, e, causal, alpha, i, h, O + (i * Hq + h) * d, Srow);
         }
         free(Srow);
+    }
+}
+
+/* Causal attention forward with the per-key fold on the diagonal tile
+ * ([FLAMIA] sec. 4): P_ij (s_j v_j) = (P_ij s_j) v_j, so the value row of key
+ * j is its per-key view Vkey_j (decoded: s_j times its codes) when j lies in
+ * the same 128-token tile of the document as query i -- the tile whose
+ * 32-token scale groups would straddle i -- and its token view Vtok_j for
+ * the fully visible tiles before it.  The softmax is the direct one of
+ * orc_attn_fwd.  Q, K [T, H*, d] score views; Vtok, Vkey [T, Hkv, d] decoded;
+ * O [T, Hq, d]; LSE [Hq, T]. */
+void orc_attn_fwd_fold(const double* Q, const double* K, const double* Vtok, const double* Vkey, int64_t T,
+                       int Hq, int Hkv, int d, const int32_t* cu, int ndocs, double alpha, double* O, double* LSE)
+{
+    int nd = num_docs_eff(cu, ndocs);
+    int grp = Hq / Hkv;
+    for (int b = 0; b < nd; ++b) {
+        int64_t s, e;
+        doc_range(cu, ndocs, T, b, &s, &e);
+        int64_t n = e - s;
+        if (n <= 0)
+            continue;
+#pragma omp parallel
+        {
+            double* Srow = (double*)malloc(sizeof(double) * (size_t)n);
+#pragma omp for schedule(dynamic, 8) collapse(2)
+            for (int h = 0; h < Hq; ++h)
+                for (int64_t i = s; i < e; ++i) {
+                    int hk = h / grp;
+                    const double* q = Q + (i * Hq + h) * d;
+                    double m = -INFINITY;
+                    for (int64_t j = s; j <= i; ++j) {
+                        Srow[j - s] = alpha * dot(q, K + (j * Hkv + hk) * d, d);
+                        if (Srow[j - s] > m)
+                            m = Srow[j - s];
+                    }
+                    double* o = O + (i * Hq + h) * d;
+                    for (int k = 0; k < d; ++k)
+                        o[k] = 0.0;
+                    double l = 0.0;
+                    int64_t diag0 = s + ((i - s) / 128) * 128; /* first key of i's tile */
+                    for (int64_t j = s; j <= i; ++j) {
+                        double p = exp(Srow[j - s] - m);
+                        l += p;
+                        const double* v = (j >= diag0 ? Vkey : Vtok) + (j * Hkv + hk) * d;
+                        for (int k = 0; k < d; ++k)
+                            o[k] += p * v[k];
+                    }
+                    for (int k = 0; k < d; ++k)
+                        o[k] /= l;
+                    LSE[(int64_t)h * T + i] = m + log(l);
+                }
+            free(Srow);
+        }
     }
 }
 

@@ -84,6 +84,8 @@ def _L():
                 "orc_quant_tokblock_f32": (None, [P, i64, i32, i32, P, i32, i32, P, P]),
                 "orc_attn_fwd_x": (None, [P, P, P, i64, i64, i32, i32, i32, P, P, i32, f64, P, P]),
                 "orc_attn_bwd_x": (None, [P] * 8 + [i64, i64, i32, i32, i32, P, P, i32, f64] + [P] * 6),
+                "orc_quant_key": (None, [P, i64, i32, i32, P, P]),
+                "orc_attn_fwd_fold": (None, [P, P, P, P, i64, i32, i32, i32, P, i32, f64, P, P]),
                 "orc_dq_row_boost": (None, [P, P, P, i64, i32, i32, i32, P, i32, i32, ctypes.c_float, P]),
                 "orc_num_threads": (i32, []),
             }
@@ -189,6 +191,24 @@ def quant_row(x):
     scales = np.empty((T, H, d // 32), np.uint8)
     _L().orc_quant_row(_p(xu), T, H, d, _p(codes), _p(scales))
     return codes, scales
+
+
+def quant_key(x):
+    """Per-key view: one scale per (token, head) over all d channels.
+    x bf16 [T,H,d] -> (codes uint8 [T,H,d], scales uint8 [T,H])."""
+    xu = _u16(x)
+    T, H, d = xu.shape
+    codes = np.empty((T, H, d), np.uint8)
+    scales = np.empty((T, H), np.uint8)
+    _L().orc_quant_key(_p(xu), T, H, d, _p(codes), _p(scales))
+    return codes, scales
+
+
+def dequant_key(codes, scales):
+    """Decoded per-key view: E4M3 code values times 2^(byte - 127)."""
+    tab = e4m3_table()
+    e = scales.astype(np.int64) - 127
+    return tab[codes] * np.exp2(e.astype(np.float64))[:, :, None]
 
 
 def quant_tok(x, cu_seqlens=None):
@@ -318,6 +338,22 @@ def attn_fwd(Q, K, V, cu_seqlens=None, causal=False, alpha=None, sel=None):
         sel = np.ascontiguousarray(np.asarray(sel, dtype=np.int32).reshape(-1, 2))
     _L().orc_attn_fwd(_p(Q), _p(K), _p(V), T, Hq, Hkv, d, _p(cu), nd, int(bool(causal)), float(alpha),
                       _p(sel), -1 if sel is None else len(sel), _p(O), _p(LSE))
+    return O, LSE
+
+
+def attn_fwd_fold(Q, K, Vtok, Vkey, cu_seqlens=None, alpha=None):
+    """Causal forward with the per-key fold on the diagonal tile (FLAMIA sec.
+    4): key j's value row is Vkey_j when j is in query i's 128-token tile of
+    the document, else Vtok_j.  Returns (O [T,Hq,d], LSE [Hq,T])."""
+    Q, K, Vtok, Vkey = (np.ascontiguousarray(a, dtype=np.float64) for a in (Q, K, Vtok, Vkey))
+    T, Hq, d = Q.shape
+    Hkv = K.shape[1]
+    if alpha is None:
+        alpha = 1.0 / math.sqrt(d)
+    cu, nd = _cu(cu_seqlens)
+    O = np.full((T, Hq, d), np.nan)
+    LSE = np.full((Hq, T), np.nan)
+    _L().orc_attn_fwd_fold(_p(Q), _p(K), _p(Vtok), _p(Vkey), T, Hq, Hkv, d, _p(cu), nd, float(alpha), _p(O), _p(LSE))
     return O, LSE
 
 

@@ -45,7 +45,7 @@ def test_struct_layouts_match_header():
     # sizes of the C structs on this platform (x86-64 / aarch64 LP64)
     assert ctypes.sizeof(mxa.c_qview) == 16
     assert ctypes.sizeof(mxa.c_shape) == 88
-    assert ctypes.sizeof(mxa.c_fwd_params) == 168
+    assert ctypes.sizeof(mxa.c_fwd_params) == 184  # + v_key
     assert ctypes.sizeof(mxa.c_bwd_params) == 248
 
 
@@ -206,3 +206,28 @@ def test_rmsnorm_quantize_rejects_bad_eps_without_launch(lib):
         assert st == mxa.MXA_ERR_ARG
     st = L.mxa_rmsnorm_quantize(256, 258, 1e-6, 256, 1, 128, None, 1, 256, 2, 0, 1, 0, qv, None, None)
     assert st == mxa.MXA_ERR_ALIGN
+
+
+def test_key_view_and_fold_reject_bad_arguments_without_launch(lib):
+    L = lib
+    P = ctypes.c_void_p
+    key = _qv()
+    ok = [P(256), 256, 2, 128, None, 1, 256, 2, ctypes.byref(key), None]
+    assert L.mxa_key_scale_bytes(2, 2) == 2 * 2 * 128
+    for i, bad, st in ((0, None, mxa.MXA_ERR_ARG), (8, None, mxa.MXA_ERR_ARG), (3, 96, mxa.MXA_ERR_UNSUPPORTED),
+                       (0, P(8), mxa.MXA_ERR_ALIGN), (1, 300, mxa.MXA_ERR_ARG)):  # T above max_seqlen
+        a = list(ok)
+        a[i] = bad
+        assert L.mxa_quantize_key(*a) == st, (i, bad)
+    misaligned = mxa.c_qview(264, 256 + 4)
+    a = list(ok)
+    a[8] = ctypes.byref(misaligned)
+    assert L.mxa_quantize_key(*a) == mxa.MXA_ERR_ALIGN
+    # the fold needs self-attention: a per-key view with a key side is refused
+    p = _fwd(T=1024, nd=2, maxlen=512, nt=8)
+    p.shape.T_k, p.shape.max_seqlen_k, p.shape.ntiles_k = 4096, 2048, 32
+    p.v_key = _qv()
+    assert L.mxa_fwd(ctypes.byref(p), None) == mxa.MXA_ERR_UNSUPPORTED
+    p = _fwd()
+    p.v_key = mxa.c_qview(256, 8)
+    assert L.mxa_fwd(ctypes.byref(p), None) == mxa.MXA_ERR_ALIGN

@@ -1,0 +1,102 @@
+"""GPU per-key view and the strict causal forward (FLAMIA reading notes sec. 4:
+each key of the diagonal tile carries its own power-of-two scale, folded into
+the probability operand) against the oracle.
+
+* mxa_quantize_key: codes and exponents bit for bit against the oracle's
+  quant_key (exponents read through the tile-padded [H, NT, 128] layout).
+* The folded forward: O and LSE against the oracle's attn_fwd_fold (key j's
+  value row is its per-key view on query i's diagonal 128-token tile, its
+  token view before it) at the parity bar of the other forward tests.
+* The property: keys, values and queries after position p change, inside
+  p's own 32-token block, and every row <= p keeps O and LSE bit for bit.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_mxfp8_gb300 import inputs as inp
+from oracle import oracle as orc
+
+from ._common import assert_close, gpu_views, metrics, oracle_views, to_np
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    inp.workload("tiny", causal=True),
+    inp.make_custom("d128_ragged_gqa_causal", lengths=[1, 129, 300, 64, 7, 515], Hq=4, Hkv=2, d=128, causal=True,
+                    seed=41),
+    inp.make_custom("d64_ragged", lengths=[256, 100, 383], Hq=2, Hkv=1, d=64, causal=True, seed=42),
+]
+
+
+def _key_scales_logical(scales: torch.Tensor, lengths):
+    """[H, NT, 128] tile-padded exponent bytes -> logical [T, H]."""
+    s = scales.cpu().numpy()
+    out, tb = [], 0
+    for n in lengths:
+        r = np.arange(n)
+        out.append(s[:, tb + r // 128, r % 128].T)
+        tb += (n + 127) // 128
+    return np.concatenate(out, 0)
+
+
+def _lengths(w):
+    return list(w.lengths) if w.lengths is not None else [w.L] * w.B
+
+
+@pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
+def test_quantize_key_bit_exact(w):
+    from block_scaled_mxfp8_gb300 import mxa
+
+    t = inp.tensors(w)
+    geo, _ = gpu_views(w, t, names=())
+    key = mxa.quantize_key(t["v"].cuda().contiguous(), geo)
+    torch.cuda.synchronize()
+    codes, scales = orc.quant_key(t["v"])
+    assert np.array_equal(key.codes.cpu().numpy(), codes)
+    assert np.array_equal(_key_scales_logical(key.scales, _lengths(w)), scales)
+
+
+def _fold_fwd(w, t):
+    from block_scaled_mxfp8_gb300 import mxa
+
+    geo, gv = gpu_views(w, t)
+    key = mxa.quantize_key(t["v"].cuda().contiguous(), geo)
+    o, lse = mxa.fwd(gv["q"][0], gv["k"][0], gv["v"][1], geo, True, v_key=key)
+    torch.cuda.synchronize()
+    mxa.check_error()
+    return o, lse
+
+
+@pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
+def test_fold_forward_matches_oracle(w):
+    t = inp.tensors(w)
+    o, lse = _fold_fwd(w, t)
+    _, d = oracle_views(w, t, names=("q", "k", "v"))
+    vk = orc.dequant_key(*orc.quant_key(t["v"]))
+    O, L = orc.attn_fwd_fold(d["q"]["row"], d["k"]["row"], d["v"]["tok"], vk, w.cu_seqlens.numpy(),
+                             1.0 / math.sqrt(w.d))
+    print(w.name, "O", metrics(to_np(o), O))
+    assert_close("O", to_np(o), O)
+    lerr = np.abs(lse.cpu().numpy().astype(np.float64) - L).max()
+    assert lerr <= 1e-3 * np.abs(L).max(), lerr
+
+
+def test_fold_forward_prefix_is_bit_identical_under_in_block_changes():
+    w = inp.make_custom("fold_prefix", lengths=[600, 333], Hq=4, Hkv=2, d=128, causal=True, seed=43)
+    t = inp.tensors(w)
+    base = _fold_fwd(w, t)
+    again = _fold_fwd(w, t)
+    assert torch.equal(base[0], again[0]) and torch.equal(base[1], again[1]), "the forward must be deterministic"
+    rng = np.random.default_rng(44)
+    for p in (35, 140, 255, 256, 300, 517):  # inside a 32-token block, tile starts and ends
+        tp = {k: x.clone() for k, x in t.items()}
+        gain = float(rng.choice([-300.0, 64.0, 1e-3]))
+        for k in ("q", "k", "v"):
+            tp[k][p + 1:600] = (tp[k][p + 1:600].float() * gain).to(torch.bfloat16)
+        o, lse = _fold_fwd(w, tp)
+        assert torch.equal(o[: p + 1], base[0][: p + 1]), p
+        assert torch.equal(lse[:, : p + 1], base[1][:, : p + 1]), p
+        assert torch.equal(o[600:], base[0][600:]) and torch.equal(lse[:, 600:], base[1][:, 600:])
