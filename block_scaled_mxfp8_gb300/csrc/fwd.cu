@@ -117,8 +117,10 @@ __device__ __forceinline__ float ue8m0_f32(uint32_t b) {
 // the weights p = 2^(s sl2 - m + 4) (summed into lsa/lsb as elsewhere),
 // times 2^e_k of each key (kexp: its 64 exponent bytes, 16-byte aligned),
 // quantized per 32 keys by the MX rule into pw; columns at or past lim are
-// masked.  Returns the sum of the weights the codes stand for,
-// code 2^e_blk 2^-e_k; the two block scale bytes go to sfb (byte blk).
+// masked.  The block's MMA scale is 2^(e_blk - 4), which also removes the
+// boost.  Returns the sum of the weights the codes stand for,
+// code 2^(e_blk - 4) 2^-e_k (the units of the L column); the two block scale
+// bytes go to sfb (byte blk).
 __device__ __forceinline__ float fold_keys(uint32_t tS, int col0, int lim, const uint8_t* kexp, uint64_t sl2x2,
                                            uint64_t neg2, uint64_t& lsa, uint64_t& lsb, uint32_t (&pw)[16],
                                            uint32_t& sfb) {
@@ -151,7 +153,11 @@ __device__ __forceinline__ float fold_keys(uint32_t tS, int col0, int lim, const
       am = fmax3(am, fmaxf(x[c], x[c + 1]), fmaxf(x[c + 2], x[c + 3]));
     }
     const int e = mx_exponent_bits(__float_as_uint(am));
-    const float sc = exp2i_neg(e), up = exp2i_neg(-e);
+    const float sc = exp2i_neg(e);
+    // the block's MMA scale 2^(e - 4) also takes out the 2^4 boost that p
+    // carries (the other K steps' constant 2^-4)
+    const int sb = e + 127 - 4 < 0 ? 0 : e + 127 - 4;
+    const float up = ue8m0_f32(static_cast<uint32_t>(sb));
 #pragma unroll
     for (int c = 0; c < 32; c += 4) {
       const uint32_t w = pack_e4m3x4(x[c] * sc, x[c + 1] * sc, x[c + 2] * sc, x[c + 3] * sc);
@@ -163,7 +169,7 @@ __device__ __forceinline__ float fold_keys(uint32_t tS, int col0, int lim, const
       lw += (d23.x * up) * exp2i_neg(static_cast<int>((eb >> 16) & 0xFFu) - 127);
       lw += (d23.y * up) * exp2i_neg(static_cast<int>(eb >> 24) - 127);
     }
-    sfb |= static_cast<uint32_t>(e + 127) << (8 * blk);
+    sfb |= static_cast<uint32_t>(sb) << (8 * blk);
   }
   return lw;
 }
@@ -373,13 +379,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         tmem_cp_desc(tSfVA, (fold_it && dh == 0) ? dSfOne : dsf);
         tmem_cp_desc(tSfVB, (fold_it && dh == 1) ? dSfOne : sdesc_adv(dsf, kAtomBytes));
         const uint64_t dv = v_adv(dV0, s * C::kKVBytes);
+        // the folded half goes last, so that the first K step of the first
+        // iteration -- the one that starts the sums -- also writes L
+        const int rot = (fold_it && dh == 0) ? 4 : 0;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // [O | L] += P [V | 1], 32 keys per step
+        for (int ki = 0; ki < 8; ++ki) {  // [O | L] += P [V | 1], 32 keys per step
+          const int kk = (ki + rot) & 7;
           // folded K steps: per-row P' scales, per-key codes, and N = D (L is summed in registers)
           const bool fk = fold_it && (kk >> 2) == dh;
           mma_mxf8_ts(tO, tP + 8 * kk, v_adv(dv, kk * C::kKStepBytes),
                       make_idesc_mxf8(128, fk ? D : D + 16, 0, 1, kk & 3, kk & 3),
-                      fk ? tSfPd + ((kk & 2) ? 4u : 0u) : tSfP, kk < 4 ? tSfVA : tSfVB, (j > 0 || kk > 0) ? 1u : 0u);
+                      fk ? tSfPd + ((kk & 2) ? 4u : 0u) : tSfP, kk < 4 ? tSfVA : tSfVB, (j > 0 || ki > 0) ? 1u : 0u);
         }
         mma_commit(&bar_o_done);
         mma_commit(&bar_v_empty[s]);

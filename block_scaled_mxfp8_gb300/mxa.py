@@ -316,13 +316,13 @@ def quantize(x: torch.Tensor, geo: Geometry, mode: int = MXA_SCALE_MX32, views: 
     return row, tok
 
 
-def quantize_key(x: torch.Tensor, geo: Geometry, stream=None) -> QView:
+def quantize_key(x: torch.Tensor, geo: Geometry, out: Optional[QView] = None, stream=None) -> QView:
     """Per-key view of x bf16 [T, H, d] (mxa_quantize_key): codes [T, H, d],
     one UE8M0 exponent per (token, head) in scales [H, NT, 128]."""
     T, H, d = x.shape
     assert T == geo.T and x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous()
-    key = QView(torch.empty((T, H, d), dtype=torch.uint8, device=x.device),
-                torch.empty((H, geo.ntiles, 128), dtype=torch.uint8, device=x.device))
+    key = out if out is not None else QView(torch.empty((T, H, d), dtype=torch.uint8, device=x.device),
+                                            torch.empty((H, geo.ntiles, 128), dtype=torch.uint8, device=x.device))
     assert key.scales.numel() == lib().mxa_key_scale_bytes(H, geo.ntiles)
     st = lib().mxa_quantize_key(_ptr(x), T, H, d, _ptr(geo.cu_seqlens), geo.num_docs, geo.max_seqlen, geo.ntiles,
                                 ctypes.byref(key.c()), _stream(stream))

@@ -59,11 +59,11 @@ def test_quantize_key_bit_exact(w):
     assert np.array_equal(_key_scales_logical(key.scales, _lengths(w)), scales)
 
 
-def _fold_fwd(w, t):
+def _fold_fwd(w, t, fold=True):
     from block_scaled_mxfp8_gb300 import mxa
 
     geo, gv = gpu_views(w, t)
-    key = mxa.quantize_key(t["v"].cuda().contiguous(), geo)
+    key = mxa.quantize_key(t["v"].cuda().contiguous(), geo) if fold else None
     o, lse = mxa.fwd(gv["q"][0], gv["k"][0], gv["v"][1], geo, True, v_key=key)
     torch.cuda.synchronize()
     mxa.check_error()
@@ -90,7 +90,9 @@ def test_fold_forward_prefix_is_bit_identical_under_in_block_changes():
     base = _fold_fwd(w, t)
     again = _fold_fwd(w, t)
     assert torch.equal(base[0], again[0]) and torch.equal(base[1], again[1]), "the forward must be deterministic"
+    plain = _fold_fwd(w, t, fold=False)
     rng = np.random.default_rng(44)
+    moved = 0
     for p in (35, 140, 255, 256, 300, 517):  # inside a 32-token block, tile starts and ends
         tp = {k: x.clone() for k, x in t.items()}
         gain = float(rng.choice([-300.0, 64.0, 1e-3]))
@@ -100,3 +102,10 @@ def test_fold_forward_prefix_is_bit_identical_under_in_block_changes():
         assert torch.equal(o[: p + 1], base[0][: p + 1]), p
         assert torch.equal(lse[:, : p + 1], base[1][:, : p + 1]), p
         assert torch.equal(o[600:], base[0][600:]) and torch.equal(lse[:, 600:], base[1][:, 600:])
+        # control: without the fold the token view's groups straddle p, and
+        # rows of p's block before p may move (rows of earlier blocks may not)
+        o0, _ = _fold_fwd(w, tp, fold=False)
+        blk = (p // 32) * 32
+        assert torch.equal(o0[:blk], plain[0][:blk]), p
+        moved += int(not torch.equal(o0[blk: p + 1], plain[0][blk: p + 1]))
+    assert moved > 0, "the perturbations never reached the unfolded prefix: the check would not discriminate"
