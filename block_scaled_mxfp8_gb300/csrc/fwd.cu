@@ -121,9 +121,20 @@ __device__ __forceinline__ float ue8m0_f32(uint32_t b) {
 // boost.  Returns the sum of the weights the codes stand for,
 // code 2^(e_blk - 4) 2^-e_k (the units of the L column); the two block scale
 // bytes go to sfb (byte blk).
-__device__ __forceinline__ float fold_keys(uint32_t tS, int col0, int lim, const uint8_t* kexp, uint64_t sl2x2,
-                                           uint64_t neg2, uint64_t& lsa, uint64_t& lsb, uint32_t (&pw)[16],
-                                           uint32_t& sfb) {
+// Out of line: it runs once per CTA, and kept apart its temporaries do not
+// raise the register demand of the main loop.
+struct FoldOut {
+  uint32_t pw[16];
+  uint32_t sfb;
+  float lw;
+  uint64_t lsa, lsb;
+};
+
+__device__ __noinline__ FoldOut fold_keys(uint32_t tS, int col0, int lim, const uint8_t* kexp, uint64_t sl2x2,
+                                          uint64_t neg2, uint64_t lsa, uint64_t lsb) {
+  FoldOut out;
+  uint32_t (&pw)[16] = out.pw;
+  uint32_t& sfb = out.sfb;
   float lw = 0.0f;
   sfb = 0u;
 #pragma unroll
@@ -171,7 +182,10 @@ __device__ __forceinline__ float fold_keys(uint32_t tS, int col0, int lim, const
     }
     sfb |= static_cast<uint32_t>(sb) << (8 * blk);
   }
-  return lw;
+  out.lw = lw;
+  out.lsa = lsa;
+  out.lsb = lsb;
+  return out;
 }
 
 }  // namespace
@@ -477,7 +491,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         // the 128 exponents of the diagonal tile (tile qt of this document),
         // 64 per column quarter; the sums run in units of 2^4 p like l16
         const uint8_t* kexp = a.vkey_sf + (static_cast<int64_t>(hk) * a.ntiles_k + ktile_base + qt) * 128 + 64 * (part & 1);
-        ldiag = fold_keys(lane_base + C::kColS + 64 * part, 64 * part, lim, kexp, sl2x2, neg2, lsa, lsb, pw, sfb);
+        const FoldOut fo = fold_keys(lane_base + C::kColS + 64 * part, 64 * part, lim, kexp, sl2x2, neg2, lsa, lsb);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) pw[k] = fo.pw[k];
+        sfb = fo.sfb;
+        ldiag = fo.lw;
+        lsa = fo.lsa;
+        lsb = fo.lsb;
       }
       const float2 la = f2_unpack(lsa), lb = f2_unpack(lsb);
       const float lsum = (la.x + la.y) + (lb.x + lb.y);
