@@ -123,7 +123,7 @@ class ClockSampler:
 
 # dram__bytes_read.sum + dram__bytes_write.sum of attn_bwd_dkdv_kernel and
 # attn_dq_gemm_kernel at B2 H32 L4096 d128 (one ncu --set full capture)
-BWD_DRAM_BYTES_B2 = (0.265042 + 1.156755 + 1.111560 + 0.063097) * 1e9
+BWD_DRAM_BYTES_B2 = (0.267132 + 1.156867 + 1.114714 + 0.062789) * 1e9
 
 
 def flops(B, H, L, d, causal, lengths=None, lengths_k=None):
