@@ -97,11 +97,12 @@ size_t bwd_rows_bytes(const mxa_shape& s) {
   return 2 * static_cast<size_t>(s.Hq) * static_cast<size_t>(s.ntiles > 0 ? s.ntiles : 0) * 128 * 4;
 }
 
-// Bytes of the emitted dS (16 KB of codes + 16 block scales per tile pair).
-size_t bwd_ds_bytes(const mxa_shape& s) {
+// Bytes of the emitted dS (16 KB of codes + 16 block scales per tile pair,
+// or a 512-byte scale atom per pair for the strict dQ operand).
+size_t bwd_ds_bytes(const mxa_shape& s, bool strict = false) {
   const int64_t ntk = k_side(s).ntiles;
   return static_cast<size_t>(s.Hq) * static_cast<size_t>(ntk > 0 ? ntk : 0) *
-         static_cast<size_t>(max_doc_tiles(s)) * (16384 + 16);
+         static_cast<size_t>(max_doc_tiles(s)) * (16384 + (strict ? kAtomBytes : 16));
 }
 
 // Bytes of one side's cost-sorted tile list.
@@ -409,7 +410,8 @@ bool bwd_shape_sizable(const mxa_bwd_params* p) {
 size_t mxa_bwd_workspace_min_bytes(const mxa_bwd_params* p) {
   if (!bwd_shape_sizable(p)) return 0;
   const size_t head = bwd_head_bytes(p->shape, p->dq_mode);
-  if (p->dq_mode == MXA_DQ_FP16_ROW) return head + bwd_ds_bytes(p->shape);  // the dQ GEMM only
+  const bool strict = p->k_key.codes != nullptr;
+  if (p->dq_mode == MXA_DQ_FP16_ROW || strict) return head + bwd_ds_bytes(p->shape, strict);  // the dQ GEMM only
   if (p->dq_mode != MXA_DQ_FP16_X512) return head;
   const size_t acc = bwd_acc16_bytes(p->shape), ds = bwd_ds_bytes(p->shape);
   return head + (acc < ds ? acc : ds);
@@ -417,7 +419,7 @@ size_t mxa_bwd_workspace_min_bytes(const mxa_bwd_params* p) {
 
 size_t mxa_bwd_workspace_bytes(const mxa_bwd_params* p) {
   if (!bwd_shape_sizable(p)) return 0;
-  return bwd_head_bytes(p->shape, p->dq_mode) + bwd_ds_bytes(p->shape);
+  return bwd_head_bytes(p->shape, p->dq_mode) + bwd_ds_bytes(p->shape, p->k_key.codes != nullptr);
 }
 
 mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cudaStream_t stream) {
@@ -435,6 +437,11 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   if (p->dq_mode != MXA_DQ_FP32 && p->dq_mode != MXA_DQ_FP16_X512 && p->dq_mode != MXA_DQ_FP16_ROW)
     return MXA_ERR_ARG;
   if (is_cross(s) && p->dq_mode != MXA_DQ_FP32) return MXA_ERR_UNSUPPORTED;
+  const bool strict = p->k_key.codes != nullptr;  // strict dQ (the dQ GEMM path only)
+  if (strict) {
+    if ((st = check_view(p->k_key)) != MXA_OK) return st;
+    if (is_cross(s)) return MXA_ERR_UNSUPPORTED;
+  }
   if (!workspace || ws_bytes < mxa_bwd_workspace_min_bytes(p)) return MXA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return MXA_ERR_ALIGN;
   if (s.T == 0) return MXA_OK;
@@ -448,6 +455,7 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
       !make_code_map(&maps.kt, p->k_tok.codes, ks.T, s.Hkv, s.d) ||
       !make_code_map(&maps.gt, p->g_tok.codes, s.T, s.Hq, s.d))
     return MXA_ERR_CUDA;
+  if (strict && !make_code_map(&maps.kkey, p->k_key.codes, ks.T, s.Hkv, s.d)) return MXA_ERR_CUDA;
   const size_t T = static_cast<size_t>(s.T), Hq = static_cast<size_t>(s.Hq), d = static_cast<size_t>(s.d);
   const size_t pad_elems = Hq * static_cast<size_t>(s.ntiles) * 128;
   const size_t dbytes = 2 * pad_elems * 4;
@@ -464,7 +472,8 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   // dS emitted by the dK/dV kernel and summed by the dQ GEMM, else (FP32: dS
   // formed again by the dQ kernel; FP16: the fused kernel's fp16 accumulator)
   const bool emit = ws_bytes >= mxa_bwd_workspace_bytes(p);
-  if (fp16 && !emit && (rowboost || ws_bytes < bwd_head_bytes(s) + bwd_acc16_bytes(s))) return MXA_ERR_WORKSPACE;
+  if (!emit && (strict || (fp16 && (rowboost || ws_bytes < bwd_head_bytes(s) + bwd_acc16_bytes(s)))))
+    return MXA_ERR_WORKSPACE;
   const size_t acc_bytes = fp16 && !emit ? T * Hq * d * 2 : 0;
   const int maxlen = s.cu_seqlens ? s.max_seqlen : static_cast<int>(s.T / s.num_docs);
 
@@ -532,6 +541,7 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
   a.dq_acc32 = nullptr;
   a.dq_acc16 = acc_bytes ? static_cast<uint16_t*>(acc) : nullptr;
   a.dq_boost = boost;
+  a.kkey_sf = strict ? p->k_key.scales : nullptr;
   a.dk = p->dk;
   a.dv = p->dv;
   a.dq_out = p->dq;

@@ -211,4 +211,27 @@ __device__ __forceinline__ uint32_t quant_ds_block32(const float (&x)[32], int s
   return static_cast<uint32_t>(e + 127);
 }
 
+// Strict dQ operand: the 32 x 32 block one row per lane (x: this lane's 32
+// values, columns 0..31, carrying a 2^shift boost) times f, quantized with
+// one exponent per column -- from the column's max over the 32 lanes by the
+// MX rule, of the values without their boost; an all-zero column keeps the
+// unit scale -- into w (byte c of this lane's row).  Returns the UE8M0 byte
+// of column `lane`.
+__device__ __forceinline__ uint8_t quant_ds_cols32(const float (&x)[32], int shift, float f, int lane,
+                                                   uint32_t (&w)[8]) {
+  uint32_t mine = 127u;
+  float y[4];
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const float v = x[c] * f;
+    const float am = warp_max_abs(v);
+    int e = am == 0.0f ? 0 : mx_exponent_bits(__float_as_uint(am)) - shift;
+    if (e < -127) e = -127;
+    y[c & 3] = v * exp2i_neg(e + shift);
+    if (lane == c) mine = static_cast<uint32_t>(e + 127);
+    if ((c & 3) == 3) w[c >> 2] = pack_e4m3x4(y[0], y[1], y[2], y[3]);
+  }
+  return static_cast<uint8_t>(mine);
+}
+
 }  // namespace mxa

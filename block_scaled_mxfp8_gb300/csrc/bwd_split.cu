@@ -110,7 +110,7 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
 }  // namespace
 
 // ========================================================================= dK, dV
-template <int D>
+template <int D, bool STRICT>
 __global__ void __launch_bounds__(kDkdvThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   using C = DkdvCfg<D>;
@@ -355,6 +355,14 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       tmem_st_wait();
     }
     bool ok = true;
+    // strict dQ: 2^e_k of this thread's key (the K fold of the diagonal pair)
+    float kfold = 1.0f;
+    if constexpr (STRICT) {
+      if (key_valid) {
+        const uint32_t kb = a.kkey_sf[(static_cast<int64_t>(hk) * a.ntiles_k + ktile_base + kt) * 128 + j];
+        kfold = kb ? __uint_as_float(kb << 23) : __uint_as_float(0x00400000u);
+      }
+    }
     for (int u = 0; u < n_work; ++u) {
       const int sa = u % C::kStagesA, sb = u % C::kStagesB;
       const int qi = qi0 + u % nq;
@@ -443,15 +451,23 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           // [32 part, 32 part + 32) -- 16-byte chunks 2 part, 2 part + 1 of
           // the row, placed at chunk ^ (j & 7) (the 128-byte swizzle); its
           // scale byte at 4 part + quad of the pair's 16 (query block major)
-          uint8_t* row = smem + C::kOffDsStage + j * 128;
-          *reinterpret_cast<uint4*>(row + (((2 * part) ^ (j & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4*>(row + (((2 * part + 1) ^ (j & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-          fence_proxy_async_smem();  // the MMA thread's bulk store reads it
-          if (lane == 0) {
-            const int h = hk * grp + u / nq;
-            const int64_t pair = (static_cast<int64_t>(h) * a.ntiles_k + ktile_base + kt) * a.mt + qi;
-            a.ds_sf[pair * 16 + part * 4 + quad] = static_cast<uint8_t>(eb);
+          const int h = hk * grp + u / nq;
+          const int64_t pair = (static_cast<int64_t>(h) * a.ntiles_k + ktile_base + kt) * a.mt + qi;
+          uint32_t we[8];
+          if constexpr (STRICT) {
+            // strict dQ: one scale per query (column c) over the block's 32
+            // keys, after the diagonal pair's K fold; lane c keeps query c's
+            const uint8_t eq = quant_ds_cols32(p, 8, (a.causal && qi == kt) ? kfold : 1.0f, lane, we);
+            a.ds_sf[pair * 512 + lane * 16 + part * 4 + quad] = eq;
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) we[k] = w[k];
+            if (lane == 0) a.ds_sf[pair * 16 + part * 4 + quad] = static_cast<uint8_t>(eb);
           }
+          uint8_t* row = smem + C::kOffDsStage + j * 128;
+          *reinterpret_cast<uint4*>(row + (((2 * part) ^ (j & 7)) << 4)) = make_uint4(we[0], we[1], we[2], we[3]);
+          *reinterpret_cast<uint4*>(row + (((2 * part + 1) ^ (j & 7)) << 4)) = make_uint4(we[4], we[5], we[6], we[7]);
+          fence_proxy_async_smem();  // the MMA thread's bulk store reads it
         }
       }
       tmem_st_wait();
@@ -751,43 +767,48 @@ cudaError_t launch_bwd_split(const BwdArgs& a, const BwdMaps& m, int d, int max_
   const dim3 g2 = a.q_items ? dim3(static_cast<unsigned>(a.ntiles * a.Hq)) : dim3(tiles, a.num_docs, a.Hq);
   cudaError_t e;
   if (d == 128) {
-    e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DkdvCfg<128>::kSmemBytes);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(attn_bwd_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DqCfg<128>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attn_bwd_dkdv_kernel<128><<<g1, kDkdvThreads, DkdvCfg<128>::kSmemBytes, stream>>>(m, a);
+    attn_bwd_dkdv_kernel<128, false><<<g1, kDkdvThreads, DkdvCfg<128>::kSmemBytes, stream>>>(m, a);
     attn_bwd_dq_kernel<128><<<g2, kSplitThreads, DqCfg<128>::kSmemBytes, stream>>>(m, a);
   } else {
-    e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DkdvCfg<64>::kSmemBytes);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(attn_bwd_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DqCfg<64>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attn_bwd_dkdv_kernel<64><<<g1, kDkdvThreads, DkdvCfg<64>::kSmemBytes, stream>>>(m, a);
+    attn_bwd_dkdv_kernel<64, false><<<g1, kDkdvThreads, DkdvCfg<64>::kSmemBytes, stream>>>(m, a);
     attn_bwd_dq_kernel<64><<<g2, kSplitThreads, DqCfg<64>::kSmemBytes, stream>>>(m, a);
   }
   return cudaGetLastError();
 }
 
+namespace {
+
+template <int D, bool STRICT>
+cudaError_t launch_dkdv_t(const BwdArgs& a, const BwdMaps& m, const dim3& g1, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, STRICT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       DkdvCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  attn_bwd_dkdv_kernel<D, STRICT><<<g1, kDkdvThreads, DkdvCfg<D>::kSmemBytes, stream>>>(m, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_bwd_emit(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
   const int tiles = (max_seqlen + 127) / 128;
   const dim3 g1 = a.k_items ? dim3(static_cast<unsigned>(a.ntiles_k * a.Hkv)) : dim3(tiles, a.num_docs, a.Hkv);
+  const bool strict = a.kkey_sf != nullptr;
   cudaError_t e;
-  if (d == 128) {
-    e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DkdvCfg<128>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attn_bwd_dkdv_kernel<128><<<g1, kDkdvThreads, DkdvCfg<128>::kSmemBytes, stream>>>(m, a);
-  } else {
-    e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DkdvCfg<64>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attn_bwd_dkdv_kernel<64><<<g1, kDkdvThreads, DkdvCfg<64>::kSmemBytes, stream>>>(m, a);
-  }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (d == 128) e = strict ? launch_dkdv_t<128, true>(a, m, g1, stream) : launch_dkdv_t<128, false>(a, m, g1, stream);
+  else e = strict ? launch_dkdv_t<64, true>(a, m, g1, stream) : launch_dkdv_t<64, false>(a, m, g1, stream);
+  if (e != cudaSuccess) return e;
   return launch_dq_gemm(a, m, d, max_seqlen, stream);
 }
 

@@ -46,12 +46,13 @@ struct DqGemmCfg {
   // scales (padded so stages stay 1024-byte aligned)
   static constexpr int kOffKt = 16384, kOffKtSf = 16384 + kTileBytes, kOffDsSf = kOffKtSf + kAtomBytes;
   static constexpr int kStageBytes = 16384 + kTileBytes + 1024;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+  static constexpr int kOffSfOne = kStages * kStageBytes;       // a scale-1 atom (strict dQ's diagonal K)
+  static constexpr int kSmemBytes = kOffSfOne + kAtomBytes + 1024;
 };
 
 }  // namespace
 
-template <int D, bool F16>
+template <int D, bool F16, bool STRICT>
 __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 2)
     attn_dq_gemm_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   using C = DqGemmCfg<D>;
@@ -95,6 +96,11 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 2)
     s_abort = 0;
     fence_barrier_init();
   }
+  if constexpr (STRICT) {
+    for (int i = tid; i < kAtomBytes / 16; i += C::kThreads)
+      reinterpret_cast<uint4*>(smem + C::kOffSfOne)[i] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    fence_proxy_async_smem();
+  }
   if (warp == 1) {
     tmem_alloc(&s_tmem, C::kTmemCols);
     tmem_relinquish();
@@ -119,11 +125,15 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 2)
         const int k0 = static_cast<int>(kdoc_start + static_cast<int64_t>(j) * 128);
         const int64_t katom = (static_cast<int64_t>(hk) * a.ntiles_k + ktile_base + j) * kAtomBytes;
         uint8_t* st = smem + s * C::kStageBytes;
-        mbar_arrive_expect_tx(&bar_full[s], 16384 + C::kTileBytes + kAtomBytes + 16);
+        // strict dQ: one scale per (query row, 32 keys) -- a whole atom per
+        // pair -- and the per-key K codes on the diagonal pair
+        const bool kdiag = STRICT && a.causal && j == qt;
+        mbar_arrive_expect_tx(&bar_full[s], 16384 + C::kTileBytes + kAtomBytes + (STRICT ? kAtomBytes : 16));
         bulk_load(st, a.ds_codes + pair * 16384, 16384, &bar_full[s]);  // stored as its swizzled image
-        tma_load_3d(st + C::kOffKt, &maps.kt, &bar_full[s], 0, hk, k0);
+        tma_load_3d(st + C::kOffKt, kdiag ? &maps.kkey : &maps.kt, &bar_full[s], 0, hk, k0);
         bulk_load(st + C::kOffKtSf, a.kt_sf + katom, kAtomBytes, &bar_full[s]);
-        bulk_load(st + C::kOffDsSf, a.ds_sf + pair * 16, 16, &bar_full[s]);
+        if constexpr (STRICT) bulk_load(st + C::kOffDsSf, a.ds_sf + pair * kAtomBytes, kAtomBytes, &bar_full[s]);
+        else bulk_load(st + C::kOffDsSf, a.ds_sf + pair * 16, 16, &bar_full[s]);
         issued = j + 1;
       }
       for (int j = (issued > C::kStages ? issued - C::kStages : 0); j < issued; ++j)
@@ -145,7 +155,8 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 2)
         if (F16 && j > 0 && !(ok = role_wait(&bar_pfree, (j - 1) & 1, abort_flag, a.err, kErrTimeoutMma))) break;
         tc_fence_after();
         const uint32_t tSfA = tmem + C::kSfDS + 4 * s, tSfB = tmem + C::kSfKt + 4 * s;
-        tmem_cp_desc(tSfB, sdesc_adv(dSf0, s * C::kStageBytes));
+        tmem_cp_desc(tSfB, (STRICT && a.causal && j == qt) ? atom_desc(smem + C::kOffSfOne)
+                                                           : sdesc_adv(dSf0, s * C::kStageBytes));
         const uint64_t da = sdesc_adv(dA0, s * C::kStageBytes), db = sdesc_adv(dB0, s * C::kStageBytes);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // 32 keys per step: 32 rows of each operand
@@ -204,7 +215,10 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 2)
     for (int j = 0; j < n_kt; ++j) {
       const int s = j % C::kStages;
       if (!(ok = warp_wait(&bar_full[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutEpilogue))) break;
-      const uint32_t sc = *reinterpret_cast<const uint32_t*>(smem + s * C::kStageBytes + C::kOffDsSf + 4 * quad);
+      // default: the 16 block scales, one word per query block; strict: the
+      // atom's word of this lane's query row (byte = key block)
+      const uint32_t sc = *reinterpret_cast<const uint32_t*>(smem + s * C::kStageBytes + C::kOffDsSf +
+                                                             (STRICT ? lane * 16 + quad * 4 : 4 * quad));
       tmem_st1(lane_base + C::kSfDS + 4 * s + quad, sc);
       tmem_st_wait();
       tc_fence_before();
@@ -266,26 +280,32 @@ __global__ void __launch_bounds__(DqGemmCfg<D>::kThreads, 2)
 
 namespace {
 
-template <int D, bool F16>
+template <int D, bool F16, bool STRICT>
 cudaError_t launch_dq_gemm_t(const BwdArgs& a, const BwdMaps& m, int max_seqlen, cudaStream_t stream) {
   using C = DqGemmCfg<D>;
   const dim3 grid = a.q_items ? dim3(static_cast<unsigned>(a.ntiles * a.Hq))
                               : dim3((max_seqlen + 127) / 128, a.num_docs, a.Hq);
-  cudaError_t e = cudaFuncSetAttribute(attn_dq_gemm_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(attn_dq_gemm_kernel<D, F16, STRICT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_dq_gemm_kernel<D, F16><<<grid, C::kThreads, C::kSmemBytes, stream>>>(m, a);
+  attn_dq_gemm_kernel<D, F16, STRICT><<<grid, C::kThreads, C::kSmemBytes, stream>>>(m, a);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_dq_gemm_d(const BwdArgs& a, const BwdMaps& m, int max_seqlen, cudaStream_t stream) {
+  const bool f16 = a.dq_mode != 0;  // FP16 x 2^9 or the per-row boost
+  if (a.kkey_sf != nullptr)
+    return f16 ? launch_dq_gemm_t<D, true, true>(a, m, max_seqlen, stream)
+               : launch_dq_gemm_t<D, false, true>(a, m, max_seqlen, stream);
+  return f16 ? launch_dq_gemm_t<D, true, false>(a, m, max_seqlen, stream)
+             : launch_dq_gemm_t<D, false, false>(a, m, max_seqlen, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_dq_gemm(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
-  const bool f16 = a.dq_mode != 0;  // FP16 x 2^9 or the per-row boost
-  if (d == 128) return f16 ? launch_dq_gemm_t<128, true>(a, m, max_seqlen, stream)
-                           : launch_dq_gemm_t<128, false>(a, m, max_seqlen, stream);
-  return f16 ? launch_dq_gemm_t<64, true>(a, m, max_seqlen, stream)
-             : launch_dq_gemm_t<64, false>(a, m, max_seqlen, stream);
+  return d == 128 ? launch_dq_gemm_d<128>(a, m, max_seqlen, stream) : launch_dq_gemm_d<64>(a, m, max_seqlen, stream);
 }
 
 }  // namespace mxa

@@ -154,6 +154,13 @@ struct BwdArgs {
   // block).
   uint8_t* ds_codes;
   uint8_t* ds_sf;
+  // strict dQ (null: off): the per-key exponents of K [Hkv, NT, 128] (its
+  // codes through BwdMaps::kkey).  The emitted dS then carries one scale per
+  // (query row, 32 keys) -- a 512-byte atom per pair in the A-scale layout,
+  // byte (q % 32) 16 + (q / 32) 4 + key block -- and on the diagonal pair
+  // each key's dS column is folded with 2^e_k and multiplied with the
+  // per-key K codes (scale 1)
+  const uint8_t* kkey_sf;
   int mt;                // max 128-token query tiles of one document
   int dq_mode;
   int* err;
@@ -220,7 +227,7 @@ struct FwdMaps {
   CUtensorMap q, k, v, vkey;  // vkey: set only when FwdArgs::vkey_sf is
 };
 struct BwdMaps {
-  CUtensorMap q, k, v, g, qt, kt, gt;
+  CUtensorMap q, k, v, g, qt, kt, gt, kkey;  // kkey: set only when BwdArgs::kkey_sf is
 };
 
 cudaError_t launch_quantize_key(const KeyQuantArgs& a, int d, int max_seqlen, cudaStream_t stream);

@@ -89,6 +89,7 @@ class c_bwd_params(ctypes.Structure):
         ("dk", ctypes.c_void_p),
         ("dv", ctypes.c_void_p),
         ("dq_mode", ctypes.c_int),
+        ("k_key", c_qview),
     ]
 
 
@@ -373,17 +374,18 @@ def fwd(q_row: QView, k_row: QView, v_tok: QView, geo: Geometry, causal: bool, s
 
 
 def bwd_params(views: dict, o, lse, dq, dk, dv, geo: Geometry, causal: bool, dq_mode: int = MXA_DQ_FP32,
-               softmax_scale: float = 0.0, kv_geo: Optional[Geometry] = None) -> c_bwd_params:
+               softmax_scale: float = 0.0, kv_geo: Optional[Geometry] = None,
+               k_key: Optional[QView] = None) -> c_bwd_params:
     T, Hq, d = views["q_row"].codes.shape
     Hkv = views["k_row"].codes.shape[1]
     return c_bwd_params(_shape(geo, Hq, Hkv, d, causal, softmax_scale, kv_geo), views["q_row"].c(), views["k_row"].c(),
                         views["v_row"].c(), views["g_row"].c(), views["q_tok"].c(), views["k_tok"].c(),
                         views["g_tok"].c(), o.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                        dv.data_ptr(), int(dq_mode))
+                        dv.data_ptr(), int(dq_mode), k_key.c() if k_key is not None else c_qview(None, None))
 
 
 def bwd(views: dict, o, lse, geo: Geometry, causal: bool, dq_mode: int = MXA_DQ_FP32, softmax_scale: float = 0.0,
-        workspace=None, out=None, stream=None, kv_geo: Optional[Geometry] = None):
+        workspace=None, out=None, stream=None, kv_geo: Optional[Geometry] = None, k_key: Optional[QView] = None):
     """views: dict with q_row, k_row, v_row, g_row, q_tok, k_tok, g_tok QViews
     (k_*, v_* over kv_geo's tokens for cross-attention).
     -> (dQ bf16 [T, Hq, d], dK, dV bf16 [Tk, Hkv, d])."""
@@ -396,7 +398,7 @@ def bwd(views: dict, o, lse, geo: Geometry, causal: bool, dq_mode: int = MXA_DQ_
         dv = torch.empty((Tk, Hkv, d), dtype=torch.bfloat16, device=dev)
     else:
         dq, dk, dv = out
-    p = bwd_params(views, o, lse, dq, dk, dv, geo, causal, dq_mode, softmax_scale, kv_geo)
+    p = bwd_params(views, o, lse, dq, dk, dv, geo, causal, dq_mode, softmax_scale, kv_geo, k_key)
     need = mxa_bwd_workspace_bytes(p)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)

@@ -281,6 +281,17 @@ typedef struct {
   void* dk;                /* out: bf16 [T (T_k for cross-attention), Hkv, d], summed over the query heads of the group */
   void* dv;                /* out: bf16 [T (T_k for cross-attention), Hkv, d] */
   mxa_dq_mode dq_mode;
+  mxa_qview k_key;         /* optional per-key view of K (mxa_quantize_key), self-attention only:
+                              with codes != NULL dQ_i depends on no position after i (FLAMIA
+                              notes sec. 4) -- the dS operand of the dQ product is quantized
+                              with one scale per (query row, 32 keys) instead of per 32 x 32
+                              block, and on each query's diagonal 128-key tile every key's dS
+                              column is folded with its 2^e_k and multiplied with its per-key
+                              codes (scale 1).  With the forward's v_key fold (so that O_i and
+                              LSE_i are strict too), rows i <= p keep dQ_i bit for bit when
+                              anything after p changes, G rows <= p fixed.  Needs the full
+                              mxa_bwd_workspace_bytes(); dK and dV are unchanged (they depend
+                              on later queries by definition).  NULL codes: off. */
 } mxa_bwd_params;
 
 /* Workspace bytes of mxa_bwd's fastest path.
@@ -294,7 +305,10 @@ typedef struct {
  *   E4M3 codes (16 KB) and the 16 UE8M0 block scales per (query head, key
  *   tile, query tile of the same document) pair, with mt = ceil(max_seqlen /
  *   128) query-tile slots per key tile: Hq * NT_k * mt * 16400 bytes, NT_k
- *   the key side's ntiles (B8 H32 L4096: 4.3 GB).
+ *   the key side's ntiles (B8 H32 L4096: 4.3 GB).  With k_key (strict dQ) each pair
+ *   carries a 512-byte scale atom instead of the 16 block scales (one UE8M0 per
+ *   query row and key block, byte (q % 32) 16 + (q / 32) 4 + key block):
+ *   Hq * NT_k * mt * (16384 + 512) bytes.
  *   FP16_ROW mode: after the D and LSE rows, before the lists, the boost
  *   2^beta_i of every query row as fp32 [Hq, T], the key bound V_t + K_t
  *   of every (token, kv head) as int32 [T, Hkv] and per-tile key maxima as

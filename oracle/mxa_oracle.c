@@ -757,6 +757,109 @@ void orc_attn_bwd(const double* Qs, const double* Ks, const double* Vo, const do
     }
 }
 
+/* Causal backward with the per-key fold on the diagonal tile ([FLAMIA] sec. 4:
+ * the K factor of dQ moves into dS, the "K fold", as the V factor of the
+ * forward moves into P).  The same direct backward as orc_attn_bwd, except
+ * that on query i's own 128-token tile of its document (keys
+ * [s + 128 floor((i - s) / 128), i]) O_i takes each key's per-key value row
+ * Vkey_j (the folded forward) and dQ_i takes each key's per-key row Kkey_j;
+ * the tiles before it use Vo and Kt.  D = G . O uses that O.  Inputs as
+ * orc_attn_bwd plus Vkey, Kkey [T, Hkv, d] (decoded per-key views); every
+ * (document, kv head) unit. */
+void orc_attn_bwd_fold(const double* Qs, const double* Ks, const double* Vo, const double* Vr, const double* Gr,
+                       const double* Qt, const double* Kt, const double* Gt, const double* Vkey, const double* Kkey,
+                       int64_t T, int Hq, int Hkv, int d, const int32_t* cu, int ndocs, double alpha, double* dQ,
+                       double* dK, double* dV, double* O, double* LSE, double* D)
+{
+    int nd = num_docs_eff(cu, ndocs);
+    int grp = Hq / Hkv;
+    for (int b = 0; b < nd; ++b) {
+        int64_t s, e;
+        doc_range(cu, ndocs, T, b, &s, &e);
+        int64_t n = e - s;
+        if (n <= 0)
+            continue;
+        for (int hk = 0; hk < Hkv; ++hk) {
+            /* pass 1: rows */
+#pragma omp parallel
+            {
+                double* Srow = (double*)malloc(sizeof(double) * (size_t)n);
+#pragma omp for schedule(dynamic, 8) collapse(2)
+                for (int hh = 0; hh < grp; ++hh)
+                    for (int64_t i = s; i < e; ++i) {
+                        int h = hk * grp + hh;
+                        int64_t diag0 = s + ((i - s) / 128) * 128;
+                        const double* q = Qs + (i * Hq + h) * d;
+                        double m = -INFINITY;
+                        for (int64_t j = s; j <= i; ++j) {
+                            Srow[j - s] = alpha * dot(q, Ks + (j * Hkv + hk) * d, d);
+                            if (Srow[j - s] > m)
+                                m = Srow[j - s];
+                        }
+                        double* o = O + (i * Hq + h) * d;
+                        for (int k = 0; k < d; ++k)
+                            o[k] = 0.0;
+                        double l = 0.0;
+                        for (int64_t j = s; j <= i; ++j) {
+                            double p = exp(Srow[j - s] - m);
+                            l += p;
+                            const double* v = (j >= diag0 ? Vkey : Vo) + (j * Hkv + hk) * d;
+                            for (int k = 0; k < d; ++k)
+                                o[k] += p * v[k];
+                        }
+                        for (int k = 0; k < d; ++k)
+                            o[k] /= l;
+                        double lse = m + log(l);
+                        LSE[(int64_t)h * T + i] = lse;
+                        const double* g = Gr + (i * Hq + h) * d;
+                        double Di = dot(g, o, d);
+                        D[(int64_t)h * T + i] = Di;
+                        double* dq = dQ + (i * Hq + h) * d;
+                        for (int k = 0; k < d; ++k)
+                            dq[k] = 0.0;
+                        for (int64_t j = s; j <= i; ++j) {
+                            double P = exp(Srow[j - s] - lse);
+                            double E = dot(g, Vr + (j * Hkv + hk) * d, d);
+                            double U = P * (E - Di);
+                            const double* kt = (j >= diag0 ? Kkey : Kt) + (j * Hkv + hk) * d;
+                            for (int k = 0; k < d; ++k)
+                                dq[k] += alpha * U * kt[k];
+                        }
+                    }
+                free(Srow);
+            }
+            /* pass 2: key columns, as orc_attn_bwd */
+#pragma omp parallel for schedule(dynamic, 8)
+            for (int64_t j = s; j < e; ++j) {
+                double* dk = dK + (j * Hkv + hk) * d;
+                double* dv = dV + (j * Hkv + hk) * d;
+                for (int k = 0; k < d; ++k) {
+                    dk[k] = 0.0;
+                    dv[k] = 0.0;
+                }
+                const double* kj = Ks + (j * Hkv + hk) * d;
+                const double* vj = Vr + (j * Hkv + hk) * d;
+                for (int hh = 0; hh < grp; ++hh) {
+                    int h = hk * grp + hh;
+                    for (int64_t i = j; i < e; ++i) {
+                        double S = alpha * dot(Qs + (i * Hq + h) * d, kj, d);
+                        double P = exp(S - LSE[(int64_t)h * T + i]);
+                        const double* g = Gr + (i * Hq + h) * d;
+                        double E = dot(g, vj, d);
+                        double U = P * (E - D[(int64_t)h * T + i]);
+                        const double* gt = Gt + (i * Hq + h) * d;
+                        const double* qt = Qt + (i * Hq + h) * d;
+                        for (int k = 0; k < d; ++k) {
+                            dv[k] += P * gt[k];
+                            dk[k] += alpha * U * qt[k];
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
 /* Cross-attention (query and key/value documents of different lengths, no
  * mask): the queries of document b, rows [cu_q[b], cu_q[b+1]) of Q, attend
  * to that document's keys and values, rows [cu_k[b], cu_k[b+1]) of K and V.

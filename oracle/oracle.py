@@ -85,6 +85,7 @@ def _L():
                 "orc_attn_fwd_x": (None, [P, P, P, i64, i64, i32, i32, i32, P, P, i32, f64, P, P]),
                 "orc_attn_bwd_x": (None, [P] * 8 + [i64, i64, i32, i32, i32, P, P, i32, f64] + [P] * 6),
                 "orc_quant_key": (None, [P, i64, i32, i32, P, P]),
+                "orc_attn_bwd_fold": (None, [P] * 10 + [i64, i32, i32, i32, P, i32, f64] + [P] * 6),
                 "orc_attn_fwd_fold": (None, [P, P, P, P, i64, i32, i32, i32, P, i32, f64, P, P]),
                 "orc_dq_row_boost": (None, [P, P, P, i64, i32, i32, i32, P, i32, i32, ctypes.c_float, P]),
                 "orc_num_threads": (i32, []),
@@ -398,6 +399,23 @@ def dq_row_boost(Gr, Vr, Kr, cu_seqlens=None, causal=False, alpha=None):
     _L().orc_dq_row_boost(_p(Gr), _p(Vr), _p(Kr), T, Hq, Hkv, d, _p(cu), nd, int(bool(causal)), float(alpha),
                           _p(beta))
     return beta
+
+
+def attn_bwd_fold(Qs, Ks, Vo, Vr, Gr, Qt, Kt, Gt, Vkey, Kkey, cu_seqlens=None, alpha=None):
+    """Causal backward with the per-key folds on the diagonal tile (FLAMIA
+    sec. 4): see orc_attn_bwd_fold.  Returns a dict with dQ, dK, dV, O, LSE,
+    D."""
+    arrs = [np.ascontiguousarray(a, dtype=np.float64) for a in (Qs, Ks, Vo, Vr, Gr, Qt, Kt, Gt, Vkey, Kkey)]
+    T, Hq, d = arrs[0].shape
+    Hkv = arrs[1].shape[1]
+    if alpha is None:
+        alpha = 1.0 / math.sqrt(d)
+    cu, nd = _cu(cu_seqlens)
+    out = {k: np.full(sh, np.nan) for k, sh in (("dQ", (T, Hq, d)), ("dK", (T, Hkv, d)), ("dV", (T, Hkv, d)),
+                                                  ("O", (T, Hq, d)), ("LSE", (Hq, T)), ("D", (Hq, T)))}
+    _L().orc_attn_bwd_fold(*[_p(a) for a in arrs], T, Hq, Hkv, d, _p(cu), nd, float(alpha),
+                           *[_p(out[k]) for k in ("dQ", "dK", "dV", "O", "LSE", "D")])
+    return out
 
 
 def attn_fwd_x(Q, K, V, cu_q, cu_k, alpha=None):

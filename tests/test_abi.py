@@ -46,7 +46,7 @@ def test_struct_layouts_match_header():
     assert ctypes.sizeof(mxa.c_qview) == 16
     assert ctypes.sizeof(mxa.c_shape) == 88
     assert ctypes.sizeof(mxa.c_fwd_params) == 184  # + v_key
-    assert ctypes.sizeof(mxa.c_bwd_params) == 248
+    assert ctypes.sizeof(mxa.c_bwd_params) == 264  # + k_key
 
 
 def test_scale_tile_helpers(lib):
@@ -231,3 +231,18 @@ def test_key_view_and_fold_reject_bad_arguments_without_launch(lib):
     p = _fwd()
     p.v_key = mxa.c_qview(256, 8)
     assert L.mxa_fwd(ctypes.byref(p), None) == mxa.MXA_ERR_ALIGN
+
+
+def test_strict_backward_workspace_and_refusals(lib):
+    L = lib
+    sh = mxa.c_shape(256, 2, 2, 128, None, 1, 256, 2, 1, 0.0)
+    bp = mxa.c_bwd_params(sh, *[_qv()] * 7, 256, 256, 256, 256, 256, 0)
+    plain = L.mxa_bwd_workspace_bytes(ctypes.byref(bp))
+    bp.k_key = _qv()
+    # one 512-byte scale atom per pair instead of 16 block scales; min == full
+    full = L.mxa_bwd_workspace_bytes(ctypes.byref(bp))
+    assert full == plain + 2 * 2 * 2 * (512 - 16)
+    assert L.mxa_bwd_workspace_min_bytes(ctypes.byref(bp)) == full
+    assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), full - 1, None) == mxa.MXA_ERR_WORKSPACE
+    bp.k_key = mxa.c_qview(256, 8)
+    assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), 1 << 30, None) == mxa.MXA_ERR_ALIGN

@@ -109,3 +109,70 @@ def test_fold_forward_prefix_is_bit_identical_under_in_block_changes():
         assert torch.equal(o0[:blk], plain[0][:blk]), p
         moved += int(not torch.equal(o0[blk: p + 1], plain[0][blk: p + 1]))
     assert moved > 0, "the perturbations never reached the unfolded prefix: the check would not discriminate"
+
+
+# ---------------------------------------------------------------- strict dQ
+
+BWD_CASES = [
+    inp.make_custom("d128_ragged_gqa_causal", lengths=[1, 129, 300, 64, 7, 515], Hq=4, Hkv=2, d=128, causal=True,
+                    seed=45),
+    inp.make_custom("d64_ragged", lengths=[256, 100, 383], Hq=2, Hkv=1, d=64, causal=True, seed=46),
+]
+
+
+def _strict_step(w, t, strict=True):
+    """Folded forward, then the backward with (strict) or without the K fold
+    and per-query dS scales.  -> (dq, dk, dv)."""
+    from block_scaled_mxfp8_gb300 import mxa
+
+    geo, gv = gpu_views(w, t)
+    vkey = mxa.quantize_key(t["v"].cuda().contiguous(), geo)
+    kkey = mxa.quantize_key(t["k"].cuda().contiguous(), geo) if strict else None
+    o, lse = mxa.fwd(gv["q"][0], gv["k"][0], gv["v"][1], geo, True, v_key=vkey)
+    views = {"q_row": gv["q"][0], "k_row": gv["k"][0], "v_row": gv["v"][0], "g_row": gv["do"][0],
+             "q_tok": gv["q"][1], "k_tok": gv["k"][1], "g_tok": gv["do"][1]}
+    out = mxa.bwd(views, o, lse, geo, True, k_key=kkey)
+    torch.cuda.synchronize()
+    mxa.check_error()
+    return out
+
+
+@pytest.mark.parametrize("w", BWD_CASES, ids=[c.name for c in BWD_CASES])
+def test_strict_backward_matches_oracle(w):
+    t = inp.tensors(w, with_grad=True)
+    dq, dk, dv = _strict_step(w, t)
+    _, d = oracle_views(w, t)
+    vk = orc.dequant_key(*orc.quant_key(t["v"]))
+    kk = orc.dequant_key(*orc.quant_key(t["k"]))
+    r = orc.attn_bwd_fold(d["q"]["row"], d["k"]["row"], d["v"]["tok"], d["v"]["row"], d["do"]["row"],
+                          d["q"]["tok"], d["k"]["tok"], d["do"]["tok"], vk, kk, w.cu_seqlens.numpy(),
+                          1.0 / math.sqrt(w.d))
+    for name, got, ref in (("dV", dv, r["dV"]), ("dK", dk, r["dK"]), ("dQ", dq, r["dQ"])):
+        print(w.name, name, metrics(to_np(got), ref))
+        assert_close(name, to_np(got), ref)
+
+
+def test_strict_dq_prefix_is_bit_identical_under_in_block_changes():
+    w = inp.make_custom("strict_prefix", lengths=[600, 333], Hq=4, Hkv=2, d=128, causal=True, seed=47)
+    t = inp.tensors(w, with_grad=True)
+    base = _strict_step(w, t)
+    again = _strict_step(w, t)
+    assert torch.equal(base[0], again[0]), "the strict backward must be deterministic"
+    plain = _strict_step(w, t, strict=False)
+    rng = np.random.default_rng(48)
+    moved = 0
+    for p in (35, 140, 255, 300, 517):
+        tp = {k: x.clone() for k, x in t.items()}
+        gain = float(rng.choice([-300.0, 64.0, 1e-3]))
+        for k in ("q", "k", "v", "do"):  # the incoming gradient of rows <= p stays fixed
+            tp[k][p + 1:600] = (tp[k][p + 1:600].float() * gain).to(torch.bfloat16)
+        dq, _, _ = _strict_step(w, tp)
+        assert torch.equal(dq[: p + 1], base[0][: p + 1]), p
+        assert torch.equal(dq[600:], base[0][600:])
+        # control: with the folded forward but block-scaled dS and the token
+        # view of K, rows of p's block before p may move, earlier blocks not
+        dq0, _, _ = _strict_step(w, tp, strict=False)
+        blk = (p // 32) * 32
+        assert torch.equal(dq0[:blk], plain[0][:blk]), p
+        moved += int(not torch.equal(dq0[blk: p + 1], plain[0][blk: p + 1]))
+    assert moved > 0, "the perturbations never reached the unfolded prefix: the check would not discriminate"

@@ -111,3 +111,40 @@ def test_fold_rows_ignore_later_keys_of_their_block():
     a, b = run(x, False), run(x2, False)
     assert not np.array_equal(a[128: p + 1], b[128: p + 1])
     assert np.array_equal(a[:128], b[:128])
+
+
+def test_backward_fold_with_equal_views_is_the_causal_backward():
+    rng = np.random.default_rng(7)
+    lens = [260, 40, 130]
+    T = sum(lens)
+    cu = np.array(np.concatenate([[0], np.cumsum(lens)]), np.int32)
+    Q, G = rng.standard_normal((T, 4, 32)), rng.standard_normal((T, 4, 32))
+    K, V = rng.standard_normal((T, 2, 32)), rng.standard_normal((T, 2, 32))
+    a = orc.attn_bwd_fold(Q, K, V, V, G, Q, K, G, V, K, cu)
+    b = orc.attn_bwd(Q, K, V, V, G, Q, K, G, cu, True)
+    for k in ("dQ", "dK", "dV", "O", "LSE", "D"):
+        assert np.abs(a[k] - b[k]).max() < 1e-10, k
+
+
+def test_backward_fold_uses_the_key_views_exactly_on_the_diagonal_tile():
+    # dQ_i = alpha sum_j U_ij Khat_j with Khat_j = Kkey_j on i's own 128-token
+    # tile and Kt_j before it; O_i takes Vkey the same way, and D = G . O
+    rng = np.random.default_rng(8)
+    T, d = 300, 32
+    Q, K, G = (rng.standard_normal((T, 1, d)) for _ in range(3))
+    Vt, Vk, Vr, Kt, Kk = (rng.standard_normal((T, 1, d)) for _ in range(5))
+    r = orc.attn_bwd_fold(Q, K, Vt, Vr, G, Q, Kt, G, Vk, Kk, None)
+    alpha = 1.0 / math.sqrt(d)
+    for i in (0, 5, 127, 128, 200, 255, 256, 299):
+        s = alpha * (K[: i + 1, 0] @ Q[i, 0])
+        p = np.exp(s - s.max())
+        P = p / p.sum()
+        t0 = (i // 128) * 128
+        V = np.concatenate([Vt[:t0, 0], Vk[t0: i + 1, 0]])
+        O = P @ V
+        Di = G[i, 0] @ O
+        U = P * (Vr[: i + 1, 0] @ G[i, 0] - Di)
+        Kh = np.concatenate([Kt[:t0, 0], Kk[t0: i + 1, 0]])
+        assert np.abs(r["O"][i, 0] - O).max() < 1e-12
+        assert abs(r["D"][0, i] - Di) < 1e-12
+        assert np.abs(r["dQ"][i, 0] - alpha * U @ Kh).max() < 1e-12
