@@ -256,13 +256,16 @@ def run_gpu(args):
     dv = torch.empty((Tk, Hkv, d), dtype=torch.bfloat16, device=dev)
     views = {"q_row": qv["q"][0], "k_row": qv["k"][0], "v_row": qv["v"][0], "g_row": qv["do"][0],
              "q_tok": qv["q"][1], "k_tok": qv["k"][1], "g_tok": qv["do"][1]}
-    bp = mxa.bwd_params(views, o, lse, dq, dk, dv, geo, w.causal, args.dq_mode, kv_geo=kv_geo)
-    fws = torch.empty(max(1, mxa.mxa_fwd_workspace_bytes(mxa.c_fwd_params(bp.shape))), dtype=torch.uint8, device=dev)
+    bp0 = mxa.bwd_params(views, o, lse, dq, dk, dv, geo, w.causal, args.dq_mode, kv_geo=kv_geo)
+    fws = torch.empty(max(1, mxa.mxa_fwd_workspace_bytes(mxa.c_fwd_params(bp0.shape))), dtype=torch.uint8, device=dev)
     # strict causal forward: the per-key view of V, folded in on the diagonal tile
     if args.fold and (cross or not w.causal):
         raise SystemExit("--fold applies to causal self-attention workloads")
-    vkey = (mxa.QView(torch.empty((T, Hkv, d), dtype=torch.uint8, device=dev),
-                      torch.empty((Hkv, geo.ntiles, 128), dtype=torch.uint8, device=dev)) if args.fold else None)
+    mk_key = lambda: mxa.QView(torch.empty((T, Hkv, d), dtype=torch.uint8, device=dev),
+                               torch.empty((Hkv, geo.ntiles, 128), dtype=torch.uint8, device=dev))
+    vkey = mk_key() if args.fold else None
+    kkey = mk_key() if args.fold else None  # strict dQ: per-key view of K
+    bp = mxa.bwd_params(views, o, lse, dq, dk, dv, geo, w.causal, args.dq_mode, kv_geo=kv_geo, k_key=kkey)
     ws = torch.empty(mxa.mxa_bwd_workspace_bytes(bp), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)
@@ -276,13 +279,14 @@ def run_gpu(args):
             mxa.quantize(src[k], gk, out=qv[k])
         if vkey is not None:
             mxa.quantize_key(src["v"], geo, out=vkey)
+            mxa.quantize_key(src["k"], geo, out=kkey)
         if e: e[1].record(stream)
         mxa.fwd(qv["q"][0], qv["k"][0], qv["v"][1], geo, w.causal, out=(o_, lse_), workspace=fws, kv_geo=kv_geo,
                 v_key=vkey)
         if e: e[2].record(stream)
         mxa.quantize(src["do"], geo, out=qv["do"])
         mxa.bwd(views, o_, lse_, geo, w.causal, dq_mode=args.dq_mode, workspace=ws, out=(dq_, dk_, dv_),
-                kv_geo=kv_geo)
+                kv_geo=kv_geo, k_key=kkey)
         if e:
             e[3].record(stream)
             rec.append(e)
@@ -321,7 +325,8 @@ def run_gpu(args):
     for _ in range(max(3, min(args.steps, 10))):
         a_, b_ = ev(), ev()
         a_.record(stream)
-        mxa.bwd(views, o, lse, geo, w.causal, dq_mode=args.dq_mode, workspace=ws, out=(dq, dk, dv), kv_geo=kv_geo)
+        mxa.bwd(views, o, lse, geo, w.causal, dq_mode=args.dq_mode, workspace=ws, out=(dq, dk, dv), kv_geo=kv_geo,
+                k_key=kkey)
         b_.record(stream)
         bw_ev.append((a_, b_))
     torch.cuda.synchronize()
@@ -458,7 +463,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "mxfp8 (e4m3 codes, ue8m0 scales, fp32 accumulate)", "data": "synthetic",
         "config": {"workload": ("%s: B%d H%d L%d d%d %s, fwd+bwd, dQ %s" % (
-            w.name, B, Hq, L, d, "causal" + (" strict (per-key V fold)" if args.fold else "") if w.causal
+            w.name, B, Hq, L, d, "causal" + (" strict (per-key folds)" if args.fold else "") if w.causal
             else "non-causal", DQ_MODE_NAMES[args.dq_mode].lower()))
             if not cross else ("%s: B%d Lq%d x jagged Lk U[1,%d] (T_k %d) H%d d%d, fwd+bwd, dQ fp32" % (
                 w.name, B, L, max(w.lengths_k), Tk, Hq, d)),
@@ -543,7 +548,8 @@ def main():
                     help="0 = fp32 dQ accumulation, 1 = fp16 x 2^9, 2 = fp16 with a per-row boost")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fold", action="store_true",
-                    help="strict causal forward: per-key V scales folded into P on the diagonal tile")
+                    help="strict causal attention: per-key V and K scales folded on the diagonal tile, "
+                         "per-query dS scales for dQ")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling only)")
     args = ap.parse_args()
     if args.warmup < 3:
