@@ -15,8 +15,16 @@
  *     product) (FLAMIA notes sec. 5 "概率上限由两个参数共同决定"); dS quantised
  *     in 32 x 32 blocks from the block max-abs, taken in the register layout
  *     without a transpose (FA4 write-up "Квантование dS без транспонирования").
- *   - dQ accumulated in FP32 or in FP16 with a 2^9 boost (FA4 write-up, same
- *     section).
+ *   - dQ accumulated in FP32, in FP16 with a 2^9 boost (FA4 write-up, same
+ *     section) or in FP16 with a per-row boost from the row's own bound
+ *     (FLAMIA notes sec. 4, the strict accumulator scale).
+ *   - Strict causal mode (FLAMIA notes sec. 4, moving the scale across the
+ *     boundary): per-key views of V and K folded into P and dS on each
+ *     query's diagonal tile, and per-query dS scales for the dQ product, so
+ *     that no output of a row depends on a later position.
+ *   - Cross-attention with separate key/value documents, cost-sorted tile
+ *     work lists for packed documents (FLAMIA notes, Algorithm 2) and a fused
+ *     RMSNorm + quantize producer (FA4 write-up).
  *   - Packed documents through cu_seqlens; scale groups never cross a
  *     document and only the scale tensors are padded ("Jagged-модуль без
  *     gather"; FLAMIA notes sec. 6).
