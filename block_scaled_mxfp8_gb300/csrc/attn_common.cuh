@@ -216,22 +216,37 @@ __device__ __forceinline__ uint32_t quant_ds_block32(const float (&x)[32], int s
 // one exponent per column -- from the column's max over the 32 lanes by the
 // MX rule, of the values without their boost; an all-zero column keeps the
 // unit scale -- into w (byte c of this lane's row).  Returns the UE8M0 byte
-// of column `lane`.
+// of column `lane`.  The column maxima come from a transpose-reduce: at the
+// step of distance o every lane keeps the half of its columns that matches
+// bit o of its lane and takes the partner's maxima of that half, so after
+// five steps lane c holds column c's max (31 shuffles); each lane then forms
+// one exponent, and the 32 scale factors go back by shuffles.
 __device__ __forceinline__ uint8_t quant_ds_cols32(const float (&x)[32], int shift, float f, int lane,
                                                    uint32_t (&w)[8]) {
-  uint32_t mine = 127u;
-  float y[4];
+  float m[32];
 #pragma unroll
-  for (int c = 0; c < 32; ++c) {
-    const float v = x[c] * f;
-    const float am = warp_max_abs(v);
-    int e = am == 0.0f ? 0 : mx_exponent_bits(__float_as_uint(am)) - shift;
-    if (e < -127) e = -127;
-    y[c & 3] = v * exp2i_neg(e + shift);
-    if (lane == c) mine = static_cast<uint32_t>(e + 127);
-    if ((c & 3) == 3) w[c >> 2] = pack_e4m3x4(y[0], y[1], y[2], y[3]);
+  for (int c = 0; c < 32; ++c) m[c] = fabsf(x[c] * f);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool hi = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = hi ? m[i] : m[i + o];
+      const float keep = hi ? m[i + o] : m[i];
+      m[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+    }
   }
-  return static_cast<uint8_t>(mine);
+  // m[0] is the max of column `lane`
+  int e = m[0] == 0.0f ? 0 : mx_exponent_bits(__float_as_uint(m[0])) - shift;
+  if (e < -127) e = -127;
+  const float sc = exp2i_neg(e + shift);
+#pragma unroll
+  for (int c = 0; c < 32; c += 4) {
+    const float s0 = __shfl_sync(0xffffffffu, sc, c), s1 = __shfl_sync(0xffffffffu, sc, c + 1);
+    const float s2 = __shfl_sync(0xffffffffu, sc, c + 2), s3 = __shfl_sync(0xffffffffu, sc, c + 3);
+    w[c >> 2] = pack_e4m3x4(x[c] * f * s0, x[c + 1] * f * s1, x[c + 2] * f * s2, x[c + 3] * f * s3);
+  }
+  return static_cast<uint8_t>(e + 127);
 }
 
 }  // namespace mxa
