@@ -48,6 +48,32 @@ GB300_SMS = 152
 DQ_MODE_NAMES = {0: "FP32", 1: "FP16x2^9", 2: "FP16 per-row boost"}
 
 
+def bind_gpu_local_cpus(dev_index):
+    """Run this process on the CPUs the GPU's PCI function lists as local, so
+    that the pinned host buffers it fills (first touch) sit in the memory
+    attached to that GPU's host socket.  Returns the CPU list as written in
+    sysfs, or None when the topology is not available (the binding is then
+    left as it was)."""
+    import torch
+
+    try:
+        pr = torch.cuda.get_device_properties(dev_index)
+        bus = "%04x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        with open("/sys/bus/pci/devices/%s/local_cpulist" % bus) as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            lo, _, hi = part.partition("-")
+            cpus.update(range(int(lo), int(hi or lo) + 1))
+        cpus &= os.sched_getaffinity(0)
+        if not cpus:
+            return None
+        os.sched_setaffinity(0, cpus)
+        return spec
+    except (AttributeError, OSError, RuntimeError, ValueError):
+        return None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -123,7 +149,7 @@ class ClockSampler:
 
 # dram__bytes_read.sum + dram__bytes_write.sum of attn_bwd_dkdv_kernel and
 # attn_dq_gemm_kernel at B2 H32 L4096 d128 (one ncu --set full capture)
-BWD_DRAM_BYTES_B2 = (0.267132 + 1.156867 + 1.114714 + 0.062789) * 1e9
+BWD_DRAM_BYTES_B2 = (0.267507 + 1.156908 + 1.114415 + 0.062640) * 1e9
 
 
 def flops(B, H, L, d, causal, lengths=None, lengths_k=None):
@@ -398,6 +424,7 @@ def run_gpu(args):
                                        "bwd": round(bwd_pf * 1e3 / micro_tflops, 4)}}
 
     # e2e through the C ABI with host buffers: H2D of q, k, v, dO and D2H of o, dq, dk, dv inside the timed region
+    host_cpus = bind_gpu_local_cpus(local)  # pinned buffers in the memory next to this GPU
     host_in = {k: v.pin_memory() for k, v in t.items()}
     host_out = {k: torch.empty(s, dtype=torch.bfloat16).pin_memory()
                 for k, s in (("o", o.shape), ("dq", dq.shape), ("dk", dk.shape), ("dv", dv.shape))}
@@ -456,7 +483,8 @@ def run_gpu(args):
     n_e2e = max(3, min(args.steps, 10))
     ms_e2e = e2e_run(n_e2e) / n_e2e
     e2e = {"value": round(world * step_flop / (ms_e2e * 1e-3) / 1e15, 4), "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3)}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3),
+           "host_cpus": host_cpus}
 
     out = {
         "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
