@@ -1,6 +1,10 @@
 // bwd.cu -- MXFP8 block-scaled attention backward (tcgen05, TMEM, TMA).
 //
-// Three launches (FLAMIA notes sec. 2 and Algorithm 1, steps 09-16):
+// The D prep and the key-bound passes of every backward call, and the fused
+// backward of the FP16 x 2^9 dQ mode when the workspace cannot hold the
+// emitted dS (the other modes and workspaces run the dK/dV kernel and a dQ
+// kernel of their own).  The fused path is three launches (FLAMIA notes
+// sec. 2 and Algorithm 1, steps 09-16):
 //   bwd_prep_kernel   : D_i = sum_c G_ic O_ic with G from its ROW view (the
 //                       same G representation the dP product uses) and O the
 //                       forward's bf16 output.
@@ -19,9 +23,10 @@
 //                         dK  += dS^T Q           (Q TOK view)
 //                         dQ_i = dS K             (K TOK view; the dS^T codes in
 //                                shared memory read as an MN-major operand)
-//                       dQ_i is added to a global accumulator in fp32, or in
-//                       fp16 after a 2^9 boost.
-//   dq_convert_kernel : dQ = acc (fp32) or acc * 2^-9 (fp16) -> bf16.
+//                       dQ_i is added to a global fp16 accumulator after a
+//                       2^9 boost (the kernel's fp32 branch is not reached
+//                       from the library's entry points).
+//   dq_convert_kernel : dQ = acc * 2^-9 (fp16) -> bf16.
 //
 // TMEM columns (512): X [0,128) holds S^T, then dP^T, then the dQ tile;
 // dV [128,256), dK [256,384); P^T codes [384,416), dS^T codes [416,448);

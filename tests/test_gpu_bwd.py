@@ -90,3 +90,35 @@ def test_bwd_min_workspace_forms_ds_again(w):
                      1.0 / math.sqrt(w.d))
     assert_close("dQ (dS formed again)", to_np(out[0]), r["dQ"])
     assert torch.equal(out[1], full[1]) and torch.equal(out[2], full[2])
+
+
+def test_fp16_mode_small_workspace_takes_the_fused_kernel():
+    """FP16 x 2^9 mode with a workspace that holds the fp16 dQ accumulator but
+    not the emitted dS: the fused backward kernel (atomics into the fp16
+    accumulator, order varies) -- same bar against the oracle; dK and dV are
+    the same computation as with the full workspace, within the bar."""
+    from block_scaled_mxfp8_gb300 import mxa
+
+    w = inp.make_custom("d128_ragged_gqa_causal", lengths=[300, 77, 512], Hq=4, Hkv=2, d=128, causal=True,
+                        seed=36)
+    t = inp.tensors(w, with_grad=True)
+    geo, gv = gpu_views(w, t)
+    o, lse = mxa.fwd(gv["q"][0], gv["k"][0], gv["v"][1], geo, w.causal)
+    views = {"q_row": gv["q"][0], "k_row": gv["k"][0], "v_row": gv["v"][0], "g_row": gv["do"][0],
+             "q_tok": gv["q"][1], "k_tok": gv["k"][1], "g_tok": gv["do"][1]}
+    T, Hq, d = views["q_row"].codes.shape
+    Hkv = views["k_row"].codes.shape[1]
+    out = tuple(torch.empty((T, H, d), dtype=torch.bfloat16, device="cuda") for H in (Hq, Hkv, Hkv))
+    p = mxa.bwd_params(views, o, lse, *out, geo, w.causal, mxa.MXA_DQ_FP16_X512)
+    need_min, need = mxa.mxa_bwd_workspace_min_bytes(p), mxa.mxa_bwd_workspace_bytes(p)
+    assert 0 < need_min < need
+    ws = torch.empty(need_min, dtype=torch.uint8, device="cuda")
+    assert mxa.mxa_bwd(p, ws, need_min) == mxa.MXA_OK
+    torch.cuda.synchronize()
+    mxa.check_error()
+    _, dd = oracle_views(w, t)
+    r = orc.attn_bwd(dd["q"]["row"], dd["k"]["row"], dd["v"]["tok"], dd["v"]["row"], dd["do"]["row"],
+                     dd["q"]["tok"], dd["k"]["tok"], dd["do"]["tok"], w.cu_seqlens.numpy(), w.causal,
+                     1.0 / math.sqrt(w.d))
+    for name, got, ref in (("dQ", out[0], r["dQ"]), ("dK", out[1], r["dK"]), ("dV", out[2], r["dV"])):
+        assert_close(name + " (fused FP16 path)", to_np(got), ref)
