@@ -1,0 +1,52 @@
+"""Host logic of bench.py that needs no GPU: binding the process to the CPUs
+local to the GPU before the end-to-end loop pins its host buffers."""
+import io
+import os
+import sys
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+class _Props:
+    pci_domain_id = 0
+    pci_bus_id = 0x1B
+    pci_device_id = 0
+
+
+def test_binds_to_the_listed_cpus_it_may_run_on(monkeypatch):
+    seen = {}
+    allowed = set(os.sched_getaffinity(0))
+    listed = sorted(allowed)[:3]
+    spec = ",".join(str(c) for c in listed) + ",%d-%d" % (10000, 10002)  # CPUs this process may not use
+    real_open = open
+
+    def fake_open(path, *a, **k):
+        if str(path).startswith("/sys/bus/pci/devices/"):
+            seen["path"] = path
+            return io.StringIO(spec + "\n")
+        return real_open(path, *a, **k)
+
+    monkeypatch.setattr(torch.cuda, "get_device_properties", lambda i: _Props())
+    monkeypatch.setattr("builtins.open", fake_open)
+    monkeypatch.setattr(os, "sched_setaffinity", lambda pid, cpus: seen.setdefault("cpus", sorted(cpus)))
+    assert bench.bind_gpu_local_cpus(0) == spec
+    assert seen["path"] == "/sys/bus/pci/devices/0000:1b:00.0/local_cpulist"
+    assert seen["cpus"] == listed
+
+
+def test_leaves_the_binding_alone_without_topology(monkeypatch):
+    called = []
+    monkeypatch.setattr(os, "sched_setaffinity", lambda pid, cpus: called.append(cpus))
+    # no GPU here: the device query raises, nothing is bound
+    if not torch.cuda.is_available():
+        assert bench.bind_gpu_local_cpus(0) is None
+    monkeypatch.setattr(torch.cuda, "get_device_properties", lambda i: _Props())
+    monkeypatch.setattr("builtins.open", lambda *a, **k: (_ for _ in ()).throw(OSError("no sysfs")))
+    assert bench.bind_gpu_local_cpus(0) is None
+    assert called == []
