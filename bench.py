@@ -292,6 +292,12 @@ def run_gpu(args):
     vkey = mk_key() if args.fold else None
     kkey = mk_key() if args.fold else None  # strict dQ: per-key view of K
     bp = mxa.bwd_params(views, o, lse, dq, dk, dv, geo, w.causal, args.dq_mode, kv_geo=kv_geo, k_key=kkey)
+    # this library's kernels per step: 4 quantizers (+2 per-key views), the
+    # forward (+ its tile list), the backward's prep, dK/dV and dQ kernels
+    # (+ two tile lists, + the two key-bound passes of the per-row FP16 mode)
+    lists = fws.numel() > 1
+    launches_per_step = (4 + (2 if args.fold else 0) + 1 + (1 if lists else 0) + 3 + (2 if lists else 0) +
+                         (2 if args.dq_mode == 2 else 0))
     ws = torch.empty(mxa.mxa_bwd_workspace_bytes(bp), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)
@@ -506,7 +512,7 @@ def run_gpu(args):
         "roofline": roofline,
         "rmsnorm_quantize": rms,
         "e2e": e2e,
-        "gpu_launches": 8 * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

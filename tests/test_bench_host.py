@@ -50,3 +50,23 @@ def test_leaves_the_binding_alone_without_topology(monkeypatch):
     monkeypatch.setattr("builtins.open", lambda *a, **k: (_ for _ in ()).throw(OSError("no sysfs")))
     assert bench.bind_gpu_local_cpus(0) is None
     assert called == []
+
+
+def test_bench_names_resolve():
+    """Every global name a function of bench.py reads exists in the module or
+    the builtins.  Most of bench.py runs on a GPU only, so this catches a
+    missing import or a misspelt helper on the CPU first."""
+    import builtins
+    import symtable
+
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    known = set(dir(bench)) | set(dir(builtins))
+
+    def unresolved(t):
+        bad = [(t.get_name(), s.get_name()) for s in t.get_symbols()
+               if s.is_global() and s.is_referenced() and not s.is_assigned() and s.get_name() not in known]
+        for ch in t.get_children():
+            bad += unresolved(ch)
+        return bad
+
+    assert unresolved(symtable.symtable(src, "bench.py", "exec")) == []
