@@ -31,7 +31,6 @@ template <int D>
 struct QCfg {
   static constexpr int TPR = D / 16;            // threads per token row (16 channels each)
   static constexpr int kThreads = 32 * TPR;     // 32 rows
-  static constexpr int kRowsPerWarp = 32 / TPR;
   static constexpr int kWarps = kThreads / 32;
 };
 
