@@ -27,6 +27,12 @@
  *     O = P V, LSE = m + ln l ([FLAMIA] sec. 2).
  *   - Backward: dV = P^T G, E = G V^T, D = G.O, U = P (E - D),
  *     dQ = alpha U K, dK = alpha U^T Q ([FLAMIA] sec. 2).
+ *   - Algorithm 1 ([FLAMIA] sec. 5): the same direct attention with the
+ *     roundings its steps name (orc_attn_fwd_alg1, orc_attn_bwd_alg1).
+ *
+ * Unpinned: none.  orc_dq_row_boost states a reading (the bound a library
+ * documents for its per-row FP16 dQ boost; the pages give only the shape of
+ * the choice), pinned by checking that the bound holds.
  *
  * Build: gcc -O2 -std=c11 -fopenmp -ffp-contract=off -fPIC -shared.
  */
@@ -995,8 +1001,10 @@ static int cl2_maxabs(const double* x, int d)
  * sums boosted by a power of two, the strict option taking each row's own G
  * norm with the maxima of V and K over the visible keys only).  The pages
  * give the shape of the choice, b_i = 2^floor(log2(h / a_i)) for a bound a_i
- * of the row's magnitude and a target h; this restates the bound the library
- * documents for its MXA_DQ_FP16_ROW mode:
+ * of the row's magnitude and a target h.  READING, not a page value: this
+ * restates the bound the library documents for its MXA_DQ_FP16_ROW mode, so
+ * comparing the library's exponents with these compares it with its own
+ * stated specification; the pins only check that the bound holds:
  *   a_i = 2^(4 + cl2(alpha) + log2(d) + s(n_i) + g_i + V_i + K_i), h = 2^15,
  *   g_i = cl2(max_c |G_ic|), V_i = max_{j visible} cl2(max_c |V_jc|),
  *   K_i = max_{j visible} cl2(max_c |K_jc|), n_i = visible keys,
@@ -1046,6 +1054,395 @@ void orc_dq_row_boost(const double* Gr, const double* Vr, const double* Kr, int6
         }
         free(ve);
         free(ke);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Algorithm 1: the low-precision forward and the matching backward recompute */
+/* ------------------------------------------------------------------------ */
+
+/* [FLAMIA] sec. 5, Algorithm 1 ("低精度前向与一致的反向重算"), with the
+ * roundings its steps name.  Each can be switched off, so that the result
+ * falls back to the direct fp64 attention above:
+ *   ORC_RND_P  - step 07: the forward's weights are quantized, E4M3(2^c p)
+ *                with c = 4 and the constant scale 2^-4 ("概率上限由两个参数
+ *                共同决定": (c, tau) = (4, 4)); O is normalised by the sum of
+ *                the quantized weights;
+ *   ORC_RND_O  - step 08: O is saved in bf16 (the D of step 09 reads it);
+ *   ORC_RND_P8 - step 15: dV's probability operand is E4M3(2^8 P) 2^-8
+ *                (the 2^8 boost of the backward, same passage);
+ *   ORC_RND_DS - step 14: U = P (E - D) is quantized per 32 x 32 block of
+ *                the tile by the MX rule ([FA4] "Квантование dS без
+ *                транспонирования": one exponent per 32 x 32 block, both axes
+ *                counted from the document start, before alpha).
+ * Reading of step 07's reference maximum: the weights are p = 2^(x - mu) in
+ * base-2 coordinates x = S log2(e), with mu = ceil(max_j x_j), an integer.
+ * The pages let an online softmax keep an older reference up to tau behind
+ * the true maximum; any integer reference mu' <= mu only multiplies every p by
+ * the power of two 2^(mu - mu'), which E4M3 rounding commutes with in its
+ * normal range ([FLAMIA] sec. 4, scale doubling), so one direct definition
+ * stands for every lazy schedule except for weights below 2^-10 (E4M3
+ * subnormals after the 2^4 boost). */
+#define ORC_RND_P 1
+#define ORC_RND_O 2
+#define ORC_RND_P8 4
+#define ORC_RND_DS 8
+
+#define ORC_LOG2E 1.4426950408889634074
+
+/* Nearest E4M3 value to y as fp64 (ties to the even code, saturating to 448,
+ * sign kept): the value orc_e4m3_decode(orc_e4m3_encode(y)) by a binary search
+ * over the ascending finite codes 0x00..0x7E instead of a scan. */
+double orc_e4m3_round(double y)
+{
+    if (isnan(y))
+        return y;
+    double a = fabs(y);
+    if (a >= 448.0)
+        return copysign(448.0, y);
+    int lo = 0, hi = 0x7E; /* invariant: decode(lo) <= a < decode(hi + 1) */
+    while (lo < hi) {
+        int mid = (lo + hi + 1) / 2;
+        if (orc_e4m3_decode((uint8_t)mid) <= a)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    double v0 = orc_e4m3_decode((uint8_t)lo), v1 = orc_e4m3_decode((uint8_t)(lo + 1));
+    double r;
+    if (a - v0 < v1 - a)
+        r = v0;
+    else if (a - v0 > v1 - a)
+        r = v1;
+    else
+        r = (lo & 1) ? v1 : v0;
+    return copysign(r, y);
+}
+
+void orc_e4m3_round_array(const double* y, int64_t n, double* out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_e4m3_round(y[i]);
+}
+
+/* Nearest bf16 value of x (8 significant bits, ties to even), as fp64. */
+double orc_round_bf16(double x)
+{
+    if (x == 0.0 || !isfinite(x))
+        return x;
+    int e;
+    frexp(x, &e); /* |x| = f 2^e, f in [0.5, 1) */
+    if (e < -125)
+        e = -125; /* bf16 subnormals: fixed spacing 2^-133 */
+    return ldexp(rint(ldexp(x, 8 - e)), e - 8);
+}
+
+void orc_round_bf16_array(const double* x, int64_t n, double* out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_round_bf16(x[i]);
+}
+
+/* MX rule on a group of values: y -> E4M3(y / 2^e) 2^e with e the group's
+ * scale exponent (orc_mx_exponent of its largest magnitude). */
+static void mx_round_group(double* y, int64_t n, int64_t stride)
+{
+    double amax = 0.0;
+    for (int64_t k = 0; k < n; ++k)
+        if (fabs(y[k * stride]) > amax)
+            amax = fabs(y[k * stride]);
+    int e = orc_mx_exponent(amax);
+    for (int64_t k = 0; k < n; ++k)
+        y[k * stride] = ldexp(orc_e4m3_round(ldexp(y[k * stride], -e)), e);
+}
+
+/* Steps 05-08 for one query row over the visible keys [ks, kend) of kv head
+ * hk (ks = the key document's first token).  Writes O_i (d values) and
+ * returns LSE_i = m + ln sum_j exp(S_j - m) (the unquantized sum).
+ *   S_j = alpha q . K_j;  mu = ceil(max_j S_j log2 e);  p_j = 2^(S_j log2 e - mu);
+ *   keys j < diag0: weight w_j = E4M3(2^4 p_j) 2^-4 (ORC_RND_P) or p_j, and
+ *     value row V_j;
+ *   keys j >= diag0 (the per-key fold of [FLAMIA] sec. 4 on the query's own
+ *     128-token tile; Vkey_j = codes_j 2^e_j with e_j = vkey_sf_j - 127):
+ *     y_j = 2^4 p_j 2^e_j, quantized per 32 keys (counted from ks) by the MX
+ *     rule (ORC_RND_P), multiplies the codes: weight y_j 2^-4 2^-e_j on the
+ *     value row Vkey_j;
+ *   O_i = sum_j w_j row_j / sum_j w_j, rounded to bf16 (ORC_RND_O).
+ * diag0 >= kend: no fold.  Srow, y: scratch of kend - ks values. */
+static double fwd_row_alg1(const double* q, const double* K, const double* V, const double* Vkey,
+                           const uint8_t* vkey_sf, int Hkv, int hk, int d, int64_t ks, int64_t kend, int64_t diag0,
+                           double alpha, int rnd, double* o, double* Srow, double* y)
+{
+    double m = -INFINITY;
+    for (int64_t j = ks; j < kend; ++j) {
+        Srow[j - ks] = alpha * dot(q, K + (j * Hkv + hk) * d, d);
+        if (Srow[j - ks] > m)
+            m = Srow[j - ks];
+    }
+    double l = 0.0;
+    for (int64_t j = ks; j < kend; ++j)
+        l += exp(Srow[j - ks] - m);
+    double lse = m + log(l);
+    double mu = ceil(m * ORC_LOG2E);
+    for (int k = 0; k < d; ++k)
+        o[k] = 0.0;
+    double W = 0.0;
+    int64_t f0 = diag0 < kend ? diag0 : kend;
+    for (int64_t j = ks; j < f0; ++j) {
+        double p = exp2(Srow[j - ks] * ORC_LOG2E - mu);
+        double w = (rnd & ORC_RND_P) ? orc_e4m3_round(16.0 * p) / 16.0 : p;
+        const double* v = V + (j * Hkv + hk) * d;
+        for (int k = 0; k < d; ++k)
+            o[k] += w * v[k];
+        W += w;
+    }
+    if (f0 < kend) {
+        for (int64_t j = f0; j < kend; ++j) {
+            int ej = (int)vkey_sf[j * Hkv + hk] - 127;
+            y[j - ks] = ldexp(16.0 * exp2(Srow[j - ks] * ORC_LOG2E - mu), ej);
+        }
+        if (rnd & ORC_RND_P)
+            for (int64_t g0 = f0; g0 < kend; g0 += 32) /* f0 - ks is a multiple of 128 */
+                mx_round_group(y + (g0 - ks), (kend - g0 < 32 ? kend - g0 : 32), 1);
+        for (int64_t j = f0; j < kend; ++j) {
+            int ej = (int)vkey_sf[j * Hkv + hk] - 127;
+            double wc = y[j - ks] / 16.0; /* the weight on the codes */
+            const double* v = Vkey + (j * Hkv + hk) * d;
+            for (int k = 0; k < d; ++k)
+                o[k] += wc * ldexp(v[k], -ej);
+            W += ldexp(wc, -ej);
+        }
+    }
+    for (int k = 0; k < d; ++k) {
+        o[k] /= W;
+        if (rnd & ORC_RND_O)
+            o[k] = orc_round_bf16(o[k]);
+    }
+    return lse;
+}
+
+/* Key side of document b: [*ks, *ke) on the key rows (cu_k == NULL: the
+ * query side's documents). */
+static void key_range(const int32_t* cu_q, const int32_t* cu_k, int ndocs, int64_t Tq, int64_t Tk, int b,
+                      int64_t* ks, int64_t* ke)
+{
+    if (cu_k)
+        doc_range(cu_k, ndocs, Tk, b, ks, ke);
+    else
+        doc_range(cu_q, ndocs, Tq, b, ks, ke);
+}
+
+/* Algorithm 1's forward (steps 04-08) in fp64, direct: every query row i of
+ * document b attends to the keys [ks, ks + (i - s) + 1) when causal, else to
+ * all keys of the document's key side.  Q [Tq, Hq, d] and K [Tk, Hkv, d]
+ * score views; V [Tk, Hkv, d] the view of the P V product; Vkey, vkey_sf
+ * (decoded per-key view of V and its UE8M0 bytes [Tk, Hkv], causal
+ * self-attention only) or NULL: the per-key fold on each query's own
+ * 128-token tile.  cu_q == NULL: one document of Tq tokens; cu_k == NULL: the
+ * key documents are the query documents (self-attention).  rnd: ORC_RND_P |
+ * ORC_RND_O for Algorithm 1, 0 for the direct softmax.  sel == NULL: every
+ * row, else nsel (token, head) pairs.  O [Tq, Hq, d]; LSE [Hq, Tq]. */
+void orc_attn_fwd_alg1(const double* Q, const double* K, const double* V, const double* Vkey,
+                       const uint8_t* vkey_sf, int64_t Tq, int64_t Tk, int Hq, int Hkv, int d, const int32_t* cu_q,
+                       const int32_t* cu_k, int ndocs, int causal, double alpha, int rnd, const int32_t* sel,
+                       int64_t nsel, double* O, double* LSE)
+{
+    int nd = num_docs_eff(cu_q, ndocs);
+    int grp = Hq / Hkv;
+    int64_t maxk = 0;
+    for (int b = 0; b < nd; ++b) {
+        int64_t ks, ke;
+        key_range(cu_q, cu_k, ndocs, Tq, Tk, b, &ks, &ke);
+        if (ke - ks > maxk)
+            maxk = ke - ks;
+    }
+    int64_t n = sel ? nsel : Tq * Hq;
+#pragma omp parallel
+    {
+        double* Srow = (double*)malloc(sizeof(double) * (size_t)(maxk + 1));
+        double* y = (double*)malloc(sizeof(double) * (size_t)(maxk + 1));
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < n; ++r) {
+            int64_t i = sel ? sel[2 * r] : r / Hq;
+            int h = sel ? sel[2 * r + 1] : (int)(r % Hq);
+            int b = doc_of(cu_q, ndocs, i);
+            int64_t s, e, ks, ke;
+            doc_range(cu_q, ndocs, Tq, b, &s, &e);
+            key_range(cu_q, cu_k, ndocs, Tq, Tk, b, &ks, &ke);
+            int64_t kend = causal ? ks + (i - s) + 1 : ke;
+            int64_t diag0 = Vkey ? ks + ((i - s) / 128) * 128 : kend;
+            LSE[(int64_t)h * Tq + i] = fwd_row_alg1(Q + (i * Hq + h) * d, K, V, Vkey, vkey_sf, Hkv, h / grp, d, ks,
+                                                    kend, diag0, alpha, rnd, O + (i * Hq + h) * d, Srow, y);
+        }
+        free(Srow);
+        free(y);
+    }
+}
+
+/* Algorithm 1's backward (steps 09-16 without the FP16 accumulator, which
+ * the tolerance covers) in fp64, direct, per (document, kv head) unit:
+ *   O_i, LSE_i from the forward above (the same views and roundings);
+ *   D_i = Gr_i . O_i                                        (step 09)
+ *   P_ij = exp(S_ij - LSE_i); E_ij = Gr_i . Vr_j              (steps 11-13)
+ *   U_ij = P_ij (E_ij - D_i); U~ = U quantized per 32 x 32 block, queries and
+ *     keys counted from their document starts (ORC_RND_DS)     (step 14)
+ *   dV_j = sum_i E4M3(2^8 P_ij) 2^-8 Gt_i (ORC_RND_P8), dK_j = alpha sum_i
+ *     U~_ij Qt_i, dQ_i = alpha sum_j U~_ij Kt_j, dK and dV summed over the
+ *     query heads of the kv group                              (step 15)
+ * Views as orc_attn_bwd (Qs, Ks, Vo, Vr, Gr, Qt, Kt, Gt), plus:
+ *   Vkey, vkey_sf: the forward's per-key fold (as orc_attn_fwd_alg1);
+ *   Kkey, kkey_sf: the strict dQ operand ([FLAMIA] sec. 4: per-query dS
+ *     scales and the K fold): dQ_i takes U quantized per (query i, 32 keys)
+ *     instead of per block, and on query i's own 128-token tile the folded
+ *     values U_ij 2^ek_j times the per-key codes Kkey_j 2^-ek_j; dK keeps
+ *     the block quantization.
+ * cu_q == NULL: one document; cu_k == NULL: self-attention (Tk = Tq).
+ * units == NULL: every (document, kv head); else nunits pairs.  Outputs
+ * dQ [Tq, Hq, d], dK and dV [Tk, Hkv, d], O [Tq, Hq, d], LSE and D [Hq, Tq]
+ * of the units' rows. */
+void orc_attn_bwd_alg1(const double* Qs, const double* Ks, const double* Vo, const double* Vr, const double* Gr,
+                       const double* Qt, const double* Kt, const double* Gt, const double* Vkey,
+                       const uint8_t* vkey_sf, const double* Kkey, const uint8_t* kkey_sf, int64_t Tq, int64_t Tk,
+                       int Hq, int Hkv, int d, const int32_t* cu_q, const int32_t* cu_k, int ndocs, int causal,
+                       double alpha, int rnd, const int32_t* units, int nunits, double* dQ, double* dK, double* dV,
+                       double* O, double* LSE, double* D)
+{
+    int nd = num_docs_eff(cu_q, ndocs);
+    int nu = units ? nunits : nd * Hkv;
+    int grp = Hq / Hkv;
+    for (int u = 0; u < nu; ++u) {
+        int b = units ? units[2 * u] : u / Hkv;
+        int hk = units ? units[2 * u + 1] : u % Hkv;
+        int64_t s, e, ks, ke;
+        doc_range(cu_q, ndocs, Tq, b, &s, &e);
+        key_range(cu_q, cu_k, ndocs, Tq, Tk, b, &ks, &ke);
+        int64_t nq = e - s, nk = ke - ks;
+        for (int64_t j = ks; j < ke; ++j)
+            for (int k = 0; k < d; ++k) {
+                dK[(j * Hkv + hk) * d + k] = 0.0;
+                dV[(j * Hkv + hk) * d + k] = 0.0;
+            }
+        if (nq <= 0 || nk <= 0)
+            continue;
+        double* Ub = (double*)malloc(sizeof(double) * (size_t)nq * (size_t)nk); /* U~ of one query head */
+        for (int hh = 0; hh < grp; ++hh) {
+            int h = hk * grp + hh;
+            /* rows, 32 at a time (one block row of U) */
+#pragma omp parallel
+            {
+                double* Srow = (double*)malloc(sizeof(double) * (size_t)nk);
+                double* y = (double*)malloc(sizeof(double) * (size_t)nk);
+#pragma omp for schedule(dynamic, 1)
+                for (int64_t qb = 0; qb < nq; qb += 32) {
+                    int64_t qn = nq - qb < 32 ? nq - qb : 32;
+                    for (int64_t r = 0; r < qn; ++r) {
+                        int64_t i = s + qb + r;
+                        int64_t kend = causal ? ks + (i - s) + 1 : ke;
+                        int64_t diag0 = Vkey ? ks + ((i - s) / 128) * 128 : kend;
+                        double* o = O + (i * Hq + h) * d;
+                        double lse = fwd_row_alg1(Qs + (i * Hq + h) * d, Ks, Vo, Vkey, vkey_sf, Hkv, hk, d, ks, kend,
+                                                  diag0, alpha, rnd, o, Srow, y);
+                        LSE[(int64_t)h * Tq + i] = lse;
+                        const double* g = Gr + (i * Hq + h) * d;
+                        double Di = dot(g, o, d);
+                        D[(int64_t)h * Tq + i] = Di;
+                        double* urow = Ub + (qb + r) * nk;
+                        for (int64_t j = ks; j < ke; ++j) {
+                            if (j < kend) {
+                                double P = exp(Srow[j - ks] - lse);
+                                double E = dot(g, Vr + (j * Hkv + hk) * d, d);
+                                urow[j - ks] = P * (E - Di);
+                            } else {
+                                urow[j - ks] = 0.0;
+                            }
+                        }
+                        /* strict dQ operand: per (query, 32 keys) from the unquantized U */
+                        if (Kkey) {
+                            int64_t kd0 = ks + ((i - s) / 128) * 128;
+                            for (int64_t j = ks; j < kend; ++j)
+                                y[j - ks] = j >= kd0 ? ldexp(urow[j - ks], (int)kkey_sf[j * Hkv + hk] - 127)
+                                                     : urow[j - ks];
+                            if (rnd & ORC_RND_DS)
+                                for (int64_t g0 = ks; g0 < kend; g0 += 32)
+                                    mx_round_group(y + (g0 - ks), (kend - g0 < 32 ? kend - g0 : 32), 1);
+                            double* dq = dQ + (i * Hq + h) * d;
+                            for (int k = 0; k < d; ++k)
+                                dq[k] = 0.0;
+                            for (int64_t j = ks; j < kend; ++j) {
+                                if (j >= kd0) {
+                                    int ek = (int)kkey_sf[j * Hkv + hk] - 127;
+                                    const double* kr = Kkey + (j * Hkv + hk) * d;
+                                    for (int k = 0; k < d; ++k)
+                                        dq[k] += alpha * y[j - ks] * ldexp(kr[k], -ek);
+                                } else {
+                                    const double* kr = Kt + (j * Hkv + hk) * d;
+                                    for (int k = 0; k < d; ++k)
+                                        dq[k] += alpha * y[j - ks] * kr[k];
+                                }
+                            }
+                        }
+                    }
+                    /* step 14: the 32 x 32 blocks of this block row */
+                    if (rnd & ORC_RND_DS)
+                        for (int64_t kb = 0; kb < nk; kb += 32) {
+                            int64_t kn = nk - kb < 32 ? nk - kb : 32;
+                            double amax = 0.0;
+                            for (int64_t r = 0; r < qn; ++r)
+                                for (int64_t c = 0; c < kn; ++c) {
+                                    double a = fabs(Ub[(qb + r) * nk + kb + c]);
+                                    if (a > amax)
+                                        amax = a;
+                                }
+                            int ex = orc_mx_exponent(amax);
+                            for (int64_t r = 0; r < qn; ++r)
+                                for (int64_t c = 0; c < kn; ++c) {
+                                    double* x = Ub + (qb + r) * nk + kb + c;
+                                    *x = ldexp(orc_e4m3_round(ldexp(*x, -ex)), ex);
+                                }
+                        }
+                    if (!Kkey)
+                        for (int64_t r = 0; r < qn; ++r) {
+                            int64_t i = s + qb + r;
+                            double* dq = dQ + (i * Hq + h) * d;
+                            for (int k = 0; k < d; ++k)
+                                dq[k] = 0.0;
+                            for (int64_t j = ks; j < ke; ++j) {
+                                double uq = Ub[(qb + r) * nk + (j - ks)];
+                                if (uq == 0.0)
+                                    continue;
+                                const double* kr = Kt + (j * Hkv + hk) * d;
+                                for (int k = 0; k < d; ++k)
+                                    dq[k] += alpha * uq * kr[k];
+                            }
+                        }
+                }
+                free(Srow);
+                free(y);
+            }
+            /* key rows: dV and dK of this query head */
+#pragma omp parallel for schedule(dynamic, 8)
+            for (int64_t j = ks; j < ke; ++j) {
+                double* dk = dK + (j * Hkv + hk) * d;
+                double* dv = dV + (j * Hkv + hk) * d;
+                const double* kj = Ks + (j * Hkv + hk) * d;
+                int64_t ibeg = causal ? s + (j - ks) : s;
+                for (int64_t i = ibeg; i < e; ++i) {
+                    double S = alpha * dot(Qs + (i * Hq + h) * d, kj, d);
+                    double P = exp(S - LSE[(int64_t)h * Tq + i]);
+                    double P8 = (rnd & ORC_RND_P8) ? orc_e4m3_round(256.0 * P) / 256.0 : P;
+                    double uq = Ub[(i - s) * nk + (j - ks)];
+                    const double* gt = Gt + (i * Hq + h) * d;
+                    const double* qt = Qt + (i * Hq + h) * d;
+                    for (int k = 0; k < d; ++k) {
+                        dv[k] += P8 * gt[k];
+                        dk[k] += alpha * uq * qt[k];
+                    }
+                }
+            }
+        }
+        free(Ub);
     }
 }
 

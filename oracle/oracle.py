@@ -18,10 +18,24 @@ Sources (page titles, sections):
     dQ reduction), sec. 5 (P cap 2^(c+tau) <= 448, cosine example), sec. 6
     (visible-pair count).
 
-Parity pins live in ``tests/test_oracle_*.py``.  Unpinned: none of the
-functions below is unpinned; the GPU-side quantisation of P and dS has no
-counterpart here (the oracle keeps P and dS in fp64) and is covered only by
-the tolerance.
+Two attention oracles:
+  * ``attn_fwd`` / ``attn_bwd`` (and the ``_x``, ``_fold`` variants): direct
+    softmax attention in fp64 over the dequantized operands, P and dS kept in
+    fp64 -- the "unquantized P" reference whose error is reported;
+  * ``attn_fwd_alg1`` / ``attn_bwd_alg1``: the same direct computation with
+    the roundings that the steps of Algorithm 1 (FLAMIA sec. 5) name -- the
+    weights E4M3(2^4 p) against an integer reference maximum, O saved in
+    bf16, dV's operand E4M3(2^8 P), U quantized per 32 x 32 block, the strict
+    dQ operand -- each switchable (``RND_*``); the parity bar is asserted
+    against this one.
+
+Parity pins live in ``tests/test_oracle_*.py``.  Unpinned: none.  One
+reading is recorded rather than derived from the pages: ``dq_row_boost``
+restates the bound that the library documents for its per-row FP16 dQ
+boost (the pages give only the shape b_i = 2^floor(log2(h / a_i))); its pins
+check that the bound holds on exact backward values, so a GPU-vs-oracle
+equality of the boost exponents compares the kernel with that stated
+reading, not with a quantity the pages fix.
 """
 from __future__ import annotations
 
@@ -89,6 +103,14 @@ def _L():
                 "orc_attn_fwd_fold": (None, [P, P, P, P, i64, i32, i32, i32, P, i32, f64, P, P]),
                 "orc_dq_row_boost": (None, [P, P, P, i64, i32, i32, i32, P, i32, i32, ctypes.c_float, P]),
                 "orc_num_threads": (i32, []),
+                "orc_e4m3_round": (f64, [f64]),
+                "orc_e4m3_round_array": (None, [P, i64, P]),
+                "orc_round_bf16": (f64, [f64]),
+                "orc_round_bf16_array": (None, [P, i64, P]),
+                "orc_attn_fwd_alg1": (None, [P] * 5 + [i64, i64, i32, i32, i32, P, P, i32, i32, f64, i32, P, i64,
+                                                       P, P]),
+                "orc_attn_bwd_alg1": (None, [P] * 12 + [i64, i64, i32, i32, i32, P, P, i32, i32, f64, i32, P, i32]
+                                      + [P] * 6),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -459,6 +481,98 @@ def attn_bwd_x(Qs, Ks, Vo, Vr, Gr, Qt, Kt, Gt, cu_q, cu_k, alpha=None):
     }
     _L().orc_attn_bwd_x(*[_p(a) for a in arrs], Tq, Tk, Hq, Hkv, d, _p(cq), _p(ck), nd, float(alpha),
                         *[_p(out[k]) for k in ("dQ", "dK", "dV", "O", "LSE", "D")])
+    return out
+
+
+# --------------------------------------------------------------------------
+# Algorithm 1 (FLAMIA sec. 5): the forward and backward with the roundings
+# its steps name
+# --------------------------------------------------------------------------
+
+RND_P = 1    # step 07: forward weights E4M3(2^4 p), p against the integer reference ceil(max)
+RND_O = 2    # step 08: O saved in bf16
+RND_P8 = 4   # step 15: dV's operand E4M3(2^8 P) 2^-8
+RND_DS = 8   # step 14: U quantized per 32 x 32 block
+RND_ALG1 = RND_P | RND_O | RND_P8 | RND_DS
+
+
+def e4m3_round_array(y) -> np.ndarray:
+    """Nearest E4M3 value of each element (ties to the even code, saturating
+    to 448, sign kept), as float64."""
+    y = np.ascontiguousarray(np.asarray(y, dtype=np.float64))
+    out = np.empty(y.shape, np.float64)
+    _L().orc_e4m3_round_array(_p(y), y.size, _p(out))
+    return out
+
+
+def round_bf16_array(x) -> np.ndarray:
+    """Nearest bf16 value of each element (ties to even), as float64."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.empty(x.shape, np.float64)
+    _L().orc_round_bf16_array(_p(x), x.size, _p(out))
+    return out
+
+
+def _opt(a, dtype):
+    return None if a is None else np.ascontiguousarray(np.asarray(a, dtype=dtype))
+
+
+def attn_fwd_alg1(Q, K, V, cu_seqlens=None, causal=False, alpha=None, rnd=RND_ALG1, cu_k=None, Vkey=None,
+                  vkey_sf=None, sel=None):
+    """Algorithm 1's forward (steps 04-08) in fp64, direct: see
+    orc_attn_fwd_alg1.  Q [Tq,Hq,d], K/V [Tk,Hkv,d] decoded views; cu_k:
+    key-side offsets for cross-attention (None: self-attention); Vkey
+    [Tk,Hkv,d] decoded per-key view of V with its UE8M0 bytes vkey_sf
+    [Tk,Hkv] for the strict fold; rnd: the roundings (RND_* bits).  Returns
+    (O [Tq,Hq,d], LSE [Hq,Tq]); rows outside sel stay NaN."""
+    Q, K, V = (np.ascontiguousarray(a, dtype=np.float64) for a in (Q, K, V))
+    Tq, Hq, d = Q.shape
+    Tk, Hkv = K.shape[:2]
+    if alpha is None:
+        alpha = 1.0 / math.sqrt(d)
+    cu, nd = _cu(cu_seqlens)
+    ck, ndk = _cu(cu_k)
+    if ck is not None:
+        assert cu is not None and ndk == nd and not causal
+    Vkey, vkey_sf = _opt(Vkey, np.float64), _opt(vkey_sf, np.uint8)
+    assert (Vkey is None) == (vkey_sf is None)
+    O = np.full((Tq, Hq, d), np.nan)
+    LSE = np.full((Hq, Tq), np.nan)
+    if sel is not None:
+        sel = np.ascontiguousarray(np.asarray(sel, dtype=np.int32).reshape(-1, 2))
+    _L().orc_attn_fwd_alg1(_p(Q), _p(K), _p(V), _p(Vkey), _p(vkey_sf), Tq, Tk, Hq, Hkv, d, _p(cu), _p(ck), nd,
+                           int(bool(causal)), float(alpha), int(rnd), _p(sel), -1 if sel is None else len(sel),
+                           _p(O), _p(LSE))
+    return O, LSE
+
+
+def attn_bwd_alg1(Qs, Ks, Vo, Vr, Gr, Qt, Kt, Gt, cu_seqlens=None, causal=False, alpha=None, rnd=RND_ALG1,
+                  cu_k=None, Vkey=None, vkey_sf=None, Kkey=None, kkey_sf=None, units=None):
+    """Algorithm 1's backward (steps 09-15) in fp64, direct: see
+    orc_attn_bwd_alg1 for the role of each view.  Kkey/kkey_sf: the strict
+    dQ operand (per-query dS scales, K fold).  units: optional (doc, kv-head)
+    pairs.  Returns a dict with dQ, dK, dV, O, LSE, D (rows outside the units
+    stay NaN)."""
+    arrs = [np.ascontiguousarray(a, dtype=np.float64) for a in (Qs, Ks, Vo, Vr, Gr, Qt, Kt, Gt)]
+    Tq, Hq, d = arrs[0].shape
+    Tk, Hkv = arrs[1].shape[:2]
+    if alpha is None:
+        alpha = 1.0 / math.sqrt(d)
+    cu, nd = _cu(cu_seqlens)
+    ck, ndk = _cu(cu_k)
+    if ck is not None:
+        assert cu is not None and ndk == nd and not causal
+    Vkey, vkey_sf = _opt(Vkey, np.float64), _opt(vkey_sf, np.uint8)
+    Kkey, kkey_sf = _opt(Kkey, np.float64), _opt(kkey_sf, np.uint8)
+    assert (Vkey is None) == (vkey_sf is None) and (Kkey is None) == (kkey_sf is None)
+    out = {k: np.full(sh, np.nan) for k, sh in (("dQ", (Tq, Hq, d)), ("dK", (Tk, Hkv, d)), ("dV", (Tk, Hkv, d)),
+                                                  ("O", (Tq, Hq, d)), ("LSE", (Hq, Tq)), ("D", (Hq, Tq)))}
+    if units is not None:
+        units = np.ascontiguousarray(np.asarray(units, dtype=np.int32).reshape(-1, 2))
+    _L().orc_attn_bwd_alg1(*[_p(a) for a in arrs], _p(Vkey), _p(vkey_sf), _p(Kkey), _p(kkey_sf), Tq, Tk, Hq, Hkv,
+                           d, _p(cu), _p(ck), nd, int(bool(causal)), float(alpha), int(rnd), _p(units),
+                           -1 if units is None else len(units),
+                           *[_p(out[k]) for k in ("dQ", "dK", "dV", "O", "LSE", "D")])
     return out
 
 
