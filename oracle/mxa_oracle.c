@@ -1074,19 +1074,41 @@ void orc_dq_row_boost(const double* Gr, const double* Vr, const double* Kr, int6
  *   ORC_RND_DS - step 14: U = P (E - D) is quantized per 32 x 32 block of
  *                the tile by the MX rule ([FA4] "Квантование dS без
  *                транспонирования": one exponent per 32 x 32 block, both axes
- *                counted from the document start, before alpha).
- * Reading of step 07's reference maximum: the weights are p = 2^(x - mu) in
- * base-2 coordinates x = S log2(e), with mu = ceil(max_j x_j), an integer.
- * The pages let an online softmax keep an older reference up to tau behind
- * the true maximum; any integer reference mu' <= mu only multiplies every p by
- * the power of two 2^(mu - mu'), which E4M3 rounding commutes with in its
- * normal range ([FLAMIA] sec. 4, scale doubling), so one direct definition
- * stands for every lazy schedule except for weights below 2^-10 (E4M3
- * subnormals after the 2^4 boost). */
+ *                counted from the document start, before alpha);
+ *   ORC_RND_LSE - step 08: the row LSE is saved in fp32 and step 12 rebuilds
+ *                P from that saved value.  At a row whose scores span
+ *                thousands of nats one fp32 ulp of the LSE is 1e-4, which
+ *                moves every P of the row by that factor; lse_ulps moves the
+ *                saved value by that many fp32 ulps, spanning the results an
+ *                fp32 LSE admits.
+ * Step 07's reference maximum follows the online statistics of steps 04-06
+ * ("概率上限由两个参数共同决定": the reference may stay up to tau = 4 behind the
+ * true maximum, in base-2 coordinates x = S log2(e)).  The keys of a row are
+ * walked in key tiles of ref_tile keys counted from the key document's start;
+ * with t_max the largest x of a tile's visible keys, the reference is
+ *   m = ceil(t_max) at the first tile, and m = ceil(t_max) again at any later
+ *   tile whose t_max exceeds m + 4 (else m stays);
+ * and every key of a tile takes the weight p = 2^(x - m) against the m in
+ * force after its tile's update.  Readings (the pages leave these open): the
+ * reference lies on the integer grid, so a raise rescales the earlier sums by
+ * an exact power of two and the E4M3 weights of the normal range equal those
+ * of any other integer reference ([FLAMIA] sec. 4, scale doubling) -- only
+ * weights below 2^-10 of the reference (E4M3 subnormals after the 2^4 boost)
+ * depend on the schedule; the integer decision is taken in IEEE fp32 from
+ * the fp32-rounded raw score q.k times the fp32 product alpha * log2(e), as a
+ * kernel holding fp32 scores takes it; ref_tile = 0 means one tile holding
+ * every visible key (m = ceil(max x) of the row).
+ * The E4M3 code of each forward weight is likewise decided in fp32, the
+ * precision in which an fp32 score holds it: the boosted weight is
+ * 2^(x32) with x32 = fma32(fl32(q.k), fl32(alpha log2 e), 4 - m), its exact
+ * power of two rounded to fp32, then to E4M3 (at scores of 10^4 an fp32
+ * score fixes a weight only to about 4e-5, so a weight near a tie between
+ * two codes is decided by that rounding). */
 #define ORC_RND_P 1
 #define ORC_RND_O 2
 #define ORC_RND_P8 4
 #define ORC_RND_DS 8
+#define ORC_RND_LSE 16 /* step 08: LSE saved in fp32; the backward rebuilds P from it */
 
 #define ORC_LOG2E 1.4426950408889634074
 
@@ -1161,7 +1183,8 @@ static void mx_round_group(double* y, int64_t n, int64_t stride)
 /* Steps 05-08 for one query row over the visible keys [ks, kend) of kv head
  * hk (ks = the key document's first token).  Writes O_i (d values) and
  * returns LSE_i = m + ln sum_j exp(S_j - m) (the unquantized sum).
- *   S_j = alpha q . K_j;  mu = ceil(max_j S_j log2 e);  p_j = 2^(S_j log2 e - mu);
+ *   S_j = alpha q . K_j;  p_j = 2^(S_j log2 e - mu_j) with mu_j the reference
+ *   in force at key j's tile (the schedule above, ref_tile keys per tile);
  *   keys j < diag0: weight w_j = E4M3(2^4 p_j) 2^-4 (ORC_RND_P) or p_j, and
  *     value row V_j;
  *   keys j >= diag0 (the per-key fold of [FLAMIA] sec. 4 on the query's own
@@ -1170,14 +1193,16 @@ static void mx_round_group(double* y, int64_t n, int64_t stride)
  *     rule (ORC_RND_P), multiplies the codes: weight y_j 2^-4 2^-e_j on the
  *     value row Vkey_j;
  *   O_i = sum_j w_j row_j / sum_j w_j, rounded to bf16 (ORC_RND_O).
- * diag0 >= kend: no fold.  Srow, y: scratch of kend - ks values. */
+ * diag0 >= kend: no fold.  Srow, y, mu, raw: scratch of kend - ks values. */
 static double fwd_row_alg1(const double* q, const double* K, const double* V, const double* Vkey,
                            const uint8_t* vkey_sf, int Hkv, int hk, int d, int64_t ks, int64_t kend, int64_t diag0,
-                           double alpha, int rnd, double* o, double* Srow, double* y)
+                           double alpha, int rnd, int64_t ref_tile, double* o, double* Srow, double* y, double* mu,
+                           double* raw)
 {
     double m = -INFINITY;
     for (int64_t j = ks; j < kend; ++j) {
-        Srow[j - ks] = alpha * dot(q, K + (j * Hkv + hk) * d, d);
+        raw[j - ks] = dot(q, K + (j * Hkv + hk) * d, d); /* the score q . k before alpha */
+        Srow[j - ks] = alpha * raw[j - ks];
         if (Srow[j - ks] > m)
             m = Srow[j - ks];
     }
@@ -1185,14 +1210,40 @@ static double fwd_row_alg1(const double* q, const double* K, const double* V, co
     for (int64_t j = ks; j < kend; ++j)
         l += exp(Srow[j - ks] - m);
     double lse = m + log(l);
-    double mu = ceil(m * ORC_LOG2E);
+    /* the reference in force at each key's tile */
+    const float sl2 = (float)alpha * 1.4426950408889634f;
+    {
+        int64_t tile = ref_tile > 0 ? ref_tile : (kend - ks > 0 ? kend - ks : 1);
+        float mref = -INFINITY;
+        for (int64_t t0 = ks; t0 < kend; t0 += tile) {
+            int64_t t1 = t0 + tile < kend ? t0 + tile : kend;
+            float tmax = -INFINITY;
+            for (int64_t j = t0; j < t1; ++j)
+                if ((float)raw[j - ks] > tmax)
+                    tmax = (float)raw[j - ks];
+            float ts = tmax * sl2;
+            if (t0 == ks || ts > mref + 4.0f)
+                mref = ceilf(ts);
+            for (int64_t j = t0; j < t1; ++j)
+                mu[j - ks] = (double)mref;
+        }
+    }
+    /* each weight joins the sums in the frame of the last reference: the
+     * sums are rescaled by 2^(m_old - m_new) whenever the reference rises */
+    const double mlast = kend > ks ? mu[kend - 1 - ks] : 0.0;
     for (int k = 0; k < d; ++k)
         o[k] = 0.0;
     double W = 0.0;
     int64_t f0 = diag0 < kend ? diag0 : kend;
     for (int64_t j = ks; j < f0; ++j) {
-        double p = exp2(Srow[j - ks] * ORC_LOG2E - mu);
-        double w = (rnd & ORC_RND_P) ? orc_e4m3_round(16.0 * p) / 16.0 : p;
+        double w;
+        if (rnd & ORC_RND_P) {
+            float x32 = fmaf((float)raw[j - ks], sl2, 4.0f - (float)mu[j - ks]);
+            w = orc_e4m3_round((double)(float)exp2((double)x32)) / 16.0;
+        } else {
+            w = exp2(Srow[j - ks] * ORC_LOG2E - mu[j - ks]);
+        }
+        w = ldexp(w, (int)(mu[j - ks] - mlast));
         const double* v = V + (j * Hkv + hk) * d;
         for (int k = 0; k < d; ++k)
             o[k] += w * v[k];
@@ -1201,7 +1252,14 @@ static double fwd_row_alg1(const double* q, const double* K, const double* V, co
     if (f0 < kend) {
         for (int64_t j = f0; j < kend; ++j) {
             int ej = (int)vkey_sf[j * Hkv + hk] - 127;
-            y[j - ks] = ldexp(16.0 * exp2(Srow[j - ks] * ORC_LOG2E - mu), ej);
+            double p16;
+            if (rnd & ORC_RND_P) {
+                float x32 = fmaf((float)raw[j - ks], sl2, 4.0f - (float)mu[j - ks]);
+                p16 = (double)(float)exp2((double)x32);
+            } else {
+                p16 = 16.0 * exp2(Srow[j - ks] * ORC_LOG2E - mu[j - ks]);
+            }
+            y[j - ks] = ldexp(p16, ej + (int)(mu[j - ks] - mlast));
         }
         if (rnd & ORC_RND_P)
             for (int64_t g0 = f0; g0 < kend; g0 += 32) /* f0 - ks is a multiple of 128 */
@@ -1223,6 +1281,17 @@ static double fwd_row_alg1(const double* q, const double* K, const double* V, co
     return lse;
 }
 
+/* The LSE as step 08 saves it: rounded to fp32, then moved by k fp32 ulps. */
+static double saved_lse(double lse, int k)
+{
+    float f = (float)lse;
+    for (; k > 0; --k)
+        f = nextafterf(f, INFINITY);
+    for (; k < 0; ++k)
+        f = nextafterf(f, -INFINITY);
+    return (double)f;
+}
+
 /* Key side of document b: [*ks, *ke) on the key rows (cu_k == NULL: the
  * query side's documents). */
 static void key_range(const int32_t* cu_q, const int32_t* cu_k, int ndocs, int64_t Tq, int64_t Tk, int b,
@@ -1242,12 +1311,13 @@ static void key_range(const int32_t* cu_q, const int32_t* cu_k, int ndocs, int64
  * self-attention only) or NULL: the per-key fold on each query's own
  * 128-token tile.  cu_q == NULL: one document of Tq tokens; cu_k == NULL: the
  * key documents are the query documents (self-attention).  rnd: ORC_RND_P |
- * ORC_RND_O for Algorithm 1, 0 for the direct softmax.  sel == NULL: every
- * row, else nsel (token, head) pairs.  O [Tq, Hq, d]; LSE [Hq, Tq]. */
+ * ORC_RND_O for Algorithm 1, 0 for the direct softmax.  ref_tile: the key
+ * tile of the reference schedule (0: one tile).  sel == NULL: every row, else
+ * nsel (token, head) pairs.  O [Tq, Hq, d]; LSE [Hq, Tq]. */
 void orc_attn_fwd_alg1(const double* Q, const double* K, const double* V, const double* Vkey,
                        const uint8_t* vkey_sf, int64_t Tq, int64_t Tk, int Hq, int Hkv, int d, const int32_t* cu_q,
-                       const int32_t* cu_k, int ndocs, int causal, double alpha, int rnd, const int32_t* sel,
-                       int64_t nsel, double* O, double* LSE)
+                       const int32_t* cu_k, int ndocs, int causal, double alpha, int rnd, int64_t ref_tile,
+                       const int32_t* sel, int64_t nsel, double* O, double* LSE)
 {
     int nd = num_docs_eff(cu_q, ndocs);
     int grp = Hq / Hkv;
@@ -1263,6 +1333,8 @@ void orc_attn_fwd_alg1(const double* Q, const double* K, const double* V, const 
     {
         double* Srow = (double*)malloc(sizeof(double) * (size_t)(maxk + 1));
         double* y = (double*)malloc(sizeof(double) * (size_t)(maxk + 1));
+        double* mu = (double*)malloc(sizeof(double) * (size_t)(maxk + 1));
+        double* raw = (double*)malloc(sizeof(double) * (size_t)(maxk + 1));
 #pragma omp for schedule(dynamic, 16)
         for (int64_t r = 0; r < n; ++r) {
             int64_t i = sel ? sel[2 * r] : r / Hq;
@@ -1274,10 +1346,13 @@ void orc_attn_fwd_alg1(const double* Q, const double* K, const double* V, const 
             int64_t kend = causal ? ks + (i - s) + 1 : ke;
             int64_t diag0 = Vkey ? ks + ((i - s) / 128) * 128 : kend;
             LSE[(int64_t)h * Tq + i] = fwd_row_alg1(Q + (i * Hq + h) * d, K, V, Vkey, vkey_sf, Hkv, h / grp, d, ks,
-                                                    kend, diag0, alpha, rnd, O + (i * Hq + h) * d, Srow, y);
+                                                    kend, diag0, alpha, rnd, ref_tile, O + (i * Hq + h) * d, Srow, y,
+                                                    mu, raw);
         }
         free(Srow);
         free(y);
+        free(mu);
+        free(raw);
     }
 }
 
@@ -1299,15 +1374,16 @@ void orc_attn_fwd_alg1(const double* Q, const double* K, const double* V, const 
  *     values U_ij 2^ek_j times the per-key codes Kkey_j 2^-ek_j; dK keeps
  *     the block quantization.
  * cu_q == NULL: one document; cu_k == NULL: self-attention (Tk = Tq).
+ * lse_ulps: with ORC_RND_LSE, the saved fp32 LSE moved by that many ulps.
  * units == NULL: every (document, kv head); else nunits pairs.  Outputs
- * dQ [Tq, Hq, d], dK and dV [Tk, Hkv, d], O [Tq, Hq, d], LSE and D [Hq, Tq]
- * of the units' rows. */
+ * dQ [Tq, Hq, d], dK and dV [Tk, Hkv, d], O [Tq, Hq, d], LSE (as saved) and
+ * D [Hq, Tq] of the units' rows. */
 void orc_attn_bwd_alg1(const double* Qs, const double* Ks, const double* Vo, const double* Vr, const double* Gr,
                        const double* Qt, const double* Kt, const double* Gt, const double* Vkey,
                        const uint8_t* vkey_sf, const double* Kkey, const uint8_t* kkey_sf, int64_t Tq, int64_t Tk,
                        int Hq, int Hkv, int d, const int32_t* cu_q, const int32_t* cu_k, int ndocs, int causal,
-                       double alpha, int rnd, const int32_t* units, int nunits, double* dQ, double* dK, double* dV,
-                       double* O, double* LSE, double* D)
+                       double alpha, int rnd, int64_t ref_tile, int lse_ulps, const int32_t* units, int nunits,
+                       double* dQ, double* dK, double* dV, double* O, double* LSE, double* D)
 {
     int nd = num_docs_eff(cu_q, ndocs);
     int nu = units ? nunits : nd * Hkv;
@@ -1334,6 +1410,8 @@ void orc_attn_bwd_alg1(const double* Qs, const double* Ks, const double* Vo, con
             {
                 double* Srow = (double*)malloc(sizeof(double) * (size_t)nk);
                 double* y = (double*)malloc(sizeof(double) * (size_t)nk);
+                double* mu = (double*)malloc(sizeof(double) * (size_t)nk);
+                double* raw = (double*)malloc(sizeof(double) * (size_t)nk);
 #pragma omp for schedule(dynamic, 1)
                 for (int64_t qb = 0; qb < nq; qb += 32) {
                     int64_t qn = nq - qb < 32 ? nq - qb : 32;
@@ -1343,7 +1421,9 @@ void orc_attn_bwd_alg1(const double* Qs, const double* Ks, const double* Vo, con
                         int64_t diag0 = Vkey ? ks + ((i - s) / 128) * 128 : kend;
                         double* o = O + (i * Hq + h) * d;
                         double lse = fwd_row_alg1(Qs + (i * Hq + h) * d, Ks, Vo, Vkey, vkey_sf, Hkv, hk, d, ks, kend,
-                                                  diag0, alpha, rnd, o, Srow, y);
+                                                  diag0, alpha, rnd, ref_tile, o, Srow, y, mu, raw);
+                        if (rnd & ORC_RND_LSE)
+                            lse = saved_lse(lse, lse_ulps);
                         LSE[(int64_t)h * Tq + i] = lse;
                         const double* g = Gr + (i * Hq + h) * d;
                         double Di = dot(g, o, d);
@@ -1420,6 +1500,8 @@ void orc_attn_bwd_alg1(const double* Qs, const double* Ks, const double* Vo, con
                 }
                 free(Srow);
                 free(y);
+                free(mu);
+                free(raw);
             }
             /* key rows: dV and dK of this query head */
 #pragma omp parallel for schedule(dynamic, 8)

@@ -107,10 +107,10 @@ def _L():
                 "orc_e4m3_round_array": (None, [P, i64, P]),
                 "orc_round_bf16": (f64, [f64]),
                 "orc_round_bf16_array": (None, [P, i64, P]),
-                "orc_attn_fwd_alg1": (None, [P] * 5 + [i64, i64, i32, i32, i32, P, P, i32, i32, f64, i32, P, i64,
-                                                       P, P]),
-                "orc_attn_bwd_alg1": (None, [P] * 12 + [i64, i64, i32, i32, i32, P, P, i32, i32, f64, i32, P, i32]
-                                      + [P] * 6),
+                "orc_attn_fwd_alg1": (None, [P] * 5 + [i64, i64, i32, i32, i32, P, P, i32, i32, f64, i32, i64, P,
+                                                       i64, P, P]),
+                "orc_attn_bwd_alg1": (None, [P] * 12 + [i64, i64, i32, i32, i32, P, P, i32, i32, f64, i32, i64, i32,
+                                                        P, i32] + [P] * 6),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -493,7 +493,11 @@ RND_P = 1    # step 07: forward weights E4M3(2^4 p), p against the integer refer
 RND_O = 2    # step 08: O saved in bf16
 RND_P8 = 4   # step 15: dV's operand E4M3(2^8 P) 2^-8
 RND_DS = 8   # step 14: U quantized per 32 x 32 block
-RND_ALG1 = RND_P | RND_O | RND_P8 | RND_DS
+RND_LSE = 16  # step 08: LSE saved in fp32, P rebuilt from it
+RND_ALG1 = RND_P | RND_O | RND_P8 | RND_DS | RND_LSE
+# key tile of the online reference schedule of step 07 (256 keys: the tile
+# the attention kernels walk); 0 = one tile holding every visible key
+REF_TILE = 256
 
 
 def e4m3_round_array(y) -> np.ndarray:
@@ -518,13 +522,14 @@ def _opt(a, dtype):
 
 
 def attn_fwd_alg1(Q, K, V, cu_seqlens=None, causal=False, alpha=None, rnd=RND_ALG1, cu_k=None, Vkey=None,
-                  vkey_sf=None, sel=None):
+                  vkey_sf=None, sel=None, ref_tile=REF_TILE):
     """Algorithm 1's forward (steps 04-08) in fp64, direct: see
     orc_attn_fwd_alg1.  Q [Tq,Hq,d], K/V [Tk,Hkv,d] decoded views; cu_k:
     key-side offsets for cross-attention (None: self-attention); Vkey
     [Tk,Hkv,d] decoded per-key view of V with its UE8M0 bytes vkey_sf
-    [Tk,Hkv] for the strict fold; rnd: the roundings (RND_* bits).  Returns
-    (O [Tq,Hq,d], LSE [Hq,Tq]); rows outside sel stay NaN."""
+    [Tk,Hkv] for the strict fold; rnd: the roundings (RND_* bits); ref_tile:
+    the key tile of the lazy reference schedule.  Returns (O [Tq,Hq,d],
+    LSE [Hq,Tq]); rows outside sel stay NaN."""
     Q, K, V = (np.ascontiguousarray(a, dtype=np.float64) for a in (Q, K, V))
     Tq, Hq, d = Q.shape
     Tk, Hkv = K.shape[:2]
@@ -541,16 +546,18 @@ def attn_fwd_alg1(Q, K, V, cu_seqlens=None, causal=False, alpha=None, rnd=RND_AL
     if sel is not None:
         sel = np.ascontiguousarray(np.asarray(sel, dtype=np.int32).reshape(-1, 2))
     _L().orc_attn_fwd_alg1(_p(Q), _p(K), _p(V), _p(Vkey), _p(vkey_sf), Tq, Tk, Hq, Hkv, d, _p(cu), _p(ck), nd,
-                           int(bool(causal)), float(alpha), int(rnd), _p(sel), -1 if sel is None else len(sel),
-                           _p(O), _p(LSE))
+                           int(bool(causal)), float(alpha), int(rnd), int(ref_tile), _p(sel),
+                           -1 if sel is None else len(sel), _p(O), _p(LSE))
     return O, LSE
 
 
 def attn_bwd_alg1(Qs, Ks, Vo, Vr, Gr, Qt, Kt, Gt, cu_seqlens=None, causal=False, alpha=None, rnd=RND_ALG1,
-                  cu_k=None, Vkey=None, vkey_sf=None, Kkey=None, kkey_sf=None, units=None):
+                  cu_k=None, Vkey=None, vkey_sf=None, Kkey=None, kkey_sf=None, units=None, ref_tile=REF_TILE,
+                  lse_ulps=0):
     """Algorithm 1's backward (steps 09-15) in fp64, direct: see
     orc_attn_bwd_alg1 for the role of each view.  Kkey/kkey_sf: the strict
-    dQ operand (per-query dS scales, K fold).  units: optional (doc, kv-head)
+    dQ operand (per-query dS scales, K fold).  lse_ulps: the saved fp32 LSE
+    moved by that many ulps (RND_LSE).  units: optional (doc, kv-head)
     pairs.  Returns a dict with dQ, dK, dV, O, LSE, D (rows outside the units
     stay NaN)."""
     arrs = [np.ascontiguousarray(a, dtype=np.float64) for a in (Qs, Ks, Vo, Vr, Gr, Qt, Kt, Gt)]
@@ -570,7 +577,8 @@ def attn_bwd_alg1(Qs, Ks, Vo, Vr, Gr, Qt, Kt, Gt, cu_seqlens=None, causal=False,
     if units is not None:
         units = np.ascontiguousarray(np.asarray(units, dtype=np.int32).reshape(-1, 2))
     _L().orc_attn_bwd_alg1(*[_p(a) for a in arrs], _p(Vkey), _p(vkey_sf), _p(Kkey), _p(kkey_sf), Tq, Tk, Hq, Hkv,
-                           d, _p(cu), _p(ck), nd, int(bool(causal)), float(alpha), int(rnd), _p(units),
+                           d, _p(cu), _p(ck), nd, int(bool(causal)), float(alpha), int(rnd), int(ref_tile),
+                           int(lse_ulps), _p(units),
                            -1 if units is None else len(units),
                            *[_p(out[k]) for k in ("dQ", "dK", "dV", "O", "LSE", "D")])
     return out

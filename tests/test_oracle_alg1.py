@@ -165,11 +165,76 @@ def test_dv_operand_boost_hand_worked():
     V = np.array([[[1.0]], [[3.0]]])
     G = np.array([[[1.0]], [[1.0]]])
     cu = _cu([2])
-    out = orc.attn_bwd_alg1(Q, K, V, V, G, Q, K, G, cu, True, alpha=1.0)
+    rnd = orc.RND_ALG1 & ~orc.RND_LSE  # P from the exact LSE
+    out = orc.attn_bwd_alg1(Q, K, V, V, G, Q, K, G, cu, True, alpha=1.0, rnd=rnd)
     assert out["dV"][0, 0, 0] == ex["dV0"]
     assert out["dV"][1, 0, 0] == ex["dV1"]
-    un = orc.attn_bwd_alg1(Q, K, V, V, G, Q, K, G, cu, True, alpha=1.0, rnd=orc.RND_ALG1 & ~orc.RND_P8)
+    un = orc.attn_bwd_alg1(Q, K, V, V, G, Q, K, G, cu, True, alpha=1.0, rnd=rnd & ~orc.RND_P8)
     assert abs(un["dV"][0, 0, 0] - ex["dV0_unrounded"]) < 1e-15
+
+
+def test_lazy_reference_row_hand_worked():
+    """Step 07's reference schedule with one key per tile: the reference
+    rises only when a tile's maximum passes it by more than tau = 4, and the
+    one weight in E4M3's subnormal range depends on it."""
+    ex = GOLD["lazy_reference_row"]
+    x = [-5.3, 2.5, 5.7]
+    Q = np.array([[[1.0]], [[0.0]], [[0.0]]])
+    K = np.array([[[v * LN2]] for v in x])
+    V = np.array([[[1000.0]], [[2.0]], [[-1.0]]])
+    O, _ = orc.attn_fwd_alg1(Q, K, V, None, False, alpha=1.0, rnd=orc.RND_P, ref_tile=1)
+    assert abs(O[0, 0, 0] - ex["O"]) < 1e-15
+    Od, _ = orc.attn_fwd_alg1(Q, K, V, None, False, alpha=1.0, rnd=orc.RND_P, ref_tile=0)
+    assert abs(Od[0, 0, 0] - ex["O_direct_reference"]) < 1e-15
+    assert ex["weights"][0] != ex["direct_weights"][0]
+
+
+def test_reference_schedule_properties():
+    """One tile covering every key is the direct reference; with scores
+    spread over a few binades every weight stays in E4M3's normal range and
+    any tile size gives the same bits; dV never depends on the schedule (its
+    operand is P = exp(S - LSE))."""
+    lens, Hq, Hkv, d = [300, 513], 2, 1, 32
+    T = sum(lens)
+    cu = _cu(lens)
+    Qs, Ks, Vo, Vr, Gr, Qt, Kt, Gt = _views(T, Hq, Hkv, d, 1400)
+    for causal in (False, True):
+        a = orc.attn_fwd_alg1(Qs, Ks, Vo, cu, causal, ref_tile=0)
+        b = orc.attn_fwd_alg1(Qs, Ks, Vo, cu, causal, ref_tile=1024)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+        small = [0.05 * v for v in (Qs, Ks)]
+        outs = [orc.attn_fwd_alg1(small[0], small[1], Vo, cu, causal, ref_tile=r)[0] for r in (0, 1, 7, 256)]
+        assert all(np.array_equal(o, outs[0]) for o in outs[1:])
+        big = [3.0 * v for v in (Qs, Ks)]
+        r0 = orc.attn_bwd_alg1(big[0], big[1], Vo, Vr, Gr, Qt, Kt, Gt, cu, causal, ref_tile=0)
+        r1 = orc.attn_bwd_alg1(big[0], big[1], Vo, Vr, Gr, Qt, Kt, Gt, cu, causal, ref_tile=16)
+        assert np.array_equal(r0["dV"], r1["dV"]) and np.array_equal(r0["LSE"], r1["LSE"])
+        assert not np.array_equal(r0["O"], r1["O"])  # wide scores: subnormal weights follow the schedule
+
+
+def test_saved_lse_is_fp32_and_moves_by_ulps():
+    """Step 08 saves the LSE in fp32 and step 12 rebuilds P from it: the LSE
+    output is the fp32 rounding of the exact one (lse_ulps moves it by whole
+    fp32 ulps), and with one-hot Gt, dV reads P = exp(S - LSE_saved)."""
+    lens, H, d = [40, 25], 1, 65
+    T = sum(lens)
+    cu = _cu(lens)
+    Qs, Ks = _rand((T, H, d), 1500, 3.0), _rand((T, H, d), 1501, 3.0)
+    Vo, Vr, Gr = _rand((T, H, d), 1502), _rand((T, H, d), 1503), _rand((T, H, d), 1504)
+    eye = np.eye(T).reshape(T, 1, T)
+    rnd = orc.RND_LSE
+    exact = orc.attn_bwd_alg1(Qs, Ks, Vo, Vr, Gr, eye, eye, eye, cu, True, rnd=0)
+    for k in (-1, 0, 2):
+        r = orc.attn_bwd_alg1(Qs, Ks, Vo, Vr, Gr, eye, eye, eye, cu, True, rnd=rnd, lse_ulps=k)
+        want = exact["LSE"].astype(np.float32)
+        for _ in range(abs(k)):
+            want = np.nextafter(want, np.float32(np.inf if k > 0 else -np.inf))
+        assert np.array_equal(r["LSE"], want.astype(np.float64)), k
+        for b in range(len(lens)):
+            s_, e = cu[b], cu[b + 1]
+            S = Qs[s_:e, 0] @ Ks[s_:e, 0].T / math.sqrt(d)
+            P = np.tril(np.exp(S - r["LSE"][0, s_:e, None]))
+            np.testing.assert_allclose(r["dV"][s_:e, 0, s_:e].T, P, rtol=1e-13, atol=0)
 
 
 def test_p_cap_keeps_algorithm1_weights_in_range():
@@ -232,6 +297,28 @@ def _scores(Qs, Ks, lo, hi, klo, khi, h, hk, alpha):
     return alpha * Qs[lo:hi, h] @ Ks[klo:khi, hk].T
 
 
+def _boosted_weights(raw, alpha, tile=256):
+    """The forward's boosted weights 2^4 p of one row from its visible raw
+    scores q.k, as the oracle defines them: the reference schedule over key
+    tiles (ceil of an fp32 tile maximum times fp32 alpha log2 e, raised when
+    it passes the reference by more than 4) and the exponent argument
+    fma32(fl32(q.k), fl32(alpha log2 e), 4 - m), whose power of two is
+    rounded to fp32.  Returns (2^4 p, the reference of each key)."""
+    sl2 = np.float32(np.float32(alpha) * np.float32(1.4426950408889634))
+    r32 = raw.astype(np.float32)
+    m = np.empty(len(raw))
+    mref = None
+    for t0 in range(0, len(raw), tile):
+        ts = np.float32(r32[t0:t0 + tile].max() * sl2)
+        if mref is None or ts > mref + 4:
+            mref = float(np.ceil(ts))
+        m[t0:t0 + tile] = mref
+    # the product of two fp32 values is exact in fp64; one rounding to fp32
+    # then gives the fused multiply-add
+    x32 = (r32.astype(np.float64) * np.float64(sl2) + (4.0 - m)).astype(np.float32)
+    return np.exp2(x32.astype(np.float64)).astype(np.float32).astype(np.float64), m
+
+
 def test_one_hot_views_read_out_the_quantized_matrices():
     """With Kt_j = e_j (and Qt_i, Gt_i = e_i) the gradients are the quantized
     matrices themselves: dQ_i[j] = alpha U~_ij, dK_j[i] = alpha U~_ij,
@@ -274,12 +361,12 @@ def test_one_hot_views_read_out_the_quantized_matrices():
         O, _ = orc.attn_fwd_alg1(Qs, Ks, eye, cu, causal, alpha, rnd=orc.RND_P)
         for b in range(len(lens)):
             s, e = cu[b], cu[b + 1]
-            x = _scores(Qs, Ks, s, e, s, e, 0, 0, alpha) / LN2
-            if causal:
-                x = np.where(np.tril(np.ones_like(x)) > 0, x, -np.inf)
-            mu = np.ceil(x.max(1, keepdims=True))
-            w = orc.e4m3_round_array(16 * np.exp2(x - mu)) / 16
-            np.testing.assert_allclose(O[s:e, 0, s:e], w / w.sum(1, keepdims=True), rtol=1e-15, atol=0)
+            raw = Qs[s:e, 0] @ Ks[s:e, 0].T
+            for i in range(e - s):
+                kend = i + 1 if causal else e - s
+                y, _ = _boosted_weights(raw[i, :kend], alpha)
+                w = orc.e4m3_round_array(y) / 16
+                np.testing.assert_allclose(O[s + i, 0, s:s + kend], w / w.sum(), rtol=1e-15, atol=0)
 
 
 def test_one_hot_strict_dq_operand():
@@ -337,13 +424,13 @@ def test_one_hot_fold_weights():
                              vkey_sf=(ev + 127).astype(np.uint8))
     for b in range(len(lens)):
         s, e = cu[b], cu[b + 1]
-        x = _scores(Qs, Ks, s, e, s, e, 0, 0, alpha) / LN2
+        raw = Qs[s:e, 0] @ Ks[s:e, 0].T
         for i in range(e - s):
-            xi = x[i, :i + 1]
-            p = np.exp2(xi - np.ceil(xi.max()))
+            p16, m = _boosted_weights(raw[i, :i + 1], alpha)
+            p16 = p16 * np.exp2(m - m[-1])  # the frame of the last reference
             t0 = (i // 128) * 128
-            w = orc.e4m3_round_array(16 * p[:t0]) / 16
-            y = 16 * p[t0:] * np.exp2(ev[s + t0:s + i + 1, 0])
+            w = orc.e4m3_round_array(p16[:t0] / np.exp2(m[:t0] - m[-1])) * np.exp2(m[:t0] - m[-1]) / 16
+            y = p16[t0:] * np.exp2(ev[s + t0:s + i + 1, 0])
             for g in range(0, len(y), 32):
                 ex = orc.mx_exponent(float(np.abs(y[g:g + 32]).max()))
                 y[g:g + 32] = np.ldexp(orc.e4m3_round_array(np.ldexp(y[g:g + 32], -ex)), ex)
