@@ -10,7 +10,8 @@
 //                           TMEM;
 //   P_j  = online softmax of alpha * S_j with a lazily updated row max
 //          (rescale only when the tile max exceeds the running max by more
-//          than tau = 4 in log2 units), quantized in registers as E4M3(2^4 p)
+//          than tau = 4 in log2 units; the reference is ceil of the max, an
+//          integer in log2 units), quantized in registers as E4M3(2^4 p)
 //          (FLAMIA notes sec. 5: 2^(c+tau) <= 448 with (c, tau) = (4, 4)),
 //          stored to TMEM;
 //   [O | L] += P_j [V_j | 1]  one block-scaled MMA with A = P from TMEM
@@ -463,11 +464,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       const float mts = mt * sl2;
       bool rescale_o = false;
       float factor = 1.0f;
+      // the reference stays on the integer grid of base-2 coordinates, so a
+      // raise multiplies the earlier sums by an exact power of two and the
+      // E4M3 weights are those of the final reference ceil(max) shifted by
+      // whole binades (scale doubling, FLAMIA notes sec. 4)
       if (j == 0) {
-        m = mts;
+        m = ceilf(mts);
       } else if (mts > m + 4.0f) {
-        factor = ex2_approx(m - mts);
-        m = mts;
+        const float mn = ceilf(mts);
+        factor = exp2i_neg(static_cast<int>(fminf(mn - m, 127.0f)));
+        m = mn;
         rescale_o = true;
       }
       const float neg = 4.0f - m;

@@ -10,19 +10,19 @@ import torch
 from block_scaled_mxfp8_gb300 import inputs as inp
 from oracle import oracle as orc
 
-# Parity bar for floating-point outputs against the oracle run on the same
-# quantized operands: cosine >= 0.999 and max|err| <= 5e-2 * max|ref|.
-# The oracle keeps the attention weights P and the score gradient dS in fp64;
-# the CUDA path rounds them to E4M3 (3 mantissa bits: up to 2^-4 relative
-# error per weight) as the method prescribes (P boosted by 2^4 in the forward
-# and 2^8 for dV, dS per 32x32 block).  A CPU emulation of the forward's exact
-# arithmetic gives max|err| / max|ref| = 0.0138 on the tiny non-causal case,
-# and the backward's dS/P^T rounding reaches 0.038 on small cases and 0.055
-# on the full-size token-block workload (the max over more elements), so a
-# 1e-2 max-abs bar is not reachable by this quantization; 8e-2 is the bar
-# used, with cosine kept at 0.999.
+# Parity bar for floating-point outputs (O, LSE, dQ, dK, dV): cosine >= 0.999
+# and max|err| <= 1e-2 * max|ref| against the oracle run on the same quantized
+# operands -- the Algorithm 1 oracle (FLAMIA reading notes, sec. 5), which
+# applies the roundings the method prescribes: the weights E4M3(2^4 p), O in
+# bf16, dV's operand E4M3(2^8 P), dS per 32 x 32 block (and the strict
+# operand where used).  What remains between it and the kernels is fp32
+# against fp64 arithmetic (an E4M3 rounding decided differently at a near-tie,
+# a block exponent at a 448 * 2^k boundary), the FP16 dQ partial sums (11
+# significant bits per add) and the bf16 rounding of the gradients.  The
+# error against the direct oracle (P and dS in fp64) and against the
+# unquantized inputs is reported, not asserted.
 COS_MIN = 0.999
-MAXERR_FRAC = 8e-2
+MAXERR_FRAC = 1e-2
 
 
 def metrics(got, ref):
@@ -90,3 +90,43 @@ def oracle_views(w: inp.Workload, t: dict, names=("q", "k", "v", "do")):
 
 def to_np(x: torch.Tensor):
     return x.detach().float().cpu().numpy().astype(np.float64)
+
+
+def lse_spread(ref: dict, moved: list, names=("dQ", "dK", "dV")) -> dict:
+    """How far the oracle's own gradients move, as a fraction of max|ref|,
+    when the fp32 LSE that the backward rebuilds P from (Algorithm 1 step 08
+    saves it in fp32) moves by one ulp either way: the results that an fp32
+    LSE admits.  Rows whose scores span thousands of nats have an LSE ulp
+    near 1e-4, enough to flip dS codes near their rounding ties."""
+    out = {}
+    for nm in names:
+        mx = float(np.nanmax(np.abs(ref[nm])))
+        out[nm] = max(float(np.nanmax(np.abs(m[nm] - ref[nm]))) / mx for m in moved)
+    return out
+
+
+def check_outputs(tag, got: dict, ref: dict, direct: dict | None = None, names=("O", "dQ", "dK", "dV"),
+                  spread: dict | None = None):
+    """Assert every named output against the Algorithm 1 oracle (ref) at the
+    parity bar; print its error against the direct oracle too.  spread (from
+    lse_spread) widens the max-abs bar of a gradient by the oracle's own
+    movement under one ulp of its fp32 LSE -- zero except where the result
+    is not fixed at fp32 resolution.  LSE (when present in got) must also
+    agree to 1e-3 * max(1, max|LSE|)."""
+    spread = spread or {}
+    for nm in names:
+        if nm not in got:
+            continue
+        line = "%s %s vs alg1 %s" % (tag, nm, metrics(got[nm], ref[nm]))
+        if nm in spread:
+            line += " lse-ulp spread %.4g" % spread[nm]
+        if direct is not None and nm in direct:
+            line += " | vs direct %s" % metrics(got[nm], direct[nm])
+        print(line)
+    for nm in names:
+        if nm in got:
+            assert_close("%s %s" % (tag, nm), got[nm], ref[nm], frac=MAXERR_FRAC + spread.get(nm, 0.0))
+    if "LSE" in got:
+        L = np.asarray(ref["LSE"], np.float64)
+        err = float(np.nanmax(np.abs(np.asarray(got["LSE"], np.float64) - L)))
+        assert err <= 1e-3 * max(1.0, float(np.nanmax(np.abs(L)))), (tag, "LSE", err)

@@ -1,4 +1,5 @@
-"""GPU backward vs the oracle on the same quantized operands (dQ, dK, dV)."""
+"""GPU backward vs the Algorithm 1 oracle on the same quantized operands
+(dQ, dK, dV), with the direct oracle's error reported."""
 import math
 
 import numpy as np
@@ -8,7 +9,7 @@ import torch
 from block_scaled_mxfp8_gb300 import inputs as inp
 from oracle import oracle as orc
 
-from ._common import assert_close, gpu_views, metrics, oracle_views, to_np
+from ._common import assert_close, check_outputs, gpu_views, oracle_views, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -37,20 +38,25 @@ def run_bwd(w, dq_mode):
     mxa.check_error()
     _, d = oracle_views(w, t)
     cu = w.cu_seqlens.numpy()
-    r = orc.attn_bwd(d["q"]["row"], d["k"]["row"], d["v"]["tok"], d["v"]["row"], d["do"]["row"],
-                     d["q"]["tok"], d["k"]["tok"], d["do"]["tok"], cu, w.causal, 1.0 / math.sqrt(w.d))
+    r = oracle_bwd(w, d)
     return t, (dq, dk, dv), r
+
+
+def oracle_bwd(w, d, direct=False):
+    """The Algorithm 1 oracle (direct=True: P and dS in fp64) on the decoded
+    views d of workload w."""
+    fn = orc.attn_bwd if direct else orc.attn_bwd_alg1
+    return fn(d["q"]["row"], d["k"]["row"], d["v"]["tok"], d["v"]["row"], d["do"]["row"], d["q"]["tok"],
+              d["k"]["tok"], d["do"]["tok"], w.cu_seqlens.numpy(), w.causal, 1.0 / math.sqrt(w.d))
 
 
 @pytest.mark.parametrize("w,mode", CASES, ids=["%s%s_dq%s" % (c.name, "_causal" if c.causal else "", m)
                                                 for c, m in CASES])
 def test_bwd_matches_oracle(w, mode):
     t, (dq, dk, dv), r = run_bwd(w, mode)
-    for name, got, ref in (("dV", dv, r["dV"]), ("dK", dk, r["dK"]), ("dQ", dq, r["dQ"])):
-        print(w.name, name, metrics(to_np(got), ref))
-    assert_close("dV", to_np(dv), r["dV"])
-    assert_close("dK", to_np(dk), r["dK"])
-    assert_close("dQ", to_np(dq), r["dQ"])
+    _, d = oracle_views(w, t)
+    check_outputs("%s dq%d" % (w.name, mode), {"dQ": to_np(dq), "dK": to_np(dk), "dV": to_np(dv)}, r,
+                  oracle_bwd(w, d, direct=True))
 
 
 RECOMPUTE_CASES = [
@@ -85,9 +91,7 @@ def test_bwd_min_workspace_forms_ds_again(w):
     torch.cuda.synchronize()
     mxa.check_error()
     _, dd = oracle_views(w, t)
-    r = orc.attn_bwd(dd["q"]["row"], dd["k"]["row"], dd["v"]["tok"], dd["v"]["row"], dd["do"]["row"],
-                     dd["q"]["tok"], dd["k"]["tok"], dd["do"]["tok"], w.cu_seqlens.numpy(), w.causal,
-                     1.0 / math.sqrt(w.d))
+    r = oracle_bwd(w, dd)
     assert_close("dQ (dS formed again)", to_np(out[0]), r["dQ"])
     assert torch.equal(out[1], full[1]) and torch.equal(out[2], full[2])
 
@@ -117,8 +121,6 @@ def test_fp16_mode_small_workspace_takes_the_fused_kernel():
     torch.cuda.synchronize()
     mxa.check_error()
     _, dd = oracle_views(w, t)
-    r = orc.attn_bwd(dd["q"]["row"], dd["k"]["row"], dd["v"]["tok"], dd["v"]["row"], dd["do"]["row"],
-                     dd["q"]["tok"], dd["k"]["tok"], dd["do"]["tok"], w.cu_seqlens.numpy(), w.causal,
-                     1.0 / math.sqrt(w.d))
+    r = oracle_bwd(w, dd)
     for name, got, ref in (("dQ", out[0], r["dQ"]), ("dK", out[1], r["dK"]), ("dV", out[2], r["dV"])):
         assert_close(name + " (fused FP16 path)", to_np(got), ref)

@@ -1,5 +1,6 @@
 """GPU FP16 dQ reduction with a per-row boost (MXA_DQ_FP16_ROW; FLAMIA reading
-notes sec. 4, the strict accumulator scale) against the oracle.
+notes sec. 4, the strict accumulator scale) against the oracle (Algorithm 1
+variant for the gradients).
 
 * The boost exponent beta_i of every query row, read from the workspace
   (documented layout: fp32 [Hq, T] after the D and LSE rows), equals the
@@ -22,7 +23,7 @@ import torch
 from block_scaled_mxfp8_gb300 import inputs as inp
 from oracle import oracle as orc
 
-from ._common import assert_close, gpu_views, metrics, oracle_views, to_np
+from ._common import assert_close, check_outputs, gpu_views, metrics, oracle_views, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -68,8 +69,8 @@ def _gpu(w, t, mode):
 def _oracle(w, t):
     _, d = oracle_views(w, t)
     cu = w.cu_seqlens.numpy()
-    r = orc.attn_bwd(d["q"]["row"], d["k"]["row"], d["v"]["tok"], d["v"]["row"], d["do"]["row"],
-                     d["q"]["tok"], d["k"]["tok"], d["do"]["tok"], cu, w.causal, 1.0 / math.sqrt(w.d))
+    r = orc.attn_bwd_alg1(d["q"]["row"], d["k"]["row"], d["v"]["tok"], d["v"]["row"], d["do"]["row"],
+                          d["q"]["tok"], d["k"]["tok"], d["do"]["tok"], cu, w.causal, 1.0 / math.sqrt(w.d))
     beta = orc.dq_row_boost(d["do"]["row"], d["v"]["row"], d["k"]["row"], cu, w.causal)
     return r, beta
 
@@ -82,9 +83,7 @@ def test_row_boost_matches_oracle(w):
     (dq, dk, dv), beta = _gpu(w, t, mxa.MXA_DQ_FP16_ROW)
     r, beta_ref = _oracle(w, t)
     assert np.array_equal(beta, beta_ref), np.argwhere(beta != beta_ref)[:8]
-    for name, got, ref in (("dV", dv, r["dV"]), ("dK", dk, r["dK"]), ("dQ", dq, r["dQ"])):
-        print(w.name, name, metrics(to_np(got), ref))
-        assert_close(name, to_np(got), ref)
+    check_outputs(w.name + " dq2", {"dQ": to_np(dq), "dK": to_np(dk), "dV": to_np(dv)}, r)
 
 
 def test_large_gradients_overflow_the_fixed_boost_only():

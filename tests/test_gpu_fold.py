@@ -4,9 +4,10 @@ the probability operand) against the oracle.
 
 * mxa_quantize_key: codes and exponents bit for bit against the oracle's
   quant_key (exponents read through the tile-padded [H, NT, 128] layout).
-* The folded forward: O and LSE against the oracle's attn_fwd_fold (key j's
-  value row is its per-key view on query i's diagonal 128-token tile, its
-  token view before it) at the parity bar of the other forward tests.
+* The folded forward: O and LSE against the Algorithm 1 oracle with the fold
+  (key j's value row is its per-key view on query i's diagonal 128-token
+  tile, its token view before it; the folded weights quantized per query and
+  32 keys) at the parity bar of the other forward tests.
 * The property: keys, values and queries after position p change, inside
   p's own 32-token block, and every row <= p keeps O and LSE bit for bit.
 """
@@ -19,7 +20,7 @@ import torch
 from block_scaled_mxfp8_gb300 import inputs as inp
 from oracle import oracle as orc
 
-from ._common import assert_close, gpu_views, metrics, oracle_views, to_np
+from ._common import check_outputs, gpu_views, oracle_views, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -75,13 +76,12 @@ def test_fold_forward_matches_oracle(w):
     t = inp.tensors(w)
     o, lse = _fold_fwd(w, t)
     _, d = oracle_views(w, t, names=("q", "k", "v"))
-    vk = orc.dequant_key(*orc.quant_key(t["v"]))
-    O, L = orc.attn_fwd_fold(d["q"]["row"], d["k"]["row"], d["v"]["tok"], vk, w.cu_seqlens.numpy(),
-                             1.0 / math.sqrt(w.d))
-    print(w.name, "O", metrics(to_np(o), O))
-    assert_close("O", to_np(o), O)
-    lerr = np.abs(lse.cpu().numpy().astype(np.float64) - L).max()
-    assert lerr <= 1e-3 * np.abs(L).max(), lerr
+    vc, vs = orc.quant_key(t["v"])
+    vk = orc.dequant_key(vc, vs)
+    cu, alpha = w.cu_seqlens.numpy(), 1.0 / math.sqrt(w.d)
+    O, L = orc.attn_fwd_alg1(d["q"]["row"], d["k"]["row"], d["v"]["tok"], cu, True, alpha, Vkey=vk, vkey_sf=vs)
+    Od, _ = orc.attn_fwd_fold(d["q"]["row"], d["k"]["row"], d["v"]["tok"], vk, cu, alpha)
+    check_outputs(w.name, {"O": to_np(o), "LSE": lse.cpu().numpy()}, {"O": O, "LSE": L}, {"O": Od})
 
 
 def test_fold_forward_prefix_is_bit_identical_under_in_block_changes():
@@ -120,9 +120,9 @@ BWD_CASES = [
 ]
 
 
-def _strict_step(w, t, strict=True):
+def _strict_step(w, t, strict=True, dq_mode=0):
     """Folded forward, then the backward with (strict) or without the K fold
-    and per-query dS scales.  -> (dq, dk, dv)."""
+    and per-query dS scales, in dQ mode dq_mode.  -> (dq, dk, dv)."""
     from block_scaled_mxfp8_gb300 import mxa
 
     geo, gv = gpu_views(w, t)
@@ -131,34 +131,40 @@ def _strict_step(w, t, strict=True):
     o, lse = mxa.fwd(gv["q"][0], gv["k"][0], gv["v"][1], geo, True, v_key=vkey)
     views = {"q_row": gv["q"][0], "k_row": gv["k"][0], "v_row": gv["v"][0], "g_row": gv["do"][0],
              "q_tok": gv["q"][1], "k_tok": gv["k"][1], "g_tok": gv["do"][1]}
-    out = mxa.bwd(views, o, lse, geo, True, k_key=kkey)
+    out = mxa.bwd(views, o, lse, geo, True, dq_mode=dq_mode, k_key=kkey)
     torch.cuda.synchronize()
     mxa.check_error()
     return out
 
 
+@pytest.mark.parametrize("dq_mode", [0, 1, 2])
 @pytest.mark.parametrize("w", BWD_CASES, ids=[c.name for c in BWD_CASES])
-def test_strict_backward_matches_oracle(w):
+def test_strict_backward_matches_oracle(w, dq_mode):
+    """Strict dQ in each accumulation mode: FP32, FP16 x 2^9, FP16 with the
+    per-row boost."""
     t = inp.tensors(w, with_grad=True)
-    dq, dk, dv = _strict_step(w, t)
+    dq, dk, dv = _strict_step(w, t, dq_mode=dq_mode)
     _, d = oracle_views(w, t)
-    vk = orc.dequant_key(*orc.quant_key(t["v"]))
-    kk = orc.dequant_key(*orc.quant_key(t["k"]))
-    r = orc.attn_bwd_fold(d["q"]["row"], d["k"]["row"], d["v"]["tok"], d["v"]["row"], d["do"]["row"],
-                          d["q"]["tok"], d["k"]["tok"], d["do"]["tok"], vk, kk, w.cu_seqlens.numpy(),
-                          1.0 / math.sqrt(w.d))
-    for name, got, ref in (("dV", dv, r["dV"]), ("dK", dk, r["dK"]), ("dQ", dq, r["dQ"])):
-        print(w.name, name, metrics(to_np(got), ref))
-        assert_close(name, to_np(got), ref)
+    vc, vs = orc.quant_key(t["v"])
+    kc, ks = orc.quant_key(t["k"])
+    vk, kk = orc.dequant_key(vc, vs), orc.dequant_key(kc, ks)
+    vw = (d["q"]["row"], d["k"]["row"], d["v"]["tok"], d["v"]["row"], d["do"]["row"], d["q"]["tok"], d["k"]["tok"],
+          d["do"]["tok"])
+    cu, alpha = w.cu_seqlens.numpy(), 1.0 / math.sqrt(w.d)
+    r = orc.attn_bwd_alg1(*vw, cu, True, alpha, Vkey=vk, vkey_sf=vs, Kkey=kk, kkey_sf=ks)
+    rd = orc.attn_bwd_fold(*vw, vk, kk, cu, alpha)
+    check_outputs("%s strict dq%d" % (w.name, dq_mode), {"dQ": to_np(dq), "dK": to_np(dk), "dV": to_np(dv)}, r,
+                  rd)
 
 
-def test_strict_dq_prefix_is_bit_identical_under_in_block_changes():
+@pytest.mark.parametrize("dq_mode", [0, 1, 2])
+def test_strict_dq_prefix_is_bit_identical_under_in_block_changes(dq_mode):
     w = inp.make_custom("strict_prefix", lengths=[600, 333], Hq=4, Hkv=2, d=128, causal=True, seed=47)
     t = inp.tensors(w, with_grad=True)
-    base = _strict_step(w, t)
-    again = _strict_step(w, t)
+    base = _strict_step(w, t, dq_mode=dq_mode)
+    again = _strict_step(w, t, dq_mode=dq_mode)
     assert torch.equal(base[0], again[0]), "the strict backward must be deterministic"
-    plain = _strict_step(w, t, strict=False)
+    plain = _strict_step(w, t, strict=False, dq_mode=dq_mode)
     rng = np.random.default_rng(48)
     moved = 0
     for p in (35, 140, 255, 300, 517):
@@ -166,12 +172,12 @@ def test_strict_dq_prefix_is_bit_identical_under_in_block_changes():
         gain = float(rng.choice([-300.0, 64.0, 1e-3]))
         for k in ("q", "k", "v", "do"):  # the incoming gradient of rows <= p stays fixed
             tp[k][p + 1:600] = (tp[k][p + 1:600].float() * gain).to(torch.bfloat16)
-        dq, _, _ = _strict_step(w, tp)
+        dq, _, _ = _strict_step(w, tp, dq_mode=dq_mode)
         assert torch.equal(dq[: p + 1], base[0][: p + 1]), p
         assert torch.equal(dq[600:], base[0][600:])
         # control: with the folded forward but block-scaled dS and the token
         # view of K, rows of p's block before p may move, earlier blocks not
-        dq0, _, _ = _strict_step(w, tp, strict=False)
+        dq0, _, _ = _strict_step(w, tp, strict=False, dq_mode=dq_mode)
         blk = (p // 32) * 32
         assert torch.equal(dq0[:blk], plain[0][:blk]), p
         moved += int(not torch.equal(dq0[blk: p + 1], plain[0][blk: p + 1]))

@@ -1,7 +1,11 @@
 """Full-size workloads in the benchmark's launch configuration, checked on
 sampled (document, kv-head) units that the oracle computes whole: the GPU
 codes/scales of the unit bit-exact, and O, LSE, dQ, dK, dV of the unit within
-the parity bar.  Quantization groups never cross heads or documents, so the
+the parity bar against the Algorithm 1 oracle (the direct oracle's error is
+reported).  A gradient's max-abs bar is widened by the oracle's own movement
+when its saved fp32 LSE moves one ulp (zero on rows of moderate scores; about
+3e-2 on a head whose x50 outlier channels coincide in Q and K, where the
+scores span thousands of nats and the LSE ulp is about 1e-4).  Quantization groups never cross heads or documents, so the
 oracle quantizes just the unit's slice."""
 import math
 
@@ -12,7 +16,7 @@ import torch
 from block_scaled_mxfp8_gb300 import inputs as inp
 from oracle import oracle as orc
 
-from ._common import assert_close, metrics, to_np
+from ._common import check_outputs, lse_spread, to_np
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -37,7 +41,7 @@ def _gpu_run(w, dq_mode=0):
     return t, geo, v, (o, lse, dq, dk, dv)
 
 
-def _check_unit(w, t, v, outs, b, hk, grad_cos=None):
+def _check_unit(w, t, v, outs, b, hk):
     """Oracle on document b, kv head hk (and its query heads)."""
     from block_scaled_mxfp8_gb300 import mxa
 
@@ -71,35 +75,30 @@ def _check_unit(w, t, v, outs, b, hk, grad_cos=None):
             assert np.array_equal(mxa.row_scales_logical(row.scales[hs, tb:tb + nt].contiguous(), [n], w.d), rs), k
             assert np.array_equal(mxa.tok_scales_logical(tok.scales[hs, tb:tb + nt].contiguous(), [n], w.d), ts), k
             deq[k] = (orc.dequant_row(rc, rs), orc.dequant_tok(tc, ts, cu))
-    r = orc.attn_bwd(deq["q"][0], deq["k"][0], deq["v"][1], deq["v"][0], deq["do"][0], deq["q"][1], deq["k"][1],
-                     deq["do"][1], cu, w.causal, 1.0 / math.sqrt(w.d))
+    args = (deq["q"][0], deq["k"][0], deq["v"][1], deq["v"][0], deq["do"][0], deq["q"][1], deq["k"][1], deq["do"][1],
+            cu, w.causal, 1.0 / math.sqrt(w.d))
+    r = orc.attn_bwd_alg1(*args)
+    moved = [orc.attn_bwd_alg1(*args, lse_ulps=k) for k in (-1, 1)]
+    rd = orc.attn_bwd(*args)
     got = {"O": to_np(o[s:s + n, hq]), "LSE": lse[hq, s:s + n].cpu().numpy().astype(np.float64),
            "dQ": to_np(dq[s:s + n, hq]), "dK": to_np(dk[s:s + n, hkv]), "dV": to_np(dv[s:s + n, hkv])}
-    for name in ("O", "dQ", "dK", "dV"):
-        print(w.name, "doc", b, "kvhead", hk, name, metrics(got[name], r[name]))
-    for name in ("O", "dQ", "dK", "dV"):
-        if name != "O" and grad_cos is not None:
-            assert_close(name, got[name], r[name], cos_min=grad_cos, frac=0.15)
-        else:
-            assert_close(name, got[name], r[name])
-    lerr = float(np.abs(got["LSE"] - r["LSE"]).max())
-    assert lerr <= 1e-3 * max(1.0, float(np.abs(r["LSE"]).max())), lerr
+    check_outputs("%s doc %d kvhead %d" % (w.name, b, hk), got, r, rd, spread=lse_spread(r, moved))
 
 
 @pytest.mark.parametrize("causal", [False, True])
 def test_llm_shape_b8_h32_l4096(causal):
+    """The x50-outlier workload, forward and backward, on eight sampled
+    (sequence, head) units spread over the batch and the heads."""
     w = inp.workload("llm", causal=causal)
     t, geo, v, outs = _gpu_run(w)
-    # Parity for this workload is specified on the forward (O, LSE).  Its
-    # backward is checked with a looser bar: with x50 outlier channels the
-    # dQ error is dominated by D = G . O taken from the forward's
-    # quantized-P output, as the method prescribes.
-    for b, hk in ((0, 0), (5, 17)):
-        _check_unit(w, t, v, outs, b, hk, grad_cos=0.995)
+    for b, hk in ((0, 0), (1, 31), (2, 9), (3, 22), (4, 4), (5, 17), (6, 13), (7, 28)):
+        _check_unit(w, t, v, outs, b, hk)
 
 
-@pytest.mark.parametrize("dq_mode", [0, 1])
+@pytest.mark.parametrize("dq_mode", [0, 1, 2])
 def test_train_shape_b4_h16_l8192_causal(dq_mode):
+    """FP32, FP16 x 2^9 and FP16 per-row-boost dQ accumulation at the
+    training shape."""
     w = inp.workload("train")
     t, geo, v, outs = _gpu_run(w, dq_mode)
     _check_unit(w, t, v, outs, 3, 9)
