@@ -353,15 +353,19 @@ mxa_status mxa_bwd(const mxa_bwd_params* p, void* workspace, size_t ws_bytes, cu
  * Same arguments, results and status codes as mxa_bwd, computed the same way;
  * the workspace is a file-scope device array of MXA_BWD_NOALLOC_MAX_WORKSPACE
  * bytes that the library owns (held on every GPU that loads the library until
- * the process exits).  Calls whose mxa_bwd_workspace_min_bytes() exceeds it
- * are rejected with MXA_ERR_WORKSPACE before any work; FP32-mode calls need
- * 2 * Hq * ntiles * 512 bytes (B8 H32 L4096: 8 MiB) and take the fast dQ path
- * only when their full mxa_bwd_workspace_bytes() also fits; FP16_X512 calls
- * also need the emitted dS or the fp16 dQ accumulator, so only small ones
- * fit.
- * The device address of the array is resolved on the first call made with a
- * given device current (cudaGetSymbolAddress); make that first call before
- * any stream capture.  The function allocates nothing.  Every call on a device
+ * the process exits).  A call whose mxa_bwd_workspace_min_bytes() exceeds it
+ * gets mxa_bwd's own argument checks and then MXA_ERR_WORKSPACE, with no
+ * work launched.  FP32-mode calls need the D and LSE rows (2 * Hq * ntiles *
+ * 512 bytes) plus, for packed or cross-attention inputs, the tile lists (16
+ * bytes per scale tile and side, plus 256): B8 H32 L4096 needs 8 MiB; they
+ * take the fast dQ path only when their full mxa_bwd_workspace_bytes() also
+ * fits, else they form dS again in the dQ kernel.  The FP16 modes and the
+ * strict dQ operand (k_key) also need the emitted dS or the fp16 dQ
+ * accumulator, so only small calls fit.
+ * Every call looks up the array's device address on the current device
+ * (cudaGetSymbolAddress, which allocates nothing); the first call on a
+ * device also loads the library's kernels there, so make it before any
+ * stream capture.  The function allocates nothing.  Every call on a device
  * shares the one array and it keeps the last call's contents (each call
  * rewrites what it reads); calls that overlap on the GPU -- on different
  * streams, or from several threads -- race on it and must be serialized by

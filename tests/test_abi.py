@@ -170,6 +170,32 @@ def test_fwd_bwd_reject_bad_arguments_without_launch(lib):
     assert L.mxa_bwd(ctypes.byref(bp), ctypes.c_void_p(256), full2, None) == mxa.MXA_ERR_ARG
 
 
+def test_noalloc_gives_mxa_bwd_status_codes_without_launch(lib):
+    """mxa_bwd_noalloc returns the status mxa_bwd gives the same arguments
+    (its argument checks run first, before any device call), and
+    MXA_ERR_WORKSPACE for a valid call too large for its scratch array."""
+    L = lib
+    big = mxa.c_shape(1 << 16, 8, 8, 128, None, 1, 1 << 16, (1 << 16) // 128, 1, 0.0)
+    small = mxa.c_shape(256, 2, 2, 128, None, 1, 256, 2, 1, 0.0)
+    for sh in (big, small):
+        bp = mxa.c_bwd_params(sh, *[_qv()] * 7, 256, 256, 256, 256, 256, 0)
+        bp.dq = None
+        assert L.mxa_bwd_noalloc(ctypes.byref(bp), None) == mxa.MXA_ERR_ARG
+        bp.dq = 256
+        bp.dq_mode = 7
+        assert L.mxa_bwd_noalloc(ctypes.byref(bp), None) == mxa.MXA_ERR_ARG
+        bp.dq_mode = 0
+        bp.o = 8
+        assert L.mxa_bwd_noalloc(ctypes.byref(bp), None) == mxa.MXA_ERR_ALIGN
+    bad_d = mxa.c_shape(256, 2, 2, 96, None, 1, 256, 2, 1, 0.0)
+    bp = mxa.c_bwd_params(bad_d, *[_qv()] * 7, 256, 256, 256, 256, 256, 0)
+    assert L.mxa_bwd_noalloc(ctypes.byref(bp), None) == mxa.MXA_ERR_UNSUPPORTED
+    assert L.mxa_bwd_noalloc(None, None) == mxa.MXA_ERR_ARG
+    bp = mxa.c_bwd_params(big, *[_qv()] * 7, 256, 256, 256, 256, 256, mxa.MXA_DQ_FP16_X512)
+    assert L.mxa_bwd_workspace_min_bytes(ctypes.byref(bp)) > mxa.MXA_BWD_NOALLOC_MAX_WORKSPACE
+    assert L.mxa_bwd_noalloc(ctypes.byref(bp), None) == mxa.MXA_ERR_WORKSPACE
+
+
 def test_cross_attention_shape_checks(lib):
     """Cross-attention (T_k > 0): no causal mask, FP32 dQ only, equal key
     documents must divide T_k; the list sizes follow each side's NT."""
