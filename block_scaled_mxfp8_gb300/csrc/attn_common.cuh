@@ -80,11 +80,12 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-// Bounded wait used by every warp role: gives up after kWaitBudgetCycles,
-// records `code` in the device error word and raises the CTA's abort flag;
-// returns early (false) once another role has raised it.
+// Bounded wait used by every warp role: gives up after `budget` SM cycles
+// (kWaitBudgetCycles in every kernel), records `code` in the device error
+// word and raises the CTA's abort flag; returns early (false) once another
+// role has raised it.
 __device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
-                                          int code) {
+                                          int code, long long budget = kWaitBudgetCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   long long t0 = clock64();
   uint32_t it = 0;
@@ -92,7 +93,7 @@ __device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait(bar, parity)) return true;
     if ((++it & 255u) == 0) {
       if (*abort_flag) return false;
-      if (clock64() - t0 > kWaitBudgetCycles) {
+      if (clock64() - t0 > budget) {
         *abort_flag = 1;
         if (err) atomicCAS(err, 0, code);
         return false;

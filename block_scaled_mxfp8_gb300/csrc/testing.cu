@@ -2,6 +2,7 @@
 // quantize P and dS inside the attention kernels, run on caller data.
 #include "../../include/mxa_testing.h"
 #include "attn_common.cuh"
+#include "kernels.cuh"
 
 namespace mxa {
 namespace {
@@ -30,8 +31,32 @@ __global__ void test_ds_kernel(const float* x, int nblocks, int shift, uint8_t* 
   if (lane == 0) scales[blk] = static_cast<uint8_t>(sb);
 }
 
+// One warp waits, through the kernels' own bounded wait, on an mbarrier that
+// nothing arrives on.  Nothing asynchronous is in flight (no bulk copy, no
+// MMA, no tensor memory), so when the budget runs out the warp records the
+// error word and returns.
+__global__ void test_wait_kernel(long long budget, int* err) {
+  __shared__ uint64_t bar;
+  __shared__ int s_abort;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  __syncwarp();
+  role_wait(&bar, 0, &s_abort, err, kErrTimeoutOther, budget);
+}
+
 }  // namespace
 }  // namespace mxa
+
+extern "C" mxa_status mxa_test_wait_timeout(long long budget_cycles, cudaStream_t stream) {
+  if (budget_cycles < 0 || budget_cycles > (1ll << 31)) return MXA_ERR_ARG;
+  int* err = mxa::device_error_word();
+  if (!err) return MXA_ERR_CUDA;
+  mxa::test_wait_kernel<<<1, 32, 0, stream>>>(budget_cycles, err);
+  return cudaGetLastError() == cudaSuccess ? MXA_OK : MXA_ERR_CUDA;
+}
 
 extern "C" mxa_status mxa_test_e4m3(const float* x, int64_t n, uint8_t* codes, cudaStream_t stream) {
   if (!x || !codes || n < 0 || (n & 3)) return MXA_ERR_ARG;

@@ -101,7 +101,7 @@ EXPORTS = [
     "mxa_bwd_noalloc", "mxa_get_error",
 ]
 # include/mxa_testing.h: the kernels' P and dS quantization run on caller data
-EXPORTS_TESTING = ["mxa_test_e4m3", "mxa_test_ds_blocks"]
+EXPORTS_TESTING = ["mxa_test_e4m3", "mxa_test_ds_blocks", "mxa_test_wait_timeout"]
 MXA_BWD_NOALLOC_MAX_WORKSPACE = 32 * 1024 * 1024
 
 
@@ -151,6 +151,8 @@ def lib():
         L.mxa_test_e4m3.argtypes = [P, i64, P, P]
         L.mxa_test_ds_blocks.restype = i32
         L.mxa_test_ds_blocks.argtypes = [P, i32, i32, P, P, P]
+        L.mxa_test_wait_timeout.restype = i32
+        L.mxa_test_wait_timeout.argtypes = [ctypes.c_longlong, P]
         _lib = L
     return _lib
 
@@ -240,6 +242,12 @@ def mxa_test_e4m3(x: torch.Tensor, codes: torch.Tensor, stream=None) -> int:
 def mxa_test_ds_blocks(x: torch.Tensor, shift: int, codes: torch.Tensor, scales: torch.Tensor, stream=None) -> int:
     """include/mxa_testing.h: the kernels' 32 x 32 dS block quantization of x [nblocks, 32, 32]."""
     return lib().mxa_test_ds_blocks(_ptr(x), x.shape[0], shift, _ptr(codes), _ptr(scales), _stream(stream))
+
+
+def mxa_test_wait_timeout(budget_cycles: int, stream=None) -> int:
+    """include/mxa_testing.h: the kernels' bounded wait, run out on purpose
+    (a barrier nothing arrives on) with a short budget."""
+    return lib().mxa_test_wait_timeout(int(budget_cycles), _stream(stream))
 
 
 def mxa_get_error(stream=None) -> int:

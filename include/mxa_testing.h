@@ -42,6 +42,16 @@ mxa_status mxa_test_e4m3(const float* x, int64_t n, uint8_t* codes, cudaStream_t
 mxa_status mxa_test_ds_blocks(const float* x, int nblocks, int shift, uint8_t* codes, uint8_t* scales,
                               cudaStream_t stream);
 
+/* Run the attention kernels' bounded wait (the one every warp role uses) in
+ * a one-warp kernel, on a barrier that nothing arrives on, with a spin budget
+ * of budget_cycles SM clocks instead of the kernels' two seconds.  Nothing
+ * asynchronous is in flight, so the wait runs out, records the device error
+ * word and the kernel returns: the next mxa_get_error() reports
+ * MXA_ERR_TIMEOUT and clears the word.  This exercises the timeout report of
+ * mxa.h's error contract without stalling any real work.  Status: MXA_OK,
+ * MXA_ERR_ARG (budget outside [0, 2^31]), MXA_ERR_CUDA. */
+mxa_status mxa_test_wait_timeout(long long budget_cycles, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
