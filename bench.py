@@ -199,9 +199,9 @@ def oracle_sample(L=4096, H=1, d=128, causal=False, seed=1002):
         tc, ts = orc.quant_tok(t[k])
         v[k] = (orc.dequant_row(rc, rs), orc.dequant_tok(tc, ts))
     alpha = 1.0 / math.sqrt(d)
-    orc.attn_fwd(v["q"][0], v["k"][0], v["v"][1], None, causal, alpha)
-    orc.attn_bwd(v["q"][0], v["k"][0], v["v"][1], v["v"][0], v["do"][0], v["q"][1], v["k"][1], v["do"][1],
-                 None, causal, alpha)
+    orc.attn_fwd_alg1(v["q"][0], v["k"][0], v["v"][1], None, causal, alpha)
+    orc.attn_bwd_alg1(v["q"][0], v["k"][0], v["v"][1], v["v"][0], v["do"][0], v["q"][1], v["k"][1], v["do"][1],
+                      None, causal, alpha)
     dt = time.perf_counter() - t0
     ff, fb = flops(1, H, L, d, causal)
     return dt, ff + fb, orc.num_threads()
@@ -224,9 +224,9 @@ def oracle_sample_cross(Lq=512, Lk=8192, H=1, d=128, seed=1006):
         tc, ts = orc.quant_tok(t[k], cu)
         v[k] = (orc.dequant_row(rc, rs), orc.dequant_tok(tc, ts, cu))
     alpha = 1.0 / math.sqrt(d)
-    orc.attn_fwd_x(v["q"][0], v["k"][0], v["v"][1], cq, ck, alpha)
-    orc.attn_bwd_x(v["q"][0], v["k"][0], v["v"][1], v["v"][0], v["do"][0], v["q"][1], v["k"][1], v["do"][1],
-                   cq, ck, alpha)
+    orc.attn_fwd_alg1(v["q"][0], v["k"][0], v["v"][1], cq, False, alpha, cu_k=ck)
+    orc.attn_bwd_alg1(v["q"][0], v["k"][0], v["v"][1], v["v"][0], v["do"][0], v["q"][1], v["k"][1], v["do"][1],
+                      cq, False, alpha, cu_k=ck)
     dt = time.perf_counter() - t0
     ff, fb = flops(1, H, Lq, d, False, [Lq], [Lk])
     return dt, ff + fb, orc.num_threads()
@@ -413,7 +413,7 @@ def run_gpu(args):
     sm_mhz = clk.summary().get("sm_mhz") or 2070.0
     micro_tflops = MXFP8_MMA_FLOP_PER_SM_CLK * GB300_SMS * sm_mhz * 1e6 / 1e12
     # DRAM bytes of the backward call's dK/dV and dQ kernels from one ncu
-    # capture at B2 (profiles/ncu_full_b2h32l4096_attention_kernels.md),
+    # capture at B2 (the --set full capture of the attention kernels),
     # scaled by the tile pairs (B / 2); only for the workload it was taken on
     traffic = None
     if w.name == "llm" and not w.causal and not args.dq_mode and w.lengths is None:
