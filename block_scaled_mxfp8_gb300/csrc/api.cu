@@ -243,9 +243,19 @@ mxa_status quantize_impl(const void* x, int64_t T, int H, int d, const int32_t* 
     }
   }
   if (T == 0) return MXA_OK;
-  const size_t sbytes = mxa_scale_bytes(H, ntiles);
-  if ((w_row || tokblock) && cudaMemsetAsync(row->scales, 0x7F, sbytes, stream) != cudaSuccess) return MXA_ERR_CUDA;
-  if ((w_tok || tokblock) && cudaMemsetAsync(tok->scales, 0x7F, sbytes, stream) != cudaSuccess) return MXA_ERR_CUDA;
+  // The plain MX32 kernel writes every byte of the scale atoms it owns
+  // (padding included); atoms no CTA owns exist only when ntiles exceeds the
+  // documents' tiles (an upper bound), which the host can rule out for equal
+  // documents only.  Every other call fills the layouts with 0x7F first.
+  const bool plain = !tokblock && !rms;
+  const bool exact_nt = !cu_seqlens && ntiles == static_cast<int64_t>(num_docs) * ((T / num_docs + 127) / 128);
+  if (!(plain && exact_nt)) {
+    const size_t sbytes = mxa_scale_bytes(H, ntiles);
+    if ((w_row || tokblock) && cudaMemsetAsync(row->scales, 0x7F, sbytes, stream) != cudaSuccess)
+      return MXA_ERR_CUDA;
+    if ((w_tok || tokblock) && cudaMemsetAsync(tok->scales, 0x7F, sbytes, stream) != cudaSuccess)
+      return MXA_ERR_CUDA;
+  }
   QuantArgs a{};
   a.x = x;
   a.T = T;

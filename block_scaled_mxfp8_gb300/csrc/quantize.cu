@@ -13,11 +13,14 @@
 //               a normalized 128-point Hadamard rotation of each token.
 // Scale rule: e = ceil(log2(amax / 448)) (FLAMIA notes sec. 4), computed
 // exactly from the fp32 bits; codes are cvt.rn.satfinite E4M3 of x * 2^-e.
-// Group max-abs: within a token row by warp shuffles; along tokens by warp
-// shuffles then one shared-memory pass across warps.
+// Group max-abs, plain MX32 views (quantize_mx_kernel): in registers, one
+// warp per 32-token group.  RMSNorm and token-block variants
+// (quantize_kernel): within a token row by warp shuffles; along tokens by
+// warp shuffles then one shared-memory pass across warps.
 // Memory-bound: 2 B read + (1 + 1/32) B written per element per view.
 #include <cuda_bf16.h>
 
+#include "attn_common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -292,6 +295,159 @@ __global__ void __launch_bounds__(QCfg<D>::kThreads) quantize_kernel(QuantArgs a
   }  // 32-token groups
 }
 
+// ------------------------------------------------------- MX32, ROW/TOK views
+// The plain MX32 path (no RMSNorm, no token blocks), laid out so that both
+// group maxima stay in registers: one CTA per (head, 128-token tile,
+// document), one warp per 32-token group.  Lane l holds channels [8 c, 8 c + 8),
+// c = l % LPR, of the group's tokens l / LPR + k RPI (k < TPL): a warp-wide
+// 16-byte load covers RPI whole token rows, so loads and stores stay
+// coalesced.  Pass 1, the maxima: TOK view, per channel over the group, a
+// register loop over the lane's TPL tokens on the bf16 bit patterns (two
+// channels per halfword max) plus one or two shuffles across the lanes of
+// the same channels; ROW view, per token over 32 channels, the lane's 8
+// channels plus two shuffles (the 4 lanes of the 32-channel group), two
+// tokens per shuffled word.  Pass 2, one token at a time: its 8 values are
+// unpacked once and scaled (packed fp32x2 multiplies by powers of two) into
+// both views.  No shared memory, no block barrier after the tile base; all
+// TPL loads are issued before any arithmetic.  Every byte of the CTA's scale
+// atoms is written, padding included (0x7F: rows past the document end, the
+// groups and rows beyond d = 64).
+template <int D>
+__global__ void __launch_bounds__(128, 5) quantize_mx_kernel(QuantArgs a) {
+  constexpr int LPR = D / 8;     // lanes per token row
+  constexpr int RPI = 32 / LPR;  // token rows per warp load
+  constexpr int TPL = 32 / RPI;  // tokens per lane
+  __shared__ int64_t s_tile_base;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cl = lane % LPR, rl = lane / LPR;
+  // head fastest: CTAs that run together read and write whole token rows
+  // (all heads of a token are contiguous) instead of 8 KB-strided pieces
+  const int h = blockIdx.x, tile = blockIdx.y, b = blockIdx.z;
+  int64_t doc_start, doc_len;
+  doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, doc_len);
+  if (static_cast<int64_t>(tile) * 128 >= doc_len) return;
+  const int64_t tok0 = static_cast<int64_t>(tile) * 128 + warp * 32;  // the group's first token (document-relative)
+
+  uint4 raw[TPL];
+#pragma unroll
+  for (int k = 0; k < TPL; ++k) {
+    const int64_t pos = tok0 + rl + k * RPI;
+    raw[k] = pos < doc_len ? __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.x) +
+                                                                  ((doc_start + pos) * a.H + h) * D + cl * 8))
+                           : make_uint4(0u, 0u, 0u, 0u);
+  }
+
+  // first scale tile of this document
+  if (a.cu_seqlens == nullptr) {
+    if (tid == 0) s_tile_base = static_cast<int64_t>(b) * ((doc_len + 127) / 128);
+  } else {
+    int64_t part = 0;
+    for (int i = tid; i < b; i += 128) part += (a.cu_seqlens[i + 1] - a.cu_seqlens[i] + 127) / 128;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (tid == 0) s_tile_base = 0;
+    __syncthreads();
+    if (lane == 0 && part) atomicAdd(reinterpret_cast<unsigned long long*>(&s_tile_base), static_cast<unsigned long long>(part));
+  }
+  __syncthreads();
+  const int64_t atom_base = (static_cast<int64_t>(h) * a.ntiles + s_tile_base + tile) * kAtomBytes;
+
+  // ---- pass 1: TOK view channel maxima -> this lane's 8 channel scales
+  uint64_t sct[4];  // (2^-e of channel 2 i, 2^-e of channel 2 i + 1) as fp32x2
+  if (a.write_tok) {
+    uint32_t m[4] = {0u, 0u, 0u, 0u};  // |x| patterns, channels (2 i, 2 i + 1) of the chunk
+#pragma unroll
+    for (int k = 0; k < TPL; ++k) {
+      m[0] = __vmaxu2(m[0], raw[k].x & 0x7FFF7FFFu);
+      m[1] = __vmaxu2(m[1], raw[k].y & 0x7FFF7FFFu);
+      m[2] = __vmaxu2(m[2], raw[k].z & 0x7FFF7FFFu);
+      m[3] = __vmaxu2(m[3], raw[k].w & 0x7FFF7FFFu);
+    }
+#pragma unroll
+    for (int o = LPR; o < 32; o <<= 1) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m[i] = __vmaxu2(m[i], __shfl_xor_sync(0xffffffffu, m[i], o));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e0 = mx_exponent_bits(m[i] << 16), e1 = mx_exponent_bits(m[i] & 0xFFFF0000u);
+      sct[i] = f2_pack(exp2i_neg(e0), exp2i_neg(e1));
+      if (rl == 0) {
+        a.tok_scales[atom_base + atom_offset(cl * 8 + 2 * i, warp)] = static_cast<uint8_t>(e0 + 127);
+        a.tok_scales[atom_base + atom_offset(cl * 8 + 2 * i + 1, warp)] = static_cast<uint8_t>(e1 + 127);
+        if (D < 128) {  // atom rows D .. 127 are padding
+          a.tok_scales[atom_base + atom_offset(D + cl * 8 + 2 * i, warp)] = 0x7F;
+          a.tok_scales[atom_base + atom_offset(D + cl * 8 + 2 * i + 1, warp)] = 0x7F;
+        }
+      }
+    }
+  }
+  // ---- pass 1: ROW view token maxima, two tokens per word
+  uint32_t pk[TPL / 2];
+  if (a.write_row) {
+#pragma unroll
+    for (int k = 0; k < TPL; k += 2) {
+      uint32_t t2[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint4 r = raw[k + j];
+        const uint32_t w = __vmaxu2(__vmaxu2(r.x & 0x7FFF7FFFu, r.y & 0x7FFF7FFFu),
+                                    __vmaxu2(r.z & 0x7FFF7FFFu, r.w & 0x7FFF7FFFu));
+        t2[j] = max(w & 0xFFFFu, w >> 16);
+      }
+      pk[k / 2] = t2[0] | (t2[1] << 16);
+    }
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {  // the 4 lanes of the 32-channel group
+#pragma unroll
+      for (int k = 0; k < TPL / 2; ++k) pk[k] = __vmaxu2(pk[k], __shfl_xor_sync(0xffffffffu, pk[k], o));
+    }
+  }
+
+  // ---- pass 2: each token's 8 values once, into both views
+#pragma unroll
+  for (int k = 0; k < TPL; ++k) {
+    const int lt = rl + k * RPI;  // token inside the group
+    const int64_t pos = tok0 + lt;
+    const bool valid = pos < doc_len;
+    const int64_t off = ((doc_start + pos) * a.H + h) * D + cl * 8;
+    uint64_t x2[4];
+    x2[0] = f2_pack(bf16_lo(raw[k].x), bf16_hi(raw[k].x));
+    x2[1] = f2_pack(bf16_lo(raw[k].y), bf16_hi(raw[k].y));
+    x2[2] = f2_pack(bf16_lo(raw[k].z), bf16_hi(raw[k].z));
+    x2[3] = f2_pack(bf16_lo(raw[k].w), bf16_hi(raw[k].w));
+    if (a.write_tok && valid) {
+      float2 y[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) y[i] = f2_unpack(f2_mul(x2[i], sct[i]));
+      uint2 out;
+      out.x = pack_e4m3x4(y[0].x, y[0].y, y[1].x, y[1].y);
+      out.y = pack_e4m3x4(y[2].x, y[2].y, y[3].x, y[3].y);
+      *reinterpret_cast<uint2*>(a.tok_codes + off) = out;
+    }
+    if (a.write_row) {
+      const uint32_t mb = (k & 1) ? (pk[k / 2] & 0xFFFF0000u) : (pk[k / 2] << 16);
+      const int e = mx_exponent_bits(mb);
+      const float sc = exp2i_neg(e);
+      if (valid) {
+        const uint64_t sc2 = f2_pack(sc, sc);
+        float2 y[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) y[i] = f2_unpack(f2_mul(x2[i], sc2));
+        uint2 out;
+        out.x = pack_e4m3x4(y[0].x, y[0].y, y[1].x, y[1].y);
+        out.y = pack_e4m3x4(y[2].x, y[2].y, y[3].x, y[3].y);
+        *reinterpret_cast<uint2*>(a.row_codes + off) = out;
+      }
+      if ((cl & 3) == 0) {
+        uint8_t* rs = a.row_scales + atom_base + lt * 16 + warp * 4;
+        rs[cl / 4] = valid ? static_cast<uint8_t>(e + 127) : 0x7F;
+        if (D < 128) rs[cl / 4 + D / 32] = 0x7F;  // groups D / 32 .. 3 are padding
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------ per-key view
 // FLAMIA notes sec. 4 (moving the scale across the boundary): on the causal
 // diagonal tile each key's V row gets its own power-of-two scale, which the
@@ -369,6 +525,12 @@ cudaError_t launch_quantize_key(const KeyQuantArgs& a, int d, int max_seqlen, cu
 cudaError_t launch_quantize(const QuantArgs& a, int d, bool tokblock, bool hadamard, int max_groups,
                             cudaStream_t stream) {
   dim3 grid((max_groups + 3) / 4, a.num_docs, a.H);  // one CTA per 128-token tile
+  if (!tokblock && !a.rms) {  // the plain MX32 views: register-resident group maxima
+    const dim3 g2(a.H, (max_groups + 3) / 4, a.num_docs);
+    if (d == 128) quantize_mx_kernel<128><<<g2, 128, 0, stream>>>(a);
+    else quantize_mx_kernel<64><<<g2, 128, 0, stream>>>(a);
+    return cudaGetLastError();
+  }
   if (d == 128) {
     constexpr int nt = QCfg<128>::kThreads;
     if (tokblock && hadamard)

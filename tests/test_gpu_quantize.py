@@ -78,3 +78,58 @@ def test_quantize_padding_and_edge_values():
     assert np.array_equal(mxa.tok_scales_logical(tok.scales, [T], d), ts)
     # unused atom bytes hold 0x7F (d=128 uses all 4 groups; pad rows beyond T do not exist here)
     assert int(row.scales.cpu()[0, 0, mxa.atom_index(1, 0)]) == 127
+
+
+def _atom_images(rs, ts, lens, H, d, NT):
+    """The full [H, NT, 512] scale layouts expected from the logical scales:
+    every byte 0x7F except the (row, group) cells the layout documents
+    (include/mxa.h: row r, group g at (r % 32) * 16 + (r / 32) * 4 + g)."""
+    from block_scaled_mxfp8_gb300 import mxa
+
+    row = np.full((H, NT, 512), 0x7F, np.uint8)
+    tok = np.full((H, NT, 512), 0x7F, np.uint8)
+    t0 = tb = nb = 0
+    for n in lens:
+        for t in range(n):
+            for g in range(d // 32):
+                row[:, tb + t // 128, mxa.atom_index(t % 128, g)] = rs[t0 + t, :, g]
+        for blk in range((n + 31) // 32):
+            for c in range(d):
+                tok[:, tb + blk // 4, mxa.atom_index(c, blk % 4)] = ts[:, c, nb + blk]
+        t0 += n
+        tb += (n + 127) // 128
+        nb += (n + 31) // 32
+    return row, tok
+
+
+@pytest.mark.parametrize("case", [("batched_d64", None, 2, 200, 64), ("batched_d128", None, 3, 130, 128),
+                                  ("packed_d64", [1, 129, 40], 0, 0, 64)], ids=lambda c: c[0])
+def test_every_scale_byte_is_written(case):
+    """Scale buffers pre-filled with two different patterns come out
+    identical and equal, byte for byte, to the documented atom image (logical
+    scales from the oracle, 0x7F in every unused byte): the call writes every
+    byte of both layouts, whether its kernel fills the padding itself (equal
+    documents) or the layouts are filled first (packed documents)."""
+    from block_scaled_mxfp8_gb300 import mxa
+
+    name, lens, B, L, d = case
+    H = 3
+    w = (inp.make_custom(name, lengths=lens, Hq=H, Hkv=H, d=d, seed=15) if lens
+         else inp.make_custom(name, B=B, L=L, Hq=H, Hkv=H, d=d, seed=15))
+    t = inp.tensors(w, with_grad=False)
+    geo, _ = gpu_views(w, t, names=())
+    x = t["q"].cuda().contiguous()
+    outs = []
+    for fill in (0x00, 0xAB):
+        mk = lambda: mxa.QView(torch.zeros((w.T, H, d), dtype=torch.uint8, device="cuda"),
+                               torch.full((H, geo.ntiles, 512), fill, dtype=torch.uint8, device="cuda"))
+        row, tok = mxa.quantize(x, geo, out=(mk(), mk()))
+        torch.cuda.synchronize()
+        outs.append((row.scales.cpu().numpy(), tok.scales.cpu().numpy()))
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+    cu = w.cu_seqlens.numpy()
+    _, rs = orc.quant_row(t["q"])
+    _, ts = orc.quant_tok(t["q"], cu)
+    want_row, want_tok = _atom_images(rs, ts, w.doc_lengths, H, d, geo.ntiles)
+    assert np.array_equal(outs[0][0], want_row)
+    assert np.array_equal(outs[0][1], want_tok)
