@@ -39,11 +39,13 @@ UNIT = "PFLOP/s"
 # fp8/bf16 ratio (4.5 / 2.25 = 2); fallback 1.9 PFLOP/s bf16 burst.
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
-# tcgen05 kind::mxf8f6f4 block-scaled MMA (M=128, N=128 or 256, K=32) issued
-# back to back from a lean loop on every SM of a GB300: 16374 FLOP per SM
-# clock (N=128 in 64 clocks, N=256 in 128).  Scaled by the SM count and the
-# clock sampled during the timed region it gives the microbenchmark peak.
+# tcgen05 kind::mxf8f6f4 block-scaled MMA (M=128, N=256, K=32) issued back
+# to back on every SM (mxa_test_mma_rate, run by every bench): FLOP per SM
+# clock, scaled by the SM count and the clock sampled during the timed region,
+# gives the microbenchmark peak.  This value (measured on a GB300 at 2070 MHz)
+# is used only if the probe cannot run.
 MXFP8_MMA_FLOP_PER_SM_CLK = 16374.0
+PROBE_FLOP_PER_ITER = 4 * 2 * 128 * 256 * 32
 GB300_SMS = 152
 DQ_MODE_NAMES = {0: "FP32", 1: "FP16x2^9", 2: "FP16 per-row boost"}
 
@@ -323,6 +325,9 @@ def run_gpu(args):
             e[3].record(stream)
             rec.append(e)
 
+    # the block-scaled MMA rate of this GPU, measured before the timed region
+    probe = mma_probe(dev)
+
     for _ in range(args.warmup):
         step(x)
     torch.cuda.synchronize()
@@ -411,7 +416,8 @@ def run_gpu(args):
            "pflops": bwd_pf}
     peak_pf = pk["mxfp8_tflops"] / 1e3
     sm_mhz = clk.summary().get("sm_mhz") or 2070.0
-    micro_tflops = MXFP8_MMA_FLOP_PER_SM_CLK * GB300_SMS * sm_mhz * 1e6 / 1e12
+    probe_rate = probe["flop_per_sm_clk"] if probe else MXFP8_MMA_FLOP_PER_SM_CLK
+    micro_tflops = probe_rate * (probe["sms"] if probe else GB300_SMS) * sm_mhz * 1e6 / 1e12
     # DRAM bytes of the backward call's dK/dV and dQ kernels from one ncu
     # capture at B2 (the --set full capture of the attention kernels),
     # scaled by the tile pairs (B / 2); only for the workload it was taken on
@@ -426,6 +432,8 @@ def run_gpu(args):
                 # dense block-scaled MXFP8 rate of a back-to-back tcgen05.mma
                 # microbenchmark at the sampled SM clock
                 "mxfp8_microbench_tflops": round(micro_tflops, 1),
+                "mma_probe": probe if probe else "not run (the measured constant %.0f FLOP/SM/clk is used)" %
+                MXFP8_MMA_FLOP_PER_SM_CLK,
                 "frac_of_microbench": {"fwd": round(fwd_pf * 1e3 / micro_tflops, 4),
                                        "bwd": round(bwd_pf * 1e3 / micro_tflops, 4)}}
 
@@ -492,6 +500,15 @@ def run_gpu(args):
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3),
            "host_cpus": host_cpus}
 
+    # the quantizer of Q, K and V (both views) against HBM: 2 B read and
+    # (1 + 1/32) B written per element per view (padding scale bytes excluded)
+    q_elems = T * Hq * d + 2 * Tk * Hkv * d
+    q_bytes = q_elems * (2.0 + 2 * (1.0 + 1.0 / 32))
+    q_gbs = q_bytes / (ms_quant * 1e-3) / 1e9
+    quant_line = {"ms": round(ms_quant, 4), "bytes": int(q_bytes), "gbs": round(q_gbs, 1),
+                  "peak_gbs": pk["hbm_gbs"], "frac_hbm": round(q_gbs / pk["hbm_gbs"], 4),
+                  "what": "Q, K, V quantized, ROW and TOK views each, bf16 in"}
+
     out = {
         "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
@@ -510,6 +527,7 @@ def run_gpu(args):
         "ms": {"quantize_qkv": round(ms_quant, 3), "fwd": round(ms_fwd, 3), "quantize_do_plus_bwd": round(ms_bwd, 3),
                "bwd": round(ms_bwd_only, 3)},
         "roofline": roofline,
+        "quantize": quant_line,
         "rmsnorm_quantize": rms,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
@@ -570,6 +588,51 @@ def run_reference(args):
     }))
 
 
+def mma_probe(dev, iters=20000):
+    """Block-scaled MMA rate on every SM (include/mxa_testing.h): one warm-up
+    launch, then one timed launch with CUDA events.  Returns a dict with the
+    FLOP per SM clock (median over the CTAs' own clock counts) and the
+    PFLOP/s over the whole GPU (events)."""
+    import torch
+    from block_scaled_mxfp8_gb300 import mxa
+
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    cyc = torch.zeros(n_sm, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    if mxa.mxa_test_mma_rate(200, cyc, stream) != mxa.MXA_OK:
+        return None
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    st = mxa.mxa_test_mma_rate(iters, cyc, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    c = cyc.cpu().tolist()
+    if st != mxa.MXA_OK or mxa.mxa_get_error() != mxa.MXA_OK or min(c) <= 0:
+        return None
+    ms = e0.elapsed_time(e1)
+    fl = float(PROBE_FLOP_PER_ITER) * iters
+    return {"flop_per_sm_clk": round(fl / statistics.median(c), 1), "sms": n_sm, "iters": iters,
+            "pflops": round(fl * n_sm / (ms * 1e-3) / 1e15, 4), "ms": round(ms, 4),
+            "what": "tcgen05.mma kind::mxf8f6f4 block_scale, M128 N256 K32, E4M3, SS operands, one issuing "
+                    "thread per SM, back to back"}
+
+
+def run_mma_probe(args):
+    import torch
+
+    from block_scaled_mxfp8_gb300 import build as mbuild
+
+    mbuild.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    with ClockSampler(0) as clk:
+        r = mma_probe(dev)
+    if r is None:
+        raise SystemExit("mma probe failed")
+    r["clocks"] = clk.summary()
+    print(json.dumps({"mma_probe": r}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -585,9 +648,14 @@ def main():
                     help="strict causal attention: per-key V and K scales folded on the diagonal tile, "
                          "per-query dS scales for dQ")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling only)")
+    ap.add_argument("--mma-probe", action="store_true",
+                    help="only measure the block-scaled MMA rate (one GPU) and print it")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.mma_probe:
+        run_mma_probe(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -47,8 +47,88 @@ __global__ void test_wait_kernel(long long budget, int* err) {
   role_wait(&bar, 0, &s_abort, err, kErrTimeoutOther, budget);
 }
 
+// Block-scaled MMA rate: one thread per CTA issues `iters` groups of four
+// back-to-back MMAs of the forward's S shape (kind::mxf8f6f4, E4M3 x E4M3,
+// M = 128, N = 256, K = 4 x 32, A and B K-major with the 128-byte swizzle,
+// UE8M0 scales from TMEM), then waits for them; cycles[cta] = the SM clocks
+// from the first issue to the completion (-1 if the bounded wait ran out).
+// Operands are the E4M3 code of 1.0 with scale 1.0.  One CTA per SM (the
+// dynamic shared memory keeps a second one off the SM).
+constexpr int kProbeSmem = 48 * 1024 + 3 * 512 + 1024;
+constexpr int kProbeDynSmem = 120 * 1024;
+
+__global__ void __launch_bounds__(128, 1) test_mma_rate_kernel(int iters, long long* cycles, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_done;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  uint8_t* sA = smem;              // 128 rows x 128 B
+  uint8_t* sB = smem + 16384;      // 256 rows x 128 B
+  uint8_t* sSf = smem + 49152;     // A atom, two B atoms
+  for (int i = tid; i < 49152 / 16; i += 128)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+  for (int i = tid; i < 3 * 512 / 16; i += 128)
+    reinterpret_cast<uint4*>(sSf)[i] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  fence_proxy_async_smem();
+  if (tid == 0) {
+    mbar_init(&bar_done, 1);
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  if (tid == 0) {
+    const uint32_t tD = tmem, tSfA = tmem + 256, tSfB = tmem + 260;
+    const uint64_t dSf = atom_desc(sSf);
+    tmem_cp_desc(tSfA, dSf);
+    tmem_cp_desc(tSfB, sdesc_adv(dSf, 512));
+    tmem_cp_desc(tSfB + 4, sdesc_adv(dSf, 1024));
+    const uint64_t dA = make_sdesc(smem_u32(sA), 16, 1024, kSwz128);
+    const uint64_t dB = make_sdesc(smem_u32(sB), 16, 1024, kSwz128);
+    const long long t0 = clock64();
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_mxf8_ss(tD, sdesc_adv(dA, 32 * kk), sdesc_adv(dB, 32 * kk), make_idesc_mxf8(128, 256, 0, 0, kk, kk), tSfA,
+                    tSfB, (it > 0 || kk > 0) ? 1u : 0u);
+    }
+    mma_commit(&bar_done);
+    bool ok = role_wait(&bar_done, 0, &s_abort, err, kErrTimeoutMma);
+    const long long t1 = clock64();
+    if (!ok) mbar_wait(&bar_done, 0, nullptr, 0);  // the MMAs must be done before the TMEM is released
+    cycles[blockIdx.x] = ok ? t1 - t0 : -1;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 }  // namespace
 }  // namespace mxa
+
+extern "C" mxa_status mxa_test_mma_rate(int iters, int ctas, long long* cycles, cudaStream_t stream) {
+  if (iters <= 0 || iters > (1 << 24) || ctas <= 0 || ctas > 4096 || !cycles) return MXA_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(cycles) & 7) return MXA_ERR_ALIGN;
+  static_assert(mxa::kProbeSmem <= mxa::kProbeDynSmem, "probe operands fit the dynamic shared memory");
+  int* err = mxa::device_error_word();
+  if (!err) return MXA_ERR_CUDA;
+  if (cudaFuncSetAttribute(mxa::test_mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           mxa::kProbeDynSmem) != cudaSuccess)
+    return MXA_ERR_CUDA;
+  mxa::test_mma_rate_kernel<<<ctas, 128, mxa::kProbeDynSmem, stream>>>(iters, cycles, err);
+  return cudaGetLastError() == cudaSuccess ? MXA_OK : MXA_ERR_CUDA;
+}
 
 extern "C" mxa_status mxa_test_wait_timeout(long long budget_cycles, cudaStream_t stream) {
   if (budget_cycles < 0 || budget_cycles > (1ll << 31)) return MXA_ERR_ARG;

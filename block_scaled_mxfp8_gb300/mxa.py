@@ -101,7 +101,7 @@ EXPORTS = [
     "mxa_bwd_noalloc", "mxa_get_error",
 ]
 # include/mxa_testing.h: the kernels' P and dS quantization run on caller data
-EXPORTS_TESTING = ["mxa_test_e4m3", "mxa_test_ds_blocks", "mxa_test_wait_timeout"]
+EXPORTS_TESTING = ["mxa_test_e4m3", "mxa_test_ds_blocks", "mxa_test_wait_timeout", "mxa_test_mma_rate"]
 MXA_BWD_NOALLOC_MAX_WORKSPACE = 32 * 1024 * 1024
 
 
@@ -153,6 +153,8 @@ def lib():
         L.mxa_test_ds_blocks.argtypes = [P, i32, i32, P, P, P]
         L.mxa_test_wait_timeout.restype = i32
         L.mxa_test_wait_timeout.argtypes = [ctypes.c_longlong, P]
+        L.mxa_test_mma_rate.restype = i32
+        L.mxa_test_mma_rate.argtypes = [i32, i32, P, P]
         _lib = L
     return _lib
 
@@ -248,6 +250,13 @@ def mxa_test_wait_timeout(budget_cycles: int, stream=None) -> int:
     """include/mxa_testing.h: the kernels' bounded wait, run out on purpose
     (a barrier nothing arrives on) with a short budget."""
     return lib().mxa_test_wait_timeout(int(budget_cycles), _stream(stream))
+
+
+def mxa_test_mma_rate(iters: int, cycles: torch.Tensor, stream=None) -> int:
+    """include/mxa_testing.h: block-scaled MMA rate probe, one CTA per
+    element of cycles (int64, device)."""
+    assert cycles.dtype == torch.int64 and cycles.is_cuda
+    return lib().mxa_test_mma_rate(int(iters), cycles.numel(), _ptr(cycles), _stream(stream))
 
 
 def mxa_get_error(stream=None) -> int:

@@ -52,6 +52,20 @@ mxa_status mxa_test_ds_blocks(const float* x, int nblocks, int shift, uint8_t* c
  * MXA_ERR_ARG (budget outside [0, 2^31]), MXA_ERR_CUDA. */
 mxa_status mxa_test_wait_timeout(long long budget_cycles, cudaStream_t stream);
 
+/* Block-scaled MMA rate probe: `ctas` CTAs (one per SM; launch at most the
+ * SM count) each issue `iters` groups of four tcgen05.mma kind::mxf8f6f4
+ * block_scale instructions of the attention forward's S shape (M = 128,
+ * N = 256, K = 32 each, E4M3 operands in 128-byte-swizzled shared memory,
+ * UE8M0 scales in tensor memory) from one thread, back to back, then wait for
+ * them.  cycles (device, int64 [ctas], 8-byte aligned, caller-owned)
+ * receives each CTA's SM clocks from its first issue to completion, or -1 if
+ * its bounded wait ran out (then mxa_get_error() reports MXA_ERR_TIMEOUT).
+ * FLOP per CTA = iters * 4 * 2 * 128 * 256 * 32.  The attention kernels'
+ * tensor-core roofline is measured with it.  Status: MXA_OK, MXA_ERR_ARG
+ * (iters outside [1, 2^24], ctas outside [1, 4096], null cycles),
+ * MXA_ERR_ALIGN, MXA_ERR_CUDA. */
+mxa_status mxa_test_mma_rate(int iters, int ctas, long long* cycles, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
