@@ -298,23 +298,23 @@ __global__ void __launch_bounds__(QCfg<D>::kThreads) quantize_kernel(QuantArgs a
 // ------------------------------------------------------- MX32, ROW/TOK views
 // The plain MX32 path (no RMSNorm, no token blocks), laid out so that both
 // group maxima stay in registers: one CTA per (head, 128-token tile,
-// document), one warp per 32-token group.  Lane l holds channels [8 c, 8 c + 8),
-// c = l % LPR, of the group's tokens l / LPR + k RPI (k < TPL): a warp-wide
-// 16-byte load covers RPI whole token rows, so loads and stores stay
-// coalesced.  Pass 1, the maxima: TOK view, per channel over the group, a
-// register loop over the lane's TPL tokens on the bf16 bit patterns (two
-// channels per halfword max) plus one or two shuffles across the lanes of
-// the same channels; ROW view, per token over 32 channels, the lane's 8
-// channels plus two shuffles (the 4 lanes of the 32-channel group), two
-// tokens per shuffled word.  Pass 2, one token at a time: its 8 values are
-// unpacked once and scaled (packed fp32x2 multiplies by powers of two) into
-// both views.  No shared memory, no block barrier after the tile base; all
-// TPL loads are issued before any arithmetic.  Every byte of the CTA's scale
+// document), one warp per 32-token group.  Lane l holds channels
+// [16 c, 16 c + 16), c = l % LPR, of the group's tokens l / LPR + k RPI
+// (k < TPL): two warp-wide 16-byte loads cover RPI whole token rows, so loads
+// and the 16-byte code stores stay coalesced.  Pass 1, the maxima: TOK view,
+// per channel over the group, a register loop over the lane's TPL tokens on
+// the bf16 bit patterns (two channels per halfword max) plus shuffles across
+// the lanes of the same channels; ROW view, per token over 32 channels, the
+// lane's 16 channels plus one shuffle (the 2 lanes of the 32-channel group),
+// two tokens per shuffled word.  Pass 2, one token at a time: its 16 values
+// are unpacked once and scaled (packed fp32x2 multiplies by powers of two)
+// into both views.  No shared memory, no block barrier after the tile base;
+// all loads are issued before any arithmetic.  Every byte of the CTA's scale
 // atoms is written, padding included (0x7F: rows past the document end, the
 // groups and rows beyond d = 64).
 template <int D>
 __global__ void __launch_bounds__(128, 5) quantize_mx_kernel(QuantArgs a) {
-  constexpr int LPR = D / 8;     // lanes per token row
+  constexpr int LPR = D / 16;    // lanes per token row
   constexpr int RPI = 32 / LPR;  // token rows per warp load
   constexpr int TPL = 32 / RPI;  // tokens per lane
   __shared__ int64_t s_tile_base;
@@ -328,13 +328,18 @@ __global__ void __launch_bounds__(128, 5) quantize_mx_kernel(QuantArgs a) {
   if (static_cast<int64_t>(tile) * 128 >= doc_len) return;
   const int64_t tok0 = static_cast<int64_t>(tile) * 128 + warp * 32;  // the group's first token (document-relative)
 
-  uint4 raw[TPL];
+  uint4 raw[TPL][2];
 #pragma unroll
   for (int k = 0; k < TPL; ++k) {
     const int64_t pos = tok0 + rl + k * RPI;
-    raw[k] = pos < doc_len ? __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.x) +
-                                                                  ((doc_start + pos) * a.H + h) * D + cl * 8))
-                           : make_uint4(0u, 0u, 0u, 0u);
+    if (pos < doc_len) {
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.x) +
+                                                        ((doc_start + pos) * a.H + h) * D + cl * 16);
+      raw[k][0] = __ldg(src);
+      raw[k][1] = __ldg(src + 1);
+    } else {
+      raw[k][0] = raw[k][1] = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
 
   // first scale tile of this document
@@ -352,32 +357,36 @@ __global__ void __launch_bounds__(128, 5) quantize_mx_kernel(QuantArgs a) {
   __syncthreads();
   const int64_t atom_base = (static_cast<int64_t>(h) * a.ntiles + s_tile_base + tile) * kAtomBytes;
 
-  // ---- pass 1: TOK view channel maxima -> this lane's 8 channel scales
-  uint64_t sct[4];  // (2^-e of channel 2 i, 2^-e of channel 2 i + 1) as fp32x2
+  // ---- pass 1: TOK view channel maxima -> this lane's 16 channel scales
+  uint64_t sct[8];  // (2^-e of channel 2 i, 2^-e of channel 2 i + 1) as fp32x2
   if (a.write_tok) {
-    uint32_t m[4] = {0u, 0u, 0u, 0u};  // |x| patterns, channels (2 i, 2 i + 1) of the chunk
+    uint32_t m[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // |x| patterns, channels (2 i, 2 i + 1) of the lane
 #pragma unroll
     for (int k = 0; k < TPL; ++k) {
-      m[0] = __vmaxu2(m[0], raw[k].x & 0x7FFF7FFFu);
-      m[1] = __vmaxu2(m[1], raw[k].y & 0x7FFF7FFFu);
-      m[2] = __vmaxu2(m[2], raw[k].z & 0x7FFF7FFFu);
-      m[3] = __vmaxu2(m[3], raw[k].w & 0x7FFF7FFFu);
+      m[0] = __vmaxu2(m[0], raw[k][0].x & 0x7FFF7FFFu);
+      m[1] = __vmaxu2(m[1], raw[k][0].y & 0x7FFF7FFFu);
+      m[2] = __vmaxu2(m[2], raw[k][0].z & 0x7FFF7FFFu);
+      m[3] = __vmaxu2(m[3], raw[k][0].w & 0x7FFF7FFFu);
+      m[4] = __vmaxu2(m[4], raw[k][1].x & 0x7FFF7FFFu);
+      m[5] = __vmaxu2(m[5], raw[k][1].y & 0x7FFF7FFFu);
+      m[6] = __vmaxu2(m[6], raw[k][1].z & 0x7FFF7FFFu);
+      m[7] = __vmaxu2(m[7], raw[k][1].w & 0x7FFF7FFFu);
     }
 #pragma unroll
     for (int o = LPR; o < 32; o <<= 1) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) m[i] = __vmaxu2(m[i], __shfl_xor_sync(0xffffffffu, m[i], o));
+      for (int i = 0; i < 8; ++i) m[i] = __vmaxu2(m[i], __shfl_xor_sync(0xffffffffu, m[i], o));
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 8; ++i) {
       const int e0 = mx_exponent_bits(m[i] << 16), e1 = mx_exponent_bits(m[i] & 0xFFFF0000u);
       sct[i] = f2_pack(exp2i_neg(e0), exp2i_neg(e1));
       if (rl == 0) {
-        a.tok_scales[atom_base + atom_offset(cl * 8 + 2 * i, warp)] = static_cast<uint8_t>(e0 + 127);
-        a.tok_scales[atom_base + atom_offset(cl * 8 + 2 * i + 1, warp)] = static_cast<uint8_t>(e1 + 127);
+        a.tok_scales[atom_base + atom_offset(cl * 16 + 2 * i, warp)] = static_cast<uint8_t>(e0 + 127);
+        a.tok_scales[atom_base + atom_offset(cl * 16 + 2 * i + 1, warp)] = static_cast<uint8_t>(e1 + 127);
         if (D < 128) {  // atom rows D .. 127 are padding
-          a.tok_scales[atom_base + atom_offset(D + cl * 8 + 2 * i, warp)] = 0x7F;
-          a.tok_scales[atom_base + atom_offset(D + cl * 8 + 2 * i + 1, warp)] = 0x7F;
+          a.tok_scales[atom_base + atom_offset(D + cl * 16 + 2 * i, warp)] = 0x7F;
+          a.tok_scales[atom_base + atom_offset(D + cl * 16 + 2 * i + 1, warp)] = 0x7F;
         }
       }
     }
@@ -390,40 +399,40 @@ __global__ void __launch_bounds__(128, 5) quantize_mx_kernel(QuantArgs a) {
       uint32_t t2[2];
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const uint4 r = raw[k + j];
-        const uint32_t w = __vmaxu2(__vmaxu2(r.x & 0x7FFF7FFFu, r.y & 0x7FFF7FFFu),
-                                    __vmaxu2(r.z & 0x7FFF7FFFu, r.w & 0x7FFF7FFFu));
+        const uint4 r0 = raw[k + j][0], r1 = raw[k + j][1];
+        const uint32_t w = __vmaxu2(__vmaxu2(__vmaxu2(r0.x & 0x7FFF7FFFu, r0.y & 0x7FFF7FFFu),
+                                             __vmaxu2(r0.z & 0x7FFF7FFFu, r0.w & 0x7FFF7FFFu)),
+                                    __vmaxu2(__vmaxu2(r1.x & 0x7FFF7FFFu, r1.y & 0x7FFF7FFFu),
+                                             __vmaxu2(r1.z & 0x7FFF7FFFu, r1.w & 0x7FFF7FFFu)));
         t2[j] = max(w & 0xFFFFu, w >> 16);
       }
       pk[k / 2] = t2[0] | (t2[1] << 16);
     }
 #pragma unroll
-    for (int o = 1; o < 4; o <<= 1) {  // the 4 lanes of the 32-channel group
-#pragma unroll
-      for (int k = 0; k < TPL / 2; ++k) pk[k] = __vmaxu2(pk[k], __shfl_xor_sync(0xffffffffu, pk[k], o));
-    }
+    for (int k = 0; k < TPL / 2; ++k) pk[k] = __vmaxu2(pk[k], __shfl_xor_sync(0xffffffffu, pk[k], 1));
   }
 
-  // ---- pass 2: each token's 8 values once, into both views
+  // ---- pass 2: each token's 16 values once, into both views
 #pragma unroll
   for (int k = 0; k < TPL; ++k) {
     const int lt = rl + k * RPI;  // token inside the group
     const int64_t pos = tok0 + lt;
     const bool valid = pos < doc_len;
-    const int64_t off = ((doc_start + pos) * a.H + h) * D + cl * 8;
-    uint64_t x2[4];
-    x2[0] = f2_pack(bf16_lo(raw[k].x), bf16_hi(raw[k].x));
-    x2[1] = f2_pack(bf16_lo(raw[k].y), bf16_hi(raw[k].y));
-    x2[2] = f2_pack(bf16_lo(raw[k].z), bf16_hi(raw[k].z));
-    x2[3] = f2_pack(bf16_lo(raw[k].w), bf16_hi(raw[k].w));
-    if (a.write_tok && valid) {
-      float2 y[4];
+    const int64_t off = ((doc_start + pos) * a.H + h) * D + cl * 16;
+    const uint32_t wv[8] = {raw[k][0].x, raw[k][0].y, raw[k][0].z, raw[k][0].w,
+                            raw[k][1].x, raw[k][1].y, raw[k][1].z, raw[k][1].w};
+    uint64_t x2[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) y[i] = f2_unpack(f2_mul(x2[i], sct[i]));
-      uint2 out;
-      out.x = pack_e4m3x4(y[0].x, y[0].y, y[1].x, y[1].y);
-      out.y = pack_e4m3x4(y[2].x, y[2].y, y[3].x, y[3].y);
-      *reinterpret_cast<uint2*>(a.tok_codes + off) = out;
+    for (int i = 0; i < 8; ++i) x2[i] = f2_pack(bf16_lo(wv[i]), bf16_hi(wv[i]));
+    if (a.write_tok && valid) {
+      uint32_t q[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 y0 = f2_unpack(f2_mul(x2[2 * i], sct[2 * i]));
+        const float2 y1 = f2_unpack(f2_mul(x2[2 * i + 1], sct[2 * i + 1]));
+        q[i] = pack_e4m3x4(y0.x, y0.y, y1.x, y1.y);
+      }
+      *reinterpret_cast<uint4*>(a.tok_codes + off) = make_uint4(q[0], q[1], q[2], q[3]);
     }
     if (a.write_row) {
       const uint32_t mb = (k & 1) ? (pk[k / 2] & 0xFFFF0000u) : (pk[k / 2] << 16);
@@ -431,18 +440,19 @@ __global__ void __launch_bounds__(128, 5) quantize_mx_kernel(QuantArgs a) {
       const float sc = exp2i_neg(e);
       if (valid) {
         const uint64_t sc2 = f2_pack(sc, sc);
-        float2 y[4];
+        uint32_t q[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) y[i] = f2_unpack(f2_mul(x2[i], sc2));
-        uint2 out;
-        out.x = pack_e4m3x4(y[0].x, y[0].y, y[1].x, y[1].y);
-        out.y = pack_e4m3x4(y[2].x, y[2].y, y[3].x, y[3].y);
-        *reinterpret_cast<uint2*>(a.row_codes + off) = out;
+        for (int i = 0; i < 4; ++i) {
+          const float2 y0 = f2_unpack(f2_mul(x2[2 * i], sc2));
+          const float2 y1 = f2_unpack(f2_mul(x2[2 * i + 1], sc2));
+          q[i] = pack_e4m3x4(y0.x, y0.y, y1.x, y1.y);
+        }
+        *reinterpret_cast<uint4*>(a.row_codes + off) = make_uint4(q[0], q[1], q[2], q[3]);
       }
-      if ((cl & 3) == 0) {
+      if ((cl & 1) == 0) {
         uint8_t* rs = a.row_scales + atom_base + lt * 16 + warp * 4;
-        rs[cl / 4] = valid ? static_cast<uint8_t>(e + 127) : 0x7F;
-        if (D < 128) rs[cl / 4 + D / 32] = 0x7F;  // groups D / 32 .. 3 are padding
+        rs[cl / 2] = valid ? static_cast<uint8_t>(e + 127) : 0x7F;
+        if (D < 128) rs[cl / 2 + D / 32] = 0x7F;  // groups D / 32 .. 3 are padding
       }
     }
   }
