@@ -30,6 +30,13 @@ int* device_error_word() {
   return g_err_ptr[dev];
 }
 
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
 namespace {
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -379,6 +386,8 @@ mxa_status mxa_fwd(const mxa_fwd_params* p, cudaStream_t stream) {
     a.items = tile_list_items(p->workspace);
     a.item_count = static_cast<const int32_t*>(p->workspace);
   }
+  a.nq_tiles_doc = static_cast<int>((s.T / s.num_docs + 127) / 128);
+  a.nk_tiles_doc = static_cast<int>((ks.T / s.num_docs + 127) / 128);
   if (launch_fwd(a, maps, s.d, maxlen, stream) != cudaSuccess) return MXA_ERR_CUDA;
   return MXA_OK;
 }

@@ -189,18 +189,72 @@ __device__ __noinline__ FoldOut fold_keys(uint32_t tS, int col0, int lim, const 
   return out;
 }
 
+// One forward work item: a (document, 128-query tile, query head) and the
+// document's first scale tiles on the query and key sides.
+struct FwdItem {
+  int b, h, qt;
+  int64_t tile_base, ktile_base;
+};
+
+// Item v of a persistent launch: item v / Hq of the cost-sorted list for head
+// v % Hq, or the v-th (query tile, document, head) of equal documents --
+// query tiles fastest, so the CTAs running together share a head's K and V
+// tiles in L2, and the heaviest tiles first when causal.  False past the
+// last item.
+__device__ __forceinline__ bool fwd_item(const FwdArgs& a, int64_t v, FwdItem& it) {
+  if (a.items) {
+    const int64_t i = v / a.Hq;
+    if (i >= __ldg(a.item_count)) return false;
+    it.h = static_cast<int>(v - i * a.Hq);
+    const int4 e = __ldg(reinterpret_cast<const int4*>(a.items + i));
+    it.b = e.x;
+    it.qt = e.y;
+    it.tile_base = e.z;
+    it.ktile_base = e.w;
+    return true;
+  }
+  const int nqt = a.nq_tiles_doc;
+  if (v >= static_cast<int64_t>(nqt) * a.num_docs * a.Hq) return false;
+  const int qi = static_cast<int>(v % nqt);
+  const int64_t rest = v / nqt;
+  it.b = static_cast<int>(rest % a.num_docs);
+  it.h = static_cast<int>(rest / a.num_docs);
+  it.qt = a.causal ? nqt - 1 - qi : qi;
+  it.tile_base = static_cast<int64_t>(it.b) * nqt;
+  it.ktile_base = static_cast<int64_t>(it.b) * a.nk_tiles_doc;
+  return true;
+}
+
+// Geometry of one item.
+struct FwdGeo {
+  int hk, nk_tiles, n_it, dh;
+  int64_t doc_start, n, kdoc_start, nk;
+};
+__device__ __forceinline__ FwdGeo fwd_geo(const FwdArgs& a, const FwdItem& it) {
+  FwdGeo g;
+  g.hk = it.h / (a.Hq / a.Hkv);
+  doc_bounds(a.cu_seqlens, a.num_docs, a.T, it.b, g.doc_start, g.n);
+  doc_bounds(a.cu_k, a.num_docs, a.Tk, it.b, g.kdoc_start, g.nk);
+  g.nk_tiles = static_cast<int>((g.nk + 127) / 128);
+  // visible keys [0, nkeys), walked 256 at a time
+  const int64_t nkeys = a.causal ? min(g.nk, static_cast<int64_t>(it.qt + 1) * 128) : g.nk;
+  g.n_it = static_cast<int>((nkeys + 255) / 256);
+  g.dh = it.qt & 1;  // strict causal fold: the last iteration's half (qt % 2) is the diagonal tile
+  return g;
+}
+
 }  // namespace
 
-template <int D, bool FOLD>
+template <int D, bool FOLD, bool PERSIST>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdArgs a) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  __shared__ uint64_t bar_q, bar_k_full[C::kStages], bar_k_empty[C::kStages], bar_v_full[C::kStages],
-      bar_v_empty[C::kStages], bar_s_full, bar_s_empty, bar_p_full, bar_o_done, bar_drain, bar_drain2, bar_mx[2][4],
-      bar_lsum;
+  __shared__ uint64_t bar_q, bar_q_free, bar_k_full[C::kStages], bar_k_empty[C::kStages], bar_v_full[C::kStages],
+      bar_v_empty[C::kStages], bar_s_full, bar_s_empty, bar_p_full, bar_o_done, bar_o_free, bar_drain, bar_drain2,
+      bar_mx[2][4], bar_lsum;
   __shared__ float s_mx[2][4][128];  // [iteration parity][column quarter][row] partial row maxima
   __shared__ float s_l[4][128];      // [column quarter][row] partial row sums
   __shared__ uint32_t s_tmem;
@@ -208,33 +262,41 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   __shared__ int64_t s_slot, s_slot_k;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int b, h, qt;
-  int64_t tile_base = -1, ktile_base = -1;  // first scale tiles of the document: queries, keys
-  if (a.items) {
-    if (!list_item(a.items, a.item_count, a.Hq, b, h, qt, tile_base, ktile_base)) return;
+  // The CTA's items.  Persistent launches (a cost-sorted list, or equal
+  // documents) walk the items blockIdx.x, blockIdx.x + gridDim.x, ... --
+  // every role the same sequence, with each barrier's phase counted across
+  // items; packed documents without a list take one item per CTA from the
+  // max_seqlen grid (heaviest query tiles first when causal).
+  FwdItem item0;
+  if constexpr (PERSIST) {
+    if (!fwd_item(a, blockIdx.x, item0)) return;
   } else {
-    // heaviest query tiles first when causal
-    b = blockIdx.y;
-    h = blockIdx.z;
-    qt = a.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+    item0.b = blockIdx.y;
+    item0.h = blockIdx.z;
+    item0.qt = a.causal ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+    int64_t ds, dn, ks, kn;
+    doc_bounds(a.cu_seqlens, a.num_docs, a.T, item0.b, ds, dn);
+    doc_bounds(a.cu_k, a.num_docs, a.Tk, item0.b, ks, kn);
+    if (item0.qt >= static_cast<int>((dn + 127) / 128)) return;
+    item0.tile_base = doc_tile_base(a.cu_seqlens, item0.b, dn, tid, C::kThreads, &s_slot);
+    item0.ktile_base = (a.cu_k == a.cu_seqlens && a.Tk == a.T)
+                           ? item0.tile_base
+                           : doc_tile_base(a.cu_k, item0.b, kn, tid, C::kThreads, &s_slot_k);
   }
-  const int hk = h / (a.Hq / a.Hkv);
-  int64_t doc_start, n, kdoc_start, nk;  // the document's queries and keys (the same for self-attention)
-  doc_bounds(a.cu_seqlens, a.num_docs, a.T, b, doc_start, n);
-  doc_bounds(a.cu_k, a.num_docs, a.Tk, b, kdoc_start, nk);
-  const int nq_tiles = static_cast<int>((n + 127) / 128);
-  const int nk_tiles = static_cast<int>((nk + 127) / 128);
-  if (qt >= nq_tiles) return;
-  // visible keys [0, nkeys), walked 256 at a time
-  const int64_t nkeys = a.causal ? min(nk, static_cast<int64_t>(qt + 1) * 128) : nk;
-  const int n_it = static_cast<int>((nkeys + 255) / 256);
-  if (tile_base < 0) tile_base = doc_tile_base(a.cu_seqlens, b, n, tid, C::kThreads, &s_slot);
-  if (ktile_base < 0)
-    ktile_base = (a.cu_k == a.cu_seqlens && a.Tk == a.T) ? tile_base
-                                                          : doc_tile_base(a.cu_k, b, nk, tid, C::kThreads, &s_slot_k);
+  // the next item of this CTA after v (false at the end of the sequence):
+  // round k of gridDim.x items takes blockIdx.x, or gridDim.x - 1 -
+  // blockIdx.x when k is odd, so that each CTA pairs heavier and lighter
+  // items of a cost-sorted list
+  auto next_item = [&](int64_t& v, FwdItem& it) -> bool {
+    if constexpr (!PERSIST) return false;
+    const int64_t G = gridDim.x, k = v / G + 1;
+    v = k * G + ((k & 1) ? G - 1 - static_cast<int64_t>(blockIdx.x) : static_cast<int64_t>(blockIdx.x));
+    return fwd_item(a, v, it);
+  };
 
   if (tid == 0) {
     mbar_init(&bar_q, 1);
+    mbar_init(&bar_q_free, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bar_k_full[s], 1);
       mbar_init(&bar_k_empty[s], 1);
@@ -245,6 +307,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     mbar_init(&bar_s_empty, C::kSoftmaxThreads);
     mbar_init(&bar_p_full, C::kSoftmaxThreads);
     mbar_init(&bar_o_done, 1);
+    mbar_init(&bar_o_free, C::kSoftmaxThreads);
     mbar_init(&bar_drain, 1);
     mbar_init(&bar_drain2, 1);
     for (int q = 0; q < 4; ++q) {
@@ -263,9 +326,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     reinterpret_cast<uint4*>(smem + C::kOffOnes)[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
   for (int i = tid; i < kAtomBytes / 16; i += C::kThreads)
     reinterpret_cast<uint4*>(smem + C::kOffSfOne)[i] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-  // strict causal fold: the last iteration's half (qt % 2) is the diagonal tile
   const bool fold = FOLD && a.causal;
-  const int dh = qt & 1;
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -279,18 +340,33 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       tma_prefetch_desc(&maps.q);
       tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.v);
-      const int q0 = static_cast<int>(doc_start + static_cast<int64_t>(qt) * 128);
-      mbar_arrive_expect_tx(&bar_q, 128 * D + kAtomBytes);
-      tma_load_3d(smem + C::kOffQ, &maps.q, &bar_q, 0, h, q0);
-      bulk_load(smem + C::kOffSfQ, a.q_sf + ((static_cast<int64_t>(h) * a.ntiles + tile_base + qt) * kAtomBytes),
-                kAtomBytes, &bar_q);
       // K and V stream through separate rings: a K stage is released as soon
       // as its S MMA has completed, a V stage after its P V MMA, so the keys
-      // of later tiles are loaded well ahead of the P V chain.
-      int issued_k = 0, issued_v = 0;
+      // of later tiles -- and of the next item -- are loaded well ahead of
+      // the P V chain.  The next item's Q loads once the S MMAs of the
+      // previous item are done with Q.
+      uint32_t issued_k = 0, issued_v = 0;  // ring iterations, counted across items
+      int issued_q = 0;
       bool ok = true;
-      for (int j = 0; ok && j < n_it; ++j) {
-        const int s = j % C::kStages;
+      FwdItem itm = item0;
+      int64_t v_it = blockIdx.x;
+      do {
+        const FwdGeo G = fwd_geo(a, itm);
+        const int hk = G.hk, h = itm.h, qt = itm.qt, n_it = G.n_it, dh = G.dh, nk_tiles = G.nk_tiles;
+        const int64_t kdoc_start = G.kdoc_start, ktile_base = itm.ktile_base;
+        if (issued_q >= 1 &&
+            !(ok = role_wait(&bar_q_free, (issued_q - 1) & 1, abort_flag, a.err, kErrTimeoutTma)))
+          break;
+        const int q0 = static_cast<int>(G.doc_start + static_cast<int64_t>(qt) * 128);
+        mbar_arrive_expect_tx(&bar_q, 128 * D + kAtomBytes);
+        tma_load_3d(smem + C::kOffQ, &maps.q, &bar_q, 0, h, q0);
+        bulk_load(smem + C::kOffSfQ,
+                  a.q_sf + ((static_cast<int64_t>(h) * a.ntiles + itm.tile_base + qt) * kAtomBytes), kAtomBytes,
+                  &bar_q);
+        ++issued_q;
+        for (int j = 0; ok && j < n_it; ++j) {
+        const uint32_t gk = issued_k;
+        const int s = static_cast<int>(gk % C::kStages);
         const int t0 = 2 * j;  // first 128-key tile of this iteration
         // the second half may lie past the document: reuse the first half's
         // atoms then (its keys are masked; the scales just have to be finite)
@@ -298,8 +374,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         const int k0 = static_cast<int>(kdoc_start + static_cast<int64_t>(t0) * 128);
         const int64_t atom0 = (static_cast<int64_t>(hk) * a.ntiles_k + ktile_base + t0) * kAtomBytes;
         const int64_t atom1 = (static_cast<int64_t>(hk) * a.ntiles_k + ktile_base + t1) * kAtomBytes;
-        if (j >= C::kStages &&
-            !(ok = role_wait(&bar_k_empty[s], ((j / C::kStages) - 1) & 1, abort_flag, a.err, kErrTimeoutTma)))
+        if (gk >= C::kStages &&
+            !(ok = role_wait(&bar_k_empty[s], ((gk / C::kStages) - 1) & 1, abort_flag, a.err, kErrTimeoutTma)))
           break;
         uint8_t* sk = smem + C::kOffK + s * C::kKVBytes;
         uint8_t* sfk = smem + C::kOffSfK + s * 2 * kAtomBytes;
@@ -308,9 +384,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         tma_load_3d(sk + C::kHalfBytes, &maps.k, &bar_k_full[s], 0, hk, k0 + 128);
         bulk_load(sfk, a.k_sf + atom0, kAtomBytes, &bar_k_full[s]);
         bulk_load(sfk + kAtomBytes, a.k_sf + atom1, kAtomBytes, &bar_k_full[s]);
-        issued_k = j + 1;
-        if (j >= C::kStages &&
-            !(ok = role_wait(&bar_v_empty[s], ((j / C::kStages) - 1) & 1, abort_flag, a.err, kErrTimeoutTma)))
+        issued_k = gk + 1;
+        if (gk >= C::kStages &&
+            !(ok = role_wait(&bar_v_empty[s], ((gk / C::kStages) - 1) & 1, abort_flag, a.err, kErrTimeoutTma)))
           break;
         uint8_t* sv = smem + C::kOffV + s * C::kKVBytes;
         uint8_t* sfv = smem + C::kOffSfV + s * 2 * kAtomBytes;
@@ -320,13 +396,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         tma_load_3d(sv + C::kHalfBytes, (fold_it && dh == 1) ? &maps.vkey : &maps.v, &bar_v_full[s], 0, hk, k0 + 128);
         bulk_load(sfv, a.v_sf + atom0, kAtomBytes, &bar_v_full[s]);
         bulk_load(sfv + kAtomBytes, a.v_sf + atom1, kAtomBytes, &bar_v_full[s]);
-        issued_v = j + 1;
-      }
+        issued_v = gk + 1;
+        }
+      } while (ok && next_item(v_it, itm));
       // drain: every load issued must have landed before the CTA exits
-      role_wait(&bar_q, 0, abort_flag, nullptr, 0);
-      for (int j = (issued_k > C::kStages ? issued_k - C::kStages : 0); j < issued_k; ++j)
+      if (issued_q) role_wait(&bar_q, (issued_q - 1) & 1, abort_flag, nullptr, 0);
+      for (uint32_t j = (issued_k > C::kStages ? issued_k - C::kStages : 0); j < issued_k; ++j)
         mbar_wait(&bar_k_full[j % C::kStages], (j / C::kStages) & 1, nullptr, 0);
-      for (int j = (issued_v > C::kStages ? issued_v - C::kStages : 0); j < issued_v; ++j)
+      for (uint32_t j = (issued_v > C::kStages ? issued_v - C::kStages : 0); j < issued_v; ++j)
         mbar_wait(&bar_v_full[j % C::kStages], (j / C::kStages) & 1, nullptr, 0);
     }
   } else if (warp == 1) {
@@ -337,19 +414,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       const uint64_t dK0 = make_sdesc(smem_u32(smem + C::kOffK), 16, C::kSBO, C::kSwz);
       const uint64_t dSfK0 = atom_desc(smem + C::kOffSfK);
       const uint32_t tS = tmem + C::kColS, tSfQ = tmem + C::kColSfQ;
-      bool ok = role_wait(&bar_q, 0, abort_flag, a.err, kErrTimeoutMma);
-      if (ok) {
+      bool ok = true;
+      // S = Q K^T, 128 x 256, for ring iteration g (j: its index in the item)
+      auto issue_s = [&](uint32_t g, int j) -> bool {
+        const int s = static_cast<int>(g % C::kStages);
+        if (!role_wait(&bar_k_full[s], (g / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
+        if (g >= 1 && !role_wait(&bar_s_empty, (g - 1) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
         tc_fence_after();
-        tmem_cp_atom(tSfQ, smem + C::kOffSfQ);
-      }
-      auto issue_s = [&](int j) -> bool {  // S = Q K^T, 128 x 256
-        const int s = j % C::kStages;
-        if (!role_wait(&bar_k_full[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
-        if (j >= 1 && !role_wait(&bar_s_empty, (j - 1) & 1, abort_flag, a.err, kErrTimeoutMma)) return false;
-        tc_fence_after();
+        // the item's Q scales, once the previous S MMA (which read the
+        // previous item's) has completed and been read out
+        if (j == 0) tmem_cp_atom(tSfQ, smem + C::kOffSfQ);
         // K-scale slots alternate between two pairs of atoms (an S MMA may be
         // issued while the previous one is still in the pipe)
-        const uint32_t tSfK = tmem + C::kColSfK + 8 * (j & 1);
+        const uint32_t tSfK = tmem + C::kColSfK + 8 * static_cast<uint32_t>(g & 1);
         const uint64_t dsf = sdesc_adv(dSfK0, s * 2 * kAtomBytes);
         tmem_cp_desc(tSfK, dsf);
         tmem_cp_desc(tSfK + 4, sdesc_adv(dsf, kAtomBytes));
@@ -362,9 +439,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         mma_commit(&bar_k_empty[s]);
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j + 1 < n_it; ++j)
-        if (!(ok = issue_s(j + 1))) break;  // waits until S_j has been read out
+      uint32_t g = 0;
+      int n_items = 0;
+      FwdItem itm = item0;
+      int64_t v_it = blockIdx.x;
+      do {
+        const int n_it = fwd_geo(a, itm).n_it;
+        if (!(ok = role_wait(&bar_q, n_items & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        for (int j = 0; ok && j < n_it; ++j, ++g)
+          if (!(ok = issue_s(g, j))) break;  // waits until S_{g-1} has been read out
+        if (!ok) break;
+        mma_commit(&bar_q_free);  // this item's S MMAs are done with Q once they complete
+        ++n_items;
+      } while (next_item(v_it, itm));
       // drain this thread's MMAs before the TMEM is released
       mma_commit(&bar_drain);
       mbar_wait(&bar_drain, 0, nullptr, 0);
@@ -384,10 +471,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       const uint32_t tO = tmem + C::kColO, tP = tmem + C::kColP, tSfP = tmem + C::kColSfP, tSfPd = tmem + C::kColSfPd;
       const uint64_t dSfOne = atom_desc(smem + C::kOffSfOne);
       const uint32_t tSfVA = tmem + C::kColSfVA, tSfVB = tmem + C::kColSfVB;
-      for (int j = 0; j < n_it; ++j) {
-        const int s = j % C::kStages;
-        if (!role_wait(&bar_v_full[s], (j / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma)) break;
-        if (!role_wait(&bar_p_full, j & 1, abort_flag, a.err, kErrTimeoutMma)) break;
+      // The first P V MMA of an item restarts [O | L]; the softmax warps
+      // arrive on p_full for an item only after all of them have read the
+      // previous item's O and L (bar_o_free), so waiting for p_full orders it.
+      uint32_t g = 0;
+      bool ok = true;
+      FwdItem itm = item0;
+      int64_t v_it = blockIdx.x;
+      do {
+      const FwdGeo G = fwd_geo(a, itm);
+      const int n_it = G.n_it, dh = G.dh;
+      for (int j = 0; j < n_it; ++j, ++g) {
+        const int s = static_cast<int>(g % C::kStages);
+        if (!(ok = role_wait(&bar_v_full[s], (g / C::kStages) & 1, abort_flag, a.err, kErrTimeoutMma))) break;
+        if (!(ok = role_wait(&bar_p_full, g & 1, abort_flag, a.err, kErrTimeoutMma))) break;
         tc_fence_after();
         const bool fold_it = fold && j == n_it - 1;
         const uint64_t dsf = sdesc_adv(dSfV0, s * 2 * kAtomBytes);
@@ -409,6 +506,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         mma_commit(&bar_o_done);
         mma_commit(&bar_v_empty[s]);
       }
+      } while (ok && next_item(v_it, itm));
       mma_commit(&bar_drain2);
       mbar_wait(&bar_drain2, 0, nullptr, 0);
     }
@@ -421,7 +519,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const int part = (warp - 2) >> 2;
     const int r = quad * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    const int64_t qpos = static_cast<int64_t>(qt) * 128 + r;  // document-relative query index
     const float sl2 = a.scale_log2;
     if (part == 0) {
       // 1.0 for the ones rows of both V atoms, 2^-4 for P
@@ -430,12 +527,33 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       tmem_st4(lane_base + C::kColSfP, 0x7B7B7B7Bu, 0x7B7B7B7Bu, 0x7B7B7B7Bu, 0x7B7B7B7Bu);
       tmem_st_wait();
     }
+    bool ok = true;
+    uint32_t g = 0;  // ring iterations, counted across items
+    int n_items = 0;
+    FwdItem itm = item0;
+    int64_t v_it = blockIdx.x;
+    do {
+    // every softmax warp has finished the previous item's epilogue: its O, L
+    // columns and the s_l / s_mx buffers are free
+    if (n_items >= 1 && !(ok = warp_wait(&bar_o_free, (n_items - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax)))
+      break;
+    int qt, hk, n_it, dh;
+    int64_t nk, ktile_base;
+    {
+      const FwdGeo G = fwd_geo(a, itm);
+      qt = itm.qt;
+      hk = G.hk;
+      n_it = G.n_it;
+      dh = G.dh;
+      nk = G.nk;
+      ktile_base = itm.ktile_base;
+    }
+    const int64_t qpos = static_cast<int64_t>(qt) * 128 + r;  // document-relative query index
     float m = -INFINITY;  // running (lazy) max of the scaled scores, log2 units
     float l16 = 0.0f;     // this warp's sum of 2^(s - m + 4) over its columns
     float ldiag = 0.0f;   // folded diagonal columns (FOLD): the weights their codes stand for
-    bool ok = true;
-    for (int j = 0; j < n_it; ++j) {
-      if (!(ok = warp_wait(&bar_s_full, j & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+    for (int j = 0; j < n_it; ++j, ++g) {
+      if (!(ok = warp_wait(&bar_s_full, g & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
       float sv[64];
       ld64(lane_base + C::kColS + 64 * part, sv);
@@ -457,10 +575,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
       }
       float mt = max64(sv);
-      s_mx[j & 1][part][r] = mt;
-      mbar_arrive(&bar_mx[j & 1][quad]);
-      if (!(ok = warp_wait(&bar_mx[j & 1][quad], (j >> 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
-      mt = fmaxf(fmaxf(s_mx[j & 1][0][r], s_mx[j & 1][1][r]), fmaxf(s_mx[j & 1][2][r], s_mx[j & 1][3][r]));
+      const int px = static_cast<int>(g & 1);
+      s_mx[px][part][r] = mt;
+      mbar_arrive(&bar_mx[px][quad]);
+      if (!(ok = warp_wait(&bar_mx[px][quad], (g >> 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      mt = fmaxf(fmaxf(s_mx[px][0][r], s_mx[px][1][r]), fmaxf(s_mx[px][2][r], s_mx[px][3][r]));
       const float mts = mt * sl2;
       bool rescale_o = false;
       float factor = 1.0f;
@@ -508,7 +627,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       const float2 la = f2_unpack(lsa), lb = f2_unpack(lsb);
       const float lsum = (la.x + la.y) + (lb.x + lb.y);
       // the previous P V must be done before P is overwritten and O rescaled
-      if (j > 0 && !(ok = warp_wait(&bar_o_done, (j - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
+      if (j > 0 && !(ok = warp_wait(&bar_o_done, (g - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
       // tcgen05.ld/st are warp-collective: the whole warp rescales its rows'
       // share of O when any of them needs it (factor 1 for the others).
@@ -572,51 +691,63 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       mbar_arrive(&bar_p_full);
     }
     // ---------------------------------------------------------- epilogue
+    if (!ok) break;
     s_l[part][r] = l16;
     // the folded weights through the maxima buffer of the parity the last
     // iteration did not use (every warp of the quadrant read it before the
     // last iteration's max barrier)
-    if (FOLD && fold) s_mx[n_it & 1][part][r] = ldiag;
+    const int pu = static_cast<int>(g & 1);
+    if (FOLD && fold) s_mx[pu][part][r] = ldiag;
     mbar_arrive(&bar_lsum);
-    if (ok) ok = role_wait(&bar_lsum, 0, abort_flag, a.err, kErrTimeoutEpilogue);
-    if (ok) ok = role_wait(&bar_o_done, (n_it - 1) & 1, abort_flag, a.err, kErrTimeoutEpilogue);
-    if (__all_sync(0xffffffffu, ok)) {
-      tc_fence_after();
-      float inv;
-      {
-        uint32_t rr[16];
-        tmem_ld16(lane_base + C::kColL, rr);
-        tmem_ld_wait();
-        float lq = __uint_as_float(rr[0]);
-        if (FOLD && fold) lq += s_mx[n_it & 1][2 * dh][r] + s_mx[n_it & 1][2 * dh + 1][r];
-        inv = 1.0f / lq;
-      }
-      const bool valid = qpos < n;
-      const int64_t t = doc_start + qpos;
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + (t * a.Hq + h) * D;
-      constexpr int kCols = D / 4;  // 32 (d128) or 16 (d64) output channels per warp
-      uint32_t rr[kCols];
-      if constexpr (kCols == 32) {
-        tmem_ld32(lane_base + C::kColO + kCols * part, rr);
-      } else {
-        tmem_ld16(lane_base + C::kColO + kCols * part, rr);
-      }
-      tmem_ld_wait();
-      if (valid) {
-#pragma unroll
-        for (int i = 0; i < kCols; i += 8) {
-          uint4 v;
-          v.x = pack_bf16x2(__uint_as_float(rr[i]) * inv, __uint_as_float(rr[i + 1]) * inv);
-          v.y = pack_bf16x2(__uint_as_float(rr[i + 2]) * inv, __uint_as_float(rr[i + 3]) * inv);
-          v.z = pack_bf16x2(__uint_as_float(rr[i + 4]) * inv, __uint_as_float(rr[i + 5]) * inv);
-          v.w = pack_bf16x2(__uint_as_float(rr[i + 6]) * inv, __uint_as_float(rr[i + 7]) * inv);
-          *reinterpret_cast<uint4*>(orow + kCols * part + i) = v;
-        }
-      }
-      if (valid && part == 0)
-        a.lse[static_cast<int64_t>(h) * a.T + t] =
-            (m - 4.0f + log2f((s_l[0][r] + s_l[1][r]) + (s_l[2][r] + s_l[3][r]))) * 0.69314718055994531f;
+    ok = role_wait(&bar_lsum, n_items & 1, abort_flag, a.err, kErrTimeoutEpilogue);
+    if (ok) ok = role_wait(&bar_o_done, (g - 1) & 1, abort_flag, a.err, kErrTimeoutEpilogue);
+    if (!__all_sync(0xffffffffu, ok)) {
+      ok = false;
+      break;
     }
+    tc_fence_after();
+    float inv;
+    {
+      uint32_t rr[16];
+      tmem_ld16(lane_base + C::kColL, rr);
+      tmem_ld_wait();
+      float lq = __uint_as_float(rr[0]);
+      if (FOLD && fold) lq += s_mx[pu][2 * dh][r] + s_mx[pu][2 * dh + 1][r];
+      inv = 1.0f / lq;
+    }
+    const FwdGeo GE = fwd_geo(a, itm);  // the epilogue's own fields, recomputed
+    const int h = itm.h;
+    const bool valid = qpos < GE.n;
+    const int64_t t = GE.doc_start + qpos;
+    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + (t * a.Hq + h) * D;
+    constexpr int kCols = D / 4;  // 32 (d128) or 16 (d64) output channels per warp
+    uint32_t rr[kCols];
+    if constexpr (kCols == 32) {
+      tmem_ld32(lane_base + C::kColO + kCols * part, rr);
+    } else {
+      tmem_ld16(lane_base + C::kColO + kCols * part, rr);
+    }
+    tmem_ld_wait();
+    // O and L of this item are in registers: the next item's first P V may
+    // restart them once every softmax warp is here
+    tc_fence_before();
+    mbar_arrive(&bar_o_free);
+    if (valid) {
+#pragma unroll
+      for (int i = 0; i < kCols; i += 8) {
+        uint4 v;
+        v.x = pack_bf16x2(__uint_as_float(rr[i]) * inv, __uint_as_float(rr[i + 1]) * inv);
+        v.y = pack_bf16x2(__uint_as_float(rr[i + 2]) * inv, __uint_as_float(rr[i + 3]) * inv);
+        v.z = pack_bf16x2(__uint_as_float(rr[i + 4]) * inv, __uint_as_float(rr[i + 5]) * inv);
+        v.w = pack_bf16x2(__uint_as_float(rr[i + 6]) * inv, __uint_as_float(rr[i + 7]) * inv);
+        *reinterpret_cast<uint4*>(orow + kCols * part + i) = v;
+      }
+    }
+    if (valid && part == 0)
+      a.lse[static_cast<int64_t>(h) * a.T + t] =
+          (m - 4.0f + log2f((s_l[0][r] + s_l[1][r]) + (s_l[2][r] + s_l[3][r]))) * 0.69314718055994531f;
+    ++n_items;
+    } while (next_item(v_it, itm));
   }
   tc_fence_before();
   __syncthreads();
@@ -628,24 +759,44 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
 namespace {
 
-template <int D, bool FOLD>
+template <int D, bool FOLD, bool PERSIST>
 cudaError_t launch_fwd_t(const FwdArgs& a, const FwdMaps& m, const dim3& grid, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_fwd_kernel<D, FOLD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, FOLD, PERSIST>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_fwd_kernel<D, FOLD><<<grid, C::kThreads, C::kSmemBytes, stream>>>(m, a);
+  attn_fwd_kernel<D, FOLD, PERSIST><<<grid, C::kThreads, C::kSmemBytes, stream>>>(m, a);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdArgs& a, const FwdMaps& m, const dim3& grid, bool fold, bool persist,
+                         cudaStream_t stream) {
+  if (persist) return fold ? launch_fwd_t<D, true, true>(a, m, grid, stream) : launch_fwd_t<D, false, true>(a, m, grid, stream);
+  return fold ? launch_fwd_t<D, true, false>(a, m, grid, stream) : launch_fwd_t<D, false, false>(a, m, grid, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, const FwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
-  const dim3 grid = a.items ? dim3(static_cast<unsigned>(a.ntiles * a.Hq))
-                            : dim3((max_seqlen + 127) / 128, a.num_docs, a.Hq);
+  // persistent: one CTA per SM (the kernel holds all 512 TMEM columns)
+  // walking the virtual items -- with a cost-sorted list, or on equal
+  // documents (heaviest query tiles first when causal); packed documents
+  // without a list keep one CTA per slot of the max_seqlen grid
+  const bool persist = a.items != nullptr || (a.cu_seqlens == nullptr && a.cu_k == nullptr);
+  dim3 grid;
+  if (persist) {
+    const int64_t total =
+        a.items ? a.ntiles * a.Hq : static_cast<int64_t>(a.nq_tiles_doc) * a.num_docs * a.Hq;
+    const int64_t sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    grid = dim3(static_cast<unsigned>(total < sms ? total : sms));
+  } else {
+    grid = dim3((max_seqlen + 127) / 128, a.num_docs, a.Hq);
+  }
   const bool fold = a.vkey_sf != nullptr && a.causal;
-  if (d == 128) return fold ? launch_fwd_t<128, true>(a, m, grid, stream) : launch_fwd_t<128, false>(a, m, grid, stream);
-  return fold ? launch_fwd_t<64, true>(a, m, grid, stream) : launch_fwd_t<64, false>(a, m, grid, stream);
+  return d == 128 ? launch_fwd_d<128>(a, m, grid, fold, persist, stream)
+                  : launch_fwd_d<64>(a, m, grid, fold, persist, stream);
 }
 
 }  // namespace mxa

@@ -22,6 +22,13 @@ CASES = [
     inp.make_custom("d64_batched_causal", B=2, L=384, Hq=2, Hkv=2, d=64, causal=True, seed=23),
     inp.make_custom("tokblock_gqa", lengths=[100, 400, 37], Hq=4, Hkv=2, d=128, causal=True, mode="tokblock",
                     hadamard=True, seed=24),
+    # more items than SMs: persistent CTAs take two items each (zig-zag
+    # rounds of 152), so the per-item barrier phases and the Q / O hand-over
+    # between items are exercised element by element
+    inp.make_custom("persist_batched_causal_gqa", B=3, L=1100, Hq=8, Hkv=4, d=128, causal=True, seed=29),
+    inp.make_custom("persist_batched_d64", B=2, L=700, Hq=16, Hkv=16, d=64, causal=False, seed=30),
+    inp.make_custom("persist_list_causal", lengths=[900, 5, 1000, 260, 700], Hq=8, Hkv=8, d=128, causal=True,
+                    seed=31),
 ]
 
 
