@@ -254,7 +254,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
   __shared__ uint64_t bar_q, bar_q_free, bar_k_full[C::kStages], bar_k_empty[C::kStages], bar_v_full[C::kStages],
       bar_v_empty[C::kStages], bar_s_full, bar_s_empty, bar_p_full, bar_o_done, bar_o_free, bar_drain, bar_drain2,
-      bar_mx[2][4], bar_lsum;
+      bar_mx[2][4], bar_lsum, bar_clc[2], bar_clc_free[2];
+  __shared__ alignas(16) uint4 s_clc[2];  // cluster-launch-control responses, by item parity
   __shared__ float s_mx[2][4][128];  // [iteration parity][column quarter][row] partial row maxima
   __shared__ float s_l[4][128];      // [column quarter][row] partial row sums
   __shared__ uint32_t s_tmem;
@@ -263,10 +264,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // The CTA's items.  Persistent launches (a cost-sorted list, or equal
-  // documents) walk the items blockIdx.x, blockIdx.x + gridDim.x, ... --
-  // every role the same sequence, with each barrier's phase counted across
-  // items; packed documents without a list take one item per CTA from the
-  // max_seqlen grid (heaviest query tiles first when causal).
+  // documents) start with item blockIdx.x of a grid with one CTA per item,
+  // heaviest first, and then take over the items of CTAs that have not
+  // started yet (cluster launch control): the producer asks for one after
+  // the last K/V load of each item, and every role reads the answer at the
+  // end of that item -- all roles walk the same sequence, with each
+  // barrier's phase counted across items.  Packed documents without a list
+  // take one item per CTA from the max_seqlen grid (heaviest query tiles
+  // first when causal).
   FwdItem item0;
   if constexpr (PERSIST) {
     if (!fwd_item(a, blockIdx.x, item0)) return;
@@ -283,15 +288,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
                            ? item0.tile_base
                            : doc_tile_base(a.cu_k, item0.b, kn, tid, C::kThreads, &s_slot_k);
   }
-  // the next item of this CTA after v (false at the end of the sequence):
-  // round k of gridDim.x items takes blockIdx.x, or gridDim.x - 1 -
-  // blockIdx.x when k is odd, so that each CTA pairs heavier and lighter
-  // items of a cost-sorted list
-  auto next_item = [&](int64_t& v, FwdItem& it) -> bool {
-    if constexpr (!PERSIST) return false;
-    const int64_t G = gridDim.x, k = v / G + 1;
-    v = k * G + ((k & 1) ? G - 1 - static_cast<int64_t>(blockIdx.x) : static_cast<int64_t>(blockIdx.x));
-    return fwd_item(a, v, it);
+  // The item after the CTA's n-th (false at the end of the sequence, or when
+  // the wait fails): the response in slot n & 1, read once its phase is
+  // complete; `release` arrives on the slot's free barrier (one thread per
+  // role and one lane per softmax warp).
+  auto next_item = [&](int n, FwdItem& it, bool release, bool& ok) -> bool {
+    if constexpr (!PERSIST) {
+      return false;
+    } else {
+      const bool got = role_wait(&bar_clc[n & 1], (n >> 1) & 1, &s_abort, a.err, kErrTimeoutOther);
+      uint32_t x = 0;
+      const bool more = got && clc_query(&s_clc[n & 1], x);
+      if (release) mbar_arrive(&bar_clc_free[n & 1]);
+      if (!got) ok = false;
+      return more && fwd_item(a, x, it);
+    }
   };
 
   if (tid == 0) {
@@ -315,6 +326,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       mbar_init(&bar_mx[1][q], 128);
     }
     mbar_init(&bar_lsum, C::kSoftmaxThreads);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_clc[i], 1);
+      mbar_init(&bar_clc_free[i], 3 + C::kSoftmaxThreads / 32);  // producer, two MMA issuers, softmax warps
+    }
     s_abort = 0;
     fence_barrier_init();
   }
@@ -349,7 +364,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       int issued_q = 0;
       bool ok = true;
       FwdItem itm = item0;
-      int64_t v_it = blockIdx.x;
+      int n = 0;  // items of this CTA so far
       do {
         const FwdGeo G = fwd_geo(a, itm);
         const int hk = G.hk, h = itm.h, qt = itm.qt, n_it = G.n_it, dh = G.dh, nk_tiles = G.nk_tiles;
@@ -398,7 +413,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         bulk_load(sfv + kAtomBytes, a.v_sf + atom1, kAtomBytes, &bar_v_full[s]);
         issued_v = gk + 1;
         }
-      } while (ok && next_item(v_it, itm));
+        if (!ok) break;
+        if constexpr (PERSIST) {
+          // dynamic fetch after the item's last K/V load: the slot is free
+          // once every role has read the response of item n - 2
+          if (n >= 2 && !(ok = role_wait(&bar_clc_free[n & 1], ((n >> 1) - 1) & 1, abort_flag, a.err,
+                                         kErrTimeoutOther)))
+            break;
+          clc_try_cancel(&s_clc[n & 1], &bar_clc[n & 1]);
+        }
+      } while (next_item(n++, itm, true, ok) && ok);
       // drain: every load issued must have landed before the CTA exits
       if (issued_q) role_wait(&bar_q, (issued_q - 1) & 1, abort_flag, nullptr, 0);
       for (uint32_t j = (issued_k > C::kStages ? issued_k - C::kStages : 0); j < issued_k; ++j)
@@ -442,7 +466,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       uint32_t g = 0;
       int n_items = 0;
       FwdItem itm = item0;
-      int64_t v_it = blockIdx.x;
       do {
         const int n_it = fwd_geo(a, itm).n_it;
         if (!(ok = role_wait(&bar_q, n_items & 1, abort_flag, a.err, kErrTimeoutMma))) break;
@@ -450,8 +473,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           if (!(ok = issue_s(g, j))) break;  // waits until S_{g-1} has been read out
         if (!ok) break;
         mma_commit(&bar_q_free);  // this item's S MMAs are done with Q once they complete
-        ++n_items;
-      } while (next_item(v_it, itm));
+      } while (next_item(n_items++, itm, true, ok) && ok);
       // drain this thread's MMAs before the TMEM is released
       mma_commit(&bar_drain);
       mbar_wait(&bar_drain, 0, nullptr, 0);
@@ -477,7 +499,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       uint32_t g = 0;
       bool ok = true;
       FwdItem itm = item0;
-      int64_t v_it = blockIdx.x;
+      int n = 0;
       do {
       const FwdGeo G = fwd_geo(a, itm);
       const int n_it = G.n_it, dh = G.dh;
@@ -506,7 +528,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         mma_commit(&bar_o_done);
         mma_commit(&bar_v_empty[s]);
       }
-      } while (ok && next_item(v_it, itm));
+      if (!ok) break;
+      } while (next_item(n++, itm, true, ok) && ok);
       mma_commit(&bar_drain2);
       mbar_wait(&bar_drain2, 0, nullptr, 0);
     }
@@ -531,7 +554,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     uint32_t g = 0;  // ring iterations, counted across items
     int n_items = 0;
     FwdItem itm = item0;
-    int64_t v_it = blockIdx.x;
+    // next_item for a softmax warp: a warp-collective wait, lane 0 releases
+    // the slot for the warp
+    auto next_item_warp = [&](int n) -> bool {
+      if constexpr (!PERSIST) {
+        return false;
+      } else {
+        const bool got = warp_wait(&bar_clc[n & 1], (n >> 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax);
+        uint32_t x = 0;
+        const bool more = got && clc_query(&s_clc[n & 1], x);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_clc_free[n & 1]);
+        if (!got) ok = false;
+        return more && ok && fwd_item(a, x, itm);
+      }
+    };
     do {
     // every softmax warp has finished the previous item's epilogue: its O, L
     // columns and the s_l / s_mx buffers are free
@@ -746,8 +783,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     if (valid && part == 0)
       a.lse[static_cast<int64_t>(h) * a.T + t] =
           (m - 4.0f + log2f((s_l[0][r] + s_l[1][r]) + (s_l[2][r] + s_l[3][r]))) * 0.69314718055994531f;
-    ++n_items;
-    } while (next_item(v_it, itm));
+    } while (next_item_warp(n_items++));
   }
   tc_fence_before();
   __syncthreads();
@@ -779,18 +815,17 @@ cudaError_t launch_fwd_d(const FwdArgs& a, const FwdMaps& m, const dim3& grid, b
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, const FwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
-  // persistent: one CTA per SM (the kernel holds all 512 TMEM columns)
-  // walking the virtual items -- with a cost-sorted list, or on equal
+  // persistent (one CTA per SM runs at a time: the kernel holds all 512 TMEM
+  // columns) over the virtual items -- with a cost-sorted list, or on equal
   // documents (heaviest query tiles first when causal); packed documents
   // without a list keep one CTA per slot of the max_seqlen grid
   const bool persist = a.items != nullptr || (a.cu_seqlens == nullptr && a.cu_k == nullptr);
   dim3 grid;
-  if (persist) {
+  if (persist) {  // one CTA per item; running CTAs take over the ones not yet started
     const int64_t total =
         a.items ? a.ntiles * a.Hq : static_cast<int64_t>(a.nq_tiles_doc) * a.num_docs * a.Hq;
-    const int64_t sms = sm_count();
-    if (sms <= 0) return cudaErrorInvalidDevice;
-    grid = dim3(static_cast<unsigned>(total < sms ? total : sms));
+    if (total <= 0 || total > 0x7FFFFFFFll) return cudaErrorInvalidValue;
+    grid = dim3(static_cast<unsigned>(total));
   } else {
     grid = dim3((max_seqlen + 127) / 128, a.num_docs, a.Hq);
   }

@@ -113,10 +113,10 @@ struct FwdArgs {
   int* err;
   // cost-sorted query-tile list: item i / Hq for head i % Hq of virtual
   // item i.  With a list, or with equal documents on both sides (no
-  // offsets), the launch is persistent: one CTA per SM walks the virtual
-  // items in rounds of gridDim.x, zig-zag (round k takes blockIdx.x, or
-  // gridDim.x - 1 - blockIdx.x when k is odd); other calls take one CTA per
-  // (tile slot, document, head) of the max_seqlen grid.
+  // offsets), the launch is persistent: one CTA per virtual item, and each
+  // running CTA takes over the items of CTAs not yet started (cluster launch
+  // control); other calls take one CTA per (tile slot, document, head) of
+  // the max_seqlen grid.
   const TileItem* items;
   const int32_t* item_count;
   int nq_tiles_doc, nk_tiles_doc;  // 128-token tiles per document (equal documents)
@@ -249,7 +249,5 @@ cudaError_t launch_bwd_prep(const PrepArgs& a, int max_seqlen, cudaStream_t stre
 cudaError_t launch_dq_convert(const DqConvArgs& a, cudaStream_t stream);
 
 int* device_error_word();
-// Streaming multiprocessors of the current device (0 if unknown).
-int sm_count();
 
 }  // namespace mxa

@@ -67,6 +67,40 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   }
 }
 
+// ---------------------------------------------------------------- cluster launch control
+// Asks the hardware to cancel the launch of a CTA of this grid that has not
+// started yet, so that the calling CTA takes over its work (Blackwell cluster
+// launch control; each CTA is a cluster of one).  The 16-byte response lands
+// in `resp` (shared memory, 16-byte aligned) and completes 16 transaction
+// bytes on `bar`.  The proxy fence orders the earlier generic reads of `resp`
+// before the asynchronous write.  After a response that reports no
+// cancellation, no further request may be issued.
+__device__ __forceinline__ void clc_try_cancel(void* resp, uint64_t* bar) {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_arrive_expect_tx(bar, 16);
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+          smem_u32(resp)),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+// Decodes a response (after its barrier phase completed): true, with the x
+// index of the cancelled CTA, when the cancellation succeeded.
+__device__ __forceinline__ bool clc_query(const void* resp, uint32_t& x) {
+  uint32_t ok, cx = 0;
+  asm volatile(
+      "{\n\t.reg .b128 h;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 h, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, h;\n\t}"
+      : "=r"(ok), "+r"(cx)
+      : "r"(smem_u32(resp))
+      : "memory");
+  x = cx;
+  return ok != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
