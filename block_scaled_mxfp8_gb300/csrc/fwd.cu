@@ -114,7 +114,7 @@ __device__ __forceinline__ float ue8m0_f32(uint32_t b) {
 }
 
 // The diagonal tile's fold for one thread's 64 key columns, 32 at a time,
-// read again from TMEM at tS (the last iteration's S is never overwritten):
+// read again from TMEM at tS (the warps release S only after this read):
 // the weights p = 2^(s sl2 - m + 4) (summed into lsa/lsb as elsewhere),
 // times 2^e_k of each key (kexp: its 64 exponent bytes, 16-byte aligned),
 // quantized per 32 keys by the MX rule into pw; columns at or past lim are
@@ -594,8 +594,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       tc_fence_after();
       float sv[64];
       ld64(lane_base + C::kColS + 64 * part, sv);
+      // S is in registers: the next S MMA may start -- except on the folded
+      // last iteration, whose diagonal half is read from TMEM again below
+      // (the next S may be the next item's first)
+      const bool hold_s = fold && j == n_it - 1;
       tc_fence_before();
-      mbar_arrive(&bar_s_empty);  // S is in registers: the next S MMA may start
+      if (!hold_s) mbar_arrive(&bar_s_empty);
       // columns >= lim are masked (keys past the document end, or after the
       // query on the causal diagonal); only the last iteration has any
       int lim = 256;
@@ -663,6 +667,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       }
       const float2 la = f2_unpack(lsa), lb = f2_unpack(lsb);
       const float lsum = (la.x + la.y) + (lb.x + lb.y);
+      if (hold_s) {
+        tc_fence_before();
+        mbar_arrive(&bar_s_empty);
+      }
       // the previous P V must be done before P is overwritten and O rescaled
       if (j > 0 && !(ok = warp_wait(&bar_o_done, (g - 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
