@@ -29,9 +29,11 @@ CASES = [
     inp.make_custom("d128_ragged_gqa_causal", lengths=[1, 129, 300, 64, 7, 515], Hq=4, Hkv=2, d=128, causal=True,
                     seed=41),
     inp.make_custom("d64_ragged", lengths=[256, 100, 383], Hq=2, Hkv=1, d=64, causal=True, seed=42),
-    # more items than SMs: persistent CTAs take several items, so the next
-    # item's first S MMA follows each diagonal tile's fold
-    inp.make_custom("persist_batched_gqa", B=3, L=1100, Hq=8, Hkv=4, d=128, causal=True, seed=48),
+    # packed documents with more list items (26 tiles x 8 heads) than SMs:
+    # persistent CTAs take several items, so the next item's first S MMA
+    # follows each diagonal tile's fold
+    inp.make_custom("persist_list_gqa", lengths=[900, 5, 1000, 260, 700], Hq=8, Hkv=4, d=128, causal=True,
+                    seed=48),
 ]
 
 
