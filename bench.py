@@ -325,8 +325,10 @@ def run_gpu(args):
             e[3].record(stream)
             rec.append(e)
 
-    # the block-scaled MMA rate of this GPU, measured before the timed region
+    # the block-scaled MMA and exponential rates of this GPU, measured before
+    # the timed region
     probe = mma_probe(dev)
+    eprobe = ex2_probe(dev)
 
     for _ in range(args.warmup):
         step(x)
@@ -436,6 +438,15 @@ def run_gpu(args):
                 MXFP8_MMA_FLOP_PER_SM_CLK,
                 "frac_of_microbench": {"fwd": round(fwd_pf * 1e3 / micro_tflops, 4),
                                        "bwd": round(bwd_pf * 1e3 / micro_tflops, 4)}}
+    # the co-bound: exponentials, one per visible (query, key) pair and head
+    # in the forward and again in the backward's P rebuild (forward FLOP / 4d)
+    n_exp = ffwd / (4.0 * w.d)
+    exp_unit = None
+    if eprobe:
+        exp_rate = eprobe["ex2_per_sm_clk"] * eprobe["sms"] * sm_mhz * 1e6  # per second at the sampled clock
+        exp_unit = {"exps_per_pass": n_exp, "peak_per_s": round(exp_rate, 1),
+                    "fwd_frac": round(n_exp / (ms_fwd * 1e-3) / exp_rate, 4),
+                    "bwd_frac": round(n_exp / (ms_bwd_only * 1e-3) / exp_rate, 4), "probe": eprobe}
 
     # e2e through the C ABI with host buffers: H2D of q, k, v, dO and D2H of o, dq, dk, dv inside the timed region
     host_cpus = bind_gpu_local_cpus(local)  # pinned buffers in the memory next to this GPU
@@ -531,6 +542,7 @@ def run_gpu(args):
         "ms": {"quantize_qkv": round(ms_quant, 3), "fwd": round(ms_fwd, 3), "quantize_do_plus_bwd": round(ms_bwd, 3),
                "bwd": round(ms_bwd_only, 3)},
         "roofline": roofline,
+        "exp_unit": exp_unit if exp_unit else "probe did not run",
         "quantize": quant_line,
         "rmsnorm_quantize": rms,
         "e2e": e2e,
@@ -635,6 +647,28 @@ def run_mma_probe(args):
         raise SystemExit("mma probe failed")
     r["clocks"] = clk.summary()
     print(json.dumps({"mma_probe": r}))
+
+
+def ex2_probe(dev, iters=4096):
+    """Exponential-unit rate on every SM (include/mxa_testing.h): one warm-up
+    launch, then one timed launch.  Returns the ex2 per SM clock (median over
+    the CTAs' own clock counts)."""
+    import torch
+    from block_scaled_mxfp8_gb300 import mxa
+
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    cyc = torch.zeros(n_sm, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    if mxa.mxa_test_ex2_rate(64, cyc, stream) != mxa.MXA_OK:
+        return None
+    st = mxa.mxa_test_ex2_rate(iters, cyc, stream)
+    torch.cuda.synchronize(dev)
+    c = cyc.cpu().tolist()
+    if st != mxa.MXA_OK or mxa.mxa_get_error() != mxa.MXA_OK or min(c) <= 0:
+        return None
+    n = float(iters) * 8 * 512
+    return {"ex2_per_sm_clk": round(n / statistics.median(c), 2), "sms": n_sm, "iters": iters,
+            "what": "ex2.approx.ftz.f32, 512 threads x 8 independent chains per SM"}
 
 
 def main():

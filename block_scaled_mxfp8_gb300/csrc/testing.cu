@@ -114,8 +114,42 @@ __global__ void __launch_bounds__(128, 1) test_mma_rate_kernel(int iters, long l
   }
 }
 
+// ex2 rate: sixteen warps per CTA (four per SM sub-partition, as the
+// attention kernels' softmax warps), each thread running eight independent
+// chains of `iters` steps x <- ex2(x) - 2 with the kernels' exponential
+// (ex2.approx.ftz.f32; for x in [-2, -1] the chain stays in [-2, -1], and the
+// subtraction runs on the FMA pipe); thread 0 stamps the SM clock between two
+// block barriers.  One CTA per SM (the dynamic shared memory keeps a second
+// one off the SM).
+__global__ void __launch_bounds__(512, 1) test_ex2_rate_kernel(int iters, long long* cycles) {
+  float x[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) x[c] = -1.0f - 0.01f * static_cast<float>(threadIdx.x & 7) - 0.1f * static_cast<float>(c);
+  __syncthreads();
+  const long long t0 = clock64();
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) x[c] = ex2_approx(x[c]) - 2.0f;
+  }
+  __syncthreads();
+  const long long t1 = clock64();
+  const float sum = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
+  if (sum > 0.0f) cycles[blockIdx.x] = -2;  // never (the chains stay negative): keeps the loop
+  else if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
+}
+
 }  // namespace
 }  // namespace mxa
+
+extern "C" mxa_status mxa_test_ex2_rate(int iters, int ctas, long long* cycles, cudaStream_t stream) {
+  if (iters <= 0 || iters > (1 << 24) || ctas <= 0 || ctas > 4096 || !cycles) return MXA_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(cycles) & 7) return MXA_ERR_ALIGN;
+  if (cudaFuncSetAttribute(mxa::test_ex2_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           mxa::kProbeDynSmem) != cudaSuccess)
+    return MXA_ERR_CUDA;
+  mxa::test_ex2_rate_kernel<<<ctas, 512, mxa::kProbeDynSmem, stream>>>(iters, cycles);
+  return cudaGetLastError() == cudaSuccess ? MXA_OK : MXA_ERR_CUDA;
+}
 
 extern "C" mxa_status mxa_test_mma_rate(int iters, int ctas, long long* cycles, cudaStream_t stream) {
   if (iters <= 0 || iters > (1 << 24) || ctas <= 0 || ctas > 4096 || !cycles) return MXA_ERR_ARG;

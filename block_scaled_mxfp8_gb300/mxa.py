@@ -101,7 +101,8 @@ EXPORTS = [
     "mxa_bwd_noalloc", "mxa_get_error",
 ]
 # include/mxa_testing.h: the kernels' P and dS quantization run on caller data
-EXPORTS_TESTING = ["mxa_test_e4m3", "mxa_test_ds_blocks", "mxa_test_wait_timeout", "mxa_test_mma_rate"]
+EXPORTS_TESTING = ["mxa_test_e4m3", "mxa_test_ds_blocks", "mxa_test_wait_timeout", "mxa_test_mma_rate",
+                   "mxa_test_ex2_rate"]
 MXA_BWD_NOALLOC_MAX_WORKSPACE = 32 * 1024 * 1024
 
 
@@ -155,6 +156,8 @@ def lib():
         L.mxa_test_wait_timeout.argtypes = [ctypes.c_longlong, P]
         L.mxa_test_mma_rate.restype = i32
         L.mxa_test_mma_rate.argtypes = [i32, i32, P, P]
+        L.mxa_test_ex2_rate.restype = i32
+        L.mxa_test_ex2_rate.argtypes = [i32, i32, P, P]
         _lib = L
     return _lib
 
@@ -257,6 +260,14 @@ def mxa_test_mma_rate(iters: int, cycles: torch.Tensor, stream=None) -> int:
     element of cycles (int64, device)."""
     assert cycles.dtype == torch.int64 and cycles.is_cuda
     return lib().mxa_test_mma_rate(int(iters), cycles.numel(), _ptr(cycles), _stream(stream))
+
+
+def mxa_test_ex2_rate(iters: int, cycles: torch.Tensor, stream=None) -> int:
+    """include/mxa_testing.h: exponential-unit rate probe (ex2.approx.ftz.f32,
+    512 threads x 8 chains per CTA), one CTA per element of cycles (int64,
+    device)."""
+    assert cycles.dtype == torch.int64 and cycles.is_cuda
+    return lib().mxa_test_ex2_rate(int(iters), cycles.numel(), _ptr(cycles), _stream(stream))
 
 
 def mxa_get_error(stream=None) -> int:

@@ -66,6 +66,17 @@ mxa_status mxa_test_wait_timeout(long long budget_cycles, cudaStream_t stream);
  * MXA_ERR_ALIGN, MXA_ERR_CUDA. */
 mxa_status mxa_test_mma_rate(int iters, int ctas, long long* cycles, cudaStream_t stream);
 
+/* Exponential-unit rate probe: `ctas` CTAs (one per SM; launch at most the
+ * SM count) of 512 threads, each thread running eight independent chains of
+ * `iters` ex2.approx.ftz.f32 (the attention kernels' exponential, FLAMIA
+ * notes sec. 7: the exponential unit is the co-bound of the tensor cores).
+ * cycles (device, int64 [ctas], 8-byte aligned, caller-owned) receives each
+ * CTA's SM clocks for its loop.  Exponentials per CTA = iters * 8 * 512.
+ * The attention kernels' exponential-unit utilisation is measured against
+ * it.  Status: MXA_OK, MXA_ERR_ARG (iters outside [1, 2^24], ctas outside
+ * [1, 4096], null cycles), MXA_ERR_ALIGN, MXA_ERR_CUDA. */
+mxa_status mxa_test_ex2_rate(int iters, int ctas, long long* cycles, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
