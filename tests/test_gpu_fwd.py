@@ -113,3 +113,30 @@ def test_fwd_work_list_schedule(w):
     assert all(it[i, 2] == base[it[i, 0]] and it[i, 3] == base[it[i, 0]] for i in range(count))
     cost = [it[i, 1] + 1 if w.causal else tiles[it[i, 0]] for i in range(count)]
     assert all(cost[i] >= cost[i + 1] for i in range(count - 1))
+
+
+REPEAT_CASES = [
+    inp.make_custom("repeat_batched_causal", B=2, L=2048, Hq=16, Hkv=8, d=128, causal=True, seed=32),
+    inp.make_custom("repeat_batched", B=2, L=2048, Hq=16, Hkv=16, d=128, causal=False, seed=33),
+    inp.make_custom("repeat_list_causal", lengths=[1500, 3, 900, 2000, 130, 700], Hq=8, Hkv=2, d=128, causal=True,
+                    seed=34),
+]
+
+
+@pytest.mark.parametrize("w", REPEAT_CASES, ids=[c.name for c in REPEAT_CASES])
+def test_fwd_repeat_is_bit_identical(w):
+    """With more items than SMs the CTAs take over items dynamically, so which
+    CTA computes which query tile changes from run to run; every item is
+    computed the same way on any CTA, so O and LSE repeat bit for bit."""
+    from block_scaled_mxfp8_gb300 import mxa
+
+    t = inp.tensors(w, with_grad=False)
+    geo, gv = gpu_views(w, t, names=("q", "k", "v"))
+    outs = []
+    for _ in range(3):
+        o, lse = mxa.fwd(gv["q"][0], gv["k"][0], gv["v"][1], geo, w.causal)
+        torch.cuda.synchronize()
+        mxa.check_error()
+        outs.append((o.view(torch.int16).clone(), lse.view(torch.int32).clone()))
+    for o, lse in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
