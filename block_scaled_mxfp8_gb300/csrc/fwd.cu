@@ -108,6 +108,17 @@ __device__ __forceinline__ void ld64(uint32_t taddr, float (&v)[64]) {
   }
 }
 
+// 64 fp32 columns and their maximum, from the loads themselves (the TMEM read
+// merged with the row-max reduction, FLAMIA notes sec. 7) -- for key tiles
+// whose columns are all visible.
+__device__ __forceinline__ void ld64_max(uint32_t taddr, float (&v)[64], float& mx) {
+  float m0, m1;
+  tmem_ld32_max(taddr, *reinterpret_cast<float(*)[32]>(&v[0]), m0);
+  tmem_ld32_max(taddr + 32, *reinterpret_cast<float(*)[32]>(&v[32]), m1);
+  tmem_ld_wait();
+  mx = fmaxf(m0, m1);
+}
+
 // 2^(b - 127) of a UE8M0 byte (b = 0: 2^-127).
 __device__ __forceinline__ float ue8m0_f32(uint32_t b) {
   return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
@@ -593,7 +604,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       if (!(ok = warp_wait(&bar_s_full, g & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
       float sv[64];
-      ld64(lane_base + C::kColS + 64 * part, sv);
+      float mt;
+      // every iteration but the last has all 256 columns visible: the load
+      // also returns their maximum
+      const bool full = j < n_it - 1;
+      if (full) {
+        ld64_max(lane_base + C::kColS + 64 * part, sv, mt);
+      } else {
+        ld64(lane_base + C::kColS + 64 * part, sv);
+      }
       // S is in registers: the next S MMA may start -- except on the folded
       // last iteration, whose diagonal half is read from TMEM again below
       // (the next S may be the next item's first)
@@ -603,7 +622,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       // columns >= lim are masked (keys past the document end, or after the
       // query on the causal diagonal); only the last iteration has any
       int lim = 256;
-      if (j == n_it - 1) {
+      if (!full) {
         const int64_t rem = nk - static_cast<int64_t>(j) * 256;
         lim = rem < 256 ? static_cast<int>(rem) : 256;
         if (a.causal) {
@@ -615,7 +634,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           for (int c = 0; c < 64; ++c) sv[c] = (64 * part + c < lim) ? sv[c] : -INFINITY;
         }
       }
-      float mt = max64(sv);
+      if (!full) mt = max64(sv);
       const int px = static_cast<int>(g & 1);
       s_mx[px][part][r] = mt;
       mbar_arrive(&bar_mx[px][quad]);

@@ -138,8 +138,65 @@ __global__ void __launch_bounds__(512, 1) test_ex2_rate_kernel(int iters, long l
   else if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
 }
 
+// The forward's row maximum on full key tiles: 128 rows (one per thread, four
+// warps, one TMEM lane quadrant each) of 64 fp32 values stored to TMEM, read
+// back with tmem_ld32_max for columns [0, 32) and [32, 64).  out[3 r] and
+// out[3 r + 1] receive the two maxima of row r, out[3 r + 2] the number of
+// values that did not read back unchanged.
+__global__ void __launch_bounds__(128, 1) test_tmem_max_kernel(const float* x, float* out) {
+  __shared__ uint32_t s_tmem;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, 64);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const float* row = x + tid * 64;
+#pragma unroll
+  for (int c = 0; c < 64; c += 8) {
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(row[c + k]);
+    tmem_st8(lane_base + c, w);
+  }
+  tmem_st_wait();
+  tc_fence_before();
+  __syncwarp();
+  tc_fence_after();
+  float v0[32], v1[32], m0, m1;
+  tmem_ld32_max(lane_base, v0, m0);
+  tmem_ld32_max(lane_base + 32, v1, m1);
+  tmem_ld_wait();
+  int bad = 0;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    bad += __float_as_uint(v0[c]) != __float_as_uint(row[c]);
+    bad += __float_as_uint(v1[c]) != __float_as_uint(row[32 + c]);
+  }
+  out[3 * tid] = m0;
+  out[3 * tid + 1] = m1;
+  out[3 * tid + 2] = static_cast<float>(bad);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+}
+
 }  // namespace
 }  // namespace mxa
+
+extern "C" mxa_status mxa_test_tmem_max(const float* x, float* out, cudaStream_t stream) {
+  if (!x || !out) return MXA_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 3) return MXA_ERR_ALIGN;
+  mxa::test_tmem_max_kernel<<<1, 128, 0, stream>>>(x, out);
+  return cudaGetLastError() == cudaSuccess ? MXA_OK : MXA_ERR_CUDA;
+}
 
 extern "C" mxa_status mxa_test_ex2_rate(int iters, int ctas, long long* cycles, cudaStream_t stream) {
   if (iters <= 0 || iters > (1 << 24) || ctas <= 0 || ctas > 4096 || !cycles) return MXA_ERR_ARG;

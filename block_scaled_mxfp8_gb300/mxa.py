@@ -102,7 +102,7 @@ EXPORTS = [
 ]
 # include/mxa_testing.h: the kernels' P and dS quantization run on caller data
 EXPORTS_TESTING = ["mxa_test_e4m3", "mxa_test_ds_blocks", "mxa_test_wait_timeout", "mxa_test_mma_rate",
-                   "mxa_test_ex2_rate"]
+                   "mxa_test_ex2_rate", "mxa_test_tmem_max"]
 MXA_BWD_NOALLOC_MAX_WORKSPACE = 32 * 1024 * 1024
 
 
@@ -158,6 +158,8 @@ def lib():
         L.mxa_test_mma_rate.argtypes = [i32, i32, P, P]
         L.mxa_test_ex2_rate.restype = i32
         L.mxa_test_ex2_rate.argtypes = [i32, i32, P, P]
+        L.mxa_test_tmem_max.restype = i32
+        L.mxa_test_tmem_max.argtypes = [P, P, P]
         _lib = L
     return _lib
 
@@ -268,6 +270,14 @@ def mxa_test_ex2_rate(iters: int, cycles: torch.Tensor, stream=None) -> int:
     device)."""
     assert cycles.dtype == torch.int64 and cycles.is_cuda
     return lib().mxa_test_ex2_rate(int(iters), cycles.numel(), _ptr(cycles), _stream(stream))
+
+
+def mxa_test_tmem_max(x: torch.Tensor, out: torch.Tensor, stream=None) -> int:
+    """include/mxa_testing.h: TMEM round trip of x (fp32 [128, 64], device)
+    with the load-with-maximum; out (fp32 [128, 3], device)."""
+    assert x.dtype == torch.float32 and x.is_cuda and out.dtype == torch.float32 and out.is_cuda
+    assert x.numel() == 128 * 64 and out.numel() == 128 * 3
+    return lib().mxa_test_tmem_max(_ptr(x), _ptr(out), _stream(stream))
 
 
 def mxa_get_error(stream=None) -> int:

@@ -77,6 +77,17 @@ mxa_status mxa_test_mma_rate(int iters, int ctas, long long* cycles, cudaStream_
  * [1, 4096], null cycles), MXA_ERR_ALIGN, MXA_ERR_CUDA. */
 mxa_status mxa_test_ex2_rate(int iters, int ctas, long long* cycles, cudaStream_t stream);
 
+/* The attention forward's row maximum on fully visible key tiles, read with
+ * the scores themselves (tcgen05.ld.red .max, sm_103a; FLAMIA notes sec. 7:
+ * on B300 the TMEM read is merged with the row-max reduction).  x (device,
+ * fp32 [128, 64], caller-owned): row r is stored to TMEM lane r, then read
+ * back as two 32-column loads with their maxima.  out (device, fp32
+ * [128, 3]): the maxima of columns [0, 32) and [32, 64) of each row, and the
+ * number of the row's values that did not read back bit for bit.  One CTA,
+ * 64 TMEM columns.  Status: MXA_OK, MXA_ERR_ARG (null pointer), MXA_ERR_ALIGN
+ * (not 4-byte aligned), MXA_ERR_CUDA. */
+mxa_status mxa_test_tmem_max(const float* x, float* out, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
