@@ -603,11 +603,22 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     for (int j = 0; j < n_it; ++j, ++g) {
       if (!(ok = warp_wait(&bar_s_full, g & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       tc_fence_after();
+      // columns >= lim are masked (keys past the document end, or after the
+      // query on the causal diagonal); only the last iteration has any
+      int lim = 256;
+      if (j == n_it - 1) {
+        const int64_t rem = nk - static_cast<int64_t>(j) * 256;
+        lim = rem < 256 ? static_cast<int>(rem) : 256;
+        if (a.causal) {
+          const int64_t c = qpos - static_cast<int64_t>(j) * 256 + 1;
+          if (c < lim) lim = static_cast<int>(c);
+        }
+      }
+      // a warp whose 64 columns are visible in all its rows takes their
+      // maximum with the load itself
+      const bool full = __all_sync(0xffffffffu, lim >= 64 * part + 64);
       float sv[64];
       float mt;
-      // every iteration but the last has all 256 columns visible: the load
-      // also returns their maximum
-      const bool full = j < n_it - 1;
       if (full) {
         ld64_max(lane_base + C::kColS + 64 * part, sv, mt);
       } else {
@@ -619,22 +630,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       const bool hold_s = fold && j == n_it - 1;
       tc_fence_before();
       if (!hold_s) mbar_arrive(&bar_s_empty);
-      // columns >= lim are masked (keys past the document end, or after the
-      // query on the causal diagonal); only the last iteration has any
-      int lim = 256;
       if (!full) {
-        const int64_t rem = nk - static_cast<int64_t>(j) * 256;
-        lim = rem < 256 ? static_cast<int>(rem) : 256;
-        if (a.causal) {
-          const int64_t c = qpos - static_cast<int64_t>(j) * 256 + 1;
-          if (c < lim) lim = static_cast<int>(c);
-        }
-        if (lim < 256) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) sv[c] = (64 * part + c < lim) ? sv[c] : -INFINITY;
-        }
+        for (int c = 0; c < 64; ++c) sv[c] = (64 * part + c < lim) ? sv[c] : -INFINITY;
+        mt = max64(sv);
       }
-      if (!full) mt = max64(sv);
       const int px = static_cast<int>(g & 1);
       s_mx[px][part][r] = mt;
       mbar_arrive(&bar_mx[px][quad]);
