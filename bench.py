@@ -304,12 +304,16 @@ def run_gpu(args):
     stream = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
-    def step(src, rec=None, outs=None):
+    def step(src, rec=None, outs=None, wait=None, fwd_done=None):
+        # wait: per-input events (each quantize waits only for its own
+        # tensor's upload); fwd_done: recorded once O is final
         o_, lse_, dq_, dk_, dv_ = outs if outs is not None else (o, lse, dq, dk, dv)
         e = [ev() for _ in range(4)] if rec is not None else None
         if e: e[0].record(stream)
+        if wait: stream.wait_event(wait["q"])
         mxa.quantize(src["q"], geo, out=qv["q"])
         for k in ("k", "v"):
+            if wait: stream.wait_event(wait[k])
             mxa.quantize(src[k], gk, out=qv[k])
         if vkey is not None:
             mxa.quantize_key(src["v"], geo, out=vkey)
@@ -318,6 +322,8 @@ def run_gpu(args):
         mxa.fwd(qv["q"][0], qv["k"][0], qv["v"][1], geo, w.causal, out=(o_, lse_), workspace=fws, kv_geo=kv_geo,
                 v_key=vkey)
         if e: e[2].record(stream)
+        if fwd_done is not None: fwd_done.record(stream)
+        if wait: stream.wait_event(wait["do"])
         mxa.quantize(src["do"], geo, out=qv["do"])
         mxa.bwd(views, o_, lse_, geo, w.causal, dq_mode=args.dq_mode, workspace=ws, out=(dq_, dk_, dv_),
                 kv_geo=kv_geo, k_key=kkey)
@@ -458,44 +464,54 @@ def run_gpu(args):
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
     # Pipelined like a training loop: step i+1's inputs go up on one stream and
-    # step i-1's outputs come down on another while step i computes; inputs and
-    # outputs are double-buffered on the device.  Every byte of every step
-    # crosses the host link inside the timed region.
+    # step i's outputs come down on another while the next step computes;
+    # inputs and outputs are double-buffered on the device.  Each quantize
+    # waits only for its own input, and O comes down once the forward is
+    # done.  Every byte of every step crosses the host link inside the timed
+    # region.  (One stream per tensor and direction was slower: the copies
+    # contend for the link.)
     dev_in2 = [dev_in, {k: torch.empty_like(v) for k, v in x.items()}]
     outs2 = [(o, lse, dq, dk, dv), tuple(torch.empty_like(tn) for tn in (o, lse, dq, dk, dv))]
     s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
 
+    def upload(b):
+        """The inputs of buffer b on the upload stream, one event per tensor."""
+        evs = {}
+        with torch.cuda.stream(s_h2d):
+            for k in dev_in2[b]:
+                dev_in2[b][k].copy_(host_in[k], non_blocking=True)
+                evs[k] = ev()
+                evs[k].record(s_h2d)
+        return evs
+
     def e2e_run(n):
         start, end = ev(), ev()
         start.record(stream)
-        in_ready = [ev(), ev()]
         done = [None, None]
         out_free = [None, None]
         s_h2d.wait_event(start)
-        with torch.cuda.stream(s_h2d):
-            for k in dev_in2[0]:
-                dev_in2[0][k].copy_(host_in[k], non_blocking=True)
-        in_ready[0].record(s_h2d)
+        in_ready = [upload(0), None]
         for i in range(n):
             bb = i % 2
-            stream.wait_event(in_ready[bb])
             if out_free[bb] is not None:
                 stream.wait_event(out_free[bb])
-            step(dev_in2[bb], outs=outs2[bb])
+            fwd_done = ev()
+            step(dev_in2[bb], outs=outs2[bb], wait=in_ready[bb], fwd_done=fwd_done)
             done[bb] = ev()
             done[bb].record(stream)
             if i + 1 < n:  # the next inputs, once the step that last read that buffer is done
                 nb = (i + 1) % 2
                 if done[nb] is not None:
                     s_h2d.wait_event(done[nb])
-                with torch.cuda.stream(s_h2d):
-                    for k in dev_in2[nb]:
-                        dev_in2[nb][k].copy_(host_in[k], non_blocking=True)
-                in_ready[nb] = ev()
-                in_ready[nb].record(s_h2d)
+                in_ready[nb] = upload(nb)
+            # O comes down as soon as the forward has written it, the
+            # gradients once the step is done
+            s_d2h.wait_event(fwd_done)
+            with torch.cuda.stream(s_d2h):
+                host_out["o"].copy_(outs2[bb][0], non_blocking=True)
             s_d2h.wait_event(done[bb])
             with torch.cuda.stream(s_d2h):
-                for k, tn in zip(("o", "dq", "dk", "dv"), (outs2[bb][0], outs2[bb][2], outs2[bb][3], outs2[bb][4])):
+                for k, tn in zip(("dq", "dk", "dv"), (outs2[bb][2], outs2[bb][3], outs2[bb][4])):
                     host_out[k].copy_(tn, non_blocking=True)
             out_free[bb] = ev()
             out_free[bb].record(s_d2h)
