@@ -261,13 +261,17 @@ typedef struct {
  * list of packed documents (FLAMIA notes, Algorithm 2): one item per
  * (document, 128-query tile), so that no CTA is launched for a tile slot past
  * a document's end, ordered by the number of key tiles it visits, longest
- * first (CTA i: item i / Hq, head i % Hq).  256 + 16 * ntiles + 8 * num_docs
+ * first (item i / Hq for head i % Hq).  256 + 16 * ntiles + 8 * num_docs
  * bytes, rounded up to 256.  Returns 0 when the list brings nothing (equal
  * documents on both sides: cu_seqlens and cu_seqlens_k NULL) or cannot be
  * built (a side's longest document above 4094 tiles); with workspace NULL or
- * smaller, mxa_fwd launches one CTA per (tile
- * slot of max_seqlen, document, head).  Every call rebuilds the list on the
- * device (cu_seqlens stays device-only). */
+ * smaller, mxa_fwd launches one CTA per (tile slot of max_seqlen, document,
+ * head).  Every call rebuilds the list on the device (cu_seqlens stays
+ * device-only).  With a list, and on equal documents, the forward is
+ * persistent: the grid holds one CTA per item and each running CTA takes
+ * over the items of CTAs that have not started (cluster launch control), so
+ * the longest items start first and the short ones fill in as CTAs free up
+ * (strict mode on equal documents keeps one CTA per tile). */
 size_t mxa_fwd_workspace_bytes(const mxa_fwd_params* p);
 
 /* Forward: O = softmax(alpha Q K^T) V over the visible keys, and LSE.
