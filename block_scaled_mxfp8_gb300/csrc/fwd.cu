@@ -1,7 +1,8 @@
 // fwd.cu -- MXFP8 block-scaled attention forward (tcgen05, TMEM, TMA).
 //
-// One CTA computes one 128-query tile of one (document, query head), walking
-// the visible keys 256 at a time:
+// A CTA computes 128-query tiles of (document, query head) items one after
+// another (persistent launches: each running CTA takes over the items of
+// CTAs not yet started), walking each tile's visible keys 256 at a time:
 //   S_j  = Q K_j^T          block-scaled MXFP8 MMA (kind::mxf8f6f4), M = 128
 //                           queries, N = 256 keys (per key, half the MMA
 //                           groups, barrier round trips and pipe drains of
