@@ -22,6 +22,14 @@ CASES = [
     (inp.make_custom("d128_ragged", lengths=[250, 33, 513], Hq=2, Hkv=1, d=128, causal=False, seed=32), 1),
     (inp.make_custom("tokblock_gqa", lengths=[100, 400, 37], Hq=4, Hkv=2, d=128, causal=True, mode="tokblock",
                      hadamard=True, seed=33), 0),
+    # d = 64 with four query heads per kv head on packed documents, in the
+    # FP32 and the per-row FP16 dQ modes; eight query heads per kv head (the
+    # dK/dV CTA walks 8 heads x its query tiles)
+    (inp.make_custom("d64_ragged_gqa4_causal", lengths=[300, 1, 129, 640], Hq=8, Hkv=2, d=64, causal=True,
+                     seed=34), 0),
+    (inp.make_custom("d64_ragged_gqa4_causal", lengths=[300, 1, 129, 640], Hq=8, Hkv=2, d=64, causal=True,
+                     seed=34), 2),
+    (inp.make_custom("d128_batched_gqa8", B=2, L=512, Hq=8, Hkv=1, d=128, causal=False, seed=35), 0),
 ]
 
 

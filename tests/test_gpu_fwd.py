@@ -22,6 +22,7 @@ CASES = [
     inp.make_custom("d64_batched_causal", B=2, L=384, Hq=2, Hkv=2, d=64, causal=True, seed=23),
     inp.make_custom("tokblock_gqa", lengths=[100, 400, 37], Hq=4, Hkv=2, d=128, causal=True, mode="tokblock",
                     hadamard=True, seed=24),
+    inp.make_custom("d64_ragged_gqa4_causal", lengths=[300, 1, 129, 640], Hq=8, Hkv=2, d=64, causal=True, seed=34),
     # more items than SMs: persistent CTAs take two items each (zig-zag
     # rounds of 152), so the per-item barrier phases and the Q / O hand-over
     # between items are exercised element by element
