@@ -34,6 +34,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "attn_common.cuh"
 
 namespace mxa {
@@ -78,7 +80,16 @@ struct BwdCfg {
 // one bulk copy; rows past a document's end get D = 0 and LSE = +inf (their
 // recomputed P is exp(-inf) = 0).  One CTA per (128-token tile, doc, head),
 // one warp per row.
+// Each warp takes its rows kRows at a time, with every load of those rows
+// issued before the first sum (read-only loads, so that the D and LSE stores of the
+// previous rows do not hold them back).  Per row the arithmetic is the same:
+// a lane's D partial over its channels in one fixed order, then the warp sum.
+template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(PrepArgs a) {
+  constexpr int kCh = D / 32;  // channels per lane
+  constexpr int kRows = 8;     // rows of a warp in flight (of its 16)
+  using CodeT = typename std::conditional<D == 128, uint32_t, uint16_t>::type;
+  using OT = typename std::conditional<D == 128, uint2, uint32_t>::type;
   __shared__ int64_t s_slot;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int i = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
@@ -88,59 +99,77 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(PrepArgs a) {
   const int64_t tb = doc_tile_base(a.cu_seqlens, b, n, tid, 256, &s_slot);
   const int64_t slot = (static_cast<int64_t>(h) * a.ntiles + tb + i) * 128;
   const uint8_t* atom = a.g_sf + (static_cast<int64_t>(h) * a.ntiles + tb + i) * kAtomBytes;
-  for (int r = warp; r < 128; r += 8) {
-    const int64_t pos = static_cast<int64_t>(i) * 128 + r;
-    if (pos >= n) {
-      if (lane == 0) {
-        a.dpad[slot + r] = 0.0f;
-        a.lpad[slot + r] = INFINITY;
-      }
-      continue;
+  const int c0 = kCh * lane;  // this lane's first channel (all in group c0 / 32)
+  const CodeT* gcodes = reinterpret_cast<const CodeT*>(a.g_codes);
+  const OT* orow = reinterpret_cast<const OT*>(a.o);
+#pragma unroll 1
+  for (int r0 = warp; r0 < 128; r0 += 8 * kRows) {  // rows r0 + 8 q
+    CodeT codes[kRows];
+    OT ov[kRows];
+    uint32_t sb[kRows];
+    float lse[kRows];
+#pragma unroll
+    for (int q = 0; q < kRows; ++q) {
+      const int r = r0 + 8 * q;
+      const int64_t pos = static_cast<int64_t>(i) * 128 + r;
+      const int64_t t = doc_start + (pos < n ? pos : 0);
+      codes[q] = __ldg(gcodes + (t * a.Hq + h) * (D / kCh) + lane);
+      ov[q] = __ldg(orow + (t * a.Hq + h) * (D / kCh) + lane);
+      sb[q] = __ldg(atom + atom_offset(r, c0 / 32));
+      lse[q] = lane == 0 ? __ldg(a.lse + static_cast<int64_t>(h) * a.T + t) : 0.0f;
     }
-    const int64_t t = doc_start + pos;
-    float acc;
-    if (a.d == 128) {
-      const int c0 = 4 * lane;
-      const uint32_t codes = *reinterpret_cast<const uint32_t*>(a.g_codes + (t * a.Hq + h) * 128 + c0);
-      const float sc = exp2f(static_cast<float>(static_cast<int>(atom[atom_offset(r, c0 / 32)]) - 127));
-      const uint2 ov = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.o) + (t * a.Hq + h) * 128 + c0);
-      const float2 g01 = e4m3x2_to_f32x2(codes & 0xFFFFu), g23 = e4m3x2_to_f32x2(codes >> 16);
-      acc = (g01.x * __uint_as_float(ov.x << 16) + g01.y * __uint_as_float(ov.x & 0xFFFF0000u) +
-             g23.x * __uint_as_float(ov.y << 16) + g23.y * __uint_as_float(ov.y & 0xFFFF0000u)) * sc;
-    } else {
-      const int c0 = 2 * lane;
-      const uint16_t codes = *reinterpret_cast<const uint16_t*>(a.g_codes + (t * a.Hq + h) * 64 + c0);
-      const float sc = exp2f(static_cast<float>(static_cast<int>(atom[atom_offset(r, c0 / 32)]) - 127));
-      const uint32_t ov = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(a.o) + (t * a.Hq + h) * 64 + c0);
-      const float2 g01 = e4m3x2_to_f32x2(codes);
-      acc = (g01.x * __uint_as_float(ov << 16) + g01.y * __uint_as_float(ov & 0xFFFF0000u)) * sc;
+    float acc[kRows];
+#pragma unroll
+    for (int q = 0; q < kRows; ++q) {
+      const float sc = exp2f(static_cast<float>(static_cast<int>(sb[q]) - 127));
+      if constexpr (D == 128) {
+        const float2 g01 = e4m3x2_to_f32x2(codes[q] & 0xFFFFu), g23 = e4m3x2_to_f32x2(codes[q] >> 16);
+        acc[q] = (g01.x * __uint_as_float(ov[q].x << 16) + g01.y * __uint_as_float(ov[q].x & 0xFFFF0000u) +
+                  g23.x * __uint_as_float(ov[q].y << 16) + g23.y * __uint_as_float(ov[q].y & 0xFFFF0000u)) * sc;
+      } else {
+        const float2 g01 = e4m3x2_to_f32x2(codes[q]);
+        acc[q] = (g01.x * __uint_as_float(ov[q] << 16) + g01.y * __uint_as_float(ov[q] & 0xFFFF0000u)) * sc;
+      }
     }
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) {
-      a.dpad[slot + r] = acc;
-      a.lpad[slot + r] = a.lse[static_cast<int64_t>(h) * a.T + t] * 1.4426950408889634f;
+    for (int o = 16; o >= 1; o >>= 1) {
+#pragma unroll
+      for (int q = 0; q < kRows; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
     }
-    if (a.dq_boost != nullptr) {
-      // g_i = cl2(max_c |G~_ic|): this lane's codes (one 32-channel group)
-      // with the group's scale, then the warp maximum
-      const int c0 = a.d == 128 ? 4 * lane : 2 * lane;
-      uint32_t w = a.d == 128 ? *reinterpret_cast<const uint32_t*>(a.g_codes + (t * a.Hq + h) * 128 + c0)
-                              : *reinterpret_cast<const uint16_t*>(a.g_codes + (t * a.Hq + h) * 64 + c0);
-      w &= 0x7F7F7F7Fu;
-      w = __vmaxu4(w, w >> 16);
-      w = __vmaxu4(w, w >> 8);
-      const uint32_t cmax = w & 0xFFu;
-      int g = cmax ? cl2_e4m3(cmax) + static_cast<int>(atom[atom_offset(r, c0 / 32)]) - 127 : kCl2None;
-      g = __reduce_max_sync(0xffffffffu, g);
+#pragma unroll
+    for (int q = 0; q < kRows; ++q) {
+      const int r = r0 + 8 * q;
+      const int64_t pos = static_cast<int64_t>(i) * 128 + r;
+      if (pos >= n) {  // past the document's end: P = exp(-inf) = 0
+        if (lane == 0) {
+          a.dpad[slot + r] = 0.0f;
+          a.lpad[slot + r] = INFINITY;
+        }
+        continue;
+      }
       if (lane == 0) {
-        const int64_t nvis = a.causal ? pos + 1 : n;
-        const int lg = cl2_count(nvis);
-        const int sp = 1 + (lg > 14 ? lg - 14 : 0);
-        const int kb = a.key_bound[t * a.Hkv + h / (a.Hq / a.Hkv)];
-        int beta = 11 - cl2_f32(a.alpha) - (a.d == 128 ? 7 : 6) - sp - g - kb;
-        beta = beta < -100 ? -100 : (beta > 100 ? 100 : beta);
-        a.dq_boost[static_cast<int64_t>(h) * a.T + t] = __uint_as_float(static_cast<uint32_t>(beta + 127) << 23);
+        a.dpad[slot + r] = acc[q];
+        a.lpad[slot + r] = lse[q] * 1.4426950408889634f;
+      }
+      if (a.dq_boost != nullptr) {
+        // g_i = cl2(max_c |G~_ic|): this lane's codes (one 32-channel group)
+        // with the group's scale, then the warp maximum
+        const int64_t t = doc_start + pos;
+        uint32_t w = static_cast<uint32_t>(codes[q]) & 0x7F7F7F7Fu;
+        w = __vmaxu4(w, w >> 16);
+        w = __vmaxu4(w, w >> 8);
+        const uint32_t cmax = w & 0xFFu;
+        int g = cmax ? cl2_e4m3(cmax) + static_cast<int>(sb[q]) - 127 : kCl2None;
+        g = __reduce_max_sync(0xffffffffu, g);
+        if (lane == 0) {
+          const int64_t nvis = a.causal ? pos + 1 : n;
+          const int lg = cl2_count(nvis);
+          const int sp = 1 + (lg > 14 ? lg - 14 : 0);
+          const int kb = a.key_bound[t * a.Hkv + h / (a.Hq / a.Hkv)];
+          int beta = 11 - cl2_f32(a.alpha) - (D == 128 ? 7 : 6) - sp - g - kb;
+          beta = beta < -100 ? -100 : (beta > 100 ? 100 : beta);
+          a.dq_boost[static_cast<int64_t>(h) * a.T + t] = __uint_as_float(static_cast<uint32_t>(beta + 127) << 23);
+        }
       }
     }
   }
@@ -729,7 +758,8 @@ cudaError_t launch_key_bound(const KeyBoundArgs& a, int max_seqlen, cudaStream_t
 cudaError_t launch_bwd_prep(const PrepArgs& a, int max_seqlen, cudaStream_t stream) {
   if (a.dq_acc_bytes && cudaMemsetAsync(a.dq_acc, 0, a.dq_acc_bytes, stream) != cudaSuccess) return cudaGetLastError();
   dim3 grid((max_seqlen + 127) / 128, a.num_docs, a.Hq);
-  bwd_prep_kernel<<<grid, 256, 0, stream>>>(a);
+  if (a.d == 128) bwd_prep_kernel<128><<<grid, 256, 0, stream>>>(a);
+  else bwd_prep_kernel<64><<<grid, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
