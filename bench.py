@@ -104,6 +104,7 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.times = []  # host arrival time of each line (time.monotonic)
 
     def __enter__(self):
         try:
@@ -119,6 +120,7 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+            self.times.append(time.monotonic())
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -128,10 +130,14 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, its maximum and the throttle reasons seen, over
+        the samples that arrived in [t0, t1] (all samples by default)."""
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln, t in zip(self.lines, self.times):
+            if (t0 is not None and t < t0) or (t1 is not None and t > t1):
+                continue
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -525,13 +531,23 @@ def run_gpu(args):
     # five passes, with their spread.  A pass runs the timed step count (at
     # most 30): its first upload and last download are not overlapped with
     # compute, and a training loop runs long enough for the steady state
+    # The SM clock of each pass comes from one sampler over all five: they
+    # run for about a second in all, long enough for the GPU to reach its
+    # power cap, unlike the 0.2 s timed region above
     n_e2e = max(3, min(args.steps, 30))
-    passes = sorted(e2e_run(n_e2e) / n_e2e for _ in range(5))
-    ms_e2e = passes[len(passes) // 2]
+    passes, windows = [], []
+    with ClockSampler(local) as eclk:
+        for _ in range(5):
+            t0 = time.monotonic()
+            passes.append(e2e_run(n_e2e) / n_e2e)
+            windows.append((t0, time.monotonic()))
+    ms_e2e = sorted(passes)[len(passes) // 2]
+    pass_clk = [eclk.summary(t0, t1) for t0, t1 in windows]
     e2e = {"value": round(world * step_flop / (ms_e2e * 1e-3) / 1e15, 4), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3),
            "ms_per_step_passes": [round(x, 3) for x in passes], "steps_per_pass": n_e2e,
-           "host_cpus": host_cpus}
+           "sm_mhz_passes": [c["sm_mhz"] for c in pass_clk],
+           "clock_reasons": sorted(set(r for c in pass_clk for r in c["reasons"])), "host_cpus": host_cpus}
 
     # the quantizer of Q, K and V (both views) against HBM: 2 B read and
     # (1 + 1/32) B written per element per view (padding scale bytes excluded)

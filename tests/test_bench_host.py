@@ -70,3 +70,27 @@ def test_bench_names_resolve():
         return bad
 
     assert unresolved(symtable.symtable(src, "bench.py", "exec")) == []
+
+
+def test_clock_summary_by_time_window():
+    """The clock record of each end-to-end pass: the samples that arrived
+    inside the pass's window, their median SM clock and the throttle reasons
+    they show (nvidia-smi csv, noheader, nounits)."""
+    c = bench.ClockSampler(0)
+    rows = [  # index, sm, max sm, power, active, hw, hw thermal, sw thermal, sw power cap
+        (1.0, "0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active"),
+        (1.1, "0, 2070, 2070, 1100.0, 0x0, Not Active, Not Active, Not Active, Not Active"),
+        (2.0, "0, 1500, 2070, 1400.0, 0x4, Not Active, Not Active, Not Active, Active"),
+        (2.1, "0, 1480, 2070, 1400.0, 0x4, Not Active, Not Active, Not Active, Active"),
+        (2.2, "0, 1490, 2070, 1399.0, 0x4, Not Active, Not Active, Not Active, Active"),
+        (2.3, "garbled line"),
+    ]
+    for t, ln in rows:
+        c.times.append(t)
+        c.lines.append(ln)
+    first = c.summary(0.9, 1.5)
+    assert first == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 2}
+    late = c.summary(1.9, 3.0)
+    assert late["sm_mhz"] == 1490.0 and late["reasons"] == ["sw_power_cap"] and late["samples"] == 3
+    assert c.summary()["samples"] == 5
+    assert c.summary(5.0, 6.0) == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
