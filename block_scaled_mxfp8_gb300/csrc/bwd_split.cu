@@ -110,7 +110,10 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
 }  // namespace
 
 // ========================================================================= dK, dV
-template <int D, bool STRICT>
+// ORDER (causal calls over equal documents, without a tile list): the launch
+// order of causal_launch_order, heaviest key tiles of the last groups first
+// (the other calls keep the grid's own order and this code out of their build).
+template <int D, bool STRICT, bool ORDER>
 __global__ void __launch_bounds__(kDkdvThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   using C = DkdvCfg<D>;
@@ -133,6 +136,14 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     kt = blockIdx.x;
     b = blockIdx.y;
     hk = blockIdx.z;
+    if constexpr (ORDER) {
+      // key tile kt carries (tiles - kt) units
+      const int v = static_cast<int>(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+      int g;
+      causal_launch_order(v, a.num_docs * a.Hkv, static_cast<int>(gridDim.x), g, kt);
+      b = g % a.num_docs;
+      hk = g / a.num_docs;
+    }
   }
   const int grp = a.Hq / a.Hkv;
   int64_t doc_start, n, kdoc_start, nk;  // the document's queries and keys (the same for self-attention)
@@ -761,53 +772,55 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
   }
 }
 
+namespace {
+
+template <int D, bool STRICT, bool ORDER>
+cudaError_t launch_dkdv_t(const BwdArgs& a, const BwdMaps& m, const dim3& g1, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, STRICT, ORDER>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  attn_bwd_dkdv_kernel<D, STRICT, ORDER><<<g1, kDkdvThreads, DkdvCfg<D>::kSmemBytes, stream>>>(m, a);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_dkdv_d(const BwdArgs& a, const BwdMaps& m, const dim3& g1, cudaStream_t stream) {
+  const bool strict = a.kkey_sf != nullptr;
+  const bool order = a.causal && !a.k_items && a.cu_seqlens == nullptr && a.cu_k == nullptr;
+  if (strict) return order ? launch_dkdv_t<D, true, true>(a, m, g1, stream) : launch_dkdv_t<D, true, false>(a, m, g1, stream);
+  return order ? launch_dkdv_t<D, false, true>(a, m, g1, stream) : launch_dkdv_t<D, false, false>(a, m, g1, stream);
+}
+
+cudaError_t launch_dkdv(const BwdArgs& a, const BwdMaps& m, int d, const dim3& g1, cudaStream_t stream) {
+  return d == 128 ? launch_dkdv_d<128>(a, m, g1, stream) : launch_dkdv_d<64>(a, m, g1, stream);
+}
+
+}  // namespace
+
 cudaError_t launch_bwd_split(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
   const int tiles = (max_seqlen + 127) / 128;
   const dim3 g1 = a.k_items ? dim3(static_cast<unsigned>(a.ntiles_k * a.Hkv)) : dim3(tiles, a.num_docs, a.Hkv);
   const dim3 g2 = a.q_items ? dim3(static_cast<unsigned>(a.ntiles * a.Hq)) : dim3(tiles, a.num_docs, a.Hq);
-  cudaError_t e;
+  cudaError_t e = launch_dkdv(a, m, d, g1, stream);
+  if (e != cudaSuccess) return e;
   if (d == 128) {
-    e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DkdvCfg<128>::kSmemBytes);
-    if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(attn_bwd_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DqCfg<128>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attn_bwd_dkdv_kernel<128, false><<<g1, kDkdvThreads, DkdvCfg<128>::kSmemBytes, stream>>>(m, a);
     attn_bwd_dq_kernel<128><<<g2, kSplitThreads, DqCfg<128>::kSmemBytes, stream>>>(m, a);
   } else {
-    e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DkdvCfg<64>::kSmemBytes);
-    if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(attn_bwd_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DqCfg<64>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attn_bwd_dkdv_kernel<64, false><<<g1, kDkdvThreads, DkdvCfg<64>::kSmemBytes, stream>>>(m, a);
     attn_bwd_dq_kernel<64><<<g2, kSplitThreads, DqCfg<64>::kSmemBytes, stream>>>(m, a);
   }
   return cudaGetLastError();
 }
 
-namespace {
-
-template <int D, bool STRICT>
-cudaError_t launch_dkdv_t(const BwdArgs& a, const BwdMaps& m, const dim3& g1, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, STRICT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       DkdvCfg<D>::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  attn_bwd_dkdv_kernel<D, STRICT><<<g1, kDkdvThreads, DkdvCfg<D>::kSmemBytes, stream>>>(m, a);
-  return cudaGetLastError();
-}
-
-}  // namespace
-
 cudaError_t launch_bwd_emit(const BwdArgs& a, const BwdMaps& m, int d, int max_seqlen, cudaStream_t stream) {
   const int tiles = (max_seqlen + 127) / 128;
   const dim3 g1 = a.k_items ? dim3(static_cast<unsigned>(a.ntiles_k * a.Hkv)) : dim3(tiles, a.num_docs, a.Hkv);
-  const bool strict = a.kkey_sf != nullptr;
-  cudaError_t e;
-  if (d == 128) e = strict ? launch_dkdv_t<128, true>(a, m, g1, stream) : launch_dkdv_t<128, false>(a, m, g1, stream);
-  else e = strict ? launch_dkdv_t<64, true>(a, m, g1, stream) : launch_dkdv_t<64, false>(a, m, g1, stream);
+  const cudaError_t e = launch_dkdv(a, m, d, g1, stream);
   if (e != cudaSuccess) return e;
   return launch_dq_gemm(a, m, d, max_seqlen, stream);
 }

@@ -211,8 +211,9 @@ struct FwdItem {
 // Item v of a persistent launch: item v / Hq of the cost-sorted list for head
 // v % Hq, or the v-th (query tile, document, head) of equal documents --
 // query tiles fastest, so the CTAs running together share a head's K and V
-// tiles in L2, and the heaviest tiles first when causal.  False past the
-// last item.
+// tiles in L2, heaviest first when causal, and the last groups' query tiles
+// interleaved heaviest first (causal_launch_order).  False past the last
+// item.
 __device__ __forceinline__ bool fwd_item(const FwdArgs& a, int64_t v, FwdItem& it) {
   if (a.items) {
     const int64_t i = v / a.Hq;
@@ -227,11 +228,19 @@ __device__ __forceinline__ bool fwd_item(const FwdArgs& a, int64_t v, FwdItem& i
   }
   const int nqt = a.nq_tiles_doc;
   if (v >= static_cast<int64_t>(nqt) * a.num_docs * a.Hq) return false;
-  const int qi = static_cast<int>(v % nqt);
-  const int64_t rest = v / nqt;
-  it.b = static_cast<int>(rest % a.num_docs);
-  it.h = static_cast<int>(rest / a.num_docs);
-  it.qt = a.causal ? nqt - 1 - qi : qi;
+  if (a.causal) {
+    int grp, qi;
+    causal_launch_order(static_cast<int>(v), a.num_docs * a.Hq, nqt, grp, qi);
+    it.b = grp % a.num_docs;
+    it.h = grp / a.num_docs;
+    it.qt = nqt - 1 - qi;
+  } else {
+    const int qi = static_cast<int>(v % nqt);
+    const int64_t rest = v / nqt;
+    it.b = static_cast<int>(rest % a.num_docs);
+    it.h = static_cast<int>(rest / a.num_docs);
+    it.qt = qi;
+  }
   it.tile_base = static_cast<int64_t>(it.b) * nqt;
   it.ktile_base = static_cast<int64_t>(it.b) * a.nk_tiles_doc;
   return true;
