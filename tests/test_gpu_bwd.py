@@ -30,6 +30,11 @@ CASES = [
     (inp.make_custom("d64_ragged_gqa4_causal", lengths=[300, 1, 129, 640], Hq=8, Hkv=2, d=64, causal=True,
                      seed=34), 2),
     (inp.make_custom("d128_batched_gqa8", B=2, L=512, Hq=8, Hkv=1, d=128, causal=False, seed=35), 0),
+    # equal documents, causal: the forward and dK/dV grids in their causal
+    # launch order (40 and 20 (document, head) groups; the last 16 of each go
+    # heaviest tile first across groups)
+    (inp.make_custom("b5_gqa2_batched_causal", B=5, L=384, Hq=8, Hkv=4, d=128, causal=True, seed=37), 0),
+    (inp.make_custom("b5_gqa2_batched_causal", B=5, L=384, Hq=8, Hkv=4, d=128, causal=True, seed=37), 1),
 ]
 
 

@@ -122,6 +122,9 @@ BWD_CASES = [
     inp.make_custom("d128_ragged_gqa_causal", lengths=[1, 129, 300, 64, 7, 515], Hq=4, Hkv=2, d=128, causal=True,
                     seed=45),
     inp.make_custom("d64_ragged", lengths=[256, 100, 383], Hq=2, Hkv=1, d=64, causal=True, seed=46),
+    # equal documents: the dK/dV grid in its causal launch order (20 (document,
+    # kv head) groups, the last 16 heaviest key tile first across groups)
+    inp.make_custom("b5_gqa2_batched", B=5, L=384, Hq=8, Hkv=4, d=128, causal=True, seed=48),
 ]
 
 
