@@ -85,7 +85,7 @@ struct BwdCfg {
 // previous rows do not hold them back).  Per row the arithmetic is the same:
 // a lane's D partial over its channels in one fixed order, then the warp sum.
 template <int D>
-__global__ void __launch_bounds__(256) bwd_prep_kernel(PrepArgs a) {
+__global__ void __launch_bounds__(256, 4) bwd_prep_kernel(PrepArgs a) {
   constexpr int kCh = D / 32;  // channels per lane
   constexpr int kRows = 8;     // rows of a warp in flight (of its 16)
   using CodeT = typename std::conditional<D == 128, uint32_t, uint16_t>::type;
