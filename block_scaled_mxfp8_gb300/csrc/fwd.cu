@@ -120,6 +120,12 @@ __device__ __forceinline__ void ld64_max(uint32_t taddr, float (&v)[64], float& 
   mx = fmaxf(m0, m1);
 }
 
+// Most binades by which O and L may trail the P reference m in the default
+// mode (each of their weights then reaches 2^(kOLag + 4): fp32 headroom for
+// |V| up to ~2^70 at hundreds of thousands of keys).  The strict mode keeps
+// them on m, as its diagonal fold scales are formed against m.
+constexpr float kOLag = 32.0f;
+
 // 2^(b - 127) of a UE8M0 byte (b = 0: 2^-127).
 __device__ __forceinline__ float ue8m0_f32(uint32_t b) {
   return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
@@ -565,7 +571,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const float sl2 = a.scale_log2;
     if (part == 0) {
-      // 1.0 for the ones rows of both V atoms, 2^-4 for P
+      // 1.0 for the ones rows of both V atoms, 2^-4 for P (the default mode
+      // rewrites the P scale with each item's first P)
       tmem_st4(lane_base + C::kColOneA, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
       tmem_st4(lane_base + C::kColOneB, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
       tmem_st4(lane_base + C::kColSfP, 0x7B7B7B7Bu, 0x7B7B7B7Bu, 0x7B7B7B7Bu, 0x7B7B7B7Bu);
@@ -608,6 +615,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
     const int64_t qpos = static_cast<int64_t>(qt) * 128 + r;  // document-relative query index
     float m = -INFINITY;  // running (lazy) max of the scaled scores, log2 units
+    // O and L run on their own reference mo, at most kOLag binades behind m:
+    // the P V MMA's A scale 2^(m - mo - 4) carries the difference, so a raise
+    // of m rescales nothing in TMEM until the lag passes kOLag.  Scaling by a
+    // power of two commutes with the fp32 sums, so O / L is the same.
+    float mo = -INFINITY;
     float l16 = 0.0f;     // this warp's sum of 2^(s - m + 4) over its columns
     float ldiag = 0.0f;   // folded diagonal columns (FOLD): the weights their codes stand for
     for (int j = 0; j < n_it; ++j, ++g) {
@@ -651,19 +663,32 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       if (!(ok = warp_wait(&bar_mx[px][quad], (g >> 1) & 1, abort_flag, a.err, kErrTimeoutSoftmax))) break;
       mt = fmaxf(fmaxf(s_mx[px][0][r], s_mx[px][1][r]), fmaxf(s_mx[px][2][r], s_mx[px][3][r]));
       const float mts = mt * sl2;
-      bool rescale_o = false;
-      float factor = 1.0f;
+      bool rescale_o = false, new_scale = j == 0;
+      float factor = 1.0f, ofactor = 1.0f;
       // the reference stays on the integer grid of base-2 coordinates, so a
       // raise multiplies the earlier sums by an exact power of two and the
       // E4M3 weights are those of the final reference ceil(max) shifted by
       // whole binades (scale doubling, FLAMIA notes sec. 4)
       if (j == 0) {
         m = ceilf(mts);
+        if constexpr (!FOLD) mo = m;
       } else if (mts > m + 4.0f) {
         const float mn = ceilf(mts);
         factor = exp2i_neg(static_cast<int>(fminf(mn - m, 127.0f)));
         m = mn;
-        rescale_o = true;
+        if constexpr (FOLD) {
+          // the strict mode keeps O on m (its diagonal fold scales are
+          // formed against m)
+          ofactor = factor;
+          rescale_o = true;
+        } else {
+          new_scale = true;
+          if (m - mo > kOLag) {  // O and L catch up
+            ofactor = exp2i_neg(static_cast<int>(fminf(m - mo, 127.0f)));
+            mo = m;
+            rescale_o = true;
+          }
+        }
       }
       const float neg = 4.0f - m;
       const uint64_t neg2 = f2_pack(neg, neg), sl2x2 = f2_pack(sl2, sl2);
@@ -706,6 +731,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       // tcgen05.ld/st are warp-collective: the whole warp rescales its rows'
       // share of O when any of them needs it (factor 1 for the others).
       if (__any_sync(0xffffffffu, rescale_o)) {
+        const float factor = ofactor;
 #pragma unroll
         for (int c = 0; c < D / 128; ++c) {
           const uint32_t col = C::kColO + (D / 4) * part + 32 * c;
@@ -752,9 +778,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
         tmem_st8(lane_base + C::kColP + 16 * part, w0);
         tmem_st8(lane_base + C::kColP + 16 * part + 8, w1);
+        // the P scale of row r sits at lane r, column base + r / 32, one byte
+        // per K step: 2^(m - mo - 4) for all of them, rewritten when m or mo
+        // moved (the previous P V, which read it, is done)
+        if constexpr (!FOLD) {
+          if (part == 0 && __any_sync(0xffffffffu, new_scale))
+            tmem_st1(lane_base + C::kColSfP + quad, static_cast<uint32_t>(123.0f + (m - mo)) * 0x01010101u);
+        }
         if (FOLD && diag) {
           // K steps 2 (part & 1) and 2 (part & 1) + 1 of the diagonal half: the
-          // scale of row r at lane r, column base + r / 32, byte = sf_id
+          // scale of row r at lane r, column base + r / 32, byte = sf_id (the
+          // strict mode keeps O on m: no lag to carry)
           const uint32_t v = (part & 1) ? (0x00007F7Fu | (sfb << 16)) : (0x7F7F0000u | sfb);
           tmem_st1(lane_base + C::kColSfPd + 4 * (part & 1) + quad, v);
         }
