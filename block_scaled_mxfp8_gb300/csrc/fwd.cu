@@ -16,7 +16,10 @@
 //          (FLAMIA notes sec. 5: 2^(c+tau) <= 448 with (c, tau) = (4, 4)),
 //          stored to TMEM;
 //   [O | L] += P_j [V_j | 1]  one block-scaled MMA with A = P from TMEM
-//          (scale 2^-4) and B = V (MN-major, TOK-view scales) widened by 16
+//          (scale 2^(m - mo - 4): O and L keep a reference mo up to 32
+//          binades behind the row max m, so that a raise of m rescales
+//          nothing in TMEM; the strict mode keeps mo = m) and B = V
+//          (MN-major, TOK-view scales) widened by 16
 //          columns of ones, so that L is the row sum of exactly the quantized
 //          weights used for O (the ones come from one shared 4 KB block that
 //          every K step reaches through the descriptor's leading byte offset);
